@@ -1,0 +1,194 @@
+/*
+ * medusa_verify.h -- C ABI of libmedusa_verify.so, the Medusa tree-verify decode step on one GB300 (sm_103a).
+ *
+ * Sources of the operations (cited by page title and section):
+ *   [M5]  "大模型推理 memory bandwidth bound (5) - Medusa" (dtcms.com): 一.1 Medusa heads, 一.2 Tree attention,
+ *         一.3 Typical acceptance, 二.2 generate_medusa_buffers(), 二.4 generate_candidates(),
+ *         二.5 tree_decoding(), 二.6 evaluate_posterior(), 二.7 update_inference_inputs().
+ *   [P3]  "Phi-3-mini-128k-instruct_rai_1.8.0_medusa_1.0_npu" article (lqnn.cn): 4️⃣ tree attention mask.
+ *   [OP]  "OpenPangu7B-with-Medusa" README: 4 (static tree tensors, fixed mask, few host-device round trips).
+ *
+ * Conventions (every entry point):
+ *   - Pointers named d_* or documented "device" are device pointers owned by the caller (e.g. PyTorch tensors);
+ *     they must stay valid until the stream work completes. Host pointers are read before the call returns.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream) and is asynchronous; no entry
+ *     point synchronises the device except mv_get_error().
+ *   - Argument errors are reported synchronously, before anything is launched. Errors found by the kernels
+ *     (a bounded wait that expired, an index read from device memory out of range) set a sticky device word
+ *     that mv_get_error() returns; the kernels then stop early and leave outputs unspecified.
+ *   - bf16 values are IEEE bfloat16 bit patterns (mv_bf16 = uint16_t), ABI-compatible with __nv_bfloat16.
+ *   - Workspaces are caller-allocated device memory of at least the size the matching *_workspace() call
+ *     returns. They must be zero-filled before their first use; every call leaves the counters it uses in
+ *     them back at zero. Calls that share a workspace must be ordered on one stream.
+ *   - Not thread-safe per handle.
+ */
+#ifndef MEDUSA_VERIFY_H
+#define MEDUSA_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t mv_bf16;
+typedef void* mv_stream; /* cudaStream_t */
+
+typedef enum mv_status {
+  MV_OK = 0,
+  MV_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum */
+  MV_ERR_SHAPE = 2,       /* sizes the kernels do not support or that disagree with a handle */
+  MV_ERR_TREE = 3,        /* malformed tree: not prefix-closed, duplicate, rank >= topk, too many nodes */
+  MV_ERR_CAPACITY = 4,    /* prefix + tree exceeds the cache, or workspace too small */
+  MV_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed */
+  MV_ERR_DEVICE = 6,      /* the device error word was set (see mv_get_error) */
+  MV_ERR_UNSUPPORTED = 7
+} mv_status;
+
+#define MV_MAX_NODES 64 /* tree nodes (root included): one 64-bit ancestor word per node */
+#define MV_MAX_DEPTH 8  /* longest root-to-leaf path, root excluded */
+
+/* ============================================================================================
+ * Static token tree  [M5 二.2 generate_medusa_buffers()], [OP 4]
+ * ============================================================================================
+ * Built once on the host from the choice list (rank tuples, root excluded); a host copy and a device copy
+ * (on the current device) are owned by the handle. Node order: root = 0, then the tuples sorted by
+ * (length, lexicographic). tree_indices[i] = 0 for the root, 1 + topk*(len-1) + last rank otherwise (index
+ * into [root, head-1 top-k, head-2 top-k, ...]). position_ids[i] = depth. retrieve: one row per leaf,
+ * leaves in descending node order, root-to-leaf node list padded with -1 to depth+1 entries.
+ * ancestors[i]: bit j set iff node j is node i or one of its ancestors (the tree attention mask row).
+ */
+typedef struct mv_tree mv_tree;
+
+typedef struct mv_tree_desc {
+  int32_t n_nodes, n_paths, depth, topk;
+  const int32_t* tree_indices;   /* host [n_nodes] */
+  const int32_t* position_ids;   /* host [n_nodes] */
+  const int32_t* retrieve;       /* host [n_paths][depth+1] */
+  const int32_t* parent;         /* host [n_nodes], -1 for the root */
+  const uint64_t* ancestors;     /* host [n_nodes] */
+  const int32_t* d_tree_indices; /* device copies of the above */
+  const int32_t* d_position_ids;
+  const int32_t* d_retrieve;
+  const int32_t* d_parent;
+  const uint64_t* d_ancestors;
+} mv_tree_desc;
+
+/* ranks: all tuples concatenated; lens[c] = length of tuple c (>= 1). topk: ranks per head (>= 1).
+ * Errors: MV_ERR_INVALID_ARG (null / n_choices < 0 / topk < 1), MV_ERR_TREE (see above; also depth >
+ * MV_MAX_DEPTH or more than MV_MAX_NODES nodes), MV_ERR_CUDA (device copy failed). *out is set on MV_OK. */
+mv_status mv_tree_create(const int32_t* ranks, const int32_t* lens, int32_t n_choices, int32_t topk, mv_tree** out);
+mv_status mv_tree_describe(const mv_tree* tree, mv_tree_desc* out);
+void mv_tree_destroy(mv_tree* tree);
+
+/* ============================================================================================
+ * Medusa heads + per-head top-k  [M5 一.1 Medusa heads, 二.4 generate_candidates()]
+ * ============================================================================================
+ * For each batch row b and head k:  z = W2_k (SiLU(W1_k h_b) + h_b);  out = the topk largest entries of z
+ * (larger value first; equal values: lower token id first). With w_lm != NULL also root[b] = argmax of
+ * W_lm h_b (lowest id on ties). Weights are bf16, accumulation fp32, SiLU output and residual kept in fp32.
+ *   h      device bf16 [B][d]            w1   device bf16 [K][d][d]  (row = output feature)
+ *   w2     device bf16 [K][V][d]         w_lm device bf16 [V][d] or NULL
+ *   out_idx device int32 [B][K][topk]    out_val device fp32 [B][K][topk]   out_root device int32 [B] or NULL
+ * Limits: 1 <= B <= 16, d % 8 == 0, 8 <= d <= 8192, 1 <= topk <= 16, topk <= V, 1 <= K <= 8.
+ */
+mv_status medusa_heads_topk_workspace(int32_t B, int32_t d, int32_t K, int32_t V, int32_t topk, size_t* bytes);
+mv_status medusa_heads_topk(const mv_bf16* h, int32_t B, int32_t d, int32_t K, const mv_bf16* w1,
+                            const mv_bf16* w2, int32_t V, int32_t topk, const mv_bf16* w_lm, int32_t* out_idx,
+                            float* out_val, int32_t* out_root, void* workspace, size_t ws_bytes, mv_stream stream);
+
+/* ============================================================================================
+ * Candidate gather into the tree  [M5 二.4 generate_candidates()]
+ * ============================================================================================
+ * candidates = [root, head_topk[0][0..topk), head_topk[1][...], ...];  tree_tokens[i] = candidates[tree_indices[i]];
+ * cart[p][j] = tree_tokens[retrieve[p][j]], or 0 where retrieve is -1.
+ *   d_root device int32 [1]; d_head_topk device int32 [K][ld_topk] (first tree.topk entries of each row used);
+ *   d_tree_tokens device int32 [n_nodes]; d_cart device int32 [n_paths][depth+1] or NULL.
+ * Limits: K >= tree depth, ld_topk >= tree topk.
+ */
+mv_status build_candidates(const int32_t* d_root, const int32_t* d_head_topk, int32_t K, int32_t ld_topk,
+                           const mv_tree* tree, int32_t* d_tree_tokens, int32_t* d_cart, mv_stream stream);
+
+/* ============================================================================================
+ * Tree attention  [M5 一.2 Tree attention, 二.5 tree_decoding()], [P3 4️⃣]
+ * ============================================================================================
+ * For tree node i and head h:  out[i][h] = softmax_j(scale * q[i][h] . K[h][j]) V[h][j]  over the keys
+ * j in [0, prefix_len) (the whole cached prefix) and j = prefix_len + a for every ancestor-or-self a of i.
+ * The tree block's keys/values must already be in the cache at rows prefix_len .. prefix_len + n_nodes - 1.
+ *   q device bf16 [n_nodes][H][D];  k_cache, v_cache device bf16 [H][S_max][D];  out device bf16 [n_nodes][H][D].
+ * Softmax and accumulation in fp32. Limits: D in {16, 32, 64, 128}; prefix_len >= 0;
+ * prefix_len + n_nodes <= S_max; 1 <= H <= 256; pointers 16-byte aligned.
+ */
+mv_status tree_attention_workspace(int32_t H, int32_t D, int32_t S_max, int32_t n_nodes, size_t* bytes);
+mv_status tree_attention(const mv_bf16* q, const mv_bf16* k_cache, const mv_bf16* v_cache, int32_t H, int32_t D,
+                         int32_t S_max, int32_t prefix_len, const mv_tree* tree, float scale, mv_bf16* out,
+                         void* workspace, size_t ws_bytes, mv_stream stream);
+
+/* ============================================================================================
+ * Posterior evaluation  [M5 一.3 Typical acceptance, 二.6 evaluate_posterior()]
+ * ============================================================================================
+ * Per tree node n (row n of logits): greedy: argmax; typical: p = softmax(z/T), H = -sum p log(p + 1e-5),
+ * tau = min(eps, delta * exp(-H)). Per path p and position j the candidate tree_tokens[retrieve[p][j+1]] is
+ * accepted iff it equals argmax of node retrieve[p][j] (greedy) or p(candidate) > tau (typical). Positions
+ * past a path's end (-1) are never accepted. acc_p = leading accepted count; best = greedy: first row with the
+ * largest acc; typical: among those rows, largest sum of log p(candidate) over the accepted positions, then
+ * first row; acc = 0 -> row 0. The root of the next step is argmax of the logits of node retrieve[best][acc]
+ * (the temperature-0 / "fast" root of [M5 二.4]).
+ */
+typedef enum { MV_GREEDY = 0, MV_TYPICAL = 1 } mv_mode;
+typedef struct mv_accept_params {
+  int32_t mode;      /* mv_mode */
+  float temperature; /* typical only, > 0 (default 0.7) */
+  float eps;         /* posterior_threshold, default 0.09 */
+  float delta;       /* posterior_alpha, default 0.3 */
+} mv_accept_params;
+
+/* Device-resident result of one verification (all int32). */
+typedef struct mv_posterior_result {
+  int32_t best;                       /* retrieve row of the best path */
+  int32_t acc;                        /* accepted candidates on it (0 .. depth) */
+  int32_t next_node;                  /* retrieve[best][acc] */
+  int32_t next_root;                  /* argmax of that node's logits */
+  int32_t n_tokens;                   /* acc + 1 */
+  int32_t nodes[MV_MAX_DEPTH + 1];    /* retrieve[best][0..acc] */
+  int32_t tokens[MV_MAX_DEPTH + 1];   /* tree_tokens[nodes[j]]: the tokens this step emits */
+} mv_posterior_result;
+
+/* logits device fp32 [n_nodes][ld] (ld >= V, ld % 4 == 0, rows 16-byte aligned); d_tree_tokens device int32
+ * [n_nodes]; d_out device mv_posterior_result; d_node_stats device fp32 [n_nodes][4] or NULL, receives
+ * (max logit, log of the softmax normaliser of z/T relative to that max, entropy H, tau) -- entries 1..3 are
+ * 0 in greedy mode; d_node_argmax device int32 [n_nodes] or NULL. */
+mv_status evaluate_posterior_workspace(int32_t n_nodes, size_t* bytes);
+mv_status evaluate_posterior(const float* logits, int32_t V, int32_t ld, const int32_t* d_tree_tokens,
+                             const mv_tree* tree, mv_accept_params params, mv_posterior_result* d_out,
+                             float* d_node_stats, int32_t* d_node_argmax, void* workspace, size_t ws_bytes,
+                             mv_stream stream);
+
+/* ============================================================================================
+ * KV compaction  [M5 二.7 update_inference_inputs()]
+ * ============================================================================================
+ * For every layer l, K/V plane c and head h:  kv[l][c][h][prefix + j] = (old) kv[l][c][h][prefix + nodes[j]]
+ * for j = 0..acc, with acc and nodes from d_res; then *d_cur_len = prefix + acc + 1. Rows are gathered before
+ * any is written, so overlapping source/destination rows are safe.
+ *   kv device bf16 [L][2][H][S_max][D]; d_cur_len device int32 [1] (may be NULL).
+ * Limits: D % 4 == 0, D <= 256, prefix_len + MV_MAX_NODES <= S_max is not required but every accessed row
+ * (prefix + nodes[j]) must be < S_max (checked on the device: MV_ERR_DEVICE).
+ */
+mv_status kv_compact(mv_bf16* kv, int32_t L, int32_t H, int32_t S_max, int32_t D, int32_t prefix_len,
+                     const mv_posterior_result* d_res, int32_t* d_cur_len, mv_stream stream);
+
+/* ============================================================================================
+ * Errors
+ * ============================================================================================
+ * Returns MV_OK if the current device's error word is clear, else MV_ERR_DEVICE and stores the word in *code
+ * (high 16 bits: the kernel site, low 16 bits: 1 = bounded wait expired, 2 = index out of range), then clears
+ * it. Synchronises the current device. */
+mv_status mv_get_error(uint32_t* code);
+/* Human-readable name of a status. */
+const char* mv_status_string(mv_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MEDUSA_VERIFY_H */

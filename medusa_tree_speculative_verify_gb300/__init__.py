@@ -1,0 +1,220 @@
+"""Python binding of libmedusa_verify.so: argument marshalling only.
+
+Every entry point has the name of its C function (see include/medusa_verify.h)
+and passes torch tensors as raw device pointers on the current CUDA stream.
+All computation happens in the library's kernels; if the library is missing
+or fails to load, :func:`lib` raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from .build import LIB, build
+
+__all__ = ["lib", "MVError", "Tree", "AcceptParams", "PosteriorResult", "GREEDY", "TYPICAL",
+           "medusa_heads_topk", "medusa_heads_topk_workspace", "build_candidates", "tree_attention",
+           "tree_attention_workspace", "evaluate_posterior", "evaluate_posterior_workspace", "kv_compact",
+           "get_error", "MAX_NODES", "MAX_DEPTH", "EXPORTED_SYMBOLS"]
+
+MAX_NODES = 64
+MAX_DEPTH = 8
+GREEDY, TYPICAL = 0, 1
+
+_lib = None
+
+
+class MVError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        name = _lib.mv_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{what}: {name} (status {status})")
+
+
+class TreeDesc(ctypes.Structure):
+    _fields_ = [("n_nodes", ctypes.c_int32), ("n_paths", ctypes.c_int32), ("depth", ctypes.c_int32),
+                ("topk", ctypes.c_int32),
+                ("tree_indices", ctypes.POINTER(ctypes.c_int32)), ("position_ids", ctypes.POINTER(ctypes.c_int32)),
+                ("retrieve", ctypes.POINTER(ctypes.c_int32)), ("parent", ctypes.POINTER(ctypes.c_int32)),
+                ("ancestors", ctypes.POINTER(ctypes.c_uint64)),
+                ("d_tree_indices", ctypes.c_void_p), ("d_position_ids", ctypes.c_void_p),
+                ("d_retrieve", ctypes.c_void_p), ("d_parent", ctypes.c_void_p), ("d_ancestors", ctypes.c_void_p)]
+
+
+class AcceptParams(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("temperature", ctypes.c_float), ("eps", ctypes.c_float),
+                ("delta", ctypes.c_float)]
+
+    def __init__(self, mode=GREEDY, temperature=0.7, eps=0.09, delta=0.3):
+        super().__init__(mode, temperature, eps, delta)
+
+
+class PosteriorResult(ctypes.Structure):
+    _fields_ = [("best", ctypes.c_int32), ("acc", ctypes.c_int32), ("next_node", ctypes.c_int32),
+                ("next_root", ctypes.c_int32), ("n_tokens", ctypes.c_int32),
+                ("nodes", ctypes.c_int32 * (MAX_DEPTH + 1)), ("tokens", ctypes.c_int32 * (MAX_DEPTH + 1))]
+
+
+RESULT_INTS = ctypes.sizeof(PosteriorResult) // 4
+
+_P, _I, _U, _F, _S = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_float, ctypes.c_size_t
+_SIGS = {
+    "mv_tree_create": ([_P, _P, _I, _I, ctypes.POINTER(_P)], _I),
+    "mv_tree_describe": ([_P, ctypes.POINTER(TreeDesc)], _I),
+    "mv_tree_destroy": ([_P], None),
+    "medusa_heads_topk_workspace": ([_I, _I, _I, _I, _I, ctypes.POINTER(_S)], _I),
+    "medusa_heads_topk": ([_P, _I, _I, _I, _P, _P, _I, _I, _P, _P, _P, _P, _P, _S, _P], _I),
+    "build_candidates": ([_P, _P, _I, _I, _P, _P, _P, _P], _I),
+    "tree_attention_workspace": ([_I, _I, _I, _I, ctypes.POINTER(_S)], _I),
+    "tree_attention": ([_P, _P, _P, _I, _I, _I, _I, _P, _F, _P, _P, _S, _P], _I),
+    "evaluate_posterior_workspace": ([_I, ctypes.POINTER(_S)], _I),
+    "evaluate_posterior": ([_P, _I, _I, _P, _P, AcceptParams, _P, _P, _P, _P, _S, _P], _I),
+    "kv_compact": ([_P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
+    "mv_get_error": ([ctypes.POINTER(_U)], _I),
+    "mv_status_string": ([_I], ctypes.c_char_p),
+}
+EXPORTED_SYMBOLS = tuple(_SIGS)
+
+
+def lib(auto_build: bool = True):
+    """The loaded library (built first if missing or stale and ``auto_build``)."""
+    global _lib
+    if _lib is None:
+        if auto_build:
+            build()
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"{LIB} is missing: build it with medusa_tree_speculative_verify_gb300.build.build()")
+        L = ctypes.CDLL(LIB)
+        for name, (args, res) in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes, f.restype = args, res
+        _lib = L
+    return _lib
+
+
+def _check(status, what):
+    if status != 0:
+        raise MVError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Tree:
+    """A static token tree (owned library handle) built from rank tuples (root excluded)."""
+
+    def __init__(self, choices, topk):
+        L = lib()
+        ranks = [int(r) for c in choices for r in c]
+        lens = [len(c) for c in choices]
+        ra = (ctypes.c_int32 * max(1, len(ranks)))(*ranks)
+        la = (ctypes.c_int32 * max(1, len(lens)))(*lens)
+        h = ctypes.c_void_p()
+        _check(L.mv_tree_create(ra, la, len(lens), topk, ctypes.byref(h)), "mv_tree_create")
+        self.handle = h
+        d = TreeDesc()
+        _check(L.mv_tree_describe(h, ctypes.byref(d)), "mv_tree_describe")
+        self.n_nodes, self.n_paths, self.depth, self.topk = d.n_nodes, d.n_paths, d.depth, d.topk
+        arr = lambda p, n: np.ctypeslib.as_array(p, shape=(n,)).copy()
+        self.tree_indices = arr(d.tree_indices, self.n_nodes)
+        self.position_ids = arr(d.position_ids, self.n_nodes)
+        self.retrieve = arr(d.retrieve, self.n_paths * (self.depth + 1)).reshape(self.n_paths, self.depth + 1)
+        self.parent = arr(d.parent, self.n_nodes)
+        self.ancestors = arr(d.ancestors, self.n_nodes)
+        self.d_ancestors = d.d_ancestors
+
+    def attn_mask(self):
+        n = self.n_nodes
+        return np.array([[(int(self.ancestors[i]) >> j) & 1 for j in range(n)] for i in range(n)], dtype=np.uint8)
+
+    def __del__(self):
+        if getattr(self, "handle", None) is not None and _lib is not None:
+            _lib.mv_tree_destroy(self.handle)
+            self.handle = None
+
+
+def _ws_size(fn, *args):
+    n = ctypes.c_size_t()
+    _check(fn(*args, ctypes.byref(n)), fn.__name__)
+    return n.value
+
+
+def medusa_heads_topk_workspace(B, d, K, V, topk):
+    return _ws_size(lib().medusa_heads_topk_workspace, B, d, K, V, topk)
+
+
+def medusa_heads_topk(h, w1, w2, topk, out_idx, out_val=None, w_lm=None, out_root=None, workspace=None,
+                      stream=None):
+    """h bf16 [B,d]; w1 bf16 [K,d,d]; w2 bf16 [K,V,d]; out_idx int32 [B,K,topk]; out_val fp32 [B,K,topk]."""
+    B, d = h.shape
+    K, V = w2.shape[0], w2.shape[1]
+    _check(lib().medusa_heads_topk(_ptr(h), B, d, K, _ptr(w1), _ptr(w2), V, topk, _ptr(w_lm), _ptr(out_idx),
+                                   _ptr(out_val), _ptr(out_root), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "medusa_heads_topk")
+
+
+def build_candidates(root, head_topk, tree: Tree, tree_tokens, cart=None, stream=None):
+    """root int32 [1]; head_topk int32 [K, ld]; tree_tokens int32 [n]; cart int32 [paths, depth+1]."""
+    K, ld = head_topk.shape
+    _check(lib().build_candidates(_ptr(root), _ptr(head_topk), K, ld, tree.handle, _ptr(tree_tokens), _ptr(cart),
+                                  _stream(stream)), "build_candidates")
+
+
+def tree_attention_workspace(H, D, S_max, n_nodes):
+    return _ws_size(lib().tree_attention_workspace, H, D, S_max, n_nodes)
+
+
+def tree_attention(q, k_cache, v_cache, prefix_len, tree: Tree, scale, out, workspace, stream=None):
+    """q bf16 [n,H,D]; k_cache/v_cache bf16 [H,S_max,D]; out bf16 [n,H,D]."""
+    H, S_max, D = k_cache.shape
+    _check(lib().tree_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), H, D, S_max, prefix_len, tree.handle,
+                                float(scale), _ptr(out), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream)), "tree_attention")
+
+
+def evaluate_posterior_workspace(n_nodes):
+    return _ws_size(lib().evaluate_posterior_workspace, n_nodes)
+
+
+def evaluate_posterior(logits, tree_tokens, tree: Tree, params: AcceptParams, out, workspace, node_stats=None,
+                       node_argmax=None, stream=None):
+    """logits fp32 [n, ld] (first V columns used, V = logits.shape[1] unless sliced); out int32 [RESULT_INTS]."""
+    n, V = logits.shape
+    ld = logits.stride(0)
+    _check(lib().evaluate_posterior(_ptr(logits), V, ld, _ptr(tree_tokens), tree.handle, params, _ptr(out),
+                                    _ptr(node_stats), _ptr(node_argmax), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)),
+           "evaluate_posterior")
+
+
+def kv_compact(kv, prefix_len, result, cur_len=None, stream=None):
+    """kv bf16 [L,2,H,S_max,D]; result: the int32 posterior result buffer; cur_len int32 [1]."""
+    L, two, H, S_max, D = kv.shape
+    assert two == 2
+    _check(lib().kv_compact(_ptr(kv), L, H, S_max, D, prefix_len, _ptr(result), _ptr(cur_len), _stream(stream)),
+           "kv_compact")
+
+
+def get_error():
+    """(status, code): reads and clears the device error word (synchronises the device)."""
+    code = ctypes.c_uint32()
+    st = lib().mv_get_error(ctypes.byref(code))
+    return st, code.value
+
+
+def result_dict(buf):
+    """Decode a PosteriorResult from an int32 tensor / array of RESULT_INTS entries."""
+    a = np.asarray(buf.cpu() if hasattr(buf, "cpu") else buf, dtype=np.int32)
+    r = PosteriorResult.from_buffer_copy(a.tobytes())
+    return dict(best=r.best, acc=r.acc, next_node=r.next_node, next_root=r.next_root, n_tokens=r.n_tokens,
+                nodes=list(r.nodes)[: r.acc + 1], tokens=list(r.tokens)[: r.acc + 1])

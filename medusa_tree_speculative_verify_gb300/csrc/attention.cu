@@ -1,0 +1,416 @@
+// Tree attention: every tree node attends to the whole cached prefix and to its own root-to-node path.
+//
+// "大模型推理 memory bandwidth bound (5) - Medusa", 一.2 Tree attention and 二.5 tree_decoding(): the tree is
+// flattened into a sequence after the prefix; the mask lets node i see only its ancestors and itself
+// ("Phi-3-mini-128k-instruct_rai_1.8.0_medusa_1.0_npu", 4️⃣: siblings never see each other). The mask is one
+// 64-bit ancestor word per node; only the key tile(s) that hold the tree block consult it.
+//
+// Layout: q [n][H][D] bf16, K/V caches as planes of [H][S_max][D] bf16. One CTA = one head x one range of
+// 64-key tiles (split-KV so that H x splits fills the GPU at batch 1). 4 warps, each owning 16 of the (up to)
+// 64 tree queries. KV tiles arrive by TMA (128-byte swizzle, 3-stage mbarrier ring); Q.K^T and P.V run on the
+// tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate); the softmax is an online (running max / sum)
+// softmax in registers. With several splits, the last CTA of a head (atomic ticket) merges the partial
+// (max, sum, output) triples.
+#include <float.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kKeys = 64;   // keys per tile
+constexpr int kRows = 64;   // query rows per CTA (tree nodes, padded)
+constexpr int kStages = 3;
+
+MV_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+MV_DEV void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+MV_DEV void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Byte offset of 16-byte chunk c of row r in a [64 rows][D] bf16 tile. D >= 64: sub-tiles of 64 columns,
+// 128-byte rows, 16-byte chunks XOR-swizzled by (row % 8) (the TMA 128B pattern). D < 64: plain rows.
+template <int D>
+MV_DEV uint32_t tile_off(int r, int c) {
+  if constexpr (D >= 64) {
+    return (uint32_t)((c >> 3) * (64 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+  } else {
+    return (uint32_t)(r * (D * 2) + c * 16);
+  }
+}
+
+struct AttnArgs {
+  const uint16_t* q;        // [n][H][D]
+  uint16_t* out;            // [n][H][D]
+  const uint64_t* anc;      // [n]
+  const int32_t* d_prefix;  // device prefix length or null
+  int prefix;               // used when d_prefix is null
+  int H, S_max, n, splits, plane_k, plane_v;
+  float scale_log2;         // scale * log2(e)
+  float* opart;             // [H][splits][64][D]
+  float* ml;                // [H][splits][64][2]
+  unsigned int* tickets;    // [H]
+  unsigned int* err;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                             const __grid_constant__ CUtensorMap vmap,
+                                                             const AttnArgs a) {
+  constexpr int kTileBytes = kKeys * D * 2;
+  constexpr int kBoxCols = D >= 64 ? 64 : D;
+  constexpr int kBoxes = D / kBoxCols;
+  constexpr int KS = D / 16;  // k-steps over the head dim
+  constexpr int DN = D / 8;   // n-tiles over the head dim
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sq = smem;                                  // [64][D]
+  uint8_t* sk = smem + kTileBytes;                     // kStages x [64][D]
+  uint8_t* sv = sk + kStages * kTileBytes;             // kStages x [64][D]
+  __shared__ __align__(8) uint64_t full[kStages];
+  __shared__ bool s_last;
+
+  const int h = blockIdx.x, split = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int P = a.d_prefix ? *a.d_prefix : a.prefix;
+  const int n = a.n;
+  if (P < 0 || P + n > a.S_max) {
+    if (tid == 0) mv_set_error(a.err, 4, MV_DEVERR_INDEX);
+    return;
+  }
+  const int total_tiles = (P + n + kKeys - 1) / kKeys;
+  const int t_begin = (int)((long long)split * total_tiles / a.splits);
+  const int t_end = (int)((long long)(split + 1) * total_tiles / a.splits);
+  const int count = t_end - t_begin;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+    mbar_fence_init();
+  }
+  // Q: plain 16-byte loads into the tile layout (rows >= n are zero)
+  for (int e = tid; e < kRows * (D / 8); e += kThreads) {
+    const int r = e / (D / 8), c = e % (D / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < n) v = *reinterpret_cast<const uint4*>(a.q + ((size_t)r * a.H + h) * D + c * 8);
+    *reinterpret_cast<uint4*>(sq + tile_off<D>(r, c)) = v;
+  }
+  __syncthreads();
+
+  auto issue = [&](int i) {  // tile t_begin + i into stage i % kStages
+    const int st = i % kStages, key0 = (t_begin + i) * kKeys;
+    mbar_arrive_expect_tx(&full[st], 2 * kTileBytes);
+#pragma unroll
+    for (int b = 0; b < kBoxes; ++b) {
+      tma_load_4d(sk + st * kTileBytes + b * (kKeys * kBoxCols * 2), &kmap, &full[st], b * kBoxCols, key0, h,
+                  a.plane_k);
+      tma_load_4d(sv + st * kTileBytes + b * (kKeys * kBoxCols * 2), &vmap, &full[st], b * kBoxCols, key0, h,
+                  a.plane_v);
+    }
+  };
+  if (tid == 0)
+    for (int i = 0; i < kStages && i < count; ++i) issue(i);
+
+  // Q fragments for this warp's 16 rows
+  uint32_t qa[KS][4];
+  const uint32_t sq_base = smem_u32(sq);
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    const int m = lane >> 3;
+    const int r = warp * 16 + 8 * (m & 1) + (lane & 7);
+    ldsm_x4(sq_base + tile_off<D>(r, 2 * ks + (m >> 1)), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+  }
+  const int q0 = warp * 16 + g, q1 = q0 + 8;
+  const uint64_t anc0 = q0 < n ? a.anc[q0] : 0ull, anc1 = q1 < n ? a.anc[q1] : 0ull;
+
+  float o[DN][4];
+#pragma unroll
+  for (int i = 0; i < DN; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+  bool ok = true;
+  int stop = 0;  // first tile not consumed (set when a wait expires)
+
+  for (int i = 0; i < count; ++i) {
+    const int st = i % kStages;
+    const bool got = mbar_wait(&full[st], (uint32_t)((i / kStages) & 1));
+    if (__syncthreads_or(!got)) {
+      if (tid == 0) mv_set_error(a.err, 4, MV_DEVERR_TIMEOUT);
+      ok = false;
+      stop = i;
+      break;
+    }
+    const uint32_t kb = smem_u32(sk + st * kTileBytes), vb = smem_u32(sv + st * kTileBytes);
+    const int key0 = (t_begin + i) * kKeys;
+    // S = Q K^T for 16 rows x 64 keys
+    float s[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {  // pairs of 8-key n-tiles
+        const int m = lane >> 3;
+        const int key = 16 * np + 8 * (m >> 1) + (lane & 7);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + tile_off<D>(key, 2 * ks + (m & 1)), b0, b1, b2, b3);
+        mma_bf16(s[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+        mma_bf16(s[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+      }
+    }
+    // mask + running max
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = key0 + 8 * nt + 2 * t4 + e;
+        const int tj = key - P;  // tree node index if >= 0
+        const bool v0 = key < P || (tj < n && ((anc0 >> tj) & 1ull));
+        const bool v1 = key < P || (tj < n && ((anc1 >> tj) & 1ull));
+        s[nt][e] = v0 ? s[nt][e] * a.scale_log2 : -INFINITY;
+        s[nt][2 + e] = v1 ? s[nt][2 + e] * a.scale_log2 : -INFINITY;
+        mx0 = fmaxf(mx0, s[nt][e]);
+        mx1 = fmaxf(mx1, s[nt][2 + e]);
+      }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float nm0 = fmaxf(m0, mx0), nm1 = fmaxf(m1, mx1);
+    const float base0 = nm0 == -INFINITY ? 0.0f : nm0, base1 = nm1 == -INFINITY ? 0.0f : nm1;
+    const float c0 = exp2f(m0 - base0), c1 = exp2f(m1 - base1);
+    m0 = nm0;
+    m1 = nm1;
+    float rs0 = 0.0f, rs1 = 0.0f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      s[nt][0] = exp2f(s[nt][0] - base0);
+      s[nt][1] = exp2f(s[nt][1] - base0);
+      s[nt][2] = exp2f(s[nt][2] - base1);
+      s[nt][3] = exp2f(s[nt][3] - base1);
+      rs0 += s[nt][0] + s[nt][1];
+      rs1 += s[nt][2] + s[nt][3];
+    }
+    l0 = l0 * c0 + rs0;
+    l1 = l1 * c1 + rs1;
+#pragma unroll
+    for (int dn = 0; dn < DN; ++dn) {
+      o[dn][0] *= c0;
+      o[dn][1] *= c0;
+      o[dn][2] *= c1;
+      o[dn][3] *= c1;
+    }
+    // O += P V
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint32_t p0 = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
+      const uint32_t p1 = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
+      const uint32_t p2 = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      const uint32_t p3 = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+      for (int dp = 0; dp < DN / 2; ++dp) {
+        const int m = lane >> 3;
+        const int key = 16 * kk + 8 * (m & 1) + (lane & 7);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vb + tile_off<D>(key, 2 * dp + (m >> 1)), b0, b1, b2, b3);
+        mma_bf16(o[2 * dp], p0, p1, p2, p3, b0, b1);
+        mma_bf16(o[2 * dp + 1], p0, p1, p2, p3, b2, b3);
+      }
+    }
+    __syncthreads();  // every warp is done with this stage
+    if (tid == 0 && i + kStages < count) issue(i + kStages);
+  }
+  if (!ok) {
+    // Let the copies already issued land before the CTA's shared memory goes away: tiles [stop, issued)
+    // are in flight, each on its stage's barrier at its own phase. Every wait here is bounded too.
+    if (tid == 0) {
+      const int issued = min(count, stop + kStages);
+      for (int j = stop; j < issued; ++j)
+        if (!mbar_wait(&full[j % kStages], (uint32_t)((j / kStages) & 1))) break;
+    }
+    __syncthreads();
+    return;
+  }
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+  if (a.splits == 1) {
+    const float i0 = l0 > 0.0f ? 1.0f / l0 : 0.0f, i1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
+#pragma unroll
+    for (int dn = 0; dn < DN; ++dn) {
+      const int col = 8 * dn + 2 * t4;
+      if (q0 < n)
+        *reinterpret_cast<uint32_t*>(a.out + ((size_t)q0 * a.H + h) * D + col) =
+            pack_bf16x2(o[dn][0] * i0, o[dn][1] * i0);
+      if (q1 < n)
+        *reinterpret_cast<uint32_t*>(a.out + ((size_t)q1 * a.H + h) * D + col) =
+            pack_bf16x2(o[dn][2] * i1, o[dn][3] * i1);
+    }
+    return;
+  }
+
+  // ---- split-KV: store the partial triple, the last CTA of the head merges
+  float* op = a.opart + ((size_t)h * a.splits + split) * kRows * D;
+#pragma unroll
+  for (int dn = 0; dn < DN; ++dn) {
+    const int col = 8 * dn + 2 * t4;
+    *reinterpret_cast<float2*>(op + (size_t)q0 * D + col) = make_float2(o[dn][0], o[dn][1]);
+    *reinterpret_cast<float2*>(op + (size_t)q1 * D + col) = make_float2(o[dn][2], o[dn][3]);
+  }
+  if (t4 == 0) {
+    float* mlp = a.ml + ((size_t)h * a.splits + split) * kRows * 2;
+    mlp[q0 * 2 + 0] = m0;
+    mlp[q0 * 2 + 1] = l0;
+    mlp[q1 * 2 + 0] = m1;
+    mlp[q1 * 2 + 1] = l1;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(a.tickets + h, 1u) == (unsigned)(a.splits - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int e = tid; e < n * (D / 4); e += kThreads) {
+    const int q = e / (D / 4), c4 = (e % (D / 4)) * 4;
+    float M = -INFINITY;
+    for (int sp = 0; sp < a.splits; ++sp)
+      M = fmaxf(M, __ldcg(a.ml + (((size_t)h * a.splits + sp) * kRows + q) * 2));
+    const float base = M == -INFINITY ? 0.0f : M;
+    float L = 0.0f, acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int sp = 0; sp < a.splits; ++sp) {
+      const float* mlp = a.ml + (((size_t)h * a.splits + sp) * kRows + q) * 2;
+      const float w = exp2f(__ldcg(mlp) - base);
+      L += w * __ldcg(mlp + 1);
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(
+          a.opart + (((size_t)h * a.splits + sp) * kRows + q) * D + c4));
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
+      acc[2] += w * v.z;
+      acc[3] += w * v.w;
+    }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    uint2 pk;
+    pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(a.out + ((size_t)q * a.H + h) * D + c4) = pk;
+  }
+  if (tid == 0) a.tickets[h] = 0u;
+}
+
+int choose_splits(int H, int max_tiles) {
+  const int sms = mv_sm_count();
+  int s = std::max(1, (2 * sms + H - 1) / H);
+  s = std::min(s, std::max(1, (max_tiles + 1) / 2));
+  return std::min(s, 64);
+}
+
+size_t smem_bytes(int D) { return 1024 + (size_t)(1 + 2 * kStages) * kKeys * D * 2; }
+
+}  // namespace
+
+size_t tree_attn_ws_bytes(int H, int D, int S_max, int n_nodes) {
+  (void)n_nodes;
+  const int splits = choose_splits(H, (S_max + kKeys - 1) / kKeys);
+  return 256 + (size_t)H * 4 + (size_t)H * splits * kRows * (D + 2) * sizeof(float) + 256;
+}
+
+bool tree_attn_make_maps(CUtensorMap* kmap, CUtensorMap* vmap, const void* k_cache, const void* v_cache, int H,
+                         int D, int S_max, int planes, size_t plane_stride_bytes) {
+  const uint64_t dims[4] = {(uint64_t)D, (uint64_t)S_max, (uint64_t)H, (uint64_t)planes};
+  const uint64_t strides[3] = {(uint64_t)D * 2, (uint64_t)S_max * D * 2, (uint64_t)plane_stride_bytes};
+  const uint32_t box[4] = {(uint32_t)(D >= 64 ? 64 : D), (uint32_t)kKeys, 1, 1};
+  const CUtensorMapSwizzle sw = D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  return mv_encode_tmap(kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k_cache, dims, strides, box, sw) &&
+         mv_encode_tmap(vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v_cache, dims, strides, box, sw);
+}
+
+mv_status launch_tree_attention(const CUtensorMap& kmap, const CUtensorMap& vmap, int plane_k, int plane_v,
+                                const mv_bf16* q, int H, int D, int S_max, const int32_t* d_prefix, int prefix,
+                                int max_prefix, const mv_tree* t, float scale, mv_bf16* out, void* ws,
+                                cudaStream_t stream) {
+  const int max_tiles = (max_prefix + t->n_nodes + kKeys - 1) / kKeys;
+  const int ws_splits = choose_splits(H, (S_max + kKeys - 1) / kKeys);
+  const int splits = std::min(ws_splits, choose_splits(H, max_tiles));
+  char* p = static_cast<char*>(ws);
+  AttnArgs a{};
+  a.q = q;
+  a.out = out;
+  a.anc = t->d_ancestors;
+  a.d_prefix = d_prefix;
+  a.prefix = prefix;
+  a.H = H;
+  a.S_max = S_max;
+  a.n = t->n_nodes;
+  a.splits = splits;
+  a.plane_k = plane_k;
+  a.plane_v = plane_v;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.tickets = reinterpret_cast<unsigned int*>(p);
+  a.opart = reinterpret_cast<float*>(p + 256 + (size_t)H * 4 + 255 - ((256 + (size_t)H * 4 + 255) % 256));
+  a.ml = a.opart + (size_t)H * ws_splits * kRows * D;
+  a.err = mv_error_word();
+  const size_t smem = smem_bytes(D);
+  const dim3 grid(H, splits);
+  switch (D) {
+#define MV_ATTN_CASE(DD)                                                                                 \
+  case DD:                                                                                             \
+    if (cudaFuncSetAttribute(tree_attn_kernel<DD>, cudaFuncAttributeMaxDynamicSharedMemorySize,         \
+                             (int)smem) != cudaSuccess)                                                \
+      return MV_ERR_CUDA;                                                                              \
+    tree_attn_kernel<DD><<<grid, kThreads, smem, stream>>>(kmap, vmap, a);                             \
+    break;
+    MV_ATTN_CASE(16)
+    MV_ATTN_CASE(32)
+    MV_ATTN_CASE(64)
+    MV_ATTN_CASE(128)
+#undef MV_ATTN_CASE
+    default:
+      return MV_ERR_SHAPE;
+  }
+  return mv_last_launch("tree_attention");
+}
+
+extern "C" mv_status tree_attention_workspace(int32_t H, int32_t D, int32_t S_max, int32_t n_nodes, size_t* bytes) {
+  if (!bytes || H < 1 || H > 256 || S_max < 1 || n_nodes < 1 || n_nodes > MV_MAX_NODES) return MV_ERR_INVALID_ARG;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return MV_ERR_SHAPE;
+  *bytes = tree_attn_ws_bytes(H, D, S_max, n_nodes);
+  return MV_OK;
+}
+
+extern "C" mv_status tree_attention(const mv_bf16* q, const mv_bf16* k_cache, const mv_bf16* v_cache, int32_t H,
+                                    int32_t D, int32_t S_max, int32_t prefix_len, const mv_tree* tree, float scale,
+                                    mv_bf16* out, void* workspace, size_t ws_bytes, mv_stream stream) {
+  if (!q || !k_cache || !v_cache || !tree || !out || !workspace) return MV_ERR_INVALID_ARG;
+  if (!tree->d_ancestors) return MV_ERR_CUDA;
+  size_t need = 0;
+  mv_status s = tree_attention_workspace(H, D, S_max, tree->n_nodes, &need);
+  if (s != MV_OK) return s;
+  if (prefix_len < 0 || prefix_len + tree->n_nodes > S_max) return MV_ERR_CAPACITY;
+  if (ws_bytes < need) return MV_ERR_CAPACITY;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(out)) & 15)
+    return MV_ERR_SHAPE;
+  CUtensorMap kmap, vmap;
+  if (!tree_attn_make_maps(&kmap, &vmap, k_cache, v_cache, H, D, S_max, 1, (size_t)H * S_max * D * 2))
+    return MV_ERR_CUDA;
+  return launch_tree_attention(kmap, vmap, 0, 0, q, H, D, S_max, nullptr, prefix_len, prefix_len, tree, scale, out,
+                               workspace, static_cast<cudaStream_t>(stream));
+}

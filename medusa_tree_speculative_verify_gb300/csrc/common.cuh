@@ -1,0 +1,141 @@
+// Shared device helpers for the Medusa tree-verify kernels (sm_103a).
+//
+// * status / error word: every bounded wait or index check that fails writes a
+//   code into one device word (first error wins) and the kernel returns early;
+//   mv_get_error() reads and clears it.
+// * PTX wrappers for mbarrier, TMA (cp.async.bulk.tensor) and tcgen05.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "medusa_verify.h"
+
+#define MV_DEV __device__ __forceinline__
+
+// error codes written to the device error word (high 16 bits: site, low 16 bits: kind)
+enum : uint32_t {
+  MV_DEVERR_TIMEOUT = 1,   // a bounded wait expired
+  MV_DEVERR_INDEX = 2,     // an index read from device memory was out of range
+};
+
+// Device error word of the current device (library-owned, no allocation: a __device__ symbol).
+unsigned int* mv_error_word();
+// Host-side helpers.
+mv_status mv_last_launch(const char* what);
+int mv_sm_count();
+
+MV_DEV void mv_set_error(unsigned int* err, uint32_t site, uint32_t kind) {
+  if (err) atomicCAS(err, 0u, (site << 16) | kind);
+}
+
+MV_DEV uint64_t mv_globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Upper bound of every spin wait in these kernels (nanoseconds of %globaltimer).
+#define MV_WAIT_LIMIT_NS 2000000000ull
+
+MV_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// ------------------------------------------------------------------------------------------
+// mbarrier
+// ------------------------------------------------------------------------------------------
+MV_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+MV_DEV void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+MV_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+MV_DEV void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+MV_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of `bar` to complete; false if MV_WAIT_LIMIT_NS passed first.
+MV_DEV bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = mv_globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (mv_globaltimer() - t0 > MV_WAIT_LIMIT_NS) return false;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// TMA (tiled tensor copies global -> shared, completion counted on an mbarrier)
+// ------------------------------------------------------------------------------------------
+MV_DEV void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+MV_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+MV_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+MV_DEV void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], [%2];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3)
+      : "memory");
+}
+
+// ------------------------------------------------------------------------------------------
+// small numeric helpers
+// ------------------------------------------------------------------------------------------
+MV_DEV float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+MV_DEV float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+MV_DEV uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&t);
+}
+MV_DEV float silu(float x) { return x / (1.0f + expf(-x)); }
+
+// (value, index) order used by every top-k / argmax here: larger value first, then lower index.
+MV_DEV bool vi_better(float va, int ia, float vb, int ib) { return va > vb || (va == vb && ia < ib); }
+
+// Host-side tensor-map encoder (driver entry point fetched through the runtime; no -lcuda).
+// Encodes a bf16 / fp32 tiled map with dims[0] innermost. Returns false on failure.
+bool mv_encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                    const uint64_t* dims, const uint64_t* strides_bytes /* rank-1 entries */,
+                    const uint32_t* box, CUtensorMapSwizzle swizzle);
+
+// Host-side view of a tree handle (defined in tree.cpp).
+struct mv_tree {
+  int32_t n_nodes, n_paths, depth, topk;
+  int32_t* h_tree_indices;
+  int32_t* h_position_ids;
+  int32_t* h_retrieve;
+  int32_t* h_parent;
+  uint64_t* h_ancestors;
+  int32_t* d_tree_indices;
+  int32_t* d_position_ids;
+  int32_t* d_retrieve;
+  int32_t* d_parent;
+  uint64_t* d_ancestors;
+  int device;
+};

@@ -1,0 +1,37 @@
+// Internal launchers shared between the standalone entry points and the whole verify step.
+#pragma once
+
+#include "common.cuh"
+
+mv_status launch_build_candidates(const int32_t* d_root, const int32_t* d_head_topk, int ld_topk, const mv_tree* t,
+                                  int32_t* d_tree_tokens, int32_t* d_cart, cudaStream_t stream);
+
+size_t posterior_ws_bytes(int n_nodes);
+mv_status launch_posterior(const float* logits, int V, int ld, const int32_t* d_tree_tokens, const mv_tree* t,
+                           mv_accept_params prm, mv_posterior_result* d_out, float* d_stats, int32_t* d_argmax,
+                           void* ws, cudaStream_t stream);
+
+// prefix from d_prefix if non-null, else `prefix`
+mv_status launch_kv_compact(mv_bf16* kv, int L, int H, int S_max, int D, const int32_t* d_prefix, int prefix,
+                            const mv_posterior_result* d_res, int32_t* d_cur_len, cudaStream_t stream);
+
+int heads_w2_ctas_per_mat(int n_mat, int V);
+size_t heads_ws_bytes(int B, int d, int K, int V, int topk);
+// h (bf16 [B][d]) or, in step mode, x (fp32 rows) + res: h = RMSNorm(x[res->next_node]); commit_len (step mode)
+// receives += res->n_tokens.
+mv_status launch_heads(const uint16_t* h, const float* x, const mv_posterior_result* res, float norm_eps, int B,
+                       int d, int K, const uint16_t* w1, const uint16_t* w2, int V, int topk, const uint16_t* w_lm,
+                       int32_t* out_idx, float* out_val, int32_t* out_root, int32_t* commit_len, void* ws,
+                       cudaStream_t stream);
+
+// Tree attention over one layer. k/v tensor maps cover [H][S_max][D] planes; prefix from d_prefix if non-null.
+struct TreeAttnPlan {
+  int H, D, S_max, n_nodes, splits;
+};
+size_t tree_attn_ws_bytes(int H, int D, int S_max, int n_nodes);
+bool tree_attn_make_maps(CUtensorMap* kmap, CUtensorMap* vmap, const void* k_cache, const void* v_cache, int H,
+                         int D, int S_max, int planes, size_t plane_stride_bytes);
+mv_status launch_tree_attention(const CUtensorMap& kmap, const CUtensorMap& vmap, int plane_k, int plane_v,
+                                const mv_bf16* q, int H, int D, int S_max, const int32_t* d_prefix, int prefix,
+                                int max_prefix, const mv_tree* t, float scale, mv_bf16* out, void* ws,
+                                cudaStream_t stream);

@@ -1,0 +1,248 @@
+// Posterior evaluation over the tree's logits: greedy or typical acceptance, best path, emitted tokens.
+//
+// "大模型推理 memory bandwidth bound (5) - Medusa", 一.3 Typical acceptance and 二.6 evaluate_posterior().
+// The page re-gathers the logits per path ([paths, depth+1, V]) before evaluating; here the per-node statistics
+// are computed once per tree node (each node's row is read once) and the per-path walk reads only the
+// candidate's own logit.
+//
+// One CTA per node row: pass 1 (max, first argmax, softmax normaliser of z/T by online rescaling), pass 2
+// (entropy, typical only; the row is then L1/L2-resident). The last CTA to finish (atomic ticket, no waiting)
+// walks the paths and writes the result.
+#include <float.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace {
+
+constexpr int kThreads = 512;
+
+struct Stat {
+  float m;  // running max of z
+  int i;    // first index of the max
+  float s;  // sum of exp((z - m) / T)
+};
+
+MV_DEV void stat_push(Stat& a, float z, int idx, float inv_t, bool typical) {
+  if (z > a.m) {
+    if (typical) a.s = a.s * expf((a.m - z) * inv_t) + 1.0f;
+    a.m = z;
+    a.i = idx;
+  } else {
+    if (typical) a.s += expf((z - a.m) * inv_t);
+    if (z == a.m && idx < a.i) a.i = idx;
+  }
+}
+
+MV_DEV Stat stat_merge(Stat a, Stat b, float inv_t, bool typical) {
+  Stat r;
+  if (b.m > a.m || (b.m == a.m && b.i < a.i)) {
+    r.m = b.m;
+    r.i = b.i;
+  } else {
+    r.m = a.m;
+    r.i = a.i;
+  }
+  if (typical) {
+    const float sa = a.s == 0.0f ? 0.0f : a.s * expf((a.m - r.m) * inv_t);
+    const float sb = b.s == 0.0f ? 0.0f : b.s * expf((b.m - r.m) * inv_t);
+    r.s = sa + sb;
+  } else {
+    r.s = 0.0f;
+  }
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads) posterior_kernel(
+    const float* __restrict__ logits, int V, int ld, const int32_t* __restrict__ tree_tokens,
+    const int32_t* __restrict__ retrieve, int n_nodes, int n_paths, int width, mv_accept_params prm,
+    mv_posterior_result* __restrict__ out, float* __restrict__ node_stats_out, int32_t* __restrict__ node_argmax_out,
+    float* __restrict__ ws_stats, int32_t* __restrict__ ws_argmax, unsigned int* __restrict__ ticket,
+    unsigned int* err) {
+  const bool typical = prm.mode == MV_TYPICAL;
+  const float inv_t = typical ? 1.0f / prm.temperature : 1.0f;
+  const int node = blockIdx.x;
+  const float* row = logits + (size_t)node * ld;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ Stat red[kThreads / 32];
+  __shared__ float fred[kThreads / 32];
+  __shared__ Stat tot;
+  __shared__ bool last;
+
+  // ---- pass 1: max, first argmax, normaliser
+  Stat a{-FLT_MAX, 0x7fffffff, 0.0f};
+  const int V4 = V >> 2;
+  const float4* row4 = reinterpret_cast<const float4*>(row);
+  for (int i = tid; i < V4; i += kThreads) {
+    const float4 z = __ldg(row4 + i);
+    stat_push(a, z.x, 4 * i + 0, inv_t, typical);
+    stat_push(a, z.y, 4 * i + 1, inv_t, typical);
+    stat_push(a, z.z, 4 * i + 2, inv_t, typical);
+    stat_push(a, z.w, 4 * i + 3, inv_t, typical);
+  }
+  for (int i = 4 * V4 + tid; i < V; i += kThreads) stat_push(a, __ldg(row + i), i, inv_t, typical);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    Stat b;
+    b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+    b.i = __shfl_xor_sync(0xffffffffu, a.i, o);
+    b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+    a = stat_merge(a, b, inv_t, typical);
+  }
+  if (lane == 0) red[warp] = a;
+  __syncthreads();
+  if (tid == 0) {
+    Stat t = red[0];
+    for (int w = 1; w < kThreads / 32; ++w) t = stat_merge(t, red[w], inv_t, typical);
+    tot = t;
+  }
+  __syncthreads();
+  const Stat T = tot;
+
+  // ---- pass 2 (typical): entropy of p = softmax(z/T), H = -sum p log(p + 1e-5)
+  float H = 0.0f, tau = 0.0f;
+  if (typical) {
+    const float inv_s = 1.0f / T.s;
+    float h = 0.0f;
+    for (int i = tid; i < V4; i += kThreads) {
+      const float4 z = __ldg(row4 + i);
+      const float p0 = expf((z.x - T.m) * inv_t) * inv_s, p1 = expf((z.y - T.m) * inv_t) * inv_s;
+      const float p2 = expf((z.z - T.m) * inv_t) * inv_s, p3 = expf((z.w - T.m) * inv_t) * inv_s;
+      h += p0 * logf(p0 + 1e-5f) + p1 * logf(p1 + 1e-5f) + p2 * logf(p2 + 1e-5f) + p3 * logf(p3 + 1e-5f);
+    }
+    for (int i = 4 * V4 + tid; i < V; i += kThreads) {
+      const float p = expf((__ldg(row + i) - T.m) * inv_t) * inv_s;
+      h += p * logf(p + 1e-5f);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
+    if (lane == 0) fred[warp] = h;
+    __syncthreads();
+    if (tid == 0) {
+      float s = 0.0f;
+      for (int w = 0; w < kThreads / 32; ++w) s += fred[w];
+      fred[0] = s;
+    }
+    __syncthreads();
+    H = -fred[0];
+    tau = fminf(prm.eps, prm.delta * expf(-H));
+  }
+
+  if (tid == 0) {
+    ws_stats[node * 4 + 0] = T.m;
+    ws_stats[node * 4 + 1] = T.s;
+    ws_stats[node * 4 + 2] = H;
+    ws_stats[node * 4 + 3] = tau;
+    ws_argmax[node] = T.i;
+    if (node_stats_out) {
+      node_stats_out[node * 4 + 0] = T.m;
+      node_stats_out[node * 4 + 1] = typical ? logf(T.s) : 0.0f;
+      node_stats_out[node * 4 + 2] = H;
+      node_stats_out[node * 4 + 3] = tau;
+    }
+    if (node_argmax_out) node_argmax_out[node] = T.i;
+    __threadfence();
+    last = atomicAdd(ticket, 1u) == (unsigned)(n_nodes - 1);
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+
+  // ---- last CTA: walk every path (one thread per path), then pick the best
+  __shared__ int s_acc[MV_MAX_NODES];
+  __shared__ float s_like[MV_MAX_NODES];
+  __shared__ int s_bad;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  if (tid < n_paths) {
+    const int32_t* r = retrieve + tid * width;
+    int acc = 0;
+    float like = 0.0f;
+    for (int j = 0; j + 1 < width; ++j) {
+      const int par = r[j], child = r[j + 1];
+      if (child < 0) break;
+      if (par < 0 || par >= n_nodes || child >= n_nodes) {
+        s_bad = 1;
+        break;
+      }
+      const int tok = tree_tokens[child];
+      if (tok < 0 || tok >= V) {
+        s_bad = 1;
+        break;
+      }
+      bool ok;
+      if (typical) {
+        const float m = __ldcg(ws_stats + par * 4 + 0), s = __ldcg(ws_stats + par * 4 + 1);
+        const float p = expf((__ldcg(logits + (size_t)par * ld + tok) - m) * inv_t) / s;
+        ok = p > __ldcg(ws_stats + par * 4 + 3);
+        if (ok) like += logf(p);
+      } else {
+        ok = tok == __ldcg(ws_argmax + par);
+      }
+      if (!ok) break;
+      ++acc;
+    }
+    s_acc[tid] = acc;
+    s_like[tid] = like;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    if (s_bad) mv_set_error(err, 3, MV_DEVERR_INDEX);
+    int best = 0;
+    for (int p = 1; p < n_paths; ++p) {
+      if (s_acc[p] > s_acc[best] || (typical && s_acc[p] == s_acc[best] && s_like[p] > s_like[best])) best = p;
+    }
+    const int acc = s_acc[best] > 0 ? s_acc[best] : 0;
+    if (acc == 0) best = 0;
+    const int32_t* r = retrieve + best * width;
+    out->best = best;
+    out->acc = acc;
+    out->n_tokens = acc + 1;
+    for (int j = 0; j <= MV_MAX_DEPTH; ++j) {
+      const int nd = j <= acc ? r[j] : -1;
+      out->nodes[j] = nd;
+      out->tokens[j] = nd >= 0 ? tree_tokens[nd] : -1;
+    }
+    const int nn = r[acc];
+    out->next_node = nn;
+    out->next_root = __ldcg(ws_argmax + nn);
+    *ticket = 0u;  // leave the counter zeroed for the next call
+  }
+}
+
+}  // namespace
+
+size_t posterior_ws_bytes(int n_nodes) { return (size_t)n_nodes * 5 * sizeof(float) + 64; }
+
+mv_status launch_posterior(const float* logits, int V, int ld, const int32_t* d_tree_tokens, const mv_tree* t,
+                           mv_accept_params prm, mv_posterior_result* d_out, float* d_stats, int32_t* d_argmax,
+                           void* ws, cudaStream_t stream) {
+  char* w = static_cast<char*>(ws);
+  unsigned int* ticket = reinterpret_cast<unsigned int*>(w);
+  float* ws_stats = reinterpret_cast<float*>(w + 64);
+  int32_t* ws_arg = reinterpret_cast<int32_t*>(w + 64 + (size_t)t->n_nodes * 4 * sizeof(float));
+  posterior_kernel<<<t->n_nodes, kThreads, 0, stream>>>(logits, V, ld, d_tree_tokens, t->d_retrieve, t->n_nodes,
+                                                        t->n_paths, t->depth + 1, prm, d_out, d_stats, d_argmax,
+                                                        ws_stats, ws_arg, ticket, mv_error_word());
+  return mv_last_launch("evaluate_posterior");
+}
+
+extern "C" mv_status evaluate_posterior_workspace(int32_t n_nodes, size_t* bytes) {
+  if (!bytes || n_nodes < 1 || n_nodes > MV_MAX_NODES) return MV_ERR_INVALID_ARG;
+  *bytes = posterior_ws_bytes(n_nodes);
+  return MV_OK;
+}
+
+extern "C" mv_status evaluate_posterior(const float* logits, int32_t V, int32_t ld, const int32_t* d_tree_tokens,
+                                        const mv_tree* tree, mv_accept_params params, mv_posterior_result* d_out,
+                                        float* d_node_stats, int32_t* d_node_argmax, void* workspace,
+                                        size_t ws_bytes, mv_stream stream) {
+  if (!logits || !d_tree_tokens || !tree || !d_out || !workspace) return MV_ERR_INVALID_ARG;
+  if (!tree->d_retrieve) return MV_ERR_CUDA;
+  if (V < 2 || ld < V || (ld & 3) || (reinterpret_cast<uintptr_t>(logits) & 15)) return MV_ERR_SHAPE;
+  if (params.mode != MV_GREEDY && params.mode != MV_TYPICAL) return MV_ERR_INVALID_ARG;
+  if (params.mode == MV_TYPICAL && !(params.temperature > 0.0f)) return MV_ERR_INVALID_ARG;
+  if (ws_bytes < posterior_ws_bytes(tree->n_nodes)) return MV_ERR_CAPACITY;
+  return launch_posterior(logits, V, ld, d_tree_tokens, tree, params, d_out, d_node_stats, d_node_argmax,
+                          workspace, static_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,93 @@
+// Library runtime: the device error word, status strings, SM count, tensor-map encoding.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+// One error word per device. A __device__ symbol: every GPU that loads the library holds it; no allocation.
+static __device__ unsigned int g_mv_error_word;
+
+unsigned int* mv_error_word() {
+  static std::mutex mu;
+  static unsigned int* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_mv_error_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned int*>(p);
+  }
+  return ptrs[dev];
+}
+
+int mv_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+mv_status mv_last_launch(const char* what) {
+  (void)what;
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? MV_OK : MV_ERR_CUDA;
+}
+
+extern "C" mv_status mv_get_error(uint32_t* code) {
+  unsigned int* w = mv_error_word();
+  if (!w) return MV_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MV_ERR_CUDA;
+  if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MV_ERR_CUDA;
+  if (code) *code = v;
+  if (v != 0) {
+    unsigned int z = 0;
+    if (cudaMemcpy(w, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return MV_ERR_CUDA;
+    return MV_ERR_DEVICE;
+  }
+  return MV_OK;
+}
+
+extern "C" const char* mv_status_string(mv_status s) {
+  switch (s) {
+    case MV_OK: return "ok";
+    case MV_ERR_INVALID_ARG: return "invalid argument";
+    case MV_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case MV_ERR_TREE: return "malformed tree";
+    case MV_ERR_CAPACITY: return "capacity exceeded";
+    case MV_ERR_CUDA: return "CUDA error";
+    case MV_ERR_DEVICE: return "device error word set";
+    case MV_ERR_UNSUPPORTED: return "unsupported";
+  }
+  return "unknown status";
+}
+
+bool mv_encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                    const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                    CUtensorMapSwizzle swizzle) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!encode) return false;
+  cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+  CUresult r = encode(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), (const cuuint64_t*)dims,
+                      (const cuuint64_t*)strides_bytes, (const cuuint32_t*)box, elem_strides,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
