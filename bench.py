@@ -1,0 +1,337 @@
+"""Benchmark of the Medusa tree-verify step at Llama-7B shape on one GB300.
+
+Workload: a random-init 32-layer Llama-7B-shaped decoder (d=4096, 32 heads x 128, FFN 11008 SiLU-gated,
+vocabulary 32000, RMSNorm, RoPE) with 4 Medusa heads and the synthetic 64-node / 41-path tree (the 63
+highest-scoring rank paths, score prod_d 0.7^d * 0.5^rank), after a random 128-token prompt, greedy
+acceptance. One step = one medusa_verify_step: candidates, the backbone over the 64 tree tokens, the LM head,
+the posterior, the KV compaction and the Medusa heads. Weights are bf16 (14.4 GB, far above the 129 MB L2,
+so every step streams them from HBM).
+
+Arms:
+  default            the library (this repository's CUDA kernels)
+  --impl reference   the CPU oracle on the host cores, each step a bounded sample of the same workload
+
+One JSON line on stdout (rank 0). Under torchrun (N > 1) every rank runs an independent replica (the step does
+not shard), the timed region is bracketed by a barrier and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "verify steps/s (7B shape, 64-node tree)"
+PROMPT_LEN = 128
+TREE = dict(n_nodes=64, depth=4, topk=10)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------------------------- CPU oracle sample
+
+def sample_weights(seed=0, layers=2, device=None):
+    """float64 host copies of the weights the oracle sample reads (generated on the GPU when there is one)."""
+    dims = synth.LLAMA7B
+    sub = synth.ModelDims(d=dims.d, n_layers=layers, n_heads=dims.n_heads, head_dim=dims.head_dim, ffn=dims.ffn,
+                          vocab=dims.vocab, n_medusa=1)
+    dev = device or ("cuda" if torch.cuda.is_available() else "cpu")
+    names = {n for n, _ in synth.weight_names(sub)}
+    w = {n: t.double().cpu().numpy() for n, t in synth.model_weights(sub, seed, torch.bfloat16, dev, names).items()}
+    return sub, w
+
+
+def oracle_sample(sub, w, seed=0, min_seconds=10.0, max_reps=20):
+    """Times the float64 oracle on a bounded sample of one 7B verify step.
+
+    Sample: sub.n_layers of the 32 decoder layers over the 64 tree tokens at prefix 128, the LM head, the
+    posterior, and 1 of the 4 Medusa heads on the accepted node, repeated until min_seconds of CPU work.
+    Scaled to a full step as 32/layers x (decoder layers) + LM head + posterior + 4 x (one head).
+    Returns (seconds per full step, sample description, wall seconds timed).
+    """
+    from oracle.model import Backbone, KVCache, medusa_heads
+    from oracle.posterior import GREEDY, evaluate_posterior
+    from oracle.tree import tree_buffers
+
+    dims = synth.LLAMA7B
+    layers = sub.n_layers
+    tree = tree_buffers(synth.synthetic_tree_choices(64, 4, 10), 10)
+    P = PROMPT_LEN
+    toks = synth.prompt_tokens(seed, 64, dims.vocab, name="tree_tokens").numpy()
+    no_lm = dict(w)
+    no_lm["lm_head"] = w["lm_head"][:1]
+    per, wall, reps = [], 0.0, 0
+    while reps < max_reps and (wall < min_seconds or reps < 2):
+        cache = KVCache(sub, P + 64)
+        cache.data[:, :, :, :P] = synth.normal(seed, "kv_prefix", cache.data[:, :, :, :P].shape,
+                                               dtype=torch.float64).numpy()
+        t0 = time.perf_counter()
+        h, _ = Backbone(sub, no_lm.__getitem__).forward(toks, P + tree["position_ids"], cache, P, tree["attn_mask"])
+        t1 = time.perf_counter()
+        logits = h @ w["lm_head"].T
+        post = evaluate_posterior(logits, toks, tree["retrieve"], GREEDY)
+        t2 = time.perf_counter()
+        medusa_heads(w.__getitem__, 1, h[post["next_node"]])
+        t3 = time.perf_counter()
+        per.append((t1 - t0) * dims.n_layers / layers + (t2 - t1) + (t3 - t2) * dims.n_medusa)
+        wall += t3 - t0
+        reps += 1
+    sample = (f"{layers} of 32 decoder layers over the 64 tree tokens at prefix {P}, the LM head, the posterior "
+              f"and 1 of 4 Medusa heads of one 7B verify step in float64 ({reps} repetitions, {wall:.1f} s); "
+              f"scaled to a full step")
+    return statistics.median(per), sample, wall
+
+
+# --------------------------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, world, rank, local):
+    import medusa_tree_speculative_verify_gb300 as mv
+    torch.cuda.set_device(local)
+    dims = synth.LLAMA7B
+    w = synth.packed_weights(dims, 0, torch.bfloat16, "cuda")
+    model = mv.Model(dims, w)
+    tree = mv.Tree(synth.synthetic_tree_choices(TREE["n_nodes"], TREE["depth"], TREE["topk"]), TREE["topk"])
+    n_steps_total = args.warmup + 2 * args.steps + 8
+    s_max = PROMPT_LEN + (TREE["depth"] + 1) * n_steps_total + 64
+    s_max = (s_max + 63) // 64 * 64
+    sess = mv.Session(model, tree, s_max)
+    prompt = synth.prompt_tokens(0, PROMPT_LEN, dims.vocab).to(torch.int32).cuda()
+    prm = mv.AcceptParams(mv.GREEDY)
+    stream = torch.cuda.current_stream()
+
+    sess.prefill(prompt)
+    for _ in range(args.warmup):
+        sess.step(prm)
+    torch.cuda.synchronize()
+    st, code = mv.get_error()
+    if st != 0:
+        raise RuntimeError(f"device error word {code:#x}")
+
+    # ---- timed: K steps, inputs resident in HBM, per-launch events of the projection kernel
+    launches_per_step = 1 + 1 + dims.n_layers * 5 + 1 + 1 + 1 + 2
+    prof = mv.Profiler(sess)
+    acc_total = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        prof.enable()
+        start.record(stream)
+        for _ in range(args.steps):
+            sess.step(prm)
+        end.record(stream)
+        torch.cuda.synchronize()
+        prof.disable()
+    per_kind = prof.read()
+    barrier(world)
+    ms = start.elapsed_time(end)
+    ms = max_over_ranks(ms, world)
+    st, code = mv.get_error()
+    if st != 0:
+        raise RuntimeError(f"device error word {code:#x}")
+    accs = []
+    r = sess.read_result()
+    accs.append(r["acc"])
+
+    # ---- e2e: the host-buffer entry point (H2D seeds, step, D2H result + next seeds, stream sync per step)
+    k = dims.n_medusa * TREE["topk"]
+    seeds = torch.zeros(1 + k, dtype=torch.int32).pin_memory()
+    seeds_next = torch.zeros(1 + k, dtype=torch.int32).pin_memory()
+    res_host = torch.zeros(mv.RESULT_INTS, dtype=torch.int32).pin_memory()
+    seeds[0] = int(r["next_root"])
+    seeds[1:] = sess.head_topk.reshape(-1).cpu()
+    torch.cuda.synchronize()
+    tok_e2e = 0
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        sess.step_host(prm, seeds, res_host, seeds_next)
+        seeds.copy_(seeds_next)
+        tok_e2e += int(res_host[4])
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    barrier(world)
+
+    steps_per_s = args.steps / (ms / 1e3) * world
+    tokens_per_step = tok_e2e / args.steps
+    peak, peak_kind = peaks()
+    gb = gemm_bytes(dims, TREE["n_nodes"])
+    g_ms = sum(per_kind[k][0] for k in gb)
+    g_n = sum(per_kind[k][1] for k in gb)
+    g_bytes = sum(gb[k] * per_kind[k][1] for k in gb)
+    achieved = g_bytes / (g_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "gemm_kernel (tcgen05 projections: QKV, O, gate/up, down, LM head)",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                "traffic": None, "algorithmic_bytes_per_launch": g_bytes / max(g_n, 1),
+                "avg_launch_us": g_ms * 1e3 / max(g_n, 1),
+                "per_kind": {k: {"launches_per_step": c / args.steps, "ms_per_step": ms / args.steps,
+                                 **({"gbs": gb[k] * c / (ms / 1e3) / 1e9} if k in gb and ms > 0 else {})}
+                             for k, (ms, c) in per_kind.items()}}
+    step_bytes = weight_bytes(dims)
+    line = {
+        "metric": METRIC, "value": steps_per_s, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights, random prompt)",
+        "config": {"workload": "Llama-7B shape (32 layers, d 4096, 32x128 heads, FFN 11008, vocab 32000) + 4 Medusa "
+                               "heads, synthetic 64-node/41-path tree, 128-token prompt, greedy verify step",
+                   "tree_nodes": 64, "prompt": PROMPT_LEN, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (14.4 GB of weights streamed per step)"},
+        "tokens_per_s": steps_per_s * tokens_per_step, "tokens_per_step": tokens_per_step,
+        "step_hbm_gbs": step_bytes / (ms / args.steps / 1e3) / 1e9,
+        "e2e": {"value": args.steps * world / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": 4 * (1 + k),
+                "d2h_bytes_per_step": 4 * mv.RESULT_INTS + 4 * (1 + k)},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roofline,
+        "clocks": clk.summary(),
+    }
+    return line
+
+
+def gemm_bytes(dims, n):
+    """Algorithmic HBM bytes of one launch of each projection: weights once, activations in and out once."""
+    d, HD, F, V = dims.d, dims.n_heads * dims.head_dim, dims.ffn, dims.vocab
+    return {"gemm_qkv": 2 * 3 * HD * d + 2 * n * d + 2 * n * 3 * HD,
+            "gemm_o": 2 * d * HD + 2 * n * HD + 4 * n * d * 2 + 2 * n * d,
+            "gemm_gate_up": 2 * 2 * F * d + 2 * n * d + 2 * n * F,
+            "gemm_down": 2 * d * F + 2 * n * F + 4 * n * d * 2 + 2 * n * d,
+            "gemm_lm": 2 * V * d + 2 * n * d + 4 * n * V}
+
+
+def weight_bytes(dims):
+    d, HD, F, V, K, L = dims.d, dims.n_heads * dims.head_dim, dims.ffn, dims.vocab, dims.n_medusa, dims.n_layers
+    per_layer = 2 * (3 * HD * d + d * HD + 2 * F * d + d * F)
+    return L * per_layer + 2 * V * d + 2 * K * (d * d + V * d)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        sub, w = sample_weights()
+        oracle_sample(sub, w, min_seconds=0.0, max_reps=max(1, min(args.warmup, 2)))   # warm-up
+        per_step, sample, _ = oracle_sample(sub, w, min_seconds=0.0, max_reps=max(2, min(args.steps, 20)))
+        v = 1.0 / per_step
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / v, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": "Llama-7B shape + 4 Medusa heads, synthetic 64-node tree, 128-token prompt"},
+                "cpu_baseline": {"value": v, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    line = run_gpu(args, world, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            sub, w = sample_weights()
+            per_step, sample, wall = oracle_sample(sub, w)
+            line["cpu_baseline"] = {"value": 1.0 / per_step, "unit": "steps/s", "cores": os.cpu_count(),
+                                    "kind": "oracle", "sample": sample, "sample_wall_s": wall}
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

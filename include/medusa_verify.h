@@ -179,6 +179,106 @@ mv_status kv_compact(mv_bf16* kv, int32_t L, int32_t H, int32_t S_max, int32_t D
                      const mv_posterior_result* d_res, int32_t* d_cur_len, mv_stream stream);
 
 /* ============================================================================================
+ * Projection over up to 64 tokens on the tcgen05 tensor cores  [M5 二.5 tree_decoding()]
+ * ============================================================================================
+ * out[j][r] = sum_k x[j][k] * w[r][k] for j < n, r < M (fp32 accumulate and output): the kernel every backbone
+ * projection of the verify step runs, exposed with a plain-store epilogue.
+ *   w device bf16 [M][K] (16-byte aligned), x device bf16 [n][K], out device fp32 [n][ld_out].
+ * Limits: 1 <= n <= 64, K % 8 == 0, ld_out >= M, at most 1024 tiles of 128 rows. */
+mv_status mv_linear_bf16_workspace(size_t* bytes);
+mv_status mv_linear_bf16(const mv_bf16* w, const mv_bf16* x, float* out, int32_t M, int32_t K, int32_t n,
+                         int32_t ld_out, void* workspace, size_t ws_bytes, mv_stream stream);
+
+/* ============================================================================================
+ * Model, decode session, verify step  [M5 二.1 medusa_generate(), 二.3 - 二.7]
+ * ============================================================================================
+ * A Llama-style decoder: x = E[token]; per layer: x += Wo . attn(RoPE(Wq a), RoPE(Wk a), Wv a) with
+ * a = RMSNorm(x); x += Wdown . (SiLU(Wgate a) * (Wup a)) with a = RMSNorm(x); logits = Wlm . RMSNorm(x).
+ * RMSNorm gains are 1 (x / sqrt(mean(x^2) + norm_eps)); RoPE pairs (i, i + head_dim/2) with base rope_theta;
+ * attention scale 1/sqrt(head_dim); q heads == kv heads. Medusa heads read RMSNorm(x) of the node that is
+ * consumed (see medusa_heads_topk).
+ * Weights are caller-owned device bf16 matrices [out][in] that must outlive the model handle. */
+typedef struct mv_model_dims {
+  int32_t d, n_layers, n_heads, head_dim, ffn, vocab, n_medusa;
+  float rope_theta, norm_eps;
+} mv_model_dims;
+
+typedef struct mv_model_weights {
+  const mv_bf16* embed;             /* [vocab][d] */
+  const mv_bf16* const* wqkv;       /* host array of n_layers device pointers, each [3*n_heads*head_dim][d]:
+                                       the q rows, then the k rows, then the v rows */
+  const mv_bf16* const* wo;         /* [d][n_heads*head_dim] per layer */
+  const mv_bf16* const* w_gate;     /* [ffn][d] per layer */
+  const mv_bf16* const* w_up;       /* [ffn][d] per layer */
+  const mv_bf16* const* w_down;     /* [d][ffn] per layer */
+  const mv_bf16* lm_head;           /* [vocab][d] */
+  const mv_bf16* medusa_w1;         /* [n_medusa][d][d] */
+  const mv_bf16* medusa_w2;         /* [n_medusa][vocab][d] */
+} mv_model_weights;
+
+typedef struct mv_model mv_model;
+typedef struct mv_session mv_session;
+
+/* Limits: d % 8 == 0, d <= 8192, head_dim in {16, 32, 64, 128}, ffn % 8 == 0, 1 <= n_medusa <= 8; every
+ * pointer 16-byte aligned. MV_ERR_SHAPE otherwise. Builds the weights' TMA descriptors (host only). */
+mv_status mv_model_create(const mv_model_dims* dims, const mv_model_weights* weights, mv_model** out);
+void mv_model_destroy(mv_model* model);
+
+/* A session binds a model, a tree, a KV cache kv [n_layers][2][n_heads][s_max][head_dim] (bf16, caller-owned,
+ * 256-byte aligned) and a workspace (caller-owned device memory of mv_session_workspace() bytes, 256-byte
+ * aligned; zero-filled by mv_session_create, which is synchronous). The decode state (current length, the
+ * last posterior result whose next_root is the next root, the head top-k) lives in the workspace.
+ * Limits: tree depth <= n_medusa, tree topk <= topk <= 16, s_max >= 65. */
+mv_status mv_session_workspace(const mv_model* model, int32_t s_max, int32_t topk, size_t* bytes);
+mv_status mv_session_create(mv_model* model, const mv_tree* tree, mv_bf16* kv, int32_t s_max, int32_t topk,
+                            void* workspace, size_t ws_bytes, mv_session** out);
+void mv_session_destroy(mv_session* session);
+
+typedef struct mv_session_state_ptrs {
+  int32_t* cur_len;             /* device [1]: tokens in the KV cache */
+  mv_posterior_result* result;  /* device: the last verification (next_root = the next step's root) */
+  int32_t* head_topk;           /* device [n_medusa][topk]: the next step's head candidates */
+  int32_t* tree_tokens;         /* device [n_nodes]: the last step's tree tokens */
+  int32_t* cart;                /* device [n_paths][depth+1] */
+  float* logits;                /* device fp32 [64][ld_logits]: the last forward's LM logits */
+  int32_t ld_logits;
+  float* hidden;                /* device fp32 [64][d]: the last forward's residual stream (before the final norm) */
+} mv_session_state_ptrs;
+mv_status mv_session_state(const mv_session* session, mv_session_state_ptrs* out);
+
+/* Prefill [M5 二.3 initialize_medusa()]: runs tokens d_tokens[0..n) causally from position 0 (chunks of 64),
+ * then sets the root (argmax of the last logits row), the head top-k (heads on the last token) and
+ * cur_len = n. Limits: 1 <= n, n + 64 <= s_max. */
+mv_status mv_prefill(mv_session* session, const int32_t* d_tokens, int32_t n, mv_stream stream);
+
+/* One verify step [M5 二.4 - 二.7]: candidates from the state, one backbone pass over the tree (positions
+ * cur_len + depth, keys/values appended at cur_len .. cur_len + n_nodes - 1), posterior, KV compaction,
+ * heads on node retrieve[best][acc]; the state and result advance; cur_len grows by acc + 1. Asynchronous,
+ * no host synchronisation; every step-varying quantity is read from device memory, so the call can be
+ * captured in a CUDA graph and replayed. The caller must keep cur_len + n_nodes <= s_max (not checked on the
+ * host; the kernels check it and set MV_ERR_DEVICE). */
+mv_status medusa_verify_step(mv_session* session, mv_accept_params params, mv_stream stream);
+
+/* The same step driven from host memory: h_seeds_in (nullable) = [root, head_topk[n_medusa][topk]] copied to
+ * the device first; afterwards the result (mv_posterior_result, as int32s) is copied to h_result and, if
+ * h_seeds_out is not NULL, the next seeds to h_seeds_out. Synchronises `stream` before returning. Host
+ * buffers should be pinned for asynchronous copies. */
+mv_status medusa_verify_step_host(mv_session* session, mv_accept_params params, const int32_t* h_seeds_in,
+                                  int32_t* h_result, int32_t* h_seeds_out, mv_stream stream);
+
+/* Per-launch timing of a session's kernels, for benchmarks: while enabled, every launch of medusa_verify_step /
+ * mv_prefill is bracketed by CUDA events on its stream (do not enable during CUDA graph capture).
+ * mv_session_profile_read waits for the last recorded event, returns the summed milliseconds and launch counts
+ * per kind (indices MV_PROF_*) since profiling was enabled or last read, and resets them. */
+enum {
+  MV_PROF_GEMM_QKV = 0, MV_PROF_ATTENTION = 1, MV_PROF_GEMM_O = 2, MV_PROF_GEMM_GATE_UP = 3, MV_PROF_GEMM_DOWN = 4,
+  MV_PROF_GEMM_LM = 5, MV_PROF_POSTERIOR = 6, MV_PROF_KV_COMPACT = 7, MV_PROF_HEADS = 8, MV_PROF_OTHER = 9,
+  MV_PROF_KINDS = 10
+};
+mv_status mv_session_profile(mv_session* session, int32_t enable);
+mv_status mv_session_profile_read(mv_session* session, float* ms_by_kind, int32_t* launches_by_kind);
+
+/* ============================================================================================
  * Errors
  * ============================================================================================
  * Returns MV_OK if the current device's error word is clear, else MV_ERR_DEVICE and stores the word in *code

@@ -14,7 +14,8 @@ import numpy as np
 
 from .build import LIB, build
 
-__all__ = ["lib", "MVError", "Tree", "AcceptParams", "PosteriorResult", "GREEDY", "TYPICAL",
+__all__ = ["lib", "MVError", "Tree", "AcceptParams", "PosteriorResult", "GREEDY", "TYPICAL", "Model", "Session",
+           "linear_bf16", "linear_bf16_workspace", "ModelDims",
            "medusa_heads_topk", "medusa_heads_topk_workspace", "build_candidates", "tree_attention",
            "tree_attention_workspace", "evaluate_posterior", "evaluate_posterior_workspace", "kv_compact",
            "get_error", "MAX_NODES", "MAX_DEPTH", "EXPORTED_SYMBOLS"]
@@ -72,6 +73,19 @@ _SIGS = {
     "evaluate_posterior_workspace": ([_I, ctypes.POINTER(_S)], _I),
     "evaluate_posterior": ([_P, _I, _I, _P, _P, AcceptParams, _P, _P, _P, _P, _S, _P], _I),
     "kv_compact": ([_P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
+    "mv_linear_bf16_workspace": ([ctypes.POINTER(_S)], _I),
+    "mv_linear_bf16": ([_P, _P, _P, _I, _I, _I, _I, _P, _S, _P], _I),
+    "mv_model_create": ([_P, _P, ctypes.POINTER(_P)], _I),
+    "mv_model_destroy": ([_P], None),
+    "mv_session_workspace": ([_P, _I, _I, ctypes.POINTER(_S)], _I),
+    "mv_session_create": ([_P, _P, _P, _I, _I, _P, _S, ctypes.POINTER(_P)], _I),
+    "mv_session_destroy": ([_P], None),
+    "mv_session_state": ([_P, _P], _I),
+    "mv_prefill": ([_P, _P, _I, _P], _I),
+    "medusa_verify_step": ([_P, AcceptParams, _P], _I),
+    "medusa_verify_step_host": ([_P, AcceptParams, _P, _P, _P, _P], _I),
+    "mv_session_profile": ([_P, _I], _I),
+    "mv_session_profile_read": ([_P, _P, _P], _I),
     "mv_get_error": ([ctypes.POINTER(_U)], _I),
     "mv_status_string": ([_I], ctypes.c_char_p),
 }
@@ -218,3 +232,140 @@ def result_dict(buf):
     r = PosteriorResult.from_buffer_copy(a.tobytes())
     return dict(best=r.best, acc=r.acc, next_node=r.next_node, next_root=r.next_root, n_tokens=r.n_tokens,
                 nodes=list(r.nodes)[: r.acc + 1], tokens=list(r.tokens)[: r.acc + 1])
+
+
+# --------------------------------------------------------------------------------------------- projections
+
+def linear_bf16_workspace():
+    return _ws_size(lib().mv_linear_bf16_workspace)
+
+
+def linear_bf16(w, x, out, workspace, stream=None):
+    """out[:n, :M] (fp32) = x[n, K] @ w[M, K]^T on the tcgen05 kernel; out may have a row stride >= M."""
+    M, K = w.shape
+    n = x.shape[0]
+    _check(lib().mv_linear_bf16(_ptr(w), _ptr(x), _ptr(out), M, K, n, out.stride(0), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream)), "mv_linear_bf16")
+
+
+# --------------------------------------------------------------------------------------------- model / session
+
+class ModelDims(ctypes.Structure):
+    _fields_ = [("d", _I), ("n_layers", _I), ("n_heads", _I), ("head_dim", _I), ("ffn", _I), ("vocab", _I),
+                ("n_medusa", _I), ("rope_theta", _F), ("norm_eps", _F)]
+
+
+class _Weights(ctypes.Structure):
+    _fields_ = [("embed", _P), ("wqkv", _P), ("wo", _P), ("w_gate", _P), ("w_up", _P), ("w_down", _P),
+                ("lm_head", _P), ("medusa_w1", _P), ("medusa_w2", _P)]
+
+
+class _StatePtrs(ctypes.Structure):
+    _fields_ = [("cur_len", _P), ("result", _P), ("head_topk", _P), ("tree_tokens", _P), ("cart", _P),
+                ("logits", _P), ("ld_logits", _I), ("hidden", _P)]
+
+
+class Model:
+    """A model handle over caller-owned bf16 device weights.
+
+    ``w`` maps embed, lm_head, medusa_w1 [K,d,d], medusa_w2 [K,V,d] to tensors and wqkv, wo, w_gate, w_up,
+    w_down to per-layer lists of tensors (see mv_model_weights in include/medusa_verify.h).
+    """
+
+    def __init__(self, dims, w):
+        self.dims = ModelDims(dims.d, dims.n_layers, dims.n_heads, dims.head_dim, dims.ffn, dims.vocab,
+                              dims.n_medusa, dims.rope_theta, dims.norm_eps)
+        self.w = w  # keep the tensors alive
+        L = dims.n_layers
+        arrs = {k: (ctypes.c_void_p * L)(*[t.data_ptr() for t in w[k]]) for k in
+                ("wqkv", "wo", "w_gate", "w_up", "w_down")}
+        self._arrs = arrs
+        cw = _Weights(w["embed"].data_ptr(), ctypes.cast(arrs["wqkv"], _P), ctypes.cast(arrs["wo"], _P),
+                      ctypes.cast(arrs["w_gate"], _P), ctypes.cast(arrs["w_up"], _P), ctypes.cast(arrs["w_down"], _P),
+                      w["lm_head"].data_ptr(), w["medusa_w1"].data_ptr(), w["medusa_w2"].data_ptr())
+        h = ctypes.c_void_p()
+        _check(lib().mv_model_create(ctypes.byref(self.dims), ctypes.byref(cw), ctypes.byref(h)), "mv_model_create")
+        self.handle = h
+
+    def __del__(self):
+        if getattr(self, "handle", None) is not None and _lib is not None:
+            _lib.mv_model_destroy(self.handle)
+            self.handle = None
+
+
+class Session:
+    """A decode session: model + tree + KV cache [L,2,H,s_max,D] (bf16) + workspace (allocated here)."""
+
+    def __init__(self, model: Model, tree: Tree, s_max, topk=None, kv=None):
+        import torch
+        d = model.dims
+        self.model, self.tree, self.s_max = model, tree, s_max
+        self.topk = topk or tree.topk
+        self.kv = kv if kv is not None else torch.zeros(d.n_layers, 2, d.n_heads, s_max, d.head_dim,
+                                                         dtype=torch.bfloat16, device="cuda")
+        nbytes = _ws_size(lib().mv_session_workspace, model.handle, s_max, self.topk)
+        self.ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+        h = ctypes.c_void_p()
+        _check(lib().mv_session_create(model.handle, tree.handle, _ptr(self.kv), s_max, self.topk, _ptr(self.ws),
+                                       nbytes, ctypes.byref(h)), "mv_session_create")
+        self.handle = h
+        sp = _StatePtrs()
+        _check(lib().mv_session_state(h, ctypes.byref(sp)), "mv_session_state")
+        base = self.ws.data_ptr()
+
+        def view(ptr, count, dtype):
+            off = ptr - base
+            esz = torch.empty(0, dtype=dtype).element_size()
+            return self.ws[off: off + count * esz].view(dtype)
+
+        K = d.n_medusa
+        self.cur_len = view(sp.cur_len, 1, torch.int32)
+        self.result = view(sp.result, RESULT_INTS, torch.int32)
+        self.head_topk = view(sp.head_topk, K * self.topk, torch.int32).view(K, self.topk)
+        self.tree_tokens = view(sp.tree_tokens, tree.n_nodes, torch.int32)
+        self.cart = view(sp.cart, tree.n_paths * (tree.depth + 1), torch.int32).view(tree.n_paths, tree.depth + 1)
+        self.ld_logits = sp.ld_logits
+        self.logits = view(sp.logits, 64 * sp.ld_logits, torch.float32).view(64, sp.ld_logits)[:, : d.vocab]
+        self.hidden = view(sp.hidden, 64 * d.d, torch.float32).view(64, d.d)
+
+    def prefill(self, tokens, stream=None):
+        _check(lib().mv_prefill(self.handle, _ptr(tokens), tokens.numel(), _stream(stream)), "mv_prefill")
+
+    def step(self, params: AcceptParams = None, stream=None):
+        _check(lib().medusa_verify_step(self.handle, params or AcceptParams(), _stream(stream)), "medusa_verify_step")
+
+    def step_host(self, params, seeds_in, result_out, seeds_out=None, stream=None):
+        """Host-buffer step: seeds_in/out int32 [1 + K*topk] (pinned CPU tensors or None), result_out int32."""
+        _check(lib().medusa_verify_step_host(self.handle, params, _ptr(seeds_in), _ptr(result_out), _ptr(seeds_out),
+                                             _stream(stream)), "medusa_verify_step_host")
+
+    def read_result(self):
+        return result_dict(self.result)
+
+    def __del__(self):
+        if getattr(self, "handle", None) is not None and _lib is not None:
+            _lib.mv_session_destroy(self.handle)
+            self.handle = None
+
+
+PROF_KINDS = ("gemm_qkv", "attention", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_lm", "posterior", "kv_compact",
+              "heads", "other")
+
+
+class Profiler:
+    """Per-kind summed kernel milliseconds of a session (CUDA events around every launch)."""
+
+    def __init__(self, sess: Session):
+        self.sess = sess
+
+    def enable(self):
+        _check(lib().mv_session_profile(self.sess.handle, 1), "mv_session_profile")
+
+    def disable(self):
+        _check(lib().mv_session_profile(self.sess.handle, 0), "mv_session_profile")
+
+    def read(self):
+        ms = (ctypes.c_float * len(PROF_KINDS))()
+        cnt = (ctypes.c_int32 * len(PROF_KINDS))()
+        _check(lib().mv_session_profile_read(self.sess.handle, ms, cnt), "mv_session_profile_read")
+        return {k: (float(ms[i]), int(cnt[i])) for i, k in enumerate(PROF_KINDS)}

@@ -346,7 +346,15 @@ mv_status launch_tree_attention(const CUtensorMap& kmap, const CUtensorMap& vmap
                                 const mv_bf16* q, int H, int D, int S_max, const int32_t* d_prefix, int prefix,
                                 int max_prefix, const mv_tree* t, float scale, mv_bf16* out, void* ws,
                                 cudaStream_t stream) {
-  const int max_tiles = (max_prefix + t->n_nodes + kKeys - 1) / kKeys;
+  return launch_tree_attention_n(kmap, vmap, plane_k, plane_v, q, H, D, S_max, d_prefix, prefix, max_prefix, t,
+                                 t->n_nodes, scale, out, ws, stream);
+}
+
+mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vmap, int plane_k, int plane_v,
+                                  const mv_bf16* q, int H, int D, int S_max, const int32_t* d_prefix, int prefix,
+                                  int max_prefix, const mv_tree* t, int n, float scale, mv_bf16* out, void* ws,
+                                  cudaStream_t stream) {
+  const int max_tiles = (max_prefix + n + kKeys - 1) / kKeys;
   const int ws_splits = choose_splits(H, (S_max + kKeys - 1) / kKeys);
   const int splits = std::min(ws_splits, choose_splits(H, max_tiles));
   char* p = static_cast<char*>(ws);
@@ -358,7 +366,7 @@ mv_status launch_tree_attention(const CUtensorMap& kmap, const CUtensorMap& vmap
   a.prefix = prefix;
   a.H = H;
   a.S_max = S_max;
-  a.n = t->n_nodes;
+  a.n = n;
   a.splits = splits;
   a.plane_k = plane_k;
   a.plane_v = plane_v;

@@ -1,0 +1,501 @@
+// Backbone projections over the (up to) 64 tree tokens on the 5th-generation tensor cores (tcgen05).
+//
+// "大模型推理 memory bandwidth bound (5) - Medusa", 二.5 tree_decoding(): the backbone runs once over all tree
+// tokens; at 64 tokens every weight byte feeds 64 multiply-adds, so these GEMMs stream the weights from HBM.
+//
+// Mapping (swap-AB): D[128 weight rows x 64 tokens] += W[128 x 64 k] . X[64 tokens x 64 k]^T per k-block, one
+// tcgen05.mma.cta_group::1.kind::f16 (M=128, N=64, K=16) per 16 k. Operands come from shared memory through
+// TMA (128-byte swizzle, K-major), the accumulator lives in tensor memory (two 64-column buffers, so the
+// epilogue of one segment overlaps the MMAs of the next).
+//
+// Work split: persistent stream-K. The (tile, k-block) iteration space is cut into one contiguous range per
+// CTA (one CTA per SM), so every SM streams the same number of weight bytes. A tile split between CTAs is
+// summed by its last contributor (atomic ticket, no waiting) in contributor order, which keeps the result
+// deterministic, and that CTA runs the fused epilogue:
+//   STORE    out[token][row] = acc * s[token]                    (LM head logits, plain projections)
+//   RESIDUAL x[token][row] += acc; bf16 copy; per-token sum of squares of the 128-row slice (next RMSNorm)
+//   SWIGLU   act[token][f] = SiLU(s*gate) * (s*up), tile = 64 gate rows + the same 64 up rows
+//   QKV      q / k / v rows, RoPE on q and k at position prefix + depth, k/v appended to the cache
+// s[token] = 1/sqrt(mean(x^2) + eps) of the RMSNorm that precedes the projection (its gains are 1), applied
+// to the accumulator instead of the input: x W^T * s = (x * s) W^T.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer + TMEM owner, warps 2..5 = epilogue
+// (warp w reads TMEM lanes 32*(w%4) .. +31). Every mbarrier wait is bounded; on expiry the kernel records
+// MV_DEVERR_TIMEOUT, lets its in-flight copies and MMAs land, frees its tensor memory and returns.
+#include "common.cuh"
+#include "gemm.cuh"
+#include "kernels.cuh"
+
+namespace {
+
+constexpr int BM = 128, BN = 64, BK = 64;
+constexpr int kStages = 6;
+constexpr int kABytes = BM * BK * 2;  // 16 KB
+constexpr int kBBytes = BN * BK * 2;  // 8 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kEpiThreads = 128;
+constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kTmemCols = 2 * BN;
+constexpr int kPitch = BN + 1;  // staging row pitch (floats)
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)BM * kPitch * 4 + 256;
+
+// kind::f16 instruction descriptor: D fp32, A/B bf16, both K-major, N = 64, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+// ---------------------------------------------------------------------------------------------- tcgen05 PTX
+MV_DEV void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+MV_DEV void tmem_relinquish() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;"); }
+MV_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+MV_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+MV_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+MV_DEV void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+MV_DEV void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+MV_DEV void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+MV_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+MV_DEV void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
+// OR of `v` over the 128 epilogue threads (named barrier 1), the same answer in every thread.
+MV_DEV bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kEpiThreads)
+      : "memory");
+  return r != 0;
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row core groups 1024 bytes apart.
+MV_DEV uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;             // leading-dimension offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;   // stride-dimension offset
+  d |= (uint64_t)1 << 46;             // descriptor version
+  d |= (uint64_t)2 << 61;             // SWIZZLE_128B
+  return d;
+}
+
+// ---------------------------------------------------------------------------------------------- stream-K
+struct Seg {
+  int tile, kb0, kb1;
+};
+MV_DEV long long unit_begin(int c, const GemmParams& p) { return (long long)c * p.units / p.grid; }
+
+// The i-th segment of CTA c; false when there is none.
+MV_DEV bool get_seg(int c, int i, const GemmParams& p, Seg& s) {
+  long long u = unit_begin(c, p);
+  const long long u1 = unit_begin(c + 1, p);
+  for (int k = 0;; ++k) {
+    if (u >= u1) return false;
+    const int tile = (int)(u / p.kbt), kb0 = (int)(u % p.kbt);
+    const int kb1 = (int)min((long long)p.kbt, kb0 + (u1 - u));
+    if (k == i) {
+      s.tile = tile;
+      s.kb0 = kb0;
+      s.kb1 = kb1;
+      return true;
+    }
+    u += kb1 - kb0;
+  }
+}
+MV_DEV int first_contributor(int tile, const GemmParams& p) {
+  const long long u = (long long)tile * p.kbt;
+  int c = (int)(u * p.grid / p.units);
+  if (c >= p.grid) c = p.grid - 1;
+  while (c + 1 < p.grid && unit_begin(c + 1, p) <= u) ++c;
+  while (c > 0 && unit_begin(c, p) > u) --c;
+  return c;
+}
+MV_DEV float* partial_slot(int c, int tile, const GemmParams& p) {
+  const int first_tile = (int)(unit_begin(c, p) / p.kbt);
+  return p.partials + ((size_t)c * 2 + (tile == first_tile ? 0 : 1)) * (BM * BN);
+}
+
+// ---------------------------------------------------------------------------------------------- epilogues
+// Per-token RMSNorm scale from the sum-of-squares partials (one per 128-row slice of the hidden state).
+MV_DEV void compute_scales(const GemmParams& p, float* s_scale, int i) {
+  if (i < BN) {
+    float s = 1.0f;
+    if (p.ssq) {
+      float t = 0.0f;
+      for (int q = 0; q < p.ssq_parts; ++q) t += p.ssq[q * BN + i];
+      s = rsqrtf(t / (float)p.norm_d + p.eps);
+    }
+    s_scale[i] = s;
+  }
+}
+
+template <int EPI>
+MV_DEV void final_epilogue(const GemmParams& p, int tile, int i, float (&v)[BN], float* stg, float* s_scale) {
+  compute_scales(p, s_scale, i);
+  epi_bar();
+  const int ntok = p.n_tok;
+  if constexpr (EPI == EPI_STORE) {
+    const int R = tile * BM + i;
+    if (R < p.M) {
+#pragma unroll
+      for (int j = 0; j < BN; ++j)
+        if (j < ntok) p.out_f32[(size_t)j * p.ld_out + R] = v[j] * s_scale[j];
+    }
+  } else if constexpr (EPI == EPI_RESIDUAL) {
+    const int R = tile * BM + i;
+    const bool ok = R < p.M;
+#pragma unroll
+    for (int j = 0; j < BN; ++j) {
+      float xn = 0.0f;
+      if (ok && j < ntok) {
+        xn = p.x[(size_t)j * p.M + R] + v[j];
+        p.x[(size_t)j * p.M + R] = xn;
+        p.xb[(size_t)j * p.M + R] = __bfloat16_as_ushort(__float2bfloat16_rn(xn));
+      }
+      stg[i * kPitch + j] = xn * xn;
+    }
+    epi_bar();
+    if (i < BN) {
+      float s = 0.0f;
+      for (int r = 0; r < BM; ++r) s += stg[r * kPitch + i];
+      p.ssq_out[tile * BN + i] = s;
+    }
+  } else if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll
+    for (int j = 0; j < BN; ++j) stg[i * kPitch + j] = v[j] * s_scale[j];
+    epi_bar();
+    if (i < 64) {
+      const int f = tile * 64 + i;
+      if (f < p.F)
+        for (int j = 0; j < ntok; ++j) {
+          const float g = stg[i * kPitch + j], u = stg[(i + 64) * kPitch + j];
+          p.act[(size_t)j * p.F + f] = __bfloat16_as_ushort(__float2bfloat16_rn(silu(g) * u));
+        }
+    }
+  } else if constexpr (EPI == EPI_QKV) {
+#pragma unroll
+    for (int j = 0; j < BN; ++j) stg[i * kPitch + j] = v[j] * s_scale[j];
+    epi_bar();
+    const int R = tile * BM + i;
+    if (R < p.M) {
+      const int HD = p.H * p.D;
+      const int which = R / HD, within = R % HD, head = within / p.D, dim = within % p.D;
+      const int half = p.D >> 1;
+      const int prefix = *p.cur_len;
+      const int pi = dim < half ? i + half : i - half;
+      const float inv_freq = exp2f(-(float)(2 * (dim % half)) / (float)p.D * p.log2_theta);
+      for (int j = 0; j < ntok; ++j) {
+        float val = stg[i * kPitch + j];
+        if (which < 2) {
+          const float pv = stg[pi * kPitch + j];
+          float sn, cs;
+          sincosf((float)(prefix + p.pos_ids[j]) * inv_freq, &sn, &cs);
+          val = dim < half ? val * cs - pv * sn : val * cs + pv * sn;
+        }
+        const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+        if (which == 0) {
+          p.q_out[((size_t)j * p.H + head) * p.D + dim] = b;
+        } else {
+          const size_t plane = (size_t)p.layer * 2 + (which - 1);
+          p.kv[((plane * p.H + head) * p.S_max + prefix + j) * p.D + dim] = b;
+        }
+      }
+    }
+  }
+  epi_bar();  // the staging buffer and scales are reused by the next segment
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap amap0,
+                                                           const __grid_constant__ CUtensorMap amap1,
+                                                           const __grid_constant__ CUtensorMap bmap,
+                                                           const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  float* stg = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int s_abort;
+  __shared__ float s_scale[BN];
+  __shared__ int s_last;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cta = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(&drain, 1);
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&amap0);
+      if (p.paired) tma_prefetch_desc(&amap1);
+      tma_prefetch_desc(&bmap);
+      int it = 0;
+      bool ok = true;
+      Seg sg;
+      for (int si = 0; ok && get_seg(cta, si, p, sg); ++si) {
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
+          const int s = it % kStages, r = it / kStages;
+          if (s_abort || !mbar_wait(&empty[s], (uint32_t)((r & 1) ^ 1))) {
+            ok = false;
+            break;
+          }
+          uint8_t* a = stages + (size_t)s * kStageBytes;
+          uint8_t* b = a + kABytes;
+          mbar_arrive_expect_tx(&full[s], kStageBytes);
+          if (p.paired) {
+            tma_load_2d(a, &amap0, &full[s], kb * BK, sg.tile * 64);
+            tma_load_2d(a + kABytes / 2, &amap1, &full[s], kb * BK, sg.tile * 64);
+          } else {
+            tma_load_2d(a, &amap0, &full[s], kb * BK, sg.tile * BM);
+          }
+          tma_load_2d(b, &bmap, &full[s], kb * BK, 0);
+        }
+      }
+      if (!ok) {
+        if (!s_abort) mv_set_error(p.err, 8, MV_DEVERR_TIMEOUT);
+        s_abort = 1;
+        // let the copies in flight land: the most recent phase of each stage
+        for (int j = max(0, it - kStages); j < it; ++j)
+          if (!mbar_wait(&full[j % kStages], (uint32_t)((j / kStages) & 1))) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      Seg sg;
+      const uint32_t st0 = smem_u32(stages);
+      for (int si = 0; ok && get_seg(cta, si, p, sg); ++si) {
+        const int buf = si & 1, rr = si >> 1;
+        if (s_abort || !mbar_wait(&tempty[buf], (uint32_t)((rr & 1) ^ 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dt = tmem_base + (uint32_t)(buf * BN);
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
+          const int s = it % kStages, r = it / kStages;
+          if (s_abort || !mbar_wait(&full[s], (uint32_t)(r & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = st0 + (uint32_t)(s * kStageBytes), b = a + kABytes;
+          const uint64_t ad = sw128_desc(a), bd = sw128_desc(b);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc_mma(dt, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), kIdesc, (kb > sg.kb0 || k > 0) ? 1u : 0u);
+          tc_commit(&empty[s]);
+        }
+        if (!ok) break;
+        tc_commit(&tfull[buf]);
+      }
+      if (!ok) {
+        if (!s_abort) mv_set_error(p.err, 9, MV_DEVERR_TIMEOUT);
+        s_abort = 1;
+        tc_commit(&drain);  // arrives once every MMA issued so far has completed
+        mbar_wait(&drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (128 threads)
+    const int sub = warp & 3;           // TMEM sub-partition this warp may read
+    const int i = sub * 32 + lane;      // tile row = TMEM lane
+    Seg sg;
+    for (int si = 0; get_seg(cta, si, p, sg); ++si) {
+      const int buf = si & 1, rr = si >> 1;
+      const bool got = !s_abort && mbar_wait(&tfull[buf], (uint32_t)(rr & 1));
+      if (epi_any(!got)) {  // uniform over the 4 epilogue warps
+        if (i == 0) mv_set_error(p.err, 10, MV_DEVERR_TIMEOUT);
+        s_abort = 1;
+        break;
+      }
+      tc_fence_after();
+      float v[BN];
+      const uint32_t ta = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(buf * BN);
+      tmem_ld32(ta, v);
+      tmem_ld32(ta + 32, v + 32);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+
+      const bool whole = sg.kb0 == 0 && sg.kb1 == p.kbt;
+      if (!whole) {
+        float* slot = partial_slot(cta, sg.tile, p);
+#pragma unroll
+        for (int j = 0; j < BN; ++j) slot[j * BM + i] = v[j];
+        __threadfence();
+        epi_bar();
+        if (i == 0) {
+          const int c0 = first_contributor(sg.tile, p);
+          int c1 = c0;
+          while (c1 + 1 < p.grid && unit_begin(c1 + 1, p) < (long long)(sg.tile + 1) * p.kbt) ++c1;
+          s_last = atomicAdd(p.tickets + sg.tile, 1u) == (unsigned)(c1 - c0);
+        }
+        epi_bar();
+        if (!s_last) continue;
+        __threadfence();
+        const int c0 = first_contributor(sg.tile, p);
+#pragma unroll
+        for (int j = 0; j < BN; ++j) v[j] = 0.0f;
+        for (int c = c0; c < p.grid && unit_begin(c, p) < (long long)(sg.tile + 1) * p.kbt; ++c) {
+          const float* ps = partial_slot(c, sg.tile, p);
+#pragma unroll
+          for (int j = 0; j < BN; ++j) v[j] += __ldcg(ps + j * BM + i);
+        }
+        if (i == 0) p.tickets[sg.tile] = 0u;
+      }
+      final_epilogue<EPI>(p, sg.tile, i, v, stg, s_scale);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes() { return kSmemBytes; }
+
+int gemm_grid(int units) {
+  const int sms = mv_sm_count();
+  return units < sms ? units : sms;
+}
+
+size_t gemm_ws_bytes() {
+  const int sms = mv_sm_count();
+  return (size_t)sms * 2 * BM * BN * sizeof(float) + kGemmMaxTiles * sizeof(unsigned int) + 256;
+}
+
+void gemm_ws_layout(void* ws, float** partials, unsigned int** tickets) {
+  char* p = static_cast<char*>(ws);
+  *tickets = reinterpret_cast<unsigned int*>(p);
+  *partials = reinterpret_cast<float*>(p + ((kGemmMaxTiles * sizeof(unsigned int) + 255) & ~size_t(255)));
+}
+
+bool gemm_weight_map(CUtensorMap* map, const void* w, int rows, int K, int box_rows) {
+  const uint64_t dims[2] = {(uint64_t)K, (uint64_t)rows};
+  const uint64_t strides[1] = {(uint64_t)K * 2};
+  const uint32_t box[2] = {(uint32_t)BK, (uint32_t)box_rows};
+  return mv_encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool gemm_act_map(CUtensorMap* map, const void* x, int rows, int K) {
+  const uint64_t dims[2] = {(uint64_t)K, (uint64_t)rows};
+  const uint64_t strides[1] = {(uint64_t)K * 2};
+  const uint32_t box[2] = {(uint32_t)BK, (uint32_t)BN};
+  return mv_encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+void gemm_finish_params(GemmParams& p) {
+  p.kbt = (p.K + BK - 1) / BK;
+  p.n_tiles = p.paired ? (p.F + 63) / 64 : (p.M + BM - 1) / BM;
+  p.units = p.n_tiles * p.kbt;
+  p.grid = gemm_grid(p.units);
+}
+
+mv_status launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
+                      const GemmParams& p, cudaStream_t stream) {
+  if (p.n_tiles > kGemmMaxTiles || p.n_tok < 1 || p.n_tok > BN) return MV_ERR_SHAPE;
+  const size_t smem = kSmemBytes;
+  switch (epi) {
+#define MV_GEMM_CASE(E)                                                                                          \
+  case E:                                                                                                        \
+    if (cudaFuncSetAttribute(gemm_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=          \
+        cudaSuccess)                                                                                             \
+      return MV_ERR_CUDA;                                                                                        \
+    gemm_kernel<E><<<p.grid, kThreads, smem, stream>>>(a0, a1, b, p);                                           \
+    break;
+    MV_GEMM_CASE(EPI_STORE)
+    MV_GEMM_CASE(EPI_RESIDUAL)
+    MV_GEMM_CASE(EPI_SWIGLU)
+    MV_GEMM_CASE(EPI_QKV)
+#undef MV_GEMM_CASE
+    default:
+      return MV_ERR_INVALID_ARG;
+  }
+  return mv_last_launch("gemm");
+}
+
+// out[n][ld] (fp32) = X[n][K] . W[M][K]^T, optionally scaled per row of X by 1/sqrt(mean(x^2)+eps) of x_f32.
+extern "C" mv_status mv_linear_bf16(const mv_bf16* w, const mv_bf16* x, float* out, int32_t M, int32_t K,
+                                    int32_t n, int32_t ld_out, void* workspace, size_t ws_bytes, mv_stream stream) {
+  if (!w || !x || !out || !workspace) return MV_ERR_INVALID_ARG;
+  if (M < 1 || K < 8 || (K & 7) || n < 1 || n > BN || ld_out < M) return MV_ERR_SHAPE;
+  if (ws_bytes < gemm_ws_bytes()) return MV_ERR_CAPACITY;
+  if ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(x)) & 15) return MV_ERR_SHAPE;
+  CUtensorMap a, b;
+  if (!gemm_weight_map(&a, w, M, K, BM) || !gemm_act_map(&b, x, n, K)) return MV_ERR_CUDA;
+  GemmParams p{};
+  p.M = M;
+  p.K = K;
+  p.n_tok = n;
+  p.out_f32 = out;
+  p.ld_out = ld_out;
+  p.err = mv_error_word();
+  gemm_ws_layout(workspace, &p.partials, &p.tickets);
+  gemm_finish_params(p);
+  return launch_gemm(EPI_STORE, a, a, b, p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" mv_status mv_linear_bf16_workspace(size_t* bytes) {
+  if (!bytes) return MV_ERR_INVALID_ARG;
+  *bytes = gemm_ws_bytes();
+  return MV_OK;
+}

@@ -1,0 +1,50 @@
+// Parameters and host helpers of the tcgen05 projection kernel (gemm.cu).
+#pragma once
+
+#include "common.cuh"
+
+enum { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_QKV = 3 };
+constexpr int kGemmMaxTiles = 1024;
+
+struct GemmParams {
+  int M;         // weight rows (output features); for SWIGLU the FFN width F (rows per gate/up matrix)
+  int K;         // reduction length
+  int n_tok;     // valid token columns (1..64)
+  int paired;    // SWIGLU: tile = 64 rows of amap0 (gate) + the same 64 rows of amap1 (up)
+  // derived (gemm_finish_params)
+  int kbt, n_tiles, units, grid;
+  // stream-K workspace
+  float* partials;
+  unsigned int* tickets;
+  // RMSNorm scale of the input columns: s = 1/sqrt(sum(ssq[0..ssq_parts)) / norm_d + eps); null = 1
+  const float* ssq;
+  int ssq_parts, norm_d;
+  float eps;
+  // EPI_STORE
+  float* out_f32;
+  int ld_out;
+  // EPI_RESIDUAL (x, xb are [n][M]; ssq_out is [n_tiles][64])
+  float* x;
+  uint16_t* xb;
+  float* ssq_out;
+  // EPI_SWIGLU (act is [n][F])
+  uint16_t* act;
+  int F;
+  // EPI_QKV: rows = [q heads | k heads | v heads] x D
+  uint16_t* q_out;  // [n][H][D]
+  uint16_t* kv;     // [L][2][H][S_max][D]
+  int H, D, S_max, layer;
+  const int32_t* cur_len;  // device prefix length
+  const int32_t* pos_ids;  // [n] depth of each token
+  float log2_theta;
+  unsigned int* err;
+};
+
+size_t gemm_smem_bytes();
+size_t gemm_ws_bytes();
+void gemm_ws_layout(void* ws, float** partials, unsigned int** tickets);
+bool gemm_weight_map(CUtensorMap* map, const void* w, int rows, int K, int box_rows);
+bool gemm_act_map(CUtensorMap* map, const void* x, int rows, int K);
+void gemm_finish_params(GemmParams& p);
+mv_status launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
+                      const GemmParams& p, cudaStream_t stream);

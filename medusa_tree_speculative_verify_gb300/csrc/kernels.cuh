@@ -35,3 +35,7 @@ mv_status launch_tree_attention(const CUtensorMap& kmap, const CUtensorMap& vmap
                                 const mv_bf16* q, int H, int D, int S_max, const int32_t* d_prefix, int prefix,
                                 int max_prefix, const mv_tree* t, float scale, mv_bf16* out, void* ws,
                                 cudaStream_t stream);
+mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vmap, int plane_k, int plane_v,
+                                  const mv_bf16* q, int H, int D, int S_max, const int32_t* d_prefix, int prefix,
+                                  int max_prefix, const mv_tree* t, int n, float scale, mv_bf16* out, void* ws,
+                                  cudaStream_t stream);

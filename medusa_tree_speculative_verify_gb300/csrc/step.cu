@@ -1,0 +1,587 @@
+// The whole verify step over a Llama-style backbone, and the prefill that starts a decode.
+//
+// "大模型推理 memory bandwidth bound (5) - Medusa", 二.1 medusa_generate() and its steps 二.4 - 二.7: candidates
+// from the previous step's root and head top-k, one backbone pass over the flattened tree with the tree mask
+// (positions = prefix + depth), posterior evaluation, KV compaction, and the next root / head top-k taken at
+// node retrieve[best][acc]. The reference runs the Medusa heads on every tree node and keeps that node's row;
+// here they run on that node only (the same consumed value). Every quantity that changes from step to step
+// (prefix length, root, head top-k, the accepted path) lives in device memory, so a step needs no host
+// synchronisation and can be captured once in a CUDA graph and replayed ("OpenPangu7B-with-Medusa" README, 4:
+// static tree tensors and few host-device round trips, here on CUDA graphs).
+//
+// Kernel sequence of one step (L layers): build_candidates, embed, L x {QKV+RoPE+KV append, tree attention,
+// O + residual, gate/up + SiLU-gate, down + residual}, LM head, posterior, KV compaction, heads W1, heads W2.
+#include <algorithm>
+#include <vector>
+
+#include "common.cuh"
+#include "gemm.cuh"
+#include "kernels.cuh"
+
+namespace {
+
+constexpr int kTok = 64;  // token columns of every activation buffer
+
+// x[j][:] = float(E[tok[j]][:]), xb = E[tok[j]] (bf16), ssq[s][j] = sum of x^2 over the 128-column slice s.
+__global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ tokens, const uint16_t* __restrict__ E,
+                                                    int vocab, int d, float* __restrict__ x, uint16_t* __restrict__ xb,
+                                                    float* __restrict__ ssq, unsigned int* err) {
+  const int j = blockIdx.x;
+  const int tok = tokens[j];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (tok < 0 || tok >= vocab) {
+    if (threadIdx.x == 0) mv_set_error(err, 11, MV_DEVERR_INDEX);
+    return;
+  }
+  const int slices = (d + 127) / 128;
+  for (int s = warp; s < slices; s += 8) {
+    float acc = 0.0f;
+    for (int c = s * 128 + lane; c < min(d, s * 128 + 128); c += 32) {
+      const uint16_t b = E[(size_t)tok * d + c];
+      const float v = __uint_as_float((uint32_t)b << 16);
+      x[(size_t)j * d + c] = v;
+      xb[(size_t)j * d + c] = b;
+      acc += v * v;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) ssq[s * kTok + j] = acc;
+  }
+}
+
+// After a prefill chunk of c tokens: the last chunk records the root (argmax of its last logits row) and the
+// node the heads read (c - 1) in the result; earlier chunks just advance the length.
+__global__ void __launch_bounds__(1024) prefill_finish_kernel(const float* __restrict__ logits, int V, int ld, int c,
+                                                             int last, int32_t* cur_len,
+                                                             mv_posterior_result* res) {
+  if (!last) {
+    if (threadIdx.x == 0) *cur_len += c;
+    return;
+  }
+  const float* row = logits + (size_t)(c - 1) * ld;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int i = threadIdx.x; i < V; i += blockDim.x) {
+    const float v = row[i];
+    if (vi_better(v, i, bv, bi)) {
+      bv = v;
+      bi = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (vi_better(ov, oi, bv, bi)) {
+      bv = ov;
+      bi = oi;
+    }
+  }
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  if ((threadIdx.x & 31) == 0) {
+    sv[threadIdx.x >> 5] = bv;
+    si[threadIdx.x >> 5] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
+      if (vi_better(sv[w], si[w], bv, bi)) {
+        bv = sv[w];
+        bi = si[w];
+      }
+    res->best = 0;
+    res->acc = c - 1;
+    res->next_node = c - 1;
+    res->next_root = bi;
+    res->n_tokens = c;  // the heads kernel commits cur_len += c
+  }
+}
+
+__global__ void set_int_kernel(int32_t* p, int v) { *p = v; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+struct mv_model {
+  mv_model_dims dims;
+  const uint16_t* embed;
+  std::vector<const uint16_t*> wqkv, wo, w_gate, w_up, w_down;
+  const uint16_t* lm_head;
+  const uint16_t* w1;
+  const uint16_t* w2;
+  std::vector<CUtensorMap> m_qkv, m_o, m_gate, m_up, m_down;
+  CUtensorMap m_lm;
+};
+
+struct mv_session {
+  mv_model* model;
+  const mv_tree* tree;
+  mv_tree* chain;  // 64-node chain tree for prefill chunks (causal mask)
+  uint16_t* kv;
+  int s_max, topk;
+  // device buffers carved from the workspace
+  int32_t* cur_len;
+  mv_posterior_result* result;
+  int32_t* head_topk;
+  int32_t* tree_tokens;
+  int32_t* cart;
+  float* x;
+  uint16_t* xb;
+  float* ssq;
+  uint16_t* q;
+  uint16_t* attn;
+  uint16_t* act;
+  float* logits;
+  int ld_logits;
+  void* ws_gemm;
+  void* ws_attn;
+  void* ws_post;
+  void* ws_heads;
+  CUtensorMap m_xb, m_attn, m_act, m_kv;
+  // optional per-launch timing (mv_session_profile): event pairs recorded around every launch
+  bool profiling = false;
+  std::vector<cudaEvent_t> ev_pool;
+  std::vector<std::pair<int, int>> ev_used;  // (kind, index of the first event of the pair)
+  size_t ev_next = 0;
+};
+
+namespace {
+
+// Records an event on `st` for a profiled launch of `kind`; returns the pool index or -1.
+int prof_mark(mv_session* s, cudaStream_t st) {
+  if (!s->profiling) return -1;
+  if (s->ev_next >= s->ev_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return -1;
+    s->ev_pool.push_back(e);
+  }
+  const int i = (int)s->ev_next++;
+  cudaEventRecord(s->ev_pool[i], st);
+  return i;
+}
+
+struct ProfScope {
+  mv_session* s;
+  cudaStream_t st;
+  int kind, first;
+  ProfScope(mv_session* s_, cudaStream_t st_, int kind_) : s(s_), st(st_), kind(kind_) { first = prof_mark(s, st); }
+  ~ProfScope() {
+    const int second = prof_mark(s, st);
+    if (first >= 0 && second == first + 1) s->ev_used.push_back({kind, first});
+  }
+};
+
+}  // namespace
+
+namespace {
+
+struct SessionLayout {
+  size_t state, tree_tokens, cart, x, xb, ssq, q, attn, act, logits, gemm, attn_ws, post, heads, total;
+};
+
+SessionLayout session_layout(const mv_model_dims& d, int s_max, int topk) {
+  SessionLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  const int HD = d.n_heads * d.head_dim;
+  const int ldl = (d.vocab + 3) & ~3;
+  L.state = take(512 + (size_t)d.n_medusa * topk * 4);
+  L.tree_tokens = take(kTok * 4);
+  L.cart = take((size_t)kTok * (MV_MAX_DEPTH + 1) * 4);
+  L.x = take((size_t)kTok * d.d * 4);
+  L.xb = take((size_t)kTok * d.d * 2);
+  L.ssq = take((size_t)((d.d + 127) / 128) * kTok * 4);
+  L.q = take((size_t)kTok * HD * 2);
+  L.attn = take((size_t)kTok * HD * 2);
+  L.act = take((size_t)kTok * d.ffn * 2);
+  L.logits = take((size_t)kTok * ldl * 4);
+  L.gemm = take(gemm_ws_bytes());
+  L.attn_ws = take(tree_attn_ws_bytes(d.n_heads, d.head_dim, s_max, kTok));
+  L.post = take(posterior_ws_bytes(kTok));
+  L.heads = take(heads_ws_bytes(1, d.d, d.n_medusa, d.vocab, topk));
+  L.total = o;
+  return L;
+}
+
+bool dims_ok(const mv_model_dims& d) {
+  const int D = d.head_dim;
+  if (d.d < 8 || (d.d & 7) || d.n_layers < 1 || d.n_heads < 1 || d.ffn < 8 || (d.ffn & 7) || d.vocab < 16 ||
+      d.n_medusa < 1 || d.n_medusa > 8)
+    return false;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return false;
+  if (((d.n_heads * D) & 7) || d.d > 8192) return false;
+  return d.norm_eps > 0.0f && d.rope_theta > 1.0f;
+}
+
+GemmParams base_params(const mv_session* s, int n_tok) {
+  GemmParams p{};
+  p.n_tok = n_tok;
+  p.eps = s->model->dims.norm_eps;
+  p.err = mv_error_word();
+  gemm_ws_layout(s->ws_gemm, &p.partials, &p.tickets);
+  return p;
+}
+
+// One backbone pass over n tokens (tree nodes or a prefill chunk) whose ids are at d_tokens. `t` gives the
+// attention mask (ancestor words) and positions (depth); the prefix length is read from s->cur_len.
+mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int n, bool lm, cudaStream_t st) {
+  const mv_model* m = s->model;
+  const mv_model_dims& d = m->dims;
+  const int HD = d.n_heads * d.head_dim;
+  const int ssq_parts = (d.d + 127) / 128;
+  mv_status rc;
+  {
+    ProfScope ps(s, st, MV_PROF_OTHER);
+    embed_kernel<<<n, 256, 0, st>>>(d_tokens, m->embed, d.vocab, d.d, s->x, s->xb, s->ssq, mv_error_word());
+    rc = mv_last_launch("embed");
+  }
+  for (int l = 0; l < d.n_layers && rc == MV_OK; ++l) {
+    {  // QKV + RoPE + KV append
+      GemmParams p = base_params(s, n);
+      p.M = 3 * HD;
+      p.K = d.d;
+      p.ssq = s->ssq;
+      p.ssq_parts = ssq_parts;
+      p.norm_d = d.d;
+      p.q_out = s->q;
+      p.kv = s->kv;
+      p.H = d.n_heads;
+      p.D = d.head_dim;
+      p.S_max = s->s_max;
+      p.layer = l;
+      p.cur_len = s->cur_len;
+      p.pos_ids = t->d_position_ids;
+      p.log2_theta = log2f(d.rope_theta);
+      gemm_finish_params(p);
+      ProfScope ps(s, st, MV_PROF_GEMM_QKV);
+      rc = launch_gemm(EPI_QKV, m->m_qkv[l], m->m_qkv[l], s->m_xb, p, st);
+    }
+    if (rc != MV_OK) break;
+    {
+      ProfScope ps(s, st, MV_PROF_ATTENTION);
+      rc = launch_tree_attention_n(s->m_kv, s->m_kv, 2 * l, 2 * l + 1, s->q, d.n_heads, d.head_dim, s->s_max,
+                                   s->cur_len, 0, s->s_max - n, t, n, 1.0f / sqrtf((float)d.head_dim), s->attn,
+                                   s->ws_attn, st);
+    }
+    if (rc != MV_OK) break;
+    {  // O projection + residual
+      GemmParams p = base_params(s, n);
+      p.M = d.d;
+      p.K = HD;
+      p.x = s->x;
+      p.xb = s->xb;
+      p.ssq_out = s->ssq;
+      gemm_finish_params(p);
+      ProfScope ps(s, st, MV_PROF_GEMM_O);
+      rc = launch_gemm(EPI_RESIDUAL, m->m_o[l], m->m_o[l], s->m_attn, p, st);
+    }
+    if (rc != MV_OK) break;
+    {  // gate/up + SiLU-gate
+      GemmParams p = base_params(s, n);
+      p.paired = 1;
+      p.F = d.ffn;
+      p.M = d.ffn;
+      p.K = d.d;
+      p.ssq = s->ssq;
+      p.ssq_parts = ssq_parts;
+      p.norm_d = d.d;
+      p.act = s->act;
+      gemm_finish_params(p);
+      ProfScope ps(s, st, MV_PROF_GEMM_GATE_UP);
+      rc = launch_gemm(EPI_SWIGLU, m->m_gate[l], m->m_up[l], s->m_xb, p, st);
+    }
+    if (rc != MV_OK) break;
+    {  // down + residual
+      GemmParams p = base_params(s, n);
+      p.M = d.d;
+      p.K = d.ffn;
+      p.x = s->x;
+      p.xb = s->xb;
+      p.ssq_out = s->ssq;
+      gemm_finish_params(p);
+      ProfScope ps(s, st, MV_PROF_GEMM_DOWN);
+      rc = launch_gemm(EPI_RESIDUAL, m->m_down[l], m->m_down[l], s->m_act, p, st);
+    }
+  }
+  if (rc == MV_OK && lm) {  // final RMSNorm (as a column scale) + LM head -> fp32 logits
+    GemmParams p = base_params(s, n);
+    p.M = d.vocab;
+    p.K = d.d;
+    p.ssq = s->ssq;
+    p.ssq_parts = ssq_parts;
+    p.norm_d = d.d;
+    p.out_f32 = s->logits;
+    p.ld_out = s->ld_logits;
+    gemm_finish_params(p);
+    ProfScope ps(s, st, MV_PROF_GEMM_LM);
+    rc = launch_gemm(EPI_STORE, m->m_lm, m->m_lm, s->m_xb, p, st);
+  }
+  return rc;
+}
+
+mv_status run_heads(mv_session* s, cudaStream_t st) {
+  ProfScope ps(s, st, MV_PROF_HEADS);
+  const mv_model* m = s->model;
+  const mv_model_dims& d = m->dims;
+  return launch_heads(nullptr, s->x, s->result, d.norm_eps, 1, d.d, d.n_medusa, m->w1, m->w2, d.vocab, s->topk,
+                      nullptr, s->head_topk, nullptr, nullptr, s->cur_len, s->ws_heads, st);
+}
+
+}  // namespace
+
+extern "C" mv_status mv_model_create(const mv_model_dims* dims, const mv_model_weights* w, mv_model** out) {
+  if (!dims || !w || !out) return MV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!dims_ok(*dims)) return MV_ERR_SHAPE;
+  const mv_model_dims& d = *dims;
+  if (!w->embed || !w->lm_head || !w->medusa_w1 || !w->medusa_w2 || !w->wqkv || !w->wo || !w->w_gate ||
+      !w->w_up || !w->w_down)
+    return MV_ERR_INVALID_ARG;
+  mv_model* m = new mv_model();
+  m->dims = d;
+  m->embed = w->embed;
+  m->lm_head = w->lm_head;
+  m->w1 = w->medusa_w1;
+  m->w2 = w->medusa_w2;
+  const int HD = d.n_heads * d.head_dim;
+  bool ok = true;
+  m->m_qkv.resize(d.n_layers);
+  m->m_o.resize(d.n_layers);
+  m->m_gate.resize(d.n_layers);
+  m->m_up.resize(d.n_layers);
+  m->m_down.resize(d.n_layers);
+  for (int l = 0; l < d.n_layers && ok; ++l) {
+    const uint16_t* ptrs[5] = {w->wqkv[l], w->wo[l], w->w_gate[l], w->w_up[l], w->w_down[l]};
+    for (const uint16_t* p : ptrs) ok = ok && p && !(reinterpret_cast<uintptr_t>(p) & 15);
+    if (!ok) break;
+    m->wqkv.push_back(w->wqkv[l]);
+    m->wo.push_back(w->wo[l]);
+    m->w_gate.push_back(w->w_gate[l]);
+    m->w_up.push_back(w->w_up[l]);
+    m->w_down.push_back(w->w_down[l]);
+    ok = gemm_weight_map(&m->m_qkv[l], w->wqkv[l], 3 * HD, d.d, 128) &&
+         gemm_weight_map(&m->m_o[l], w->wo[l], d.d, HD, 128) &&
+         gemm_weight_map(&m->m_gate[l], w->w_gate[l], d.ffn, d.d, 64) &&
+         gemm_weight_map(&m->m_up[l], w->w_up[l], d.ffn, d.d, 64) &&
+         gemm_weight_map(&m->m_down[l], w->w_down[l], d.d, d.ffn, 128);
+  }
+  ok = ok && gemm_weight_map(&m->m_lm, w->lm_head, d.vocab, d.d, 128);
+  if (!ok) {
+    delete m;
+    return MV_ERR_SHAPE;
+  }
+  *out = m;
+  return MV_OK;
+}
+
+extern "C" void mv_model_destroy(mv_model* m) { delete m; }
+
+extern "C" mv_status mv_session_workspace(const mv_model* m, int32_t s_max, int32_t topk, size_t* bytes) {
+  if (!m || !bytes || s_max < 1 || topk < 1 || topk > 16) return MV_ERR_INVALID_ARG;
+  *bytes = session_layout(m->dims, s_max, topk).total;
+  return MV_OK;
+}
+
+extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16* kv, int32_t s_max, int32_t topk,
+                                       void* ws, size_t ws_bytes, mv_session** out) {
+  if (!m || !tree || !kv || !ws || !out) return MV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!tree->d_ancestors) return MV_ERR_CUDA;
+  const mv_model_dims& d = m->dims;
+  if (topk < tree->topk || topk > 16 || tree->depth > d.n_medusa || tree->n_nodes > kTok) return MV_ERR_SHAPE;
+  if (s_max < kTok + 1) return MV_ERR_CAPACITY;
+  const SessionLayout L = session_layout(d, s_max, topk);
+  if (ws_bytes < L.total) return MV_ERR_CAPACITY;
+  if ((reinterpret_cast<uintptr_t>(ws) | reinterpret_cast<uintptr_t>(kv)) & 255) return MV_ERR_INVALID_ARG;
+  mv_session* s = new mv_session();
+  s->model = m;
+  s->tree = tree;
+  s->kv = kv;
+  s->s_max = s_max;
+  s->topk = topk;
+  char* b = static_cast<char*>(ws);
+  s->cur_len = reinterpret_cast<int32_t*>(b + L.state);
+  s->result = reinterpret_cast<mv_posterior_result*>(b + L.state + 64);
+  s->head_topk = reinterpret_cast<int32_t*>(b + L.state + 512);
+  s->tree_tokens = reinterpret_cast<int32_t*>(b + L.tree_tokens);
+  s->cart = reinterpret_cast<int32_t*>(b + L.cart);
+  s->x = reinterpret_cast<float*>(b + L.x);
+  s->xb = reinterpret_cast<uint16_t*>(b + L.xb);
+  s->ssq = reinterpret_cast<float*>(b + L.ssq);
+  s->q = reinterpret_cast<uint16_t*>(b + L.q);
+  s->attn = reinterpret_cast<uint16_t*>(b + L.attn);
+  s->act = reinterpret_cast<uint16_t*>(b + L.act);
+  s->logits = reinterpret_cast<float*>(b + L.logits);
+  s->ld_logits = (d.vocab + 3) & ~3;
+  s->ws_gemm = b + L.gemm;
+  s->ws_attn = b + L.attn_ws;
+  s->ws_post = b + L.post;
+  s->ws_heads = b + L.heads;
+  const int HD = d.n_heads * d.head_dim;
+  bool ok = gemm_act_map(&s->m_xb, s->xb, kTok, d.d) && gemm_act_map(&s->m_attn, s->attn, kTok, HD) &&
+            gemm_act_map(&s->m_act, s->act, kTok, d.ffn);
+  CUtensorMap vdummy;
+  ok = ok && tree_attn_make_maps(&s->m_kv, &vdummy, kv, kv, d.n_heads, d.head_dim, s_max, 2 * d.n_layers,
+                                 (size_t)d.n_heads * s_max * d.head_dim * 2);
+  // 64-node chain (causal) tree for prefill chunks
+  s->chain = nullptr;
+  if (ok) {
+    // the chain is deeper than MV_MAX_DEPTH, so it is built directly rather than through mv_tree_create
+    mv_tree* c = new mv_tree();
+    c->n_nodes = kTok;
+    c->n_paths = 1;
+    c->depth = kTok - 1;
+    c->topk = 1;
+    std::vector<int32_t> pos(kTok);
+    std::vector<uint64_t> anc(kTok);
+    for (int i = 0; i < kTok; ++i) {
+      pos[i] = i;
+      anc[i] = (i == 63) ? ~0ull : ((1ull << (i + 1)) - 1);
+    }
+    c->h_tree_indices = c->h_retrieve = c->h_parent = nullptr;
+    c->h_position_ids = nullptr;
+    c->h_ancestors = nullptr;
+    c->d_tree_indices = c->d_retrieve = c->d_parent = nullptr;
+    c->device = tree->device;
+    ok = cudaMalloc(&c->d_position_ids, kTok * 4) == cudaSuccess &&
+         cudaMalloc(&c->d_ancestors, kTok * 8) == cudaSuccess &&
+         cudaMemcpy(c->d_position_ids, pos.data(), kTok * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemcpy(c->d_ancestors, anc.data(), kTok * 8, cudaMemcpyHostToDevice) == cudaSuccess;
+    s->chain = c;
+  }
+  ok = ok && cudaMemset(ws, 0, L.total) == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
+  if (!ok) {
+    mv_session_destroy(s);
+    return MV_ERR_CUDA;
+  }
+  *out = s;
+  return MV_OK;
+}
+
+extern "C" void mv_session_destroy(mv_session* s) {
+  if (!s) return;
+  for (cudaEvent_t e : s->ev_pool) cudaEventDestroy(e);
+  if (s->chain) {
+    cudaFree(s->chain->d_position_ids);
+    cudaFree(s->chain->d_ancestors);
+    delete s->chain;
+  }
+  delete s;
+}
+
+extern "C" mv_status mv_session_state(const mv_session* s, mv_session_state_ptrs* out) {
+  if (!s || !out) return MV_ERR_INVALID_ARG;
+  out->cur_len = s->cur_len;
+  out->result = s->result;
+  out->head_topk = s->head_topk;
+  out->tree_tokens = s->tree_tokens;
+  out->cart = s->cart;
+  out->logits = s->logits;
+  out->ld_logits = s->ld_logits;
+  out->hidden = s->x;
+  return MV_OK;
+}
+
+extern "C" mv_status mv_prefill(mv_session* s, const int32_t* d_tokens, int32_t n, mv_stream stream) {
+  if (!s || !d_tokens || n < 1) return MV_ERR_INVALID_ARG;
+  if (n + kTok > s->s_max) return MV_ERR_CAPACITY;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  set_int_kernel<<<1, 1, 0, st>>>(s->cur_len, 0);
+  mv_status rc = mv_last_launch("prefill");
+  for (int o = 0; o < n && rc == MV_OK; o += kTok) {
+    const int c = std::min(kTok, n - o);
+    const bool last = o + c == n;
+    rc = forward(s, s->chain, d_tokens + o, c, last, st);
+    if (rc != MV_OK) break;
+    prefill_finish_kernel<<<1, 1024, 0, st>>>(s->logits, s->model->dims.vocab, s->ld_logits, c, last ? 1 : 0,
+                                              s->cur_len, s->result);
+    rc = mv_last_launch("prefill_finish");
+  }
+  if (rc == MV_OK) rc = run_heads(s, st);
+  return rc;
+}
+
+extern "C" mv_status medusa_verify_step(mv_session* s, mv_accept_params prm, mv_stream stream) {
+  if (!s) return MV_ERR_INVALID_ARG;
+  if (prm.mode != MV_GREEDY && prm.mode != MV_TYPICAL) return MV_ERR_INVALID_ARG;
+  if (prm.mode == MV_TYPICAL && !(prm.temperature > 0.0f)) return MV_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const mv_tree* t = s->tree;
+  const mv_model_dims& d = s->model->dims;
+  // candidates from the previous step's root (result.next_root) and head top-k
+  mv_status rc;
+  {
+    ProfScope ps(s, st, MV_PROF_OTHER);
+    rc = launch_build_candidates(&s->result->next_root, s->head_topk, s->topk, t, s->tree_tokens, s->cart, st);
+  }
+  if (rc == MV_OK) rc = forward(s, t, s->tree_tokens, t->n_nodes, true, st);
+  if (rc == MV_OK) {
+    ProfScope ps(s, st, MV_PROF_POSTERIOR);
+    rc = launch_posterior(s->logits, d.vocab, s->ld_logits, s->tree_tokens, t, prm, s->result, nullptr, nullptr,
+                          s->ws_post, st);
+  }
+  if (rc == MV_OK) {
+    ProfScope ps(s, st, MV_PROF_KV_COMPACT);
+    rc = launch_kv_compact(s->kv, d.n_layers, d.n_heads, s->s_max, d.head_dim, s->cur_len, 0, s->result, nullptr,
+                           st);
+  }
+  if (rc == MV_OK) rc = run_heads(s, st);
+  return rc;
+}
+
+extern "C" mv_status medusa_verify_step_host(mv_session* s, mv_accept_params prm, const int32_t* h_seeds_in,
+                                             int32_t* h_result, int32_t* h_seeds_out, mv_stream stream) {
+  if (!s || !h_result) return MV_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int k = s->model->dims.n_medusa * s->topk;
+  if (h_seeds_in) {
+    if (cudaMemcpyAsync(&s->result->next_root, h_seeds_in, 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(s->head_topk, h_seeds_in + 1, (size_t)k * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return MV_ERR_CUDA;
+  }
+  mv_status rc = medusa_verify_step(s, prm, stream);
+  if (rc != MV_OK) return rc;
+  if (cudaMemcpyAsync(h_result, s->result, sizeof(mv_posterior_result), cudaMemcpyDeviceToHost, st) !=
+      cudaSuccess)
+    return MV_ERR_CUDA;
+  if (h_seeds_out) {  // the next step's seeds: new root, then the head top-k
+    if (cudaMemcpyAsync(h_seeds_out, &s->result->next_root, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(h_seeds_out + 1, s->head_topk, (size_t)k * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return MV_ERR_CUDA;
+  }
+  return cudaStreamSynchronize(st) == cudaSuccess ? MV_OK : MV_ERR_CUDA;
+}
+
+extern "C" mv_status mv_session_profile(mv_session* s, int32_t enable) {
+  if (!s) return MV_ERR_INVALID_ARG;
+  s->profiling = enable != 0;
+  if (s->profiling) {
+    s->ev_used.clear();
+    s->ev_next = 0;
+  }
+  return MV_OK;
+}
+
+extern "C" mv_status mv_session_profile_read(mv_session* s, float* ms_by_kind, int32_t* launches_by_kind) {
+  if (!s || !ms_by_kind || !launches_by_kind) return MV_ERR_INVALID_ARG;
+  for (int k = 0; k < MV_PROF_KINDS; ++k) {
+    ms_by_kind[k] = 0.0f;
+    launches_by_kind[k] = 0;
+  }
+  if (s->ev_next > 0 && cudaEventSynchronize(s->ev_pool[s->ev_next - 1]) != cudaSuccess) return MV_ERR_CUDA;
+  for (const auto& u : s->ev_used) {
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, s->ev_pool[u.second], s->ev_pool[u.second + 1]) != cudaSuccess) return MV_ERR_CUDA;
+    ms_by_kind[u.first] += ms;
+    launches_by_kind[u.first] += 1;
+  }
+  s->ev_used.clear();
+  s->ev_next = 0;
+  return MV_OK;
+}

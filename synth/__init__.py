@@ -33,7 +33,7 @@ __all__ = [
     "GAMMA", "stream_key", "hash_words", "normal", "uniform01", "randint",
     "ModelDims", "TINY", "LLAMA7B", "model_weights", "weight_names",
     "dense_tree_choices", "synthetic_tree_choices", "prompt_tokens",
-    "planted_tokens_and_logits", "kv_cache",
+    "planted_tokens_and_logits", "kv_cache", "packed_weights",
 ]
 
 MASK64 = (1 << 64) - 1
@@ -157,6 +157,64 @@ def model_weights(dims: ModelDims, seed: int = 0, dtype=torch.float32, device="c
     sel = None if names is None else set(names)
     return {n: normal(seed, n, s, dims.std, dtype=dtype, device=device)
             for n, s in weight_names(dims) if sel is None or n in sel}
+
+
+def packed_weights(dims: ModelDims, seed: int = 0, dtype=torch.bfloat16, device="cpu"):
+    """The same weights as ``model_weights``, laid out for the verify library.
+
+    wqkv[l] = rows of wq, then wk, then wv of layer l (one [3*H*D, d] matrix); medusa_w1 / medusa_w2 stack the
+    heads ([K, d, d] / [K, V, d]). Pure layout: every value is the one ``model_weights`` draws.
+    """
+    d, qd, v, K = dims.d, dims.n_heads * dims.head_dim, dims.vocab, dims.n_medusa
+    g = lambda name, shape: normal(seed, name, shape, dims.std, dtype=dtype, device=device)
+    w = {"embed": g("embed", (v, d)), "lm_head": g("lm_head", (v, d)),
+         "wqkv": [], "wo": [], "w_gate": [], "w_up": [], "w_down": []}
+    for l in range(dims.n_layers):
+        qkv = torch.empty(3 * qd, d, dtype=dtype, device=device)
+        for i, c in enumerate("qkv"):
+            qkv[i * qd:(i + 1) * qd] = g(f"layer{l}.w{c}", (qd, d))
+        w["wqkv"].append(qkv)
+        w["wo"].append(g(f"layer{l}.wo", (d, qd)))
+        w["w_gate"].append(g(f"layer{l}.w_gate", (dims.ffn, d)))
+        w["w_up"].append(g(f"layer{l}.w_up", (dims.ffn, d)))
+        w["w_down"].append(g(f"layer{l}.w_down", (d, dims.ffn)))
+    w1 = torch.empty(K, d, d, dtype=dtype, device=device)
+    w2 = torch.empty(K, v, d, dtype=dtype, device=device)
+    for k in range(K):
+        w1[k] = g(f"medusa{k}.w1", (d, d))
+        w2[k] = g(f"medusa{k}.w2", (v, d))
+    w["medusa_w1"], w["medusa_w2"] = w1, w2
+    return w
+
+
+def unpacked_getter(dims: ModelDims, w):
+    """name -> float64 numpy view of one logical weight of a ``packed_weights`` dict (for the oracle)."""
+    qd = dims.n_heads * dims.head_dim
+    cache = {}
+
+    def get(name):
+        if name in cache:
+            return cache[name]
+        if name.startswith("layer"):
+            l, key = name[5:].split(".")
+            l = int(l)
+            if key in ("wq", "wk", "wv"):
+                i = "qkv".index(key[1])
+                t = w["wqkv"][l][i * qd:(i + 1) * qd]
+            else:
+                t = w[key][l]
+        elif name.startswith("medusa"):
+            k, key = name[6:].split(".")
+            t = w["medusa_" + key][int(k)]
+        else:
+            t = w[name]
+        a = t.double().cpu().numpy()
+        if len(cache) > 64:
+            cache.clear()
+        cache[name] = a
+        return a
+
+    return get
 
 
 def prompt_tokens(seed: int, n: int, vocab: int, name: str = "prompt", device="cpu") -> torch.Tensor:
