@@ -185,7 +185,7 @@ def run_gpu(args, world, rank, local):
     w = synth.packed_weights(dims, 0, torch.bfloat16, "cuda")
     model = mv.Model(dims, w)
     tree = mv.Tree(synth.synthetic_tree_choices(TREE["n_nodes"], TREE["depth"], TREE["topk"]), TREE["topk"])
-    n_steps_total = args.warmup + 2 * args.steps + 8
+    n_steps_total = args.warmup + 5 * args.steps + 8
     s_max = PROMPT_LEN + (TREE["depth"] + 1) * n_steps_total + 64
     s_max = (s_max + 63) // 64 * 64
     sess = mv.Session(model, tree, s_max)
@@ -194,38 +194,52 @@ def run_gpu(args, world, rank, local):
     stream = torch.cuda.current_stream()
 
     sess.prefill(prompt)
-    for _ in range(args.warmup):
+    for _ in range(args.warmup):  # eager warm-up steps
         sess.step(prm)
+    torch.cuda.synchronize()
+    sess.steps_graph(args.steps, prm)  # capture K steps into one CUDA graph + one warm replay
     torch.cuda.synchronize()
     st, code = mv.get_error()
     if st != 0:
         raise RuntimeError(f"device error word {code:#x}")
 
-    # ---- timed: K steps, inputs resident in HBM, per-launch events of the projection kernel
+    # ---- timed: K steps (one graph replay), inputs resident in HBM
     launches_per_step = 1 + 1 + dims.n_layers * 5 + 1 + 1 + 1 + 2
-    prof = mv.Profiler(sess)
-    acc_total = 0
     barrier(world)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
-        prof.enable()
         start.record(stream)
-        for _ in range(args.steps):
-            sess.step(prm)
+        sess.steps_graph(args.steps, prm)
         end.record(stream)
         torch.cuda.synchronize()
-        prof.disable()
-    per_kind = prof.read()
     barrier(world)
-    ms = start.elapsed_time(end)
-    ms = max_over_ranks(ms, world)
+    ms = max_over_ranks(start.elapsed_time(end), world)
+    r = sess.read_result()
+
+    # ---- the same K steps again with CUDA events around every launch (graph with event nodes): per-kernel time
+    prof = mv.Profiler(sess)
+    prof.enable()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    sess.steps_graph(args.steps, prm)
+    b.record(stream)
+    torch.cuda.synchronize()
+    per_kind = prof.read()
+    prof.disable()
+    profiled_ms = a.elapsed_time(b)
+
+    # ---- eager launches of K steps (no graph), for comparison
+    a.record(stream)
+    for _ in range(args.steps):
+        sess.step(prm)
+    b.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = a.elapsed_time(b)
     st, code = mv.get_error()
     if st != 0:
         raise RuntimeError(f"device error word {code:#x}")
-    accs = []
     r = sess.read_result()
-    accs.append(r["acc"])
 
     # ---- e2e: the host-buffer entry point (H2D seeds, step, D2H result + next seeds, stream sync per step)
     k = dims.n_medusa * TREE["topk"]
@@ -274,6 +288,8 @@ def run_gpu(args, world, rank, local):
         "e2e": {"value": args.steps * world / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": 4 * (1 + k),
                 "d2h_bytes_per_step": 4 * mv.RESULT_INTS + 4 * (1 + k)},
         "gpu_launches": launches_per_step * args.steps,
+        "timing": {"graph_ms_per_step": ms / args.steps, "profiled_graph_ms_per_step": profiled_ms / args.steps,
+                   "eager_ms_per_step": eager_ms / args.steps},
         "roofline": roofline,
         "clocks": clk.summary(),
     }
@@ -290,6 +306,41 @@ def gemm_bytes(dims, n):
             "gemm_lm": 2 * V * d + 2 * n * d + 4 * n * V}
 
 
+MICRO = {  # name -> (M, K, n): projections of the 7B step, timed alone through mv_linear_bf16
+    "lm_head": (32000, 4096, 64), "gate_up": (22016, 4096, 64), "down": (4096, 11008, 64),
+    "qkv": (12288, 4096, 64), "o": (4096, 4096, 64),
+}
+
+
+def run_micro(name, steps, warmup):
+    """The projection kernel alone on one shape: HBM GB/s of weights + activations per launch (CUDA events)."""
+    import medusa_tree_speculative_verify_gb300 as mv
+    M, K, n = MICRO[name]
+    w = synth.normal(1, "w", (M, K), 0.02, dtype=torch.bfloat16, device="cuda")
+    x = synth.normal(2, "x", (n, K), 1.0, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(n, M, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(mv.linear_bf16_workspace(), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")  # 256 MB > L2, written between launches
+    for _ in range(warmup):
+        mv.linear_bf16(w, x, out, ws)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        mv.linear_bf16(w, x, out, ws)
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    nbytes = 2 * M * K + 2 * n * K + 4 * n * M
+    peak, kind = peaks()
+    return {"micro": name, "M": M, "K": K, "n": n, "median_us": ms * 1e3, "gbs": nbytes / (ms / 1e3) / 1e9,
+            "frac": nbytes / (ms / 1e3) / 1e9 / peak, "peak": peak, "peak_kind": kind, "l2": "flushed"}
+
+
 def weight_bytes(dims):
     d, HD, F, V, K, L = dims.d, dims.n_heads * dims.head_dim, dims.ffn, dims.vocab, dims.n_medusa, dims.n_layers
     per_layer = 2 * (3 * HD * d + d * HD + 2 * F * d + d * F)
@@ -303,8 +354,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--micro", choices=sorted(MICRO), help="time one projection shape alone and exit")
     args = ap.parse_args()
     world, rank, local = dist_setup()
+    if args.micro:
+        print(json.dumps(run_micro(args.micro, args.steps, args.warmup)))
+        return
 
     if args.impl == "reference":
         if rank != 0:

@@ -266,6 +266,13 @@ mv_status medusa_verify_step(mv_session* session, mv_accept_params params, mv_st
 mv_status medusa_verify_step_host(mv_session* session, mv_accept_params params, const int32_t* h_seeds_in,
                                   int32_t* h_result, int32_t* h_seeds_out, mv_stream stream);
 
+/* n_steps consecutive verify steps as one CUDA graph: captured (on a library-owned stream) on the first call
+ * with these params / n_steps / profiling setting, then replayed on `stream` with a single launch. The graph
+ * reads every step-varying quantity from device memory, so each replay continues the decode. Results of the
+ * intermediate steps are not kept (the session result holds the last one). With profiling enabled at capture
+ * the graph records the per-launch events of all n steps; mv_session_profile_read after a replay returns them. */
+mv_status medusa_verify_steps_graph(mv_session* session, mv_accept_params params, int32_t n_steps, mv_stream stream);
+
 /* Per-launch timing of a session's kernels, for benchmarks: while enabled, every launch of medusa_verify_step /
  * mv_prefill is bracketed by CUDA events on its stream (do not enable during CUDA graph capture).
  * mv_session_profile_read waits for the last recorded event, returns the summed milliseconds and launch counts

@@ -84,6 +84,7 @@ _SIGS = {
     "mv_prefill": ([_P, _P, _I, _P], _I),
     "medusa_verify_step": ([_P, AcceptParams, _P], _I),
     "medusa_verify_step_host": ([_P, AcceptParams, _P, _P, _P, _P], _I),
+    "medusa_verify_steps_graph": ([_P, AcceptParams, _I, _P], _I),
     "mv_session_profile": ([_P, _I], _I),
     "mv_session_profile_read": ([_P, _P, _P], _I),
     "mv_get_error": ([ctypes.POINTER(_U)], _I),
@@ -333,6 +334,11 @@ class Session:
 
     def step(self, params: AcceptParams = None, stream=None):
         _check(lib().medusa_verify_step(self.handle, params or AcceptParams(), _stream(stream)), "medusa_verify_step")
+
+    def steps_graph(self, n_steps, params: AcceptParams = None, stream=None):
+        """n_steps verify steps replayed as one CUDA graph (captured on first use)."""
+        _check(lib().medusa_verify_steps_graph(self.handle, params or AcceptParams(), n_steps, _stream(stream)),
+               "medusa_verify_steps_graph")
 
     def step_host(self, params, seeds_in, result_out, seeds_out=None, stream=None):
         """Host-buffer step: seeds_in/out int32 [1 + K*topk] (pinned CPU tensors or None), result_out int32."""

@@ -379,12 +379,12 @@ mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vm
   const dim3 grid(H, splits);
   switch (D) {
 #define MV_ATTN_CASE(DD)                                                                                 \
-  case DD:                                                                                             \
-    if (cudaFuncSetAttribute(tree_attn_kernel<DD>, cudaFuncAttributeMaxDynamicSharedMemorySize,         \
-                             (int)smem) != cudaSuccess)                                                \
-      return MV_ERR_CUDA;                                                                              \
+  case DD: {                                                                                           \
+    static int flags[64] = {0};                                                                        \
+    if (!mv_set_smem_once((const void*)tree_attn_kernel<DD>, (int)smem, flags)) return MV_ERR_CUDA;    \
     tree_attn_kernel<DD><<<grid, kThreads, smem, stream>>>(kmap, vmap, a);                             \
-    break;
+    break;                                                                                             \
+  }
     MV_ATTN_CASE(16)
     MV_ATTN_CASE(32)
     MV_ATTN_CASE(64)

@@ -26,6 +26,10 @@ unsigned int* mv_error_word();
 // Host-side helpers.
 mv_status mv_last_launch(const char* what);
 int mv_sm_count();
+int mv_device();
+// Sets the dynamic shared-memory limit of `func` once per device (later calls are free, so launches stay
+// capturable in CUDA graphs). `flags` must point to a zero-initialised int[64] owned by the caller.
+bool mv_set_smem_once(const void* func, int bytes, int* flags);
 
 MV_DEV void mv_set_error(unsigned int* err, uint32_t site, uint32_t kind) {
   if (err) atomicCAS(err, 0u, (site << 16) | kind);

@@ -456,12 +456,12 @@ mv_status launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, con
   const size_t smem = kSmemBytes;
   switch (epi) {
 #define MV_GEMM_CASE(E)                                                                                          \
-  case E:                                                                                                        \
-    if (cudaFuncSetAttribute(gemm_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=          \
-        cudaSuccess)                                                                                             \
-      return MV_ERR_CUDA;                                                                                        \
+  case E: {                                                                                                      \
+    static int flags[64] = {0};                                                                                  \
+    if (!mv_set_smem_once((const void*)gemm_kernel<E>, (int)smem, flags)) return MV_ERR_CUDA;                    \
     gemm_kernel<E><<<p.grid, kThreads, smem, stream>>>(a0, a1, b, p);                                           \
-    break;
+    break;                                                                                                       \
+  }
     MV_GEMM_CASE(EPI_STORE)
     MV_GEMM_CASE(EPI_RESIDUAL)
     MV_GEMM_CASE(EPI_SWIGLU)

@@ -311,8 +311,8 @@ mv_status launch_pair(HeadsArgs a, int V, bool with_lm, int w2_ctas, cudaStream_
   const size_t smem = std::max<size_t>((size_t)slice * B * sizeof(float),
                                        (size_t)a2.ctas_per_mat * a.topk * B * (sizeof(float) + sizeof(int32_t)));
   auto kern = heads_kernel<B, NS, true>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return MV_ERR_CUDA;
+  static int flags[64] = {0};
+  if (!mv_set_smem_once((const void*)kern, (int)smem, flags)) return MV_ERR_CUDA;
   kern<<<dim3(a2.ctas_per_mat, n_mat), kT, smem, stream>>>(a2);
   return mv_last_launch("heads_w2");
 }

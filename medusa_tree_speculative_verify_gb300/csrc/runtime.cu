@@ -35,6 +35,21 @@ int mv_sm_count() {
   return cached[dev];
 }
 
+int mv_device() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return dev;
+}
+
+bool mv_set_smem_once(const void* func, int bytes, int* flags) {
+  const int dev = mv_device();
+  if (dev < 0 || dev >= 64) return false;
+  if (flags[dev] >= bytes) return true;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  flags[dev] = bytes;
+  return true;
+}
+
 mv_status mv_last_launch(const char* what) {
   (void)what;
   cudaError_t e = cudaGetLastError();

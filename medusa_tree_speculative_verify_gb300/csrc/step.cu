@@ -140,10 +140,18 @@ struct mv_session {
   void* ws_post;
   void* ws_heads;
   CUtensorMap m_xb, m_attn, m_act, m_kv;
+  // CUDA graph of n consecutive steps (medusa_verify_steps_graph), captured on first use
+  cudaGraphExec_t graph_exec = nullptr;
+  cudaStream_t capture_stream = nullptr;
+  mv_accept_params graph_prm{};
+  int graph_steps = 0;
+  bool graph_profiled = false;
   // optional per-launch timing (mv_session_profile): event pairs recorded around every launch
   bool profiling = false;
   std::vector<cudaEvent_t> ev_pool;
   std::vector<std::pair<int, int>> ev_used;  // (kind, index of the first event of the pair)
+  std::vector<std::pair<int, int>> profiled_graph_events;  // the pairs a profiled graph records
+  size_t profiled_graph_ev_next = 0;
   size_t ev_next = 0;
 };
 
@@ -466,6 +474,8 @@ extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16
 
 extern "C" void mv_session_destroy(mv_session* s) {
   if (!s) return;
+  if (s->graph_exec) cudaGraphExecDestroy(s->graph_exec);
+  if (s->capture_stream) cudaStreamDestroy(s->capture_stream);
   for (cudaEvent_t e : s->ev_pool) cudaEventDestroy(e);
   if (s->chain) {
     cudaFree(s->chain->d_position_ids);
@@ -584,4 +594,52 @@ extern "C" mv_status mv_session_profile_read(mv_session* s, float* ms_by_kind, i
   s->ev_used.clear();
   s->ev_next = 0;
   return MV_OK;
+}
+
+extern "C" mv_status medusa_verify_steps_graph(mv_session* s, mv_accept_params prm, int32_t n_steps,
+                                               mv_stream stream) {
+  if (!s || n_steps < 1 || n_steps > 4096) return MV_ERR_INVALID_ARG;
+  if (prm.mode != MV_GREEDY && prm.mode != MV_TYPICAL) return MV_ERR_INVALID_ARG;
+  if (prm.mode == MV_TYPICAL && !(prm.temperature > 0.0f)) return MV_ERR_INVALID_ARG;
+  const bool same = s->graph_exec && s->graph_steps == n_steps && s->graph_profiled == s->profiling &&
+                    s->graph_prm.mode == prm.mode && s->graph_prm.temperature == prm.temperature &&
+                    s->graph_prm.eps == prm.eps && s->graph_prm.delta == prm.delta;
+  if (!same) {
+    if (s->graph_exec) {
+      cudaGraphExecDestroy(s->graph_exec);
+      s->graph_exec = nullptr;
+    }
+    if (!s->capture_stream && cudaStreamCreateWithFlags(&s->capture_stream, cudaStreamNonBlocking) != cudaSuccess)
+      return MV_ERR_CUDA;
+    if (s->profiling) {  // the graph records its own events; readings start from this capture
+      s->ev_used.clear();
+      s->ev_next = 0;
+    }
+    if (cudaStreamBeginCapture(s->capture_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+      return MV_ERR_CUDA;
+    mv_status rc = MV_OK;
+    for (int i = 0; i < n_steps && rc == MV_OK; ++i) rc = medusa_verify_step(s, prm, s->capture_stream);
+    cudaGraph_t g = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(s->capture_stream, &g);
+    if (rc != MV_OK || e != cudaSuccess) {
+      if (g) cudaGraphDestroy(g);
+      return rc != MV_OK ? rc : MV_ERR_CUDA;
+    }
+    const cudaError_t ei = cudaGraphInstantiate(&s->graph_exec, g, 0);
+    cudaGraphDestroy(g);
+    if (ei != cudaSuccess) {
+      s->graph_exec = nullptr;
+      return MV_ERR_CUDA;
+    }
+    s->graph_prm = prm;
+    s->graph_steps = n_steps;
+    s->graph_profiled = s->profiling;
+    s->profiled_graph_events = s->ev_used;
+    s->profiled_graph_ev_next = s->ev_next;
+  }
+  if (s->graph_profiled) {  // this replay re-records the captured events
+    s->ev_used = s->profiled_graph_events;
+    s->ev_next = s->profiled_graph_ev_next;
+  }
+  return cudaGraphLaunch(s->graph_exec, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MV_OK : MV_ERR_CUDA;
 }

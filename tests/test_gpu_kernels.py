@@ -138,9 +138,21 @@ def test_posterior_small_ragged(mode, V):
     # plant node 0 -> node 2 -> node 7
     z[0, tokens[2]] = z[0].max() + 3
     z[2, tokens[7]] = z[2].max() + 3
-    res, _, _ = _run_posterior(torch.tensor(z).cuda(), i32(tokens), t, mode, T=1.0)
+    ld = (V + 3) // 4 * 4                        # rows padded to a multiple of 4 floats (API contract)
+    zp = torch.full((9, ld), float("nan"), dtype=torch.float32)
+    zp[:, :V] = torch.tensor(z)
+    res, _, _ = _run_posterior(zp.cuda()[:, :V], i32(tokens), t, mode, T=1.0)
     ref = oracle_posterior(z, tokens, o["retrieve"], mode, 1.0)
     assert _decisions_match(res, ref, mode)
+
+
+def test_posterior_rejects_unaligned_rows():
+    t, _ = both_trees("dense1x2x3")
+    out = torch.zeros(mv.RESULT_INTS, dtype=torch.int32, device="cuda")
+    with pytest.raises(mv.MVError) as e:
+        mv.evaluate_posterior(torch.zeros(9, 7, device="cuda"), i32(np.zeros(9)), t, mv.AcceptParams(), out,
+                              ws(mv.evaluate_posterior_workspace(9)))
+    assert e.value.status == 2
 
 
 def test_posterior_strided_rows_and_typical_tie_break():
