@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
   const int h = blockIdx.x, split = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t4 = lane & 3;
+  pdl_trigger();
+  pdl_wait();  // q, the cache and the prefix length come from earlier kernels
   const int P = a.d_prefix ? *a.d_prefix : a.prefix;
   const int n = a.n;
   if (P < 0 || P + n > a.S_max) {
@@ -382,7 +384,8 @@ mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vm
   case DD: {                                                                                           \
     static int flags[64] = {0};                                                                        \
     if (!mv_set_smem_once((const void*)tree_attn_kernel<DD>, (int)smem, flags)) return MV_ERR_CUDA;    \
-    tree_attn_kernel<DD><<<grid, kThreads, smem, stream>>>(kmap, vmap, a);                             \
+    if (mv_launch(tree_attn_kernel<DD>, grid, dim3(kThreads), smem, stream, kmap, vmap, a) != cudaSuccess) \
+      return MV_ERR_CUDA;                                                                              \
     break;                                                                                             \
   }
     MV_ATTN_CASE(16)

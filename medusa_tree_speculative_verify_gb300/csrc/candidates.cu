@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(128) build_candidates_kernel(const int32_t* __
                                                                const int32_t* __restrict__ retrieve, int n_nodes,
                                                                int n_cart, int32_t* __restrict__ tree_tokens,
                                                                int32_t* __restrict__ cart) {
+  pdl_trigger();
+  pdl_wait();
   for (int i = threadIdx.x; i < n_nodes; i += blockDim.x)
     tree_tokens[i] = candidate(tree_indices[i], root, head_topk, topk, ld);
   if (cart) {
@@ -36,9 +38,10 @@ __global__ void __launch_bounds__(128) build_candidates_kernel(const int32_t* __
 
 mv_status launch_build_candidates(const int32_t* d_root, const int32_t* d_head_topk, int ld_topk, const mv_tree* t,
                                   int32_t* d_tree_tokens, int32_t* d_cart, cudaStream_t stream) {
-  build_candidates_kernel<<<1, 128, 0, stream>>>(d_root, d_head_topk, t->topk, ld_topk, t->d_tree_indices,
-                                                 t->d_retrieve, t->n_nodes, t->n_paths * (t->depth + 1),
-                                                 d_tree_tokens, d_cart);
+  if (mv_launch(build_candidates_kernel, dim3(1), dim3(128), 0, stream, d_root, d_head_topk, t->topk, ld_topk,
+                t->d_tree_indices, t->d_retrieve, t->n_nodes, t->n_paths * (t->depth + 1), d_tree_tokens,
+                d_cart) != cudaSuccess)
+    return MV_ERR_CUDA;
   return mv_last_launch("build_candidates");
 }
 

@@ -31,6 +31,33 @@ int mv_device();
 // capturable in CUDA graphs). `flags` must point to a zero-initialised int[64] owned by the caller.
 bool mv_set_smem_once(const void* func, int bytes, int* flags);
 
+// Programmatic dependent launch: every kernel of the step is launched with programmatic stream serialization,
+// so it may start while the previous kernel drains. pdl_wait() blocks until the previous grid has finished and
+// its writes are visible (a no-op when launched without the attribute); work before it may only read data no
+// earlier kernel writes (the weights). pdl_trigger() lets the next grid start launching.
+MV_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MV_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Whether launches use programmatic dependent launch (default on; MV_PDL=0 in the environment turns it off).
+bool mv_pdl_enabled();
+
+// Launches `kernel` on `st` with the programmatic-stream-serialization attribute when PDL is enabled.
+template <typename... KArgs, typename... Args>
+cudaError_t mv_launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = mv_pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 MV_DEV void mv_set_error(unsigned int* err, uint32_t site, uint32_t kind) {
   if (err) atomicCAS(err, 0u, (site << 16) | kind);
 }

@@ -29,7 +29,7 @@
 namespace {
 
 constexpr int BM = 128, BN = 64, BK = 64;
-constexpr int kStages = 6;
+constexpr int kStages = 8;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kBBytes = BN * BK * 2;  // 8 KB
 constexpr int kStageBytes = kABytes + kBBytes;
@@ -37,7 +37,8 @@ constexpr int kEpiThreads = 128;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kTmemCols = 2 * BN;
 constexpr int kPitch = BN + 1;  // staging row pitch (floats)
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)BM * kPitch * 4 + 256;
+constexpr int kStageRows = 64;  // epilogue staging holds half a tile; exchanges run in two rounds
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)kStageRows * kPitch * 4 + 256;
 
 // kind::f16 instruction descriptor: D fp32, A/B bf16, both K-major, N = 64, M = 128.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
@@ -160,6 +161,8 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int i, float (&v)[BN],
   compute_scales(p, s_scale, i);
   epi_bar();
   const int ntok = p.n_tok;
+  const bool lo = i < 64;
+  float* my = stg + (i & 63) * kPitch;  // staging row shared by rows i and i^64, one round each
   if constexpr (EPI == EPI_STORE) {
     const int R = tile * BM + i;
     if (R < p.M) {
@@ -178,54 +181,80 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int i, float (&v)[BN],
         p.x[(size_t)j * p.M + R] = xn;
         p.xb[(size_t)j * p.M + R] = __bfloat16_as_ushort(__float2bfloat16_rn(xn));
       }
-      stg[i * kPitch + j] = xn * xn;
+      v[j] = xn * xn;
+    }
+    // per-token sum of squares over the tile's 128 rows: upper half staged, lower half adds, then columns
+    if (!lo) {
+#pragma unroll
+      for (int j = 0; j < BN; ++j) my[j] = v[j];
+    }
+    epi_bar();
+    if (lo) {
+#pragma unroll
+      for (int j = 0; j < BN; ++j) my[j] += v[j];
     }
     epi_bar();
     if (i < BN) {
-      float s = 0.0f;
-      for (int r = 0; r < BM; ++r) s += stg[r * kPitch + i];
-      p.ssq_out[tile * BN + i] = s;
+      float sum = 0.0f;
+      for (int r = 0; r < kStageRows; ++r) sum += stg[r * kPitch + i];
+      p.ssq_out[tile * BN + i] = sum;
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
+    // rows 0..63: gate, rows 64..127: the matching up rows
+    if (!lo) {
 #pragma unroll
-    for (int j = 0; j < BN; ++j) stg[i * kPitch + j] = v[j] * s_scale[j];
+      for (int j = 0; j < BN; ++j) my[j] = v[j] * s_scale[j];
+    }
     epi_bar();
-    if (i < 64) {
+    if (lo) {
       const int f = tile * 64 + i;
-      if (f < p.F)
-        for (int j = 0; j < ntok; ++j) {
-          const float g = stg[i * kPitch + j], u = stg[(i + 64) * kPitch + j];
-          p.act[(size_t)j * p.F + f] = __bfloat16_as_ushort(__float2bfloat16_rn(silu(g) * u));
-        }
+      if (f < p.F) {
+#pragma unroll
+        for (int j = 0; j < BN; ++j)
+          if (j < ntok)
+            p.act[(size_t)j * p.F + f] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(silu(v[j] * s_scale[j]) * my[j]));
+      }
     }
   } else if constexpr (EPI == EPI_QKV) {
 #pragma unroll
-    for (int j = 0; j < BN; ++j) stg[i * kPitch + j] = v[j] * s_scale[j];
-    epi_bar();
+    for (int j = 0; j < BN; ++j) v[j] *= s_scale[j];
     const int R = tile * BM + i;
-    if (R < p.M) {
-      const int HD = p.H * p.D;
-      const int which = R / HD, within = R % HD, head = within / p.D, dim = within % p.D;
-      const int half = p.D >> 1;
-      const int prefix = *p.cur_len;
-      const int pi = dim < half ? i + half : i - half;
-      const float inv_freq = exp2f(-(float)(2 * (dim % half)) / (float)p.D * p.log2_theta);
-      for (int j = 0; j < ntok; ++j) {
-        float val = stg[i * kPitch + j];
-        if (which < 2) {
-          const float pv = stg[pi * kPitch + j];
-          float sn, cs;
-          sincosf((float)(prefix + p.pos_ids[j]) * inv_freq, &sn, &cs);
-          val = dim < half ? val * cs - pv * sn : val * cs + pv * sn;
-        }
-        const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(val));
-        if (which == 0) {
-          p.q_out[((size_t)j * p.H + head) * p.D + dim] = b;
-        } else {
-          const size_t plane = (size_t)p.layer * 2 + (which - 1);
-          p.kv[((plane * p.H + head) * p.S_max + prefix + j) * p.D + dim] = b;
+    const bool valid = R < p.M;
+    const int HD = p.H * p.D;
+    const int which = R / HD, within = R % HD, head = within / p.D, dim = within % p.D;
+    const int half = p.D >> 1;
+    const int prefix = *p.cur_len;
+    const int pi = dim < half ? i + half : i - half;  // RoPE partner row (same head, same tile)
+    const float inv_freq = exp2f(-(float)(2 * (dim % half)) / (float)p.D * p.log2_theta);
+    for (int round = 0; round < 2; ++round) {
+      if ((i >> 6) == round) {
+#pragma unroll
+        for (int j = 0; j < BN; ++j) my[j] = v[j];
+      }
+      epi_bar();
+      if (valid && (which == 2 ? round == 0 : (pi >> 6) == round)) {
+        const float* pr = stg + (pi & 63) * kPitch;
+#pragma unroll
+        for (int j = 0; j < BN; ++j) {
+          if (j >= ntok) break;
+          float val = v[j];
+          if (which < 2) {
+            const float pv = pr[j];
+            float sn, cs;
+            sincosf((float)(prefix + p.pos_ids[j]) * inv_freq, &sn, &cs);
+            val = dim < half ? val * cs - pv * sn : val * cs + pv * sn;
+          }
+          const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(val));
+          if (which == 0) {
+            p.q_out[((size_t)j * p.H + head) * p.D + dim] = b;
+          } else {
+            const size_t plane = (size_t)p.layer * 2 + (which - 1);
+            p.kv[((plane * p.H + head) * p.S_max + prefix + j) * p.D + dim] = b;
+          }
         }
       }
+      epi_bar();
     }
   }
   epi_bar();  // the staging buffer and scales are reused by the next segment
@@ -248,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -278,7 +308,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       if (p.paired) tma_prefetch_desc(&amap1);
       tma_prefetch_desc(&bmap);
       int it = 0;
-      bool ok = true;
+      bool ok = true, waited = false;
+      int pend_kb[kStages];  // k-blocks whose weight tile was issued before the previous grid finished
+      int pend = 0;
+      auto issue_b = [&](int stage, int kb) {
+        tma_load_2d(stages + (size_t)stage * kStageBytes + kABytes, &bmap, &full[stage], kb * BK, 0);
+      };
+      auto release = [&]() {  // the activations come from the previous kernel: wait for it, then load them
+        pdl_wait();
+        waited = true;
+        for (int q = 0; q < pend; ++q) issue_b(q, pend_kb[q]);
+      };
       Seg sg;
       for (int si = 0; ok && get_seg(cta, si, p, sg); ++si) {
         for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
@@ -288,7 +328,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             break;
           }
           uint8_t* a = stages + (size_t)s * kStageBytes;
-          uint8_t* b = a + kABytes;
           mbar_arrive_expect_tx(&full[s], kStageBytes);
           if (p.paired) {
             tma_load_2d(a, &amap0, &full[s], kb * BK, sg.tile * 64);
@@ -296,9 +335,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           } else {
             tma_load_2d(a, &amap0, &full[s], kb * BK, sg.tile * BM);
           }
-          tma_load_2d(b, &bmap, &full[s], kb * BK, 0);
+          if (waited) {
+            issue_b(s, kb);
+          } else {
+            pend_kb[pend++] = kb;  // stage == pend - 1 while it < kStages
+            if (pend == kStages) release();
+          }
         }
       }
+      if (!waited) release();
       if (!ok) {
         if (!s_abort) mv_set_error(p.err, 8, MV_DEVERR_TIMEOUT);
         s_abort = 1;
@@ -350,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     // ------------------------------------------------------------------ epilogue (128 threads)
     const int sub = warp & 3;           // TMEM sub-partition this warp may read
     const int i = sub * 32 + lane;      // tile row = TMEM lane
+    pdl_wait();                         // the epilogue reads what earlier kernels wrote
     Seg sg;
     for (int si = 0; get_seg(cta, si, p, sg); ++si) {
       const int buf = si & 1, rr = si >> 1;
@@ -459,7 +505,8 @@ mv_status launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, con
   case E: {                                                                                                      \
     static int flags[64] = {0};                                                                                  \
     if (!mv_set_smem_once((const void*)gemm_kernel<E>, (int)smem, flags)) return MV_ERR_CUDA;                    \
-    gemm_kernel<E><<<p.grid, kThreads, smem, stream>>>(a0, a1, b, p);                                           \
+    if (mv_launch(gemm_kernel<E>, dim3(p.grid), dim3(kThreads), smem, stream, a0, a1, b, p) != cudaSuccess)     \
+      return MV_ERR_CUDA;                                                                                        \
     break;                                                                                                       \
   }
     MV_GEMM_CASE(EPI_STORE)

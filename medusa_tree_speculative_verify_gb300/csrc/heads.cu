@@ -176,6 +176,8 @@ __global__ void __launch_bounds__(kT, 1) heads_kernel(const HeadsArgs a) {
   extern __shared__ float smem[];
   __shared__ float s_red[kR * B * (kT / 32) + 8];
   __shared__ bool s_last;
+  pdl_trigger();
+  pdl_wait();
   const int mat = blockIdx.y, cta = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int S = a.d >> 3;
@@ -299,7 +301,8 @@ mv_status launch_pair(HeadsArgs a, int V, bool with_lm, int w2_ctas, cudaStream_
   a1.rows = a.d;
   a1.ctas_per_mat = max(1, (2 * sms + a.K - 1) / a.K);
   a1.ctas_per_mat = min(a1.ctas_per_mat, max(1, a.d / kR));
-  heads_kernel<B, NS, false><<<dim3(a1.ctas_per_mat, a.K), kT, 0, stream>>>(a1);
+  if (mv_launch(heads_kernel<B, NS, false>, dim3(a1.ctas_per_mat, a.K), dim3(kT), 0, stream, a1) != cudaSuccess)
+    return MV_ERR_CUDA;
   mv_status s = mv_last_launch("heads_w1");
   if (s != MV_OK) return s;
   // W2: K matrices (+ the LM head) of V rows
@@ -313,7 +316,7 @@ mv_status launch_pair(HeadsArgs a, int V, bool with_lm, int w2_ctas, cudaStream_
   auto kern = heads_kernel<B, NS, true>;
   static int flags[64] = {0};
   if (!mv_set_smem_once((const void*)kern, (int)smem, flags)) return MV_ERR_CUDA;
-  kern<<<dim3(a2.ctas_per_mat, n_mat), kT, smem, stream>>>(a2);
+  if (mv_launch(kern, dim3(a2.ctas_per_mat, n_mat), dim3(kT), smem, stream, a2) != cudaSuccess) return MV_ERR_CUDA;
   return mv_last_launch("heads_w2");
 }
 

@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(kWarps * 32) kv_compact_kernel(uint2* __restri
                                                                  int prefix_host,
                                                                  const mv_posterior_result* __restrict__ res,
                                                                  int32_t* __restrict__ cur_len, unsigned int* err) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int unit = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int prefix = prefix_dev ? *prefix_dev : prefix_host;
@@ -66,8 +68,9 @@ mv_status launch_kv_compact(mv_bf16* kv, int L, int H, int S_max, int D, const i
                             const mv_posterior_result* d_res, int32_t* d_cur_len, cudaStream_t stream) {
   const int units = L * 2 * H;
   const int blocks = (units + kWarps - 1) / kWarps;
-  kv_compact_kernel<<<blocks, kWarps * 32, 0, stream>>>(reinterpret_cast<uint2*>(kv), units, S_max, D / 4, d_prefix,
-                                                        prefix, d_res, d_cur_len, mv_error_word());
+  if (mv_launch(kv_compact_kernel, dim3(blocks), dim3(kWarps * 32), 0, stream, reinterpret_cast<uint2*>(kv), units,
+                S_max, D / 4, d_prefix, prefix, d_res, d_cur_len, mv_error_word()) != cudaSuccess)
+    return MV_ERR_CUDA;
   return mv_last_launch("kv_compact");
 }
 

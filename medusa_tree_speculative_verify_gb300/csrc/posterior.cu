@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
     mv_posterior_result* __restrict__ out, float* __restrict__ node_stats_out, int32_t* __restrict__ node_argmax_out,
     float* __restrict__ ws_stats, int32_t* __restrict__ ws_argmax, unsigned int* __restrict__ ticket,
     unsigned int* err) {
+  pdl_trigger();
+  pdl_wait();
   const bool typical = prm.mode == MV_TYPICAL;
   const float inv_t = typical ? 1.0f / prm.temperature : 1.0f;
   const int node = blockIdx.x;
@@ -221,9 +223,10 @@ mv_status launch_posterior(const float* logits, int V, int ld, const int32_t* d_
   unsigned int* ticket = reinterpret_cast<unsigned int*>(w);
   float* ws_stats = reinterpret_cast<float*>(w + 64);
   int32_t* ws_arg = reinterpret_cast<int32_t*>(w + 64 + (size_t)t->n_nodes * 4 * sizeof(float));
-  posterior_kernel<<<t->n_nodes, kThreads, 0, stream>>>(logits, V, ld, d_tree_tokens, t->d_retrieve, t->n_nodes,
-                                                        t->n_paths, t->depth + 1, prm, d_out, d_stats, d_argmax,
-                                                        ws_stats, ws_arg, ticket, mv_error_word());
+  if (mv_launch(posterior_kernel, dim3(t->n_nodes), dim3(kThreads), 0, stream, logits, V, ld, d_tree_tokens,
+                t->d_retrieve, t->n_nodes, t->n_paths, t->depth + 1, prm, d_out, d_stats, d_argmax, ws_stats, ws_arg,
+                ticket, mv_error_word()) != cudaSuccess)
+    return MV_ERR_CUDA;
   return mv_last_launch("evaluate_posterior");
 }
 
@@ -246,3 +249,4 @@ extern "C" mv_status evaluate_posterior(const float* logits, int32_t V, int32_t 
   return launch_posterior(logits, V, ld, d_tree_tokens, tree, params, d_out, d_node_stats, d_node_argmax,
                           workspace, static_cast<cudaStream_t>(stream));
 }
+

@@ -1,6 +1,7 @@
 // Library runtime: the device error word, status strings, SM count, tensor-map encoding.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -33,6 +34,14 @@ int mv_sm_count() {
     cached[dev] = n > 0 ? n : 148;
   }
   return cached[dev];
+}
+
+bool mv_pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("MV_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
 }
 
 int mv_device() {

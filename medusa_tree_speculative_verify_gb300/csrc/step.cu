@@ -26,6 +26,8 @@ constexpr int kTok = 64;  // token columns of every activation buffer
 __global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ tokens, const uint16_t* __restrict__ E,
                                                     int vocab, int d, float* __restrict__ x, uint16_t* __restrict__ xb,
                                                     float* __restrict__ ssq, unsigned int* err) {
+  pdl_trigger();
+  pdl_wait();
   const int j = blockIdx.x;
   const int tok = tokens[j];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -54,6 +56,8 @@ __global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ 
 __global__ void __launch_bounds__(1024) prefill_finish_kernel(const float* __restrict__ logits, int V, int ld, int c,
                                                              int last, int32_t* cur_len,
                                                              mv_posterior_result* res) {
+  pdl_trigger();
+  pdl_wait();
   if (!last) {
     if (threadIdx.x == 0) *cur_len += c;
     return;
@@ -98,7 +102,11 @@ __global__ void __launch_bounds__(1024) prefill_finish_kernel(const float* __res
   }
 }
 
-__global__ void set_int_kernel(int32_t* p, int v) { *p = v; }
+__global__ void set_int_kernel(int32_t* p, int v) {
+  pdl_trigger();
+  pdl_wait();
+  *p = v;
+}
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -246,8 +254,10 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
   mv_status rc;
   {
     ProfScope ps(s, st, MV_PROF_OTHER);
-    embed_kernel<<<n, 256, 0, st>>>(d_tokens, m->embed, d.vocab, d.d, s->x, s->xb, s->ssq, mv_error_word());
-    rc = mv_last_launch("embed");
+    rc = mv_launch(embed_kernel, dim3(n), dim3(256), 0, st, d_tokens, m->embed, d.vocab, d.d, s->x, s->xb, s->ssq,
+                   mv_error_word()) == cudaSuccess
+             ? mv_last_launch("embed")
+             : MV_ERR_CUDA;
   }
   for (int l = 0; l < d.n_layers && rc == MV_OK; ++l) {
     {  // QKV + RoPE + KV append
@@ -502,16 +512,18 @@ extern "C" mv_status mv_prefill(mv_session* s, const int32_t* d_tokens, int32_t 
   if (!s || !d_tokens || n < 1) return MV_ERR_INVALID_ARG;
   if (n + kTok > s->s_max) return MV_ERR_CAPACITY;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  set_int_kernel<<<1, 1, 0, st>>>(s->cur_len, 0);
-  mv_status rc = mv_last_launch("prefill");
+  mv_status rc = mv_launch(set_int_kernel, dim3(1), dim3(1), 0, st, s->cur_len, 0) == cudaSuccess
+                     ? mv_last_launch("prefill")
+                     : MV_ERR_CUDA;
   for (int o = 0; o < n && rc == MV_OK; o += kTok) {
     const int c = std::min(kTok, n - o);
     const bool last = o + c == n;
     rc = forward(s, s->chain, d_tokens + o, c, last, st);
     if (rc != MV_OK) break;
-    prefill_finish_kernel<<<1, 1024, 0, st>>>(s->logits, s->model->dims.vocab, s->ld_logits, c, last ? 1 : 0,
-                                              s->cur_len, s->result);
-    rc = mv_last_launch("prefill_finish");
+    rc = mv_launch(prefill_finish_kernel, dim3(1), dim3(1024), 0, st, s->logits, s->model->dims.vocab,
+                   s->ld_logits, c, last ? 1 : 0, s->cur_len, s->result) == cudaSuccess
+             ? mv_last_launch("prefill_finish")
+             : MV_ERR_CUDA;
   }
   if (rc == MV_OK) rc = run_heads(s, st);
   return rc;
