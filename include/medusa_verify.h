@@ -165,6 +165,20 @@ mv_status evaluate_posterior(const float* logits, int32_t V, int32_t ld, const i
                              float* d_node_stats, int32_t* d_node_argmax, void* workspace, size_t ws_bytes,
                              mv_stream stream);
 
+/* evaluate_posterior without a workspace. The paper has no counterpart: this entry point exists for callers
+ * that cannot call cudaMalloc -- code running under another runtime's memory manager that owns every device
+ * allocation, or a serving loop that must not touch the device allocator after start-up. It computes exactly
+ * what evaluate_posterior computes (same arguments minus the workspace). Its scratch is a fixed 2048-byte
+ * __device__ array inside the library (every GPU that loads the library holds it until the process exits),
+ * enough for MV_MAX_NODES = 64 tree nodes; a larger tree is rejected with MV_ERR_CAPACITY. The first call on
+ * a device looks up that array's device address (cudaGetSymbolAddress) with the device current; make that
+ * first call before any stream capture. Each call clears the array's completion counter on `stream` before
+ * its kernel. All calls share the one array, so calls that overlap on the GPU (other streams, other threads)
+ * race: order them. Never allocates. */
+mv_status evaluate_posterior_noalloc(const float* logits, int32_t V, int32_t ld, const int32_t* d_tree_tokens,
+                                     const mv_tree* tree, mv_accept_params params, mv_posterior_result* d_out,
+                                     float* d_node_stats, int32_t* d_node_argmax, mv_stream stream);
+
 /* ============================================================================================
  * KV compaction  [M5 二.7 update_inference_inputs()]
  * ============================================================================================

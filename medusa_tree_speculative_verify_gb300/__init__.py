@@ -73,6 +73,7 @@ _SIGS = {
     "evaluate_posterior_workspace": ([_I, ctypes.POINTER(_S)], _I),
     "evaluate_posterior": ([_P, _I, _I, _P, _P, AcceptParams, _P, _P, _P, _P, _S, _P], _I),
     "kv_compact": ([_P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
+    "evaluate_posterior_noalloc": ([_P, _I, _I, _P, _P, AcceptParams, _P, _P, _P, _P], _I),
     "mv_linear_bf16_workspace": ([ctypes.POINTER(_S)], _I),
     "mv_linear_bf16": ([_P, _P, _P, _I, _I, _I, _I, _P, _S, _P], _I),
     "mv_model_create": ([_P, _P, ctypes.POINTER(_P)], _I),
@@ -210,6 +211,15 @@ def evaluate_posterior(logits, tree_tokens, tree: Tree, params: AcceptParams, ou
                                     _ptr(node_stats), _ptr(node_argmax), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream)),
            "evaluate_posterior")
+
+
+def evaluate_posterior_noalloc(logits, tree_tokens, tree: Tree, params: AcceptParams, out, node_stats=None,
+                               node_argmax=None, stream=None):
+    """evaluate_posterior with the library's fixed scratch array instead of a workspace (allocates nothing)."""
+    n, V = logits.shape
+    _check(lib().evaluate_posterior_noalloc(_ptr(logits), V, logits.stride(0), _ptr(tree_tokens), tree.handle,
+                                            params, _ptr(out), _ptr(node_stats), _ptr(node_argmax), _stream(stream)),
+           "evaluate_posterior_noalloc")
 
 
 def kv_compact(kv, prefix_len, result, cur_len=None, stream=None):

@@ -10,6 +10,8 @@
 // walks the paths and writes the result.
 #include <float.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -250,3 +252,53 @@ extern "C" mv_status evaluate_posterior(const float* logits, int32_t V, int32_t 
                           workspace, static_cast<cudaStream_t>(stream));
 }
 
+// ------------------------------------------------------------------------------------------------------------
+// Allocation-free variant. Some callers cannot call cudaMalloc: code that runs inside another runtime's memory
+// manager (which owns every device allocation and forbids raw ones), or a serving loop that must not touch the
+// device allocator once it is running (cudaMalloc may synchronise the device and serialises on a global lock).
+// They get the same posterior with its scratch in a fixed array that is part of the library's device image:
+// every GPU that loads the library holds these bytes until the process exits.
+// ------------------------------------------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 2048;  // >= posterior_ws_bytes(MV_MAX_NODES) = 64 * 20 + 64 = 1344
+static __device__ __align__(256) unsigned char g_posterior_scratch[kNoAllocScratchBytes];
+
+// Device address of g_posterior_scratch on the current device, looked up once per device with that device
+// current. In host code the symbol's name is only a host-side stand-in, so the address must come from
+// cudaGetSymbolAddress; it is then passed to the kernel like any workspace pointer.
+void* noalloc_scratch() {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_posterior_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" mv_status evaluate_posterior_noalloc(const float* logits, int32_t V, int32_t ld,
+                                                const int32_t* d_tree_tokens, const mv_tree* tree,
+                                                mv_accept_params params, mv_posterior_result* d_out,
+                                                float* d_node_stats, int32_t* d_node_argmax, mv_stream stream) {
+  if (!logits || !d_tree_tokens || !tree || !d_out) return MV_ERR_INVALID_ARG;
+  if (!tree->d_retrieve) return MV_ERR_CUDA;
+  if (V < 2 || ld < V || (ld & 3) || (reinterpret_cast<uintptr_t>(logits) & 15)) return MV_ERR_SHAPE;
+  if (params.mode != MV_GREEDY && params.mode != MV_TYPICAL) return MV_ERR_INVALID_ARG;
+  if (params.mode == MV_TYPICAL && !(params.temperature > 0.0f)) return MV_ERR_INVALID_ARG;
+  if (tree->n_nodes > MV_MAX_NODES || posterior_ws_bytes(tree->n_nodes) > kNoAllocScratchBytes)
+    return MV_ERR_CAPACITY;  // more nodes than the fixed scratch array holds
+  void* scratch = noalloc_scratch();
+  if (!scratch) return MV_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The array keeps whatever the last call left; the completion counter at its start must begin at zero.
+  if (cudaMemsetAsync(scratch, 0, 64, st) != cudaSuccess) return MV_ERR_CUDA;
+  return launch_posterior(logits, V, ld, d_tree_tokens, tree, params, d_out, d_node_stats, d_node_argmax, scratch,
+                          st);
+}
