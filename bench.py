@@ -182,7 +182,7 @@ def run_gpu(args, world, rank, local):
     import medusa_tree_speculative_verify_gb300 as mv
     torch.cuda.set_device(local)
     dims = synth.LLAMA7B
-    w = synth.packed_weights(dims, 0, torch.bfloat16, "cuda")
+    w = mv.pack_model_weights(synth.packed_weights(dims, 0, torch.bfloat16, "cuda"), drop_source=True)
     model = mv.Model(dims, w)
     tree = mv.Tree(synth.synthetic_tree_choices(TREE["n_nodes"], TREE["depth"], TREE["topk"]), TREE["topk"])
     n_steps_total = args.warmup + 5 * args.steps + 8
@@ -311,6 +311,85 @@ MICRO = {  # name -> (M, K, n): projections of the 7B step, timed alone through 
     "lm_head": (32000, 4096, 64), "gate_up": (22016, 4096, 64), "down": (4096, 11008, 64),
     "qkv": (12288, 4096, 64), "o": (4096, 4096, 64),
 }
+MICRO_OTHER = ["heads_b1", "heads_b4", "heads_b16", "attn_p64", "attn_p512", "attn_p1024", "attn_p4096",
+               "posterior_greedy", "posterior_typical", "kv_compact_acc4"]
+
+
+def _time_launches(fn, steps, warmup, flush=True):
+    """Median CUDA-event time (ms) of fn() on the current stream, L2 flushed (256 MB write) before each."""
+    buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush else None
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(steps):
+        if buf is not None:
+            buf.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.median(times)
+
+
+def run_micro_other(name, steps, warmup):
+    """One standalone kernel of the path at the sizes of its workload; GB/s of its algorithmic bytes."""
+    import medusa_tree_speculative_verify_gb300 as mv
+    peak, kind = peaks()
+    ws = lambda n: torch.zeros(max(n, 16), dtype=torch.uint8, device="cuda")
+    tree = mv.Tree(synth.synthetic_tree_choices(64, 4, 10), 10)
+    if name.startswith("heads_b"):
+        B, d, K, V = int(name[7:]), 4096, 4, 32000
+        w1 = synth.normal(0, "w1", (K, d, d), 0.02, dtype=torch.bfloat16, device="cuda")
+        w2 = synth.normal(0, "w2", (K, V, d), 0.02, dtype=torch.bfloat16, device="cuda")
+        wl = synth.normal(0, "lm", (V, d), 0.02, dtype=torch.bfloat16, device="cuda")
+        h = synth.normal(0, "h", (B, d), 1.0, dtype=torch.bfloat16, device="cuda")
+        oi = torch.empty(B, K, 10, dtype=torch.int32, device="cuda")
+        ov = torch.empty(B, K, 10, dtype=torch.float32, device="cuda")
+        root = torch.empty(B, dtype=torch.int32, device="cuda")
+        w = ws(mv.medusa_heads_topk_workspace(B, d, K, V, 10))
+        fn = lambda: mv.medusa_heads_topk(h, w1, w2, 10, oi, ov, w_lm=wl, out_root=root, workspace=w)
+        nbytes = 2 * (K * d * d + K * V * d + V * d) + 2 * B * d
+    elif name.startswith("attn_p"):
+        P, H, D = int(name[6:]), 32, 128
+        n = tree.n_nodes
+        q = synth.normal(0, "q", (n, H, D), dtype=torch.bfloat16, device="cuda")
+        k = synth.normal(0, "k", (H, P + n, D), dtype=torch.bfloat16, device="cuda")
+        v = synth.normal(0, "v", (H, P + n, D), dtype=torch.bfloat16, device="cuda")
+        out = torch.empty_like(q)
+        w = ws(mv.tree_attention_workspace(H, D, P + n, n))
+        fn = lambda: mv.tree_attention(q, k, v, P, tree, D ** -0.5, out, w)
+        nbytes = (P + n) * H * D * 2 * 2 + 2 * n * H * D * 2
+    elif name.startswith("posterior"):
+        mode = mv.TYPICAL if name.endswith("typical") else mv.GREEDY
+        path = [int(x) for x in tree.retrieve[0] if x >= 0]
+        toks, logits = synth.planted_tokens_and_logits(0, tree.n_nodes, 32000, path, len(path) - 1)
+        logits, toks = logits.cuda(), torch.as_tensor(toks, dtype=torch.int32, device="cuda")
+        out = torch.empty(mv.RESULT_INTS, dtype=torch.int32, device="cuda")
+        w = ws(mv.evaluate_posterior_workspace(tree.n_nodes))
+        prm = mv.AcceptParams(mode, 0.7, 0.09, 0.3)
+        fn = lambda: mv.evaluate_posterior(logits, toks, tree, prm, out, w)
+        nbytes = tree.n_nodes * 32000 * 4
+    else:  # kv_compact_acc4: 32 layers x 32 heads x 128, prefix 1024, path of 5 nodes
+        kv = synth.kv_cache(0, (32, 2, 32, 1088, 128), device="cuda")
+        r = mv.PosteriorResult()
+        r.acc, r.n_tokens = 4, 5
+        for j, nd in enumerate([0, 1, 11, 34, 57]):
+            r.nodes[j] = nd
+        res = torch.tensor(np.frombuffer(bytes(r), dtype=np.int32).copy(), device="cuda")
+        cur = torch.zeros(1, dtype=torch.int32, device="cuda")
+        fn = lambda: mv.kv_compact(kv, 1024, res, cur)
+        nbytes = 2 * 5 * 32 * 2 * 32 * 128 * 2
+    ms = _time_launches(fn, steps, warmup)
+    st, code = mv.get_error()
+    if st != 0:
+        raise RuntimeError(f"device error word {code:#x}")
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"micro": name, "median_us": ms * 1e3, "algorithmic_bytes": nbytes, "gbs": gbs, "frac": gbs / peak,
+            "peak": peak, "peak_kind": kind, "l2": "flushed"}
 
 
 def run_micro(name, steps, warmup):
@@ -318,28 +397,18 @@ def run_micro(name, steps, warmup):
     import medusa_tree_speculative_verify_gb300 as mv
     M, K, n = MICRO[name]
     w = synth.normal(1, "w", (M, K), 0.02, dtype=torch.bfloat16, device="cuda")
+    wp = mv.pack_weight(w, 128)
     x = synth.normal(2, "x", (n, K), 1.0, dtype=torch.bfloat16, device="cuda")
     out = torch.empty(n, M, dtype=torch.float32, device="cuda")
     ws = torch.zeros(mv.linear_bf16_workspace(), dtype=torch.uint8, device="cuda")
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")  # 256 MB > L2, written between launches
-    for _ in range(warmup):
-        mv.linear_bf16(w, x, out, ws)
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    times = []
-    for _ in range(steps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        mv.linear_bf16(w, x, out, ws)
-        b.record(stream)
-        torch.cuda.synchronize()
-        times.append(a.elapsed_time(b))
-    ms = statistics.median(times)
     nbytes = 2 * M * K + 2 * n * K + 4 * n * M
     peak, kind = peaks()
-    return {"micro": name, "M": M, "K": K, "n": n, "median_us": ms * 1e3, "gbs": nbytes / (ms / 1e3) / 1e9,
-            "frac": nbytes / (ms / 1e3) / 1e9 / peak, "peak": peak, "peak_kind": kind, "l2": "flushed"}
+    ms_packed = _time_launches(lambda: mv.linear_bf16_packed(wp, M, K, x, out, ws), steps, warmup)
+    ms_rowmajor = _time_launches(lambda: mv.linear_bf16(w, x, out, ws), steps, warmup)
+    gbs = nbytes / (ms_packed / 1e3) / 1e9
+    return {"micro": name, "M": M, "K": K, "n": n, "median_us": ms_packed * 1e3, "gbs": gbs, "frac": gbs / peak,
+            "rowmajor_us": ms_rowmajor * 1e3, "rowmajor_gbs": nbytes / (ms_rowmajor / 1e3) / 1e9,
+            "peak": peak, "peak_kind": kind, "l2": "flushed", "layout": "packed"}
 
 
 def weight_bytes(dims):
@@ -355,11 +424,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--micro", choices=sorted(MICRO), help="time one projection shape alone and exit")
+    ap.add_argument("--micro", choices=sorted(MICRO) + MICRO_OTHER, help="time one kernel alone and exit")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.micro:
-        print(json.dumps(run_micro(args.micro, args.steps, args.warmup)))
+        fn = run_micro if args.micro in MICRO else run_micro_other
+        print(json.dumps(fn(args.micro, args.steps, args.warmup)))
         return
 
     if args.impl == "reference":

@@ -202,6 +202,9 @@ mv_status kv_compact(mv_bf16* kv, int32_t L, int32_t H, int32_t S_max, int32_t D
 mv_status mv_linear_bf16_workspace(size_t* bytes);
 mv_status mv_linear_bf16(const mv_bf16* w, const mv_bf16* x, float* out, int32_t M, int32_t K, int32_t n,
                          int32_t ld_out, void* workspace, size_t ws_bytes, mv_stream stream);
+/* The same with w_packed = mv_pack_weight(w, tile_rows = 128). */
+mv_status mv_linear_bf16_packed(const mv_bf16* w_packed, const mv_bf16* x, float* out, int32_t M, int32_t K,
+                                int32_t n, int32_t ld_out, void* workspace, size_t ws_bytes, mv_stream stream);
 
 /* ============================================================================================
  * Model, decode session, verify step  [M5 二.1 medusa_generate(), 二.3 - 二.7]
@@ -228,7 +231,17 @@ typedef struct mv_model_weights {
   const mv_bf16* lm_head;           /* [vocab][d] */
   const mv_bf16* medusa_w1;         /* [n_medusa][d][d] */
   const mv_bf16* medusa_w2;         /* [n_medusa][vocab][d] */
+  int32_t packed;                   /* 0: every matrix row-major as above. 1: wqkv, wo, w_down, lm_head in the
+                                       packed layout of mv_pack_weight with tile_rows 128, w_gate and w_up with
+                                       tile_rows 64 (embed and the Medusa matrices stay row-major) */
 } mv_model_weights;
+
+/* Packed weight layout for the projection kernel: dst[tm][kb][r][c] = src[tm*tile_rows + r][kb*64 + c]
+ * (zero where out of range), tile_rows in {64, 128}. Each (tile_rows x 64) block the kernel loads is then one
+ * contiguous run of memory. src device bf16 [M][K]; dst device bf16 of mv_packed_weight_bytes() bytes.
+ * Asynchronous on `stream`. */
+mv_status mv_packed_weight_bytes(int32_t M, int32_t K, int32_t tile_rows, size_t* bytes);
+mv_status mv_pack_weight(const mv_bf16* src, mv_bf16* dst, int32_t M, int32_t K, int32_t tile_rows, mv_stream stream);
 
 typedef struct mv_model mv_model;
 typedef struct mv_session mv_session;

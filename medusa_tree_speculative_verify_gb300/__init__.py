@@ -76,6 +76,9 @@ _SIGS = {
     "evaluate_posterior_noalloc": ([_P, _I, _I, _P, _P, AcceptParams, _P, _P, _P, _P], _I),
     "mv_linear_bf16_workspace": ([ctypes.POINTER(_S)], _I),
     "mv_linear_bf16": ([_P, _P, _P, _I, _I, _I, _I, _P, _S, _P], _I),
+    "mv_linear_bf16_packed": ([_P, _P, _P, _I, _I, _I, _I, _P, _S, _P], _I),
+    "mv_packed_weight_bytes": ([_I, _I, _I, ctypes.POINTER(_S)], _I),
+    "mv_pack_weight": ([_P, _P, _I, _I, _I, _P], _I),
     "mv_model_create": ([_P, _P, ctypes.POINTER(_P)], _I),
     "mv_model_destroy": ([_P], None),
     "mv_session_workspace": ([_P, _I, _I, ctypes.POINTER(_S)], _I),
@@ -259,6 +262,39 @@ def linear_bf16(w, x, out, workspace, stream=None):
                                 workspace.numel() * workspace.element_size(), _stream(stream)), "mv_linear_bf16")
 
 
+def linear_bf16_packed(w_packed, M, K, x, out, workspace, stream=None):
+    """linear_bf16 with the weight in the packed layout (pack_weight(w, 128))."""
+    n = x.shape[0]
+    _check(lib().mv_linear_bf16_packed(_ptr(w_packed), _ptr(x), _ptr(out), M, K, n, out.stride(0), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)),
+           "mv_linear_bf16_packed")
+
+
+def pack_weight(w, tile_rows, stream=None):
+    """A new bf16 tensor with w [M, K] in the projection kernel's packed layout (see mv_pack_weight)."""
+    import torch
+    M, K = w.shape
+    nbytes = _ws_size(lib().mv_packed_weight_bytes, M, K, tile_rows)
+    out = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=w.device)
+    _check(lib().mv_pack_weight(_ptr(w), _ptr(out), M, K, tile_rows, _stream(stream)), "mv_pack_weight")
+    return out
+
+
+def pack_model_weights(w, drop_source=False):
+    """Model weights with the projection matrices packed (embed and the Medusa matrices unchanged)."""
+    out = dict(w)
+    for key, tr in (("wqkv", 128), ("wo", 128), ("w_gate", 64), ("w_up", 64), ("w_down", 128)):
+        packed = []
+        for i in range(len(w[key])):
+            packed.append(pack_weight(w[key][i], tr))
+            if drop_source:
+                w[key][i] = None
+        out[key] = packed
+    out["lm_head"] = pack_weight(w["lm_head"], 128)
+    out["packed"] = True
+    return out
+
+
 # --------------------------------------------------------------------------------------------- model / session
 
 class ModelDims(ctypes.Structure):
@@ -268,7 +304,7 @@ class ModelDims(ctypes.Structure):
 
 class _Weights(ctypes.Structure):
     _fields_ = [("embed", _P), ("wqkv", _P), ("wo", _P), ("w_gate", _P), ("w_up", _P), ("w_down", _P),
-                ("lm_head", _P), ("medusa_w1", _P), ("medusa_w2", _P)]
+                ("lm_head", _P), ("medusa_w1", _P), ("medusa_w2", _P), ("packed", _I)]
 
 
 class _StatePtrs(ctypes.Structure):
@@ -293,7 +329,8 @@ class Model:
         self._arrs = arrs
         cw = _Weights(w["embed"].data_ptr(), ctypes.cast(arrs["wqkv"], _P), ctypes.cast(arrs["wo"], _P),
                       ctypes.cast(arrs["w_gate"], _P), ctypes.cast(arrs["w_up"], _P), ctypes.cast(arrs["w_down"], _P),
-                      w["lm_head"].data_ptr(), w["medusa_w1"].data_ptr(), w["medusa_w2"].data_ptr())
+                      w["lm_head"].data_ptr(), w["medusa_w1"].data_ptr(), w["medusa_w2"].data_ptr(),
+                      1 if w.get("packed") else 0)
         h = ctypes.c_void_p()
         _check(lib().mv_model_create(ctypes.byref(self.dims), ctypes.byref(cw), ctypes.byref(h)), "mv_model_create")
         self.handle = h

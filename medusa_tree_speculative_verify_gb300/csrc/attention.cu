@@ -97,8 +97,12 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
     return;
   }
   const int total_tiles = (P + n + kKeys - 1) / kKeys;
-  const int t_begin = (int)((long long)split * total_tiles / a.splits);
-  const int t_end = (int)((long long)(split + 1) * total_tiles / a.splits);
+  // The grid is sized for the longest prefix; at this prefix only `splits` CTAs per head get tiles, the
+  // others leave at once and the merge reads only the real partials.
+  const int splits = min(a.splits, total_tiles);
+  if (split >= splits) return;
+  const int t_begin = (int)((long long)split * total_tiles / splits);
+  const int t_end = (int)((long long)(split + 1) * total_tiles / splits);
   const int count = t_end - t_begin;
 
   if (tid == 0) {
@@ -254,7 +258,7 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-  if (a.splits == 1) {
+  if (splits == 1) {
     const float i0 = l0 > 0.0f ? 1.0f / l0 : 0.0f, i1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
 #pragma unroll
     for (int dn = 0; dn < DN; ++dn) {
@@ -286,18 +290,18 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.tickets + h, 1u) == (unsigned)(a.splits - 1);
+  if (tid == 0) s_last = atomicAdd(a.tickets + h, 1u) == (unsigned)(splits - 1);
   __syncthreads();
   if (!s_last) return;
   __threadfence();
   for (int e = tid; e < n * (D / 4); e += kThreads) {
     const int q = e / (D / 4), c4 = (e % (D / 4)) * 4;
     float M = -INFINITY;
-    for (int sp = 0; sp < a.splits; ++sp)
+    for (int sp = 0; sp < splits; ++sp)
       M = fmaxf(M, __ldcg(a.ml + (((size_t)h * a.splits + sp) * kRows + q) * 2));
     const float base = M == -INFINITY ? 0.0f : M;
     float L = 0.0f, acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int sp = 0; sp < a.splits; ++sp) {
+    for (int sp = 0; sp < splits; ++sp) {
       const float* mlp = a.ml + (((size_t)h * a.splits + sp) * kRows + q) * 2;
       const float w = exp2f(__ldcg(mlp) - base);
       L += w * __ldcg(mlp + 1);

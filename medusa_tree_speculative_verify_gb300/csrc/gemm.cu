@@ -144,22 +144,42 @@ MV_DEV float* partial_slot(int c, int tile, const GemmParams& p) {
 
 // ---------------------------------------------------------------------------------------------- epilogues
 // Per-token RMSNorm scale from the sum-of-squares partials (one per 128-row slice of the hidden state).
-MV_DEV void compute_scales(const GemmParams& p, float* s_scale, int i) {
-  if (i < BN) {
-    float s = 1.0f;
-    if (p.ssq) {
-      float t = 0.0f;
-      for (int q = 0; q < p.ssq_parts; ++q) t += p.ssq[q * BN + i];
-      s = rsqrtf(t / (float)p.norm_d + p.eps);
+// Per-CTA constants of the epilogue, loaded once (after the previous kernel finished) into shared memory:
+// the per-token RMSNorm scale s[j] = 1/sqrt(sum of the sum-of-squares partials / norm_d + eps) (1 without a
+// norm), and for the QKV epilogue the token positions prefix + depth. The 128 epilogue threads split the
+// partial sums so the loads are independent and in flight together.
+struct EpiConst {
+  float scale[BN];
+  int pos[BN];
+  float part[2][BN];
+  int kv_row0;
+};
+
+MV_DEV void load_epi_const(const GemmParams& p, EpiConst* ec, int i) {
+  const int j = i & (BN - 1), half = i >> 6;  // two threads per token, each summing half of the partials
+  float t = 0.0f;
+  if (p.ssq) {
+    const int q0 = half * ((p.ssq_parts + 1) / 2), q1 = min(p.ssq_parts, q0 + (p.ssq_parts + 1) / 2);
+    float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+    int q = q0;
+    for (; q + 8 <= q1; q += 8) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u] += __ldcg(p.ssq + (q + u) * BN + j);
     }
-    s_scale[i] = s;
+    for (; q < q1; ++q) acc[0] += __ldcg(p.ssq + q * BN + j);
+    t = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
   }
+  ec->part[half][j] = t;
+  if (half == 0 && p.pos_ids) ec->pos[j] = j < p.n_tok ? *p.cur_len + p.pos_ids[j] : 0;
+  if (i == 0) ec->kv_row0 = p.cur_len ? *p.cur_len : 0;
+  epi_bar();
+  if (half == 0) ec->scale[j] = p.ssq ? rsqrtf((ec->part[0][j] + ec->part[1][j]) / (float)p.norm_d + p.eps) : 1.0f;
+  epi_bar();
 }
 
 template <int EPI>
-MV_DEV void final_epilogue(const GemmParams& p, int tile, int i, float (&v)[BN], float* stg, float* s_scale) {
-  compute_scales(p, s_scale, i);
-  epi_bar();
+MV_DEV void final_epilogue(const GemmParams& p, int tile, int i, float (&v)[BN], float* stg, const EpiConst* ec) {
+  const float* s_scale = ec->scale;
   const int ntok = p.n_tok;
   const bool lo = i < 64;
   float* my = stg + (i & 63) * kPitch;  // staging row shared by rows i and i^64, one round each
@@ -173,11 +193,13 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int i, float (&v)[BN],
   } else if constexpr (EPI == EPI_RESIDUAL) {
     const int R = tile * BM + i;
     const bool ok = R < p.M;
+    // all residual loads first (independent, in flight together), then the adds and stores
+#pragma unroll
+    for (int j = 0; j < BN; ++j) v[j] += (ok && j < ntok) ? __ldcg(p.x + (size_t)j * p.M + R) : 0.0f;
 #pragma unroll
     for (int j = 0; j < BN; ++j) {
-      float xn = 0.0f;
+      const float xn = (ok && j < ntok) ? v[j] : 0.0f;
       if (ok && j < ntok) {
-        xn = p.x[(size_t)j * p.M + R] + v[j];
         p.x[(size_t)j * p.M + R] = xn;
         p.xb[(size_t)j * p.M + R] = __bfloat16_as_ushort(__float2bfloat16_rn(xn));
       }
@@ -224,7 +246,7 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int i, float (&v)[BN],
     const int HD = p.H * p.D;
     const int which = R / HD, within = R % HD, head = within / p.D, dim = within % p.D;
     const int half = p.D >> 1;
-    const int prefix = *p.cur_len;
+    const int kv_row0 = ec->kv_row0;  // prefix length: the tree block's keys/values go to rows kv_row0 + j
     const int pi = dim < half ? i + half : i - half;  // RoPE partner row (same head, same tile)
     const float inv_freq = exp2f(-(float)(2 * (dim % half)) / (float)p.D * p.log2_theta);
     for (int round = 0; round < 2; ++round) {
@@ -242,7 +264,7 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int i, float (&v)[BN],
           if (which < 2) {
             const float pv = pr[j];
             float sn, cs;
-            sincosf((float)(prefix + p.pos_ids[j]) * inv_freq, &sn, &cs);
+            sincosf((float)ec->pos[j] * inv_freq, &sn, &cs);
             val = dim < half ? val * cs - pv * sn : val * cs + pv * sn;
           }
           const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(val));
@@ -250,7 +272,7 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int i, float (&v)[BN],
             p.q_out[((size_t)j * p.H + head) * p.D + dim] = b;
           } else {
             const size_t plane = (size_t)p.layer * 2 + (which - 1);
-            p.kv[((plane * p.H + head) * p.S_max + prefix + j) * p.D + dim] = b;
+            p.kv[((plane * p.H + head) * p.S_max + kv_row0 + j) * p.D + dim] = b;
           }
         }
       }
@@ -272,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int s_abort;
-  __shared__ float s_scale[BN];
+  __shared__ EpiConst s_ec;
   __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -329,7 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           }
           uint8_t* a = stages + (size_t)s * kStageBytes;
           mbar_arrive_expect_tx(&full[s], kStageBytes);
-          if (p.paired) {
+          if (p.packed_a) {  // one contiguous block per matrix
+            const int tb = sg.tile * p.kbt + kb;
+            tma_load_3d(a, &amap0, &full[s], 0, 0, tb);
+            if (p.paired) tma_load_3d(a + kABytes / 2, &amap1, &full[s], 0, 0, tb);
+          } else if (p.paired) {
             tma_load_2d(a, &amap0, &full[s], kb * BK, sg.tile * 64);
             tma_load_2d(a + kABytes / 2, &amap1, &full[s], kb * BK, sg.tile * 64);
           } else {
@@ -396,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int sub = warp & 3;           // TMEM sub-partition this warp may read
     const int i = sub * 32 + lane;      // tile row = TMEM lane
     pdl_wait();                         // the epilogue reads what earlier kernels wrote
+    load_epi_const(p, &s_ec, i);        // scales and positions: the same for every tile of this launch
     Seg sg;
     for (int si = 0; get_seg(cta, si, p, sg); ++si) {
       const int buf = si & 1, rr = si >> 1;
@@ -441,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
         if (i == 0) p.tickets[sg.tile] = 0u;
       }
-      final_epilogue<EPI>(p, sg.tile, i, v, stg, s_scale);
+      final_epilogue<EPI>(p, sg.tile, i, v, stg, &s_ec);
     }
   }
 
@@ -478,6 +505,15 @@ bool gemm_weight_map(CUtensorMap* map, const void* w, int rows, int K, int box_r
   const uint64_t strides[1] = {(uint64_t)K * 2};
   const uint32_t box[2] = {(uint32_t)BK, (uint32_t)box_rows};
   return mv_encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool gemm_weight_map_packed(CUtensorMap* map, const void* w, int rows, int K, int tile_rows) {
+  const uint64_t n_blocks = (uint64_t)((rows + tile_rows - 1) / tile_rows) * ((K + BK - 1) / BK);
+  const uint64_t dims[3] = {(uint64_t)BK, (uint64_t)tile_rows, n_blocks};
+  const uint64_t strides[2] = {(uint64_t)BK * 2, (uint64_t)tile_rows * BK * 2};
+  const uint32_t box[3] = {(uint32_t)BK, (uint32_t)tile_rows, 1};
+  return mv_encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, strides, box,
                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -533,6 +569,29 @@ extern "C" mv_status mv_linear_bf16(const mv_bf16* w, const mv_bf16* x, float* o
   p.M = M;
   p.K = K;
   p.n_tok = n;
+  p.out_f32 = out;
+  p.ld_out = ld_out;
+  p.err = mv_error_word();
+  gemm_ws_layout(workspace, &p.partials, &p.tickets);
+  gemm_finish_params(p);
+  return launch_gemm(EPI_STORE, a, a, b, p, static_cast<cudaStream_t>(stream));
+}
+
+// The same projection with w in the packed layout (mv_pack_weight with tile_rows = 128).
+extern "C" mv_status mv_linear_bf16_packed(const mv_bf16* w_packed, const mv_bf16* x, float* out, int32_t M,
+                                           int32_t K, int32_t n, int32_t ld_out, void* workspace, size_t ws_bytes,
+                                           mv_stream stream) {
+  if (!w_packed || !x || !out || !workspace) return MV_ERR_INVALID_ARG;
+  if (M < 1 || K < 8 || (K & 7) || n < 1 || n > BN || ld_out < M) return MV_ERR_SHAPE;
+  if (ws_bytes < gemm_ws_bytes()) return MV_ERR_CAPACITY;
+  if ((reinterpret_cast<uintptr_t>(w_packed) | reinterpret_cast<uintptr_t>(x)) & 15) return MV_ERR_SHAPE;
+  CUtensorMap a, b;
+  if (!gemm_weight_map_packed(&a, w_packed, M, K, BM) || !gemm_act_map(&b, x, n, K)) return MV_ERR_CUDA;
+  GemmParams p{};
+  p.M = M;
+  p.K = K;
+  p.n_tok = n;
+  p.packed_a = 1;
   p.out_f32 = out;
   p.ld_out = ld_out;
   p.err = mv_error_word();

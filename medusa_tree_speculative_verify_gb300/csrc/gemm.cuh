@@ -11,6 +11,7 @@ struct GemmParams {
   int K;         // reduction length
   int n_tok;     // valid token columns (1..64)
   int paired;    // SWIGLU: tile = 64 rows of amap0 (gate) + the same 64 rows of amap1 (up)
+  int packed_a;  // weights in the [row tile][k-block][rows][64] layout (3-D maps, one contiguous box per load)
   // derived (gemm_finish_params)
   int kbt, n_tiles, units, grid;
   // stream-K workspace
@@ -44,6 +45,7 @@ size_t gemm_smem_bytes();
 size_t gemm_ws_bytes();
 void gemm_ws_layout(void* ws, float** partials, unsigned int** tickets);
 bool gemm_weight_map(CUtensorMap* map, const void* w, int rows, int K, int box_rows);
+bool gemm_weight_map_packed(CUtensorMap* map, const void* w, int rows, int K, int tile_rows);
 bool gemm_act_map(CUtensorMap* map, const void* x, int rows, int K);
 void gemm_finish_params(GemmParams& p);
 mv_status launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,

@@ -114,6 +114,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct mv_model {
   mv_model_dims dims;
+  int packed;  // projection weights in the packed layout
   const uint16_t* embed;
   std::vector<const uint16_t*> wqkv, wo, w_gate, w_up, w_down;
   const uint16_t* lm_head;
@@ -238,6 +239,7 @@ bool dims_ok(const mv_model_dims& d) {
 GemmParams base_params(const mv_session* s, int n_tok) {
   GemmParams p{};
   p.n_tok = n_tok;
+  p.packed_a = s->model->packed;
   p.eps = s->model->dims.norm_eps;
   p.err = mv_error_word();
   gemm_ws_layout(s->ws_gemm, &p.partials, &p.tickets);
@@ -363,6 +365,7 @@ extern "C" mv_status mv_model_create(const mv_model_dims* dims, const mv_model_w
     return MV_ERR_INVALID_ARG;
   mv_model* m = new mv_model();
   m->dims = d;
+  m->packed = w->packed ? 1 : 0;
   m->embed = w->embed;
   m->lm_head = w->lm_head;
   m->w1 = w->medusa_w1;
@@ -383,13 +386,15 @@ extern "C" mv_status mv_model_create(const mv_model_dims* dims, const mv_model_w
     m->w_gate.push_back(w->w_gate[l]);
     m->w_up.push_back(w->w_up[l]);
     m->w_down.push_back(w->w_down[l]);
-    ok = gemm_weight_map(&m->m_qkv[l], w->wqkv[l], 3 * HD, d.d, 128) &&
-         gemm_weight_map(&m->m_o[l], w->wo[l], d.d, HD, 128) &&
-         gemm_weight_map(&m->m_gate[l], w->w_gate[l], d.ffn, d.d, 64) &&
-         gemm_weight_map(&m->m_up[l], w->w_up[l], d.ffn, d.d, 64) &&
-         gemm_weight_map(&m->m_down[l], w->w_down[l], d.d, d.ffn, 128);
+    auto map = [&](CUtensorMap* t, const void* p, int rows, int K, int tr) {
+      return m->packed ? gemm_weight_map_packed(t, p, rows, K, tr) : gemm_weight_map(t, p, rows, K, tr);
+    };
+    ok = map(&m->m_qkv[l], w->wqkv[l], 3 * HD, d.d, 128) && map(&m->m_o[l], w->wo[l], d.d, HD, 128) &&
+         map(&m->m_gate[l], w->w_gate[l], d.ffn, d.d, 64) && map(&m->m_up[l], w->w_up[l], d.ffn, d.d, 64) &&
+         map(&m->m_down[l], w->w_down[l], d.d, d.ffn, 128);
   }
-  ok = ok && gemm_weight_map(&m->m_lm, w->lm_head, d.vocab, d.d, 128);
+  ok = ok && (m->packed ? gemm_weight_map_packed(&m->m_lm, w->lm_head, d.vocab, d.d, 128)
+                        : gemm_weight_map(&m->m_lm, w->lm_head, d.vocab, d.d, 128));
   if (!ok) {
     delete m;
     return MV_ERR_SHAPE;

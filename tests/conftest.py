@@ -17,3 +17,17 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(autouse=True)
+def _device_error_word(request):
+    """GPU tests: the library's sticky device error word must be clear after every test (read and cleared)."""
+    yield
+    if request.node.get_closest_marker("gpu") is None:
+        return
+    import torch
+    if not torch.cuda.is_available():
+        return
+    import medusa_tree_speculative_verify_gb300 as mv
+    st, code = mv.get_error()
+    assert st == 0, f"device error word set during {request.node.name}: {code:#x}"

@@ -77,6 +77,14 @@ def test_tree_errors(choices, topk):
     assert e.value.status == 3            # MV_ERR_TREE
 
 
+def test_packed_weight_sizes():
+    import ctypes
+    n = ctypes.c_size_t()
+    assert mv.lib().mv_packed_weight_bytes(300, 72, 128, ctypes.byref(n)) == 0
+    assert n.value == 3 * 2 * 128 * 64 * 2            # 3 row tiles x 2 k-blocks, zero padded
+    assert mv.lib().mv_packed_weight_bytes(300, 70, 128, ctypes.byref(n)) == 2   # K % 8 != 0
+
+
 def test_workspace_queries_and_shape_errors():
     assert mv.evaluate_posterior_workspace(64) > 64 * 16
     assert mv.tree_attention_workspace(32, 128, 4160, 64) > 0

@@ -37,16 +37,22 @@ def _cuda():
 
 # --------------------------------------------------------------------------------------------- projection kernel
 
+@pytest.mark.parametrize("packed", [False, True])
 @pytest.mark.parametrize("M,K,n", [(128, 64, 64), (300, 72, 9), (256, 4096, 64), (4096, 4096, 64),
                                    (12288, 4096, 1), (4096, 11008, 64), (32000, 4096, 64), (200, 8, 3)])
-def test_linear_bf16_vs_float64(M, K, n):
+def test_linear_bf16_vs_float64(M, K, n, packed):
     w = synth.normal(1, "w", (M, K), 1.0, dtype=torch.bfloat16, device="cuda")
     x = synth.normal(2, "x", (n, K), 1.0, dtype=torch.bfloat16, device="cuda")
     ld = M + 4
     out = torch.full((n, ld), float("nan"), dtype=torch.float32, device="cuda")
     ws = torch.zeros(mv.linear_bf16_workspace(), dtype=torch.uint8, device="cuda")
-    mv.linear_bf16(w, x, out, ws)
-    mv.linear_bf16(w, x, out, ws)  # twice: the stream-K tickets must be back at zero
+    if packed:
+        wp = mv.pack_weight(w, 128)
+        run = lambda: mv.linear_bf16_packed(wp, M, K, x, out, ws)
+    else:
+        run = lambda: mv.linear_bf16(w, x, out, ws)
+    run()
+    run()  # twice: the stream-K tickets must be back at zero
     got = out[:, :M].double().cpu().numpy()
     ref = x.double().cpu().numpy() @ w.double().cpu().numpy().T
     assert np.allclose(got, ref, rtol=1e-4, atol=1e-4 * math.sqrt(K))
@@ -59,9 +65,9 @@ DIMS = synth.TINY
 S_MAX = 256
 
 
-def _setup(tree_choices, topk=10):
+def _setup(tree_choices, topk=10, packed=True):
     w = synth.packed_weights(DIMS, 0, torch.bfloat16, "cuda")
-    model = mv.Model(DIMS, w)
+    model = mv.Model(DIMS, mv.pack_model_weights(w) if packed else w)
     tree = mv.Tree(tree_choices, topk)
     sess = mv.Session(model, tree, S_MAX)
     om = Backbone(DIMS, synth.unpacked_getter(DIMS, w))
@@ -150,10 +156,10 @@ def _margin_ok(gen, prompt, om):
     return first_close
 
 
-@pytest.mark.parametrize("tree", ["dense", "synthetic"])
-def test_greedy_decode_equals_ar(tree):
+@pytest.mark.parametrize("tree,packed", [("dense", True), ("synthetic", True), ("dense", False)])
+def test_greedy_decode_equals_ar(tree, packed):
     choices = synth.dense_tree_choices([2, 3]) if tree == "dense" else synth.synthetic_tree_choices(64, 2, 10)
-    _, _, _, sess, om, ot = _setup(choices)
+    _, _, _, sess, om, ot = _setup(choices, packed=packed)
     p = _prompt().numpy()
     gen, accs = _gpu_decode(sess, p, 16, mv.AcceptParams(GREEDY))
     first_close = _margin_ok(gen, p, om)
