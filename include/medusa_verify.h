@@ -319,6 +319,9 @@ mv_status mv_session_profile_read(mv_session* session, float* ms_by_kind, int32_
  * (high 16 bits: the kernel site, low 16 bits: 1 = bounded wait expired, 2 = index out of range), then clears
  * it. Synchronises the current device. */
 mv_status mv_get_error(uint32_t* code);
+/* Detail value recorded with the first device error since the last clear (e.g. an offending index); read
+ * it before mv_get_error(), which clears both. Synchronous. */
+mv_status mv_get_error_detail(uint32_t* detail);
 /* Human-readable name of a status. */
 const char* mv_status_string(mv_status s);
 

@@ -92,6 +92,7 @@ _SIGS = {
     "mv_session_profile": ([_P, _I], _I),
     "mv_session_profile_read": ([_P, _P, _P], _I),
     "mv_get_error": ([ctypes.POINTER(_U)], _I),
+    "mv_get_error_detail": ([ctypes.POINTER(_U)], _I),
     "mv_status_string": ([_I], ctypes.c_char_p),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
@@ -233,11 +234,12 @@ def kv_compact(kv, prefix_len, result, cur_len=None, stream=None):
            "kv_compact")
 
 
-def get_error():
-    """(status, code): reads and clears the device error word (synchronises the device)."""
-    code = ctypes.c_uint32()
+def get_error(with_detail=False):
+    """(status, code[, detail]): reads and clears the device error word (synchronises the device)."""
+    code, detail = ctypes.c_uint32(), ctypes.c_uint32()
+    lib().mv_get_error_detail(ctypes.byref(detail))
     st = lib().mv_get_error(ctypes.byref(code))
-    return st, code.value
+    return (st, code.value, detail.value) if with_detail else (st, code.value)
 
 
 def result_dict(buf):

@@ -294,28 +294,47 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int e = tid; e < n * (D / 4); e += kThreads) {
-    const int q = e / (D / 4), c4 = (e % (D / 4)) * 4;
+  // per-row merge weights once: w[q][s] = 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s'  (the pipeline buffers are free)
+  float* sw = reinterpret_cast<float*>(smem);  // [64][splits]
+  float* sl = sw + kRows * splits;              // [64][splits]
+  for (int e = tid; e < n * splits; e += kThreads) {
+    const int q = e / splits, sp = e % splits;
+    const float* mlp = a.ml + (((size_t)h * a.splits + sp) * kRows + q) * 2;
+    sw[e] = __ldcg(mlp);
+    sl[e] = __ldcg(mlp + 1);
+  }
+  __syncthreads();
+  if (tid < n) {
+    float* w = sw + tid * splits;
+    const float* l = sl + tid * splits;
     float M = -INFINITY;
-    for (int sp = 0; sp < splits; ++sp)
-      M = fmaxf(M, __ldcg(a.ml + (((size_t)h * a.splits + sp) * kRows + q) * 2));
+    for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, w[sp]);
     const float base = M == -INFINITY ? 0.0f : M;
-    float L = 0.0f, acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float L = 0.0f;
     for (int sp = 0; sp < splits; ++sp) {
-      const float* mlp = a.ml + (((size_t)h * a.splits + sp) * kRows + q) * 2;
-      const float w = exp2f(__ldcg(mlp) - base);
-      L += w * __ldcg(mlp + 1);
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(
-          a.opart + (((size_t)h * a.splits + sp) * kRows + q) * D + c4));
-      acc[0] += w * v.x;
-      acc[1] += w * v.y;
-      acc[2] += w * v.z;
-      acc[3] += w * v.w;
+      w[sp] = exp2f(w[sp] - base);
+      L += w[sp] * l[sp];
     }
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    for (int sp = 0; sp < splits; ++sp) w[sp] *= inv;
+  }
+  __syncthreads();
+  for (int e = tid; e < n * (D / 4); e += kThreads) {
+    const int q = e / (D / 4), c4 = (e % (D / 4)) * 4;
+    const float* w = sw + q * splits;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+    for (int sp = 0; sp < splits; ++sp) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(
+          a.opart + (((size_t)h * a.splits + sp) * kRows + q) * D + c4));
+      acc[0] += w[sp] * v.x;
+      acc[1] += w[sp] * v.y;
+      acc[2] += w[sp] * v.z;
+      acc[3] += w[sp] * v.w;
+    }
     uint2 pk;
-    pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    pk.x = pack_bf16x2(acc[0], acc[1]);
+    pk.y = pack_bf16x2(acc[2], acc[3]);
     *reinterpret_cast<uint2*>(a.out + ((size_t)q * a.H + h) * D + c4) = pk;
   }
   if (tid == 0) a.tickets[h] = 0u;
@@ -328,7 +347,11 @@ int choose_splits(int H, int max_tiles) {
   return std::min(s, 64);
 }
 
-size_t smem_bytes(int D) { return 1024 + (size_t)(1 + 2 * kStages) * kKeys * D * 2; }
+size_t smem_bytes(int D) {
+  const size_t pipeline = (size_t)(1 + 2 * kStages) * kKeys * D * 2;
+  const size_t merge = (size_t)2 * kRows * 64 * sizeof(float);  // weights + sums for up to 64 splits
+  return 1024 + (pipeline > merge ? pipeline : merge);
+}
 
 }  // namespace
 

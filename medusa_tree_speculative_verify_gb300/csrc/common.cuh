@@ -21,7 +21,8 @@ enum : uint32_t {
   MV_DEVERR_INDEX = 2,     // an index read from device memory was out of range
 };
 
-// Device error word of the current device (library-owned, no allocation: a __device__ symbol).
+// Device error word of the current device (library-owned, no allocation: a __device__ symbol). The word
+// after it holds a detail value of the first error (e.g. the offending index), see mv_get_error_detail().
 unsigned int* mv_error_word();
 // Host-side helpers.
 mv_status mv_last_launch(const char* what);
@@ -60,6 +61,9 @@ cudaError_t mv_launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
 
 MV_DEV void mv_set_error(unsigned int* err, uint32_t site, uint32_t kind) {
   if (err) atomicCAS(err, 0u, (site << 16) | kind);
+}
+MV_DEV void mv_set_error_detail(unsigned int* err, uint32_t site, uint32_t kind, uint32_t detail) {
+  if (err && atomicCAS(err, 0u, (site << 16) | kind) == 0u) err[1] = detail;
 }
 
 MV_DEV uint64_t mv_globaltimer() {

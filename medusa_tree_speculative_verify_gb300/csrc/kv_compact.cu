@@ -24,7 +24,8 @@ __global__ void __launch_bounds__(kWarps * 32) kv_compact_kernel(uint2* __restri
   const int prefix = prefix_dev ? *prefix_dev : prefix_host;
   const int acc = res->acc;
   if (acc < 0 || acc > MV_MAX_DEPTH || prefix < 0 || prefix + acc >= S_max) {
-    if (threadIdx.x == 0) mv_set_error(err, 5, MV_DEVERR_INDEX);
+    if (threadIdx.x == 0)
+      mv_set_error_detail(err, 5, MV_DEVERR_INDEX, ((uint32_t)(acc & 0xff) << 24) | ((uint32_t)prefix & 0xffffff));
     return;
   }
   int src[MV_MAX_DEPTH + 1];
@@ -32,7 +33,7 @@ __global__ void __launch_bounds__(kWarps * 32) kv_compact_kernel(uint2* __restri
   for (int j = 0; j <= MV_MAX_DEPTH; ++j) {
     src[j] = j <= acc ? prefix + res->nodes[j] : -1;
     if (j <= acc && (src[j] < prefix || src[j] >= S_max)) {
-      if (lane == 0) mv_set_error(err, 5, MV_DEVERR_INDEX);
+      if (lane == 0) mv_set_error_detail(err, 6, MV_DEVERR_INDEX, ((uint32_t)j << 24) | ((uint32_t)src[j] & 0xffffff));
       return;
     }
   }

@@ -18,6 +18,7 @@
 namespace {
 
 constexpr int kThreads = 512;
+constexpr int kBatch = 16;  // float4 per thread per chunk: 512 x 16 x 4 = 32768 logits
 
 struct Stat {
   float m;  // running max of z
@@ -73,16 +74,28 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
   __shared__ Stat tot;
   __shared__ bool last;
 
-  // ---- pass 1: max, first argmax, normaliser
+  // ---- pass 1: max, first argmax, normaliser. The row is read in chunks of kBatch float4 per thread, all
+  // loads of a chunk issued before any is used (a 32000-wide row is one chunk, kept for pass 2).
   Stat a{-FLT_MAX, 0x7fffffff, 0.0f};
   const int V4 = V >> 2;
   const float4* row4 = reinterpret_cast<const float4*>(row);
-  for (int i = tid; i < V4; i += kThreads) {
-    const float4 z = __ldg(row4 + i);
-    stat_push(a, z.x, 4 * i + 0, inv_t, typical);
-    stat_push(a, z.y, 4 * i + 1, inv_t, typical);
-    stat_push(a, z.z, 4 * i + 2, inv_t, typical);
-    stat_push(a, z.w, 4 * i + 3, inv_t, typical);
+  float4 buf[kBatch];
+  for (int c0 = 0; c0 < V4; c0 += kBatch * kThreads) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = c0 + tid + u * kThreads;
+      buf[u] = i < V4 ? __ldg(row4 + i) : make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = c0 + tid + u * kThreads;
+      if (i < V4) {
+        stat_push(a, buf[u].x, 4 * i + 0, inv_t, typical);
+        stat_push(a, buf[u].y, 4 * i + 1, inv_t, typical);
+        stat_push(a, buf[u].z, 4 * i + 2, inv_t, typical);
+        stat_push(a, buf[u].w, 4 * i + 3, inv_t, typical);
+      }
+    }
   }
   for (int i = 4 * V4 + tid; i < V; i += kThreads) stat_push(a, __ldg(row + i), i, inv_t, typical);
 #pragma unroll
@@ -108,11 +121,26 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
   if (typical) {
     const float inv_s = 1.0f / T.s;
     float h = 0.0f;
-    for (int i = tid; i < V4; i += kThreads) {
-      const float4 z = __ldg(row4 + i);
+    auto ent = [&](const float4& z) {
       const float p0 = expf((z.x - T.m) * inv_t) * inv_s, p1 = expf((z.y - T.m) * inv_t) * inv_s;
       const float p2 = expf((z.z - T.m) * inv_t) * inv_s, p3 = expf((z.w - T.m) * inv_t) * inv_s;
       h += p0 * logf(p0 + 1e-5f) + p1 * logf(p1 + 1e-5f) + p2 * logf(p2 + 1e-5f) + p3 * logf(p3 + 1e-5f);
+    };
+    if (V4 <= kBatch * kThreads) {  // the whole row is still in registers
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (tid + u * kThreads < V4) ent(buf[u]);
+    } else {
+      for (int c0 = 0; c0 < V4; c0 += kBatch * kThreads) {
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int i = c0 + tid + u * kThreads;
+          buf[u] = i < V4 ? __ldg(row4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+          if (c0 + tid + u * kThreads < V4) ent(buf[u]);
+      }
     }
     for (int i = 4 * V4 + tid; i < V; i += kThreads) {
       const float p = expf((__ldg(row + i) - T.m) * inv_t) * inv_s;

@@ -7,7 +7,7 @@
 #include "common.cuh"
 
 // One error word per device. A __device__ symbol: every GPU that loads the library holds it; no allocation.
-static __device__ unsigned int g_mv_error_word;
+static __device__ unsigned int g_mv_error_word[2];
 
 unsigned int* mv_error_word() {
   static std::mutex mu;
@@ -73,10 +73,17 @@ extern "C" mv_status mv_get_error(uint32_t* code) {
   if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MV_ERR_CUDA;
   if (code) *code = v;
   if (v != 0) {
-    unsigned int z = 0;
-    if (cudaMemcpy(w, &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return MV_ERR_CUDA;
+    unsigned int z[2] = {0, 0};
+    if (cudaMemcpy(w, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return MV_ERR_CUDA;
     return MV_ERR_DEVICE;
   }
+  return MV_OK;
+}
+
+extern "C" mv_status mv_get_error_detail(uint32_t* detail) {
+  unsigned int* w = mv_error_word();
+  if (!w || !detail) return MV_ERR_INVALID_ARG;
+  if (cudaMemcpy(detail, w + 1, sizeof(unsigned int), cudaMemcpyDeviceToHost) != cudaSuccess) return MV_ERR_CUDA;
   return MV_OK;
 }
 

@@ -29,5 +29,5 @@ def _device_error_word(request):
     if not torch.cuda.is_available():
         return
     import medusa_tree_speculative_verify_gb300 as mv
-    st, code = mv.get_error()
-    assert st == 0, f"device error word set during {request.node.name}: {code:#x}"
+    st, code, detail = mv.get_error(with_detail=True)
+    assert st == 0, f"device error word set during {request.node.name}: {code:#x} (detail {detail:#x})"
