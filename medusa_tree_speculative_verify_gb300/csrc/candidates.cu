@@ -16,12 +16,11 @@ __device__ __forceinline__ int candidate(int idx, const int32_t* root, const int
   return head_topk[k * ld + r];
 }
 
-__global__ void __launch_bounds__(128) build_candidates_kernel(const int32_t* __restrict__ root,
-                                                               const int32_t* __restrict__ head_topk, int topk,
-                                                               int ld, const int32_t* __restrict__ tree_indices,
+__global__ void __launch_bounds__(128) build_candidates_kernel(const int32_t* root, const int32_t* head_topk,
+                                                               int topk, int ld,
+                                                               const int32_t* __restrict__ tree_indices,
                                                                const int32_t* __restrict__ retrieve, int n_nodes,
-                                                               int n_cart, int32_t* __restrict__ tree_tokens,
-                                                               int32_t* __restrict__ cart) {
+                                                               int n_cart, int32_t* tree_tokens, int32_t* cart) {
   pdl_trigger();
   pdl_wait();
   for (int i = threadIdx.x; i < n_nodes; i += blockDim.x)

@@ -37,6 +37,10 @@ bool mv_set_smem_once(const void* func, int bytes, int* flags);
 // its writes are visible (a no-op when launched without the attribute); work before it may only read data no
 // earlier kernel writes (the weights). pdl_trigger() lets the next grid start launching.
 MV_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Data written by an earlier kernel of the stream is never read through the non-coherent path (__ldg,
+// const __restrict__): that path assumes the data is constant for the whole kernel, and under programmatic
+// dependent launch a kernel starts while its predecessor is still writing. Such data is read with plain or
+// .cg loads after pdl_wait(); only weights and tree buffers (written before any launch) use .nc loads.
 MV_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Whether launches use programmatic dependent launch (default on; MV_PDL=0 in the environment turns it off).

@@ -12,11 +12,10 @@ namespace {
 
 constexpr int kWarps = 8;
 
-__global__ void __launch_bounds__(kWarps * 32) kv_compact_kernel(uint2* __restrict__ kv, int units, int S_max,
-                                                                 int chunks, const int32_t* __restrict__ prefix_dev,
-                                                                 int prefix_host,
-                                                                 const mv_posterior_result* __restrict__ res,
-                                                                 int32_t* __restrict__ cur_len, unsigned int* err) {
+__global__ void __launch_bounds__(kWarps * 32) kv_compact_kernel(uint2* kv, int units, int S_max, int chunks,
+                                                                 const int32_t* prefix_dev, int prefix_host,
+                                                                 const mv_posterior_result* res, int32_t* cur_len,
+                                                                 unsigned int* err) {
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;

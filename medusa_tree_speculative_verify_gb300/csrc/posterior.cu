@@ -57,11 +57,9 @@ MV_DEV Stat stat_merge(Stat a, Stat b, float inv_t, bool typical) {
 }
 
 __global__ void __launch_bounds__(kThreads) posterior_kernel(
-    const float* __restrict__ logits, int V, int ld, const int32_t* __restrict__ tree_tokens,
-    const int32_t* __restrict__ retrieve, int n_nodes, int n_paths, int width, mv_accept_params prm,
-    mv_posterior_result* __restrict__ out, float* __restrict__ node_stats_out, int32_t* __restrict__ node_argmax_out,
-    float* __restrict__ ws_stats, int32_t* __restrict__ ws_argmax, unsigned int* __restrict__ ticket,
-    unsigned int* err) {
+    const float* logits, int V, int ld, const int32_t* tree_tokens, const int32_t* __restrict__ retrieve,
+    int n_nodes, int n_paths, int width, mv_accept_params prm, mv_posterior_result* out, float* node_stats_out,
+    int32_t* node_argmax_out, float* ws_stats, int32_t* ws_argmax, unsigned int* ticket, unsigned int* err) {
   pdl_trigger();
   pdl_wait();
   const bool typical = prm.mode == MV_TYPICAL;
@@ -84,7 +82,7 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int i = c0 + tid + u * kThreads;
-      buf[u] = i < V4 ? __ldg(row4 + i) : make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
+      buf[u] = i < V4 ? __ldcg(row4 + i) : make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
@@ -97,7 +95,7 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
       }
     }
   }
-  for (int i = 4 * V4 + tid; i < V; i += kThreads) stat_push(a, __ldg(row + i), i, inv_t, typical);
+  for (int i = 4 * V4 + tid; i < V; i += kThreads) stat_push(a, __ldcg(row + i), i, inv_t, typical);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
     Stat b;
@@ -135,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           const int i = c0 + tid + u * kThreads;
-          buf[u] = i < V4 ? __ldg(row4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          buf[u] = i < V4 ? __ldcg(row4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u)
@@ -143,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
       }
     }
     for (int i = 4 * V4 + tid; i < V; i += kThreads) {
-      const float p = expf((__ldg(row + i) - T.m) * inv_t) * inv_s;
+      const float p = expf((__ldcg(row + i) - T.m) * inv_t) * inv_s;
       h += p * logf(p + 1e-5f);
     }
 #pragma unroll

@@ -23,9 +23,8 @@ namespace {
 constexpr int kTok = 64;  // token columns of every activation buffer
 
 // x[j][:] = float(E[tok[j]][:]), xb = E[tok[j]] (bf16), ssq[s][j] = sum of x^2 over the 128-column slice s.
-__global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ tokens, const uint16_t* __restrict__ E,
-                                                    int vocab, int d, float* __restrict__ x, uint16_t* __restrict__ xb,
-                                                    float* __restrict__ ssq, unsigned int* err) {
+__global__ void __launch_bounds__(256) embed_kernel(const int32_t* tokens, const uint16_t* __restrict__ E, int vocab,
+                                                    int d, float* x, uint16_t* xb, float* ssq, unsigned int* err) {
   pdl_trigger();
   pdl_wait();
   const int j = blockIdx.x;
@@ -53,7 +52,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const int32_t* __restrict__ 
 
 // After a prefill chunk of c tokens: the last chunk records the root (argmax of its last logits row) and the
 // node the heads read (c - 1) in the result; earlier chunks just advance the length.
-__global__ void __launch_bounds__(1024) prefill_finish_kernel(const float* __restrict__ logits, int V, int ld, int c,
+__global__ void __launch_bounds__(1024) prefill_finish_kernel(const float* logits, int V, int ld, int c,
                                                              int last, int32_t* cur_len,
                                                              mv_posterior_result* res) {
   pdl_trigger();
@@ -175,7 +174,8 @@ int prof_mark(mv_session* s, cudaStream_t st) {
     s->ev_pool.push_back(e);
   }
   const int i = (int)s->ev_next++;
-  cudaEventRecord(s->ev_pool[i], st);
+  // external record: inside a stream capture this becomes a real event-record node whose timestamps can be read
+  cudaEventRecordWithFlags(s->ev_pool[i], st, cudaEventRecordExternal);
   return i;
 }
 
