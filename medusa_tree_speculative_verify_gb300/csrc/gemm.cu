@@ -29,7 +29,7 @@
 namespace {
 
 constexpr int BM = 128, BN = 64, BK = 64;
-constexpr int kStages = 8;
+constexpr int kStages = 6;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kBBytes = BN * BK * 2;  // 8 KB
 constexpr int kStageBytes = kABytes + kBBytes;
@@ -37,8 +37,7 @@ constexpr int kEpiThreads = 128;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kTmemCols = 2 * BN;
 constexpr int kPitch = BN + 1;  // staging row pitch (floats)
-constexpr int kStageRows = 64;  // epilogue staging holds half a tile; exchanges run in two rounds
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)kStageRows * kPitch * 4 + 256;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)BM * kPitch * 4 + 256;
 
 // kind::f16 instruction descriptor: D fp32, A/B bf16, both K-major, N = 64, M = 128.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
@@ -177,109 +176,85 @@ MV_DEV void load_epi_const(const GemmParams& p, EpiConst* ec, int i) {
   epi_bar();
 }
 
+// The finished 128 x 64 accumulator tile is in the staging buffer (row i = weight row, column j = token,
+// pitch kPitch). Every epilogue is a short rolled loop over it: the code stays small, which matters because
+// it first runs at the very end of the kernel, and it needs no register arrays indexed at run time.
 template <int EPI>
-MV_DEV void final_epilogue(const GemmParams& p, int tile, int i, float (&v)[BN], float* stg, const EpiConst* ec) {
+MV_DEV void final_epilogue(const GemmParams& p, int tile, int i, float* stg, const EpiConst* ec) {
   const float* s_scale = ec->scale;
   const int ntok = p.n_tok;
-  const bool lo = i < 64;
-  float* my = stg + (i & 63) * kPitch;  // staging row shared by rows i and i^64, one round each
+  const float* row = stg + i * kPitch;
   if constexpr (EPI == EPI_STORE) {
     const int R = tile * BM + i;
     if (R < p.M) {
-#pragma unroll
-      for (int j = 0; j < BN; ++j)
-        if (j < ntok) p.out_f32[(size_t)j * p.ld_out + R] = v[j] * s_scale[j];
+#pragma unroll 4
+      for (int j = 0; j < ntok; ++j) p.out_f32[(size_t)j * p.ld_out + R] = row[j] * s_scale[j];
     }
   } else if constexpr (EPI == EPI_RESIDUAL) {
     const int R = tile * BM + i;
-    const bool ok = R < p.M;
-    // all residual loads first (independent, in flight together), then the adds and stores
-#pragma unroll
-    for (int j = 0; j < BN; ++j) v[j] += (ok && j < ntok) ? __ldcg(p.x + (size_t)j * p.M + R) : 0.0f;
-#pragma unroll
-    for (int j = 0; j < BN; ++j) {
-      const float xn = (ok && j < ntok) ? v[j] : 0.0f;
-      if (ok && j < ntok) {
+    float* srow = stg + i * kPitch;
+    if (R < p.M) {
+#pragma unroll 8
+      for (int j = 0; j < ntok; ++j) {
+        const float xn = __ldcg(p.x + (size_t)j * p.M + R) + srow[j];
         p.x[(size_t)j * p.M + R] = xn;
         p.xb[(size_t)j * p.M + R] = __bfloat16_as_ushort(__float2bfloat16_rn(xn));
+        srow[j] = xn * xn;
       }
-      v[j] = xn * xn;
-    }
-    // per-token sum of squares over the tile's 128 rows: upper half staged, lower half adds, then columns
-    if (!lo) {
-#pragma unroll
-      for (int j = 0; j < BN; ++j) my[j] = v[j];
+    } else {
+      for (int j = 0; j < ntok; ++j) srow[j] = 0.0f;
     }
     epi_bar();
-    if (lo) {
-#pragma unroll
-      for (int j = 0; j < BN; ++j) my[j] += v[j];
-    }
-    epi_bar();
-    if (i < BN) {
+    if (i < ntok) {  // per-token sum of squares over the tile's rows (input of the next RMSNorm)
       float sum = 0.0f;
-      for (int r = 0; r < kStageRows; ++r) sum += stg[r * kPitch + i];
+#pragma unroll 8
+      for (int r = 0; r < BM; ++r) sum += stg[r * kPitch + i];
       p.ssq_out[tile * BN + i] = sum;
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
     // rows 0..63: gate, rows 64..127: the matching up rows
-    if (!lo) {
-#pragma unroll
-      for (int j = 0; j < BN; ++j) my[j] = v[j] * s_scale[j];
-    }
-    epi_bar();
-    if (lo) {
-      const int f = tile * 64 + i;
-      if (f < p.F) {
-#pragma unroll
-        for (int j = 0; j < BN; ++j)
-          if (j < ntok)
-            p.act[(size_t)j * p.F + f] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(silu(v[j] * s_scale[j]) * my[j]));
+    const int f = tile * 64 + i;
+    if (i < 64 && f < p.F) {
+      const float* up = stg + (i + 64) * kPitch;
+#pragma unroll 4
+      for (int j = 0; j < ntok; ++j) {
+        const float s = s_scale[j];
+        p.act[(size_t)j * p.F + f] = __bfloat16_as_ushort(__float2bfloat16_rn(silu(row[j] * s) * (up[j] * s)));
       }
     }
   } else if constexpr (EPI == EPI_QKV) {
-#pragma unroll
-    for (int j = 0; j < BN; ++j) v[j] *= s_scale[j];
     const int R = tile * BM + i;
-    const bool valid = R < p.M;
-    const int HD = p.H * p.D;
-    const int which = R / HD, within = R % HD, head = within / p.D, dim = within % p.D;
-    const int half = p.D >> 1;
-    const int kv_row0 = ec->kv_row0;  // prefix length: the tree block's keys/values go to rows kv_row0 + j
-    const int pi = dim < half ? i + half : i - half;  // RoPE partner row (same head, same tile)
-    const float inv_freq = exp2f(-(float)(2 * (dim % half)) / (float)p.D * p.log2_theta);
-    for (int round = 0; round < 2; ++round) {
-      if ((i >> 6) == round) {
-#pragma unroll
-        for (int j = 0; j < BN; ++j) my[j] = v[j];
+    if (R < p.M) {
+      const int HD = p.H * p.D;
+      const int which = R / HD, within = R % HD, head = within / p.D, dim = within % p.D;
+      const int half = p.D >> 1;
+      const int kv_row0 = ec->kv_row0;  // prefix length: the tree block's keys/values go to rows kv_row0 + j
+      const float* prow = stg + (dim < half ? i + half : i - half) * kPitch;  // RoPE partner (same head)
+      const float inv_freq = exp2f(-(float)(2 * (dim % half)) / (float)p.D * p.log2_theta);
+      uint16_t* dst;
+      size_t stride;
+      if (which == 0) {
+        dst = p.q_out + (size_t)head * p.D + dim;
+        stride = (size_t)p.H * p.D;
+      } else {
+        const size_t plane = (size_t)p.layer * 2 + (which - 1);
+        dst = p.kv + ((plane * p.H + head) * p.S_max + kv_row0) * p.D + dim;
+        stride = (size_t)p.D;
       }
-      epi_bar();
-      if (valid && (which == 2 ? round == 0 : (pi >> 6) == round)) {
-        const float* pr = stg + (pi & 63) * kPitch;
-#pragma unroll
-        for (int j = 0; j < BN; ++j) {
-          if (j >= ntok) break;
-          float val = v[j];
-          if (which < 2) {
-            const float pv = pr[j];
-            float sn, cs;
-            sincosf((float)ec->pos[j] * inv_freq, &sn, &cs);
-            val = dim < half ? val * cs - pv * sn : val * cs + pv * sn;
-          }
-          const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(val));
-          if (which == 0) {
-            p.q_out[((size_t)j * p.H + head) * p.D + dim] = b;
-          } else {
-            const size_t plane = (size_t)p.layer * 2 + (which - 1);
-            p.kv[((plane * p.H + head) * p.S_max + kv_row0 + j) * p.D + dim] = b;
-          }
+#pragma unroll 2
+      for (int j = 0; j < ntok; ++j) {
+        float val = row[j] * s_scale[j];
+        if (which < 2) {
+          const float pv = prow[j] * s_scale[j];
+          float sn, cs;
+          sincosf((float)ec->pos[j] * inv_freq, &sn, &cs);
+          val = dim < half ? val * cs - pv * sn : val * cs + pv * sn;
         }
+        dst[(size_t)j * stride] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
       }
-      epi_bar();
     }
   }
-  epi_bar();  // the staging buffer and scales are reused by the next segment
+  epi_bar();  // the staging buffer is reused by the next segment
 }
 
 template <int EPI>
@@ -443,7 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       if (lane == 0) mbar_arrive(&tempty[buf]);
 
       const bool whole = sg.kb0 == 0 && sg.kb1 == p.kbt;
-      if (!whole) {
+      float* srow = stg + i * kPitch;
+      if (whole) {
+#pragma unroll
+        for (int j = 0; j < BN; ++j) srow[j] = v[j];
+      } else {
+        // stream-K: publish this CTA's partial tile; the last contributor sums all of them in contributor
+        // order (the same order whichever CTA is last, so the result is deterministic)
         float* slot = partial_slot(cta, sg.tile, p);
 #pragma unroll
         for (int j = 0; j < BN; ++j) slot[j * BM + i] = v[j];
@@ -459,16 +440,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         if (!s_last) continue;
         __threadfence();
         const int c0 = first_contributor(sg.tile, p);
-#pragma unroll
-        for (int j = 0; j < BN; ++j) v[j] = 0.0f;
+        for (int j = 0; j < BN; ++j) srow[j] = 0.0f;
         for (int c = c0; c < p.grid && unit_begin(c, p) < (long long)(sg.tile + 1) * p.kbt; ++c) {
-          const float* ps = partial_slot(c, sg.tile, p);
-#pragma unroll
-          for (int j = 0; j < BN; ++j) v[j] += __ldcg(ps + j * BM + i);
+          const float* ps = partial_slot(c, sg.tile, p) + i;
+#pragma unroll 8
+          for (int j = 0; j < BN; ++j) srow[j] += __ldcg(ps + j * BM);
         }
         if (i == 0) p.tickets[sg.tile] = 0u;
       }
-      final_epilogue<EPI>(p, sg.tile, i, v, stg, &s_ec);
+      epi_bar();
+      final_epilogue<EPI>(p, sg.tile, i, stg, &s_ec);
     }
   }
 
