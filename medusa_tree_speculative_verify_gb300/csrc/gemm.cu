@@ -194,12 +194,17 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int i, float* stg, con
     const int R = tile * BM + i;
     float* srow = stg + i * kPitch;
     if (R < p.M) {
-#pragma unroll 8
-      for (int j = 0; j < ntok; ++j) {
-        const float xn = __ldcg(p.x + (size_t)j * p.M + R) + srow[j];
-        p.x[(size_t)j * p.M + R] = xn;
-        p.xb[(size_t)j * p.M + R] = __bfloat16_as_ushort(__float2bfloat16_rn(xn));
-        srow[j] = xn * xn;
+      float xo[BN];  // every residual load in flight before the first use
+#pragma unroll
+      for (int j = 0; j < BN; ++j) xo[j] = j < ntok ? __ldcg(p.x + (size_t)j * p.M + R) : 0.0f;
+#pragma unroll
+      for (int j = 0; j < BN; ++j) {
+        if (j < ntok) {
+          const float xn = xo[j] + srow[j];
+          p.x[(size_t)j * p.M + R] = xn;
+          p.xb[(size_t)j * p.M + R] = __bfloat16_as_ushort(__float2bfloat16_rn(xn));
+          srow[j] = xn * xn;
+        }
       }
     } else {
       for (int j = 0; j < ntok; ++j) srow[j] = 0.0f;
@@ -440,12 +445,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         if (!s_last) continue;
         __threadfence();
         const int c0 = first_contributor(sg.tile, p);
-        for (int j = 0; j < BN; ++j) srow[j] = 0.0f;
+        // all 64 loads of a contributor in flight at once: at the end of the kernel every dependent round
+        // trip to L2 costs about a microsecond
+#pragma unroll
+        for (int j = 0; j < BN; ++j) v[j] = 0.0f;
         for (int c = c0; c < p.grid && unit_begin(c, p) < (long long)(sg.tile + 1) * p.kbt; ++c) {
           const float* ps = partial_slot(c, sg.tile, p) + i;
-#pragma unroll 8
-          for (int j = 0; j < BN; ++j) srow[j] += __ldcg(ps + j * BM);
+#pragma unroll
+          for (int j = 0; j < BN; ++j) v[j] += __ldcg(ps + j * BM);
         }
+#pragma unroll
+        for (int j = 0; j < BN; ++j) srow[j] = v[j];
         if (i == 0) p.tickets[sg.tile] = 0u;
       }
       epi_bar();
