@@ -1,0 +1,77 @@
+"""Full-size parity of the verify loop at Llama-7B shape (32 layers, d 4096, 32 x 128 heads, FFN 11008,
+vocabulary 32000, 4 Medusa heads, the synthetic 64-node tree, a random 128-token prompt), in the launch
+configuration bench.py times (packed weights, CUDA-graph replay of the steps).
+
+The float64 oracle cannot decode 64 tokens of a 7B model one by one in reasonable time, so it checks sampled
+outputs and properties that hold at any size:
+* teacher forcing: one causal oracle forward over prompt + the 64 GPU tokens; every GPU token must be the
+  oracle argmax or within the bf16 tolerance of it ("Phi-3-mini-128k-instruct_rai_1.8.0_medusa_1.0_npu", 2️⃣:
+  greedy Medusa output equals the base model's; "大模型推理 memory bandwidth bound (5) - Medusa", 二.1);
+* the first verify step's LM logits on sampled tree nodes against the oracle's tree forward (二.5).
+"""
+import numpy as np
+import pytest
+import torch
+
+import medusa_tree_speculative_verify_gb300 as mv
+import synth
+from oracle.decode import chain_mask
+from oracle.model import Backbone, KVCache
+from oracle.tree import tree_buffers
+
+pytestmark = pytest.mark.gpu
+DIMS = synth.LLAMA7B
+P, N_NEW = 128, 64
+
+
+@pytest.fixture(scope="module")
+def model7b():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    w = synth.packed_weights(DIMS, 0, torch.bfloat16, "cuda")
+    wp = mv.pack_model_weights(w)
+    return w, mv.Model(DIMS, wp)
+
+
+def test_7b_greedy_stream_teacher_forced(model7b):
+    w, model = model7b
+    choices = synth.synthetic_tree_choices(64, 4, 10)
+    tree = mv.Tree(choices, 10)
+    sess = mv.Session(model, tree, 1024)
+    prompt = synth.prompt_tokens(0, P, DIMS.vocab)
+    sess.prefill(torch.as_tensor(prompt, dtype=torch.int32, device="cuda"))
+    gen, first_logits = [], None
+    while len(gen) < N_NEW:
+        if first_logits is None:
+            sess.step(mv.AcceptParams(mv.GREEDY))
+            first_logits = sess.logits[: tree.n_nodes].double().cpu().numpy()
+            first_tree_tokens = sess.tree_tokens.cpu().numpy().copy()
+        else:
+            sess.steps_graph(1, mv.AcceptParams(mv.GREEDY))
+        gen += sess.read_result()["tokens"]
+    gen = np.asarray(gen[:N_NEW])
+
+    cache = {}
+
+    def get(name):  # every logical weight converted once to float64 (about 63 GB of host memory)
+        if name not in cache:
+            cache[name] = synth.unpacked_getter(DIMS, w)(name)
+        return cache[name]
+
+    om = Backbone(DIMS, get)
+    o = tree_buffers(choices, 10)
+    kv = KVCache(DIMS, P + 64 + N_NEW)
+    _, lg_prompt = om.forward(prompt.numpy(), np.arange(P), kv, 0, chain_mask(P))
+    kv_tree = KVCache(DIMS, P + 64 + N_NEW, kv.data)
+    _, tl = om.forward(first_tree_tokens, P + o["position_ids"], kv_tree, P, o["attn_mask"])
+    _, lg_gen = om.forward(gen, P + np.arange(N_NEW), kv, P, chain_mask(N_NEW))
+    # 1) teacher forcing: the logits that predict gen[i] are the prompt's last row (i = 0) or gen[i-1]'s row
+    lg = np.concatenate([lg_prompt[-1:], lg_gen[:-1]])
+    for i, t in enumerate(gen):
+        top = lg[i].max()
+        assert top - lg[i, t] <= 1e-2 + 2e-2 * abs(top), (i, int(t), int(np.argmax(lg[i])), top - lg[i, t])
+    # 2) the first step's LM logits on sampled tree nodes against the oracle's tree forward at prefix P
+    rows = [0, 1, 7, 30, 63]
+    assert np.allclose(first_logits[rows], tl[rows], rtol=2e-2, atol=1e-2)
+    rel = np.linalg.norm(first_logits[rows] - tl[rows]) / np.linalg.norm(tl[rows])
+    assert rel < 2e-2, rel
