@@ -23,7 +23,8 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kKeys = 64;   // keys per tile
 constexpr int kRows = 64;   // query rows per CTA (tree nodes, padded)
-constexpr int kStages = 3;
+constexpr int kStages = 2;  // 80 KB of shared memory at D = 128: two CTAs share an SM
+constexpr int kMinTiles = 4;  // key tiles per split at least
 
 MV_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -97,26 +98,14 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
     return;
   }
   const int total_tiles = (P + n + kKeys - 1) / kKeys;
-  // The grid is sized for the longest prefix; at this prefix only `splits` CTAs per head get tiles, the
-  // others leave at once and the merge reads only the real partials.
-  const int splits = min(a.splits, total_tiles);
+  // The grid is sized for the longest prefix; at this prefix only `splits` CTAs per head get tiles (at least
+  // kMinTiles each, so a short prefix is not spread over partials that cost more to merge than to compute),
+  // the others leave at once and the merge reads only the real partials.
+  const int splits = max(1, min(a.splits, (total_tiles + kMinTiles - 1) / kMinTiles));
   if (split >= splits) return;
   const int t_begin = (int)((long long)split * total_tiles / splits);
   const int t_end = (int)((long long)(split + 1) * total_tiles / splits);
   const int count = t_end - t_begin;
-
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
-    mbar_fence_init();
-  }
-  // Q: plain 16-byte loads into the tile layout (rows >= n are zero)
-  for (int e = tid; e < kRows * (D / 8); e += kThreads) {
-    const int r = e / (D / 8), c = e % (D / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < n) v = *reinterpret_cast<const uint4*>(a.q + ((size_t)r * a.H + h) * D + c * 8);
-    *reinterpret_cast<uint4*>(sq + tile_off<D>(r, c)) = v;
-  }
-  __syncthreads();
 
   auto issue = [&](int i) {  // tile t_begin + i into stage i % kStages
     const int st = i % kStages, key0 = (t_begin + i) * kKeys;
@@ -129,8 +118,20 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
                   a.plane_v);
     }
   };
-  if (tid == 0)
+  // the first key/value tiles are requested before Q is loaded, so the two latencies overlap
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+    mbar_fence_init();
     for (int i = 0; i < kStages && i < count; ++i) issue(i);
+  }
+  // Q: plain 16-byte loads into the tile layout (rows >= n are zero)
+  for (int e = tid; e < kRows * (D / 8); e += kThreads) {
+    const int r = e / (D / 8), c = e % (D / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < n) v = *reinterpret_cast<const uint4*>(a.q + ((size_t)r * a.H + h) * D + c * 8);
+    *reinterpret_cast<uint4*>(sq + tile_off<D>(r, c)) = v;
+  }
+  __syncthreads();
 
   // Q fragments for this warp's 16 rows
   uint32_t qa[KS][4];
@@ -319,31 +320,47 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
     for (int sp = 0; sp < splits; ++sp) w[sp] *= inv;
   }
   __syncthreads();
-  for (int e = tid; e < n * (D / 4); e += kThreads) {
-    const int q = e / (D / 4), c4 = (e % (D / 4)) * 4;
-    const float* w = sw + q * splits;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-    for (int sp = 0; sp < splits; ++sp) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(
-          a.opart + (((size_t)h * a.splits + sp) * kRows + q) * D + c4));
-      acc[0] += w[sp] * v.x;
-      acc[1] += w[sp] * v.y;
-      acc[2] += w[sp] * v.z;
-      acc[3] += w[sp] * v.w;
+  // each thread owns kPer (row, 4-column) chunks; per split, the loads of all of them are in flight together
+  constexpr int kPer = kRows * (D / 4) / kThreads;
+  float acc[kPer][4];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.0f;
+  for (int sp = 0; sp < splits; ++sp) {
+    const float* base = a.opart + ((size_t)h * a.splits + sp) * kRows * D;
+    float4 v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = tid + u * kThreads, q = e / (D / 4), c4 = (e % (D / 4)) * 4;
+      v[u] = q < n ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)q * D + c4)) : make_float4(0, 0, 0, 0);
     }
-    uint2 pk;
-    pk.x = pack_bf16x2(acc[0], acc[1]);
-    pk.y = pack_bf16x2(acc[2], acc[3]);
-    *reinterpret_cast<uint2*>(a.out + ((size_t)q * a.H + h) * D + c4) = pk;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = tid + u * kThreads, q = e / (D / 4);
+      const float w = q < n ? sw[q * splits + sp] : 0.0f;
+      acc[u][0] += w * v[u].x;
+      acc[u][1] += w * v[u].y;
+      acc[u][2] += w * v[u].z;
+      acc[u][3] += w * v[u].w;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int e = tid + u * kThreads, q = e / (D / 4), c4 = (e % (D / 4)) * 4;
+    if (q < n) {
+      uint2 pk;
+      pk.x = pack_bf16x2(acc[u][0], acc[u][1]);
+      pk.y = pack_bf16x2(acc[u][2], acc[u][3]);
+      *reinterpret_cast<uint2*>(a.out + ((size_t)q * a.H + h) * D + c4) = pk;
+    }
   }
   if (tid == 0) a.tickets[h] = 0u;
 }
 
 int choose_splits(int H, int max_tiles) {
+  // one wave of two CTAs per SM, at least kMinTiles key tiles per split
   const int sms = mv_sm_count();
-  int s = std::max(1, (2 * sms + H - 1) / H);
-  s = std::min(s, std::max(1, (max_tiles + 1) / 2));
+  int s = std::max(1, (2 * sms) / H);
+  s = std::min(s, std::max(1, (max_tiles + kMinTiles - 1) / kMinTiles));
   return std::min(s, 64);
 }
 

@@ -72,62 +72,93 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
   __shared__ Stat tot;
   __shared__ bool last;
 
-  // ---- pass 1: max, first argmax, normaliser. The row is read in chunks of kBatch float4 per thread, all
-  // loads of a chunk issued before any is used (a 32000-wide row is one chunk, kept for pass 2).
-  Stat a{-FLT_MAX, 0x7fffffff, 0.0f};
+  // The row (32000 logits) is held in registers, kBatch float4 per thread, all loaded before any is used.
+  // pass 1: max and first argmax; pass 2 (typical): e = exp((z - max) / T) kept in place, Z = sum e;
+  // pass 3 (typical): H = -sum p log(p + 1e-5) with p = e / Z. Rows longer than 32768 stream in chunks with
+  // an online (rescaled) normaliser instead.
   const int V4 = V >> 2;
   const float4* row4 = reinterpret_cast<const float4*>(row);
+  const bool in_regs = V4 <= kBatch * kThreads;
   float4 buf[kBatch];
+  Stat a{-FLT_MAX, 0x7fffffff, 0.0f};
   for (int c0 = 0; c0 < V4; c0 += kBatch * kThreads) {
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int i = c0 + tid + u * kThreads;
       buf[u] = i < V4 ? __ldcg(row4 + i) : make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
     }
+    const bool online = typical && !in_regs;
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int i = c0 + tid + u * kThreads;
       if (i < V4) {
-        stat_push(a, buf[u].x, 4 * i + 0, inv_t, typical);
-        stat_push(a, buf[u].y, 4 * i + 1, inv_t, typical);
-        stat_push(a, buf[u].z, 4 * i + 2, inv_t, typical);
-        stat_push(a, buf[u].w, 4 * i + 3, inv_t, typical);
+        stat_push(a, buf[u].x, 4 * i + 0, inv_t, online);
+        stat_push(a, buf[u].y, 4 * i + 1, inv_t, online);
+        stat_push(a, buf[u].z, 4 * i + 2, inv_t, online);
+        stat_push(a, buf[u].w, 4 * i + 3, inv_t, online);
       }
     }
   }
-  for (int i = 4 * V4 + tid; i < V; i += kThreads) stat_push(a, __ldcg(row + i), i, inv_t, typical);
+  for (int i = 4 * V4 + tid; i < V; i += kThreads) stat_push(a, __ldcg(row + i), i, inv_t, typical && !in_regs);
+  const bool online = typical && !in_regs;
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
     Stat b;
     b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
     b.i = __shfl_xor_sync(0xffffffffu, a.i, o);
     b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
-    a = stat_merge(a, b, inv_t, typical);
+    a = stat_merge(a, b, inv_t, online);
   }
   if (lane == 0) red[warp] = a;
   __syncthreads();
   if (tid == 0) {
     Stat t = red[0];
-    for (int w = 1; w < kThreads / 32; ++w) t = stat_merge(t, red[w], inv_t, typical);
+    for (int w = 1; w < kThreads / 32; ++w) t = stat_merge(t, red[w], inv_t, online);
     tot = t;
   }
   __syncthreads();
-  const Stat T = tot;
+  Stat T = tot;
 
-  // ---- pass 2 (typical): entropy of p = softmax(z/T), H = -sum p log(p + 1e-5)
   float H = 0.0f, tau = 0.0f;
   if (typical) {
+    auto block_sum = [&](float v) {
+      __syncthreads();
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) fred[warp] = v;
+      __syncthreads();
+      float s = 0.0f;
+      for (int w = 0; w < kThreads / 32; ++w) s += fred[w];
+      return s;
+    };
+    if (in_regs) {  // pass 2: exponentials in place and their sum
+      float z = 0.0f;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (tid + u * kThreads < V4) {
+          buf[u].x = expf((buf[u].x - T.m) * inv_t);
+          buf[u].y = expf((buf[u].y - T.m) * inv_t);
+          buf[u].z = expf((buf[u].z - T.m) * inv_t);
+          buf[u].w = expf((buf[u].w - T.m) * inv_t);
+          z += (buf[u].x + buf[u].y) + (buf[u].z + buf[u].w);
+        }
+      }
+      for (int i = 4 * V4 + tid; i < V; i += kThreads) z += expf((__ldcg(row + i) - T.m) * inv_t);
+      T.s = block_sum(z);
+    }
     const float inv_s = 1.0f / T.s;
     float h = 0.0f;
-    auto ent = [&](const float4& z) {
-      const float p0 = expf((z.x - T.m) * inv_t) * inv_s, p1 = expf((z.y - T.m) * inv_t) * inv_s;
-      const float p2 = expf((z.z - T.m) * inv_t) * inv_s, p3 = expf((z.w - T.m) * inv_t) * inv_s;
-      h += p0 * logf(p0 + 1e-5f) + p1 * logf(p1 + 1e-5f) + p2 * logf(p2 + 1e-5f) + p3 * logf(p3 + 1e-5f);
-    };
-    if (V4 <= kBatch * kThreads) {  // the whole row is still in registers
+    auto ent = [&](float p) { h += p * logf(p + 1e-5f); };
+    if (in_regs) {  // pass 3
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u)
-        if (tid + u * kThreads < V4) ent(buf[u]);
+      for (int u = 0; u < kBatch; ++u) {
+        if (tid + u * kThreads < V4) {
+          ent(buf[u].x * inv_s);
+          ent(buf[u].y * inv_s);
+          ent(buf[u].z * inv_s);
+          ent(buf[u].w * inv_s);
+        }
+      }
     } else {
       for (int c0 = 0; c0 < V4; c0 += kBatch * kThreads) {
 #pragma unroll
@@ -136,25 +167,18 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
           buf[u] = i < V4 ? __ldcg(row4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u)
-          if (c0 + tid + u * kThreads < V4) ent(buf[u]);
+        for (int u = 0; u < kBatch; ++u) {
+          if (c0 + tid + u * kThreads < V4) {
+            ent(expf((buf[u].x - T.m) * inv_t) * inv_s);
+            ent(expf((buf[u].y - T.m) * inv_t) * inv_s);
+            ent(expf((buf[u].z - T.m) * inv_t) * inv_s);
+            ent(expf((buf[u].w - T.m) * inv_t) * inv_s);
+          }
+        }
       }
     }
-    for (int i = 4 * V4 + tid; i < V; i += kThreads) {
-      const float p = expf((__ldcg(row + i) - T.m) * inv_t) * inv_s;
-      h += p * logf(p + 1e-5f);
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
-    if (lane == 0) fred[warp] = h;
-    __syncthreads();
-    if (tid == 0) {
-      float s = 0.0f;
-      for (int w = 0; w < kThreads / 32; ++w) s += fred[w];
-      fred[0] = s;
-    }
-    __syncthreads();
-    H = -fred[0];
+    for (int i = 4 * V4 + tid; i < V; i += kThreads) ent(expf((__ldcg(row + i) - T.m) * inv_t) * inv_s);
+    H = -block_sum(h);
     tau = fminf(prm.eps, prm.delta * expf(-H));
   }
 
