@@ -311,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       tma_prefetch_desc(&bmap);
       int it = 0;
       bool ok = true, waited = false;
+      const uint64_t wpol = l2_evict_first_policy();  // weights are read once per step
       int pend_kb[kStages];  // k-blocks whose weight tile was issued before the previous grid finished
       int pend = 0;
       auto issue_b = [&](int stage, int kb) {
@@ -333,13 +334,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           mbar_arrive_expect_tx(&full[s], kStageBytes);
           if (p.packed_a) {  // one contiguous block per matrix
             const int tb = sg.tile * p.kbt + kb;
-            tma_load_3d(a, &amap0, &full[s], 0, 0, tb);
-            if (p.paired) tma_load_3d(a + kABytes / 2, &amap1, &full[s], 0, 0, tb);
+            tma_load_3d_hint(a, &amap0, &full[s], 0, 0, tb, wpol);
+            if (p.paired) tma_load_3d_hint(a + kABytes / 2, &amap1, &full[s], 0, 0, tb, wpol);
           } else if (p.paired) {
-            tma_load_2d(a, &amap0, &full[s], kb * BK, sg.tile * 64);
-            tma_load_2d(a + kABytes / 2, &amap1, &full[s], kb * BK, sg.tile * 64);
+            tma_load_2d_hint(a, &amap0, &full[s], kb * BK, sg.tile * 64, wpol);
+            tma_load_2d_hint(a + kABytes / 2, &amap1, &full[s], kb * BK, sg.tile * 64, wpol);
           } else {
-            tma_load_2d(a, &amap0, &full[s], kb * BK, sg.tile * BM);
+            tma_load_2d_hint(a, &amap0, &full[s], kb * BK, sg.tile * BM, wpol);
           }
           if (waited) {
             issue_b(s, kb);

@@ -91,11 +91,22 @@ class KVCache:
         return self.data[l, 1].transpose(1, 0, 2)
 
 
-class Backbone:
-    """The decoder. ``get(name)`` returns the float64 weight ``name`` (see synth.weight_names)."""
+def _exact(name, v):
+    return v
 
-    def __init__(self, dims, get):
-        self.dims, self.get = dims, get
+
+class Backbone:
+    """The decoder. ``get(name)`` returns the float64 weight ``name`` (see synth.weight_names).
+
+    ``store(name, v)`` is applied to each intermediate that a path keeps in memory between its stages: the
+    normalised projection operands ("a"), the rotated queries and keys and the values ("q", "k", "v"), the
+    attention output ("o") and the SiLU-gate product ("act"). It is the identity by default, so the oracle is
+    exact; rounding there to a storage precision measures how sensitive the model's outputs are to that
+    precision (it changes no arithmetic step).
+    """
+
+    def __init__(self, dims, get, store=_exact):
+        self.dims, self.get, self.store = dims, get, store
 
     def forward(self, tokens, positions, cache: KVCache, cache_len, block_mask):
         """Run ``tokens`` [n] at ``positions`` [n] after ``cache_len`` cached rows.
@@ -106,23 +117,24 @@ class Backbone:
         ancestor mask for a tree). Returns (h, logits): the final-normed
         hidden states [n, d] and the LM-head logits [n, V].
         """
-        D, H, g = self.dims.head_dim, self.dims.n_heads, self.get
+        D, H, g, st = self.dims.head_dim, self.dims.n_heads, self.get, self.store
         eps, n = self.dims.norm_eps, len(tokens)
         x = g("embed")[np.asarray(tokens)]
         for l in range(self.dims.n_layers):
-            a = rms_norm(x, eps)
+            a = st("a", rms_norm(x, eps))
             q = (a @ g(f"layer{l}.wq").T).reshape(n, H, D)
             k = (a @ g(f"layer{l}.wk").T).reshape(n, H, D)
             v = (a @ g(f"layer{l}.wv").T).reshape(n, H, D)
             q, k = rope(q, positions, self.dims.rope_theta), rope(k, positions, self.dims.rope_theta)
+            q, k, v = st("q", q), st("k", k), st("v", v)
             cache.k(l)[cache_len:cache_len + n] = k
             cache.v(l)[cache_len:cache_len + n] = v
-            o = tree_attention(q, cache.k(l), cache.v(l), cache_len, block_mask, 1.0 / np.sqrt(D))
+            o = st("o", tree_attention(q, cache.k(l), cache.v(l), cache_len, block_mask, 1.0 / np.sqrt(D)))
             x = x + o.reshape(n, H * D) @ g(f"layer{l}.wo").T
-            a = rms_norm(x, eps)
-            u = silu(a @ g(f"layer{l}.w_gate").T) * (a @ g(f"layer{l}.w_up").T)
+            a = st("a", rms_norm(x, eps))
+            u = st("act", silu(a @ g(f"layer{l}.w_gate").T) * (a @ g(f"layer{l}.w_up").T))
             x = x + u @ g(f"layer{l}.w_down").T
-        h = rms_norm(x, eps)
+        h = st("a", rms_norm(x, eps))
         return h, h @ g("lm_head").T
 
 

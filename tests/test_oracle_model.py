@@ -167,3 +167,27 @@ def test_backbone_layer_vs_torch_functional():
                      T(w["layer0.w_down"]))
     ref = F.rms_norm(x, (one.d,), eps=1e-5).numpy()
     assert np.allclose(h, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_backbone_store_hook_placement():
+    """The storage hook sits on the named intermediates: zeroing one of them equals zeroing the weight that
+    produces it (or the one that consumes it), and the default hook changes nothing."""
+    dims, w = _tiny_model()
+    toks, n = np.array([3, 17, 400, 9]), 4
+
+    def run(weights, store=None):
+        m = Backbone(dims, weights.__getitem__) if store is None else Backbone(dims, weights.__getitem__, store)
+        return m.forward(toks, np.arange(n), KVCache(dims, 8), 0, chain_mask(n))[1]
+
+    base = run(w)
+    assert np.array_equal(run(w, lambda name, v: v), base)
+    for name, zeroed in (("o", "wo"), ("v", "wo"), ("act", "w_down")):
+        wz = dict(w)
+        for l in range(dims.n_layers):
+            wz[f"layer{l}.{zeroed}"] = np.zeros_like(w[f"layer{l}.{zeroed}"])
+        got = run(w, lambda nm, v, name=name: np.zeros_like(v) if nm == name else v)
+        assert np.allclose(got, run(wz), rtol=1e-12, atol=1e-13), name
+    # rounding the stored intermediates to bf16 moves the tiny model's logits by a small, nonzero amount
+    bf = lambda nm, v: torch.tensor(v).to(torch.bfloat16).double().numpy()
+    rel = np.linalg.norm(run(w, bf) - base) / np.linalg.norm(base)
+    assert 1e-5 < rel < 2e-2, rel
