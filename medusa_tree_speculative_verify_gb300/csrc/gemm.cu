@@ -36,8 +36,7 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kEpiThreads = 128;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kTmemCols = 2 * BN;
-constexpr int kPitch = BN + 1;  // staging row pitch (floats)
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)BM * kPitch * 4 + 256;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)BM * BN * 4 + 256;
 
 // kind::f16 instruction descriptor: D fp32, A/B bf16, both K-major, N = 64, M = 128.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
@@ -176,90 +175,150 @@ MV_DEV void load_epi_const(const GemmParams& p, EpiConst* ec, int i) {
   epi_bar();
 }
 
-// The finished 128 x 64 accumulator tile is in the staging buffer (row i = weight row, column j = token,
-// pitch kPitch). Every epilogue is a short rolled loop over it: the code stays small, which matters because
-// it first runs at the very end of the kernel, and it needs no register arrays indexed at run time.
+// ---- token-major epilogue: thread (warp w, lane l) owns rows 4l..4l+3 of the tile for tokens j = w + 4t
+// (t = 0..15), so every global access of the epilogue is one 16-byte (fp32) or 8-byte (bf16) vector per lane and
+// a warp covers one token's 128 contiguous rows. Partner rows (RoPE d +- D/2, SwiGLU gate/up) sit in lane l ^ k.
+constexpr int kTokPerThread = BN / 4;
+
+MV_DEV void add4(float4& a, const float4& b) {
+  a.x += b.x;
+  a.y += b.y;
+  a.z += b.z;
+  a.w += b.w;
+}
+MV_DEV float4 shfl_xor4(const float4& v, int m) {
+  return make_float4(__shfl_xor_sync(0xffffffffu, v.x, m), __shfl_xor_sync(0xffffffffu, v.y, m),
+                     __shfl_xor_sync(0xffffffffu, v.z, m), __shfl_xor_sync(0xffffffffu, v.w, m));
+}
+MV_DEV uint2 pack_bf16x4(float a, float b, float c, float d) {
+  const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+                      ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+  const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(c)) |
+                      ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d)) << 16);
+  return make_uint2(lo, hi);
+}
+// SiLU for a bf16 result: hardware exp2 and an approximate divide (relative error far below bf16's 2^-9).
+MV_DEV float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+// sin and cos of a rotary angle (at most a few thousand radians): Cody-Waite reduction by 2*pi split into a float
+// and its remainder, then the hardware sine/cosine on [-pi, pi] (absolute error about 1e-6, below bf16's step).
+MV_DEV void rope_sincos(float a, float* s, float* c) {
+  const float k = rintf(a * 0.159154943091895336f);  // 1 / (2 pi)
+  float r = fmaf(-k, 6.28318548202514648f, a);       // float(2 pi)
+  r = fmaf(-k, -1.74845553146951715e-7f, r);         // 2 pi - float(2 pi)
+  __sincosf(r, s, c);
+}
+
+// acc[t] holds token j = w + 4t (rows 4l..4l+3, already summed over every K contributor). Writes the outputs of
+// the launch's epilogue kind.
 template <int EPI>
-MV_DEV void final_epilogue(const GemmParams& p, int tile, int i, float* stg, const EpiConst* ec) {
-  const float* s_scale = ec->scale;
+MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, float4 (&acc)[kTokPerThread],
+                           const EpiConst* ec) {
   const int ntok = p.n_tok;
-  const float* row = stg + i * kPitch;
   if constexpr (EPI == EPI_STORE) {
-    const int R = tile * BM + i;
-    if (R < p.M) {
-#pragma unroll 4
-      for (int j = 0; j < ntok; ++j) p.out_f32[(size_t)j * p.ld_out + R] = row[j] * s_scale[j];
+    const int R = tile * BM + 4 * l;
+    const bool vec = ((reinterpret_cast<uintptr_t>(p.out_f32) & 15) == 0) && ((p.ld_out & 3) == 0) && R + 3 < p.M;
+#pragma unroll
+    for (int t = 0; t < kTokPerThread; ++t) {
+      const int j = w + 4 * t;
+      if (j >= ntok || R >= p.M) continue;
+      const float s = ec->scale[j];
+      const float4 v = make_float4(acc[t].x * s, acc[t].y * s, acc[t].z * s, acc[t].w * s);
+      float* o = p.out_f32 + (size_t)j * p.ld_out + R;
+      if (vec) {
+        *reinterpret_cast<float4*>(o) = v;
+      } else {
+        o[0] = v.x;
+        if (R + 1 < p.M) o[1] = v.y;
+        if (R + 2 < p.M) o[2] = v.z;
+        if (R + 3 < p.M) o[3] = v.w;
+      }
     }
   } else if constexpr (EPI == EPI_RESIDUAL) {
-    const int R = tile * BM + i;
-    float* srow = stg + i * kPitch;
-    if (R < p.M) {
-      float xo[BN];  // every residual load in flight before the first use
+    // M is a multiple of 4 (host check): a lane's 4 rows are all valid or all past the end
+    const int R = tile * BM + 4 * l;
+    const bool valid = R < p.M;
+    float4 xo[kTokPerThread];
 #pragma unroll
-      for (int j = 0; j < BN; ++j) xo[j] = j < ntok ? __ldcg(p.x + (size_t)j * p.M + R) : 0.0f;
-#pragma unroll
-      for (int j = 0; j < BN; ++j) {
-        if (j < ntok) {
-          const float xn = xo[j] + srow[j];
-          p.x[(size_t)j * p.M + R] = xn;
-          p.xb[(size_t)j * p.M + R] = __bfloat16_as_ushort(__float2bfloat16_rn(xn));
-          srow[j] = xn * xn;
-        }
-      }
-    } else {
-      for (int j = 0; j < ntok; ++j) srow[j] = 0.0f;
+    for (int t = 0; t < kTokPerThread; ++t) {  // every residual load in flight before the first use
+      const int j = w + 4 * t;
+      xo[t] = (valid && j < ntok) ? __ldcg(reinterpret_cast<const float4*>(p.x + (size_t)j * p.M + R))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    epi_bar();
-    if (i < ntok) {  // per-token sum of squares over the tile's rows (input of the next RMSNorm)
-      float sum = 0.0f;
-#pragma unroll 8
-      for (int r = 0; r < BM; ++r) sum += stg[r * kPitch + i];
-      p.ssq_out[tile * BN + i] = sum;
+#pragma unroll
+    for (int t = 0; t < kTokPerThread; ++t) {
+      const int j = w + 4 * t;
+      if (j >= ntok) continue;  // uniform over the warp
+      float4 xn = xo[t];
+      add4(xn, acc[t]);
+      float sq = 0.0f;
+      if (valid) {
+        *reinterpret_cast<float4*>(p.x + (size_t)j * p.M + R) = xn;
+        *reinterpret_cast<uint2*>(p.xb + (size_t)j * p.M + R) = pack_bf16x4(xn.x, xn.y, xn.z, xn.w);
+        sq = (xn.x * xn.x + xn.y * xn.y) + (xn.z * xn.z + xn.w * xn.w);
+      }
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, m);
+      if (l == 0) p.ssq_out[tile * BN + j] = sq;  // per-token sum of squares over the tile's rows
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
-    // rows 0..63: gate, rows 64..127: the matching up rows
-    const int f = tile * 64 + i;
-    if (i < 64 && f < p.F) {
-      const float* up = stg + (i + 64) * kPitch;
-#pragma unroll 4
-      for (int j = 0; j < ntok; ++j) {
-        const float s = s_scale[j];
-        p.act[(size_t)j * p.F + f] = __bfloat16_as_ushort(__float2bfloat16_rn(silu(row[j] * s) * (up[j] * s)));
+    // lanes 0..15: gate rows 4l..4l+3 (features f0 + 4l ..); lanes 16..31: the matching up rows
+    const int f = tile * 64 + 4 * l;
+#pragma unroll
+    for (int t = 0; t < kTokPerThread; ++t) {
+      const int j = w + 4 * t;
+      if (j >= ntok) continue;  // uniform over the warp
+      const float4 up = shfl_xor4(acc[t], 16);
+      if (l < 16 && f < p.F) {
+        const float s = ec->scale[j];
+        const float4 g = acc[t];
+        *reinterpret_cast<uint2*>(p.act + (size_t)j * p.F + f) =
+            pack_bf16x4(silu_fast(g.x * s) * (up.x * s), silu_fast(g.y * s) * (up.y * s),
+                        silu_fast(g.z * s) * (up.z * s), silu_fast(g.w * s) * (up.w * s));
       }
     }
   } else if constexpr (EPI == EPI_QKV) {
-    const int R = tile * BM + i;
-    if (R < p.M) {
-      const int HD = p.H * p.D;
-      const int which = R / HD, within = R % HD, head = within / p.D, dim = within % p.D;
-      const int half = p.D >> 1;
-      const int kv_row0 = ec->kv_row0;  // prefix length: the tree block's keys/values go to rows kv_row0 + j
-      const float* prow = stg + (dim < half ? i + half : i - half) * kPitch;  // RoPE partner (same head)
-      const float inv_freq = exp2f(-(float)(2 * (dim % half)) / (float)p.D * p.log2_theta);
-      uint16_t* dst;
-      size_t stride;
-      if (which == 0) {
-        dst = p.q_out + (size_t)head * p.D + dim;
-        stride = (size_t)p.H * p.D;
-      } else {
-        const size_t plane = (size_t)p.layer * 2 + (which - 1);
-        dst = p.kv + ((plane * p.H + head) * p.S_max + kv_row0) * p.D + dim;
-        stride = (size_t)p.D;
-      }
-#pragma unroll 2
-      for (int j = 0; j < ntok; ++j) {
-        float val = row[j] * s_scale[j];
-        if (which < 2) {
-          const float pv = prow[j] * s_scale[j];
+    // a tile holds whole heads (D divides 128); rows = [q heads | k heads | v heads] x D
+    const int R = tile * BM + 4 * l;
+    const bool valid = R < p.M;
+    const int HD = p.H * p.D;
+    const int which = R / HD, within = R % HD, head = within / p.D, dim = within % p.D;
+    const int half = p.D >> 1;
+    const bool lo = dim < half;
+    float inv_freq[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      inv_freq[q] = exp2f(-(float)(2 * ((dim + q) % half)) / (float)p.D * p.log2_theta);
+    uint16_t* dst;
+    size_t stride;
+    if (which == 0) {
+      dst = p.q_out + (size_t)head * p.D + dim;
+      stride = (size_t)p.H * p.D;
+    } else {
+      const size_t plane = (size_t)p.layer * 2 + (which - 1);
+      dst = p.kv + ((plane * p.H + head) * p.S_max + ec->kv_row0) * p.D + dim;
+      stride = (size_t)p.D;
+    }
+#pragma unroll
+    for (int t = 0; t < kTokPerThread; ++t) {
+      const int j = w + 4 * t;
+      if (j >= ntok) continue;  // uniform over the warp
+      const float4 pr = shfl_xor4(acc[t], p.D >> 3);  // the RoPE partner rows (dim -+ D/2, same head)
+      if (!valid) continue;
+      const float s = ec->scale[j];
+      float v[4] = {acc[t].x * s, acc[t].y * s, acc[t].z * s, acc[t].w * s};
+      if (which < 2) {
+        const float pv[4] = {pr.x * s, pr.y * s, pr.z * s, pr.w * s};
+        const float pos = (float)ec->pos[j];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
           float sn, cs;
-          sincosf((float)ec->pos[j] * inv_freq, &sn, &cs);
-          val = dim < half ? val * cs - pv * sn : val * cs + pv * sn;
+          rope_sincos(pos * inv_freq[q], &sn, &cs);
+          v[q] = lo ? v[q] * cs - pv[q] * sn : v[q] * cs + pv[q] * sn;
         }
-        dst[(size_t)j * stride] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
       }
+      *reinterpret_cast<uint2*>(dst + (size_t)j * stride) = pack_bf16x4(v[0], v[1], v[2], v[3]);
     }
   }
-  epi_bar();  // the staging buffer is reused by the next segment
 }
 
 template <int EPI>
@@ -404,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int i = sub * 32 + lane;      // tile row = TMEM lane
     pdl_wait();                         // the epilogue reads what earlier kernels wrote
     load_epi_const(p, &s_ec, i);        // scales and positions: the same for every tile of this launch
+    const int ntok = p.n_tok;
     Seg sg;
     for (int si = 0; get_seg(cta, si, p, sg); ++si) {
       const int buf = si & 1, rr = si >> 1;
@@ -414,53 +474,70 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         break;
       }
       tc_fence_after();
-      float v[BN];
-      const uint32_t ta = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(buf * BN);
-      tmem_ld32(ta, v);
-      tmem_ld32(ta + 32, v + 32);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
-
-      const bool whole = sg.kb0 == 0 && sg.kb1 == p.kbt;
-      float* srow = stg + i * kPitch;
-      if (whole) {
+      {
+        float v[BN];
+        const uint32_t ta = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(buf * BN);
+        tmem_ld32(ta, v);
+        tmem_ld32(ta + 32, v + 32);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+        // token-major stage: stg[j][row], conflict-free (consecutive rows in consecutive lanes)
 #pragma unroll
-        for (int j = 0; j < BN; ++j) srow[j] = v[j];
-      } else {
-        // stream-K: publish this CTA's partial tile; the last contributor sums all of them in contributor
-        // order (the same order whichever CTA is last, so the result is deterministic)
-        float* slot = partial_slot(cta, sg.tile, p);
-#pragma unroll
-        for (int j = 0; j < BN; ++j) slot[j * BM + i] = v[j];
-        __threadfence();
-        epi_bar();
-        if (i == 0) {
-          const int c0 = first_contributor(sg.tile, p);
-          int c1 = c0;
-          while (c1 + 1 < p.grid && unit_begin(c1 + 1, p) < (long long)(sg.tile + 1) * p.kbt) ++c1;
-          s_last = atomicAdd(p.tickets + sg.tile, 1u) == (unsigned)(c1 - c0);
-        }
-        epi_bar();
-        if (!s_last) continue;
-        __threadfence();
-        const int c0 = first_contributor(sg.tile, p);
-        // all 64 loads of a contributor in flight at once: at the end of the kernel every dependent round
-        // trip to L2 costs about a microsecond
-#pragma unroll
-        for (int j = 0; j < BN; ++j) v[j] = 0.0f;
-        for (int c = c0; c < p.grid && unit_begin(c, p) < (long long)(sg.tile + 1) * p.kbt; ++c) {
-          const float* ps = partial_slot(c, sg.tile, p) + i;
-#pragma unroll
-          for (int j = 0; j < BN; ++j) v[j] += __ldcg(ps + j * BM);
-        }
-#pragma unroll
-        for (int j = 0; j < BN; ++j) srow[j] = v[j];
-        if (i == 0) p.tickets[sg.tile] = 0u;
+        for (int j = 0; j < BN; ++j) stg[j * BM + i] = v[j];
       }
       epi_bar();
-      final_epilogue<EPI>(p, sg.tile, i, stg, &s_ec);
+      const float4* st4 = reinterpret_cast<const float4*>(stg) + lane;  // + j * (BM / 4)
+      float4 acc[kTokPerThread];
+      const bool whole = sg.kb0 == 0 && sg.kb1 == p.kbt;
+      if (whole) {
+#pragma unroll
+        for (int t = 0; t < kTokPerThread; ++t) acc[t] = st4[(sub + 4 * t) * (BM / 4)];
+      } else {
+        // stream-K: publish this CTA's partial tile (token-major, 16-byte vectors); the last contributor sums
+        // all of them in contributor order (the same order whichever CTA is last: deterministic)
+        float4* slot = reinterpret_cast<float4*>(partial_slot(cta, sg.tile, p)) + lane;
+#pragma unroll
+        for (int t = 0; t < kTokPerThread; ++t) {
+          const int j = sub + 4 * t;
+          if (j < ntok) slot[j * (BM / 4)] = st4[j * (BM / 4)];
+        }
+        __threadfence();
+        epi_bar();
+        const int c0 = first_contributor(sg.tile, p);
+        int c1 = c0;
+        while (c1 + 1 < p.grid && unit_begin(c1 + 1, p) < (long long)(sg.tile + 1) * p.kbt) ++c1;
+        if (i == 0) s_last = atomicAdd(p.tickets + sg.tile, 1u) == (unsigned)(c1 - c0);
+        epi_bar();
+        if (!s_last) continue;  // the stage is rewritten only after the next segment's epi_bar
+        __threadfence();
+#pragma unroll
+        for (int t = 0; t < kTokPerThread; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        // two contributors' loads in flight per round; the sum keeps contributor order
+        for (int c = c0; c <= c1; c += 2) {
+          float4 a[kTokPerThread], b[kTokPerThread];
+          const float4* pa = reinterpret_cast<const float4*>(partial_slot(c, sg.tile, p)) + lane;
+          const bool has_b = c + 1 <= c1;
+          const float4* pb =
+              reinterpret_cast<const float4*>(partial_slot(has_b ? c + 1 : c, sg.tile, p)) + lane;
+#pragma unroll
+          for (int t = 0; t < kTokPerThread; ++t) {
+            const int j = sub + 4 * t;
+            a[t] = j < ntok ? (c == cta ? st4[j * (BM / 4)] : __ldcg(pa + j * (BM / 4))) : make_float4(0.f, 0.f, 0.f, 0.f);
+            b[t] = (has_b && j < ntok) ? (c + 1 == cta ? st4[j * (BM / 4)] : __ldcg(pb + j * (BM / 4)))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int t = 0; t < kTokPerThread; ++t) {
+            add4(acc[t], a[t]);
+            add4(acc[t], b[t]);
+          }
+        }
+        if (i == 0) p.tickets[sg.tile] = 0u;
+      }
+      final_epilogue<EPI>(p, sg.tile, sub, lane, acc, &s_ec);
+      epi_bar();  // the stage is reused by the next segment
     }
   }
 
