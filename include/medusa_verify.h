@@ -198,7 +198,9 @@ mv_status kv_compact(mv_bf16* kv, int32_t L, int32_t H, int32_t S_max, int32_t D
  * out[j][r] = sum_k x[j][k] * w[r][k] for j < n, r < M (fp32 accumulate and output): the kernel every backbone
  * projection of the verify step runs, exposed with a plain-store epilogue.
  *   w device bf16 [M][K] (16-byte aligned), x device bf16 [n][K], out device fp32 [n][ld_out].
- * Limits: 1 <= n <= 64, K % 8 == 0, ld_out >= M, at most 1024 tiles of 128 rows. */
+ * Limits: 1 <= n <= 64, K % 8 == 0, ld_out >= M, at most 1024 tiles of 128 rows.
+ * workspace / ws_bytes are reserved: the kernel keeps its split-K partial sums in on-chip (distributed shared)
+ * memory, mv_linear_bf16_workspace reports 0 bytes and workspace may be null. */
 mv_status mv_linear_bf16_workspace(size_t* bytes);
 mv_status mv_linear_bf16(const mv_bf16* w, const mv_bf16* x, float* out, int32_t M, int32_t K, int32_t n,
                          int32_t ld_out, void* workspace, size_t ws_bytes, mv_stream stream);

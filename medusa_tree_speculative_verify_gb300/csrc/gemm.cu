@@ -8,10 +8,12 @@
 // TMA (128-byte swizzle, K-major), the accumulator lives in tensor memory (two 64-column buffers, so the
 // epilogue of one segment overlaps the MMAs of the next).
 //
-// Work split: persistent stream-K. The (tile, k-block) iteration space is cut into one contiguous range per
-// CTA (one CTA per SM), so every SM streams the same number of weight bytes. A tile split between CTAs is
-// summed by its last contributor (atomic ticket, no waiting) in contributor order, which keeps the result
-// deterministic, and that CTA runs the fused epilogue:
+// Work split: split-K inside a thread-block cluster. Cluster q of C CTAs owns tiles q, q + n_clusters, ...;
+// CTA rank r of the cluster streams k-blocks [r*kbt/C, (r+1)*kbt/C) of each, so the weight bytes of a tile are
+// read once. The C partial accumulators of a tile meet in distributed shared memory: each CTA writes its
+// partial (token-major fp32) into its own shared memory, signals every CTA of the cluster through a remote
+// mbarrier arrive, and then sums the C partials (in rank order: deterministic) for its own share of the tokens
+// and runs the fused epilogue on that share, so the epilogue is spread over the cluster as well:
 //   STORE    out[token][row] = acc * s[token]                    (LM head logits, plain projections)
 //   RESIDUAL x[token][row] += acc; bf16 copy; per-token sum of squares of the 128-row slice (next RMSNorm)
 //   SWIGLU   act[token][f] = SiLU(s*gate) * (s*up), tile = 64 gate rows + the same 64 up rows
@@ -36,6 +38,7 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kEpiThreads = 128;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kTmemCols = 2 * BN;
+constexpr int kMaxCluster = 8;  // CTAs per cluster (portable limit)
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)BM * BN * 4 + 256;
 
 // kind::f16 instruction descriptor: D fp32, A/B bf16, both K-major, N = 64, M = 128.
@@ -104,40 +107,51 @@ MV_DEV uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// ---------------------------------------------------------------------------------------------- stream-K
-struct Seg {
-  int tile, kb0, kb1;
-};
-MV_DEV long long unit_begin(int c, const GemmParams& p) { return (long long)c * p.units / p.grid; }
-
-// The i-th segment of CTA c; false when there is none.
-MV_DEV bool get_seg(int c, int i, const GemmParams& p, Seg& s) {
-  long long u = unit_begin(c, p);
-  const long long u1 = unit_begin(c + 1, p);
-  for (int k = 0;; ++k) {
-    if (u >= u1) return false;
-    const int tile = (int)(u / p.kbt), kb0 = (int)(u % p.kbt);
-    const int kb1 = (int)min((long long)p.kbt, kb0 + (u1 - u));
-    if (k == i) {
-      s.tile = tile;
-      s.kb0 = kb0;
-      s.kb1 = kb1;
-      return true;
-    }
-    u += kb1 - kb0;
+// ---------------------------------------------------------------------------------------------- cluster PTX
+MV_DEV uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// address of the same shared-memory object in CTA `rank` of this cluster
+MV_DEV uint32_t map_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+MV_DEV void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+MV_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded like mbar_wait; acquire at cluster scope (the arrivals come from other CTAs of the cluster)
+MV_DEV bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = mv_globaltimer();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (mv_globaltimer() - t0 > MV_WAIT_LIMIT_NS) return false;
   }
 }
-MV_DEV int first_contributor(int tile, const GemmParams& p) {
-  const long long u = (long long)tile * p.kbt;
-  int c = (int)(u * p.grid / p.units);
-  if (c >= p.grid) c = p.grid - 1;
-  while (c + 1 < p.grid && unit_begin(c + 1, p) <= u) ++c;
-  while (c > 0 && unit_begin(c, p) > u) --c;
-  return c;
+MV_DEV float4 ld_cluster_f4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
 }
-MV_DEV float* partial_slot(int c, int tile, const GemmParams& p) {
-  const int first_tile = (int)(unit_begin(c, p) / p.kbt);
-  return p.partials + ((size_t)c * 2 + (tile == first_tile ? 0 : 1)) * (BM * BN);
+// every thread of every CTA of the cluster (all paths reach it: each wait before it is bounded)
+MV_DEV void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------------------------- epilogues
@@ -208,21 +222,23 @@ MV_DEV void rope_sincos(float a, float* s, float* c) {
   __sincosf(r, s, c);
 }
 
-// acc[t] holds token j = w + 4t (rows 4l..4l+3, already summed over every K contributor). Writes the outputs of
-// the launch's epilogue kind.
+// This CTA's share of the tile: tokens j = w + 4t for t = r0, r0 + cs, ... (acc[u] holds t = r0 + u * cs, rows
+// 4l..4l+3, summed over every K slice of the cluster). Writes the outputs of the launch's epilogue kind.
 template <int EPI>
-MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, float4 (&acc)[kTokPerThread],
-                           const EpiConst* ec) {
+MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, int cs,
+                           float4 (&acc)[kTokPerThread], const EpiConst* ec) {
   const int ntok = p.n_tok;
   if constexpr (EPI == EPI_STORE) {
     const int R = tile * BM + 4 * l;
     const bool vec = ((reinterpret_cast<uintptr_t>(p.out_f32) & 15) == 0) && ((p.ld_out & 3) == 0) && R + 3 < p.M;
 #pragma unroll
-    for (int t = 0; t < kTokPerThread; ++t) {
+    for (int u = 0; u < kTokPerThread; ++u) {
+      const int t = r0 + u * cs;
+      if (t >= kTokPerThread) break;
       const int j = w + 4 * t;
       if (j >= ntok || R >= p.M) continue;
       const float s = ec->scale[j];
-      const float4 v = make_float4(acc[t].x * s, acc[t].y * s, acc[t].z * s, acc[t].w * s);
+      const float4 v = make_float4(acc[u].x * s, acc[u].y * s, acc[u].z * s, acc[u].w * s);
       float* o = p.out_f32 + (size_t)j * p.ld_out + R;
       if (vec) {
         *reinterpret_cast<float4*>(o) = v;
@@ -239,17 +255,21 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, float4 (
     const bool valid = R < p.M;
     float4 xo[kTokPerThread];
 #pragma unroll
-    for (int t = 0; t < kTokPerThread; ++t) {  // every residual load in flight before the first use
+    for (int u = 0; u < kTokPerThread; ++u) {  // every residual load in flight before the first use
+      const int t = r0 + u * cs;
+      if (t >= kTokPerThread) break;
       const int j = w + 4 * t;
-      xo[t] = (valid && j < ntok) ? __ldcg(reinterpret_cast<const float4*>(p.x + (size_t)j * p.M + R))
+      xo[u] = (valid && j < ntok) ? __ldcg(reinterpret_cast<const float4*>(p.x + (size_t)j * p.M + R))
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int t = 0; t < kTokPerThread; ++t) {
+    for (int u = 0; u < kTokPerThread; ++u) {
+      const int t = r0 + u * cs;
+      if (t >= kTokPerThread) break;
       const int j = w + 4 * t;
       if (j >= ntok) continue;  // uniform over the warp
-      float4 xn = xo[t];
-      add4(xn, acc[t]);
+      float4 xn = xo[u];
+      add4(xn, acc[u]);
       float sq = 0.0f;
       if (valid) {
         *reinterpret_cast<float4*>(p.x + (size_t)j * p.M + R) = xn;
@@ -264,13 +284,15 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, float4 (
     // lanes 0..15: gate rows 4l..4l+3 (features f0 + 4l ..); lanes 16..31: the matching up rows
     const int f = tile * 64 + 4 * l;
 #pragma unroll
-    for (int t = 0; t < kTokPerThread; ++t) {
+    for (int u = 0; u < kTokPerThread; ++u) {
+      const int t = r0 + u * cs;
+      if (t >= kTokPerThread) break;
       const int j = w + 4 * t;
       if (j >= ntok) continue;  // uniform over the warp
-      const float4 up = shfl_xor4(acc[t], 16);
+      const float4 up = shfl_xor4(acc[u], 16);
       if (l < 16 && f < p.F) {
         const float s = ec->scale[j];
-        const float4 g = acc[t];
+        const float4 g = acc[u];
         *reinterpret_cast<uint2*>(p.act + (size_t)j * p.F + f) =
             pack_bf16x4(silu_fast(g.x * s) * (up.x * s), silu_fast(g.y * s) * (up.y * s),
                         silu_fast(g.z * s) * (up.z * s), silu_fast(g.w * s) * (up.w * s));
@@ -299,13 +321,15 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, float4 (
       stride = (size_t)p.D;
     }
 #pragma unroll
-    for (int t = 0; t < kTokPerThread; ++t) {
+    for (int u = 0; u < kTokPerThread; ++u) {
+      const int t = r0 + u * cs;
+      if (t >= kTokPerThread) break;
       const int j = w + 4 * t;
       if (j >= ntok) continue;  // uniform over the warp
-      const float4 pr = shfl_xor4(acc[t], p.D >> 3);  // the RoPE partner rows (dim -+ D/2, same head)
+      const float4 pr = shfl_xor4(acc[u], p.D >> 3);  // the RoPE partner rows (dim -+ D/2, same head)
       if (!valid) continue;
       const float s = ec->scale[j];
-      float v[4] = {acc[t].x * s, acc[t].y * s, acc[t].z * s, acc[t].w * s};
+      float v[4] = {acc[u].x * s, acc[u].y * s, acc[u].z * s, acc[u].w * s};
       if (which < 2) {
         const float pv[4] = {pr.x * s, pr.y * s, pr.z * s, pr.w * s};
         const float pos = (float)ec->pos[j];
@@ -329,15 +353,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  float* stg = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], drain;
+  float* part = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);  // [BN tokens][BM rows]
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], drain, pfull, pfree;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int s_abort;
   __shared__ EpiConst s_ec;
-  __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cta = blockIdx.x;
+  const int C = p.csize;                       // CTAs per cluster = K slices per tile
+  const int rank = (int)cluster_rank();        // this CTA's K slice and token share
+  const int q0 = blockIdx.x / C, ncl = gridDim.x / C;
+  const int kb0 = rank * p.kbt / C, kb1 = (rank + 1) * p.kbt / C;
   pdl_trigger();
 
   if (threadIdx.x == 0) {
@@ -349,6 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 4);
     }
+    mbar_init(&pfull, C);  // one arrive from every CTA of the cluster: all partials of the tile written
+    mbar_init(&pfree, C);  // one arrive from every CTA of the cluster: all reads of this CTA's partial done
     mbar_init(&drain, 1);
     s_abort = 0;
     mbar_fence_init();
@@ -359,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // every CTA's barriers are initialised before the first remote arrive
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
 
@@ -381,9 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         waited = true;
         for (int q = 0; q < pend; ++q) issue_b(q, pend_kb[q]);
       };
-      Seg sg;
-      for (int si = 0; ok && get_seg(cta, si, p, sg); ++si) {
-        for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
+      for (int tile = q0; ok && tile < p.n_tiles; tile += ncl) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % kStages, r = it / kStages;
           if (s_abort || !mbar_wait(&empty[s], (uint32_t)((r & 1) ^ 1))) {
             ok = false;
@@ -392,14 +420,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           uint8_t* a = stages + (size_t)s * kStageBytes;
           mbar_arrive_expect_tx(&full[s], kStageBytes);
           if (p.packed_a) {  // one contiguous block per matrix
-            const int tb = sg.tile * p.kbt + kb;
+            const int tb = tile * p.kbt + kb;
             tma_load_3d_hint(a, &amap0, &full[s], 0, 0, tb, wpol);
             if (p.paired) tma_load_3d_hint(a + kABytes / 2, &amap1, &full[s], 0, 0, tb, wpol);
           } else if (p.paired) {
-            tma_load_2d_hint(a, &amap0, &full[s], kb * BK, sg.tile * 64, wpol);
-            tma_load_2d_hint(a + kABytes / 2, &amap1, &full[s], kb * BK, sg.tile * 64, wpol);
+            tma_load_2d_hint(a, &amap0, &full[s], kb * BK, tile * 64, wpol);
+            tma_load_2d_hint(a + kABytes / 2, &amap1, &full[s], kb * BK, tile * 64, wpol);
           } else {
-            tma_load_2d_hint(a, &amap0, &full[s], kb * BK, sg.tile * BM, wpol);
+            tma_load_2d_hint(a, &amap0, &full[s], kb * BK, tile * BM, wpol);
           }
           if (waited) {
             issue_b(s, kb);
@@ -421,19 +449,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int it = 0;
+      int it = 0, n = 0;
       bool ok = true;
-      Seg sg;
       const uint32_t st0 = smem_u32(stages);
-      for (int si = 0; ok && get_seg(cta, si, p, sg); ++si) {
-        const int buf = si & 1, rr = si >> 1;
+      for (int tile = q0; ok && tile < p.n_tiles; tile += ncl, ++n) {
+        const int buf = n & 1, rr = n >> 1;
         if (s_abort || !mbar_wait(&tempty[buf], (uint32_t)((rr & 1) ^ 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t dt = tmem_base + (uint32_t)(buf * BN);
-        for (int kb = sg.kb0; kb < sg.kb1; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % kStages, r = it / kStages;
           if (s_abort || !mbar_wait(&full[s], (uint32_t)(r & 1))) {
             ok = false;
@@ -444,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           const uint64_t ad = sw128_desc(a), bd = sw128_desc(b);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc_mma(dt, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), kIdesc, (kb > sg.kb0 || k > 0) ? 1u : 0u);
+            tc_mma(dt, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
           tc_commit(&empty[s]);
         }
         if (!ok) break;
@@ -459,18 +486,62 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
   } else {
     // ------------------------------------------------------------------ epilogue (128 threads)
+    // Pipelined over the tiles: iteration n first sums and finishes tile n-1 (its partials were published a
+    // whole tile ago, and this runs while the MMA works on tile n), then drains tile n's accumulator from TMEM
+    // into this CTA's partial buffer and signals the cluster. The last tile's finish is the only one in the tail.
     const int sub = warp & 3;           // TMEM sub-partition this warp may read
     const int i = sub * 32 + lane;      // tile row = TMEM lane
     pdl_wait();                         // the epilogue reads what earlier kernels wrote
     load_epi_const(p, &s_ec, i);        // scales and positions: the same for every tile of this launch
     const int ntok = p.n_tok;
-    Seg sg;
-    for (int si = 0; get_seg(cta, si, p, sg); ++si) {
-      const int buf = si & 1, rr = si >> 1;
-      const bool got = !s_abort && mbar_wait(&tfull[buf], (uint32_t)(rr & 1));
+    const uint32_t part_s = smem_u32(part) + (uint32_t)(lane * 16);  // + token row
+    bool ok = true;
+    // Sum the C partials of tile iteration nr (this CTA's token share, rank order) and run the fused epilogue.
+    auto finish = [&](int tile_r, int nr) {
+      const bool all = mbar_wait_cluster(&pfull, (uint32_t)(nr & 1));
+      if (epi_any(!all)) {
+        if (i == 0) mv_set_error(p.err, 11, MV_DEVERR_TIMEOUT);
+        s_abort = 1;
+        ok = false;
+        return;
+      }
+      float4 acc[kTokPerThread];
+#pragma unroll
+      for (int u = 0; u < kTokPerThread; ++u) {
+        acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int t = rank + u * C;
+        if (t >= kTokPerThread) break;
+        const int j = sub + 4 * t;
+        if (j >= ntok) continue;
+        const uint32_t off = part_s + (uint32_t)(j * BM * 4);
+        float4 part_c[kMaxCluster];
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+          if (c < C) part_c[c] = ld_cluster_f4(map_rank(off, (uint32_t)c));
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+          if (c < C) add4(acc[u], part_c[c]);
+      }
+      final_epilogue<EPI>(p, tile_r, sub, lane, rank, C, acc, &s_ec);
+      // the partials were consumed above (stores issued from them): release the buffers to their owners, one
+      // release arrive per CTA of the cluster from C lanes at once (each costs a cluster round trip)
+      epi_bar();
+      if (i < C) mbar_arrive_remote(map_rank(smem_u32(&pfree), (uint32_t)i));
+    };
+    int n = 0, prev = -1;
+    for (int tile = q0; tile < p.n_tiles; tile += ncl, ++n) {
+      if (n >= 1) {
+        finish(prev, n - 1);
+        if (!ok) break;
+      }
+      const int buf = n & 1;
+      bool got = !s_abort && mbar_wait(&tfull[buf], (uint32_t)((n >> 1) & 1));
+      // the partial buffer is free again once every CTA of the cluster has finished tile n - 1
+      if (got && n >= 1) got = mbar_wait_cluster(&pfree, (uint32_t)((n - 1) & 1));
       if (epi_any(!got)) {  // uniform over the 4 epilogue warps
         if (i == 0) mv_set_error(p.err, 10, MV_DEVERR_TIMEOUT);
         s_abort = 1;
+        ok = false;
         break;
       }
       tc_fence_after();
@@ -483,66 +554,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
-        // token-major stage: stg[j][row], conflict-free (consecutive rows in consecutive lanes)
+        // this CTA's partial, token-major: part[j][row] (consecutive rows in consecutive lanes)
 #pragma unroll
-        for (int j = 0; j < BN; ++j) stg[j * BM + i] = v[j];
+        for (int j = 0; j < BN; ++j) part[j * BM + i] = v[j];
       }
-      epi_bar();
-      const float4* st4 = reinterpret_cast<const float4*>(stg) + lane;  // + j * (BM / 4)
-      float4 acc[kTokPerThread];
-      const bool whole = sg.kb0 == 0 && sg.kb1 == p.kbt;
-      if (whole) {
-#pragma unroll
-        for (int t = 0; t < kTokPerThread; ++t) acc[t] = st4[(sub + 4 * t) * (BM / 4)];
-      } else {
-        // stream-K: publish this CTA's partial tile (token-major, 16-byte vectors); the last contributor sums
-        // all of them in contributor order (the same order whichever CTA is last: deterministic)
-        float4* slot = reinterpret_cast<float4*>(partial_slot(cta, sg.tile, p)) + lane;
-#pragma unroll
-        for (int t = 0; t < kTokPerThread; ++t) {
-          const int j = sub + 4 * t;
-          if (j < ntok) slot[j * (BM / 4)] = st4[j * (BM / 4)];
-        }
-        __threadfence();
-        epi_bar();
-        const int c0 = first_contributor(sg.tile, p);
-        int c1 = c0;
-        while (c1 + 1 < p.grid && unit_begin(c1 + 1, p) < (long long)(sg.tile + 1) * p.kbt) ++c1;
-        if (i == 0) s_last = atomicAdd(p.tickets + sg.tile, 1u) == (unsigned)(c1 - c0);
-        epi_bar();
-        if (!s_last) continue;  // the stage is rewritten only after the next segment's epi_bar
-        __threadfence();
-#pragma unroll
-        for (int t = 0; t < kTokPerThread; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-        // two contributors' loads in flight per round; the sum keeps contributor order
-        for (int c = c0; c <= c1; c += 2) {
-          float4 a[kTokPerThread], b[kTokPerThread];
-          const float4* pa = reinterpret_cast<const float4*>(partial_slot(c, sg.tile, p)) + lane;
-          const bool has_b = c + 1 <= c1;
-          const float4* pb =
-              reinterpret_cast<const float4*>(partial_slot(has_b ? c + 1 : c, sg.tile, p)) + lane;
-#pragma unroll
-          for (int t = 0; t < kTokPerThread; ++t) {
-            const int j = sub + 4 * t;
-            a[t] = j < ntok ? (c == cta ? st4[j * (BM / 4)] : __ldcg(pa + j * (BM / 4))) : make_float4(0.f, 0.f, 0.f, 0.f);
-            b[t] = (has_b && j < ntok) ? (c + 1 == cta ? st4[j * (BM / 4)] : __ldcg(pb + j * (BM / 4)))
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-          for (int t = 0; t < kTokPerThread; ++t) {
-            add4(acc[t], a[t]);
-            add4(acc[t], b[t]);
-          }
-        }
-        if (i == 0) p.tickets[sg.tile] = 0u;
-      }
-      final_epilogue<EPI>(p, sg.tile, sub, lane, acc, &s_ec);
-      epi_bar();  // the stage is reused by the next segment
+      epi_bar();  // the CTA's writes are ordered before the cluster-scope release arrives below
+      if (i < C) mbar_arrive_remote(map_rank(smem_u32(&pfull), (uint32_t)i));
+      prev = tile;
     }
+    if (ok && n >= 1) finish(prev, n - 1);
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // no CTA leaves while another CTA of its cluster may still read its shared memory
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
@@ -551,23 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
 }  // namespace
 
+
 size_t gemm_smem_bytes() { return kSmemBytes; }
-
-int gemm_grid(int units) {
-  const int sms = mv_sm_count();
-  return units < sms ? units : sms;
-}
-
-size_t gemm_ws_bytes() {
-  const int sms = mv_sm_count();
-  return (size_t)sms * 2 * BM * BN * sizeof(float) + kGemmMaxTiles * sizeof(unsigned int) + 256;
-}
-
-void gemm_ws_layout(void* ws, float** partials, unsigned int** tickets) {
-  char* p = static_cast<char*>(ws);
-  *tickets = reinterpret_cast<unsigned int*>(p);
-  *partials = reinterpret_cast<float*>(p + ((kGemmMaxTiles * sizeof(unsigned int) + 255) & ~size_t(255)));
-}
 
 bool gemm_weight_map(CUtensorMap* map, const void* w, int rows, int K, int box_rows) {
   const uint64_t dims[2] = {(uint64_t)K, (uint64_t)rows};
@@ -594,25 +604,88 @@ bool gemm_act_map(CUtensorMap* map, const void* x, int rows, int K) {
                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// Clusters of c CTAs (one CTA per SM) that can be resident at once on this device, c = 1..kMaxCluster; 0 when
+// the size cannot be launched. Asked once per device and size.
+int gemm_max_clusters(int c) {
+  static int cache[64][kMaxCluster + 1];  // 0 = not asked yet, -1 = not launchable
+  const int dev = mv_device();
+  if (dev < 0 || dev >= 64 || c < 1 || c > kMaxCluster) return 0;
+  int& slot = cache[dev][c];
+  if (slot == 0) {
+    static int flags[64] = {0};
+    int n = 0;
+    if (mv_set_smem_once((const void*)gemm_kernel<EPI_STORE>, (int)kSmemBytes, flags)) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(c * mv_sm_count());
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = kSmemBytes;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = c;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<EPI_STORE>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+    }
+    slot = n > 0 ? n : -1;
+  }
+  return slot > 0 ? slot : 0;
+}
+
+// Cluster size and count for n_tiles tiles of kbt k-blocks: the smallest largest per-CTA share of k-blocks,
+// ceil(tiles per cluster) * ceil(kbt / c), with all clusters resident at once (ties: the smaller cluster).
 void gemm_finish_params(GemmParams& p) {
   p.kbt = (p.K + BK - 1) / BK;
   p.n_tiles = p.paired ? (p.F + 63) / 64 : (p.M + BM - 1) / BM;
-  p.units = p.n_tiles * p.kbt;
-  p.grid = gemm_grid(p.units);
+  long long best = -1;
+  p.csize = 1;
+  p.n_clusters = p.n_tiles < mv_sm_count() ? p.n_tiles : mv_sm_count();
+  for (int c = 1; c <= kMaxCluster && c <= p.kbt; ++c) {
+    const int mc = gemm_max_clusters(c);
+    if (mc < 1) continue;
+    const int ncl = mc < p.n_tiles ? mc : p.n_tiles;
+    const long long cost = (long long)((p.n_tiles + ncl - 1) / ncl) * ((p.kbt + c - 1) / c);
+    if (best < 0 || cost < best) {
+      best = cost;
+      p.csize = c;
+      p.n_clusters = ncl;
+    }
+  }
+  p.grid = p.csize * p.n_clusters;
 }
 
 mv_status launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                       const GemmParams& p, cudaStream_t stream) {
   if (p.n_tiles > kGemmMaxTiles || p.n_tok < 1 || p.n_tok > BN) return MV_ERR_SHAPE;
-  const size_t smem = kSmemBytes;
+  if (p.csize < 1 || p.csize > kMaxCluster || p.n_clusters < 1 || p.grid != p.csize * p.n_clusters ||
+      p.csize > p.kbt)
+    return MV_ERR_INVALID_ARG;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = p.csize;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = mv_pdl_enabled() ? 2 : 1;
+  cudaError_t e;
   switch (epi) {
-#define MV_GEMM_CASE(E)                                                                                          \
-  case E: {                                                                                                      \
-    static int flags[64] = {0};                                                                                  \
-    if (!mv_set_smem_once((const void*)gemm_kernel<E>, (int)smem, flags)) return MV_ERR_CUDA;                    \
-    if (mv_launch(gemm_kernel<E>, dim3(p.grid), dim3(kThreads), smem, stream, a0, a1, b, p) != cudaSuccess)     \
-      return MV_ERR_CUDA;                                                                                        \
-    break;                                                                                                       \
+#define MV_GEMM_CASE(E)                                                                        \
+  case E: {                                                                                    \
+    static int flags[64] = {0};                                                                \
+    if (!mv_set_smem_once((const void*)gemm_kernel<E>, (int)kSmemBytes, flags)) return MV_ERR_CUDA; \
+    e = cudaLaunchKernelEx(&cfg, gemm_kernel<E>, a0, a1, b, p);                                \
+    break;                                                                                     \
   }
     MV_GEMM_CASE(EPI_STORE)
     MV_GEMM_CASE(EPI_RESIDUAL)
@@ -622,15 +695,17 @@ mv_status launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, con
     default:
       return MV_ERR_INVALID_ARG;
   }
+  if (e != cudaSuccess) return MV_ERR_CUDA;
   return mv_last_launch("gemm");
 }
 
 // out[n][ld] (fp32) = X[n][K] . W[M][K]^T, optionally scaled per row of X by 1/sqrt(mean(x^2)+eps) of x_f32.
 extern "C" mv_status mv_linear_bf16(const mv_bf16* w, const mv_bf16* x, float* out, int32_t M, int32_t K,
                                     int32_t n, int32_t ld_out, void* workspace, size_t ws_bytes, mv_stream stream) {
-  if (!w || !x || !out || !workspace) return MV_ERR_INVALID_ARG;
+  (void)workspace;  // reserved: the kernel needs no global scratch
+  (void)ws_bytes;
+  if (!w || !x || !out) return MV_ERR_INVALID_ARG;
   if (M < 1 || K < 8 || (K & 7) || n < 1 || n > BN || ld_out < M) return MV_ERR_SHAPE;
-  if (ws_bytes < gemm_ws_bytes()) return MV_ERR_CAPACITY;
   if ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(x)) & 15) return MV_ERR_SHAPE;
   CUtensorMap a, b;
   if (!gemm_weight_map(&a, w, M, K, BM) || !gemm_act_map(&b, x, n, K)) return MV_ERR_CUDA;
@@ -641,7 +716,6 @@ extern "C" mv_status mv_linear_bf16(const mv_bf16* w, const mv_bf16* x, float* o
   p.out_f32 = out;
   p.ld_out = ld_out;
   p.err = mv_error_word();
-  gemm_ws_layout(workspace, &p.partials, &p.tickets);
   gemm_finish_params(p);
   return launch_gemm(EPI_STORE, a, a, b, p, static_cast<cudaStream_t>(stream));
 }
@@ -650,9 +724,10 @@ extern "C" mv_status mv_linear_bf16(const mv_bf16* w, const mv_bf16* x, float* o
 extern "C" mv_status mv_linear_bf16_packed(const mv_bf16* w_packed, const mv_bf16* x, float* out, int32_t M,
                                            int32_t K, int32_t n, int32_t ld_out, void* workspace, size_t ws_bytes,
                                            mv_stream stream) {
-  if (!w_packed || !x || !out || !workspace) return MV_ERR_INVALID_ARG;
+  (void)workspace;  // reserved: the kernel needs no global scratch
+  (void)ws_bytes;
+  if (!w_packed || !x || !out) return MV_ERR_INVALID_ARG;
   if (M < 1 || K < 8 || (K & 7) || n < 1 || n > BN || ld_out < M) return MV_ERR_SHAPE;
-  if (ws_bytes < gemm_ws_bytes()) return MV_ERR_CAPACITY;
   if ((reinterpret_cast<uintptr_t>(w_packed) | reinterpret_cast<uintptr_t>(x)) & 15) return MV_ERR_SHAPE;
   CUtensorMap a, b;
   if (!gemm_weight_map_packed(&a, w_packed, M, K, BM) || !gemm_act_map(&b, x, n, K)) return MV_ERR_CUDA;
@@ -664,13 +739,12 @@ extern "C" mv_status mv_linear_bf16_packed(const mv_bf16* w_packed, const mv_bf1
   p.out_f32 = out;
   p.ld_out = ld_out;
   p.err = mv_error_word();
-  gemm_ws_layout(workspace, &p.partials, &p.tickets);
   gemm_finish_params(p);
   return launch_gemm(EPI_STORE, a, a, b, p, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" mv_status mv_linear_bf16_workspace(size_t* bytes) {
   if (!bytes) return MV_ERR_INVALID_ARG;
-  *bytes = gemm_ws_bytes();
+  *bytes = 0;  // reserved
   return MV_OK;
 }

@@ -12,11 +12,8 @@ struct GemmParams {
   int n_tok;     // valid token columns (1..64)
   int paired;    // SWIGLU: tile = 64 rows of amap0 (gate) + the same 64 rows of amap1 (up)
   int packed_a;  // weights in the [row tile][k-block][rows][64] layout (3-D maps, one contiguous box per load)
-  // derived (gemm_finish_params)
-  int kbt, n_tiles, units, grid;
-  // stream-K workspace
-  float* partials;
-  unsigned int* tickets;
+  // derived (gemm_finish_params): k-blocks, tiles, CTAs per cluster (K slices per tile), clusters, CTAs
+  int kbt, n_tiles, csize, n_clusters, grid;
   // RMSNorm scale of the input columns: s = 1/sqrt(sum(ssq[0..ssq_parts)) / norm_d + eps); null = 1
   const float* ssq;
   int ssq_parts, norm_d;
@@ -42,8 +39,6 @@ struct GemmParams {
 };
 
 size_t gemm_smem_bytes();
-size_t gemm_ws_bytes();
-void gemm_ws_layout(void* ws, float** partials, unsigned int** tickets);
 bool gemm_weight_map(CUtensorMap* map, const void* w, int rows, int K, int box_rows);
 bool gemm_weight_map_packed(CUtensorMap* map, const void* w, int rows, int K, int tile_rows);
 bool gemm_act_map(CUtensorMap* map, const void* x, int rows, int K);

@@ -143,7 +143,6 @@ struct mv_session {
   uint16_t* act;
   float* logits;
   int ld_logits;
-  void* ws_gemm;
   void* ws_attn;
   void* ws_post;
   void* ws_heads;
@@ -195,7 +194,7 @@ struct ProfScope {
 namespace {
 
 struct SessionLayout {
-  size_t state, tree_tokens, cart, x, xb, ssq, q, attn, act, logits, gemm, attn_ws, post, heads, total;
+  size_t state, tree_tokens, cart, x, xb, ssq, q, attn, act, logits, attn_ws, post, heads, total;
 };
 
 SessionLayout session_layout(const mv_model_dims& d, int s_max, int topk) {
@@ -218,7 +217,6 @@ SessionLayout session_layout(const mv_model_dims& d, int s_max, int topk) {
   L.attn = take((size_t)kTok * HD * 2);
   L.act = take((size_t)kTok * d.ffn * 2);
   L.logits = take((size_t)kTok * ldl * 4);
-  L.gemm = take(gemm_ws_bytes());
   L.attn_ws = take(tree_attn_ws_bytes(d.n_heads, d.head_dim, s_max, kTok));
   L.post = take(posterior_ws_bytes(kTok));
   L.heads = take(heads_ws_bytes(1, d.d, d.n_medusa, d.vocab, topk));
@@ -242,7 +240,6 @@ GemmParams base_params(const mv_session* s, int n_tok) {
   p.packed_a = s->model->packed;
   p.eps = s->model->dims.norm_eps;
   p.err = mv_error_word();
-  gemm_ws_layout(s->ws_gemm, &p.partials, &p.tickets);
   return p;
 }
 
@@ -442,7 +439,6 @@ extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16
   s->act = reinterpret_cast<uint16_t*>(b + L.act);
   s->logits = reinterpret_cast<float*>(b + L.logits);
   s->ld_logits = (d.vocab + 3) & ~3;
-  s->ws_gemm = b + L.gemm;
   s->ws_attn = b + L.attn_ws;
   s->ws_post = b + L.post;
   s->ws_heads = b + L.heads;
