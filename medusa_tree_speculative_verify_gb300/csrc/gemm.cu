@@ -8,7 +8,7 @@
 // TMA (128-byte swizzle, K-major), the accumulator lives in tensor memory (two 64-column buffers, so the
 // epilogue of one segment overlaps the MMAs of the next).
 //
-// Work split: split-K inside a thread-block cluster. Cluster q of C CTAs owns tiles q, q + n_clusters, ...;
+// Work split: split-K inside a thread-block cluster. Cluster q of C CTAs owns a contiguous range of tiles;
 // CTA rank r of the cluster streams k-blocks [r*kbt/C, (r+1)*kbt/C) of each, so the weight bytes of a tile are
 // read once. The C partial accumulators of a tile meet in distributed shared memory: each CTA writes its
 // partial (token-major fp32) into its own shared memory, signals every CTA of the cluster through a remote
@@ -362,8 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = p.csize;                       // CTAs per cluster = K slices per tile
   const int rank = (int)cluster_rank();        // this CTA's K slice and token share
-  const int q0 = blockIdx.x / C, ncl = gridDim.x / C;
-  const int kb0 = rank * p.kbt / C, kb1 = (rank + 1) * p.kbt / C;
+  // cluster q owns the contiguous tiles [t0, t1): consecutive tiles are adjacent in the packed weight layout
+  const int q = blockIdx.x / C, ncl = gridDim.x / C;
+  const int t0 = (int)((long long)q * p.n_tiles / ncl), t1 = (int)((long long)(q + 1) * p.n_tiles / ncl);
+  const int kb0 = rank * p.kbt / C, kb1 = (rank + 1) * p.kbt / C;  // this CTA's K slice
   pdl_trigger();
 
   if (threadIdx.x == 0) {
@@ -410,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         waited = true;
         for (int q = 0; q < pend; ++q) issue_b(q, pend_kb[q]);
       };
-      for (int tile = q0; ok && tile < p.n_tiles; tile += ncl) {
+      for (int tile = t0; ok && tile < t1; ++tile) {
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % kStages, r = it / kStages;
           if (s_abort || !mbar_wait(&empty[s], (uint32_t)((r & 1) ^ 1))) {
@@ -452,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       int it = 0, n = 0;
       bool ok = true;
       const uint32_t st0 = smem_u32(stages);
-      for (int tile = q0; ok && tile < p.n_tiles; tile += ncl, ++n) {
+      for (int tile = t0; ok && tile < t1; ++tile, ++n) {
         const int buf = n & 1, rr = n >> 1;
         if (s_abort || !mbar_wait(&tempty[buf], (uint32_t)((rr & 1) ^ 1))) {
           ok = false;
@@ -529,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       if (i < C) mbar_arrive_remote(map_rank(smem_u32(&pfree), (uint32_t)i));
     };
     int n = 0, prev = -1;
-    for (int tile = q0; tile < p.n_tiles; tile += ncl, ++n) {
+    for (int tile = t0; tile < t1; ++tile, ++n) {
       if (n >= 1) {
         finish(prev, n - 1);
         if (!ok) break;
