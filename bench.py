@@ -49,7 +49,8 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms while running; the sampler is started (and its
+    first sample awaited) before the timed region, and only the samples taken inside it are summarised."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -61,7 +62,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -75,6 +76,18 @@ class ClockSampler:
             if len(parts) == 7:
                 self.rows.append(parts)
 
+    def ready(self, timeout=5.0):
+        """Wait for the first sample (nvidia-smi takes a moment to start), then mark where the timed region begins."""
+        t0 = time.time()
+        while self.proc is not None and not self.rows and time.time() - t0 < timeout:
+            time.sleep(0.01)
+        self.mark = len(self.rows)
+        return self
+
+    def stop(self):
+        """End of the timed region: later samples are ignored."""
+        self.end = len(self.rows)
+
     def __exit__(self, *a):
         if self.proc is not None:
             self.proc.terminate()
@@ -84,6 +97,10 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        lo = getattr(self, "mark", 0)
+        hi = getattr(self, "end", len(self.rows))
+        rows = self.rows[lo:hi] if hi > lo else self.rows[lo:lo + 1]
+        self.rows = rows
         if not self.rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
@@ -209,10 +226,12 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        clk.ready()
         start.record(stream)
         sess.steps_graph(args.steps, prm)
         end.record(stream)
         torch.cuda.synchronize()
+        clk.stop()
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(end), world)
     r = sess.read_result()
@@ -273,7 +292,10 @@ def run_gpu(args, world, rank, local):
     achieved = g_bytes / (g_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": "gemm_kernel (tcgen05 projections: QKV, O, gate/up, down, LM head)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
-                "traffic": None, "algorithmic_bytes_per_launch": g_bytes / max(g_n, 1),
+                "traffic": GEMM_TRAFFIC_PER_ALGORITHMIC_BYTE * g_bytes / max(g_n, 1),
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the LM-head and gate/up "
+                                  "launches, scaled to the step's average projection launch by its algorithmic bytes",
+                "algorithmic_bytes_per_launch": g_bytes / max(g_n, 1),
                 "avg_launch_us": g_ms * 1e3 / max(g_n, 1),
                 "per_kind": {k: {"launches_per_step": c / args.steps, "ms_per_step": ms / args.steps,
                                  **({"gbs": gb[k] * c / (ms / 1e3) / 1e9} if k in gb and ms > 0 else {})}
@@ -298,6 +320,12 @@ def run_gpu(args, world, rank, local):
         "clocks": clk.summary(),
     }
     return line
+
+
+# DRAM bytes (read + write) per algorithmic byte of the projection kernel, from one ncu capture of the LM-head
+# launch (32000 x 4096, 64 tokens: 267.7 MB measured for 270.9 MB algorithmic) and one of the gate/up launch
+# (184.7 / 186.5 MB): the kernel reads every weight byte once, so the traffic of a launch scales with its bytes.
+GEMM_TRAFFIC_PER_ALGORITHMIC_BYTE = 0.988
 
 
 def gemm_bytes(dims, n):
@@ -424,7 +452,7 @@ def weight_bytes(dims):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
