@@ -5,12 +5,13 @@
 // ("Phi-3-mini-128k-instruct_rai_1.8.0_medusa_1.0_npu", 4️⃣: siblings never see each other). The mask is one
 // 64-bit ancestor word per node; only the key tile(s) that hold the tree block consult it.
 //
-// Layout: q [n][H][D] bf16, K/V caches as planes of [H][S_max][D] bf16. One CTA = one head x one range of
-// 64-key tiles (split-KV so that H x splits fills the GPU at batch 1). 4 warps, each owning 16 of the (up to)
-// 64 tree queries. KV tiles arrive by TMA (128-byte swizzle, 3-stage mbarrier ring); Q.K^T and P.V run on the
-// tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate); the softmax is an online (running max / sum)
-// softmax in registers. With several splits, the last CTA of a head (atomic ticket) merges the partial
-// (max, sum, output) triples.
+// Layout: q [n][H][D] bf16, K/V caches as planes of [H][S_max][D] bf16. One thread-block cluster per head;
+// its CTAs split the head's 64-key tiles (split-KV, so that H x splits fills the GPU at batch 1). 4 warps per
+// CTA, each owning 16 of the (up to) 64 tree queries. KV tiles arrive by TMA (128-byte swizzle, 2-stage mbarrier
+// ring); Q.K^T and P.V run on the tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate); the softmax is an
+// online (running max / sum) softmax in registers. Each CTA leaves its partial (max, sum, output) in its own
+// shared memory and, after a cluster barrier, merges a slice of the query rows by reading the partials of the
+// whole cluster over distributed shared memory (in rank order, so the result is deterministic).
 #include <float.h>
 
 #include <algorithm>
@@ -24,7 +25,8 @@ constexpr int kThreads = 128;
 constexpr int kKeys = 64;   // keys per tile
 constexpr int kRows = 64;   // query rows per CTA (tree nodes, padded)
 constexpr int kStages = 2;  // 80 KB of shared memory at D = 128: two CTAs share an SM
-constexpr int kMinTiles = 4;  // key tiles per split at least
+constexpr int kMinTiles = 2;    // key tiles per split at the longest prefix, at least
+constexpr int kMaxSplits = 8;   // CTAs per cluster (portable cluster size)
 
 MV_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -61,11 +63,8 @@ struct AttnArgs {
   const uint64_t* anc;      // [n]
   const int32_t* d_prefix;  // device prefix length or null
   int prefix;               // used when d_prefix is null
-  int H, S_max, n, splits, plane_k, plane_v;
+  int H, S_max, n, splits, plane_k, plane_v;  // splits = CTAs per cluster (gridDim.x)
   float scale_log2;         // scale * log2(e)
-  float* opart;             // [H][splits][64][D]
-  float* ml;                // [H][splits][64][2]
-  unsigned int* tickets;    // [H]
   unsigned int* err;
 };
 
@@ -84,9 +83,10 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
   uint8_t* sk = smem + kTileBytes;                     // kStages x [64][D]
   uint8_t* sv = sk + kStages * kTileBytes;             // kStages x [64][D]
   __shared__ __align__(8) uint64_t full[kStages];
-  __shared__ bool s_last;
+  constexpr int kPo = D + 4;  // row pitch (floats) of the partial output in shared memory
 
-  const int h = blockIdx.x, split = blockIdx.y;
+  const int split = blockIdx.x, h = blockIdx.y;  // split = rank in the head's cluster
+  const int C = a.splits;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t4 = lane & 3;
   pdl_trigger();
@@ -98,13 +98,10 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
     return;
   }
   const int total_tiles = (P + n + kKeys - 1) / kKeys;
-  // The grid is sized for the longest prefix; at this prefix only `splits` CTAs per head get tiles (at least
-  // kMinTiles each, so a short prefix is not spread over partials that cost more to merge than to compute),
-  // the others leave at once and the merge reads only the real partials.
-  const int splits = max(1, min(a.splits, (total_tiles + kMinTiles - 1) / kMinTiles));
-  if (split >= splits) return;
-  const int t_begin = (int)((long long)split * total_tiles / splits);
-  const int t_end = (int)((long long)(split + 1) * total_tiles / splits);
+  // The cluster is sized for the longest prefix; at a shorter one some splits get no tile and contribute an
+  // empty partial (max -inf, sum 0) to the merge.
+  const int t_begin = (int)((long long)split * total_tiles / C);
+  const int t_end = (int)((long long)(split + 1) * total_tiles / C);
   const int count = t_end - t_begin;
 
   auto issue = [&](int i) {  // tile t_begin + i into stage i % kStages
@@ -244,22 +241,20 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
     if (tid == 0 && i + kStages < count) issue(i + kStages);
   }
   if (!ok) {
-    // Let the copies already issued land before the CTA's shared memory goes away: tiles [stop, issued)
+    // Let the copies already issued land before the pipeline buffers are reused below: tiles [stop, issued)
     // are in flight, each on its stage's barrier at its own phase. Every wait here is bounded too.
     if (tid == 0) {
       const int issued = min(count, stop + kStages);
       for (int j = stop; j < issued; ++j)
         if (!mbar_wait(&full[j % kStages], (uint32_t)((j / kStages) & 1))) break;
     }
-    __syncthreads();
-    return;
   }
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-  if (splits == 1) {
+  if (C == 1) {  // one split per head (a short prefix): normalise and write, nothing to merge
     const float i0 = l0 > 0.0f ? 1.0f / l0 : 0.0f, i1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
 #pragma unroll
     for (int dn = 0; dn < DN; ++dn) {
@@ -274,108 +269,100 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
     return;
   }
 
-  // ---- split-KV: store the partial triple, the last CTA of the head merges
-  float* op = a.opart + ((size_t)h * a.splits + split) * kRows * D;
+  // ---- this CTA's partial (unnormalised output, running max, sum) into its own shared memory; the CTAs of
+  // the cluster (the key splits of this head) then merge it over distributed shared memory, each CTA a slice
+  // of the query rows. The pipeline buffers are free once every warp has left the loop.
+  __syncthreads();
+  float* po = reinterpret_cast<float*>(smem);  // [64][D + 4] (padded rows: conflict-free float2 stores)
+  float* pml = po + kRows * kPo;               // [64][2] running max (log2 domain) and sum
+  float* pw = pml + kRows * 2;                 // [64][kMaxSplits] merge weights of this CTA's rows
 #pragma unroll
   for (int dn = 0; dn < DN; ++dn) {
     const int col = 8 * dn + 2 * t4;
-    *reinterpret_cast<float2*>(op + (size_t)q0 * D + col) = make_float2(o[dn][0], o[dn][1]);
-    *reinterpret_cast<float2*>(op + (size_t)q1 * D + col) = make_float2(o[dn][2], o[dn][3]);
+    *reinterpret_cast<float2*>(po + q0 * kPo + col) = make_float2(o[dn][0], o[dn][1]);
+    *reinterpret_cast<float2*>(po + q1 * kPo + col) = make_float2(o[dn][2], o[dn][3]);
   }
   if (t4 == 0) {
-    float* mlp = a.ml + ((size_t)h * a.splits + split) * kRows * 2;
-    mlp[q0 * 2 + 0] = m0;
-    mlp[q0 * 2 + 1] = l0;
-    mlp[q1 * 2 + 0] = m1;
-    mlp[q1 * 2 + 1] = l1;
+    pml[q0 * 2 + 0] = m0;
+    pml[q0 * 2 + 1] = l0;
+    pml[q1 * 2 + 0] = m1;
+    pml[q1 * 2 + 1] = l1;
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.tickets + h, 1u) == (unsigned)(splits - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  // per-row merge weights once: w[q][s] = 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s'  (the pipeline buffers are free)
-  float* sw = reinterpret_cast<float*>(smem);  // [64][splits]
-  float* sl = sw + kRows * splits;              // [64][splits]
-  for (int e = tid; e < n * splits; e += kThreads) {
-    const int q = e / splits, sp = e % splits;
-    const float* mlp = a.ml + (((size_t)h * a.splits + sp) * kRows + q) * 2;
-    sw[e] = __ldcg(mlp);
-    sl[e] = __ldcg(mlp + 1);
-  }
-  __syncthreads();
-  if (tid < n) {
-    float* w = sw + tid * splits;
-    const float* l = sl + tid * splits;
+  cluster_sync_all();  // every partial of the head is in place
+  const int r0 = split * n / C, r1 = (split + 1) * n / C;  // this CTA's query rows
+  const uint32_t ml_s = smem_u32(pml), po_s = smem_u32(po);
+  if (tid < r1 - r0) {
+    // w_s = 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s' for the row's C splits (rank order)
+    const int q = r0 + tid;
+    float m[kMaxSplits], l[kMaxSplits];
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) {
+      m[s] = -INFINITY;
+      l[s] = 0.0f;
+      if (s < C) {
+        const float2 v = ld_cluster_f2(map_rank(ml_s + (uint32_t)(q * 8), (uint32_t)s));
+        m[s] = v.x;
+        l[s] = v.y;
+      }
+    }
     float M = -INFINITY;
-    for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, w[sp]);
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, m[s]);
     const float base = M == -INFINITY ? 0.0f : M;
     float L = 0.0f;
-    for (int sp = 0; sp < splits; ++sp) {
-      w[sp] = exp2f(w[sp] - base);
-      L += w[sp] * l[sp];
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) {
+      m[s] = s < C ? exp2f(m[s] - base) : 0.0f;
+      L += m[s] * l[s];
     }
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    for (int sp = 0; sp < splits; ++sp) w[sp] *= inv;
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) pw[tid * kMaxSplits + s] = m[s] * inv;
   }
   __syncthreads();
-  // each thread owns kPer (row, 4-column) chunks; per split, the loads of all of them are in flight together
-  constexpr int kPer = kRows * (D / 4) / kThreads;
-  float acc[kPer][4];
+  for (int e = tid; e < (r1 - r0) * (D / 4); e += kThreads) {
+    const int rq = e / (D / 4), c4 = (e % (D / 4)) * 4, q = r0 + rq;
+    const uint32_t off = po_s + (uint32_t)((q * kPo + c4) * 4);
+    float4 v[kMaxSplits];
 #pragma unroll
-  for (int u = 0; u < kPer; ++u) acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.0f;
-  for (int sp = 0; sp < splits; ++sp) {
-    const float* base = a.opart + ((size_t)h * a.splits + sp) * kRows * D;
-    float4 v[kPer];
+    for (int s = 0; s < kMaxSplits; ++s)
+      if (s < C) v[s] = ld_cluster_f4(map_rank(off, (uint32_t)s));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int e = tid + u * kThreads, q = e / (D / 4), c4 = (e % (D / 4)) * 4;
-      v[u] = q < n ? __ldcg(reinterpret_cast<const float4*>(base + (size_t)q * D + c4)) : make_float4(0, 0, 0, 0);
+    for (int s = 0; s < kMaxSplits; ++s) {
+      if (s < C) {
+        const float w = pw[rq * kMaxSplits + s];
+        acc.x += w * v[s].x;
+        acc.y += w * v[s].y;
+        acc.z += w * v[s].z;
+        acc.w += w * v[s].w;
+      }
     }
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int e = tid + u * kThreads, q = e / (D / 4);
-      const float w = q < n ? sw[q * splits + sp] : 0.0f;
-      acc[u][0] += w * v[u].x;
-      acc[u][1] += w * v[u].y;
-      acc[u][2] += w * v[u].z;
-      acc[u][3] += w * v[u].w;
-    }
+    uint2 pk;
+    pk.x = pack_bf16x2(acc.x, acc.y);
+    pk.y = pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(a.out + ((size_t)q * a.H + h) * D + c4) = pk;
   }
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int e = tid + u * kThreads, q = e / (D / 4), c4 = (e % (D / 4)) * 4;
-    if (q < n) {
-      uint2 pk;
-      pk.x = pack_bf16x2(acc[u][0], acc[u][1]);
-      pk.y = pack_bf16x2(acc[u][2], acc[u][3]);
-      *reinterpret_cast<uint2*>(a.out + ((size_t)q * a.H + h) * D + c4) = pk;
-    }
-  }
-  if (tid == 0) a.tickets[h] = 0u;
+  cluster_sync_all();  // no CTA leaves while another may still read its partial
 }
 
-int choose_splits(int H, int max_tiles) {
-  // one wave of two CTAs per SM, at least kMinTiles key tiles per split
-  const int sms = mv_sm_count();
-  int s = std::max(1, (2 * sms) / H);
-  s = std::min(s, std::max(1, (max_tiles + kMinTiles - 1) / kMinTiles));
-  return std::min(s, 64);
+// Key splits per head (= CTAs per cluster): enough that each split has about kMinTiles key tiles at the
+// longest prefix this launch may see, at most kMaxSplits.
+int choose_splits(int max_tiles) {
+  return std::max(1, std::min(kMaxSplits, (max_tiles + kMinTiles - 1) / kMinTiles));
 }
 
 size_t smem_bytes(int D) {
   const size_t pipeline = (size_t)(1 + 2 * kStages) * kKeys * D * 2;
-  const size_t merge = (size_t)2 * kRows * 64 * sizeof(float);  // weights + sums for up to 64 splits
+  const size_t merge = ((size_t)kRows * (D + 4) + kRows * 2 + kRows * kMaxSplits) * sizeof(float);
   return 1024 + (pipeline > merge ? pipeline : merge);
 }
 
 }  // namespace
 
 size_t tree_attn_ws_bytes(int H, int D, int S_max, int n_nodes) {
-  (void)n_nodes;
-  const int splits = choose_splits(H, (S_max + kKeys - 1) / kKeys);
-  return 256 + (size_t)H * 4 + (size_t)H * splits * kRows * (D + 2) * sizeof(float) + 256;
+  (void)H, (void)D, (void)S_max, (void)n_nodes;
+  return 256;  // reserved: the split partials are merged on chip
 }
 
 bool tree_attn_make_maps(CUtensorMap* kmap, CUtensorMap* vmap, const void* k_cache, const void* v_cache, int H,
@@ -400,10 +387,9 @@ mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vm
                                   const mv_bf16* q, int H, int D, int S_max, const int32_t* d_prefix, int prefix,
                                   int max_prefix, const mv_tree* t, int n, float scale, mv_bf16* out, void* ws,
                                   cudaStream_t stream) {
+  (void)ws;  // reserved
   const int max_tiles = (max_prefix + n + kKeys - 1) / kKeys;
-  const int ws_splits = choose_splits(H, (S_max + kKeys - 1) / kKeys);
-  const int splits = std::min(ws_splits, choose_splits(H, max_tiles));
-  char* p = static_cast<char*>(ws);
+  const int splits = choose_splits(max_tiles);
   AttnArgs a{};
   a.q = q;
   a.out = out;
@@ -417,20 +403,30 @@ mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vm
   a.plane_k = plane_k;
   a.plane_v = plane_v;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.tickets = reinterpret_cast<unsigned int*>(p);
-  a.opart = reinterpret_cast<float*>(p + 256 + (size_t)H * 4 + 255 - ((256 + (size_t)H * 4 + 255) % 256));
-  a.ml = a.opart + (size_t)H * ws_splits * kRows * D;
   a.err = mv_error_word();
   const size_t smem = smem_bytes(D);
-  const dim3 grid(H, splits);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(splits, H);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;  // one cluster = the key splits of one head
+  at[0].val.clusterDim.x = splits;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = mv_pdl_enabled() ? 2 : 1;
+  cudaError_t e;
   switch (D) {
-#define MV_ATTN_CASE(DD)                                                                                 \
-  case DD: {                                                                                           \
-    static int flags[64] = {0};                                                                        \
-    if (!mv_set_smem_once((const void*)tree_attn_kernel<DD>, (int)smem, flags)) return MV_ERR_CUDA;    \
-    if (mv_launch(tree_attn_kernel<DD>, grid, dim3(kThreads), smem, stream, kmap, vmap, a) != cudaSuccess) \
-      return MV_ERR_CUDA;                                                                              \
-    break;                                                                                             \
+#define MV_ATTN_CASE(DD)                                                                               \
+  case DD: {                                                                                         \
+    static int flags[64] = {0};                                                                      \
+    if (!mv_set_smem_once((const void*)tree_attn_kernel<DD>, (int)smem, flags)) return MV_ERR_CUDA;  \
+    e = cudaLaunchKernelEx(&cfg, tree_attn_kernel<DD>, kmap, vmap, a);                               \
+    break;                                                                                           \
   }
     MV_ATTN_CASE(16)
     MV_ATTN_CASE(32)
@@ -440,6 +436,7 @@ mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vm
     default:
       return MV_ERR_SHAPE;
   }
+  if (e != cudaSuccess) return MV_ERR_CUDA;
   return mv_last_launch("tree_attention");
 }
 

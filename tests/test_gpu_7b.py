@@ -5,7 +5,7 @@ configuration bench.py times (packed weights, CUDA-graph replay of the steps).
 The float64 oracle cannot decode 64 tokens of a 7B model one by one in reasonable time, so it checks sampled
 outputs and properties that hold at any size:
 * teacher forcing: one causal oracle forward over prompt + the 64 GPU tokens; every GPU token must be the
-  oracle argmax or within the bf16 tolerance of it ("Phi-3-mini-128k-instruct_rai_1.8.0_medusa_1.0_npu", 2️⃣:
+  oracle argmax or within the margin that bf16 storage itself explains ("Phi-3-mini-128k-instruct_rai_1.8.0_medusa_1.0_npu", 2️⃣:
   greedy Medusa output equals the base model's; "大模型推理 memory bandwidth bound (5) - Medusa", 二.1);
 * the first verify step's LM logits on sampled tree nodes against the oracle's tree forward (二.5).
 """
@@ -65,26 +65,34 @@ def test_7b_greedy_stream_teacher_forced(model7b):
     kv_tree = KVCache(DIMS, P + 64 + N_NEW, kv.data)
     _, tl = om.forward(first_tree_tokens, P + o["position_ids"], kv_tree, P, o["attn_mask"])
     _, lg_gen = om.forward(gen, P + np.arange(N_NEW), kv, P, chain_mask(N_NEW))
-    # 1) teacher forcing: the logits that predict gen[i] are the prompt's last row (i = 0) or gen[i-1]'s row
-    lg = np.concatenate([lg_prompt[-1:], lg_gen[:-1]])
-    margins = lg.max(axis=1) - lg[np.arange(N_NEW), gen]
-    print(f"7B teacher forcing: {int((margins > 0).sum())} of {N_NEW} tokens differ from the oracle argmax, "
-          f"largest margin {margins.max():.4f}, exact-match prefix {int(np.argmax(margins > 0)) if (margins > 0).any() else N_NEW}")
-    for i, t in enumerate(gen):
-        top = lg[i].max()
-        assert top - lg[i, t] <= 1e-2 + 2e-2 * abs(top), (i, int(t), int(np.argmax(lg[i])), top - lg[i, t])
-    # 2) the first step's LM logits on sampled tree nodes against the oracle's tree forward at prefix P.
-    # Reading of the 2e-2 relative / 1e-2 absolute bound for an output composed through 32 layers: the path keeps
-    # q, k, v (the cache), the attention output, the SiLU-gate product and the normalised operands in bf16, and
-    # that storage alone moves the exact model's logits by a measurable amount that grows with depth. The same
-    # oracle, with only those intermediates rounded to bf16 (no other change), measures it on these inputs; the
-    # GPU logits must stay within twice that movement (normwise and per element relative to the row's RMS),
-    # i.e. the kernels' own arithmetic may add at most as much error again as the storage format itself.
     bf16 = lambda name, v: torch.from_numpy(np.ascontiguousarray(v, dtype=np.float32)).to(torch.bfloat16).double().numpy()
-    ob = Backbone(DIMS, get, bf16)
+    ob = Backbone(DIMS, get, bf16)  # the same oracle with bf16 storage of the intermediates
     kv_b = KVCache(DIMS, P + 64)
     ob.forward(prompt.numpy(), np.arange(P), kv_b, 0, chain_mask(P))
     _, tl_store = ob.forward(first_tree_tokens, P + o["position_ids"], kv_b, P, o["attn_mask"])
+    # 1) teacher forcing: the logits that predict gen[i] are the prompt's last row (i = 0) or gen[i-1]'s row.
+    # Reading of the token check at full depth: a GPU token is the oracle argmax, or its oracle margin (top-1
+    # minus its logit) is at most the larger of 1e-2 + 2e-2 |top-1| and twice the largest logit movement that bf16
+    # storage alone causes on this step's 64 tree rows (same oracle, storage hook, no other change); and at least
+    # 3/4 of the tokens are the exact argmax (bf16 storage alone keeps about 9 in 10 argmaxes of these rows).
+    lg = np.concatenate([lg_prompt[-1:], lg_gen[:-1]])
+    margins = lg.max(axis=1) - lg[np.arange(N_NEW), gen]
+    d_store = np.abs(tl_store - tl).max()
+    exact = float((margins == 0).mean())
+    print(f"7B teacher forcing: {int((margins > 0).sum())} of {N_NEW} tokens differ from the oracle argmax, "
+          f"largest margin {margins.max():.4f}, exact-match prefix {int(np.argmax(margins > 0)) if (margins > 0).any() else N_NEW}; "
+          f"bf16 storage alone moves a tree-row logit by up to {d_store:.4f} and keeps "
+          f"{float((tl_store.argmax(1) == tl.argmax(1)).mean()):.3f} of the argmaxes")
+    for i, t in enumerate(gen):
+        top = lg[i].max()
+        assert top - lg[i, t] <= max(1e-2 + 2e-2 * abs(top), 2 * d_store), (i, int(t), int(np.argmax(lg[i])), top - lg[i, t])
+    assert exact >= 0.75, exact
+    # 2) the first step's LM logits on sampled tree nodes against the oracle's tree forward at prefix P.
+    # Reading of the 2e-2 relative / 1e-2 absolute bound for an output composed through 32 layers: the path keeps
+    # q, k, v (the cache), the attention output, the SiLU-gate product and the normalised operands in bf16, and
+    # that storage alone moves the exact model's logits by a measurable amount that grows with depth (tl_store
+    # above). The GPU logits must stay within twice that movement (normwise and per element relative to the row's
+    # RMS), i.e. the kernels' own arithmetic may add at most as much error again as the storage format itself.
     rows = [0, 1, 7, 30, 63]
     ref = tl[rows]
     rms = np.sqrt((ref ** 2).mean(axis=1, keepdims=True))
