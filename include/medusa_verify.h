@@ -305,11 +305,14 @@ mv_status medusa_verify_steps_graph(mv_session* session, mv_accept_params params
 /* Per-launch timing of a session's kernels, for benchmarks: while enabled, every launch of medusa_verify_step /
  * mv_prefill is bracketed by CUDA events on its stream (do not enable during CUDA graph capture).
  * mv_session_profile_read waits for the last recorded event, returns the summed milliseconds and launch counts
- * per kind (indices MV_PROF_*) since profiling was enabled or last read, and resets them. */
+ * per kind (indices MV_PROF_*) since profiling was enabled or last read, and resets them.
+ * The verify step runs each layer's O, gate/up and down projections and the next layer's QKV projection (the
+ * LM head after the last layer) as one launch, counted as MV_PROF_GEMM_CHAIN; MV_PROF_GEMM_QKV is then the first
+ * layer's QKV projection alone. MV_PROF_GEMM_O / _GATE_UP / _DOWN / _LM stay for launches of a single projection. */
 enum {
   MV_PROF_GEMM_QKV = 0, MV_PROF_ATTENTION = 1, MV_PROF_GEMM_O = 2, MV_PROF_GEMM_GATE_UP = 3, MV_PROF_GEMM_DOWN = 4,
   MV_PROF_GEMM_LM = 5, MV_PROF_POSTERIOR = 6, MV_PROF_KV_COMPACT = 7, MV_PROF_HEADS = 8, MV_PROF_OTHER = 9,
-  MV_PROF_KINDS = 10
+  MV_PROF_GEMM_CHAIN = 10, MV_PROF_KINDS = 11
 };
 mv_status mv_session_profile(mv_session* session, int32_t enable);
 mv_status mv_session_profile_read(mv_session* session, float* ms_by_kind, int32_t* launches_by_kind);

@@ -404,7 +404,7 @@ class Session:
 
 
 PROF_KINDS = ("gemm_qkv", "attention", "gemm_o", "gemm_gate_up", "gemm_down", "gemm_lm", "posterior", "kv_compact",
-              "heads", "other")
+              "heads", "other", "gemm_chain")
 
 
 class Profiler:

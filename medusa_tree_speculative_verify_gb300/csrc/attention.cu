@@ -26,7 +26,10 @@ constexpr int kKeys = 64;   // keys per tile
 constexpr int kRows = 64;   // query rows per CTA (tree nodes, padded)
 constexpr int kStages = 2;  // 80 KB of shared memory at D = 128: two CTAs share an SM
 constexpr int kMinTiles = 2;    // key tiles per split at the longest prefix, at least
-constexpr int kMaxSplits = 8;   // CTAs per cluster (portable cluster size)
+// CTAs per cluster. Measured on GB300: with clusters of 8 (two 81 KB CTAs per SM) a few clusters of a 32-head
+// launch only start when others leave (a second wave, +11 us at short prefixes), although the occupancy query
+// reports room for all; clusters of 4 start together.
+constexpr int kMaxSplits = 4;
 
 MV_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -352,6 +355,55 @@ int choose_splits(int max_tiles) {
   return std::max(1, std::min(kMaxSplits, (max_tiles + kMinTiles - 1) / kMinTiles));
 }
 
+size_t smem_bytes(int D);
+
+// Clusters of c CTAs of tree_attn_kernel<D> that can be resident at once (asked once per device, D and c).
+int max_active_clusters(int D, int c) {
+  static int cache[64][4][kMaxSplits + 1];  // 0 = not asked yet, -1 = none
+  const int dev = mv_device();
+  const int di = D == 16 ? 0 : D == 32 ? 1 : D == 64 ? 2 : 3;
+  if (dev < 0 || dev >= 64 || c < 1 || c > kMaxSplits) return 0;
+  int& slot = cache[dev][di][c];
+  if (slot == 0) {
+    const size_t smem = smem_bytes(D);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(c, 1024);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = c;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (D) {
+#define MV_ATTN_OCC(DD)                                                                                \
+  case DD: {                                                                                         \
+    static int flags[64] = {0};                                                                      \
+    if (mv_set_smem_once((const void*)tree_attn_kernel<DD>, (int)smem, flags))                       \
+      e = cudaOccupancyMaxActiveClusters(&n, tree_attn_kernel<DD>, &cfg);                            \
+    break;                                                                                           \
+  }
+      MV_ATTN_OCC(16)
+      MV_ATTN_OCC(32)
+      MV_ATTN_OCC(64)
+      MV_ATTN_OCC(128)
+#undef MV_ATTN_OCC
+      default:
+        break;
+    }
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    slot = n > 0 ? n : -1;
+  }
+  return slot > 0 ? slot : 0;
+}
+
 size_t smem_bytes(int D) {
   const size_t pipeline = (size_t)(1 + 2 * kStages) * kKeys * D * 2;
   const size_t merge = ((size_t)kRows * (D + 4) + kRows * 2 + kRows * kMaxSplits) * sizeof(float);
@@ -389,7 +441,9 @@ mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vm
                                   cudaStream_t stream) {
   (void)ws;  // reserved
   const int max_tiles = (max_prefix + n + kKeys - 1) / kKeys;
-  const int splits = choose_splits(max_tiles);
+  int splits = choose_splits(max_tiles);
+  // all H clusters resident at once: a cluster that has to wait for another to leave costs a whole second wave
+  while (splits > 1 && max_active_clusters(D, splits) < H) --splits;
   AttnArgs a{};
   a.q = q;
   a.out = out;

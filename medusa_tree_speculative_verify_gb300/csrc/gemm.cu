@@ -24,6 +24,9 @@
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer + TMEM owner, warps 2..5 = epilogue
 // (warp w reads TMEM lanes 32*(w%4) .. +31). Every mbarrier wait is bounded; on expiry the kernel records
 // MV_DEVERR_TIMEOUT, lets its in-flight copies and MMAs land, frees its tensor memory and returns.
+#include <algorithm>
+#include <cstring>
+
 #include "common.cuh"
 #include "gemm.cuh"
 #include "kernels.cuh"
@@ -146,6 +149,7 @@ MV_DEV void load_epi_const(const GemmParams& p, EpiConst* ec, int i) {
 // (t = 0..15), so every global access of the epilogue is one 16-byte (fp32) or 8-byte (bf16) vector per lane and
 // a warp covers one token's 128 contiguous rows. Partner rows (RoPE d +- D/2, SwiGLU gate/up) sit in lane l ^ k.
 constexpr int kTokPerThread = BN / 4;
+constexpr int kChunk = 4;  // tokens per thread finished at once
 
 MV_DEV void add4(float4& a, const float4& b) {
   a.x += b.x;
@@ -177,15 +181,15 @@ MV_DEV void rope_sincos(float a, float* s, float* c) {
 
 // This CTA's share of the tile: tokens j = w + 4t for t = r0, r0 + cs, ... (acc[u] holds t = r0 + u * cs, rows
 // 4l..4l+3, summed over every K slice of the cluster). Writes the outputs of the launch's epilogue kind.
-template <int EPI>
+template <int EPI, int NU>
 MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, int cs,
-                           float4 (&acc)[kTokPerThread], const EpiConst* ec) {
+                           float4 (&acc)[NU], const EpiConst* ec) {
   const int ntok = p.n_tok;
   if constexpr (EPI == EPI_STORE) {
     const int R = tile * BM + 4 * l;
     const bool vec = ((reinterpret_cast<uintptr_t>(p.out_f32) & 15) == 0) && ((p.ld_out & 3) == 0) && R + 3 < p.M;
 #pragma unroll
-    for (int u = 0; u < kTokPerThread; ++u) {
+    for (int u = 0; u < NU; ++u) {
       const int t = r0 + u * cs;
       if (t >= kTokPerThread) break;
       const int j = w + 4 * t;
@@ -206,9 +210,9 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, 
     // M is a multiple of 4 (host check): a lane's 4 rows are all valid or all past the end
     const int R = tile * BM + 4 * l;
     const bool valid = R < p.M;
-    float4 xo[kTokPerThread];
+    float4 xo[NU];
 #pragma unroll
-    for (int u = 0; u < kTokPerThread; ++u) {  // every residual load in flight before the first use
+    for (int u = 0; u < NU; ++u) {  // every residual load in flight before the first use
       const int t = r0 + u * cs;
       if (t >= kTokPerThread) break;
       const int j = w + 4 * t;
@@ -216,7 +220,7 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, 
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < kTokPerThread; ++u) {
+    for (int u = 0; u < NU; ++u) {
       const int t = r0 + u * cs;
       if (t >= kTokPerThread) break;
       const int j = w + 4 * t;
@@ -237,7 +241,7 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, 
     // lanes 0..15: gate rows 4l..4l+3 (features f0 + 4l ..); lanes 16..31: the matching up rows
     const int f = tile * 64 + 4 * l;
 #pragma unroll
-    for (int u = 0; u < kTokPerThread; ++u) {
+    for (int u = 0; u < NU; ++u) {
       const int t = r0 + u * cs;
       if (t >= kTokPerThread) break;
       const int j = w + 4 * t;
@@ -274,7 +278,7 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, 
       stride = (size_t)p.D;
     }
 #pragma unroll
-    for (int u = 0; u < kTokPerThread; ++u) {
+    for (int u = 0; u < NU; ++u) {
       const int t = r0 + u * cs;
       if (t >= kTokPerThread) break;
       const int j = w + 4 * t;
@@ -298,11 +302,30 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, 
   }
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap amap0,
-                                                           const __grid_constant__ CUtensorMap amap1,
-                                                           const __grid_constant__ CUtensorMap bmap,
-                                                           const GemmParams p) {
+struct ChainMaps {
+  CUtensorMap a0[kGemmMaxPhases], a1[kGemmMaxPhases], b[kGemmMaxPhases];
+};
+struct ChainArgs {
+  GemmParams ph[kGemmMaxPhases];
+  int epi[kGemmMaxPhases];
+  int n_phases, csize;
+  unsigned int* flags;  // [kGemmChainFlagWords]: phase-done counters, then the exit counter
+};
+
+// Bounded wait until *p >= target (acquire at GPU scope); false when it expires.
+MV_DEV bool wait_count(const unsigned int* p, unsigned int target) {
+  const uint64_t t0 = mv_globaltimer();
+  while (true) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    if (mv_globaltimer() - t0 > MV_WAIT_LIMIT_NS) return false;
+    __nanosleep(64);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ ChainMaps maps,
+                                                           const __grid_constant__ ChainArgs ca) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
@@ -313,12 +336,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   __shared__ EpiConst s_ec;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int C = p.csize;                       // CTAs per cluster = K slices per tile
-  const int rank = (int)cluster_rank();        // this CTA's K slice and token share
-  // cluster q owns the contiguous tiles [t0, t1): consecutive tiles are adjacent in the packed weight layout
+  const int C = ca.csize;                  // CTAs per cluster = K slices per tile
+  const int rank = (int)cluster_rank();    // this CTA's K slice and token share
+  // in every phase cluster q owns the contiguous tiles [t0, t1) (adjacent in the packed weight layout)
   const int q = blockIdx.x / C, ncl = gridDim.x / C;
-  const int t0 = (int)((long long)q * p.n_tiles / ncl), t1 = (int)((long long)(q + 1) * p.n_tiles / ncl);
-  const int kb0 = rank * p.kbt / C, kb1 = (rank + 1) * p.kbt / C;  // this CTA's K slice
+  auto tile_range = [&](const GemmParams& p, int& t0, int& t1) {
+    t0 = (int)((long long)q * p.n_tiles / ncl);
+    t1 = (int)((long long)(q + 1) * p.n_tiles / ncl);
+  };
+  unsigned int* err = ca.ph[0].err;
   pdl_trigger();
 
   if (threadIdx.x == 0) {
@@ -349,52 +375,78 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&amap0);
-      if (p.paired) tma_prefetch_desc(&amap1);
-      tma_prefetch_desc(&bmap);
+      for (int ph = 0; ph < ca.n_phases; ++ph) {
+        tma_prefetch_desc(&maps.a0[ph]);
+        if (ca.ph[ph].paired) tma_prefetch_desc(&maps.a1[ph]);
+        tma_prefetch_desc(&maps.b[ph]);
+      }
       int it = 0;
-      bool ok = true, waited = false;
+      bool ok = true, flag_timeout = false;
       const uint64_t wpol = l2_evict_first_policy();  // weights are read once per step
-      int pend_kb[kStages];  // k-blocks whose weight tile was issued before the previous grid finished
-      int pend = 0;
-      auto issue_b = [&](int stage, int kb) {
-        tma_load_2d(stages + (size_t)stage * kStageBytes + kABytes, &bmap, &full[stage], kb * BK, 0);
-      };
-      auto release = [&]() {  // the activations come from the previous kernel: wait for it, then load them
-        pdl_wait();
-        waited = true;
-        for (int q = 0; q < pend; ++q) issue_b(q, pend_kb[q]);
-      };
-      for (int tile = t0; ok && tile < t1; ++tile) {
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % kStages, r = it / kStages;
-          if (s_abort || !mbar_wait(&empty[s], (uint32_t)((r & 1) ^ 1))) {
-            ok = false;
-            break;
-          }
-          uint8_t* a = stages + (size_t)s * kStageBytes;
-          mbar_arrive_expect_tx(&full[s], kStageBytes);
-          if (p.packed_a) {  // one contiguous block per matrix
-            const int tb = tile * p.kbt + kb;
-            tma_load_3d_hint(a, &amap0, &full[s], 0, 0, tb, wpol);
-            if (p.paired) tma_load_3d_hint(a + kABytes / 2, &amap1, &full[s], 0, 0, tb, wpol);
-          } else if (p.paired) {
-            tma_load_2d_hint(a, &amap0, &full[s], kb * BK, tile * 64, wpol);
-            tma_load_2d_hint(a + kABytes / 2, &amap1, &full[s], kb * BK, tile * 64, wpol);
+      for (int ph = 0; ok && ph < ca.n_phases; ++ph) {
+        const GemmParams& p = ca.ph[ph];
+        const CUtensorMap* am0 = &maps.a0[ph];
+        const CUtensorMap* am1 = &maps.a1[ph];
+        const CUtensorMap* bm = &maps.b[ph];
+        int t0, t1;
+        tile_range(p, t0, t1);
+        const int kb0 = rank * p.kbt / C, kb1 = (rank + 1) * p.kbt / C;  // this CTA's K slice
+        // The weights do not depend on anything: their loads run ahead. The activations are the previous
+        // kernel's output (phase 0: wait for that grid) or the previous phase's (wait for its counter).
+        bool waited = false;
+        int pend_s[kStages], pend_kb[kStages];
+        int pend = 0;
+        auto issue_b = [&](int stage, int kb) {
+          tma_load_2d(stages + (size_t)stage * kStageBytes + kABytes, bm, &full[stage], kb * BK, 0);
+        };
+        auto release = [&]() -> bool {  // on an expired wait the loads are still issued, so every barrier completes
+          bool got = true;
+          if (ph == 0) {
+            pdl_wait();
           } else {
-            tma_load_2d_hint(a, &amap0, &full[s], kb * BK, tile * BM, wpol);
+            got = wait_count(ca.flags + ph - 1, gridDim.x);
+            flag_timeout |= !got;
+            asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes -> TMA reads
           }
-          if (waited) {
-            issue_b(s, kb);
-          } else {
-            pend_kb[pend++] = kb;  // stage == pend - 1 while it < kStages
-            if (pend == kStages) release();
+          waited = true;
+          for (int j = 0; j < pend; ++j) issue_b(pend_s[j], pend_kb[j]);
+          return got;
+        };
+        for (int tile = t0; ok && tile < t1; ++tile) {
+          for (int kb = kb0; kb < kb1; ++kb, ++it) {
+            const int s = it % kStages, r = it / kStages;
+            if (s_abort || !mbar_wait(&empty[s], (uint32_t)((r & 1) ^ 1))) {
+              ok = false;
+              break;
+            }
+            uint8_t* a = stages + (size_t)s * kStageBytes;
+            mbar_arrive_expect_tx(&full[s], kStageBytes);
+            if (p.packed_a) {  // one contiguous block per matrix
+              const int tb = tile * p.kbt + kb;
+              tma_load_3d_hint(a, am0, &full[s], 0, 0, tb, wpol);
+              if (p.paired) tma_load_3d_hint(a + kABytes / 2, am1, &full[s], 0, 0, tb, wpol);
+            } else if (p.paired) {
+              tma_load_2d_hint(a, am0, &full[s], kb * BK, tile * 64, wpol);
+              tma_load_2d_hint(a + kABytes / 2, am1, &full[s], kb * BK, tile * 64, wpol);
+            } else {
+              tma_load_2d_hint(a, am0, &full[s], kb * BK, tile * BM, wpol);
+            }
+            if (waited) {
+              issue_b(s, kb);
+            } else {
+              pend_s[pend] = s;
+              pend_kb[pend] = kb;
+              if (++pend == kStages && !release()) {
+                ok = false;
+                break;
+              }
+            }
           }
         }
+        if (ok && !waited && pend > 0 && !release()) ok = false;
       }
-      if (!waited) release();
       if (!ok) {
-        if (!s_abort) mv_set_error(p.err, 8, MV_DEVERR_TIMEOUT);
+        if (!s_abort) mv_set_error(err, flag_timeout ? 12 : 8, MV_DEVERR_TIMEOUT);
         s_abort = 1;
         // let the copies in flight land: the most recent phase of each stage
         for (int j = max(0, it - kStages); j < it; ++j)
@@ -407,33 +459,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       int it = 0, n = 0;
       bool ok = true;
       const uint32_t st0 = smem_u32(stages);
-      for (int tile = t0; ok && tile < t1; ++tile, ++n) {
-        const int buf = n & 1, rr = n >> 1;
-        if (s_abort || !mbar_wait(&tempty[buf], (uint32_t)((rr & 1) ^ 1))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t dt = tmem_base + (uint32_t)(buf * BN);
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % kStages, r = it / kStages;
-          if (s_abort || !mbar_wait(&full[s], (uint32_t)(r & 1))) {
+      for (int ph = 0; ok && ph < ca.n_phases; ++ph) {
+        const GemmParams& p = ca.ph[ph];
+        int t0, t1;
+        tile_range(p, t0, t1);
+        const int kb0 = rank * p.kbt / C, kb1 = (rank + 1) * p.kbt / C;
+        for (int tile = t0; ok && tile < t1; ++tile, ++n) {
+          const int buf = n & 1, rr = n >> 1;
+          if (s_abort || !mbar_wait(&tempty[buf], (uint32_t)((rr & 1) ^ 1))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a = st0 + (uint32_t)(s * kStageBytes), b = a + kABytes;
-          const uint64_t ad = sw128_desc(a), bd = sw128_desc(b);
+          const uint32_t dt = tmem_base + (uint32_t)(buf * BN);
+          for (int kb = kb0; kb < kb1; ++kb, ++it) {
+            const int s = it % kStages, r = it / kStages;
+            if (s_abort || !mbar_wait(&full[s], (uint32_t)(r & 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a = st0 + (uint32_t)(s * kStageBytes), b = a + kABytes;
+            const uint64_t ad = sw128_desc(a), bd = sw128_desc(b);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            tc_mma(dt, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
-          tc_commit(&empty[s]);
+            for (int k = 0; k < BK / 16; ++k)
+              tc_mma(dt, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            tc_commit(&empty[s]);
+          }
+          if (!ok) break;
+          tc_commit(&tfull[buf]);
         }
-        if (!ok) break;
-        tc_commit(&tfull[buf]);
       }
       if (!ok) {
-        if (!s_abort) mv_set_error(p.err, 9, MV_DEVERR_TIMEOUT);
+        if (!s_abort) mv_set_error(err, 9, MV_DEVERR_TIMEOUT);
         s_abort = 1;
         tc_commit(&drain);  // arrives once every MMA issued so far has completed
         mbar_wait(&drain, 0);
@@ -443,58 +501,107 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     // ------------------------------------------------------------------ epilogue (128 threads)
     // Pipelined over the tiles: iteration n first sums and finishes tile n-1 (its partials were published a
     // whole tile ago, and this runs while the MMA works on tile n), then drains tile n's accumulator from TMEM
-    // into this CTA's partial buffer and signals the cluster. The last tile's finish is the only one in the tail.
-    const int sub = warp & 3;           // TMEM sub-partition this warp may read
-    const int i = sub * 32 + lane;      // tile row = TMEM lane
-    pdl_wait();                         // the epilogue reads what earlier kernels wrote
-    load_epi_const(p, &s_ec, i);        // scales and positions: the same for every tile of this launch
-    const int ntok = p.n_tok;
+    // into this CTA's partial buffer and signals the cluster. At a phase boundary the last tile of the phase is
+    // finished, the phase is published (one count per CTA), and this phase's scales wait for every CTA.
+    const int sub = warp & 3;       // TMEM sub-partition this warp may read
+    const int i = sub * 32 + lane;  // tile row = TMEM lane
+    pdl_wait();                     // the epilogue reads what earlier kernels wrote
     const uint32_t part_s = smem_u32(part) + (uint32_t)(lane * 16);  // + token row
     bool ok = true;
-    // Sum the C partials of tile iteration nr (this CTA's token share, rank order) and run the fused epilogue.
-    auto finish = [&](int tile_r, int nr) {
+    int n = 0, prev_tile = -1, prev_ph = 0;
+    auto finish = [&](int ph_r, int tile_r, int nr) {
       const bool all = mbar_wait_cluster(&pfull, (uint32_t)(nr & 1));
       if (epi_any(!all)) {
-        if (i == 0) mv_set_error(p.err, 11, MV_DEVERR_TIMEOUT);
+        if (i == 0) mv_set_error(err, 11, MV_DEVERR_TIMEOUT);
         s_abort = 1;
         ok = false;
         return;
       }
-      float4 acc[kTokPerThread];
+      const GemmParams& pr = ca.ph[ph_r];
+      const int epi = ca.epi[ph_r];
+      // this CTA's token share t = rank, rank + C, ... in chunks of kChunk tokens per thread (one chunk at
+      // C >= 4), each summed over the C partials of the cluster in rank order (16-byte DSMEM loads); only the
+      // fused epilogue itself depends on the kind
+      for (int u0 = 0; rank + u0 * C < kTokPerThread; u0 += kChunk) {
+        float4 acc[kChunk];
 #pragma unroll
-      for (int u = 0; u < kTokPerThread; ++u) {
-        acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        const int t = rank + u * C;
-        if (t >= kTokPerThread) break;
-        const int j = sub + 4 * t;
-        if (j >= ntok) continue;
-        const uint32_t off = part_s + (uint32_t)(j * BM * 4);
-        float4 part_c[kMaxCluster];
+        for (int u = 0; u < kChunk; ++u) {
+          acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          const int t = rank + (u0 + u) * C;
+          if (t >= kTokPerThread) break;
+          const int j = sub + 4 * t;
+          if (j >= pr.n_tok) continue;
+          const uint32_t off = part_s + (uint32_t)(j * BM * 4);
+          float4 part_c[kMaxCluster];
 #pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c)
-          if (c < C) part_c[c] = ld_cluster_f4(map_rank(off, (uint32_t)c));
+          for (int c = 0; c < kMaxCluster; ++c)
+            if (c < C) part_c[c] = ld_cluster_f4(map_rank(off, (uint32_t)c));
 #pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c)
-          if (c < C) add4(acc[u], part_c[c]);
+          for (int c = 0; c < kMaxCluster; ++c)
+            if (c < C) add4(acc[u], part_c[c]);
+        }
+        const int r0 = rank + u0 * C;
+        if (epi == EPI_RESIDUAL)
+          final_epilogue<EPI_RESIDUAL, kChunk>(pr, tile_r, sub, lane, r0, C, acc, &s_ec);
+        else if (epi == EPI_SWIGLU)
+          final_epilogue<EPI_SWIGLU, kChunk>(pr, tile_r, sub, lane, r0, C, acc, &s_ec);
+        else if (epi == EPI_QKV)
+          final_epilogue<EPI_QKV, kChunk>(pr, tile_r, sub, lane, r0, C, acc, &s_ec);
+        else
+          final_epilogue<EPI_STORE, kChunk>(pr, tile_r, sub, lane, r0, C, acc, &s_ec);
       }
-      final_epilogue<EPI>(p, tile_r, sub, lane, rank, C, acc, &s_ec);
       // the partials were consumed above (stores issued from them): release the buffers to their owners, one
       // release arrive per CTA of the cluster from C lanes at once (each costs a cluster round trip)
       epi_bar();
       if (i < C) mbar_arrive_remote(map_rank(smem_u32(&pfree), (uint32_t)i));
     };
-    int n = 0, prev = -1;
-    for (int tile = t0; tile < t1; ++tile, ++n) {
-      if (n >= 1) {
-        finish(prev, n - 1);
+    // One loop over this CTA's tiles of every phase, so that each tile is finished at a single place in the code.
+    const int NP = ca.n_phases;
+    int ph = 0, t0 = 0, t1 = 0, tile = 0, published = 0, ec_ph = -1;
+    tile_range(ca.ph[0], t0, t1);
+    tile = t0;
+    while (true) {
+      while (ph < NP && tile >= t1) {  // the next tile to drain: skip exhausted phases
+        if (++ph < NP) {
+          tile_range(ca.ph[ph], t0, t1);
+          tile = t0;
+        }
+      }
+      if (prev_tile >= 0) {
+        finish(prev_ph, prev_tile, n - 1);
+        prev_tile = -1;
         if (!ok) break;
+      }
+      // every phase before `upto` is finished in this CTA: publish them, in order (one count per CTA and phase)
+      const int upto = ph < NP ? ph : NP - 1;
+      if (published < upto) {
+        epi_bar();  // every output of those phases written by this CTA
+        if (i == 0) {
+          __threadfence();
+          for (int k = published; k < upto; ++k) atomicAdd(ca.flags + k, 1u);
+        }
+        published = upto;
+      }
+      if (ph >= NP) break;
+      if (ec_ph != ph) {
+        // this phase's scales are sums of squares the previous phase wrote: wait until every CTA finished it
+        bool got = true;
+        if (ph > 0 && i == 0) got = wait_count(ca.flags + ph - 1, gridDim.x);
+        if (epi_any(!got)) {
+          if (i == 0) mv_set_error(err, 12, MV_DEVERR_TIMEOUT);
+          s_abort = 1;
+          ok = false;
+          break;
+        }
+        load_epi_const(ca.ph[ph], &s_ec, i);  // scales and positions: the same for every tile of the phase
+        ec_ph = ph;
       }
       const int buf = n & 1;
       bool got = !s_abort && mbar_wait(&tfull[buf], (uint32_t)((n >> 1) & 1));
       // the partial buffer is free again once every CTA of the cluster has finished tile n - 1
       if (got && n >= 1) got = mbar_wait_cluster(&pfree, (uint32_t)((n - 1) & 1));
       if (epi_any(!got)) {  // uniform over the 4 epilogue warps
-        if (i == 0) mv_set_error(p.err, 10, MV_DEVERR_TIMEOUT);
+        if (i == 0) mv_set_error(err, 10, MV_DEVERR_TIMEOUT);
         s_abort = 1;
         ok = false;
         break;
@@ -515,9 +622,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
       epi_bar();  // the CTA's writes are ordered before the cluster-scope release arrives below
       if (i < C) mbar_arrive_remote(map_rank(smem_u32(&pfull), (uint32_t)i));
-      prev = tile;
+      prev_tile = tile;
+      prev_ph = ph;
+      ++tile;
+      ++n;
     }
-    if (ok && n >= 1) finish(prev, n - 1);
   }
 
   tc_fence_before();
@@ -526,6 +635,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+  // the last CTA out leaves the chain's counters at zero for the next launch
+  if (threadIdx.x == 0 && ca.flags && ca.n_phases > 1) {
+    __threadfence();
+    if (atomicAdd(ca.flags + kGemmMaxPhases, 1u) == gridDim.x - 1) {
+      for (int k = 0; k < kGemmChainFlagWords; ++k) ca.flags[k] = 0u;
+      __threadfence();
+    }
   }
 }
 
@@ -569,7 +686,7 @@ int gemm_max_clusters(int c) {
   if (slot == 0) {
     static int flags[64] = {0};
     int n = 0;
-    if (mv_set_smem_once((const void*)gemm_kernel<EPI_STORE>, (int)kSmemBytes, flags)) {
+    if (mv_set_smem_once((const void*)gemm_kernel, (int)kSmemBytes, flags)) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(c * mv_sm_count());
       cfg.blockDim = dim3(kThreads);
@@ -581,7 +698,7 @@ int gemm_max_clusters(int c) {
       at[0].val.clusterDim.z = 1;
       cfg.attrs = at;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<EPI_STORE>, &cfg) != cudaSuccess) {
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel, &cfg) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
       }
@@ -591,67 +708,102 @@ int gemm_max_clusters(int c) {
   return slot > 0 ? slot : 0;
 }
 
-// Cluster size and count for n_tiles tiles of kbt k-blocks: the smallest largest per-CTA share of k-blocks,
-// ceil(tiles per cluster) * ceil(kbt / c), with all clusters resident at once (ties: the smaller cluster).
-void gemm_finish_params(GemmParams& p) {
+namespace {
+void shape_params(GemmParams& p) {
   p.kbt = (p.K + BK - 1) / BK;
   p.n_tiles = p.paired ? (p.F + 63) / 64 : (p.M + BM - 1) / BM;
+}
+// One cluster shape for a chain: the cluster size c and count that minimise the summed largest per-CTA share
+// of k-blocks, sum over phases of ceil(tiles / clusters) * ceil(kbt / c), with all clusters resident at once
+// (ties: the smaller cluster). Every CTA is resident, which the counters between phases rely on.
+void plan_chain(GemmParams* p, int n, int* csize, int* ncl_out) {
+  int max_tiles = 1, min_kbt = 1 << 30;
+  for (int i = 0; i < n; ++i) {
+    max_tiles = std::max(max_tiles, p[i].n_tiles);
+    min_kbt = std::min(min_kbt, p[i].kbt);
+  }
   long long best = -1;
-  p.csize = 1;
-  p.n_clusters = p.n_tiles < mv_sm_count() ? p.n_tiles : mv_sm_count();
-  for (int c = 1; c <= kMaxCluster && c <= p.kbt; ++c) {
+  *csize = 1;
+  *ncl_out = std::min(max_tiles, mv_sm_count());
+  for (int c = 1; c <= kMaxCluster && c <= min_kbt; ++c) {
     const int mc = gemm_max_clusters(c);
     if (mc < 1) continue;
-    const int ncl = mc < p.n_tiles ? mc : p.n_tiles;
-    const long long cost = (long long)((p.n_tiles + ncl - 1) / ncl) * ((p.kbt + c - 1) / c);
+    const int ncl = std::min(mc, max_tiles);
+    long long cost = 0;
+    for (int i = 0; i < n; ++i) cost += (long long)((p[i].n_tiles + ncl - 1) / ncl) * ((p[i].kbt + c - 1) / c);
     if (best < 0 || cost < best) {
       best = cost;
-      p.csize = c;
-      p.n_clusters = ncl;
+      *csize = c;
+      *ncl_out = ncl;
     }
   }
+}
+}  // namespace
+
+void gemm_finish_params(GemmParams& p) {
+  shape_params(p);
+  plan_chain(&p, 1, &p.csize, &p.n_clusters);
   p.grid = p.csize * p.n_clusters;
 }
 
-mv_status launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
-                      const GemmParams& p, cudaStream_t stream) {
-  if (p.n_tiles > kGemmMaxTiles || p.n_tok < 1 || p.n_tok > BN) return MV_ERR_SHAPE;
-  if (p.csize < 1 || p.csize > kMaxCluster || p.n_clusters < 1 || p.grid != p.csize * p.n_clusters ||
-      p.csize > p.kbt)
-    return MV_ERR_INVALID_ARG;
+mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStream_t stream) {
+  if (n < 1 || n > kGemmMaxPhases || (n > 1 && !flags)) return MV_ERR_INVALID_ARG;
+  ChainMaps maps;
+  ChainArgs ca;
+  memset(&maps, 0, sizeof(maps));
+  memset(&ca, 0, sizeof(ca));
+  GemmParams ps[kGemmMaxPhases];
+  for (int i = 0; i < n; ++i) {
+    ps[i] = ph[i].p;
+    shape_params(ps[i]);
+    if (ps[i].n_tiles > kGemmMaxTiles || ps[i].n_tok < 1 || ps[i].n_tok > BN) return MV_ERR_SHAPE;
+    if (ph[i].epi < EPI_STORE || ph[i].epi > EPI_QKV) return MV_ERR_INVALID_ARG;
+  }
+  int csize = 1, ncl = 1;
+  plan_chain(ps, n, &csize, &ncl);
+  for (int i = 0; i < n; ++i) {
+    ps[i].csize = csize;
+    ps[i].n_clusters = ncl;
+    ps[i].grid = csize * ncl;
+    ph[i].p = ps[i];
+    ca.ph[i] = ps[i];
+    ca.epi[i] = ph[i].epi;
+    maps.a0[i] = ph[i].a0;
+    maps.a1[i] = ph[i].a1;
+    maps.b[i] = ph[i].b;
+  }
+  ca.n_phases = n;
+  ca.csize = csize;
+  ca.flags = flags;
+  static int smem_flags[64] = {0};
+  if (!mv_set_smem_once((const void*)gemm_kernel, (int)kSmemBytes, smem_flags)) return MV_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.grid);
+  cfg.gridDim = dim3(csize * ncl);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = p.csize;
+  at[0].val.clusterDim.x = csize;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = mv_pdl_enabled() ? 2 : 1;
-  cudaError_t e;
-  switch (epi) {
-#define MV_GEMM_CASE(E)                                                                        \
-  case E: {                                                                                    \
-    static int flags[64] = {0};                                                                \
-    if (!mv_set_smem_once((const void*)gemm_kernel<E>, (int)kSmemBytes, flags)) return MV_ERR_CUDA; \
-    e = cudaLaunchKernelEx(&cfg, gemm_kernel<E>, a0, a1, b, p);                                \
-    break;                                                                                     \
-  }
-    MV_GEMM_CASE(EPI_STORE)
-    MV_GEMM_CASE(EPI_RESIDUAL)
-    MV_GEMM_CASE(EPI_SWIGLU)
-    MV_GEMM_CASE(EPI_QKV)
-#undef MV_GEMM_CASE
-    default:
-      return MV_ERR_INVALID_ARG;
-  }
-  if (e != cudaSuccess) return MV_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, gemm_kernel, maps, ca) != cudaSuccess) return MV_ERR_CUDA;
   return mv_last_launch("gemm");
+}
+
+mv_status launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
+                      const GemmParams& p, cudaStream_t stream) {
+  GemmPhase ph;
+  ph.epi = epi;
+  ph.a0 = a0;
+  ph.a1 = a1;
+  ph.b = b;
+  ph.p = p;
+  return launch_gemm_chain(&ph, 1, nullptr, stream);
 }
 
 // out[n][ld] (fp32) = X[n][K] . W[M][K]^T, optionally scaled per row of X by 1/sqrt(mean(x^2)+eps) of x_f32.

@@ -38,6 +38,19 @@ struct GemmParams {
   unsigned int* err;
 };
 
+// A chain of up to kGemmMaxPhases projections in one persistent launch: phase i+1's activations are phase i's
+// output, so its activation loads wait for a device counter that every CTA bumps once it has finished phase i
+// (its weight loads run ahead meanwhile). One cluster shape for all phases.
+constexpr int kGemmMaxPhases = 4;
+struct GemmPhase {
+  int epi;
+  CUtensorMap a0, a1, b;  // weights (a1: the up matrix of a paired phase), activations
+  GemmParams p;
+};
+// Phase-done counters of a chain (kGemmMaxPhases + 1 words, zero before the first launch; every launch leaves
+// them zero again).
+constexpr int kGemmChainFlagWords = kGemmMaxPhases + 1;
+
 size_t gemm_smem_bytes();
 bool gemm_weight_map(CUtensorMap* map, const void* w, int rows, int K, int box_rows);
 bool gemm_weight_map_packed(CUtensorMap* map, const void* w, int rows, int K, int tile_rows);
@@ -45,3 +58,6 @@ bool gemm_act_map(CUtensorMap* map, const void* x, int rows, int K);
 void gemm_finish_params(GemmParams& p);
 mv_status launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                       const GemmParams& p, cudaStream_t stream);
+// ph[i].p must have its shape fields set (M, K, paired, F); the cluster plan is computed here. flags: see above
+// (may be null when n == 1).
+mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStream_t stream);

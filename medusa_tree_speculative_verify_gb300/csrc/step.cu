@@ -146,6 +146,7 @@ struct mv_session {
   void* ws_attn;
   void* ws_post;
   void* ws_heads;
+  unsigned int* chain_flags;  // phase counters of the projection chains (zero between launches)
   CUtensorMap m_xb, m_attn, m_act, m_kv;
   // CUDA graph of n consecutive steps (medusa_verify_steps_graph), captured on first use
   cudaGraphExec_t graph_exec = nullptr;
@@ -194,7 +195,7 @@ struct ProfScope {
 namespace {
 
 struct SessionLayout {
-  size_t state, tree_tokens, cart, x, xb, ssq, q, attn, act, logits, attn_ws, post, heads, total;
+  size_t state, tree_tokens, cart, x, xb, ssq, q, attn, act, logits, attn_ws, post, heads, chain, total;
 };
 
 SessionLayout session_layout(const mv_model_dims& d, int s_max, int topk) {
@@ -220,6 +221,7 @@ SessionLayout session_layout(const mv_model_dims& d, int s_max, int topk) {
   L.attn_ws = take(tree_attn_ws_bytes(d.n_heads, d.head_dim, s_max, kTok));
   L.post = take(posterior_ws_bytes(kTok));
   L.heads = take(heads_ws_bytes(1, d.d, d.n_medusa, d.vocab, topk));
+  L.chain = take(kGemmChainFlagWords * sizeof(unsigned int));  // zero at creation; each chain launch leaves it so
   L.total = o;
   return L;
 }
@@ -258,76 +260,65 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
              ? mv_last_launch("embed")
              : MV_ERR_CUDA;
   }
-  for (int l = 0; l < d.n_layers && rc == MV_OK; ++l) {
-    {  // QKV + RoPE + KV append
-      GemmParams p = base_params(s, n);
-      p.M = 3 * HD;
-      p.K = d.d;
-      p.ssq = s->ssq;
-      p.ssq_parts = ssq_parts;
-      p.norm_d = d.d;
-      p.q_out = s->q;
-      p.kv = s->kv;
-      p.H = d.n_heads;
-      p.D = d.head_dim;
-      p.S_max = s->s_max;
-      p.layer = l;
-      p.cur_len = s->cur_len;
-      p.pos_ids = t->d_position_ids;
-      p.log2_theta = log2f(d.rope_theta);
-      gemm_finish_params(p);
-      ProfScope ps(s, st, MV_PROF_GEMM_QKV);
-      rc = launch_gemm(EPI_QKV, m->m_qkv[l], m->m_qkv[l], s->m_xb, p, st);
-    }
-    if (rc != MV_OK) break;
-    {
-      ProfScope ps(s, st, MV_PROF_ATTENTION);
-      rc = launch_tree_attention_n(s->m_kv, s->m_kv, 2 * l, 2 * l + 1, s->q, d.n_heads, d.head_dim, s->s_max,
-                                   s->cur_len, 0, s->s_max - n, t, n, 1.0f / sqrtf((float)d.head_dim), s->attn,
-                                   s->ws_attn, st);
-    }
-    if (rc != MV_OK) break;
-    {  // O projection + residual
-      GemmParams p = base_params(s, n);
-      p.M = d.d;
-      p.K = HD;
-      p.x = s->x;
-      p.xb = s->xb;
-      p.ssq_out = s->ssq;
-      gemm_finish_params(p);
-      ProfScope ps(s, st, MV_PROF_GEMM_O);
-      rc = launch_gemm(EPI_RESIDUAL, m->m_o[l], m->m_o[l], s->m_attn, p, st);
-    }
-    if (rc != MV_OK) break;
-    {  // gate/up + SiLU-gate
-      GemmParams p = base_params(s, n);
-      p.paired = 1;
-      p.F = d.ffn;
-      p.M = d.ffn;
-      p.K = d.d;
-      p.ssq = s->ssq;
-      p.ssq_parts = ssq_parts;
-      p.norm_d = d.d;
-      p.act = s->act;
-      gemm_finish_params(p);
-      ProfScope ps(s, st, MV_PROF_GEMM_GATE_UP);
-      rc = launch_gemm(EPI_SWIGLU, m->m_gate[l], m->m_up[l], s->m_xb, p, st);
-    }
-    if (rc != MV_OK) break;
-    {  // down + residual
-      GemmParams p = base_params(s, n);
-      p.M = d.d;
-      p.K = d.ffn;
-      p.x = s->x;
-      p.xb = s->xb;
-      p.ssq_out = s->ssq;
-      gemm_finish_params(p);
-      ProfScope ps(s, st, MV_PROF_GEMM_DOWN);
-      rc = launch_gemm(EPI_RESIDUAL, m->m_down[l], m->m_down[l], s->m_act, p, st);
-    }
-  }
-  if (rc == MV_OK && lm) {  // final RMSNorm (as a column scale) + LM head -> fp32 logits
-    GemmParams p = base_params(s, n);
+  // the projections, as chain phases: each phase's activations are the previous phase's output
+  auto qkv_phase = [&](int l) {  // QKV + RoPE + KV append
+    GemmPhase g;
+    g.epi = EPI_QKV;
+    g.a0 = g.a1 = m->m_qkv[l];
+    g.b = s->m_xb;
+    GemmParams& p = g.p = base_params(s, n);
+    p.M = 3 * HD;
+    p.K = d.d;
+    p.ssq = s->ssq;
+    p.ssq_parts = ssq_parts;
+    p.norm_d = d.d;
+    p.q_out = s->q;
+    p.kv = s->kv;
+    p.H = d.n_heads;
+    p.D = d.head_dim;
+    p.S_max = s->s_max;
+    p.layer = l;
+    p.cur_len = s->cur_len;
+    p.pos_ids = t->d_position_ids;
+    p.log2_theta = log2f(d.rope_theta);
+    return g;
+  };
+  auto residual_phase = [&](const CUtensorMap& w, const CUtensorMap& act, int K) {  // O or down + residual
+    GemmPhase g;
+    g.epi = EPI_RESIDUAL;
+    g.a0 = g.a1 = w;
+    g.b = act;
+    GemmParams& p = g.p = base_params(s, n);
+    p.M = d.d;
+    p.K = K;
+    p.x = s->x;
+    p.xb = s->xb;
+    p.ssq_out = s->ssq;
+    return g;
+  };
+  auto gate_up_phase = [&](int l) {  // gate/up + SiLU-gate
+    GemmPhase g;
+    g.epi = EPI_SWIGLU;
+    g.a0 = m->m_gate[l];
+    g.a1 = m->m_up[l];
+    g.b = s->m_xb;
+    GemmParams& p = g.p = base_params(s, n);
+    p.paired = 1;
+    p.F = d.ffn;
+    p.M = d.ffn;
+    p.K = d.d;
+    p.ssq = s->ssq;
+    p.ssq_parts = ssq_parts;
+    p.norm_d = d.d;
+    p.act = s->act;
+    return g;
+  };
+  auto lm_phase = [&]() {  // final RMSNorm (as a column scale) + LM head -> fp32 logits
+    GemmPhase g;
+    g.epi = EPI_STORE;
+    g.a0 = g.a1 = m->m_lm;
+    g.b = s->m_xb;
+    GemmParams& p = g.p = base_params(s, n);
     p.M = d.vocab;
     p.K = d.d;
     p.ssq = s->ssq;
@@ -335,9 +326,33 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     p.norm_d = d.d;
     p.out_f32 = s->logits;
     p.ld_out = s->ld_logits;
-    gemm_finish_params(p);
-    ProfScope ps(s, st, MV_PROF_GEMM_LM);
-    rc = launch_gemm(EPI_STORE, m->m_lm, m->m_lm, s->m_xb, p, st);
+    return g;
+  };
+  if (rc == MV_OK) {
+    GemmPhase g = qkv_phase(0);
+    ProfScope ps(s, st, MV_PROF_GEMM_QKV);
+    rc = launch_gemm_chain(&g, 1, nullptr, st);
+  }
+  for (int l = 0; l < d.n_layers && rc == MV_OK; ++l) {
+    {
+      ProfScope ps(s, st, MV_PROF_ATTENTION);
+      rc = launch_tree_attention_n(s->m_kv, s->m_kv, 2 * l, 2 * l + 1, s->q, d.n_heads, d.head_dim, s->s_max,
+                                   s->cur_len, 0, s->s_max - n, t, n, 1.0f / sqrtf((float)d.head_dim), s->attn,
+                                   s->ws_attn, st);
+    }
+    if (rc != MV_OK) break;
+    // O, gate/up and down of this layer, then the next layer's QKV (or the LM head): one launch
+    GemmPhase ch[kGemmMaxPhases];
+    int nph = 0;
+    ch[nph++] = residual_phase(m->m_o[l], s->m_attn, HD);
+    ch[nph++] = gate_up_phase(l);
+    ch[nph++] = residual_phase(m->m_down[l], s->m_act, d.ffn);
+    if (l + 1 < d.n_layers)
+      ch[nph++] = qkv_phase(l + 1);
+    else if (lm)
+      ch[nph++] = lm_phase();
+    ProfScope ps(s, st, MV_PROF_GEMM_CHAIN);
+    rc = launch_gemm_chain(ch, nph, s->chain_flags, st);
   }
   return rc;
 }
@@ -442,6 +457,7 @@ extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16
   s->ws_attn = b + L.attn_ws;
   s->ws_post = b + L.post;
   s->ws_heads = b + L.heads;
+  s->chain_flags = reinterpret_cast<unsigned int*>(b + L.chain);
   const int HD = d.n_heads * d.head_dim;
   bool ok = gemm_act_map(&s->m_xb, s->xb, kTok, d.d) && gemm_act_map(&s->m_attn, s->attn, kTok, HD) &&
             gemm_act_map(&s->m_act, s->act, kTok, d.ffn);
