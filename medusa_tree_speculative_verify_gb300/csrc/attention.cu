@@ -25,7 +25,8 @@ constexpr int kThreads = 128;
 constexpr int kKeys = 64;   // keys per tile
 constexpr int kRows = 64;   // query rows per CTA (tree nodes, padded)
 constexpr int kStages = 2;  // 80 KB of shared memory at D = 128: two CTAs share an SM
-constexpr int kMinTiles = 2;    // key tiles per split at the longest prefix, at least
+constexpr int kMinTiles = 2;       // key tiles per split at the longest prefix, at least (sets the cluster size)
+constexpr int kTilesPerSplit = 1;  // key tiles per working split at the actual prefix (measured best)
 // CTAs per cluster. Measured on GB300: with clusters of 8 (two 81 KB CTAs per SM) a few clusters of a 32-head
 // launch only start when others leave (a second wave, +11 us at short prefixes), although the occupancy query
 // reports room for all; clusters of 4 start together.
@@ -101,10 +102,14 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
     return;
   }
   const int total_tiles = (P + n + kKeys - 1) / kKeys;
-  // The cluster is sized for the longest prefix; at a shorter one some splits get no tile and contribute an
-  // empty partial (max -inf, sum 0) to the merge.
-  const int t_begin = (int)((long long)split * total_tiles / C);
-  const int t_end = (int)((long long)(split + 1) * total_tiles / C);
+  // The cluster is sized for the longest prefix. At this prefix only S splits get tiles, about kTilesPerSplit
+  // each (a split costs a merge). With S = 1 the first CTA does the whole head and writes it directly; the
+  // others leave at once (no cluster barrier is used then). With S > 1 the idle splits still take part in the
+  // barriers but contribute nothing to the merge.
+  const int S = max(1, min(C, (total_tiles + kTilesPerSplit - 1) / kTilesPerSplit));
+  if (S == 1 && split > 0) return;
+  const int t_begin = split < S ? (int)((long long)split * total_tiles / S) : 0;
+  const int t_end = split < S ? (int)((long long)(split + 1) * total_tiles / S) : 0;
   const int count = t_end - t_begin;
 
   auto issue = [&](int i) {  // tile t_begin + i into stage i % kStages
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-  if (C == 1) {  // one split per head (a short prefix): normalise and write, nothing to merge
+  if (S == 1) {  // one split for the head (a short prefix): normalise and write, nothing to merge
     const float i0 = l0 > 0.0f ? 1.0f / l0 : 0.0f, i1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
 #pragma unroll
     for (int dn = 0; dn < DN; ++dn) {
@@ -295,14 +300,14 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
   const int r0 = split * n / C, r1 = (split + 1) * n / C;  // this CTA's query rows
   const uint32_t ml_s = smem_u32(pml), po_s = smem_u32(po);
   if (tid < r1 - r0) {
-    // w_s = 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s' for the row's C splits (rank order)
+    // w_s = 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s' for the row's S splits (rank order)
     const int q = r0 + tid;
     float m[kMaxSplits], l[kMaxSplits];
 #pragma unroll
     for (int s = 0; s < kMaxSplits; ++s) {
       m[s] = -INFINITY;
       l[s] = 0.0f;
-      if (s < C) {
+      if (s < S) {
         const float2 v = ld_cluster_f2(map_rank(ml_s + (uint32_t)(q * 8), (uint32_t)s));
         m[s] = v.x;
         l[s] = v.y;
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
     float L = 0.0f;
 #pragma unroll
     for (int s = 0; s < kMaxSplits; ++s) {
-      m[s] = s < C ? exp2f(m[s] - base) : 0.0f;
+      m[s] = s < S ? exp2f(m[s] - base) : 0.0f;
       L += m[s] * l[s];
     }
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
@@ -329,11 +334,11 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
     float4 v[kMaxSplits];
 #pragma unroll
     for (int s = 0; s < kMaxSplits; ++s)
-      if (s < C) v[s] = ld_cluster_f4(map_rank(off, (uint32_t)s));
+      if (s < S) v[s] = ld_cluster_f4(map_rank(off, (uint32_t)s));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int s = 0; s < kMaxSplits; ++s) {
-      if (s < C) {
+      if (s < S) {
         const float w = pw[rq * kMaxSplits + s];
         acc.x += w * v[s].x;
         acc.y += w * v[s].y;
