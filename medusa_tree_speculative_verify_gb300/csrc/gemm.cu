@@ -40,7 +40,8 @@ constexpr int kBBytes = BN * BK * 2;  // 8 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kEpiThreads = 128;
 constexpr int kThreads = 64 + kEpiThreads;
-constexpr int kTmemCols = 2 * BN;
+constexpr int kAcc = 2;  // accumulator buffers in tensor memory (the MMA may run kAcc - 1 tiles ahead)
+constexpr int kTmemCols = kAcc * BN;
 constexpr int kMaxCluster = 8;  // CTAs per cluster (portable limit)
 constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)BM * BN * 4 + 256;
 
@@ -309,6 +310,7 @@ struct ChainArgs {
   GemmParams ph[kGemmMaxPhases];
   int epi[kGemmMaxPhases];
   int n_phases, csize;
+  int indep;            // 1: the phases do not read each other's outputs (no counters, no waits)
   unsigned int* flags;  // [kGemmChainFlagWords]: phase-done counters, then the exit counter
 };
 
@@ -330,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
   float* part = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);  // [BN tokens][BM rows]
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], drain, pfull, pfree;
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[kAcc], tempty[kAcc], drain, pfull, pfree;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int s_abort;
   __shared__ EpiConst s_ec;
@@ -352,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kAcc; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 4);
     }
@@ -403,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           bool got = true;
           if (ph == 0) {
             pdl_wait();
-          } else {
+          } else if (!ca.indep) {
             got = wait_count(ca.flags + ph - 1, gridDim.x);
             flag_timeout |= !got;
             asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes -> TMA reads
@@ -465,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         tile_range(p, t0, t1);
         const int kb0 = rank * p.kbt / C, kb1 = (rank + 1) * p.kbt / C;
         for (int tile = t0; ok && tile < t1; ++tile, ++n) {
-          const int buf = n & 1, rr = n >> 1;
+          const int buf = n % kAcc, rr = n / kAcc;
           if (s_abort || !mbar_wait(&tempty[buf], (uint32_t)((rr & 1) ^ 1))) {
             ok = false;
             break;
@@ -573,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         if (!ok) break;
       }
       // every phase before `upto` is finished in this CTA: publish them, in order (one count per CTA and phase)
-      const int upto = ph < NP ? ph : NP - 1;
+      const int upto = ca.indep ? 0 : (ph < NP ? ph : NP - 1);
       if (published < upto) {
         epi_bar();  // every output of those phases written by this CTA
         if (i == 0) {
@@ -586,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       if (ec_ph != ph) {
         // this phase's scales are sums of squares the previous phase wrote: wait until every CTA finished it
         bool got = true;
-        if (ph > 0 && i == 0) got = wait_count(ca.flags + ph - 1, gridDim.x);
+        if (ph > 0 && !ca.indep && i == 0) got = wait_count(ca.flags + ph - 1, gridDim.x);
         if (epi_any(!got)) {
           if (i == 0) mv_set_error(err, 12, MV_DEVERR_TIMEOUT);
           s_abort = 1;
@@ -596,8 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         load_epi_const(ca.ph[ph], &s_ec, i);  // scales and positions: the same for every tile of the phase
         ec_ph = ph;
       }
-      const int buf = n & 1;
-      bool got = !s_abort && mbar_wait(&tfull[buf], (uint32_t)((n >> 1) & 1));
+      const int buf = n % kAcc;
+      bool got = !s_abort && mbar_wait(&tfull[buf], (uint32_t)((n / kAcc) & 1));
       // the partial buffer is free again once every CTA of the cluster has finished tile n - 1
       if (got && n >= 1) got = mbar_wait_cluster(&pfree, (uint32_t)((n - 1) & 1));
       if (epi_any(!got)) {  // uniform over the 4 epilogue warps
@@ -637,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     tmem_dealloc(tmem_base, kTmemCols);
   }
   // the last CTA out leaves the chain's counters at zero for the next launch
-  if (threadIdx.x == 0 && ca.flags && ca.n_phases > 1) {
+  if (threadIdx.x == 0 && ca.flags && ca.n_phases > 1 && !ca.indep) {
     __threadfence();
     if (atomicAdd(ca.flags + kGemmMaxPhases, 1u) == gridDim.x - 1) {
       for (int k = 0; k < kGemmChainFlagWords; ++k) ca.flags[k] = 0u;
@@ -665,6 +667,14 @@ bool gemm_weight_map_packed(CUtensorMap* map, const void* w, int rows, int K, in
   const uint64_t strides[2] = {(uint64_t)BK * 2, (uint64_t)tile_rows * BK * 2};
   const uint32_t box[3] = {(uint32_t)BK, (uint32_t)tile_rows, 1};
   return mv_encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool gemm_act_map_strided(CUtensorMap* map, const void* x, int rows, int K, int ld) {
+  const uint64_t dims[2] = {(uint64_t)K, (uint64_t)rows};
+  const uint64_t strides[1] = {(uint64_t)ld * 2};
+  const uint32_t box[2] = {(uint32_t)BK, (uint32_t)BN};
+  return mv_encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, strides, box,
                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -746,8 +756,8 @@ void gemm_finish_params(GemmParams& p) {
   p.grid = p.csize * p.n_clusters;
 }
 
-mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStream_t stream) {
-  if (n < 1 || n > kGemmMaxPhases || (n > 1 && !flags)) return MV_ERR_INVALID_ARG;
+mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStream_t stream, bool independent) {
+  if (n < 1 || n > kGemmMaxPhases || (n > 1 && !independent && !flags)) return MV_ERR_INVALID_ARG;
   ChainMaps maps;
   ChainArgs ca;
   memset(&maps, 0, sizeof(maps));
@@ -774,7 +784,8 @@ mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStrea
   }
   ca.n_phases = n;
   ca.csize = csize;
-  ca.flags = flags;
+  ca.indep = independent ? 1 : 0;
+  ca.flags = independent ? nullptr : flags;
   static int smem_flags[64] = {0};
   if (!mv_set_smem_once((const void*)gemm_kernel, (int)kSmemBytes, smem_flags)) return MV_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};

@@ -55,9 +55,13 @@ size_t gemm_smem_bytes();
 bool gemm_weight_map(CUtensorMap* map, const void* w, int rows, int K, int box_rows);
 bool gemm_weight_map_packed(CUtensorMap* map, const void* w, int rows, int K, int tile_rows);
 bool gemm_act_map(CUtensorMap* map, const void* x, int rows, int K);
+// rows x K bf16 activations whose rows are ld elements apart (ld % 8 == 0)
+bool gemm_act_map_strided(CUtensorMap* map, const void* x, int rows, int K, int ld);
 void gemm_finish_params(GemmParams& p);
 mv_status launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                       const GemmParams& p, cudaStream_t stream);
 // ph[i].p must have its shape fields set (M, K, paired, F); the cluster plan is computed here. flags: see above
 // (may be null when n == 1).
-mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStream_t stream);
+// independent: the phases read nothing another phase writes (no counters; flags may be null).
+mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStream_t stream,
+                            bool independent = false);

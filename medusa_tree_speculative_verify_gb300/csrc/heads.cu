@@ -17,6 +17,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "gemm.cuh"
 #include "kernels.cuh"
 
 namespace {
@@ -332,6 +333,207 @@ mv_status launch_group(HeadsArgs a, int B, int V, bool with_lm, int w2_ctas, cud
 
 }  // namespace
 
+
+// ---------------------------------------------------------------------------------------------------------
+// Batched path (B >= 2): the heads as tcgen05 projections over the B rows, which read every weight once (the
+// split-K GEMV above re-reads them per group of rows and its CUDA-core multiply-adds grow with B).
+//   t = W1 h                      one projection over the K heads' W1 stacked ([K*d][d]), fp32 out
+//   u = SiLU(t) + h               kept to about fp32 precision as a bf16 pair: u_hi = bf16(u), u_lo = bf16(u - u_hi)
+//                                 in token rows b and 16 + b of the activations
+//   z_k = W2_k u_hi + W2_k u_lo   one projection per head over those 32 rows (one launch, independent phases)
+//   top-k of z_k per row; root = argmax of W_lm h
+// ---------------------------------------------------------------------------------------------------------
+namespace {
+
+constexpr int kHiLo = 16;  // lo rows start here (B <= 16)
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__global__ void __launch_bounds__(256) heads_prep_kernel(const float* t, const uint16_t* h, int B, int Kd, int d,
+                                                         uint16_t* u) {
+  pdl_wait();
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < (size_t)kHiLo * Kd;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const int j = (int)(e / Kd), R = (int)(e % Kd);
+    uint16_t hi = 0, lo = 0;
+    if (j < B) {
+      const float uf = silu(__ldcg(t + (size_t)j * Kd + R)) +
+                       __bfloat162float(__ushort_as_bfloat16(h[(size_t)j * d + R % d]));
+      const __nv_bfloat16 bh = __float2bfloat16_rn(uf);
+      hi = __bfloat16_as_ushort(bh);
+      lo = __bfloat16_as_ushort(__float2bfloat16_rn(uf - __bfloat162float(bh)));
+    }
+    u[(size_t)j * Kd + R] = hi;
+    u[(size_t)(kHiLo + j) * Kd + R] = lo;
+  }
+}
+
+// One CTA per (head or LM row, batch row). The row (hi + lo products summed) is staged in shared memory when it
+// fits, then k rounds of a block-wide argmax each take the best entry that comes after the previous pick in the
+// order (larger value first, lower id on ties), so nothing has to be marked as taken.
+constexpr int kTopThreads = 256;
+constexpr size_t kTopSmemMax = 160 * 1024;
+
+MV_DEV void better_of(float& bv, int& bi, float v, int i) {
+  if (bi < 0 || (i >= 0 && vi_better(v, i, bv, bi))) {
+    bv = v;
+    bi = i;
+  }
+}
+
+template <bool kStaged>
+__global__ void __launch_bounds__(kTopThreads) heads_topk_kernel(const float* zl, int ldz, const float* lm, int V,
+                                                                 int K, int topk, int32_t* out_idx, float* out_val,
+                                                                 int32_t* out_root) {
+  extern __shared__ float row[];  // [V] when staged
+  __shared__ float s_v[kTopThreads / 32];
+  __shared__ int s_i[kTopThreads / 32];
+  pdl_wait();
+  const int mat = blockIdx.x, b = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool is_lm = mat == K;
+  const int k = is_lm ? 1 : topk;
+  const float* z0 = is_lm ? lm + (size_t)b * V : zl + (size_t)b * ldz + (size_t)mat * V;
+  const float* z1 = is_lm ? nullptr : zl + (size_t)(kHiLo + b) * ldz + (size_t)mat * V;
+  auto zat = [&](int v) { return z1 ? __ldcg(z0 + v) + __ldcg(z1 + v) : __ldcg(z0 + v); };
+  if constexpr (kStaged) {
+    for (int v = tid; v < V; v += kTopThreads) row[v] = zat(v);
+    __syncthreads();
+  }
+  float pv = INFINITY;  // the previous pick (none yet: every entry comes after it)
+  int pi = -1;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int bi = -1;
+    for (int v = tid; v < V; v += kTopThreads) {
+      const float z = kStaged ? row[v] : zat(v);
+      if (pi < 0 || vi_better(pv, pi, z, v)) better_of(bv, bi, z, v);  // z comes after the previous pick
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      better_of(bv, bi, ov, oi);
+    }
+    if (lane == 0) {
+      s_v[warp] = bv;
+      s_i[warp] = bi;
+    }
+    __syncthreads();
+    bv = s_v[0];
+    bi = s_i[0];
+#pragma unroll
+    for (int w = 1; w < kTopThreads / 32; ++w) better_of(bv, bi, s_v[w], s_i[w]);
+    __syncthreads();  // every thread read this round's partials
+    if (tid == 0) {
+      if (is_lm) {
+        if (out_root) out_root[b] = bi;
+      } else {
+        out_idx[((size_t)b * K + mat) * topk + r] = bi;
+        if (out_val) out_val[((size_t)b * K + mat) * topk + r] = bv;
+      }
+    }
+    pv = bv;
+    pi = bi;
+    if (bi < 0) break;  // fewer than k entries (cannot happen for topk <= V)
+  }
+}
+
+size_t heads_gemm_ws_bytes(int B, int d, int K, int V, bool lm) {
+  const size_t Kd = (size_t)K * d;
+  size_t bytes = 0;
+  bytes += align256((size_t)B * Kd * 4);            // t
+  bytes += align256((size_t)2 * kHiLo * Kd * 2);    // u (hi rows, lo rows)
+  bytes += align256((size_t)2 * kHiLo * K * V * 4); // z (hi and lo products)
+  if (lm) bytes += align256((size_t)B * V * 4);     // LM row
+  return bytes + 256;
+}
+
+mv_status launch_heads_gemm(const uint16_t* h, int B, int d, int K, const uint16_t* w1, const uint16_t* w2, int V,
+                            int topk, const uint16_t* w_lm, int32_t* out_idx, float* out_val, int32_t* out_root,
+                            void* ws, cudaStream_t stream) {
+  const int Kd = K * d;
+  char* p = static_cast<char*>(ws);
+  float* t = reinterpret_cast<float*>(p);
+  p += align256((size_t)B * Kd * 4);
+  uint16_t* u = reinterpret_cast<uint16_t*>(p);
+  p += align256((size_t)2 * kHiLo * Kd * 2);
+  float* zl = reinterpret_cast<float*>(p);
+  p += align256((size_t)2 * kHiLo * K * V * 4);
+  float* lmz = w_lm ? reinterpret_cast<float*>(p) : nullptr;
+  auto base = [&](int n) {
+    GemmParams q{};
+    q.n_tok = n;
+    q.err = mv_error_word();
+    return q;
+  };
+  // t = W1 h (and the LM row, independent of it, in the same launch)
+  GemmPhase ph[kGemmMaxPhases];
+  int np = 0;
+  {
+    GemmPhase& g = ph[np++];
+    g.epi = EPI_STORE;
+    if (!gemm_weight_map(&g.a0, w1, Kd, d, 128) || !gemm_act_map(&g.b, h, B, d)) return MV_ERR_CUDA;
+    g.a1 = g.a0;
+    g.p = base(B);
+    g.p.M = Kd;
+    g.p.K = d;
+    g.p.out_f32 = t;
+    g.p.ld_out = Kd;
+  }
+  if (w_lm) {
+    GemmPhase& g = ph[np++];
+    g.epi = EPI_STORE;
+    if (!gemm_weight_map(&g.a0, w_lm, V, d, 128) || !gemm_act_map(&g.b, h, B, d)) return MV_ERR_CUDA;
+    g.a1 = g.a0;
+    g.p = base(B);
+    g.p.M = V;
+    g.p.K = d;
+    g.p.out_f32 = lmz;
+    g.p.ld_out = V;
+  }
+  mv_status s = launch_gemm_chain(ph, np, nullptr, stream, true);
+  if (s != MV_OK) return s;
+  // u = SiLU(t) + h as a bf16 (hi, lo) pair
+  const int blocks = (int)std::min<size_t>(((size_t)kHiLo * Kd + 255) / 256, (size_t)mv_sm_count() * 8);
+  if (mv_launch(heads_prep_kernel, dim3(blocks), dim3(256), 0, stream, t, h, B, Kd, d, u) != cudaSuccess)
+    return MV_ERR_CUDA;
+  if ((s = mv_last_launch("heads_prep")) != MV_OK) return s;
+  // z_k = W2_k u for the 32 rows (hi and lo), up to kGemmMaxPhases heads per launch
+  for (int k0 = 0; k0 < K; k0 += kGemmMaxPhases) {
+    const int nk = std::min(kGemmMaxPhases, K - k0);
+    for (int i = 0; i < nk; ++i) {
+      const int kk = k0 + i;
+      GemmPhase& g = ph[i];
+      g.epi = EPI_STORE;
+      if (!gemm_weight_map(&g.a0, w2 + (size_t)kk * V * d, V, d, 128) ||
+          !gemm_act_map_strided(&g.b, u + (size_t)kk * d, 2 * kHiLo, d, Kd))
+        return MV_ERR_CUDA;
+      g.a1 = g.a0;
+      g.p = base(2 * kHiLo);
+      g.p.M = V;
+      g.p.K = d;
+      g.p.out_f32 = zl + (size_t)kk * V;
+      g.p.ld_out = K * V;
+    }
+    if ((s = launch_gemm_chain(ph, nk, nullptr, stream, true)) != MV_OK) return s;
+  }
+  const size_t row_bytes = (size_t)V * sizeof(float);
+  const dim3 grid(K + (w_lm ? 1 : 0), B);
+  cudaError_t e;
+  if (row_bytes <= kTopSmemMax) {
+    static int flags[64] = {0};
+    if (!mv_set_smem_once((const void*)heads_topk_kernel<true>, (int)row_bytes, flags)) return MV_ERR_CUDA;
+    e = mv_launch(heads_topk_kernel<true>, grid, dim3(kTopThreads), row_bytes, stream, (const float*)zl, K * V,
+                  (const float*)lmz, V, K, topk, out_idx, out_val, out_root);
+  } else {
+    e = mv_launch(heads_topk_kernel<false>, grid, dim3(kTopThreads), 0, stream, (const float*)zl, K * V,
+                  (const float*)lmz, V, K, topk, out_idx, out_val, out_root);
+  }
+  if (e != cudaSuccess) return MV_ERR_CUDA;
+  return mv_last_launch("heads_topk");
+}
+
+}  // namespace
+
 int heads_w2_ctas_per_mat(int n_mat, int V) {
   const int sms = mv_sm_count();
   int c = max(1, (2 * sms + n_mat - 1) / n_mat);
@@ -344,7 +546,9 @@ size_t heads_ws_bytes(int B, int d, int K, int V, int topk) {
   size_t bytes = 256;                                                   // tickets
   bytes += (size_t)min(B, 4) * K * d * sizeof(float);                   // u
   bytes += (size_t)n_mat * c * min(B, 4) * topk * (sizeof(float) + 4);  // candidates
-  return bytes + 256;
+  bytes += 256;
+  if (B >= 2) bytes = std::max(bytes, heads_gemm_ws_bytes(B, d, K, V, true));  // the batched path
+  return bytes;
 }
 
 mv_status launch_heads(const uint16_t* h, const float* x, const mv_posterior_result* res, float norm_eps, int B,
@@ -417,6 +621,9 @@ extern "C" mv_status medusa_heads_topk(const mv_bf16* h, int32_t B, int32_t d, i
   if ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(w1) | reinterpret_cast<uintptr_t>(w2) |
        reinterpret_cast<uintptr_t>(w_lm)) & 15)
     return MV_ERR_SHAPE;
+  if (B >= 2)  // several rows: the weights are read once by the tensor-core projections
+    return launch_heads_gemm(h, B, d, K, w1, w2, V, topk, w_lm, out_idx, out_val, out_root, workspace,
+                             static_cast<cudaStream_t>(stream));
   return launch_heads(h, nullptr, nullptr, 0.0f, B, d, K, w1, w2, V, topk, w_lm, out_idx, out_val, out_root,
                       nullptr, workspace, static_cast<cudaStream_t>(stream));
 }
