@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(256) heads_prep_kernel(const float* t, const u
 // One CTA per (head or LM row, batch row). The row (hi + lo products summed) is staged in shared memory when it
 // fits, then k rounds of a block-wide argmax each take the best entry that comes after the previous pick in the
 // order (larger value first, lower id on ties), so nothing has to be marked as taken.
-constexpr int kTopThreads = 256;
+constexpr int kTopThreads = 1024;
 constexpr size_t kTopSmemMax = 160 * 1024;
 
 MV_DEV void better_of(float& bv, int& bi, float v, int i) {
