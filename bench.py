@@ -39,6 +39,15 @@ PROMPT_LEN = 128
 TREE = dict(n_nodes=64, depth=4, topk=10)
 
 
+def tree_choices(name):
+    """The bench's tree: the synthetic 64-node tree (default) or the page's own 63 choices ("大模型推理 memory
+    bandwidth bound (5) - Medusa", 二.2), both 64 nodes of depth 4 with top-10 heads."""
+    if name == "page":
+        with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "tests", "golden", "page4_tree.json")) as f:
+            return [tuple(c) for c in json.load(f)["medusa_choices"]]
+    return synth.synthetic_tree_choices(TREE["n_nodes"], TREE["depth"], TREE["topk"])
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -152,7 +161,7 @@ def sample_weights(seed=0, layers=2, device=None):
     return sub, w
 
 
-def oracle_sample(sub, w, seed=0, min_seconds=10.0, max_reps=20):
+def oracle_sample(sub, w, seed=0, min_seconds=10.0, max_reps=20, tree_name="synthetic"):
     """Times the float64 oracle on a bounded sample of one 7B verify step.
 
     Sample: sub.n_layers of the 32 decoder layers over the 64 tree tokens at prefix 128, the LM head, the
@@ -166,7 +175,7 @@ def oracle_sample(sub, w, seed=0, min_seconds=10.0, max_reps=20):
 
     dims = synth.LLAMA7B
     layers = sub.n_layers
-    tree = tree_buffers(synth.synthetic_tree_choices(64, 4, 10), 10)
+    tree = tree_buffers(tree_choices(tree_name), TREE["topk"])
     P = PROMPT_LEN
     toks = synth.prompt_tokens(seed, 64, dims.vocab, name="tree_tokens").numpy()
     no_lm = dict(w)
@@ -201,7 +210,7 @@ def run_gpu(args, world, rank, local):
     dims = synth.LLAMA7B
     w = mv.pack_model_weights(synth.packed_weights(dims, 0, torch.bfloat16, "cuda"), drop_source=True)
     model = mv.Model(dims, w)
-    tree = mv.Tree(synth.synthetic_tree_choices(TREE["n_nodes"], TREE["depth"], TREE["topk"]), TREE["topk"])
+    tree = mv.Tree(tree_choices(args.tree), TREE["topk"])
     n_steps_total = args.warmup + 7 * args.steps + 8
     s_max = PROMPT_LEN + (TREE["depth"] + 1) * n_steps_total + 64
     s_max = (s_max + 63) // 64 * 64
@@ -308,7 +317,9 @@ def run_gpu(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights, random prompt)",
         "config": {"workload": "Llama-7B shape (32 layers, d 4096, 32x128 heads, FFN 11008, vocab 32000) + 4 Medusa "
-                               "heads, synthetic 64-node/41-path tree, 128-token prompt, greedy verify step",
+                               "heads, " + ("the page's own 63-choice (64-node, 42-path) tree" if args.tree == "page"
+                                            else "synthetic 64-node/41-path tree") +
+                               ", 128-token prompt, greedy verify step",
                    "tree_nodes": 64, "prompt": PROMPT_LEN, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (14.4 GB of weights streamed per step)"},
         "tokens_per_s": steps_per_s * tokens_per_step, "tokens_per_step": tokens_per_step,
@@ -463,6 +474,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tree", default="synthetic", choices=["synthetic", "page"],
+                    help="the tree of the verify step: the synthetic 64-node tree or the page's own 63 choices")
     ap.add_argument("--micro", choices=sorted(MICRO) + MICRO_OTHER, help="time one kernel alone and exit")
     args = ap.parse_args()
     world, rank, local = dist_setup()
@@ -475,8 +488,8 @@ def main():
         if rank != 0:
             return
         sub, w = sample_weights()
-        oracle_sample(sub, w, min_seconds=0.0, max_reps=max(1, min(args.warmup, 2)))   # warm-up
-        per_step, sample, _ = oracle_sample(sub, w, min_seconds=0.0, max_reps=max(2, min(args.steps, 20)))
+        oracle_sample(sub, w, min_seconds=0.0, max_reps=max(1, min(args.warmup, 2)), tree_name=args.tree)   # warm-up
+        per_step, sample, _ = oracle_sample(sub, w, min_seconds=0.0, max_reps=max(2, min(args.steps, 20)), tree_name=args.tree)
         v = 1.0 / per_step
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / v, "higher_is_better": True,
@@ -492,7 +505,7 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
             sub, w = sample_weights()
-            per_step, sample, wall = oracle_sample(sub, w)
+            per_step, sample, wall = oracle_sample(sub, w, tree_name=args.tree)
             line["cpu_baseline"] = {"value": 1.0 / per_step, "unit": "steps/s", "cores": os.cpu_count(),
                                     "kind": "oracle", "sample": sample, "sample_wall_s": wall}
         print(json.dumps(line))

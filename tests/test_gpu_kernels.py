@@ -5,7 +5,9 @@ outputs must be within 2e-2 relative / 1e-2 absolute of the float64 oracle; an a
 only where the oracle's margin is below 1e-3; a top-k index may differ only where the two values it separates
 are within 1e-3 of each other (a near tie).
 """
+import json
 import math
+import os
 
 import numpy as np
 import pytest
@@ -41,8 +43,15 @@ def i32(a):
     return torch.as_tensor(np.asarray(a), dtype=torch.int32, device="cuda")
 
 
+def page_tree_choices():
+    """The 63 choices printed on "大模型推理 memory bandwidth bound (5) - Medusa", 二.2 (64 nodes, 42 paths, depth 4)."""
+    with open(os.path.join(os.path.dirname(__file__), "golden", "page4_tree.json")) as f:
+        return [tuple(c) for c in json.load(f)["medusa_choices"]]
+
+
 TREES = {
     "synthetic64": (lambda: synth.synthetic_tree_choices(64, 4, 10), 10),
+    "page63": (page_tree_choices, 10),
     "dense1x2x3": (lambda: synth.dense_tree_choices([2, 3]), 10),
     "chain5": (lambda: [tuple([0] * k) for k in range(1, 6)], 10),
     "root": (lambda: [], 10),
@@ -57,7 +66,7 @@ def both_trees(name):
 
 # --------------------------------------------------------------------------------------------- candidates
 
-@pytest.mark.parametrize("name", ["synthetic64", "dense1x2x3", "chain5", "root"])
+@pytest.mark.parametrize("name", ["synthetic64", "page63", "dense1x2x3", "chain5", "root"])
 def test_build_candidates_bit_exact(name):
     t, o = both_trees(name)
     K = max(1, o["depth"])
@@ -98,11 +107,12 @@ def _run_posterior(logits, tokens, t, mode, T=0.7, eps=0.09, delta=0.3):
     return mv.result_dict(out), stats.cpu().numpy(), amax.cpu().numpy()
 
 
+@pytest.mark.parametrize("tree", ["synthetic64", "page63"])
 @pytest.mark.parametrize("mode", [GREEDY, TYPICAL])
 @pytest.mark.parametrize("seed", range(10))
-def test_posterior_planted_full_size(mode, seed):
+def test_posterior_planted_full_size(mode, seed, tree):
     """64 nodes x 32000 vocabulary, logits ~N(0, 3^2), an agreement planted along a random path."""
-    t, o = both_trees("synthetic64")
+    t, o = both_trees(tree)
     r = o["retrieve"]
     p = int(synth.randint(seed, "plant_path", 1, 0, len(r))[0])
     path = [int(x) for x in r[p] if x >= 0]
@@ -276,9 +286,10 @@ def _attn_case(H, D, P, tree_name, S_max=None, seed=0):
 
 
 @pytest.mark.parametrize("P", [64, 512, 1024, 4096])
-def test_tree_attention_full_size(P):
-    """32 heads x 128 dims, the synthetic 64-node tree, q/k/v ~N(0,1)."""
-    _attn_case(32, 128, P, "synthetic64")
+@pytest.mark.parametrize("tree", ["synthetic64", "page63"])
+def test_tree_attention_full_size(P, tree):
+    """32 heads x 128 dims, the synthetic 64-node tree or the page's own, q/k/v ~N(0,1)."""
+    _attn_case(32, 128, P, tree)
 
 
 @pytest.mark.parametrize("H,D,P,tree,S_max", [(3, 16, 0, "dense1x2x3", None), (2, 32, 5, "dense1x2x3", 40),

@@ -7,7 +7,10 @@ margin is below the bf16 tolerance; every GPU token is also checked by teacher f
 ("大模型推理 memory bandwidth bound (5) - Medusa", 二.1 medusa_generate(); greedy output identical to the base
 model: "Phi-3-mini-128k-instruct_rai_1.8.0_medusa_1.0_npu", 2️⃣).
 """
+import dataclasses
+import json
 import math
+import os
 
 import numpy as np
 import pytest
@@ -65,12 +68,12 @@ DIMS = synth.TINY
 S_MAX = 256
 
 
-def _setup(tree_choices, topk=10, packed=True):
-    w = synth.packed_weights(DIMS, 0, torch.bfloat16, "cuda")
-    model = mv.Model(DIMS, mv.pack_model_weights(w) if packed else w)
+def _setup(tree_choices, topk=10, packed=True, dims=DIMS):
+    w = synth.packed_weights(dims, 0, torch.bfloat16, "cuda")
+    model = mv.Model(dims, mv.pack_model_weights(w) if packed else w)
     tree = mv.Tree(tree_choices, topk)
     sess = mv.Session(model, tree, S_MAX)
-    om = Backbone(DIMS, synth.unpacked_getter(DIMS, w))
+    om = Backbone(dims, synth.unpacked_getter(dims, w))
     return w, model, tree, sess, om, tree_buffers(tree_choices, topk)
 
 
@@ -156,10 +159,18 @@ def _margin_ok(gen, prompt, om):
     return first_close
 
 
-@pytest.mark.parametrize("tree,packed", [("dense", True), ("synthetic", True), ("dense", False)])
+@pytest.mark.parametrize("tree,packed", [("dense", True), ("synthetic", True), ("dense", False), ("page", True)])
 def test_greedy_decode_equals_ar(tree, packed):
-    choices = synth.dense_tree_choices([2, 3]) if tree == "dense" else synth.synthetic_tree_choices(64, 2, 10)
-    _, _, _, sess, om, ot = _setup(choices, packed=packed)
+    dims = DIMS
+    if tree == "dense":
+        choices = synth.dense_tree_choices([2, 3])
+    elif tree == "synthetic":
+        choices = synth.synthetic_tree_choices(64, 2, 10)
+    else:  # the page's own 63-choice tree ("大模型推理 memory bandwidth bound (5) - Medusa", 二.2): depth 4, 4 heads
+        with open(os.path.join(os.path.dirname(__file__), "golden", "page4_tree.json")) as f:
+            choices = [tuple(c) for c in json.load(f)["medusa_choices"]]
+        dims = dataclasses.replace(DIMS, n_medusa=4)
+    _, _, _, sess, om, ot = _setup(choices, packed=packed, dims=dims)
     p = _prompt().numpy()
     gen, accs = _gpu_decode(sess, p, 16, mv.AcceptParams(GREEDY))
     first_close = _margin_ok(gen, p, om)
