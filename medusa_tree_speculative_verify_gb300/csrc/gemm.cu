@@ -24,6 +24,8 @@
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer + TMEM owner, warps 2..5 = epilogue
 // (warp w reads TMEM lanes 32*(w%4) .. +31). Every mbarrier wait is bounded; on expiry the kernel records
 // MV_DEVERR_TIMEOUT, lets its in-flight copies and MMAs land, frees its tensor memory and returns.
+#include <float.h>
+
 #include <algorithm>
 #include <cstring>
 
@@ -194,9 +196,31 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, 
       const int t = r0 + u * cs;
       if (t >= kTokPerThread) break;
       const int j = w + 4 * t;
-      if (j >= ntok || R >= p.M) continue;
+      if (j >= ntok) continue;  // uniform over the warp (the shuffles below need every lane)
       const float s = ec->scale[j];
       const float4 v = make_float4(acc[u].x * s, acc[u].y * s, acc[u].z * s, acc[u].w * s);
+      if (p.row_max) {  // the tile's max and first argmax for token j (the posterior's greedy statistics)
+        float m = -FLT_MAX;
+        int mi = 0x7fffffff;
+        const float vq[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (R + q < p.M && vq[q] > m) {
+            m = vq[q];
+            mi = R + q;
+          }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+          const float om = __shfl_xor_sync(0xffffffffu, m, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, mi, o);
+          if (om > m || (om == m && oi < mi)) {
+            m = om;
+            mi = oi;
+          }
+        }
+        if (l == 0) p.row_max[tile * BN + j] = make_float2(m, __int_as_float(mi));
+      }
+      if (R >= p.M) continue;
       float* o = p.out_f32 + (size_t)j * p.ld_out + R;
       if (vec) {
         *reinterpret_cast<float4*>(o) = v;

@@ -21,6 +21,7 @@ struct GemmParams {
   // EPI_STORE
   float* out_f32;
   int ld_out;
+  float2* row_max;  // optional [n_tiles][64]: per 128-row tile and token, (max, first argmax as int bits)
   // EPI_RESIDUAL (x, xb are [n][M]; ssq_out is [n_tiles][64])
   float* x;
   uint16_t* xb;

@@ -59,7 +59,8 @@ MV_DEV Stat stat_merge(Stat a, Stat b, float inv_t, bool typical) {
 __global__ void __launch_bounds__(kThreads) posterior_kernel(
     const float* logits, int V, int ld, const int32_t* tree_tokens, const int32_t* __restrict__ retrieve,
     int n_nodes, int n_paths, int width, mv_accept_params prm, mv_posterior_result* out, float* node_stats_out,
-    int32_t* node_argmax_out, float* ws_stats, int32_t* ws_argmax, unsigned int* ticket, unsigned int* err) {
+    int32_t* node_argmax_out, float* ws_stats, int32_t* ws_argmax, unsigned int* ticket, unsigned int* err,
+    const float2* row_max, int n_row_tiles) {
   pdl_trigger();
   pdl_wait();
   const bool typical = prm.mode == MV_TYPICAL;
@@ -76,11 +77,20 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
   // pass 1: max and first argmax; pass 2 (typical): e = exp((z - max) / T) kept in place, Z = sum e;
   // pass 3 (typical): H = -sum p log(p + 1e-5) with p = e / Z. Rows longer than 32768 stream in chunks with
   // an online (rescaled) normaliser instead.
-  const int V4 = V >> 2;
+  // Greedy with row_max: the LM-head projection already left each 128-row tile's max and first argmax of
+  // every token; merging those replaces the pass over the row.
+  const bool from_tiles = row_max && !typical;
+  const int V4 = from_tiles ? 0 : V >> 2;
   const float4* row4 = reinterpret_cast<const float4*>(row);
   const bool in_regs = V4 <= kBatch * kThreads;
   float4 buf[kBatch];
   Stat a{-FLT_MAX, 0x7fffffff, 0.0f};
+  if (from_tiles) {
+    for (int t = tid; t < n_row_tiles; t += kThreads) {
+      const float2 e = __ldcg(row_max + (size_t)t * 64 + node);
+      a = stat_merge(a, Stat{e.x, __float_as_int(e.y), 0.0f}, 1.0f, false);
+    }
+  }
   for (int c0 = 0; c0 < V4; c0 += kBatch * kThreads) {
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
@@ -99,7 +109,8 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
       }
     }
   }
-  for (int i = 4 * V4 + tid; i < V; i += kThreads) stat_push(a, __ldcg(row + i), i, inv_t, typical && !in_regs);
+  if (!from_tiles)
+    for (int i = 4 * V4 + tid; i < V; i += kThreads) stat_push(a, __ldcg(row + i), i, inv_t, typical && !in_regs);
   const bool online = typical && !in_regs;
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
@@ -270,14 +281,14 @@ size_t posterior_ws_bytes(int n_nodes) { return (size_t)n_nodes * 5 * sizeof(flo
 
 mv_status launch_posterior(const float* logits, int V, int ld, const int32_t* d_tree_tokens, const mv_tree* t,
                            mv_accept_params prm, mv_posterior_result* d_out, float* d_stats, int32_t* d_argmax,
-                           void* ws, cudaStream_t stream) {
+                           void* ws, cudaStream_t stream, const float2* row_max, int n_row_tiles) {
   char* w = static_cast<char*>(ws);
   unsigned int* ticket = reinterpret_cast<unsigned int*>(w);
   float* ws_stats = reinterpret_cast<float*>(w + 64);
   int32_t* ws_arg = reinterpret_cast<int32_t*>(w + 64 + (size_t)t->n_nodes * 4 * sizeof(float));
   if (mv_launch(posterior_kernel, dim3(t->n_nodes), dim3(kThreads), 0, stream, logits, V, ld, d_tree_tokens,
                 t->d_retrieve, t->n_nodes, t->n_paths, t->depth + 1, prm, d_out, d_stats, d_argmax, ws_stats, ws_arg,
-                ticket, mv_error_word()) != cudaSuccess)
+                ticket, mv_error_word(), row_max, n_row_tiles) != cudaSuccess)
     return MV_ERR_CUDA;
   return mv_last_launch("evaluate_posterior");
 }

@@ -147,6 +147,7 @@ struct mv_session {
   void* ws_post;
   void* ws_heads;
   unsigned int* chain_flags;  // phase counters of the projection chains (zero between launches)
+  float2* row_max;            // [vocab/128][64]: per LM-head tile and token, max and first argmax
   CUtensorMap m_xb, m_attn, m_act, m_kv;
   // CUDA graph of n consecutive steps (medusa_verify_steps_graph), captured on first use
   cudaGraphExec_t graph_exec = nullptr;
@@ -195,7 +196,7 @@ struct ProfScope {
 namespace {
 
 struct SessionLayout {
-  size_t state, tree_tokens, cart, x, xb, ssq, q, attn, act, logits, attn_ws, post, heads, chain, total;
+  size_t state, tree_tokens, cart, x, xb, ssq, q, attn, act, logits, attn_ws, post, heads, chain, row_max, total;
 };
 
 SessionLayout session_layout(const mv_model_dims& d, int s_max, int topk) {
@@ -222,6 +223,7 @@ SessionLayout session_layout(const mv_model_dims& d, int s_max, int topk) {
   L.post = take(posterior_ws_bytes(kTok));
   L.heads = take(heads_ws_bytes(1, d.d, d.n_medusa, d.vocab, topk));
   L.chain = take(kGemmChainFlagWords * sizeof(unsigned int));  // zero at creation; each chain launch leaves it so
+  L.row_max = take((size_t)((d.vocab + 127) / 128) * kTok * sizeof(float2));  // LM-head tile max / argmax
   L.total = o;
   return L;
 }
@@ -326,6 +328,7 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     p.norm_d = d.d;
     p.out_f32 = s->logits;
     p.ld_out = s->ld_logits;
+    p.row_max = s->row_max;  // the greedy posterior merges these instead of re-reading the logits
     return g;
   };
   if (rc == MV_OK) {
@@ -458,6 +461,7 @@ extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16
   s->ws_post = b + L.post;
   s->ws_heads = b + L.heads;
   s->chain_flags = reinterpret_cast<unsigned int*>(b + L.chain);
+  s->row_max = reinterpret_cast<float2*>(b + L.row_max);
   const int HD = d.n_heads * d.head_dim;
   bool ok = gemm_act_map(&s->m_xb, s->xb, kTok, d.d) && gemm_act_map(&s->m_attn, s->attn, kTok, HD) &&
             gemm_act_map(&s->m_act, s->act, kTok, d.ffn);
@@ -563,7 +567,7 @@ extern "C" mv_status medusa_verify_step(mv_session* s, mv_accept_params prm, mv_
   if (rc == MV_OK) {
     ProfScope ps(s, st, MV_PROF_POSTERIOR);
     rc = launch_posterior(s->logits, d.vocab, s->ld_logits, s->tree_tokens, t, prm, s->result, nullptr, nullptr,
-                          s->ws_post, st);
+                          s->ws_post, st, s->row_max, (d.vocab + 127) / 128);
   }
   if (rc == MV_OK) {
     ProfScope ps(s, st, MV_PROF_KV_COMPACT);
