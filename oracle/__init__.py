@@ -19,7 +19,8 @@ Sources (cited by page title and section):
 
 Modules: ``tree`` (static tree buffers), ``model`` (Llama-style backbone,
 Medusa heads, tree attention), ``posterior`` (greedy and typical acceptance),
-``kv`` (KV compaction), ``decode`` (candidates, verify step, greedy loops).
+``kv`` (KV compaction), ``decode`` (candidates, verify step, greedy loops),
+``sampling`` (typical and nucleus one-token root sampling).
 
 Pins (what ties each function to something other than itself) are the
 ``-m "not gpu"`` tests in ``tests/test_oracle_*.py``. Every function here is

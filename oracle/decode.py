@@ -12,7 +12,8 @@ cache; the next LM/Medusa logits are those of node retrieve[best, acc]).
 The reference evaluates the Medusa heads on all tree nodes and keeps the row
 of node retrieve[best, acc]; here the heads run on that node only, which is
 the same consumed value. The root is the argmax of the LM logits (the
-temperature-0 / "fast" branch of generate_candidates()).
+temperature-0 / "fast" branch of generate_candidates()), or drawn by a root
+sampler of ``sampling`` (the branch for temperature > 0 without "fast").
 
 Greedy equivalence ("Phi-3-mini-128k-instruct_rai_1.8.0_medusa_1.0_npu",
 2️⃣: under greedy decoding the output is identical token for token) is the
@@ -51,17 +52,21 @@ def chain_mask(n):
     return np.tril(np.ones((n, n), dtype=np.uint8))
 
 
-def prefill(model: Backbone, prompt, s_max, topk):
-    """Forward the prompt causally; root = argmax of its last logits, heads on its last state."""
+def prefill(model: Backbone, prompt, s_max, topk, root=None):
+    """Forward the prompt causally; root = argmax of its last logits (or ``root(logits row)``, e.g. a
+    ``sampling.RootSampler``), heads on its last state."""
     cache = KVCache(model.dims, s_max)
     P = len(prompt)
     h, logits = model.forward(np.asarray(prompt), np.arange(P), cache, 0, chain_mask(P))
     z = medusa_heads(model.get, model.dims.n_medusa, h[-1])
-    return DecodeState(cache, P, argmax_first(logits[-1]), np.stack([topk_ids(r, topk) for r in z]))
+    r0 = argmax_first(logits[-1]) if root is None else root(logits[-1])
+    return DecodeState(cache, P, r0, np.stack([topk_ids(r, topk) for r in z]))
 
 
-def verify_step(model: Backbone, st: DecodeState, tree, mode=GREEDY, temperature=1.0, eps=0.09, delta=0.3):
-    """One Medusa verify step. Returns (accepted tokens, details) and advances ``st``."""
+def verify_step(model: Backbone, st: DecodeState, tree, mode=GREEDY, temperature=1.0, eps=0.09, delta=0.3,
+                root=None):
+    """One Medusa verify step. Returns (accepted tokens, details) and advances ``st``. The next root is the
+    argmax of node retrieve[best, acc]'s logits, or ``root(that row)`` when a root sampler is given."""
     tree_tokens, cart = generate_candidates(st.root, st.head_topk, tree)
     pos = st.cur_len + tree["position_ids"]
     h, logits = model.forward(tree_tokens, pos, st.cache, st.cur_len, tree["attn_mask"])
@@ -71,7 +76,8 @@ def verify_step(model: Backbone, st: DecodeState, tree, mode=GREEDY, temperature
     nn = post["next_node"]
     z = medusa_heads(model.get, model.dims.n_medusa, h[nn])
     prev_len = st.cur_len
-    st.cur_len, st.root = new_len, argmax_first(logits[nn])
+    st.cur_len = new_len
+    st.root = argmax_first(logits[nn]) if root is None else root(logits[nn])
     st.head_topk = np.stack([topk_ids(r, tree["topk"]) for r in z])
     return out, dict(post=post, tree_tokens=tree_tokens, cart=cart, logits=logits, hidden=h,
                      prefix_len=prev_len, head_logits=z)
