@@ -361,7 +361,7 @@ MICRO = {  # name -> (M, K, n): projections of the 7B step, timed alone through 
     "qkv": (12288, 4096, 64), "o": (4096, 4096, 64),
 }
 MICRO_OTHER = ["heads_b1", "heads_b4", "heads_b16", "attn_p64", "attn_p512", "attn_p1024", "attn_p4096",
-               "posterior_greedy", "posterior_typical", "kv_compact_acc4"]
+               "posterior_greedy", "posterior_typical", "kv_compact_acc4", "root_typical", "root_nucleus"]
 
 
 def _time_launches(fn, steps, warmup, flush=True):
@@ -423,6 +423,13 @@ def run_micro_other(name, steps, warmup):
         prm = mv.AcceptParams(mode, 0.7, 0.09, 0.3)
         fn = lambda: mv.evaluate_posterior(logits, toks, tree, prm, out, w)
         nbytes = tree.n_nodes * 32000 * 4
+    elif name.startswith("root_"):  # one stochastic root draw from a 32000-logit row (T 0.7, top_p 0.8)
+        mode = mv.ROOT_TYPICAL if name.endswith("typical") else mv.ROOT_NUCLEUS
+        row = synth.normal(0, "root_row", (32000,), 2.0, device="cuda")
+        out = torch.empty(1, dtype=torch.int32, device="cuda")
+        prm = mv.RootParams(mode, 0.7, 0.09, 0.3, 0.8, key=1)
+        fn = lambda: mv.sample_root(row, prm, 0, out)
+        nbytes = 32000 * 4
     else:  # kv_compact_acc4: 32 layers x 32 heads x 128, prefix 1024, path of 5 nodes
         kv = synth.kv_cache(0, (32, 2, 32, 1088, 128), device="cuda")
         r = mv.PosteriorResult()

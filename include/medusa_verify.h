@@ -180,6 +180,39 @@ mv_status evaluate_posterior_noalloc(const float* logits, int32_t V, int32_t ld,
                                      float* d_node_stats, int32_t* d_node_argmax, mv_stream stream);
 
 /* ============================================================================================
+ * Stochastic root  [M5 二.4 generate_candidates(): get_typical_one_token, get_nucleus_one_token; 一.3]
+ * ============================================================================================
+ * For temperature > 0 without the "fast" flag the page draws the root token (the first candidate) from the
+ * LM logits instead of taking their argmax; 二.1 medusa_generate() defaults top_p = 0.8. The pages do not print
+ * the two samplers; this library computes these readings of them:
+ *   MV_ROOT_TYPICAL: p = softmax(z / T) restricted to {p > tau}, tau = min(eps, delta * exp(-H)),
+ *                    H = -sum p log(p + 1e-5) (the typical-acceptance quantities of 一.3), renormalised;
+ *   MV_ROOT_NUCLEUS: the smallest leading set of tokens (logits descending, equal logits by lower index) whose
+ *                    probability mass reaches top_p, renormalised;
+ *   MV_ROOT_ARGMAX:  the first largest logit (the "fast" root; temperature and the rest are ignored).
+ * The draw takes u = (w >> 11) * 2^-53 with w = SplitMix64 word `counter` of the stream with 64-bit `key`
+ * (mix(key + (counter + 1) * 0x9E3779B97F4A7C15), Steele, Lea and Flood, OOPSLA 2014) and returns the first
+ * token in vocabulary order whose cumulative kept probability exceeds u. Probability masses are summed as
+ * fixed-point integers (exp((z - max) / T) * 2^40), so the token does not depend on the order of additions.
+ */
+typedef enum { MV_ROOT_ARGMAX = 0, MV_ROOT_TYPICAL = 1, MV_ROOT_NUCLEUS = 2 } mv_root_mode;
+typedef struct mv_root_params {
+  int32_t mode;      /* mv_root_mode */
+  float temperature; /* > 0 for TYPICAL / NUCLEUS */
+  float eps;         /* TYPICAL: posterior_threshold (0.09), >= 0 */
+  float delta;       /* TYPICAL: posterior_alpha (0.3), >= 0 */
+  float top_p;       /* NUCLEUS: 0 < top_p <= 1 (0.8) */
+  uint32_t reserved; /* 0 */
+  uint64_t key;      /* generator key */
+} mv_root_params;
+
+/* One draw from the logits row d_logits[0..V) (device fp32) into *d_token (device int32), on one CTA.
+ * Errors: MV_ERR_INVALID_ARG (null pointer, V < 1, bad mode, temperature <= 0, top_p outside (0, 1], negative
+ * eps / delta). A row whose logits are all NaN gives token 0. */
+mv_status sample_root(const float* d_logits, int32_t V, mv_root_params params, uint64_t counter, int32_t* d_token,
+                      mv_stream stream);
+
+/* ============================================================================================
  * KV compaction  [M5 二.7 update_inference_inputs()]
  * ============================================================================================
  * For every layer l, K/V plane c and head h:  kv[l][c][h][prefix + j] = (old) kv[l][c][h][prefix + nodes[j]]
@@ -272,6 +305,7 @@ typedef struct mv_session_state_ptrs {
   float* logits;                /* device fp32 [64][ld_logits]: the last forward's LM logits */
   int32_t ld_logits;
   float* hidden;                /* device fp32 [64][d]: the last forward's residual stream (before the final norm) */
+  uint64_t* root_counter;       /* device [1]: generator counter of the next sampled root */
 } mv_session_state_ptrs;
 mv_status mv_session_state(const mv_session* session, mv_session_state_ptrs* out);
 
@@ -279,6 +313,15 @@ mv_status mv_session_state(const mv_session* session, mv_session_state_ptrs* out
  * then sets the root (argmax of the last logits row), the head top-k (heads on the last token) and
  * cur_len = n. Limits: 1 <= n, n + 64 <= s_max. */
 mv_status mv_prefill(mv_session* session, const int32_t* d_tokens, int32_t n, mv_stream stream);
+
+/* Root sampling of a session (default MV_ROOT_ARGMAX): the root after mv_prefill and after every verify step
+ * is drawn as sample_root() describes from the logits row of node retrieve[best][acc] (the prefill: the
+ * prompt's last row), with the counter held in device memory, starting at `counter` and advancing by one per
+ * draw. The verify step's acceptance rule stays the one of its mv_accept_params. Enqueues the counter store on
+ * `stream`; CUDA graphs captured earlier by medusa_verify_steps_graph are re-captured on their next call.
+ * Errors: MV_ERR_INVALID_ARG as for sample_root. */
+mv_status mv_session_set_root_sampling(mv_session* session, mv_root_params params, uint64_t counter,
+                                       mv_stream stream);
 
 /* One verify step [M5 二.4 - 二.7]: candidates from the state, one backbone pass over the tree (positions
  * cur_len + depth, keys/values appended at cur_len .. cur_len + n_nodes - 1), posterior, KV compaction,

@@ -15,6 +15,7 @@ import numpy as np
 from .build import LIB, build
 
 __all__ = ["lib", "MVError", "Tree", "AcceptParams", "PosteriorResult", "GREEDY", "TYPICAL", "Model", "Session",
+           "RootParams", "ROOT_ARGMAX", "ROOT_TYPICAL", "ROOT_NUCLEUS", "sample_root",
            "linear_bf16", "linear_bf16_workspace", "ModelDims",
            "medusa_heads_topk", "medusa_heads_topk_workspace", "build_candidates", "tree_attention",
            "tree_attention_workspace", "evaluate_posterior", "evaluate_posterior_workspace", "kv_compact",
@@ -23,6 +24,7 @@ __all__ = ["lib", "MVError", "Tree", "AcceptParams", "PosteriorResult", "GREEDY"
 MAX_NODES = 64
 MAX_DEPTH = 8
 GREEDY, TYPICAL = 0, 1
+ROOT_ARGMAX, ROOT_TYPICAL, ROOT_NUCLEUS = 0, 1, 2
 
 _lib = None
 
@@ -52,6 +54,15 @@ class AcceptParams(ctypes.Structure):
         super().__init__(mode, temperature, eps, delta)
 
 
+class RootParams(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("temperature", ctypes.c_float), ("eps", ctypes.c_float),
+                ("delta", ctypes.c_float), ("top_p", ctypes.c_float), ("reserved", ctypes.c_uint32),
+                ("key", ctypes.c_uint64)]
+
+    def __init__(self, mode=ROOT_ARGMAX, temperature=0.7, eps=0.09, delta=0.3, top_p=0.8, key=0):
+        super().__init__(mode, temperature, eps, delta, top_p, 0, key % 2 ** 64)
+
+
 class PosteriorResult(ctypes.Structure):
     _fields_ = [("best", ctypes.c_int32), ("acc", ctypes.c_int32), ("next_node", ctypes.c_int32),
                 ("next_root", ctypes.c_int32), ("n_tokens", ctypes.c_int32),
@@ -73,6 +84,7 @@ _SIGS = {
     "evaluate_posterior_workspace": ([_I, ctypes.POINTER(_S)], _I),
     "evaluate_posterior": ([_P, _I, _I, _P, _P, AcceptParams, _P, _P, _P, _P, _S, _P], _I),
     "kv_compact": ([_P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
+    "sample_root": ([_P, _I, RootParams, ctypes.c_uint64, _P, _P], _I),
     "evaluate_posterior_noalloc": ([_P, _I, _I, _P, _P, AcceptParams, _P, _P, _P, _P], _I),
     "mv_linear_bf16_workspace": ([ctypes.POINTER(_S)], _I),
     "mv_linear_bf16": ([_P, _P, _P, _I, _I, _I, _I, _P, _S, _P], _I),
@@ -86,6 +98,7 @@ _SIGS = {
     "mv_session_destroy": ([_P], None),
     "mv_session_state": ([_P, _P], _I),
     "mv_prefill": ([_P, _P, _I, _P], _I),
+    "mv_session_set_root_sampling": ([_P, RootParams, ctypes.c_uint64, _P], _I),
     "medusa_verify_step": ([_P, AcceptParams, _P], _I),
     "medusa_verify_step_host": ([_P, AcceptParams, _P, _P, _P, _P], _I),
     "medusa_verify_steps_graph": ([_P, AcceptParams, _I, _P], _I),
@@ -234,6 +247,12 @@ def kv_compact(kv, prefix_len, result, cur_len=None, stream=None):
            "kv_compact")
 
 
+def sample_root(logits_row, params: RootParams, counter, out, stream=None):
+    """One root draw from logits_row fp32 [V] (contiguous) into out int32 [1] with generator counter ``counter``."""
+    _check(lib().sample_root(_ptr(logits_row), logits_row.numel(), params, counter % 2 ** 64, _ptr(out),
+                             _stream(stream)), "sample_root")
+
+
 def get_error(with_detail=False):
     """(status, code[, detail]): reads and clears the device error word (synchronises the device)."""
     code, detail = ctypes.c_uint32(), ctypes.c_uint32()
@@ -311,7 +330,7 @@ class _Weights(ctypes.Structure):
 
 class _StatePtrs(ctypes.Structure):
     _fields_ = [("cur_len", _P), ("result", _P), ("head_topk", _P), ("tree_tokens", _P), ("cart", _P),
-                ("logits", _P), ("ld_logits", _I), ("hidden", _P)]
+                ("logits", _P), ("ld_logits", _I), ("hidden", _P), ("root_counter", _P)]
 
 
 class Model:
@@ -377,9 +396,15 @@ class Session:
         self.ld_logits = sp.ld_logits
         self.logits = view(sp.logits, 64 * sp.ld_logits, torch.float32).view(64, sp.ld_logits)[:, : d.vocab]
         self.hidden = view(sp.hidden, 64 * d.d, torch.float32).view(64, d.d)
+        self.root_counter = view(sp.root_counter, 1, torch.int64)
 
     def prefill(self, tokens, stream=None):
         _check(lib().mv_prefill(self.handle, _ptr(tokens), tokens.numel(), _stream(stream)), "mv_prefill")
+
+    def set_root_sampling(self, params: RootParams, counter=0, stream=None):
+        """Draw the root after prefill / every step with ``params`` (ROOT_ARGMAX restores the argmax root)."""
+        _check(lib().mv_session_set_root_sampling(self.handle, params, counter % 2 ** 64, _stream(stream)),
+               "mv_session_set_root_sampling")
 
     def step(self, params: AcceptParams = None, stream=None):
         _check(lib().medusa_verify_step(self.handle, params or AcceptParams(), _stream(stream)), "medusa_verify_step")

@@ -427,9 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         };
         auto release = [&]() -> bool {  // on an expired wait the loads are still issued, so every barrier completes
           bool got = true;
-          if (ph == 0) {
-            pdl_wait();
-          } else if (!ca.indep) {
+          // Every activation load follows the previous kernel's completion, in any phase: a CTA may have no
+          // tile in phase 0 (or the phases may be independent), and a chain that starts early under
+          // programmatic launch would otherwise read the previous chain's counters and activations.
+          pdl_wait();
+          if (ph > 0 && !ca.indep) {
             got = wait_count(ca.flags + ph - 1, gridDim.x);
             flag_timeout |= !got;
             asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes -> TMA reads

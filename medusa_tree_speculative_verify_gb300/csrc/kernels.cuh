@@ -13,6 +13,14 @@ mv_status launch_posterior(const float* logits, int V, int ld, const int32_t* d_
                            mv_accept_params prm, mv_posterior_result* d_out, float* d_stats, int32_t* d_argmax,
                            void* ws, cudaStream_t stream, const float2* row_max = nullptr, int n_row_tiles = 0);
 
+// One root draw (see sample_root in medusa_verify.h). Row = res->next_node (checked against n_rows) when res is
+// set, else row 0; the token goes to res->next_root and/or out_token; with d_counter the draw takes its counter
+// from there and stores counter + 1, else it uses `counter`.
+bool mv_root_params_valid(const mv_root_params& p);
+mv_status launch_sample_root(const float* logits, int V, int ld, int n_rows, mv_posterior_result* res,
+                             int32_t* out_token, const mv_root_params& prm, uint64_t counter, uint64_t* d_counter,
+                             cudaStream_t stream);
+
 // prefix from d_prefix if non-null, else `prefix`
 mv_status launch_kv_compact(mv_bf16* kv, int L, int H, int S_max, int D, const int32_t* d_prefix, int prefix,
                             const mv_posterior_result* d_res, int32_t* d_cur_len, cudaStream_t stream);

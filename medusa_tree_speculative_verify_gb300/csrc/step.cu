@@ -107,6 +107,12 @@ __global__ void set_int_kernel(int32_t* p, int v) {
   *p = v;
 }
 
+__global__ void set_u64_kernel(uint64_t* p, uint64_t v) {
+  pdl_trigger();
+  pdl_wait();
+  *p = v;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
@@ -148,12 +154,16 @@ struct mv_session {
   void* ws_heads;
   unsigned int* chain_flags;  // phase counters of the projection chains (zero between launches)
   float2* row_max;            // [vocab/128][64]: per LM-head tile and token, max and first argmax
+  uint64_t* root_counter;     // generator counter of the next sampled root
+  mv_root_params root{};      // root rule (MV_ROOT_ARGMAX: the posterior's argmax stands)
+  int root_epoch = 0;         // bumped by every mv_session_set_root_sampling
   CUtensorMap m_xb, m_attn, m_act, m_kv;
   // CUDA graph of n consecutive steps (medusa_verify_steps_graph), captured on first use
   cudaGraphExec_t graph_exec = nullptr;
   cudaStream_t capture_stream = nullptr;
   mv_accept_params graph_prm{};
   int graph_steps = 0;
+  int graph_root_epoch = 0;
   bool graph_profiled = false;
   // optional per-launch timing (mv_session_profile): event pairs recorded around every launch
   bool profiling = false;
@@ -445,6 +455,7 @@ extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16
   s->topk = topk;
   char* b = static_cast<char*>(ws);
   s->cur_len = reinterpret_cast<int32_t*>(b + L.state);
+  s->root_counter = reinterpret_cast<uint64_t*>(b + L.state + 16);
   s->result = reinterpret_cast<mv_posterior_result*>(b + L.state + 64);
   s->head_topk = reinterpret_cast<int32_t*>(b + L.state + 512);
   s->tree_tokens = reinterpret_cast<int32_t*>(b + L.tree_tokens);
@@ -526,6 +537,7 @@ extern "C" mv_status mv_session_state(const mv_session* s, mv_session_state_ptrs
   out->logits = s->logits;
   out->ld_logits = s->ld_logits;
   out->hidden = s->x;
+  out->root_counter = s->root_counter;
   return MV_OK;
 }
 
@@ -545,9 +557,25 @@ extern "C" mv_status mv_prefill(mv_session* s, const int32_t* d_tokens, int32_t 
                    s->ld_logits, c, last ? 1 : 0, s->cur_len, s->result) == cudaSuccess
              ? mv_last_launch("prefill_finish")
              : MV_ERR_CUDA;
+    if (rc == MV_OK && last && s->root.mode != MV_ROOT_ARGMAX)  // the root drawn from the prompt's last row
+      rc = launch_sample_root(s->logits, s->model->dims.vocab, s->ld_logits, c, s->result, nullptr, s->root, 0,
+                              s->root_counter, st);
   }
   if (rc == MV_OK) rc = run_heads(s, st);
   return rc;
+}
+
+extern "C" mv_status mv_session_set_root_sampling(mv_session* s, mv_root_params params, uint64_t counter,
+                                                  mv_stream stream) {
+  if (!s || !mv_root_params_valid(params)) return MV_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (mv_launch(set_u64_kernel, dim3(1), dim3(1), 0, st, s->root_counter, counter) != cudaSuccess)
+    return MV_ERR_CUDA;
+  const mv_status rc = mv_last_launch("mv_session_set_root_sampling");
+  if (rc != MV_OK) return rc;
+  s->root = params;
+  ++s->root_epoch;
+  return MV_OK;
 }
 
 extern "C" mv_status medusa_verify_step(mv_session* s, mv_accept_params prm, mv_stream stream) {
@@ -568,6 +596,11 @@ extern "C" mv_status medusa_verify_step(mv_session* s, mv_accept_params prm, mv_
     ProfScope ps(s, st, MV_PROF_POSTERIOR);
     rc = launch_posterior(s->logits, d.vocab, s->ld_logits, s->tree_tokens, t, prm, s->result, nullptr, nullptr,
                           s->ws_post, st, s->row_max, (d.vocab + 127) / 128);
+  }
+  if (rc == MV_OK && s->root.mode != MV_ROOT_ARGMAX) {  // the next root drawn from node retrieve[best][acc]
+    ProfScope ps(s, st, MV_PROF_OTHER);
+    rc = launch_sample_root(s->logits, d.vocab, s->ld_logits, t->n_nodes, s->result, nullptr, s->root, 0,
+                            s->root_counter, st);
   }
   if (rc == MV_OK) {
     ProfScope ps(s, st, MV_PROF_KV_COMPACT);
@@ -636,7 +669,8 @@ extern "C" mv_status medusa_verify_steps_graph(mv_session* s, mv_accept_params p
   if (prm.mode == MV_TYPICAL && !(prm.temperature > 0.0f)) return MV_ERR_INVALID_ARG;
   const bool same = s->graph_exec && s->graph_steps == n_steps && s->graph_profiled == s->profiling &&
                     s->graph_prm.mode == prm.mode && s->graph_prm.temperature == prm.temperature &&
-                    s->graph_prm.eps == prm.eps && s->graph_prm.delta == prm.delta;
+                    s->graph_prm.eps == prm.eps && s->graph_prm.delta == prm.delta &&
+                    s->graph_root_epoch == s->root_epoch;
   if (!same) {
     if (s->graph_exec) {
       cudaGraphExecDestroy(s->graph_exec);
@@ -666,6 +700,7 @@ extern "C" mv_status medusa_verify_steps_graph(mv_session* s, mv_accept_params p
     }
     s->graph_prm = prm;
     s->graph_steps = n_steps;
+    s->graph_root_epoch = s->root_epoch;
     s->graph_profiled = s->profiling;
     s->profiled_graph_events = s->ev_used;
     s->profiled_graph_ev_next = s->ev_next;

@@ -93,3 +93,21 @@ def test_workspace_queries_and_shape_errors():
         mv.tree_attention_workspace(32, 96, 4160, 64)        # unsupported head dim
     with pytest.raises(mv.MVError):
         mv.medusa_heads_topk_workspace(17, 4096, 4, 32000, 10)  # batch above 16
+
+
+def test_root_sampling_argument_errors():
+    """sample_root / mv_session_set_root_sampling reject bad arguments on the host, before any launch."""
+    L = mv.lib()
+    fake = ctypes.c_void_p(0x1000)                              # never dereferenced: validation fails first
+    bad = [mv.RootParams(3), mv.RootParams(mv.ROOT_NUCLEUS, 0.0), mv.RootParams(mv.ROOT_NUCLEUS, -1.0),
+           mv.RootParams(mv.ROOT_NUCLEUS, float("nan")), mv.RootParams(mv.ROOT_NUCLEUS, top_p=0.0),
+           mv.RootParams(mv.ROOT_NUCLEUS, top_p=1.01), mv.RootParams(mv.ROOT_TYPICAL, eps=-0.1),
+           mv.RootParams(mv.ROOT_TYPICAL, delta=-0.1)]
+    for prm in bad:
+        assert L.sample_root(fake, 100, prm, 0, fake, None) == 1, (prm.mode, prm.temperature, prm.top_p)
+    good = mv.RootParams(mv.ROOT_NUCLEUS)
+    assert L.sample_root(None, 100, good, 0, fake, None) == 1    # null logits
+    assert L.sample_root(fake, 0, good, 0, fake, None) == 1      # empty row
+    assert L.sample_root(fake, 100, good, 0, None, None) == 1    # null output
+    assert L.mv_session_set_root_sampling(None, good, 0, None) == 1
+    assert ctypes.sizeof(mv.RootParams) == 32

@@ -229,3 +229,30 @@ def test_host_step_api_matches_device_step():
         sess2.step(mv.AcceptParams(GREEDY))
         toks_dev += sess2.read_result()["tokens"]
     assert toks_host == toks_dev
+
+
+@pytest.mark.parametrize("mode", [GREEDY, TYPICAL])
+def test_multi_step_graph_equals_eager(mode):
+    """Several steps in one CUDA graph (consecutive launches overlap under programmatic launch) give the same
+    decode as eager steps, and as one-step graphs."""
+    prm = mv.AcceptParams(mode, 0.7, 0.09, 0.3)
+    p = torch.as_tensor(_prompt(), dtype=torch.int32, device="cuda")
+    outs = []
+    for how in ("eager", "graph3", "graph1"):
+        _, _, _, sess, _, _ = _setup(synth.dense_tree_choices([2, 3]))
+        sess.prefill(p)
+        if how == "eager":
+            for _ in range(6):
+                sess.step(prm)
+        elif how == "graph3":
+            sess.steps_graph(3, prm)
+            sess.steps_graph(3, prm)
+        else:
+            for _ in range(6):
+                sess.steps_graph(1, prm)
+        torch.cuda.synchronize()
+        outs.append((sess.read_result(), int(sess.cur_len.item()), sess.head_topk.cpu().tolist(),
+                     sess.kv[:, :, :, : int(sess.cur_len.item())].cpu()))
+    for o in outs[1:]:
+        assert o[0] == outs[0][0] and o[1] == outs[0][1] and o[2] == outs[0][2]
+        assert torch.equal(o[3], outs[0][3])
