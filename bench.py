@@ -229,6 +229,9 @@ def run_gpu(args, world, rank, local):
     if st != 0:
         raise RuntimeError(f"device error word {code:#x}")
 
+    # the decode state before the timed replay: the eager pass below restarts from it and must reach the same state
+    snap_ws, snap_kv = sess.ws.clone(), sess.kv.clone()
+
     # ---- timed: K steps (one graph replay), inputs resident in HBM
     # candidates, embed, first QKV, per layer attention + projection chain, posterior, KV compaction, heads x 2
     launches_per_step = 1 + 1 + 1 + dims.n_layers * 2 + 1 + 1 + 2
@@ -245,6 +248,8 @@ def run_gpu(args, world, rank, local):
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(end), world)
     r = sess.read_result()
+    len_graph = int(sess.cur_len.item())
+    state_graph = (r, len_graph, sess.head_topk.clone(), sess.kv[:, :, :, :len_graph].clone())
 
     # ---- the same K steps as a graph with a CUDA event recorded around every launch: per-kernel device time
     # (the event nodes sit between kernels, so this pass runs without launch overlap; its total is reported)
@@ -262,7 +267,11 @@ def run_gpu(args, world, rank, local):
     prof.disable()
     profiled_ms = a.elapsed_time(b)
 
-    # ---- K eager steps without events, for comparison with the graph replay
+    # ---- K eager steps without events from the same starting state, for comparison with the graph replay
+    sess.ws.copy_(snap_ws)
+    sess.kv.copy_(snap_kv)
+    del snap_ws, snap_kv
+    torch.cuda.synchronize()
     a.record(stream)
     for _ in range(args.steps):
         sess.step(prm)
@@ -273,6 +282,13 @@ def run_gpu(args, world, rank, local):
     if st != 0:
         raise RuntimeError(f"device error word {code:#x}")
     r = sess.read_result()
+    len_eager = int(sess.cur_len.item())
+    graph_equals_eager = (r == state_graph[0] and len_eager == state_graph[1]
+                          and torch.equal(sess.head_topk, state_graph[2])
+                          and torch.equal(sess.kv[:, :, :, :len_eager], state_graph[3]))
+    if not graph_equals_eager:
+        raise RuntimeError("the timed graph replay and the same steps run eagerly reached different decode states")
+    del state_graph
 
     # ---- e2e: the host-buffer entry point (H2D seeds, step, D2H result + next seeds, stream sync per step)
     k = dims.n_medusa * TREE["topk"]
@@ -328,7 +344,7 @@ def run_gpu(args, world, rank, local):
                 "d2h_bytes_per_step": 4 * mv.RESULT_INTS + 4 * (1 + k)},
         "gpu_launches": launches_per_step * args.steps,
         "timing": {"graph_ms_per_step": ms / args.steps, "profiled_graph_ms_per_step": profiled_ms / args.steps,
-                   "eager_ms_per_step": eager_ms / args.steps},
+                   "eager_ms_per_step": eager_ms / args.steps, "graph_equals_eager": graph_equals_eager},
         "roofline": roofline,
         "clocks": clk.summary(),
     }
