@@ -484,6 +484,46 @@ def run_micro(name, steps, warmup):
             "peak": peak, "peak_kind": kind, "l2": "flushed", "layout": "packed"}
 
 
+def run_sweep_nodes(sizes, steps, warmup):
+    """Verify-step speed against the number of tree nodes (candidate tokens): the synthetic tree's n - 1
+    highest-scoring paths for each n, the same 7B-shape model, K steps as one graph replay after a 128-token
+    prompt. One JSON line per size. (The acceleration side of the trade-off, tokens accepted per step, needs
+    trained heads; with random weights almost nothing is accepted, so only the cost side is measured.)"""
+    import medusa_tree_speculative_verify_gb300 as mv
+    dims = synth.LLAMA7B
+    w = mv.pack_model_weights(synth.packed_weights(dims, 0, torch.bfloat16, "cuda"), drop_source=True)
+    model = mv.Model(dims, w)
+    prompt = synth.prompt_tokens(0, PROMPT_LEN, dims.vocab).to(torch.int32).cuda()
+    prm = mv.AcceptParams(mv.GREEDY)
+    stream = torch.cuda.current_stream()
+    wb = weight_bytes(dims)
+    for n in sizes:
+        tree = mv.Tree(synth.synthetic_tree_choices(n, TREE["depth"], TREE["topk"]), TREE["topk"])
+        s_max = (PROMPT_LEN + (TREE["depth"] + 1) * (warmup + 2 * steps + 2) + 64 + 63) // 64 * 64
+        sess = mv.Session(model, tree, s_max)
+        sess.prefill(prompt)
+        for _ in range(warmup):
+            sess.step(prm)
+        sess.steps_graph(steps, prm)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(0) as clk:
+            clk.ready()
+            a.record(stream)
+            sess.steps_graph(steps, prm)
+            b.record(stream)
+            torch.cuda.synchronize()
+            clk.stop()
+        ms = a.elapsed_time(b) / steps
+        st, code = mv.get_error()
+        if st != 0:
+            raise RuntimeError(f"device error word {code:#x}")
+        print(json.dumps({"sweep": "tree_nodes", "n_nodes": n, "n_paths": tree.n_paths, "depth": tree.depth,
+                          "steps": steps, "ms_per_step": ms, "steps_per_s": 1e3 / ms,
+                          "weight_gbs": wb / (ms / 1e3) / 1e9, "clocks": clk.summary()}), flush=True)
+        del sess, tree
+
+
 def weight_bytes(dims):
     d, HD, F, V, K, L = dims.d, dims.n_heads * dims.head_dim, dims.ffn, dims.vocab, dims.n_medusa, dims.n_layers
     per_layer = 2 * (3 * HD * d + d * HD + 2 * F * d + d * F)
@@ -500,8 +540,13 @@ def main():
     ap.add_argument("--tree", default="synthetic", choices=["synthetic", "page"],
                     help="the tree of the verify step: the synthetic 64-node tree or the page's own 63 choices")
     ap.add_argument("--micro", choices=sorted(MICRO) + MICRO_OTHER, help="time one kernel alone and exit")
+    ap.add_argument("--sweep-nodes", default=None,
+                    help="comma-separated tree sizes (2..64): time the verify step per size and exit")
     args = ap.parse_args()
     world, rank, local = dist_setup()
+    if args.sweep_nodes:
+        run_sweep_nodes([int(x) for x in args.sweep_nodes.split(",")], args.steps, args.warmup)
+        return
     if args.micro:
         fn = run_micro if args.micro in MICRO else run_micro_other
         print(json.dumps(fn(args.micro, args.steps, args.warmup)))
