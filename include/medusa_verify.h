@@ -46,7 +46,8 @@ typedef enum mv_status {
   MV_ERR_UNSUPPORTED = 7
 } mv_status;
 
-#define MV_MAX_NODES 64 /* tree nodes (root included): one 64-bit ancestor word per node */
+#define MV_MAX_NODES 256 /* tree nodes (root included) */
+#define MV_MASK_WORDS 4  /* 64-bit ancestor words per node: the attention mask row of MV_MAX_NODES bits */
 #define MV_MAX_DEPTH 8  /* longest root-to-leaf path, root excluded */
 
 /* ============================================================================================
@@ -57,7 +58,8 @@ typedef enum mv_status {
  * (length, lexicographic). tree_indices[i] = 0 for the root, 1 + topk*(len-1) + last rank otherwise (index
  * into [root, head-1 top-k, head-2 top-k, ...]). position_ids[i] = depth. retrieve: one row per leaf,
  * leaves in descending node order, root-to-leaf node list padded with -1 to depth+1 entries.
- * ancestors[i]: bit j set iff node j is node i or one of its ancestors (the tree attention mask row).
+ * ancestors[i][w]: bit b set iff node 64w + b is node i or one of its ancestors (the tree attention mask row;
+ * MV_MASK_WORDS words per node, words past the tree's last node zero).
  */
 typedef struct mv_tree mv_tree;
 
@@ -67,7 +69,7 @@ typedef struct mv_tree_desc {
   const int32_t* position_ids;   /* host [n_nodes] */
   const int32_t* retrieve;       /* host [n_paths][depth+1] */
   const int32_t* parent;         /* host [n_nodes], -1 for the root */
-  const uint64_t* ancestors;     /* host [n_nodes] */
+  const uint64_t* ancestors;     /* host [n_nodes][MV_MASK_WORDS] */
   const int32_t* d_tree_indices; /* device copies of the above */
   const int32_t* d_position_ids;
   const int32_t* d_retrieve;
@@ -170,7 +172,7 @@ mv_status evaluate_posterior(const float* logits, int32_t V, int32_t ld, const i
  * allocation, or a serving loop that must not touch the device allocator after start-up. It computes exactly
  * what evaluate_posterior computes (same arguments minus the workspace). Its scratch is a fixed 2048-byte
  * __device__ array inside the library (every GPU that loads the library holds it until the process exits),
- * enough for MV_MAX_NODES = 64 tree nodes; a larger tree is rejected with MV_ERR_CAPACITY. The first call on
+ * enough for 64 tree nodes; a larger tree is rejected with MV_ERR_CAPACITY. The first call on
  * a device looks up that array's device address (cudaGetSymbolAddress) with the device current; make that
  * first call before any stream capture. Each call clears the array's completion counter on `stream` before
  * its kernel. All calls share the one array, so calls that overlap on the GPU (other streams, other threads)
@@ -226,12 +228,13 @@ mv_status kv_compact(mv_bf16* kv, int32_t L, int32_t H, int32_t S_max, int32_t D
                      const mv_posterior_result* d_res, int32_t* d_cur_len, mv_stream stream);
 
 /* ============================================================================================
- * Projection over up to 64 tokens on the tcgen05 tensor cores  [M5 二.5 tree_decoding()]
+ * Projection over up to 256 tokens on the tcgen05 tensor cores  [M5 二.5 tree_decoding()]
  * ============================================================================================
  * out[j][r] = sum_k x[j][k] * w[r][k] for j < n, r < M (fp32 accumulate and output): the kernel every backbone
  * projection of the verify step runs, exposed with a plain-store epilogue.
  *   w device bf16 [M][K] (16-byte aligned), x device bf16 [n][K], out device fp32 [n][ld_out].
- * Limits: 1 <= n <= 64, K % 8 == 0, ld_out >= M, at most 1024 tiles of 128 rows.
+ * Limits: 1 <= n <= 256, K % 8 == 0, ld_out >= M, at most 1024 tiles of 128 rows. The tokens go through the
+ * tensor cores in groups of 64 (one, two or four per launch), every weight block read once for all of them.
  * workspace / ws_bytes are reserved: the kernel keeps its split-K partial sums in on-chip (distributed shared)
  * memory, mv_linear_bf16_workspace reports 0 bytes and workspace may be null. */
 mv_status mv_linear_bf16_workspace(size_t* bytes);
@@ -302,9 +305,10 @@ typedef struct mv_session_state_ptrs {
   int32_t* head_topk;           /* device [n_medusa][topk]: the next step's head candidates */
   int32_t* tree_tokens;         /* device [n_nodes]: the last step's tree tokens */
   int32_t* cart;                /* device [n_paths][depth+1] */
-  float* logits;                /* device fp32 [64][ld_logits]: the last forward's LM logits */
+  float* logits;                /* device fp32 [MV_MAX_NODES][ld_logits]: the last forward's LM logits */
   int32_t ld_logits;
-  float* hidden;                /* device fp32 [64][d]: the last forward's residual stream (before the final norm) */
+  float* hidden;                /* device fp32 [MV_MAX_NODES][d]: the last forward's residual stream (before the
+                                   final norm) */
   uint64_t* root_counter;       /* device [1]: generator counter of the next sampled root */
 } mv_session_state_ptrs;
 mv_status mv_session_state(const mv_session* session, mv_session_state_ptrs* out);

@@ -21,8 +21,9 @@ __all__ = ["lib", "MVError", "Tree", "AcceptParams", "PosteriorResult", "GREEDY"
            "tree_attention_workspace", "evaluate_posterior", "evaluate_posterior_workspace", "kv_compact",
            "get_error", "MAX_NODES", "MAX_DEPTH", "EXPORTED_SYMBOLS"]
 
-MAX_NODES = 64
+MAX_NODES = 256
 MAX_DEPTH = 8
+MASK_WORDS = 4
 GREEDY, TYPICAL = 0, 1
 ROOT_ARGMAX, ROOT_TYPICAL, ROOT_NUCLEUS = 0, 1, 2
 
@@ -162,12 +163,13 @@ class Tree:
         self.position_ids = arr(d.position_ids, self.n_nodes)
         self.retrieve = arr(d.retrieve, self.n_paths * (self.depth + 1)).reshape(self.n_paths, self.depth + 1)
         self.parent = arr(d.parent, self.n_nodes)
-        self.ancestors = arr(d.ancestors, self.n_nodes)
+        self.ancestors = arr(d.ancestors, self.n_nodes * MASK_WORDS).reshape(self.n_nodes, MASK_WORDS)
         self.d_ancestors = d.d_ancestors
 
     def attn_mask(self):
         n = self.n_nodes
-        return np.array([[(int(self.ancestors[i]) >> j) & 1 for j in range(n)] for i in range(n)], dtype=np.uint8)
+        return np.array([[(int(self.ancestors[i, j >> 6]) >> (j & 63)) & 1 for j in range(n)] for i in range(n)],
+                        dtype=np.uint8)
 
     def __del__(self):
         if getattr(self, "handle", None) is not None and _lib is not None:
@@ -394,8 +396,8 @@ class Session:
         self.tree_tokens = view(sp.tree_tokens, tree.n_nodes, torch.int32)
         self.cart = view(sp.cart, tree.n_paths * (tree.depth + 1), torch.int32).view(tree.n_paths, tree.depth + 1)
         self.ld_logits = sp.ld_logits
-        self.logits = view(sp.logits, 64 * sp.ld_logits, torch.float32).view(64, sp.ld_logits)[:, : d.vocab]
-        self.hidden = view(sp.hidden, 64 * d.d, torch.float32).view(64, d.d)
+        self.logits = view(sp.logits, MAX_NODES * sp.ld_logits, torch.float32).view(MAX_NODES, sp.ld_logits)[:, : d.vocab]
+        self.hidden = view(sp.hidden, MAX_NODES * d.d, torch.float32).view(MAX_NODES, d.d)
         self.root_counter = view(sp.root_counter, 1, torch.int64)
 
     def prefill(self, tokens, stream=None):

@@ -2,8 +2,10 @@
 //
 // "大模型推理 memory bandwidth bound (5) - Medusa", 一.2 Tree attention and 二.5 tree_decoding(): the tree is
 // flattened into a sequence after the prefix; the mask lets node i see only its ancestors and itself
-// ("Phi-3-mini-128k-instruct_rai_1.8.0_medusa_1.0_npu", 4️⃣: siblings never see each other). The mask is one
-// 64-bit ancestor word per node; only the key tile(s) that hold the tree block consult it.
+// ("Phi-3-mini-128k-instruct_rai_1.8.0_medusa_1.0_npu", 4️⃣: siblings never see each other). The mask is
+// MV_MASK_WORDS 64-bit ancestor words per node; only the key tiles that hold the tree block consult it. Trees
+// of more than 64 nodes run as blocks of 64 query rows (grid z); block b needs only the tree keys up to its
+// last row, since a node's ancestors precede it.
 //
 // Layout: q [n][H][D] bf16, K/V caches as planes of [H][S_max][D] bf16. One thread-block cluster per head;
 // its CTAs split the head's 64-key tiles (split-KV, so that H x splits fills the GPU at batch 1). 4 warps per
@@ -61,10 +63,23 @@ MV_DEV uint32_t tile_off(int r, int c) {
   }
 }
 
+// Visibility of the 64 keys key0 .. key0 + 63 for one query row, as bits: keys before the tree block (s < 0
+// positions) are all visible, tree key tj = key0 + k - P is visible iff bit tj of the row's ancestor words
+// w0..w3 (nodes 0-63, 64-127, 128-191, 192-255) is set; s = key0 - P < 256. Bits past the tree are 0 (a node's
+// ancestors precede it).
+MV_DEV uint64_t tile_bits(uint64_t w0, uint64_t w1, uint64_t w2, uint64_t w3, int s) {
+  if (s <= -64) return ~0ull;
+  if (s < 0) return (w0 << -s) | ((1ull << -s) - 1ull);
+  const int k = s >> 6, b = s & 63;
+  const uint64_t lo = k == 0 ? w0 : k == 1 ? w1 : k == 2 ? w2 : w3;
+  const uint64_t hi = k == 0 ? w1 : k == 1 ? w2 : k == 2 ? w3 : 0ull;
+  return b == 0 ? lo : (lo >> b) | (hi << (64 - b));
+}
+
 struct AttnArgs {
   const uint16_t* q;        // [n][H][D]
   uint16_t* out;            // [n][H][D]
-  const uint64_t* anc;      // [n]
+  const uint64_t* anc;      // [n][MV_MASK_WORDS]
   const int32_t* d_prefix;  // device prefix length or null
   int prefix;               // used when d_prefix is null
   int H, S_max, n, splits, plane_k, plane_v;  // splits = CTAs per cluster (gridDim.x)
@@ -90,18 +105,21 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
   constexpr int kPo = D + 4;  // row pitch (floats) of the partial output in shared memory
 
   const int split = blockIdx.x, h = blockIdx.y;  // split = rank in the head's cluster
+  const int row0 = blockIdx.z * kRows;           // this CTA's query rows: tree nodes row0 .. row0 + 63
   const int C = a.splits;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t4 = lane & 3;
   pdl_trigger();
   pdl_wait();  // q, the cache and the prefix length come from earlier kernels
   const int P = a.d_prefix ? *a.d_prefix : a.prefix;
-  const int n = a.n;
-  if (P < 0 || P + n > a.S_max) {
+  const int n_all = a.n;
+  if (P < 0 || P + n_all > a.S_max) {
     if (tid == 0) mv_set_error(a.err, 4, MV_DEVERR_INDEX);
     return;
   }
-  const int total_tiles = (P + n + kKeys - 1) / kKeys;
+  const int n = min(kRows, n_all - row0);         // query rows of this block
+  const int n_keys = min(n_all, row0 + kRows);    // tree keys any of them can see
+  const int total_tiles = (P + n_keys + kKeys - 1) / kKeys;
   // The cluster is sized for the longest prefix. At this prefix only S splits get tiles, about kTilesPerSplit
   // each (a split costs a merge). With S = 1 the first CTA does the whole head and writes it directly; the
   // others leave at once (no cluster barrier is used then). With S > 1 the idle splits still take part in the
@@ -133,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
   for (int e = tid; e < kRows * (D / 8); e += kThreads) {
     const int r = e / (D / 8), c = e % (D / 8);
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < n) v = *reinterpret_cast<const uint4*>(a.q + ((size_t)r * a.H + h) * D + c * 8);
+    if (r < n) v = *reinterpret_cast<const uint4*>(a.q + ((size_t)(row0 + r) * a.H + h) * D + c * 8);
     *reinterpret_cast<uint4*>(sq + tile_off<D>(r, c)) = v;
   }
   __syncthreads();
@@ -147,8 +165,14 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
     const int r = warp * 16 + 8 * (m & 1) + (lane & 7);
     ldsm_x4(sq_base + tile_off<D>(r, 2 * ks + (m >> 1)), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
   }
-  const int q0 = warp * 16 + g, q1 = q0 + 8;
-  const uint64_t anc0 = q0 < n ? a.anc[q0] : 0ull, anc1 = q1 < n ? a.anc[q1] : 0ull;
+  const int q0 = warp * 16 + g, q1 = q0 + 8;  // rows within the block
+  static_assert(MV_MASK_WORDS == 4, "four ancestor words per node");
+  const uint64_t* ar0 = a.anc + (size_t)(row0 + q0) * MV_MASK_WORDS;
+  const uint64_t* ar1 = a.anc + (size_t)(row0 + q1) * MV_MASK_WORDS;
+  const uint64_t a00 = q0 < n ? ar0[0] : 0ull, a01 = q0 < n ? ar0[1] : 0ull, a02 = q0 < n ? ar0[2] : 0ull,
+                 a03 = q0 < n ? ar0[3] : 0ull;
+  const uint64_t a10 = q1 < n ? ar1[0] : 0ull, a11 = q1 < n ? ar1[1] : 0ull, a12 = q1 < n ? ar1[2] : 0ull,
+                 a13 = q1 < n ? ar1[3] : 0ull;
 
   float o[DN][4];
 #pragma unroll
@@ -185,15 +209,15 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
       }
     }
     // mask + running max
+    const uint64_t tb0 = tile_bits(a00, a01, a02, a03, key0 - P), tb1 = tile_bits(a10, a11, a12, a13, key0 - P);
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int key = key0 + 8 * nt + 2 * t4 + e;
-        const int tj = key - P;  // tree node index if >= 0
-        const bool v0 = key < P || (tj < n && ((anc0 >> tj) & 1ull));
-        const bool v1 = key < P || (tj < n && ((anc1 >> tj) & 1ull));
+        const int k = 8 * nt + 2 * t4 + e;
+        const bool v0 = (tb0 >> k) & 1ull;
+        const bool v1 = (tb1 >> k) & 1ull;
         s[nt][e] = v0 ? s[nt][e] * a.scale_log2 : -INFINITY;
         s[nt][2 + e] = v1 ? s[nt][2 + e] * a.scale_log2 : -INFINITY;
         mx0 = fmaxf(mx0, s[nt][e]);
@@ -268,10 +292,10 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
     for (int dn = 0; dn < DN; ++dn) {
       const int col = 8 * dn + 2 * t4;
       if (q0 < n)
-        *reinterpret_cast<uint32_t*>(a.out + ((size_t)q0 * a.H + h) * D + col) =
+        *reinterpret_cast<uint32_t*>(a.out + ((size_t)(row0 + q0) * a.H + h) * D + col) =
             pack_bf16x2(o[dn][0] * i0, o[dn][1] * i0);
       if (q1 < n)
-        *reinterpret_cast<uint32_t*>(a.out + ((size_t)q1 * a.H + h) * D + col) =
+        *reinterpret_cast<uint32_t*>(a.out + ((size_t)(row0 + q1) * a.H + h) * D + col) =
             pack_bf16x2(o[dn][2] * i1, o[dn][3] * i1);
     }
     return;
@@ -349,7 +373,7 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
     uint2 pk;
     pk.x = pack_bf16x2(acc.x, acc.y);
     pk.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(a.out + ((size_t)q * a.H + h) * D + c4) = pk;
+    *reinterpret_cast<uint2*>(a.out + ((size_t)(row0 + q) * a.H + h) * D + c4) = pk;
   }
   cluster_sync_all();  // no CTA leaves while another may still read its partial
 }
@@ -445,10 +469,13 @@ mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vm
                                   int max_prefix, const mv_tree* t, int n, float scale, mv_bf16* out, void* ws,
                                   cudaStream_t stream) {
   (void)ws;  // reserved
+  if (n < 1 || n > MV_MAX_NODES) return MV_ERR_SHAPE;
+  const int blocks = (n + kRows - 1) / kRows;  // blocks of 64 query rows
   const int max_tiles = (max_prefix + n + kKeys - 1) / kKeys;
   int splits = choose_splits(max_tiles);
-  // all H clusters resident at once: a cluster that has to wait for another to leave costs a whole second wave
-  while (splits > 1 && max_active_clusters(D, splits) < H) --splits;
+  // all H x blocks clusters resident at once: a cluster that has to wait for another to leave costs a whole
+  // second wave
+  while (splits > 1 && max_active_clusters(D, splits) < H * blocks) --splits;
   AttnArgs a{};
   a.q = q;
   a.out = out;
@@ -465,7 +492,7 @@ mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vm
   a.err = mv_error_word();
   const size_t smem = smem_bytes(D);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(splits, H);
+  cfg.gridDim = dim3(splits, H, blocks);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

@@ -247,11 +247,11 @@ struct mv_tree {
   int32_t* h_position_ids;
   int32_t* h_retrieve;
   int32_t* h_parent;
-  uint64_t* h_ancestors;
+  uint64_t* h_ancestors;  // [n_nodes][MV_MASK_WORDS]
   int32_t* d_tree_indices;
   int32_t* d_position_ids;
   int32_t* d_retrieve;
   int32_t* d_parent;
-  uint64_t* d_ancestors;
+  uint64_t* d_ancestors;  // [n_nodes][MV_MASK_WORDS]
   int device;
 };

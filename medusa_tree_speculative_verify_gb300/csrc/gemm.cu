@@ -35,21 +35,28 @@
 
 namespace {
 
-constexpr int BM = 128, BN = 64, BK = 64;
-constexpr int kStages = 6;
+constexpr int BM = 128, BN = 64, BK = 64;  // BN: tokens per token group
+constexpr int kMaxGroups = 4;              // token groups per launch: up to 256 tokens
+constexpr int kTokMax = BN * kMaxGroups;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
-constexpr int kBBytes = BN * BK * 2;  // 8 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kBBytes = BN * BK * 2;  // 8 KB per token group
 constexpr int kEpiThreads = 128;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kAcc = 2;  // accumulator buffers in tensor memory (the MMA may run kAcc - 1 tiles ahead)
-constexpr int kTmemCols = kAcc * BN;
 constexpr int kMaxCluster = 8;  // CTAs per cluster (portable limit)
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)BM * BN * 4 + 256;
 
-// kind::f16 instruction descriptor: D fp32, A/B bf16, both K-major, N = 64, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+// Per number of token groups NT (1, 2 or 4): a stage holds one weight block and NT activation blocks, so
+// fewer stages fit; one MMA of N = 64 NT per 16 k; the accumulator buffers take 2 x 64 NT TMEM columns.
+template <int NT>
+struct Cfg {
+  static constexpr int kStages = NT == 1 ? 6 : NT == 2 ? 5 : 3;
+  static constexpr int kStageBytes = kABytes + NT * kBBytes;
+  static constexpr int kTmemCols = kAcc * BN * NT;
+  static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)BM * BN * 4 + 256;
+  // kind::f16 instruction descriptor: D fp32, A/B bf16, both K-major, N = 64 NT, M = 128.
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)((BN * NT) >> 3) << 17) |
+                                     ((uint32_t)(BM >> 4) << 24);
+};
 
 // ---------------------------------------------------------------------------------------------- tcgen05 PTX
 MV_DEV void tmem_alloc(uint32_t* dst, uint32_t ncols) {
@@ -120,31 +127,45 @@ MV_DEV uint64_t sw128_desc(uint32_t saddr) {
 // norm), and for the QKV epilogue the token positions prefix + depth. The 128 epilogue threads split the
 // partial sums so the loads are independent and in flight together.
 struct EpiConst {
-  float scale[BN];
-  int pos[BN];
-  float part[2][BN];
-  int kv_row0;
+  float scale[kTokMax];
+  int pos[kTokMax];
+  float part[2][kTokMax];
+  int kv_row0;  // -1: the cache rows would run past S_max (nothing is appended)
 };
 
-MV_DEV void load_epi_const(const GemmParams& p, EpiConst* ec, int i) {
-  const int j = i & (BN - 1), half = i >> 6;  // two threads per token, each summing half of the partials
-  float t = 0.0f;
-  if (p.ssq) {
-    const int q0 = half * ((p.ssq_parts + 1) / 2), q1 = min(p.ssq_parts, q0 + (p.ssq_parts + 1) / 2);
-    float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-    int q = q0;
-    for (; q + 8 <= q1; q += 8) {
+MV_DEV void load_epi_const(const GemmParams& p, EpiConst* ec, int i, int ngroups) {
+  const int half = i >> 6;  // two threads per token, each summing half of the partials
+  for (int g = 0; g < ngroups; ++g) {
+    const int j = g * BN + (i & (BN - 1));
+    float t = 0.0f;
+    if (p.ssq) {
+      const int q0 = half * ((p.ssq_parts + 1) / 2), q1 = min(p.ssq_parts, q0 + (p.ssq_parts + 1) / 2);
+      float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+      int q = q0;
+      for (; q + 8 <= q1; q += 8) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) acc[u] += __ldcg(p.ssq + (q + u) * BN + j);
+        for (int u = 0; u < 8; ++u) acc[u] += __ldcg(p.ssq + (size_t)(q + u) * p.tok_ld + j);
+      }
+      for (; q < q1; ++q) acc[0] += __ldcg(p.ssq + (size_t)q * p.tok_ld + j);
+      t = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     }
-    for (; q < q1; ++q) acc[0] += __ldcg(p.ssq + q * BN + j);
-    t = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    ec->part[half][j] = t;
+    if (half == 0 && p.pos_ids) ec->pos[j] = j < p.n_tok ? *p.cur_len + p.pos_ids[j] : 0;
   }
-  ec->part[half][j] = t;
-  if (half == 0 && p.pos_ids) ec->pos[j] = j < p.n_tok ? *p.cur_len + p.pos_ids[j] : 0;
-  if (i == 0) ec->kv_row0 = p.cur_len ? *p.cur_len : 0;
+  if (i == 0) {
+    int r0 = p.cur_len ? *p.cur_len : 0;
+    if (p.kv && (r0 < 0 || r0 + p.n_tok > p.S_max)) {  // appending would write past the cache planes
+      mv_set_error_detail(p.err, 14, MV_DEVERR_INDEX, (uint32_t)r0);
+      r0 = -1;
+    }
+    ec->kv_row0 = r0;
+  }
   epi_bar();
-  if (half == 0) ec->scale[j] = p.ssq ? rsqrtf((ec->part[0][j] + ec->part[1][j]) / (float)p.norm_d + p.eps) : 1.0f;
+  for (int g = 0; g < ngroups; ++g) {
+    const int j = g * BN + (i & (BN - 1));
+    if (half == 0)
+      ec->scale[j] = p.ssq ? rsqrtf((ec->part[0][j] + ec->part[1][j]) / (float)p.norm_d + p.eps) : 1.0f;
+  }
   epi_bar();
 }
 
@@ -185,7 +206,7 @@ MV_DEV void rope_sincos(float a, float* s, float* c) {
 // This CTA's share of the tile: tokens j = w + 4t for t = r0, r0 + cs, ... (acc[u] holds t = r0 + u * cs, rows
 // 4l..4l+3, summed over every K slice of the cluster). Writes the outputs of the launch's epilogue kind.
 template <int EPI, int NU>
-MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, int cs,
+MV_DEV void final_epilogue(const GemmParams& p, int tile, int jb, int w, int l, int r0, int cs,
                            float4 (&acc)[NU], const EpiConst* ec) {
   const int ntok = p.n_tok;
   if constexpr (EPI == EPI_STORE) {
@@ -195,7 +216,7 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, 
     for (int u = 0; u < NU; ++u) {
       const int t = r0 + u * cs;
       if (t >= kTokPerThread) break;
-      const int j = w + 4 * t;
+      const int j = jb + w + 4 * t;
       if (j >= ntok) continue;  // uniform over the warp (the shuffles below need every lane)
       const float s = ec->scale[j];
       const float4 v = make_float4(acc[u].x * s, acc[u].y * s, acc[u].z * s, acc[u].w * s);
@@ -218,7 +239,7 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, 
             mi = oi;
           }
         }
-        if (l == 0) p.row_max[tile * BN + j] = make_float2(m, __int_as_float(mi));
+        if (l == 0) p.row_max[(size_t)tile * p.tok_ld + j] = make_float2(m, __int_as_float(mi));
       }
       if (R >= p.M) continue;
       float* o = p.out_f32 + (size_t)j * p.ld_out + R;
@@ -240,7 +261,7 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, 
     for (int u = 0; u < NU; ++u) {  // every residual load in flight before the first use
       const int t = r0 + u * cs;
       if (t >= kTokPerThread) break;
-      const int j = w + 4 * t;
+      const int j = jb + w + 4 * t;
       xo[u] = (valid && j < ntok) ? __ldcg(reinterpret_cast<const float4*>(p.x + (size_t)j * p.M + R))
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -248,7 +269,7 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, 
     for (int u = 0; u < NU; ++u) {
       const int t = r0 + u * cs;
       if (t >= kTokPerThread) break;
-      const int j = w + 4 * t;
+      const int j = jb + w + 4 * t;
       if (j >= ntok) continue;  // uniform over the warp
       float4 xn = xo[u];
       add4(xn, acc[u]);
@@ -260,7 +281,7 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, 
       }
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, m);
-      if (l == 0) p.ssq_out[tile * BN + j] = sq;  // per-token sum of squares over the tile's rows
+      if (l == 0) p.ssq_out[(size_t)tile * p.tok_ld + j] = sq;  // per-token sum of squares over the tile's rows
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
     // lanes 0..15: gate rows 4l..4l+3 (features f0 + 4l ..); lanes 16..31: the matching up rows
@@ -269,7 +290,7 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, 
     for (int u = 0; u < NU; ++u) {
       const int t = r0 + u * cs;
       if (t >= kTokPerThread) break;
-      const int j = w + 4 * t;
+      const int j = jb + w + 4 * t;
       if (j >= ntok) continue;  // uniform over the warp
       const float4 up = shfl_xor4(acc[u], 16);
       if (l < 16 && f < p.F) {
@@ -299,17 +320,18 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int w, int l, int r0, 
       stride = (size_t)p.H * p.D;
     } else {
       const size_t plane = (size_t)p.layer * 2 + (which - 1);
-      dst = p.kv + ((plane * p.H + head) * p.S_max + ec->kv_row0) * p.D + dim;
+      dst = p.kv + ((plane * p.H + head) * p.S_max + max(ec->kv_row0, 0)) * p.D + dim;
       stride = (size_t)p.D;
     }
+    const bool store = valid && (which == 0 || ec->kv_row0 >= 0);
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
       const int t = r0 + u * cs;
       if (t >= kTokPerThread) break;
-      const int j = w + 4 * t;
+      const int j = jb + w + 4 * t;
       if (j >= ntok) continue;  // uniform over the warp
       const float4 pr = shfl_xor4(acc[u], p.D >> 3);  // the RoPE partner rows (dim -+ D/2, same head)
-      if (!valid) continue;
+      if (!store) continue;
       const float s = ec->scale[j];
       float v[4] = {acc[u].x * s, acc[u].y * s, acc[u].z * s, acc[u].w * s};
       if (which < 2) {
@@ -350,12 +372,17 @@ MV_DEV bool wait_count(const unsigned int* p, unsigned int target) {
   }
 }
 
+template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ ChainMaps maps,
                                                            const __grid_constant__ ChainArgs ca) {
+  constexpr int kStages = Cfg<NT>::kStages;
+  constexpr int kStageBytes = Cfg<NT>::kStageBytes;
+  constexpr int kTmemCols = Cfg<NT>::kTmemCols;
+  constexpr uint32_t kIdesc = Cfg<NT>::kIdesc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  float* part = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);  // [BN tokens][BM rows]
+  float* part = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);  // [BN tokens][BM rows], a group
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[kAcc], tempty[kAcc], drain, pfull, pfree;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int s_abort;
@@ -422,8 +449,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         bool waited = false;
         int pend_s[kStages], pend_kb[kStages];
         int pend = 0;
-        auto issue_b = [&](int stage, int kb) {
-          tma_load_2d(stages + (size_t)stage * kStageBytes + kABytes, bm, &full[stage], kb * BK, 0);
+        auto issue_b = [&](int stage, int kb) {  // the activation blocks of the NT token groups
+#pragma unroll
+          for (int g = 0; g < NT; ++g)
+            tma_load_2d(stages + (size_t)stage * kStageBytes + kABytes + g * kBBytes, bm, &full[stage], kb * BK,
+                        g * BN);
         };
         auto release = [&]() -> bool {  // on an expired wait the loads are still issued, so every barrier completes
           bool got = true;
@@ -499,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             break;
           }
           tc_fence_after();
-          const uint32_t dt = tmem_base + (uint32_t)(buf * BN);
+          const uint32_t dt = tmem_base + (uint32_t)(buf * BN * NT);
           for (int kb = kb0; kb < kb1; ++kb, ++it) {
             const int s = it % kStages, r = it / kStages;
             if (s_abort || !mbar_wait(&full[s], (uint32_t)(r & 1))) {
@@ -536,8 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     pdl_wait();                     // the epilogue reads what earlier kernels wrote
     const uint32_t part_s = smem_u32(part) + (uint32_t)(lane * 16);  // + token row
     bool ok = true;
-    int n = 0, prev_tile = -1, prev_ph = 0;
-    auto finish = [&](int ph_r, int tile_r, int nr) {
+    int n = 0, m = 0, prev_tile = -1, prev_ph = 0;
+    auto finish = [&](int ph_r, int tile_r, int g_r, int nr) {  // token group g_r of the tile; nr: item number
       const bool all = mbar_wait_cluster(&pfull, (uint32_t)(nr & 1));
       if (epi_any(!all)) {
         if (i == 0) mv_set_error(err, 11, MV_DEVERR_TIMEOUT);
@@ -557,8 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
           const int t = rank + (u0 + u) * C;
           if (t >= kTokPerThread) break;
-          const int j = sub + 4 * t;
-          if (j >= pr.n_tok) continue;
+          const int j = sub + 4 * t;  // token within the group
+          if (g_r * BN + j >= pr.n_tok) continue;
           const uint32_t off = part_s + (uint32_t)(j * BM * 4);
           float4 part_c[kMaxCluster];
 #pragma unroll
@@ -570,13 +600,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
         const int r0 = rank + u0 * C;
         if (epi == EPI_RESIDUAL)
-          final_epilogue<EPI_RESIDUAL, kChunk>(pr, tile_r, sub, lane, r0, C, acc, &s_ec);
+          final_epilogue<EPI_RESIDUAL, kChunk>(pr, tile_r, g_r * BN, sub, lane, r0, C, acc, &s_ec);
         else if (epi == EPI_SWIGLU)
-          final_epilogue<EPI_SWIGLU, kChunk>(pr, tile_r, sub, lane, r0, C, acc, &s_ec);
+          final_epilogue<EPI_SWIGLU, kChunk>(pr, tile_r, g_r * BN, sub, lane, r0, C, acc, &s_ec);
         else if (epi == EPI_QKV)
-          final_epilogue<EPI_QKV, kChunk>(pr, tile_r, sub, lane, r0, C, acc, &s_ec);
+          final_epilogue<EPI_QKV, kChunk>(pr, tile_r, g_r * BN, sub, lane, r0, C, acc, &s_ec);
         else
-          final_epilogue<EPI_STORE, kChunk>(pr, tile_r, sub, lane, r0, C, acc, &s_ec);
+          final_epilogue<EPI_STORE, kChunk>(pr, tile_r, g_r * BN, sub, lane, r0, C, acc, &s_ec);
       }
       // the partials were consumed above (stores issued from them): release the buffers to their owners, one
       // release arrive per CTA of the cluster from C lanes at once (each costs a cluster round trip)
@@ -596,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
       }
       if (prev_tile >= 0) {
-        finish(prev_ph, prev_tile, n - 1);
+        finish(prev_ph, prev_tile, NT - 1, m - 1);
         prev_tile = -1;
         if (!ok) break;
       }
@@ -621,13 +651,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           ok = false;
           break;
         }
-        load_epi_const(ca.ph[ph], &s_ec, i);  // scales and positions: the same for every tile of the phase
+        load_epi_const(ca.ph[ph], &s_ec, i, NT);  // scales and positions: the same for every tile of the phase
         ec_ph = ph;
       }
       const int buf = n % kAcc;
       bool got = !s_abort && mbar_wait(&tfull[buf], (uint32_t)((n / kAcc) & 1));
-      // the partial buffer is free again once every CTA of the cluster has finished tile n - 1
-      if (got && n >= 1) got = mbar_wait_cluster(&pfree, (uint32_t)((n - 1) & 1));
+      // the partial buffer is free again once every CTA of the cluster has finished item m - 1
+      if (got && m >= 1) got = mbar_wait_cluster(&pfree, (uint32_t)((m - 1) & 1));
       if (epi_any(!got)) {  // uniform over the 4 epilogue warps
         if (i == 0) mv_set_error(err, 10, MV_DEVERR_TIMEOUT);
         s_abort = 1;
@@ -635,21 +665,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         break;
       }
       tc_fence_after();
-      {
+      // The tile's token groups one after another through the partial buffer (item m = one group of one tile):
+      // group g - 1 of this tile is finished before group g is drained into the buffer it frees.
+      for (int g = 0; g < NT; ++g) {
+        if (g > 0) {
+          finish(ph, tile, g - 1, m - 1);
+          if (!ok) break;
+          const bool free_ok = mbar_wait_cluster(&pfree, (uint32_t)((m - 1) & 1));
+          if (epi_any(!free_ok)) {
+            if (i == 0) mv_set_error(err, 10, MV_DEVERR_TIMEOUT);
+            s_abort = 1;
+            ok = false;
+            break;
+          }
+        }
         float v[BN];
-        const uint32_t ta = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(buf * BN);
+        const uint32_t ta = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(buf * BN * NT + g * BN);
         tmem_ld32(ta, v);
         tmem_ld32(ta + 32, v + 32);
         tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[buf]);
+        if (g == NT - 1) {  // the whole accumulator buffer is read: the MMA may reuse it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[buf]);
+        }
         // this CTA's partial, token-major: part[j][row] (consecutive rows in consecutive lanes)
 #pragma unroll
         for (int j = 0; j < BN; ++j) part[j * BM + i] = v[j];
+        epi_bar();  // the CTA's writes are ordered before the cluster-scope release arrives below
+        if (i < C) mbar_arrive_remote(map_rank(smem_u32(&pfull), (uint32_t)i));
+        ++m;
       }
-      epi_bar();  // the CTA's writes are ordered before the cluster-scope release arrives below
-      if (i < C) mbar_arrive_remote(map_rank(smem_u32(&pfull), (uint32_t)i));
+      if (!ok) break;
       prev_tile = tile;
       prev_ph = ph;
       ++tile;
@@ -677,7 +724,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 }  // namespace
 
 
-size_t gemm_smem_bytes() { return kSmemBytes; }
+// Token groups of a launch over n_tok tokens: 1, 2 or 4 (0 when n_tok > 256).
+int token_groups(int n_tok) { return n_tok <= BN ? 1 : n_tok <= 2 * BN ? 2 : n_tok <= kTokMax ? 4 : 0; }
+
+size_t smem_bytes_for(int nt) {
+  return nt == 1 ? Cfg<1>::kSmemBytes : nt == 2 ? Cfg<2>::kSmemBytes : Cfg<4>::kSmemBytes;
+}
+const void* kernel_for(int nt) {
+  return nt == 1 ? (const void*)gemm_kernel<1> : nt == 2 ? (const void*)gemm_kernel<2> : (const void*)gemm_kernel<4>;
+}
+// Raises the dynamic shared memory limit of the instantiation for nt token groups once per device.
+bool set_smem_for(int nt) {
+  static int flags[3][64] = {};
+  const int k = nt == 1 ? 0 : nt == 2 ? 1 : 2;
+  return mv_set_smem_once(kernel_for(nt), (int)smem_bytes_for(nt), flags[k]);
+}
 
 bool gemm_weight_map(CUtensorMap* map, const void* w, int rows, int K, int box_rows) {
   const uint64_t dims[2] = {(uint64_t)K, (uint64_t)rows};
@@ -714,19 +775,19 @@ bool gemm_act_map(CUtensorMap* map, const void* x, int rows, int K) {
 
 // Clusters of c CTAs (one CTA per SM) that can be resident at once on this device, c = 1..kMaxCluster; 0 when
 // the size cannot be launched. Asked once per device and size.
-int gemm_max_clusters(int c) {
-  static int cache[64][kMaxCluster + 1];  // 0 = not asked yet, -1 = not launchable
+int gemm_max_clusters(int c, int nt) {
+  static int cache[64][3][kMaxCluster + 1];  // 0 = not asked yet, -1 = not launchable
   const int dev = mv_device();
+  const int k = nt == 1 ? 0 : nt == 2 ? 1 : 2;
   if (dev < 0 || dev >= 64 || c < 1 || c > kMaxCluster) return 0;
-  int& slot = cache[dev][c];
+  int& slot = cache[dev][k][c];
   if (slot == 0) {
-    static int flags[64] = {0};
     int n = 0;
-    if (mv_set_smem_once((const void*)gemm_kernel, (int)kSmemBytes, flags)) {
+    if (set_smem_for(nt)) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(c * mv_sm_count());
       cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = kSmemBytes;
+      cfg.dynamicSmemBytes = smem_bytes_for(nt);
       cudaLaunchAttribute at[1];
       at[0].id = cudaLaunchAttributeClusterDimension;
       at[0].val.clusterDim.x = c;
@@ -734,7 +795,14 @@ int gemm_max_clusters(int c) {
       at[0].val.clusterDim.z = 1;
       cfg.attrs = at;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel, &cfg) != cudaSuccess) {
+      cudaError_t e;
+      if (nt == 1)
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<1>, &cfg);
+      else if (nt == 2)
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<2>, &cfg);
+      else
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<4>, &cfg);
+      if (e != cudaSuccess) {
         cudaGetLastError();
         n = 0;
       }
@@ -752,7 +820,7 @@ void shape_params(GemmParams& p) {
 // One cluster shape for a chain: the cluster size c and count that minimise the summed largest per-CTA share
 // of k-blocks, sum over phases of ceil(tiles / clusters) * ceil(kbt / c), with all clusters resident at once
 // (ties: the smaller cluster). Every CTA is resident, which the counters between phases rely on.
-void plan_chain(GemmParams* p, int n, int* csize, int* ncl_out) {
+void plan_chain(GemmParams* p, int n, int nt, int* csize, int* ncl_out) {
   int max_tiles = 1, min_kbt = 1 << 30;
   for (int i = 0; i < n; ++i) {
     max_tiles = std::max(max_tiles, p[i].n_tiles);
@@ -762,7 +830,7 @@ void plan_chain(GemmParams* p, int n, int* csize, int* ncl_out) {
   *csize = 1;
   *ncl_out = std::min(max_tiles, mv_sm_count());
   for (int c = 1; c <= kMaxCluster && c <= min_kbt; ++c) {
-    const int mc = gemm_max_clusters(c);
+    const int mc = gemm_max_clusters(c, nt);
     if (mc < 1) continue;
     const int ncl = std::min(mc, max_tiles);
     long long cost = 0;
@@ -778,7 +846,7 @@ void plan_chain(GemmParams* p, int n, int* csize, int* ncl_out) {
 
 void gemm_finish_params(GemmParams& p) {
   shape_params(p);
-  plan_chain(&p, 1, &p.csize, &p.n_clusters);
+  plan_chain(&p, 1, std::max(1, token_groups(p.n_tok)), &p.csize, &p.n_clusters);
   p.grid = p.csize * p.n_clusters;
 }
 
@@ -789,14 +857,21 @@ mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStrea
   memset(&maps, 0, sizeof(maps));
   memset(&ca, 0, sizeof(ca));
   GemmParams ps[kGemmMaxPhases];
+  int max_tok = 1;
   for (int i = 0; i < n; ++i) {
     ps[i] = ph[i].p;
     shape_params(ps[i]);
-    if (ps[i].n_tiles > kGemmMaxTiles || ps[i].n_tok < 1 || ps[i].n_tok > BN) return MV_ERR_SHAPE;
+    if (ps[i].n_tiles > kGemmMaxTiles || ps[i].n_tok < 1 || ps[i].n_tok > kTokMax) return MV_ERR_SHAPE;
     if (ph[i].epi < EPI_STORE || ph[i].epi > EPI_QKV) return MV_ERR_INVALID_ARG;
+    max_tok = std::max(max_tok, ps[i].n_tok);
+  }
+  const int nt = token_groups(max_tok);
+  for (int i = 0; i < n; ++i) {
+    if (ps[i].tok_ld == 0) ps[i].tok_ld = BN * nt;
+    if (ps[i].tok_ld < ps[i].n_tok) return MV_ERR_SHAPE;
   }
   int csize = 1, ncl = 1;
-  plan_chain(ps, n, &csize, &ncl);
+  plan_chain(ps, n, nt, &csize, &ncl);
   for (int i = 0; i < n; ++i) {
     ps[i].csize = csize;
     ps[i].n_clusters = ncl;
@@ -812,12 +887,11 @@ mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStrea
   ca.csize = csize;
   ca.indep = independent ? 1 : 0;
   ca.flags = independent ? nullptr : flags;
-  static int smem_flags[64] = {0};
-  if (!mv_set_smem_once((const void*)gemm_kernel, (int)kSmemBytes, smem_flags)) return MV_ERR_CUDA;
+  if (!set_smem_for(nt)) return MV_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize * ncl);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes_for(nt);
   cfg.stream = stream;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -828,7 +902,14 @@ mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStrea
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = mv_pdl_enabled() ? 2 : 1;
-  if (cudaLaunchKernelEx(&cfg, gemm_kernel, maps, ca) != cudaSuccess) return MV_ERR_CUDA;
+  cudaError_t e;
+  if (nt == 1)
+    e = cudaLaunchKernelEx(&cfg, gemm_kernel<1>, maps, ca);
+  else if (nt == 2)
+    e = cudaLaunchKernelEx(&cfg, gemm_kernel<2>, maps, ca);
+  else
+    e = cudaLaunchKernelEx(&cfg, gemm_kernel<4>, maps, ca);
+  if (e != cudaSuccess) return MV_ERR_CUDA;
   return mv_last_launch("gemm");
 }
 
@@ -849,7 +930,7 @@ extern "C" mv_status mv_linear_bf16(const mv_bf16* w, const mv_bf16* x, float* o
   (void)workspace;  // reserved: the kernel needs no global scratch
   (void)ws_bytes;
   if (!w || !x || !out) return MV_ERR_INVALID_ARG;
-  if (M < 1 || K < 8 || (K & 7) || n < 1 || n > BN || ld_out < M) return MV_ERR_SHAPE;
+  if (M < 1 || K < 8 || (K & 7) || n < 1 || n > kTokMax || ld_out < M) return MV_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(x)) & 15) return MV_ERR_SHAPE;
   CUtensorMap a, b;
   if (!gemm_weight_map(&a, w, M, K, BM) || !gemm_act_map(&b, x, n, K)) return MV_ERR_CUDA;
@@ -871,7 +952,7 @@ extern "C" mv_status mv_linear_bf16_packed(const mv_bf16* w_packed, const mv_bf1
   (void)workspace;  // reserved: the kernel needs no global scratch
   (void)ws_bytes;
   if (!w_packed || !x || !out) return MV_ERR_INVALID_ARG;
-  if (M < 1 || K < 8 || (K & 7) || n < 1 || n > BN || ld_out < M) return MV_ERR_SHAPE;
+  if (M < 1 || K < 8 || (K & 7) || n < 1 || n > kTokMax || ld_out < M) return MV_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(w_packed) | reinterpret_cast<uintptr_t>(x)) & 15) return MV_ERR_SHAPE;
   CUtensorMap a, b;
   if (!gemm_weight_map_packed(&a, w_packed, M, K, BM) || !gemm_act_map(&b, x, n, K)) return MV_ERR_CUDA;

@@ -9,7 +9,8 @@ constexpr int kGemmMaxTiles = 1024;
 struct GemmParams {
   int M;         // weight rows (output features); for SWIGLU the FFN width F (rows per gate/up matrix)
   int K;         // reduction length
-  int n_tok;     // valid token columns (1..64)
+  int n_tok;     // valid token columns (1..256; up to 64 per token group)
+  int tok_ld;    // token stride of ssq, ssq_out and row_max (0: 64 x the launch's token groups)
   int paired;    // SWIGLU: tile = 64 rows of amap0 (gate) + the same 64 rows of amap1 (up)
   int packed_a;  // weights in the [row tile][k-block][rows][64] layout (3-D maps, one contiguous box per load)
   // derived (gemm_finish_params): k-blocks, tiles, CTAs per cluster (K slices per tile), clusters, CTAs
@@ -21,8 +22,8 @@ struct GemmParams {
   // EPI_STORE
   float* out_f32;
   int ld_out;
-  float2* row_max;  // optional [n_tiles][64]: per 128-row tile and token, (max, first argmax as int bits)
-  // EPI_RESIDUAL (x, xb are [n][M]; ssq_out is [n_tiles][64])
+  float2* row_max;  // optional [n_tiles][tok_ld]: per 128-row tile and token, (max, first argmax as int bits)
+  // EPI_RESIDUAL (x, xb are [n][M]; ssq_out is [n_tiles][tok_ld])
   float* x;
   uint16_t* xb;
   float* ssq_out;
@@ -52,7 +53,6 @@ struct GemmPhase {
 // them zero again).
 constexpr int kGemmChainFlagWords = kGemmMaxPhases + 1;
 
-size_t gemm_smem_bytes();
 bool gemm_weight_map(CUtensorMap* map, const void* w, int rows, int K, int box_rows);
 bool gemm_weight_map_packed(CUtensorMap* map, const void* w, int rows, int K, int tile_rows);
 bool gemm_act_map(CUtensorMap* map, const void* x, int rows, int K);

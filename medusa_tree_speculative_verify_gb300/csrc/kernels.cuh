@@ -7,11 +7,13 @@ mv_status launch_build_candidates(const int32_t* d_root, const int32_t* d_head_t
                                   int32_t* d_tree_tokens, int32_t* d_cart, cudaStream_t stream);
 
 size_t posterior_ws_bytes(int n_nodes);
-// row_max / n_row_tiles: optional per-(128-row tile, node) max and first argmax left by the LM-head projection
-// ([n_row_tiles][64] float2, the index as int bits); greedy acceptance then does not read the logits rows.
+// row_max / n_row_tiles / row_ld: optional per-(128-row tile, node) max and first argmax left by the LM-head
+// projection ([n_row_tiles][row_ld] float2, the index as int bits); greedy acceptance then does not read the
+// logits rows.
 mv_status launch_posterior(const float* logits, int V, int ld, const int32_t* d_tree_tokens, const mv_tree* t,
                            mv_accept_params prm, mv_posterior_result* d_out, float* d_stats, int32_t* d_argmax,
-                           void* ws, cudaStream_t stream, const float2* row_max = nullptr, int n_row_tiles = 0);
+                           void* ws, cudaStream_t stream, const float2* row_max = nullptr, int n_row_tiles = 0,
+                           int row_ld = 0);
 
 // One root draw (see sample_root in medusa_verify.h). Row = res->next_node (checked against n_rows) when res is
 // set, else row 0; the token goes to res->next_root and/or out_token; with d_counter the draw takes its counter

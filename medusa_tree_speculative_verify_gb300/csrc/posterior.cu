@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
     const float* logits, int V, int ld, const int32_t* tree_tokens, const int32_t* __restrict__ retrieve,
     int n_nodes, int n_paths, int width, mv_accept_params prm, mv_posterior_result* out, float* node_stats_out,
     int32_t* node_argmax_out, float* ws_stats, int32_t* ws_argmax, unsigned int* ticket, unsigned int* err,
-    const float2* row_max, int n_row_tiles) {
+    const float2* row_max, int n_row_tiles, int row_ld) {
   pdl_trigger();
   pdl_wait();
   const bool typical = prm.mode == MV_TYPICAL;
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
   Stat a{-FLT_MAX, 0x7fffffff, 0.0f};
   if (from_tiles) {
     for (int t = tid; t < n_row_tiles; t += kThreads) {
-      const float2 e = __ldcg(row_max + (size_t)t * 64 + node);
+      const float2 e = __ldcg(row_max + (size_t)t * row_ld + node);
       a = stat_merge(a, Stat{e.x, __float_as_int(e.y), 0.0f}, 1.0f, false);
     }
   }
@@ -281,14 +281,14 @@ size_t posterior_ws_bytes(int n_nodes) { return (size_t)n_nodes * 5 * sizeof(flo
 
 mv_status launch_posterior(const float* logits, int V, int ld, const int32_t* d_tree_tokens, const mv_tree* t,
                            mv_accept_params prm, mv_posterior_result* d_out, float* d_stats, int32_t* d_argmax,
-                           void* ws, cudaStream_t stream, const float2* row_max, int n_row_tiles) {
+                           void* ws, cudaStream_t stream, const float2* row_max, int n_row_tiles, int row_ld) {
   char* w = static_cast<char*>(ws);
   unsigned int* ticket = reinterpret_cast<unsigned int*>(w);
   float* ws_stats = reinterpret_cast<float*>(w + 64);
   int32_t* ws_arg = reinterpret_cast<int32_t*>(w + 64 + (size_t)t->n_nodes * 4 * sizeof(float));
   if (mv_launch(posterior_kernel, dim3(t->n_nodes), dim3(kThreads), 0, stream, logits, V, ld, d_tree_tokens,
                 t->d_retrieve, t->n_nodes, t->n_paths, t->depth + 1, prm, d_out, d_stats, d_argmax, ws_stats, ws_arg,
-                ticket, mv_error_word(), row_max, n_row_tiles) != cudaSuccess)
+                ticket, mv_error_word(), row_max, n_row_tiles, row_ld) != cudaSuccess)
     return MV_ERR_CUDA;
   return mv_last_launch("evaluate_posterior");
 }
@@ -322,7 +322,8 @@ extern "C" mv_status evaluate_posterior(const float* logits, int32_t V, int32_t 
 // ------------------------------------------------------------------------------------------------------------
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = 2048;  // >= posterior_ws_bytes(MV_MAX_NODES) = 64 * 20 + 64 = 1344
+constexpr int kNoAllocMaxNodes = 64;
+constexpr size_t kNoAllocScratchBytes = 2048;  // >= posterior_ws_bytes(kNoAllocMaxNodes) = 64 * 20 + 64 = 1344
 static __device__ __align__(256) unsigned char g_posterior_scratch[kNoAllocScratchBytes];
 
 // Device address of g_posterior_scratch on the current device, looked up once per device with that device
@@ -353,7 +354,7 @@ extern "C" mv_status evaluate_posterior_noalloc(const float* logits, int32_t V, 
   if (V < 2 || ld < V || (ld & 3) || (reinterpret_cast<uintptr_t>(logits) & 15)) return MV_ERR_SHAPE;
   if (params.mode != MV_GREEDY && params.mode != MV_TYPICAL) return MV_ERR_INVALID_ARG;
   if (params.mode == MV_TYPICAL && !(params.temperature > 0.0f)) return MV_ERR_INVALID_ARG;
-  if (tree->n_nodes > MV_MAX_NODES || posterior_ws_bytes(tree->n_nodes) > kNoAllocScratchBytes)
+  if (tree->n_nodes > kNoAllocMaxNodes || posterior_ws_bytes(tree->n_nodes) > kNoAllocScratchBytes)
     return MV_ERR_CAPACITY;  // more nodes than the fixed scratch array holds
   void* scratch = noalloc_scratch();
   if (!scratch) return MV_ERR_CUDA;

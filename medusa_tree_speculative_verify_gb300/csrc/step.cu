@@ -20,7 +20,8 @@
 
 namespace {
 
-constexpr int kTok = 64;  // token columns of every activation buffer
+constexpr int kTok = MV_MAX_NODES;  // token rows of every activation buffer (the largest tree)
+constexpr int kChunk = 64;         // prefill chunk: one token group, run as a causal chain
 
 // x[j][:] = float(E[tok[j]][:]), xb = E[tok[j]] (bf16), ssq[s][j] = sum of x^2 over the 128-column slice s.
 __global__ void __launch_bounds__(256) embed_kernel(const int32_t* tokens, const uint16_t* __restrict__ E, int vocab,
@@ -251,6 +252,7 @@ bool dims_ok(const mv_model_dims& d) {
 GemmParams base_params(const mv_session* s, int n_tok) {
   GemmParams p{};
   p.n_tok = n_tok;
+  p.tok_ld = kTok;  // the stride of the session's sum-of-squares and tile-statistics arrays
   p.packed_a = s->model->packed;
   p.eps = s->model->dims.norm_eps;
   p.err = mv_error_word();
@@ -443,7 +445,7 @@ extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16
   if (!tree->d_ancestors) return MV_ERR_CUDA;
   const mv_model_dims& d = m->dims;
   if (topk < tree->topk || topk > 16 || tree->depth > d.n_medusa || tree->n_nodes > kTok) return MV_ERR_SHAPE;
-  if (s_max < kTok + 1) return MV_ERR_CAPACITY;
+  if (s_max < kChunk + 1) return MV_ERR_CAPACITY;
   const SessionLayout L = session_layout(d, s_max, topk);
   if (ws_bytes < L.total) return MV_ERR_CAPACITY;
   if ((reinterpret_cast<uintptr_t>(ws) | reinterpret_cast<uintptr_t>(kv)) & 255) return MV_ERR_INVALID_ARG;
@@ -484,25 +486,25 @@ extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16
   if (ok) {
     // the chain is deeper than MV_MAX_DEPTH, so it is built directly rather than through mv_tree_create
     mv_tree* c = new mv_tree();
-    c->n_nodes = kTok;
+    c->n_nodes = kChunk;
     c->n_paths = 1;
-    c->depth = kTok - 1;
+    c->depth = kChunk - 1;
     c->topk = 1;
-    std::vector<int32_t> pos(kTok);
-    std::vector<uint64_t> anc(kTok);
-    for (int i = 0; i < kTok; ++i) {
+    std::vector<int32_t> pos(kChunk);
+    std::vector<uint64_t> anc((size_t)kChunk * MV_MASK_WORDS, 0ull);
+    for (int i = 0; i < kChunk; ++i) {
       pos[i] = i;
-      anc[i] = (i == 63) ? ~0ull : ((1ull << (i + 1)) - 1);
+      anc[(size_t)i * MV_MASK_WORDS] = (i == 63) ? ~0ull : ((1ull << (i + 1)) - 1);  // kChunk = 64: one word
     }
     c->h_tree_indices = c->h_retrieve = c->h_parent = nullptr;
     c->h_position_ids = nullptr;
     c->h_ancestors = nullptr;
     c->d_tree_indices = c->d_retrieve = c->d_parent = nullptr;
     c->device = tree->device;
-    ok = cudaMalloc(&c->d_position_ids, kTok * 4) == cudaSuccess &&
-         cudaMalloc(&c->d_ancestors, kTok * 8) == cudaSuccess &&
-         cudaMemcpy(c->d_position_ids, pos.data(), kTok * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
-         cudaMemcpy(c->d_ancestors, anc.data(), kTok * 8, cudaMemcpyHostToDevice) == cudaSuccess;
+    ok = cudaMalloc(&c->d_position_ids, kChunk * 4) == cudaSuccess &&
+         cudaMalloc(&c->d_ancestors, anc.size() * 8) == cudaSuccess &&
+         cudaMemcpy(c->d_position_ids, pos.data(), kChunk * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemcpy(c->d_ancestors, anc.data(), anc.size() * 8, cudaMemcpyHostToDevice) == cudaSuccess;
     s->chain = c;
   }
   ok = ok && cudaMemset(ws, 0, L.total) == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
@@ -543,13 +545,13 @@ extern "C" mv_status mv_session_state(const mv_session* s, mv_session_state_ptrs
 
 extern "C" mv_status mv_prefill(mv_session* s, const int32_t* d_tokens, int32_t n, mv_stream stream) {
   if (!s || !d_tokens || n < 1) return MV_ERR_INVALID_ARG;
-  if (n + kTok > s->s_max) return MV_ERR_CAPACITY;
+  if (n + kChunk > s->s_max) return MV_ERR_CAPACITY;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   mv_status rc = mv_launch(set_int_kernel, dim3(1), dim3(1), 0, st, s->cur_len, 0) == cudaSuccess
                      ? mv_last_launch("prefill")
                      : MV_ERR_CUDA;
-  for (int o = 0; o < n && rc == MV_OK; o += kTok) {
-    const int c = std::min(kTok, n - o);
+  for (int o = 0; o < n && rc == MV_OK; o += kChunk) {
+    const int c = std::min(kChunk, n - o);
     const bool last = o + c == n;
     rc = forward(s, s->chain, d_tokens + o, c, last, st);
     if (rc != MV_OK) break;
@@ -595,7 +597,7 @@ extern "C" mv_status medusa_verify_step(mv_session* s, mv_accept_params prm, mv_
   if (rc == MV_OK) {
     ProfScope ps(s, st, MV_PROF_POSTERIOR);
     rc = launch_posterior(s->logits, d.vocab, s->ld_logits, s->tree_tokens, t, prm, s->result, nullptr, nullptr,
-                          s->ws_post, st, s->row_max, (d.vocab + 127) / 128);
+                          s->ws_post, st, s->row_max, (d.vocab + 127) / 128, kTok);
   }
   if (rc == MV_OK && s->root.mode != MV_ROOT_ARGMAX) {  // the next root drawn from node retrieve[best][acc]
     ProfScope ps(s, st, MV_PROF_OTHER);

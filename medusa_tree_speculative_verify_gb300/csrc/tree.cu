@@ -3,7 +3,8 @@
 // "大模型推理 memory bandwidth bound (5) - Medusa", 二.2 generate_medusa_buffers(): the tree is fixed before
 // decoding and turned once into index buffers that stay resident on the device (also "OpenPangu7B-with-Medusa"
 // README, 4: static tree tensors, fixed mask). Node order: root, then the rank tuples by (length, tuple).
-// The attention mask is kept as one 64-bit word per node (bit j = node j is an ancestor-or-self).
+// The attention mask is kept as MV_MASK_WORDS 64-bit words per node (bit j of the row = node j is an
+// ancestor-or-self).
 #include <algorithm>
 #include <map>
 #include <vector>
@@ -63,11 +64,11 @@ extern "C" mv_status mv_tree_create(const int32_t* ranks, const int32_t* lens, i
   for (int i = 0; i < n_choices; ++i) node_of[paths[i]] = i + 1;
 
   std::vector<int32_t> tree_indices(n), position_ids(n), parent(n);
-  std::vector<uint64_t> anc(n);
+  std::vector<uint64_t> anc((size_t)n * MV_MASK_WORDS, 0ull);
   tree_indices[0] = 0;
   position_ids[0] = 0;
   parent[0] = -1;
-  anc[0] = 1ull;
+  anc[0] = 1ull;  // the root sees itself
   int depth = 0;
   for (int i = 1; i < n; ++i) {
     const Path& p = paths[i - 1];
@@ -77,7 +78,9 @@ extern "C" mv_status mv_tree_create(const int32_t* ranks, const int32_t* lens, i
     parent[i] = it->second;
     position_ids[i] = (int32_t)p.size();
     tree_indices[i] = 1 + topk * ((int32_t)p.size() - 1) + p.back();
-    anc[i] = anc[parent[i]] | (1ull << i);  // parents precede children in this order
+    for (int w = 0; w < MV_MASK_WORDS; ++w)  // parents precede children in this order
+      anc[(size_t)i * MV_MASK_WORDS + w] = anc[(size_t)parent[i] * MV_MASK_WORDS + w];
+    anc[(size_t)i * MV_MASK_WORDS + (i >> 6)] |= 1ull << (i & 63);
     depth = std::max(depth, (int)p.size());
   }
 

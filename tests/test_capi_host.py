@@ -51,9 +51,11 @@ def test_tree_page_example():
     assert t.retrieve.tolist() == g["retrieve_indices"]
 
 
-@pytest.mark.parametrize("kind", ["synthetic", "dense", "chain", "root_only"])
+@pytest.mark.parametrize("kind", ["synthetic", "dense", "chain", "root_only", "synthetic130", "synthetic256"])
 def test_tree_matches_oracle(kind):
     choices = {"synthetic": synth.synthetic_tree_choices(64, 4, 10),
+               "synthetic130": synth.synthetic_tree_choices(130, 4, 10),   # masks of three words
+               "synthetic256": synth.synthetic_tree_choices(256, 4, 10),
                "dense": synth.dense_tree_choices([2, 3]),
                "chain": [tuple([0] * k) for k in range(1, 9)],
                "root_only": []}[kind]
@@ -69,7 +71,7 @@ def test_tree_matches_oracle(kind):
     ([(0,), (0,)], 10),                  # duplicate
     ([(3,)], 3),                         # rank >= topk
     ([(0,) * 9], 10),                    # deeper than MAX_DEPTH (and not prefix-closed)
-    ([(i,) for i in range(64)], 64),     # 65 nodes > MAX_NODES
+    ([(i,) for i in range(200)] + [(0, j) for j in range(56)], 200),   # 257 nodes > MAX_NODES
 ])
 def test_tree_errors(choices, topk):
     with pytest.raises(mv.MVError) as e:

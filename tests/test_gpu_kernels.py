@@ -55,6 +55,8 @@ TREES = {
     "dense1x2x3": (lambda: synth.dense_tree_choices([2, 3]), 10),
     "chain5": (lambda: [tuple([0] * k) for k in range(1, 6)], 10),
     "root": (lambda: [], 10),
+    "synthetic100": (lambda: synth.synthetic_tree_choices(100, 4, 10), 10),   # two query blocks, two mask words
+    "synthetic256": (lambda: synth.synthetic_tree_choices(256, 4, 10), 10),   # the largest tree: four of each
 }
 
 
@@ -66,7 +68,7 @@ def both_trees(name):
 
 # --------------------------------------------------------------------------------------------- candidates
 
-@pytest.mark.parametrize("name", ["synthetic64", "page63", "dense1x2x3", "chain5", "root"])
+@pytest.mark.parametrize("name", ["synthetic64", "page63", "dense1x2x3", "chain5", "root", "synthetic256"])
 def test_build_candidates_bit_exact(name):
     t, o = both_trees(name)
     K = max(1, o["depth"])
@@ -107,7 +109,7 @@ def _run_posterior(logits, tokens, t, mode, T=0.7, eps=0.09, delta=0.3):
     return mv.result_dict(out), stats.cpu().numpy(), amax.cpu().numpy()
 
 
-@pytest.mark.parametrize("tree", ["synthetic64", "page63"])
+@pytest.mark.parametrize("tree", ["synthetic64", "page63", "synthetic256"])
 @pytest.mark.parametrize("mode", [GREEDY, TYPICAL])
 @pytest.mark.parametrize("seed", range(10))
 def test_posterior_planted_full_size(mode, seed, tree):
@@ -286,7 +288,7 @@ def _attn_case(H, D, P, tree_name, S_max=None, seed=0):
 
 
 @pytest.mark.parametrize("P", [64, 512, 1024, 4096])
-@pytest.mark.parametrize("tree", ["synthetic64", "page63"])
+@pytest.mark.parametrize("tree", ["synthetic64", "page63", "synthetic100", "synthetic256"])
 def test_tree_attention_full_size(P, tree):
     """32 heads x 128 dims, the synthetic 64-node tree or the page's own, q/k/v ~N(0,1)."""
     _attn_case(32, 128, P, tree)
@@ -294,6 +296,8 @@ def test_tree_attention_full_size(P, tree):
 
 @pytest.mark.parametrize("H,D,P,tree,S_max", [(3, 16, 0, "dense1x2x3", None), (2, 32, 5, "dense1x2x3", 40),
                                               (4, 64, 130, "chain5", None), (1, 128, 7, "root", None),
-                                              (5, 128, 0, "synthetic64", 64), (2, 128, 200, "synthetic64", 300)])
+                                              (5, 128, 0, "synthetic64", 64), (2, 128, 200, "synthetic64", 300),
+                                              (2, 64, 37, "synthetic100", None), (3, 128, 0, "synthetic256", 256),
+                                              (1, 32, 70, "synthetic256", None)])
 def test_tree_attention_small_ragged(H, D, P, tree, S_max):
     _attn_case(H, D, P, tree, S_max)

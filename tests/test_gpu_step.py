@@ -42,7 +42,9 @@ def _cuda():
 
 @pytest.mark.parametrize("packed", [False, True])
 @pytest.mark.parametrize("M,K,n", [(128, 64, 64), (300, 72, 9), (256, 4096, 64), (4096, 4096, 64),
-                                   (12288, 4096, 1), (4096, 11008, 64), (32000, 4096, 64), (200, 8, 3)])
+                                   (12288, 4096, 1), (4096, 11008, 64), (32000, 4096, 64), (200, 8, 3),
+                                   (300, 72, 65), (4096, 4096, 128), (4096, 11008, 130), (32000, 4096, 256),
+                                   (200, 8, 255)])
 def test_linear_bf16_vs_float64(M, K, n, packed):
     w = synth.normal(1, "w", (M, K), 1.0, dtype=torch.bfloat16, device="cuda")
     x = synth.normal(2, "x", (n, K), 1.0, dtype=torch.bfloat16, device="cuda")
@@ -107,11 +109,15 @@ def test_prefill_matches_oracle():
     _check_topk_rows(sess.head_topk.cpu().numpy(), medusa_heads(om.get, DIMS.n_medusa, hs[-1]), 10)
 
 
-def test_one_step_internals():
-    _, _, tree, sess, om, ot = _setup(synth.dense_tree_choices([2, 3]))
+@pytest.mark.parametrize("wide", [False, True])
+def test_one_step_internals(wide):
+    """One verify step against the oracle: candidates, every node's logits, the accepted path, the compacted
+    cache and the next top-k. wide: a 200-node tree (four token groups, four query blocks, four mask words)."""
+    choices, topk = (synth.synthetic_tree_choices(200, 2, 16), 16) if wide else (synth.dense_tree_choices([2, 3]), 10)
+    _, _, tree, sess, om, ot = _setup(choices, topk=topk)
     p = _prompt()
     sess.prefill(torch.as_tensor(p, dtype=torch.int32, device="cuda"))
-    st = o_prefill(om, p.numpy(), S_MAX, 10)
+    st = o_prefill(om, p.numpy(), S_MAX, topk)
     sess.step(mv.AcceptParams(GREEDY))
     torch.cuda.synchronize()
     toks, info = o_verify_step(om, st, ot, GREEDY)
@@ -127,7 +133,7 @@ def test_one_step_internals():
         assert int(sess.cur_len.item()) == L
         kv = sess.kv[:, :, :, :L].double().cpu().numpy()
         assert np.allclose(kv, st.cache.data[:, :, :, :L], rtol=RTOL, atol=ATOL)
-        _check_topk_rows(sess.head_topk.cpu().numpy(), info["head_logits"], 10)
+        _check_topk_rows(sess.head_topk.cpu().numpy(), info["head_logits"], topk)
         assert res["next_root"] == st.root
 
 
@@ -159,18 +165,22 @@ def _margin_ok(gen, prompt, om):
     return first_close
 
 
-@pytest.mark.parametrize("tree,packed", [("dense", True), ("synthetic", True), ("dense", False), ("page", True)])
+@pytest.mark.parametrize("tree,packed", [("dense", True), ("synthetic", True), ("dense", False), ("page", True),
+                                         ("wide200", True)])
 def test_greedy_decode_equals_ar(tree, packed):
     dims = DIMS
+    topk = 10
     if tree == "dense":
         choices = synth.dense_tree_choices([2, 3])
+    elif tree == "wide200":  # 200 nodes: four token groups in the projections, four query blocks in the attention
+        choices, topk = synth.synthetic_tree_choices(200, 2, 16), 16
     elif tree == "synthetic":
         choices = synth.synthetic_tree_choices(64, 2, 10)
     else:  # the page's own 63-choice tree ("大模型推理 memory bandwidth bound (5) - Medusa", 二.2): depth 4, 4 heads
         with open(os.path.join(os.path.dirname(__file__), "golden", "page4_tree.json")) as f:
             choices = [tuple(c) for c in json.load(f)["medusa_choices"]]
         dims = dataclasses.replace(DIMS, n_medusa=4)
-    _, _, _, sess, om, ot = _setup(choices, packed=packed, dims=dims)
+    _, _, _, sess, om, ot = _setup(choices, topk=topk, packed=packed, dims=dims)
     p = _prompt().numpy()
     gen, accs = _gpu_decode(sess, p, 16, mv.AcceptParams(GREEDY))
     first_close = _margin_ok(gen, p, om)
