@@ -320,8 +320,9 @@ def run_gpu(args, world, rank, local):
                                           "down and the next QKV, plus the first QKV)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": GEMM_TRAFFIC_PER_ALGORITHMIC_BYTE * g_bytes / max(g_n, 1),
-                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the LM-head and batched-heads "
-                                  "W2 launches, scaled to the step's average projection launch by its algorithmic bytes",
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the LM-head launch "
+                                  "(profiles/gemm_kernel_lm_head_32000x4096_t64.md), scaled to the step's average "
+                                  "projection launch by its algorithmic bytes",
                 "algorithmic_bytes_per_launch": g_bytes / max(g_n, 1),
                 "avg_launch_us": g_ms * 1e3 / max(g_n, 1),
                 "per_kind": {k: {"launches_per_step": c / args.steps, "ms_per_step": ms / args.steps,
@@ -351,10 +352,10 @@ def run_gpu(args, world, rank, local):
     return line
 
 
-# DRAM bytes (read + write) per algorithmic byte of the projection kernel, from ncu captures of the LM-head launch
-# (32000 x 4096, 64 tokens: 268.2 MB measured for 270.9 MB algorithmic) and of the batched heads' W2 launch
-# (1056.8 / 1066.0 MB): the kernel reads every weight byte once, so the traffic of a launch scales with its bytes.
-GEMM_TRAFFIC_PER_ALGORITHMIC_BYTE = 0.990
+# DRAM bytes (read + write) per algorithmic byte of the projection kernel, from the ncu capture of the LM-head
+# launch (32000 x 4096, 64 tokens: 267.9 MB measured for 270.9 MB algorithmic): the kernel reads every weight byte
+# once, so the traffic of a launch scales with its bytes.
+GEMM_TRAFFIC_PER_ALGORITHMIC_BYTE = 0.989
 
 
 def gemm_bytes(dims, n):
