@@ -525,6 +525,43 @@ def run_sweep_nodes(sizes, steps, warmup):
         del sess, tree
 
 
+def run_sweep_batch(batches, steps, warmup, tree_name):
+    """Verify steps of B independent sequences per session (one backbone pass for all B trees per step): one JSON
+    line per B with the step time and the sequence-steps per second. Each sequence has its own 128-token prompt."""
+    import medusa_tree_speculative_verify_gb300 as mv
+    dims = synth.LLAMA7B
+    w = mv.pack_model_weights(synth.packed_weights(dims, 0, torch.bfloat16, "cuda"), drop_source=True)
+    model = mv.Model(dims, w)
+    tree = mv.Tree(tree_choices(tree_name), TREE["topk"])
+    prm = mv.AcceptParams(mv.GREEDY)
+    stream = torch.cuda.current_stream()
+    for B in batches:
+        s_max = (PROMPT_LEN + (TREE["depth"] + 1) * (warmup + 2 * steps + 2) + 64 + 63) // 64 * 64
+        sess = mv.Session(model, tree, s_max, batch=B)
+        for b in range(B):
+            sess.prefill_seq(b, synth.prompt_tokens(b, PROMPT_LEN, dims.vocab).to(torch.int32).cuda())
+        for _ in range(warmup):
+            sess.step(prm)
+        sess.steps_graph(steps, prm)
+        torch.cuda.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(0) as clk:
+            clk.ready()
+            a.record(stream)
+            sess.steps_graph(steps, prm)
+            b_.record(stream)
+            torch.cuda.synchronize()
+            clk.stop()
+        ms = a.elapsed_time(b_) / steps
+        st, code = mv.get_error()
+        if st != 0:
+            raise RuntimeError(f"device error word {code:#x}")
+        print(json.dumps({"sweep": "batch", "batch": B, "n_nodes": tree.n_nodes, "steps": steps, "ms_per_step": ms,
+                          "steps_per_s": 1e3 / ms, "sequence_steps_per_s": B * 1e3 / ms,
+                          "clocks": clk.summary()}), flush=True)
+        del sess
+
+
 def weight_bytes(dims):
     d, HD, F, V, K, L = dims.d, dims.n_heads * dims.head_dim, dims.ffn, dims.vocab, dims.n_medusa, dims.n_layers
     per_layer = 2 * (3 * HD * d + d * HD + 2 * F * d + d * F)
@@ -542,11 +579,16 @@ def main():
                     help="the tree of the verify step: the synthetic 64-node tree or the page's own 63 choices")
     ap.add_argument("--micro", choices=sorted(MICRO) + MICRO_OTHER, help="time one kernel alone and exit")
     ap.add_argument("--sweep-nodes", default=None,
-                    help="comma-separated tree sizes (2..64): time the verify step per size and exit")
+                    help="comma-separated tree sizes (2..256): time the verify step per size and exit")
+    ap.add_argument("--sweep-batch", default=None,
+                    help="comma-separated batch sizes (1..4): time the batched verify step per size and exit")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.sweep_nodes:
         run_sweep_nodes([int(x) for x in args.sweep_nodes.split(",")], args.steps, args.warmup)
+        return
+    if args.sweep_batch:
+        run_sweep_batch([int(x) for x in args.sweep_batch.split(",")], args.steps, args.warmup, args.tree)
         return
     if args.micro:
         fn = run_micro if args.micro in MICRO else run_micro_other

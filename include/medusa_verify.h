@@ -49,6 +49,7 @@ typedef enum mv_status {
 #define MV_MAX_NODES 256 /* tree nodes (root included) */
 #define MV_MASK_WORDS 4  /* 64-bit ancestor words per node: the attention mask row of MV_MAX_NODES bits */
 #define MV_MAX_DEPTH 8  /* longest root-to-leaf path, root excluded */
+#define MV_MAX_BATCH 4  /* sequences of one batched session */
 
 /* ============================================================================================
  * Static token tree  [M5 二.2 generate_medusa_buffers()], [OP 4]
@@ -297,6 +298,15 @@ void mv_model_destroy(mv_model* model);
 mv_status mv_session_workspace(const mv_model* model, int32_t s_max, int32_t topk, size_t* bytes);
 mv_status mv_session_create(mv_model* model, const mv_tree* tree, mv_bf16* kv, int32_t s_max, int32_t topk,
                             void* workspace, size_t ws_bytes, mv_session** out);
+/* Batch > 1 verify (the pages' code supports only batch 1, 二.1 medusa_generate()): `batch` independent
+ * sequences (1 .. MV_MAX_BATCH) of the same tree (at most 64 nodes when batch > 1) in one session, kv
+ * [batch][n_layers][2][n_heads][s_max][head_dim]. Each verify step runs one backbone pass over all the
+ * sequences' trees, so every weight byte is read once per step for the whole batch; candidates, posterior,
+ * root, KV compaction and heads run per sequence. Same workspace size as mv_session_workspace(). A batch of one
+ * is mv_session_create. Errors: MV_ERR_INVALID_ARG (batch outside 1 .. MV_MAX_BATCH, null pointers),
+ * MV_ERR_SHAPE (as mv_session_create; also a tree over 64 nodes with batch > 1). */
+mv_status mv_batch_session_create(mv_model* model, const mv_tree* tree, int32_t batch, mv_bf16* kv, int32_t s_max,
+                                  int32_t topk, void* workspace, size_t ws_bytes, mv_session** out);
 void mv_session_destroy(mv_session* session);
 
 typedef struct mv_session_state_ptrs {
@@ -309,19 +319,26 @@ typedef struct mv_session_state_ptrs {
   int32_t ld_logits;
   float* hidden;                /* device fp32 [MV_MAX_NODES][d]: the last forward's residual stream (before the
                                    final norm) */
-  uint64_t* root_counter;       /* device [1]: generator counter of the next sampled root */
+  uint64_t* root_counter;       /* device [batch]: generator counter of each sequence's next sampled root */
+  int32_t batch;                /* sequences of the session; the arrays above then hold one entry per sequence:
+                                   cur_len[b], result[b], head_topk[b][n_medusa][topk], root_counter[b];
+                                   tree_tokens, logits and hidden rows of sequence b start at row 64 b, cart rows
+                                   at 64 b (9 entries each) */
 } mv_session_state_ptrs;
 mv_status mv_session_state(const mv_session* session, mv_session_state_ptrs* out);
 
 /* Prefill [M5 二.3 initialize_medusa()]: runs tokens d_tokens[0..n) causally from position 0 (chunks of 64),
  * then sets the root (argmax of the last logits row), the head top-k (heads on the last token) and
- * cur_len = n. Limits: 1 <= n, n + 64 <= s_max. */
+ * cur_len = n. Limits: 1 <= n, n + 64 <= s_max. A batched session returns MV_ERR_UNSUPPORTED (use
+ * mv_prefill_seq). */
 mv_status mv_prefill(mv_session* session, const int32_t* d_tokens, int32_t n, mv_stream stream);
+/* The same for sequence `seq` (0 <= seq < batch) of a session: its cache, length, root and head top-k. */
+mv_status mv_prefill_seq(mv_session* session, int32_t seq, const int32_t* d_tokens, int32_t n, mv_stream stream);
 
 /* Root sampling of a session (default MV_ROOT_ARGMAX): the root after mv_prefill and after every verify step
  * is drawn as sample_root() describes from the logits row of node retrieve[best][acc] (the prefill: the
- * prompt's last row), with the counter held in device memory, starting at `counter` and advancing by one per
- * draw. The verify step's acceptance rule stays the one of its mv_accept_params. Enqueues the counter store on
+ * prompt's last row), with the counter held in device memory, starting at `counter` (sequence b of a batched
+ * session at counter + b * 2^32) and advancing by one per draw. The verify step's acceptance rule stays the one of its mv_accept_params. Enqueues the counter store on
  * `stream`; CUDA graphs captured earlier by medusa_verify_steps_graph are re-captured on their next call.
  * Errors: MV_ERR_INVALID_ARG as for sample_root. */
 mv_status mv_session_set_root_sampling(mv_session* session, mv_root_params params, uint64_t counter,
@@ -338,7 +355,7 @@ mv_status medusa_verify_step(mv_session* session, mv_accept_params params, mv_st
 /* The same step driven from host memory: h_seeds_in (nullable) = [root, head_topk[n_medusa][topk]] copied to
  * the device first; afterwards the result (mv_posterior_result, as int32s) is copied to h_result and, if
  * h_seeds_out is not NULL, the next seeds to h_seeds_out. Synchronises `stream` before returning. Host
- * buffers should be pinned for asynchronous copies. */
+ * buffers should be pinned for asynchronous copies. A batched session returns MV_ERR_UNSUPPORTED. */
 mv_status medusa_verify_step_host(mv_session* session, mv_accept_params params, const int32_t* h_seeds_in,
                                   int32_t* h_result, int32_t* h_seeds_out, mv_stream stream);
 

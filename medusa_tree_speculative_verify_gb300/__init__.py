@@ -96,9 +96,11 @@ _SIGS = {
     "mv_model_destroy": ([_P], None),
     "mv_session_workspace": ([_P, _I, _I, ctypes.POINTER(_S)], _I),
     "mv_session_create": ([_P, _P, _P, _I, _I, _P, _S, ctypes.POINTER(_P)], _I),
+    "mv_batch_session_create": ([_P, _P, _I, _P, _I, _I, _P, _S, ctypes.POINTER(_P)], _I),
     "mv_session_destroy": ([_P], None),
     "mv_session_state": ([_P, _P], _I),
     "mv_prefill": ([_P, _P, _I, _P], _I),
+    "mv_prefill_seq": ([_P, _I, _P, _I, _P], _I),
     "mv_session_set_root_sampling": ([_P, RootParams, ctypes.c_uint64, _P], _I),
     "medusa_verify_step": ([_P, AcceptParams, _P], _I),
     "medusa_verify_step_host": ([_P, AcceptParams, _P, _P, _P, _P], _I),
@@ -332,7 +334,7 @@ class _Weights(ctypes.Structure):
 
 class _StatePtrs(ctypes.Structure):
     _fields_ = [("cur_len", _P), ("result", _P), ("head_topk", _P), ("tree_tokens", _P), ("cart", _P),
-                ("logits", _P), ("ld_logits", _I), ("hidden", _P), ("root_counter", _P)]
+                ("logits", _P), ("ld_logits", _I), ("hidden", _P), ("root_counter", _P), ("batch", _I)]
 
 
 class Model:
@@ -365,20 +367,23 @@ class Model:
 
 
 class Session:
-    """A decode session: model + tree + KV cache [L,2,H,s_max,D] (bf16) + workspace (allocated here)."""
+    """A decode session: model + tree + KV cache + workspace (allocated here). batch > 1: that many sequences
+    verified together (KV cache [batch,L,2,H,s_max,D]); the state views then have a leading batch dimension."""
 
-    def __init__(self, model: Model, tree: Tree, s_max, topk=None, kv=None):
+    def __init__(self, model: Model, tree: Tree, s_max, topk=None, kv=None, batch=1):
         import torch
         d = model.dims
-        self.model, self.tree, self.s_max = model, tree, s_max
+        self.model, self.tree, self.s_max, self.batch = model, tree, s_max, batch
         self.topk = topk or tree.topk
-        self.kv = kv if kv is not None else torch.zeros(d.n_layers, 2, d.n_heads, s_max, d.head_dim,
-                                                         dtype=torch.bfloat16, device="cuda")
+        shape = (d.n_layers, 2, d.n_heads, s_max, d.head_dim)
+        if batch > 1:
+            shape = (batch,) + shape
+        self.kv = kv if kv is not None else torch.zeros(*shape, dtype=torch.bfloat16, device="cuda")
         nbytes = _ws_size(lib().mv_session_workspace, model.handle, s_max, self.topk)
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
         h = ctypes.c_void_p()
-        _check(lib().mv_session_create(model.handle, tree.handle, _ptr(self.kv), s_max, self.topk, _ptr(self.ws),
-                                       nbytes, ctypes.byref(h)), "mv_session_create")
+        _check(lib().mv_batch_session_create(model.handle, tree.handle, batch, _ptr(self.kv), s_max, self.topk,
+                                             _ptr(self.ws), nbytes, ctypes.byref(h)), "mv_batch_session_create")
         self.handle = h
         sp = _StatePtrs()
         _check(lib().mv_session_state(h, ctypes.byref(sp)), "mv_session_state")
@@ -389,19 +394,27 @@ class Session:
             esz = torch.empty(0, dtype=dtype).element_size()
             return self.ws[off: off + count * esz].view(dtype)
 
-        K = d.n_medusa
-        self.cur_len = view(sp.cur_len, 1, torch.int32)
-        self.result = view(sp.result, RESULT_INTS, torch.int32)
-        self.head_topk = view(sp.head_topk, K * self.topk, torch.int32).view(K, self.topk)
+        K, B = d.n_medusa, batch
+        if B == 1:
+            self.cur_len = view(sp.cur_len, 1, torch.int32)
+            self.result = view(sp.result, RESULT_INTS, torch.int32)
+            self.head_topk = view(sp.head_topk, K * self.topk, torch.int32).view(K, self.topk)
+        else:
+            self.cur_len = view(sp.cur_len, B, torch.int32)
+            self.result = view(sp.result, B * RESULT_INTS, torch.int32).view(B, RESULT_INTS)
+            self.head_topk = view(sp.head_topk, B * K * self.topk, torch.int32).view(B, K, self.topk)
         self.tree_tokens = view(sp.tree_tokens, tree.n_nodes, torch.int32)
         self.cart = view(sp.cart, tree.n_paths * (tree.depth + 1), torch.int32).view(tree.n_paths, tree.depth + 1)
         self.ld_logits = sp.ld_logits
         self.logits = view(sp.logits, MAX_NODES * sp.ld_logits, torch.float32).view(MAX_NODES, sp.ld_logits)[:, : d.vocab]
         self.hidden = view(sp.hidden, MAX_NODES * d.d, torch.float32).view(MAX_NODES, d.d)
-        self.root_counter = view(sp.root_counter, 1, torch.int64)
+        self.root_counter = view(sp.root_counter, B, torch.int64)
 
     def prefill(self, tokens, stream=None):
         _check(lib().mv_prefill(self.handle, _ptr(tokens), tokens.numel(), _stream(stream)), "mv_prefill")
+
+    def prefill_seq(self, seq, tokens, stream=None):
+        _check(lib().mv_prefill_seq(self.handle, seq, _ptr(tokens), tokens.numel(), _stream(stream)), "mv_prefill_seq")
 
     def set_root_sampling(self, params: RootParams, counter=0, stream=None):
         """Draw the root after prefill / every step with ``params`` (ROOT_ARGMAX restores the argmax root)."""
@@ -421,8 +434,9 @@ class Session:
         _check(lib().medusa_verify_step_host(self.handle, params, _ptr(seeds_in), _ptr(result_out), _ptr(seeds_out),
                                              _stream(stream)), "medusa_verify_step_host")
 
-    def read_result(self):
-        return result_dict(self.result)
+    def read_result(self, seq=None):
+        """The last verification of the session (batch 1) or of sequence ``seq``."""
+        return result_dict(self.result if seq is None and self.batch == 1 else self.result[seq or 0])
 
     def __del__(self):
         if getattr(self, "handle", None) is not None and _lib is not None:

@@ -80,9 +80,13 @@ struct AttnArgs {
   const uint16_t* q;        // [n][H][D]
   uint16_t* out;            // [n][H][D]
   const uint64_t* anc;      // [n][MV_MASK_WORDS]
-  const int32_t* d_prefix;  // device prefix length or null
+  const int32_t* d_prefix;  // device prefix length (one per sequence when seq_rows > 0) or null
   int prefix;               // used when d_prefix is null
   int H, S_max, n, splits, plane_k, plane_v;  // splits = CTAs per cluster (gridDim.x)
+  // Several sequences (grid z = sequence): sequence b's queries are rows b * seq_rows + 0 .. n - 1, its cache
+  // planes plane_k / plane_v + b * seq_planes, its prefix d_prefix[b]. seq_rows = 0: grid z = blocks of 64 rows
+  // of one tree.
+  int seq_rows, seq_planes;
   float scale_log2;         // scale * log2(e)
   unsigned int* err;
 };
@@ -105,13 +109,17 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
   constexpr int kPo = D + 4;  // row pitch (floats) of the partial output in shared memory
 
   const int split = blockIdx.x, h = blockIdx.y;  // split = rank in the head's cluster
-  const int row0 = blockIdx.z * kRows;           // this CTA's query rows: tree nodes row0 .. row0 + 63
+  const int seq = a.seq_rows ? (int)blockIdx.z : 0;
+  // this CTA's query rows: q / out rows qrow0 .. qrow0 + 63, tree nodes row0 .. row0 + 63
+  const int row0 = a.seq_rows ? 0 : (int)blockIdx.z * kRows;
+  const int qrow0 = a.seq_rows ? seq * a.seq_rows : row0;
+  const int plane_k = a.plane_k + seq * a.seq_planes, plane_v = a.plane_v + seq * a.seq_planes;
   const int C = a.splits;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t4 = lane & 3;
   pdl_trigger();
   pdl_wait();  // q, the cache and the prefix length come from earlier kernels
-  const int P = a.d_prefix ? *a.d_prefix : a.prefix;
+  const int P = a.d_prefix ? a.d_prefix[seq] : a.prefix;
   const int n_all = a.n;
   if (P < 0 || P + n_all > a.S_max) {
     if (tid == 0) mv_set_error(a.err, 4, MV_DEVERR_INDEX);
@@ -136,9 +144,9 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
 #pragma unroll
     for (int b = 0; b < kBoxes; ++b) {
       tma_load_4d(sk + st * kTileBytes + b * (kKeys * kBoxCols * 2), &kmap, &full[st], b * kBoxCols, key0, h,
-                  a.plane_k);
+                  plane_k);
       tma_load_4d(sv + st * kTileBytes + b * (kKeys * kBoxCols * 2), &vmap, &full[st], b * kBoxCols, key0, h,
-                  a.plane_v);
+                  plane_v);
     }
   };
   // the first key/value tiles are requested before Q is loaded, so the two latencies overlap
@@ -151,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
   for (int e = tid; e < kRows * (D / 8); e += kThreads) {
     const int r = e / (D / 8), c = e % (D / 8);
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < n) v = *reinterpret_cast<const uint4*>(a.q + ((size_t)(row0 + r) * a.H + h) * D + c * 8);
+    if (r < n) v = *reinterpret_cast<const uint4*>(a.q + ((size_t)(qrow0 + r) * a.H + h) * D + c * 8);
     *reinterpret_cast<uint4*>(sq + tile_off<D>(r, c)) = v;
   }
   __syncthreads();
@@ -292,10 +300,10 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
     for (int dn = 0; dn < DN; ++dn) {
       const int col = 8 * dn + 2 * t4;
       if (q0 < n)
-        *reinterpret_cast<uint32_t*>(a.out + ((size_t)(row0 + q0) * a.H + h) * D + col) =
+        *reinterpret_cast<uint32_t*>(a.out + ((size_t)(qrow0 + q0) * a.H + h) * D + col) =
             pack_bf16x2(o[dn][0] * i0, o[dn][1] * i0);
       if (q1 < n)
-        *reinterpret_cast<uint32_t*>(a.out + ((size_t)(row0 + q1) * a.H + h) * D + col) =
+        *reinterpret_cast<uint32_t*>(a.out + ((size_t)(qrow0 + q1) * a.H + h) * D + col) =
             pack_bf16x2(o[dn][2] * i1, o[dn][3] * i1);
     }
     return;
@@ -373,7 +381,7 @@ __global__ void __launch_bounds__(kThreads) tree_attn_kernel(const __grid_consta
     uint2 pk;
     pk.x = pack_bf16x2(acc.x, acc.y);
     pk.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(a.out + ((size_t)(row0 + q) * a.H + h) * D + c4) = pk;
+    *reinterpret_cast<uint2*>(a.out + ((size_t)(qrow0 + q) * a.H + h) * D + c4) = pk;
   }
   cluster_sync_all();  // no CTA leaves while another may still read its partial
 }
@@ -467,10 +475,11 @@ mv_status launch_tree_attention(const CUtensorMap& kmap, const CUtensorMap& vmap
 mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vmap, int plane_k, int plane_v,
                                   const mv_bf16* q, int H, int D, int S_max, const int32_t* d_prefix, int prefix,
                                   int max_prefix, const mv_tree* t, int n, float scale, mv_bf16* out, void* ws,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, int nseq, int seq_planes) {
   (void)ws;  // reserved
-  if (n < 1 || n > MV_MAX_NODES) return MV_ERR_SHAPE;
-  const int blocks = (n + kRows - 1) / kRows;  // blocks of 64 query rows
+  if (n < 1 || n > MV_MAX_NODES || nseq < 1 || (nseq > 1 && (n > kRows || !d_prefix))) return MV_ERR_SHAPE;
+  // blocks of 64 query rows of one tree, or one block per sequence
+  const int blocks = nseq > 1 ? nseq : (n + kRows - 1) / kRows;
   const int max_tiles = (max_prefix + n + kKeys - 1) / kKeys;
   int splits = choose_splits(max_tiles);
   // all H x blocks clusters resident at once: a cluster that has to wait for another to leave costs a whole
@@ -488,6 +497,8 @@ mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vm
   a.splits = splits;
   a.plane_k = plane_k;
   a.plane_v = plane_v;
+  a.seq_rows = nseq > 1 ? kRows : 0;
+  a.seq_planes = seq_planes;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.err = mv_error_word();
   const size_t smem = smem_bytes(D);

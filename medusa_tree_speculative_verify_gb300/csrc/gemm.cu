@@ -126,11 +126,12 @@ MV_DEV uint64_t sw128_desc(uint32_t saddr) {
 // the per-token RMSNorm scale s[j] = 1/sqrt(sum of the sum-of-squares partials / norm_d + eps) (1 without a
 // norm), and for the QKV epilogue the token positions prefix + depth. The 128 epilogue threads split the
 // partial sums so the loads are independent and in flight together.
+constexpr int kMaxSeq = kTokMax / BN;  // sequences of one pass (one token group each)
 struct EpiConst {
   float scale[kTokMax];
   int pos[kTokMax];
   float part[2][kTokMax];
-  int kv_row0;  // -1: the cache rows would run past S_max (nothing is appended)
+  int kv_row0[kMaxSeq];  // per sequence; -1: the cache rows would run past S_max (nothing is appended)
 };
 
 MV_DEV void load_epi_const(const GemmParams& p, EpiConst* ec, int i, int ngroups) {
@@ -150,15 +151,23 @@ MV_DEV void load_epi_const(const GemmParams& p, EpiConst* ec, int i, int ngroups
       t = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     }
     ec->part[half][j] = t;
-    if (half == 0 && p.pos_ids) ec->pos[j] = j < p.n_tok ? *p.cur_len + p.pos_ids[j] : 0;
-  }
-  if (i == 0) {
-    int r0 = p.cur_len ? *p.cur_len : 0;
-    if (p.kv && (r0 < 0 || r0 + p.n_tok > p.S_max)) {  // appending would write past the cache planes
-      mv_set_error_detail(p.err, 14, MV_DEVERR_INDEX, (uint32_t)r0);
-      r0 = -1;
+    if (half == 0 && p.pos_ids) {
+      const int b = p.seq_rows ? j / p.seq_rows : 0, r = j - b * p.seq_rows;
+      ec->pos[j] = (j < p.n_tok && (!p.seq_rows || r < p.seq_n)) ? p.cur_len[b] + p.pos_ids[r] : 0;
     }
-    ec->kv_row0 = r0;
+  }
+  if (i < kMaxSeq) {
+    const int nseq = p.seq_rows ? (p.n_tok + p.seq_rows - 1) / p.seq_rows : 1;
+    int r0 = -1;
+    if (i < nseq) {
+      r0 = p.cur_len ? p.cur_len[i] : 0;
+      const int rows = p.seq_rows ? p.seq_n : p.n_tok;
+      if (p.kv && (r0 < 0 || r0 + rows > p.S_max)) {  // appending would write past the cache planes
+        mv_set_error_detail(p.err, 14, MV_DEVERR_INDEX, (uint32_t)r0);
+        r0 = -1;
+      }
+    }
+    ec->kv_row0[i] = r0;
   }
   epi_bar();
   for (int g = 0; g < ngroups; ++g) {
@@ -313,17 +322,9 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int jb, int w, int l, 
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       inv_freq[q] = exp2f(-(float)(2 * ((dim + q) % half)) / (float)p.D * p.log2_theta);
-    uint16_t* dst;
-    size_t stride;
-    if (which == 0) {
-      dst = p.q_out + (size_t)head * p.D + dim;
-      stride = (size_t)p.H * p.D;
-    } else {
-      const size_t plane = (size_t)p.layer * 2 + (which - 1);
-      dst = p.kv + ((plane * p.H + head) * p.S_max + max(ec->kv_row0, 0)) * p.D + dim;
-      stride = (size_t)p.D;
-    }
-    const bool store = valid && (which == 0 || ec->kv_row0 >= 0);
+    // q: row j of q_out; k / v: row kv_row0[b] + r of sequence b's cache plane (j = b * seq_rows + r)
+    const size_t plane = (size_t)p.layer * 2 + ((which == 1 || which == 2) ? which - 1 : 0);
+    uint16_t* const kv_base = p.kv ? p.kv + (plane * p.H + head) * p.S_max * p.D + dim : nullptr;
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
       const int t = r0 + u * cs;
@@ -331,7 +332,15 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int jb, int w, int l, 
       const int j = jb + w + 4 * t;
       if (j >= ntok) continue;  // uniform over the warp
       const float4 pr = shfl_xor4(acc[u], p.D >> 3);  // the RoPE partner rows (dim -+ D/2, same head)
-      if (!store) continue;
+      const int b = p.seq_rows ? j / p.seq_rows : 0, r = j - b * p.seq_rows;
+      if (!valid || (p.seq_rows && r >= p.seq_n)) continue;  // past the weights, or a padding row
+      uint16_t* dst;
+      if (which == 0) {
+        dst = p.q_out + (size_t)j * p.H * p.D + (size_t)head * p.D + dim;
+      } else {
+        if (ec->kv_row0[b] < 0) continue;
+        dst = kv_base + (size_t)b * p.kv_seq_stride + (size_t)(ec->kv_row0[b] + r) * p.D;
+      }
       const float s = ec->scale[j];
       float v[4] = {acc[u].x * s, acc[u].y * s, acc[u].z * s, acc[u].w * s};
       if (which < 2) {
@@ -344,7 +353,7 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int jb, int w, int l, 
           v[q] = lo ? v[q] * cs - pv[q] * sn : v[q] * cs + pv[q] * sn;
         }
       }
-      *reinterpret_cast<uint2*>(dst + (size_t)j * stride) = pack_bf16x4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<uint2*>(dst) = pack_bf16x4(v[0], v[1], v[2], v[3]);
     }
   }
 }

@@ -34,8 +34,13 @@ struct GemmParams {
   uint16_t* q_out;  // [n][H][D]
   uint16_t* kv;     // [L][2][H][S_max][D]
   int H, D, S_max, layer;
-  const int32_t* cur_len;  // device prefix length
-  const int32_t* pos_ids;  // [n] depth of each token
+  const int32_t* cur_len;  // device prefix length (one per sequence when seq_rows > 0)
+  const int32_t* pos_ids;  // [n] depth of each token (of each tree row when seq_rows > 0)
+  // Several sequences in one pass (QKV): token j is row j % seq_rows of sequence j / seq_rows's tree; rows at or
+  // past seq_n are padding (nothing is appended). The sequences' caches are kv_seq_stride elements apart.
+  // seq_rows = 0: one sequence.
+  int seq_rows, seq_n;
+  size_t kv_seq_stride;
   float log2_theta;
   unsigned int* err;
 };

@@ -47,7 +47,9 @@ mv_status launch_tree_attention(const CUtensorMap& kmap, const CUtensorMap& vmap
                                 const mv_bf16* q, int H, int D, int S_max, const int32_t* d_prefix, int prefix,
                                 int max_prefix, const mv_tree* t, float scale, mv_bf16* out, void* ws,
                                 cudaStream_t stream);
+// nseq > 1: nseq sequences of the same tree (n <= 64 nodes each): sequence b's queries / outputs are rows
+// 64 b .. 64 b + n - 1, its cache planes plane_k / plane_v + b * seq_planes, its prefix d_prefix[b].
 mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vmap, int plane_k, int plane_v,
                                   const mv_bf16* q, int H, int D, int S_max, const int32_t* d_prefix, int prefix,
                                   int max_prefix, const mv_tree* t, int n, float scale, mv_bf16* out, void* ws,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, int nseq = 1, int seq_planes = 0);

@@ -23,12 +23,25 @@ namespace {
 constexpr int kTok = MV_MAX_NODES;  // token rows of every activation buffer (the largest tree)
 constexpr int kChunk = 64;         // prefill chunk: one token group, run as a causal chain
 
+constexpr int kSeqRows = 64;       // rows per sequence when several sequences share a pass
+
 // x[j][:] = float(E[tok[j]][:]), xb = E[tok[j]] (bf16), ssq[s][j] = sum of x^2 over the 128-column slice s.
+// With seq_rows > 0, rows j with j % seq_rows >= seq_n are padding between sequences: zeroed, so that what the
+// projections compute for them stays finite (no output of a real row depends on them).
 __global__ void __launch_bounds__(256) embed_kernel(const int32_t* tokens, const uint16_t* __restrict__ E, int vocab,
-                                                    int d, float* x, uint16_t* xb, float* ssq, unsigned int* err) {
+                                                    int d, float* x, uint16_t* xb, float* ssq, unsigned int* err,
+                                                    int seq_rows, int seq_n) {
   pdl_trigger();
   pdl_wait();
   const int j = blockIdx.x;
+  if (seq_rows && j % seq_rows >= seq_n) {
+    for (int c = threadIdx.x; c < d; c += blockDim.x) {
+      x[(size_t)j * d + c] = 0.0f;
+      xb[(size_t)j * d + c] = 0;
+    }
+    for (int s = threadIdx.x; s < (d + 127) / 128; s += blockDim.x) ssq[s * kTok + j] = 0.0f;
+    return;
+  }
   const int tok = tokens[j];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (tok < 0 || tok >= vocab) {
@@ -108,10 +121,11 @@ __global__ void set_int_kernel(int32_t* p, int v) {
   *p = v;
 }
 
-__global__ void set_u64_kernel(uint64_t* p, uint64_t v) {
+// p[b] = v + b * 2^32 for the n sequences of a session (each draws from its own range of counters)
+__global__ void set_counters_kernel(uint64_t* p, uint64_t v, int n) {
   pdl_trigger();
   pdl_wait();
-  *p = v;
+  for (int b = 0; b < n; ++b) p[b] = v + ((uint64_t)b << 32);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -136,10 +150,12 @@ struct mv_session {
   mv_tree* chain;  // 64-node chain tree for prefill chunks (causal mask)
   uint16_t* kv;
   int s_max, topk;
-  // device buffers carved from the workspace
+  int batch;            // sequences verified together (1 .. MV_MAX_BATCH)
+  size_t kv_seq_elems;  // elements of one sequence's KV cache
+  // device buffers carved from the workspace; the per-sequence state is an array of `batch` entries
   int32_t* cur_len;
   mv_posterior_result* result;
-  int32_t* head_topk;
+  int32_t* head_topk;   // [batch][n_medusa][topk]
   int32_t* tree_tokens;
   int32_t* cart;
   float* x;
@@ -155,7 +171,7 @@ struct mv_session {
   void* ws_heads;
   unsigned int* chain_flags;  // phase counters of the projection chains (zero between launches)
   float2* row_max;            // [vocab/128][64]: per LM-head tile and token, max and first argmax
-  uint64_t* root_counter;     // generator counter of the next sampled root
+  uint64_t* root_counter;     // per sequence: generator counter of the next sampled root
   mv_root_params root{};      // root rule (MV_ROOT_ARGMAX: the posterior's argmax stands)
   int root_epoch = 0;         // bumped by every mv_session_set_root_sampling
   CUtensorMap m_xb, m_attn, m_act, m_kv;
@@ -220,7 +236,9 @@ SessionLayout session_layout(const mv_model_dims& d, int s_max, int topk) {
   };
   const int HD = d.n_heads * d.head_dim;
   const int ldl = (d.vocab + 3) & ~3;
-  L.state = take(512 + (size_t)d.n_medusa * topk * 4);
+  // cur_len [MV_MAX_BATCH] at 0, root counters at 16, results at 64, head top-k at 512
+  static_assert(64 + MV_MAX_BATCH * sizeof(mv_posterior_result) <= 512, "session state layout");
+  L.state = take(512 + (size_t)MV_MAX_BATCH * d.n_medusa * topk * 4);
   L.tree_tokens = take(kTok * 4);
   L.cart = take((size_t)kTok * (MV_MAX_DEPTH + 1) * 4);
   L.x = take((size_t)kTok * d.d * 4);
@@ -259,18 +277,22 @@ GemmParams base_params(const mv_session* s, int n_tok) {
   return p;
 }
 
-// One backbone pass over n tokens (tree nodes or a prefill chunk) whose ids are at d_tokens. `t` gives the
-// attention mask (ancestor words) and positions (depth); the prefix length is read from s->cur_len.
-mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int n, bool lm, cudaStream_t st) {
+// One backbone pass over the n tokens (tree nodes or a prefill chunk) of nseq sequences b0 .. b0 + nseq - 1,
+// whose ids are at d_tokens (sequence b's at row 64 (b - b0) when nseq > 1). `t` gives the attention mask
+// (ancestor words) and positions (depth); each prefix length is read from s->cur_len[b].
+mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int n, bool lm, cudaStream_t st,
+                  int nseq = 1, int b0 = 0) {
   const mv_model* m = s->model;
   const mv_model_dims& d = m->dims;
   const int HD = d.n_heads * d.head_dim;
   const int ssq_parts = (d.d + 127) / 128;
+  const int seq_rows = nseq > 1 ? kSeqRows : 0;
+  const int rows = nseq > 1 ? kSeqRows * (nseq - 1) + n : n;  // token rows of the pass, padding included
   mv_status rc;
   {
     ProfScope ps(s, st, MV_PROF_OTHER);
-    rc = mv_launch(embed_kernel, dim3(n), dim3(256), 0, st, d_tokens, m->embed, d.vocab, d.d, s->x, s->xb, s->ssq,
-                   mv_error_word()) == cudaSuccess
+    rc = mv_launch(embed_kernel, dim3(rows), dim3(256), 0, st, d_tokens, m->embed, d.vocab, d.d, s->x, s->xb,
+                   s->ssq, mv_error_word(), seq_rows, n) == cudaSuccess
              ? mv_last_launch("embed")
              : MV_ERR_CUDA;
   }
@@ -280,20 +302,23 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     g.epi = EPI_QKV;
     g.a0 = g.a1 = m->m_qkv[l];
     g.b = s->m_xb;
-    GemmParams& p = g.p = base_params(s, n);
+    GemmParams& p = g.p = base_params(s, rows);
     p.M = 3 * HD;
     p.K = d.d;
     p.ssq = s->ssq;
     p.ssq_parts = ssq_parts;
     p.norm_d = d.d;
     p.q_out = s->q;
-    p.kv = s->kv;
+    p.kv = s->kv + (size_t)b0 * s->kv_seq_elems;
     p.H = d.n_heads;
     p.D = d.head_dim;
     p.S_max = s->s_max;
     p.layer = l;
-    p.cur_len = s->cur_len;
+    p.cur_len = s->cur_len + b0;
     p.pos_ids = t->d_position_ids;
+    p.seq_rows = seq_rows;
+    p.seq_n = n;
+    p.kv_seq_stride = s->kv_seq_elems;
     p.log2_theta = log2f(d.rope_theta);
     return g;
   };
@@ -302,7 +327,7 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     g.epi = EPI_RESIDUAL;
     g.a0 = g.a1 = w;
     g.b = act;
-    GemmParams& p = g.p = base_params(s, n);
+    GemmParams& p = g.p = base_params(s, rows);
     p.M = d.d;
     p.K = K;
     p.x = s->x;
@@ -316,7 +341,7 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     g.a0 = m->m_gate[l];
     g.a1 = m->m_up[l];
     g.b = s->m_xb;
-    GemmParams& p = g.p = base_params(s, n);
+    GemmParams& p = g.p = base_params(s, rows);
     p.paired = 1;
     p.F = d.ffn;
     p.M = d.ffn;
@@ -332,7 +357,7 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     g.epi = EPI_STORE;
     g.a0 = g.a1 = m->m_lm;
     g.b = s->m_xb;
-    GemmParams& p = g.p = base_params(s, n);
+    GemmParams& p = g.p = base_params(s, rows);
     p.M = d.vocab;
     p.K = d.d;
     p.ssq = s->ssq;
@@ -351,9 +376,10 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
   for (int l = 0; l < d.n_layers && rc == MV_OK; ++l) {
     {
       ProfScope ps(s, st, MV_PROF_ATTENTION);
-      rc = launch_tree_attention_n(s->m_kv, s->m_kv, 2 * l, 2 * l + 1, s->q, d.n_heads, d.head_dim, s->s_max,
-                                   s->cur_len, 0, s->s_max - n, t, n, 1.0f / sqrtf((float)d.head_dim), s->attn,
-                                   s->ws_attn, st);
+      const int pl = b0 * 2 * d.n_layers + 2 * l;  // sequence b0's planes of layer l
+      rc = launch_tree_attention_n(s->m_kv, s->m_kv, pl, pl + 1, s->q, d.n_heads, d.head_dim, s->s_max,
+                                   s->cur_len + b0, 0, s->s_max - n, t, n, 1.0f / sqrtf((float)d.head_dim), s->attn,
+                                   s->ws_attn, st, nseq, 2 * d.n_layers);
     }
     if (rc != MV_OK) break;
     // O, gate/up and down of this layer, then the next layer's QKV (or the LM head): one launch
@@ -372,12 +398,15 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
   return rc;
 }
 
-mv_status run_heads(mv_session* s, cudaStream_t st) {
+// Medusa heads of sequence b on row result[b].next_node of its block of the pass (x rows from row0), then
+// cur_len[b] += result[b].n_tokens.
+mv_status run_heads(mv_session* s, int b, int row0, cudaStream_t st) {
   ProfScope ps(s, st, MV_PROF_HEADS);
   const mv_model* m = s->model;
   const mv_model_dims& d = m->dims;
-  return launch_heads(nullptr, s->x, s->result, d.norm_eps, 1, d.d, d.n_medusa, m->w1, m->w2, d.vocab, s->topk,
-                      nullptr, s->head_topk, nullptr, nullptr, s->cur_len, s->ws_heads, st);
+  return launch_heads(nullptr, s->x + (size_t)row0 * d.d, s->result + b, d.norm_eps, 1, d.d, d.n_medusa, m->w1,
+                      m->w2, d.vocab, s->topk, nullptr, s->head_topk + (size_t)b * d.n_medusa * s->topk, nullptr,
+                      nullptr, s->cur_len + b, s->ws_heads, st);
 }
 
 }  // namespace
@@ -438,13 +467,15 @@ extern "C" mv_status mv_session_workspace(const mv_model* m, int32_t s_max, int3
   return MV_OK;
 }
 
-extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16* kv, int32_t s_max, int32_t topk,
-                                       void* ws, size_t ws_bytes, mv_session** out) {
-  if (!m || !tree || !kv || !ws || !out) return MV_ERR_INVALID_ARG;
+extern "C" mv_status mv_batch_session_create(mv_model* m, const mv_tree* tree, int32_t batch, mv_bf16* kv,
+                                             int32_t s_max, int32_t topk, void* ws, size_t ws_bytes,
+                                             mv_session** out) {
+  if (!m || !tree || !kv || !ws || !out || batch < 1 || batch > MV_MAX_BATCH) return MV_ERR_INVALID_ARG;
   *out = nullptr;
   if (!tree->d_ancestors) return MV_ERR_CUDA;
   const mv_model_dims& d = m->dims;
   if (topk < tree->topk || topk > 16 || tree->depth > d.n_medusa || tree->n_nodes > kTok) return MV_ERR_SHAPE;
+  if (batch > 1 && tree->n_nodes > kSeqRows) return MV_ERR_SHAPE;  // one token group per sequence
   if (s_max < kChunk + 1) return MV_ERR_CAPACITY;
   const SessionLayout L = session_layout(d, s_max, topk);
   if (ws_bytes < L.total) return MV_ERR_CAPACITY;
@@ -455,6 +486,8 @@ extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16
   s->kv = kv;
   s->s_max = s_max;
   s->topk = topk;
+  s->batch = batch;
+  s->kv_seq_elems = (size_t)d.n_layers * 2 * d.n_heads * s_max * d.head_dim;
   char* b = static_cast<char*>(ws);
   s->cur_len = reinterpret_cast<int32_t*>(b + L.state);
   s->root_counter = reinterpret_cast<uint64_t*>(b + L.state + 16);
@@ -479,7 +512,7 @@ extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16
   bool ok = gemm_act_map(&s->m_xb, s->xb, kTok, d.d) && gemm_act_map(&s->m_attn, s->attn, kTok, HD) &&
             gemm_act_map(&s->m_act, s->act, kTok, d.ffn);
   CUtensorMap vdummy;
-  ok = ok && tree_attn_make_maps(&s->m_kv, &vdummy, kv, kv, d.n_heads, d.head_dim, s_max, 2 * d.n_layers,
+  ok = ok && tree_attn_make_maps(&s->m_kv, &vdummy, kv, kv, d.n_heads, d.head_dim, s_max, 2 * d.n_layers * batch,
                                  (size_t)d.n_heads * s_max * d.head_dim * 2);
   // 64-node chain (causal) tree for prefill chunks
   s->chain = nullptr;
@@ -516,6 +549,11 @@ extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16
   return MV_OK;
 }
 
+extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16* kv, int32_t s_max, int32_t topk,
+                                       void* ws, size_t ws_bytes, mv_session** out) {
+  return mv_batch_session_create(m, tree, 1, kv, s_max, topk, ws, ws_bytes, out);
+}
+
 extern "C" void mv_session_destroy(mv_session* s) {
   if (!s) return;
   if (s->graph_exec) cudaGraphExecDestroy(s->graph_exec);
@@ -540,38 +578,46 @@ extern "C" mv_status mv_session_state(const mv_session* s, mv_session_state_ptrs
   out->ld_logits = s->ld_logits;
   out->hidden = s->x;
   out->root_counter = s->root_counter;
+  out->batch = s->batch;
   return MV_OK;
 }
 
-extern "C" mv_status mv_prefill(mv_session* s, const int32_t* d_tokens, int32_t n, mv_stream stream) {
-  if (!s || !d_tokens || n < 1) return MV_ERR_INVALID_ARG;
+extern "C" mv_status mv_prefill_seq(mv_session* s, int32_t b, const int32_t* d_tokens, int32_t n,
+                                     mv_stream stream) {
+  if (!s || !d_tokens || n < 1 || b < 0 || b >= s->batch) return MV_ERR_INVALID_ARG;
   if (n + kChunk > s->s_max) return MV_ERR_CAPACITY;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  mv_status rc = mv_launch(set_int_kernel, dim3(1), dim3(1), 0, st, s->cur_len, 0) == cudaSuccess
+  mv_status rc = mv_launch(set_int_kernel, dim3(1), dim3(1), 0, st, s->cur_len + b, 0) == cudaSuccess
                      ? mv_last_launch("prefill")
                      : MV_ERR_CUDA;
   for (int o = 0; o < n && rc == MV_OK; o += kChunk) {
     const int c = std::min(kChunk, n - o);
     const bool last = o + c == n;
-    rc = forward(s, s->chain, d_tokens + o, c, last, st);
+    rc = forward(s, s->chain, d_tokens + o, c, last, st, 1, b);
     if (rc != MV_OK) break;
     rc = mv_launch(prefill_finish_kernel, dim3(1), dim3(1024), 0, st, s->logits, s->model->dims.vocab,
-                   s->ld_logits, c, last ? 1 : 0, s->cur_len, s->result) == cudaSuccess
+                   s->ld_logits, c, last ? 1 : 0, s->cur_len + b, s->result + b) == cudaSuccess
              ? mv_last_launch("prefill_finish")
              : MV_ERR_CUDA;
     if (rc == MV_OK && last && s->root.mode != MV_ROOT_ARGMAX)  // the root drawn from the prompt's last row
-      rc = launch_sample_root(s->logits, s->model->dims.vocab, s->ld_logits, c, s->result, nullptr, s->root, 0,
-                              s->root_counter, st);
+      rc = launch_sample_root(s->logits, s->model->dims.vocab, s->ld_logits, c, s->result + b, nullptr, s->root, 0,
+                              s->root_counter + b, st);
   }
-  if (rc == MV_OK) rc = run_heads(s, st);
+  if (rc == MV_OK) rc = run_heads(s, b, 0, st);
   return rc;
+}
+
+extern "C" mv_status mv_prefill(mv_session* s, const int32_t* d_tokens, int32_t n, mv_stream stream) {
+  if (!s) return MV_ERR_INVALID_ARG;
+  if (s->batch != 1) return MV_ERR_UNSUPPORTED;  // a batched session prefills each sequence (mv_prefill_seq)
+  return mv_prefill_seq(s, 0, d_tokens, n, stream);
 }
 
 extern "C" mv_status mv_session_set_root_sampling(mv_session* s, mv_root_params params, uint64_t counter,
                                                   mv_stream stream) {
   if (!s || !mv_root_params_valid(params)) return MV_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (mv_launch(set_u64_kernel, dim3(1), dim3(1), 0, st, s->root_counter, counter) != cudaSuccess)
+  if (mv_launch(set_counters_kernel, dim3(1), dim3(1), 0, st, s->root_counter, counter, s->batch) != cudaSuccess)
     return MV_ERR_CUDA;
   const mv_status rc = mv_last_launch("mv_session_set_root_sampling");
   if (rc != MV_OK) return rc;
@@ -587,35 +633,46 @@ extern "C" mv_status medusa_verify_step(mv_session* s, mv_accept_params prm, mv_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const mv_tree* t = s->tree;
   const mv_model_dims& d = s->model->dims;
+  const int B = s->batch;
+  const int K = d.n_medusa;
+  const int cart_ld = kSeqRows * (MV_MAX_DEPTH + 1);
+  // sequence b's tree tokens, logits and hidden rows start at row 64 b (a batch of one uses rows 0 .. n - 1)
+  auto row0 = [&](int b) { return b * kSeqRows; };
   // candidates from the previous step's root (result.next_root) and head top-k
-  mv_status rc;
-  {
+  mv_status rc = MV_OK;
+  for (int b = 0; b < B && rc == MV_OK; ++b) {
     ProfScope ps(s, st, MV_PROF_OTHER);
-    rc = launch_build_candidates(&s->result->next_root, s->head_topk, s->topk, t, s->tree_tokens, s->cart, st);
+    rc = launch_build_candidates(&s->result[b].next_root, s->head_topk + (size_t)b * K * s->topk, s->topk, t,
+                                 s->tree_tokens + row0(b), s->cart + (size_t)b * cart_ld, st);
   }
-  if (rc == MV_OK) rc = forward(s, t, s->tree_tokens, t->n_nodes, true, st);
-  if (rc == MV_OK) {
-    ProfScope ps(s, st, MV_PROF_POSTERIOR);
-    rc = launch_posterior(s->logits, d.vocab, s->ld_logits, s->tree_tokens, t, prm, s->result, nullptr, nullptr,
-                          s->ws_post, st, s->row_max, (d.vocab + 127) / 128, kTok);
+  // one backbone pass over every sequence's tree: each weight byte is read once for all of them
+  if (rc == MV_OK) rc = forward(s, t, s->tree_tokens, t->n_nodes, true, st, B, 0);
+  for (int b = 0; b < B && rc == MV_OK; ++b) {
+    const float* lg = s->logits + (size_t)row0(b) * s->ld_logits;
+    {
+      ProfScope ps(s, st, MV_PROF_POSTERIOR);
+      rc = launch_posterior(lg, d.vocab, s->ld_logits, s->tree_tokens + row0(b), t, prm, s->result + b, nullptr,
+                            nullptr, s->ws_post, st, s->row_max + row0(b), (d.vocab + 127) / 128, kTok);
+    }
+    if (rc == MV_OK && s->root.mode != MV_ROOT_ARGMAX) {  // the next root drawn from node retrieve[best][acc]
+      ProfScope ps(s, st, MV_PROF_OTHER);
+      rc = launch_sample_root(lg, d.vocab, s->ld_logits, t->n_nodes, s->result + b, nullptr, s->root, 0,
+                              s->root_counter + b, st);
+    }
+    if (rc == MV_OK) {
+      ProfScope ps(s, st, MV_PROF_KV_COMPACT);
+      rc = launch_kv_compact(s->kv + (size_t)b * s->kv_seq_elems, d.n_layers, d.n_heads, s->s_max, d.head_dim,
+                             s->cur_len + b, 0, s->result + b, nullptr, st);
+    }
+    if (rc == MV_OK) rc = run_heads(s, b, row0(b), st);
   }
-  if (rc == MV_OK && s->root.mode != MV_ROOT_ARGMAX) {  // the next root drawn from node retrieve[best][acc]
-    ProfScope ps(s, st, MV_PROF_OTHER);
-    rc = launch_sample_root(s->logits, d.vocab, s->ld_logits, t->n_nodes, s->result, nullptr, s->root, 0,
-                            s->root_counter, st);
-  }
-  if (rc == MV_OK) {
-    ProfScope ps(s, st, MV_PROF_KV_COMPACT);
-    rc = launch_kv_compact(s->kv, d.n_layers, d.n_heads, s->s_max, d.head_dim, s->cur_len, 0, s->result, nullptr,
-                           st);
-  }
-  if (rc == MV_OK) rc = run_heads(s, st);
   return rc;
 }
 
 extern "C" mv_status medusa_verify_step_host(mv_session* s, mv_accept_params prm, const int32_t* h_seeds_in,
                                              int32_t* h_result, int32_t* h_seeds_out, mv_stream stream) {
   if (!s || !h_result) return MV_ERR_INVALID_ARG;
+  if (s->batch != 1) return MV_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int k = s->model->dims.n_medusa * s->topk;
   if (h_seeds_in) {
