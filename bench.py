@@ -553,12 +553,22 @@ def run_sweep_batch(batches, steps, warmup, tree_name):
             torch.cuda.synchronize()
             clk.stop()
         ms = a.elapsed_time(b_) / steps
+        # per-kind device time per step from a replay with an event pair around every launch
+        prof = mv.Profiler(sess)
+        prof.enable()
+        sess.steps_graph(steps, prm)
+        torch.cuda.synchronize()
+        prof.read()
+        sess.steps_graph(steps, prm)
+        torch.cuda.synchronize()
+        per_kind = {k: round(1e3 * v[0] / steps, 1) for k, v in prof.read().items() if v[1]}
+        prof.disable()
         st, code = mv.get_error()
         if st != 0:
             raise RuntimeError(f"device error word {code:#x}")
         print(json.dumps({"sweep": "batch", "batch": B, "n_nodes": tree.n_nodes, "steps": steps, "ms_per_step": ms,
                           "steps_per_s": 1e3 / ms, "sequence_steps_per_s": B * 1e3 / ms,
-                          "clocks": clk.summary()}), flush=True)
+                          "profiled_us_per_step_by_kind": per_kind, "clocks": clk.summary()}), flush=True)
         del sess
 
 

@@ -45,13 +45,15 @@ constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kAcc = 2;  // accumulator buffers in tensor memory (the MMA may run kAcc - 1 tiles ahead)
 constexpr int kMaxCluster = 8;  // CTAs per cluster (portable limit)
 
-// Per number of token groups NT (1, 2 or 4): a stage holds one weight block and NT activation blocks, so
-// fewer stages fit; one MMA of N = 64 NT per 16 k; the accumulator buffers take 2 x 64 NT TMEM columns.
+// Per number of token groups NT (1 to 4): a stage holds one weight block and NT activation blocks, so fewer
+// stages fit; one MMA of N = 64 NT per 16 k; the accumulator buffers take 2 x 64 NT TMEM columns (allocated as
+// a power of two).
 template <int NT>
 struct Cfg {
-  static constexpr int kStages = NT == 1 ? 6 : NT == 2 ? 5 : 3;
+  static constexpr int kStages = NT == 1 ? 6 : NT == 2 ? 5 : NT == 3 ? 4 : 3;
   static constexpr int kStageBytes = kABytes + NT * kBBytes;
   static constexpr int kTmemCols = kAcc * BN * NT;
+  static constexpr int kTmemAlloc = kTmemCols <= 128 ? 128 : kTmemCols <= 256 ? 256 : 512;
   static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)BM * BN * 4 + 256;
   // kind::f16 instruction descriptor: D fp32, A/B bf16, both K-major, N = 64 NT, M = 128.
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)((BN * NT) >> 3) << 17) |
@@ -152,7 +154,7 @@ MV_DEV void load_epi_const(const GemmParams& p, EpiConst* ec, int i, int ngroups
     }
     ec->part[half][j] = t;
     if (half == 0 && p.pos_ids) {
-      const int b = p.seq_rows ? j / p.seq_rows : 0, r = j - b * p.seq_rows;
+      const int b = p.seq_rows ? j / BN : 0, r = p.seq_rows ? j % BN : j;  // sequences: one group each
       ec->pos[j] = (j < p.n_tok && (!p.seq_rows || r < p.seq_n)) ? p.cur_len[b] + p.pos_ids[r] : 0;
     }
   }
@@ -332,7 +334,7 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int jb, int w, int l, 
       const int j = jb + w + 4 * t;
       if (j >= ntok) continue;  // uniform over the warp
       const float4 pr = shfl_xor4(acc[u], p.D >> 3);  // the RoPE partner rows (dim -+ D/2, same head)
-      const int b = p.seq_rows ? j / p.seq_rows : 0, r = j - b * p.seq_rows;
+      const int b = p.seq_rows ? j / BN : 0, r = p.seq_rows ? j % BN : j;  // sequences: one group each
       if (!valid || (p.seq_rows && r >= p.seq_n)) continue;  // past the weights, or a padding row
       uint16_t* dst;
       if (which == 0) {
@@ -386,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                                                            const __grid_constant__ ChainArgs ca) {
   constexpr int kStages = Cfg<NT>::kStages;
   constexpr int kStageBytes = Cfg<NT>::kStageBytes;
-  constexpr int kTmemCols = Cfg<NT>::kTmemCols;
+  constexpr int kTmemAlloc = Cfg<NT>::kTmemAlloc;
   constexpr uint32_t kIdesc = Cfg<NT>::kIdesc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -425,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     mbar_fence_init();
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_alloc(&tmem_base_sh, kTmemAlloc);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -718,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   cluster_sync_all();  // no CTA leaves while another CTA of its cluster may still read its shared memory
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc(tmem_base, kTmemAlloc);
   }
   // the last CTA out leaves the chain's counters at zero for the next launch
   if (threadIdx.x == 0 && ca.flags && ca.n_phases > 1 && !ca.indep) {
@@ -733,20 +735,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 }  // namespace
 
 
-// Token groups of a launch over n_tok tokens: 1, 2 or 4 (0 when n_tok > 256).
-int token_groups(int n_tok) { return n_tok <= BN ? 1 : n_tok <= 2 * BN ? 2 : n_tok <= kTokMax ? 4 : 0; }
+// Token groups of a launch over n_tok tokens: 1 to 4 (0 when n_tok > 256).
+int token_groups(int n_tok) { return n_tok < 1 || n_tok > kTokMax ? 0 : (n_tok + BN - 1) / BN; }
 
 size_t smem_bytes_for(int nt) {
-  return nt == 1 ? Cfg<1>::kSmemBytes : nt == 2 ? Cfg<2>::kSmemBytes : Cfg<4>::kSmemBytes;
+  return nt == 1 ? Cfg<1>::kSmemBytes : nt == 2 ? Cfg<2>::kSmemBytes : nt == 3 ? Cfg<3>::kSmemBytes
+                                                                               : Cfg<4>::kSmemBytes;
 }
 const void* kernel_for(int nt) {
-  return nt == 1 ? (const void*)gemm_kernel<1> : nt == 2 ? (const void*)gemm_kernel<2> : (const void*)gemm_kernel<4>;
+  return nt == 1 ? (const void*)gemm_kernel<1> : nt == 2 ? (const void*)gemm_kernel<2>
+                 : nt == 3 ? (const void*)gemm_kernel<3> : (const void*)gemm_kernel<4>;
 }
 // Raises the dynamic shared memory limit of the instantiation for nt token groups once per device.
 bool set_smem_for(int nt) {
-  static int flags[3][64] = {};
-  const int k = nt == 1 ? 0 : nt == 2 ? 1 : 2;
-  return mv_set_smem_once(kernel_for(nt), (int)smem_bytes_for(nt), flags[k]);
+  static int flags[4][64] = {};
+  return mv_set_smem_once(kernel_for(nt), (int)smem_bytes_for(nt), flags[nt - 1]);
 }
 
 bool gemm_weight_map(CUtensorMap* map, const void* w, int rows, int K, int box_rows) {
@@ -785,9 +788,9 @@ bool gemm_act_map(CUtensorMap* map, const void* x, int rows, int K) {
 // Clusters of c CTAs (one CTA per SM) that can be resident at once on this device, c = 1..kMaxCluster; 0 when
 // the size cannot be launched. Asked once per device and size.
 int gemm_max_clusters(int c, int nt) {
-  static int cache[64][3][kMaxCluster + 1];  // 0 = not asked yet, -1 = not launchable
+  static int cache[64][4][kMaxCluster + 1];  // 0 = not asked yet, -1 = not launchable
   const int dev = mv_device();
-  const int k = nt == 1 ? 0 : nt == 2 ? 1 : 2;
+  const int k = nt - 1;
   if (dev < 0 || dev >= 64 || c < 1 || c > kMaxCluster) return 0;
   int& slot = cache[dev][k][c];
   if (slot == 0) {
@@ -809,6 +812,8 @@ int gemm_max_clusters(int c, int nt) {
         e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<1>, &cfg);
       else if (nt == 2)
         e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<2>, &cfg);
+      else if (nt == 3)
+        e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<3>, &cfg);
       else
         e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<4>, &cfg);
       if (e != cudaSuccess) {
@@ -871,6 +876,7 @@ mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStrea
     ps[i] = ph[i].p;
     shape_params(ps[i]);
     if (ps[i].n_tiles > kGemmMaxTiles || ps[i].n_tok < 1 || ps[i].n_tok > kTokMax) return MV_ERR_SHAPE;
+    if (ps[i].seq_rows && (ps[i].seq_rows != BN || ps[i].seq_n < 1 || ps[i].seq_n > BN)) return MV_ERR_SHAPE;
     if (ph[i].epi < EPI_STORE || ph[i].epi > EPI_QKV) return MV_ERR_INVALID_ARG;
     max_tok = std::max(max_tok, ps[i].n_tok);
   }
@@ -916,6 +922,8 @@ mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStrea
     e = cudaLaunchKernelEx(&cfg, gemm_kernel<1>, maps, ca);
   else if (nt == 2)
     e = cudaLaunchKernelEx(&cfg, gemm_kernel<2>, maps, ca);
+  else if (nt == 3)
+    e = cudaLaunchKernelEx(&cfg, gemm_kernel<3>, maps, ca);
   else
     e = cudaLaunchKernelEx(&cfg, gemm_kernel<4>, maps, ca);
   if (e != cudaSuccess) return MV_ERR_CUDA;

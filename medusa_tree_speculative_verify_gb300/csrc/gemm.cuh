@@ -38,7 +38,7 @@ struct GemmParams {
   const int32_t* pos_ids;  // [n] depth of each token (of each tree row when seq_rows > 0)
   // Several sequences in one pass (QKV): token j is row j % seq_rows of sequence j / seq_rows's tree; rows at or
   // past seq_n are padding (nothing is appended). The sequences' caches are kv_seq_stride elements apart.
-  // seq_rows = 0: one sequence.
+  // seq_rows is 0 (one sequence) or 64 (one token group per sequence).
   int seq_rows, seq_n;
   size_t kv_seq_stride;
   float log2_theta;

@@ -348,16 +348,22 @@ namespace {
 constexpr int kHiLo = 16;  // lo rows start here (B <= 16)
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// pair: h (and so t) holds a hi row j and a lo row kHiLo + j per input row, summed here.
 __global__ void __launch_bounds__(256) heads_prep_kernel(const float* t, const uint16_t* h, int B, int Kd, int d,
-                                                         uint16_t* u) {
+                                                         uint16_t* u, int pair) {
   pdl_wait();
   for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < (size_t)kHiLo * Kd;
        e += (size_t)gridDim.x * blockDim.x) {
     const int j = (int)(e / Kd), R = (int)(e % Kd);
     uint16_t hi = 0, lo = 0;
     if (j < B) {
-      const float uf = silu(__ldcg(t + (size_t)j * Kd + R)) +
-                       __bfloat162float(__ushort_as_bfloat16(h[(size_t)j * d + R % d]));
+      float tv = __ldcg(t + (size_t)j * Kd + R);
+      float hv = __bfloat162float(__ushort_as_bfloat16(h[(size_t)j * d + R % d]));
+      if (pair) {
+        tv += __ldcg(t + (size_t)(kHiLo + j) * Kd + R);
+        hv += __bfloat162float(__ushort_as_bfloat16(h[(size_t)(kHiLo + j) * d + R % d]));
+      }
+      const float uf = silu(tv) + hv;
       const __nv_bfloat16 bh = __float2bfloat16_rn(uf);
       hi = __bfloat16_as_ushort(bh);
       lo = __bfloat16_as_ushort(__float2bfloat16_rn(uf - __bfloat162float(bh)));
@@ -440,7 +446,7 @@ __global__ void __launch_bounds__(kTopThreads) heads_topk_kernel(const float* zl
 size_t heads_gemm_ws_bytes(int B, int d, int K, int V, bool lm) {
   const size_t Kd = (size_t)K * d;
   size_t bytes = 0;
-  bytes += align256((size_t)B * Kd * 4);            // t
+  bytes += align256((size_t)2 * kHiLo * Kd * 4);    // t (hi and lo rows when h is a pair)
   bytes += align256((size_t)2 * kHiLo * Kd * 2);    // u (hi rows, lo rows)
   bytes += align256((size_t)2 * kHiLo * K * V * 4); // z (hi and lo products)
   if (lm) bytes += align256((size_t)B * V * 4);     // LM row
@@ -449,11 +455,12 @@ size_t heads_gemm_ws_bytes(int B, int d, int K, int V, bool lm) {
 
 mv_status launch_heads_gemm(const uint16_t* h, int B, int d, int K, const uint16_t* w1, const uint16_t* w2, int V,
                             int topk, const uint16_t* w_lm, int32_t* out_idx, float* out_val, int32_t* out_root,
-                            void* ws, cudaStream_t stream) {
+                            void* ws, cudaStream_t stream, bool pair = false) {
   const int Kd = K * d;
+  const int hrows = pair ? 2 * kHiLo : B;  // rows of h (and of t): hi rows, then lo rows from kHiLo
   char* p = static_cast<char*>(ws);
   float* t = reinterpret_cast<float*>(p);
-  p += align256((size_t)B * Kd * 4);
+  p += align256((size_t)2 * kHiLo * Kd * 4);
   uint16_t* u = reinterpret_cast<uint16_t*>(p);
   p += align256((size_t)2 * kHiLo * Kd * 2);
   float* zl = reinterpret_cast<float*>(p);
@@ -471,9 +478,9 @@ mv_status launch_heads_gemm(const uint16_t* h, int B, int d, int K, const uint16
   {
     GemmPhase& g = ph[np++];
     g.epi = EPI_STORE;
-    if (!gemm_weight_map(&g.a0, w1, Kd, d, 128) || !gemm_act_map(&g.b, h, B, d)) return MV_ERR_CUDA;
+    if (!gemm_weight_map(&g.a0, w1, Kd, d, 128) || !gemm_act_map(&g.b, h, hrows, d)) return MV_ERR_CUDA;
     g.a1 = g.a0;
-    g.p = base(B);
+    g.p = base(hrows);
     g.p.M = Kd;
     g.p.K = d;
     g.p.out_f32 = t;
@@ -494,7 +501,8 @@ mv_status launch_heads_gemm(const uint16_t* h, int B, int d, int K, const uint16
   if (s != MV_OK) return s;
   // u = SiLU(t) + h as a bf16 (hi, lo) pair
   const int blocks = (int)std::min<size_t>(((size_t)kHiLo * Kd + 255) / 256, (size_t)mv_sm_count() * 8);
-  if (mv_launch(heads_prep_kernel, dim3(blocks), dim3(256), 0, stream, t, h, B, Kd, d, u) != cudaSuccess)
+  if (mv_launch(heads_prep_kernel, dim3(blocks), dim3(256), 0, stream, t, h, B, Kd, d, u, pair ? 1 : 0) !=
+      cudaSuccess)
     return MV_ERR_CUDA;
   if ((s = mv_last_launch("heads_prep")) != MV_OK) return s;
   // z_k = W2_k u for the 32 rows (hi and lo), up to kGemmMaxPhases heads per launch
@@ -533,6 +541,12 @@ mv_status launch_heads_gemm(const uint16_t* h, int B, int d, int K, const uint16
 }
 
 }  // namespace
+
+mv_status launch_heads_rows_pair(const uint16_t* h_pair, int B, int d, int K, const uint16_t* w1, const uint16_t* w2,
+                                 int V, int topk, int32_t* out_idx, void* ws, cudaStream_t stream) {
+  if (B < 1 || B > kHiLo) return MV_ERR_SHAPE;
+  return launch_heads_gemm(h_pair, B, d, K, w1, w2, V, topk, nullptr, out_idx, nullptr, nullptr, ws, stream, true);
+}
 
 int heads_w2_ctas_per_mat(int n_mat, int V) {
   const int sms = mv_sm_count();

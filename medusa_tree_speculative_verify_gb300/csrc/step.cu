@@ -121,6 +121,39 @@ __global__ void set_int_kernel(int32_t* p, int v) {
   *p = v;
 }
 
+// The Medusa heads' inputs of a batch: for sequence b (one CTA each), h = RMSNorm(x[64 b + result[b].next_node])
+// as a bf16 (hi, lo) pair in rows b and 16 + b of h_pair; then cur_len[b] += result[b].n_tokens.
+__global__ void __launch_bounds__(256) heads_gather_kernel(const float* x, int d, float eps,
+                                                           const mv_posterior_result* res, int32_t* cur_len,
+                                                           uint16_t* h_pair, unsigned int* err) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x, tid = threadIdx.x;
+  __shared__ float red[8];
+  const int node = res[b].next_node;
+  if (node < 0 || node >= kSeqRows) {
+    if (tid == 0) mv_set_error_detail(err, 15, MV_DEVERR_INDEX, (uint32_t)node);
+    return;
+  }
+  const float* xr = x + (size_t)(b * kSeqRows + node) * d;
+  float ss = 0.0f;
+  for (int c = tid; c < d; c += 256) ss += xr[c] * xr[c];
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  float tot = 0.0f;
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float inv = rsqrtf(tot / d + eps);
+  for (int c = tid; c < d; c += 256) {
+    const float v = xr[c] * inv;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    h_pair[(size_t)b * d + c] = __bfloat16_as_ushort(hi);
+    h_pair[(size_t)(16 + b) * d + c] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
+  }
+  if (tid == 0) cur_len[b] += res[b].n_tokens;
+}
+
 // p[b] = v + b * 2^32 for the n sequences of a session (each draws from its own range of counters)
 __global__ void set_counters_kernel(uint64_t* p, uint64_t v, int n) {
   pdl_trigger();
@@ -171,6 +204,7 @@ struct mv_session {
   void* ws_heads;
   unsigned int* chain_flags;  // phase counters of the projection chains (zero between launches)
   float2* row_max;            // [vocab/128][64]: per LM-head tile and token, max and first argmax
+  uint16_t* h_pair;           // [32][d] bf16: the heads' inputs of a batch as (hi, lo) rows
   uint64_t* root_counter;     // per sequence: generator counter of the next sampled root
   mv_root_params root{};      // root rule (MV_ROOT_ARGMAX: the posterior's argmax stands)
   int root_epoch = 0;         // bumped by every mv_session_set_root_sampling
@@ -223,7 +257,8 @@ struct ProfScope {
 namespace {
 
 struct SessionLayout {
-  size_t state, tree_tokens, cart, x, xb, ssq, q, attn, act, logits, attn_ws, post, heads, chain, row_max, total;
+  size_t state, tree_tokens, cart, x, xb, ssq, q, attn, act, logits, attn_ws, post, heads, chain, row_max, h_pair,
+      total;
 };
 
 SessionLayout session_layout(const mv_model_dims& d, int s_max, int topk) {
@@ -250,9 +285,10 @@ SessionLayout session_layout(const mv_model_dims& d, int s_max, int topk) {
   L.logits = take((size_t)kTok * ldl * 4);
   L.attn_ws = take(tree_attn_ws_bytes(d.n_heads, d.head_dim, s_max, kTok));
   L.post = take(posterior_ws_bytes(kTok));
-  L.heads = take(heads_ws_bytes(1, d.d, d.n_medusa, d.vocab, topk));
+  L.heads = take(heads_ws_bytes(MV_MAX_BATCH, d.d, d.n_medusa, d.vocab, topk));  // B = 1 GEMV or the batched path
   L.chain = take(kGemmChainFlagWords * sizeof(unsigned int));  // zero at creation; each chain launch leaves it so
   L.row_max = take((size_t)((d.vocab + 127) / 128) * kTok * sizeof(float2));  // LM-head tile max / argmax
+  L.h_pair = take((size_t)32 * d.d * 2);
   L.total = o;
   return L;
 }
@@ -508,6 +544,7 @@ extern "C" mv_status mv_batch_session_create(mv_model* m, const mv_tree* tree, i
   s->ws_heads = b + L.heads;
   s->chain_flags = reinterpret_cast<unsigned int*>(b + L.chain);
   s->row_max = reinterpret_cast<float2*>(b + L.row_max);
+  s->h_pair = reinterpret_cast<uint16_t*>(b + L.h_pair);
   const int HD = d.n_heads * d.head_dim;
   bool ok = gemm_act_map(&s->m_xb, s->xb, kTok, d.d) && gemm_act_map(&s->m_attn, s->attn, kTok, HD) &&
             gemm_act_map(&s->m_act, s->act, kTok, d.ffn);
@@ -664,9 +701,18 @@ extern "C" mv_status medusa_verify_step(mv_session* s, mv_accept_params prm, mv_
       rc = launch_kv_compact(s->kv + (size_t)b * s->kv_seq_elems, d.n_layers, d.n_heads, s->s_max, d.head_dim,
                              s->cur_len + b, 0, s->result + b, nullptr, st);
     }
-    if (rc == MV_OK) rc = run_heads(s, b, row0(b), st);
   }
-  return rc;
+  if (rc != MV_OK) return rc;
+  if (B == 1) return run_heads(s, 0, 0, st);
+  // several sequences: their heads' inputs gathered as (hi, lo) rows, then one tensor-core pass over the heads'
+  // weights for all of them
+  ProfScope ps(s, st, MV_PROF_HEADS);
+  if (mv_launch(heads_gather_kernel, dim3(B), dim3(256), 0, st, (const float*)s->x, d.d, d.norm_eps,
+                (const mv_posterior_result*)s->result, s->cur_len, s->h_pair, mv_error_word()) != cudaSuccess)
+    return MV_ERR_CUDA;
+  if ((rc = mv_last_launch("heads_gather")) != MV_OK) return rc;
+  const mv_model* m = s->model;
+  return launch_heads_rows_pair(s->h_pair, B, d.d, K, m->w1, m->w2, d.vocab, s->topk, s->head_topk, s->ws_heads, st);
 }
 
 extern "C" mv_status medusa_verify_step_host(mv_session* s, mv_accept_params prm, const int32_t* h_seeds_in,
