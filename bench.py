@@ -233,8 +233,6 @@ def run_gpu(args, world, rank, local):
     snap_ws, snap_kv = sess.ws.clone(), sess.kv.clone()
 
     # ---- timed: K steps (one graph replay), inputs resident in HBM
-    # candidates, embed, first QKV, per layer attention + projection chain, posterior, KV compaction, heads x 2
-    launches_per_step = 1 + 1 + 1 + dims.n_layers * 2 + 1 + 1 + 2
     barrier(world)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -259,11 +257,17 @@ def run_gpu(args, world, rank, local):
     torch.cuda.synchronize()
     prof.read()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    len_before = int(sess.cur_len.item())
     a.record(stream)
     sess.steps_graph(args.steps, prm)
     b.record(stream)
     torch.cuda.synchronize()
     per_kind = prof.read()
+    mean_prefix = 0.5 * (len_before + int(sess.cur_len.item()))
+    # candidates, embed, first QKV, per layer one projection chain (with the layer's attention inside it, or a
+    # separate attention launch before it), posterior, KV compaction, heads x 2
+    attn_launches = round(per_kind["attention"][1] / args.steps)
+    launches_per_step = 1 + 1 + 1 + dims.n_layers + attn_launches + 1 + 1 + 2
     prof.disable()
     profiled_ms = a.elapsed_time(b)
 
@@ -312,12 +316,14 @@ def run_gpu(args, world, rank, local):
     tokens_per_step = tok_e2e / args.steps
     peak, peak_kind = peaks()
     gb = gemm_bytes(dims, TREE["n_nodes"])
+    if attn_launches == 0:  # each layer's attention runs inside its chain: its bytes are the chain's too
+        gb["gemm_chain"] += attention_bytes(dims, TREE["n_nodes"], mean_prefix)
     g_ms = sum(per_kind[k][0] for k in gb)
     g_n = sum(per_kind[k][1] for k in gb)
     g_bytes = sum(gb[k] * per_kind[k][1] for k in gb)
     achieved = g_bytes / (g_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "gemm_kernel (tcgen05 projections; per layer one launch of O, gate/up, "
-                                          "down and the next QKV, plus the first QKV)",
+    roofline = {"bound": "hbm", "kernel": "gemm_kernel (tcgen05 projections; per layer one launch of the layer's "
+                                          "tree attention, O, gate/up, down and the next QKV, plus the first QKV)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": GEMM_TRAFFIC_PER_ALGORITHMIC_BYTE * g_bytes / max(g_n, 1),
                 "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the LM-head launch "
@@ -371,6 +377,12 @@ def gemm_bytes(dims, n):
     layer = b["gemm_o"] + b["gemm_gate_up"] + b["gemm_down"]
     b["gemm_chain"] = layer + ((L - 1) * b["gemm_qkv"] + b["gemm_lm"]) / L
     return b
+
+
+def attention_bytes(dims, n, prefix):
+    """Algorithmic bytes of one layer's tree attention: the prefix and tree keys and values once, q in, out."""
+    HD = dims.n_heads * dims.head_dim
+    return (prefix + n) * HD * 2 * 2 + 2 * n * HD * 2
 
 
 MICRO = {  # name -> (M, K, n): projections of the 7B step, timed alone through mv_linear_bf16

@@ -48,13 +48,17 @@ constexpr int kMaxCluster = 8;  // CTAs per cluster (portable limit)
 // Per number of token groups NT (1 to 4): a stage holds one weight block and NT activation blocks, so fewer
 // stages fit; one MMA of N = 64 NT per 16 k; the accumulator buffers take 2 x 64 NT TMEM columns (allocated as
 // a power of two).
-template <int NT>
+template <int NT, bool kAttn = false>
 struct Cfg {
   static constexpr int kStages = NT == 1 ? 6 : NT == 2 ? 5 : NT == 3 ? 4 : 3;
+  // after the stages: the cluster partial buffer, which a fused attention head uses first (kAttn)
+  static constexpr size_t kPartBytes = (size_t)BM * BN * 4;
+  static constexpr size_t kRegionBytes =
+      kAttn && attn::smem_bytes<128>() > kPartBytes ? attn::smem_bytes<128>() : kPartBytes;
   static constexpr int kStageBytes = kABytes + NT * kBBytes;
   static constexpr int kTmemCols = kAcc * BN * NT;
   static constexpr int kTmemAlloc = kTmemCols <= 128 ? 128 : kTmemCols <= 256 ? 256 : 512;
-  static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + (size_t)BM * BN * 4 + 256;
+  static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kRegionBytes + 256;
   // kind::f16 instruction descriptor: D fp32, A/B bf16, both K-major, N = 64 NT, M = 128.
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)((BN * NT) >> 3) << 17) |
                                      ((uint32_t)(BM >> 4) << 24);
@@ -362,13 +366,32 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int jb, int w, int l, 
 
 struct ChainMaps {
   CUtensorMap a0[kGemmMaxPhases], a1[kGemmMaxPhases], b[kGemmMaxPhases];
+  CUtensorMap kmap, vmap;  // fused attention: the KV cache planes
 };
 struct ChainArgs {
   GemmParams ph[kGemmMaxPhases];
   int epi[kGemmMaxPhases];
   int n_phases, csize;
   int indep;            // 1: the phases do not read each other's outputs (no counters, no waits)
-  unsigned int* flags;  // [kGemmChainFlagWords]: phase-done counters, then the exit counter
+  unsigned int* flags;  // [kGemmChainFlagWords]: phase-done counters, the exit counter, the attention counter
+  attn::Args attn;      // fused attention (attn_D > 0) of the layer, before phase 0
+  int attn_D;
+};
+
+// Cluster-wide steps of a fused attention head: only the epilogue warps of the C CTAs take part (the producer
+// and MMA warps are busy streaming), so they meet on an mbarrier per step with one remote arrive per CTA.
+struct EpiClusterSync {
+  uint64_t* rbar;
+  uint64_t* dbar;
+  int C, i;
+  unsigned int* err;
+  MV_DEV void step(uint64_t* bar) {
+    attn::grp_bar();  // this CTA's attention threads are done with their shared-memory writes / reads
+    if (i < C) mbar_arrive_remote(map_rank(smem_u32(bar), (uint32_t)i));
+    if (!mbar_wait_cluster(bar, 0u) && i == 0) mv_set_error(err, 16, MV_DEVERR_TIMEOUT);
+  }
+  MV_DEV void ready() { step(rbar); }
+  MV_DEV void done() { step(dbar); }
 };
 
 // Bounded wait until *p >= target (acquire at GPU scope); false when it expires.
@@ -383,7 +406,7 @@ MV_DEV bool wait_count(const unsigned int* p, unsigned int target) {
   }
 }
 
-template <int NT>
+template <int NT, bool kAttn>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ ChainMaps maps,
                                                            const __grid_constant__ ChainArgs ca) {
   constexpr int kStages = Cfg<NT>::kStages;
@@ -395,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   uint8_t* stages = smem;
   float* part = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);  // [BN tokens][BM rows], a group
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[kAcc], tempty[kAcc], drain, pfull, pfree;
+  __shared__ __align__(8) uint64_t afull[attn::kStages], aready, adone;  // fused attention
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int s_abort;
   __shared__ EpiConst s_ec;
@@ -423,6 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     mbar_init(&pfull, C);  // one arrive from every CTA of the cluster: all partials of the tile written
     mbar_init(&pfree, C);  // one arrive from every CTA of the cluster: all reads of this CTA's partial done
     mbar_init(&drain, 1);
+    for (int s = 0; s < attn::kStages; ++s) mbar_init(&afull[s], 1);
+    mbar_init(&aready, C);  // one arrive from every CTA of the cluster per attention step
+    mbar_init(&adone, C);
     s_abort = 0;
     mbar_fence_init();
   }
@@ -476,6 +503,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             got = wait_count(ca.flags + ph - 1, gridDim.x);
             flag_timeout |= !got;
             asm volatile("fence.proxy.async.global;" ::: "memory");  // generic-proxy writes -> TMA reads
+          } else if (ph == 0 && ca.attn_D) {  // phase 0's activations are the fused attention's output
+            got = wait_count(ca.flags + kGemmAttnFlag, gridDim.x);
+            flag_timeout |= !got;
+            asm volatile("fence.proxy.async.global;" ::: "memory");
           }
           waited = true;
           for (int j = 0; j < pend; ++j) issue_b(pend_s[j], pend_kb[j]);
@@ -575,6 +606,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int sub = warp & 3;       // TMEM sub-partition this warp may read
     const int i = sub * 32 + lane;  // tile row = TMEM lane
     pdl_wait();                     // the epilogue reads what earlier kernels wrote
+    if constexpr (kAttn) {
+      if (ca.attn_D) {  // the layer's attention first: cluster q = head q, CTA rank = key split
+        if (q < ca.attn.H) {
+          EpiClusterSync sy{&aready, &adone, C, i, err};
+          uint8_t* region = reinterpret_cast<uint8_t*>(part);  // the partial buffer is not in use yet
+          if (ca.attn_D == 128)
+            attn::head<128>(ca.attn, &maps.kmap, &maps.vmap, region, afull, rank, q, 0, 0, i, sy);
+          else
+            attn::head<64>(ca.attn, &maps.kmap, &maps.vmap, region, afull, rank, q, 0, 0, i, sy);
+        }
+        epi_bar();  // this CTA's attention outputs are stored
+        if (i == 0) {
+          __threadfence();
+          atomicAdd(ca.flags + kGemmAttnFlag, 1u);
+        }
+      }
+    }
     const uint32_t part_s = smem_u32(part) + (uint32_t)(lane * 16);  // + token row
     bool ok = true;
     int n = 0, m = 0, prev_tile = -1, prev_ph = 0;
@@ -723,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     tmem_dealloc(tmem_base, kTmemAlloc);
   }
   // the last CTA out leaves the chain's counters at zero for the next launch
-  if (threadIdx.x == 0 && ca.flags && ca.n_phases > 1 && !ca.indep) {
+  if (threadIdx.x == 0 && ca.flags && (ca.n_phases > 1 || ca.attn_D) && !ca.indep) {
     __threadfence();
     if (atomicAdd(ca.flags + kGemmMaxPhases, 1u) == gridDim.x - 1) {
       for (int k = 0; k < kGemmChainFlagWords; ++k) ca.flags[k] = 0u;
@@ -738,18 +786,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 // Token groups of a launch over n_tok tokens: 1 to 4 (0 when n_tok > 256).
 int token_groups(int n_tok) { return n_tok < 1 || n_tok > kTokMax ? 0 : (n_tok + BN - 1) / BN; }
 
-size_t smem_bytes_for(int nt) {
-  return nt == 1 ? Cfg<1>::kSmemBytes : nt == 2 ? Cfg<2>::kSmemBytes : nt == 3 ? Cfg<3>::kSmemBytes
-                                                                               : Cfg<4>::kSmemBytes;
+// Kernel variants: v = nt - 1 for nt token groups (0..3), v = 4 for one group with the layer's attention fused.
+constexpr int kVariants = 5;
+int variant_of(int nt, bool attn) { return attn ? 4 : nt - 1; }
+size_t smem_bytes_for(int v) {
+  switch (v) {
+    case 0: return Cfg<1>::kSmemBytes;
+    case 1: return Cfg<2>::kSmemBytes;
+    case 2: return Cfg<3>::kSmemBytes;
+    case 3: return Cfg<4>::kSmemBytes;
+    default: return Cfg<1, true>::kSmemBytes;
+  }
 }
-const void* kernel_for(int nt) {
-  return nt == 1 ? (const void*)gemm_kernel<1> : nt == 2 ? (const void*)gemm_kernel<2>
-                 : nt == 3 ? (const void*)gemm_kernel<3> : (const void*)gemm_kernel<4>;
+const void* kernel_for(int v) {
+  switch (v) {
+    case 0: return (const void*)gemm_kernel<1, false>;
+    case 1: return (const void*)gemm_kernel<2, false>;
+    case 2: return (const void*)gemm_kernel<3, false>;
+    case 3: return (const void*)gemm_kernel<4, false>;
+    default: return (const void*)gemm_kernel<1, true>;
+  }
 }
-// Raises the dynamic shared memory limit of the instantiation for nt token groups once per device.
-bool set_smem_for(int nt) {
-  static int flags[4][64] = {};
-  return mv_set_smem_once(kernel_for(nt), (int)smem_bytes_for(nt), flags[nt - 1]);
+// Raises the dynamic shared memory limit of a variant once per device.
+bool set_smem_for(int v) {
+  static int flags[kVariants][64] = {};
+  return mv_set_smem_once(kernel_for(v), (int)smem_bytes_for(v), flags[v]);
 }
 
 bool gemm_weight_map(CUtensorMap* map, const void* w, int rows, int K, int box_rows) {
@@ -787,19 +848,18 @@ bool gemm_act_map(CUtensorMap* map, const void* x, int rows, int K) {
 
 // Clusters of c CTAs (one CTA per SM) that can be resident at once on this device, c = 1..kMaxCluster; 0 when
 // the size cannot be launched. Asked once per device and size.
-int gemm_max_clusters(int c, int nt) {
-  static int cache[64][4][kMaxCluster + 1];  // 0 = not asked yet, -1 = not launchable
+int gemm_max_clusters(int c, int v) {
+  static int cache[64][kVariants][kMaxCluster + 1];  // 0 = not asked yet, -1 = not launchable
   const int dev = mv_device();
-  const int k = nt - 1;
-  if (dev < 0 || dev >= 64 || c < 1 || c > kMaxCluster) return 0;
-  int& slot = cache[dev][k][c];
+  if (dev < 0 || dev >= 64 || c < 1 || c > kMaxCluster || v < 0 || v >= kVariants) return 0;
+  int& slot = cache[dev][v][c];
   if (slot == 0) {
     int n = 0;
-    if (set_smem_for(nt)) {
+    if (set_smem_for(v)) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(c * mv_sm_count());
       cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = smem_bytes_for(nt);
+      cfg.dynamicSmemBytes = smem_bytes_for(v);
       cudaLaunchAttribute at[1];
       at[0].id = cudaLaunchAttributeClusterDimension;
       at[0].val.clusterDim.x = c;
@@ -807,15 +867,7 @@ int gemm_max_clusters(int c, int nt) {
       at[0].val.clusterDim.z = 1;
       cfg.attrs = at;
       cfg.numAttrs = 1;
-      cudaError_t e;
-      if (nt == 1)
-        e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<1>, &cfg);
-      else if (nt == 2)
-        e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<2>, &cfg);
-      else if (nt == 3)
-        e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<3>, &cfg);
-      else
-        e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<4>, &cfg);
+      const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel_for(v), &cfg);
       if (e != cudaSuccess) {
         cudaGetLastError();
         n = 0;
@@ -834,7 +886,7 @@ void shape_params(GemmParams& p) {
 // One cluster shape for a chain: the cluster size c and count that minimise the summed largest per-CTA share
 // of k-blocks, sum over phases of ceil(tiles / clusters) * ceil(kbt / c), with all clusters resident at once
 // (ties: the smaller cluster). Every CTA is resident, which the counters between phases rely on.
-void plan_chain(GemmParams* p, int n, int nt, int* csize, int* ncl_out) {
+void plan_chain(GemmParams* p, int n, int v, int* csize, int* ncl_out) {
   int max_tiles = 1, min_kbt = 1 << 30;
   for (int i = 0; i < n; ++i) {
     max_tiles = std::max(max_tiles, p[i].n_tiles);
@@ -844,7 +896,7 @@ void plan_chain(GemmParams* p, int n, int nt, int* csize, int* ncl_out) {
   *csize = 1;
   *ncl_out = std::min(max_tiles, mv_sm_count());
   for (int c = 1; c <= kMaxCluster && c <= min_kbt; ++c) {
-    const int mc = gemm_max_clusters(c, nt);
+    const int mc = gemm_max_clusters(c, v);
     if (mc < 1) continue;
     const int ncl = std::min(mc, max_tiles);
     long long cost = 0;
@@ -860,12 +912,14 @@ void plan_chain(GemmParams* p, int n, int nt, int* csize, int* ncl_out) {
 
 void gemm_finish_params(GemmParams& p) {
   shape_params(p);
-  plan_chain(&p, 1, std::max(1, token_groups(p.n_tok)), &p.csize, &p.n_clusters);
+  plan_chain(&p, 1, variant_of(std::max(1, token_groups(p.n_tok)), false), &p.csize, &p.n_clusters);
   p.grid = p.csize * p.n_clusters;
 }
 
-mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStream_t stream, bool independent) {
+mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStream_t stream, bool independent,
+                            const GemmAttn* attn) {
   if (n < 1 || n > kGemmMaxPhases || (n > 1 && !independent && !flags)) return MV_ERR_INVALID_ARG;
+  if (attn && (independent || !flags)) return MV_ERR_INVALID_ARG;
   ChainMaps maps;
   ChainArgs ca;
   memset(&maps, 0, sizeof(maps));
@@ -885,8 +939,12 @@ mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStrea
     if (ps[i].tok_ld == 0) ps[i].tok_ld = BN * nt;
     if (ps[i].tok_ld < ps[i].n_tok) return MV_ERR_SHAPE;
   }
+  const int v = variant_of(nt, attn != nullptr && nt == 1);
   int csize = 1, ncl = 1;
-  plan_chain(ps, n, nt, &csize, &ncl);
+  plan_chain(ps, n, v, &csize, &ncl);
+  if (attn && (nt != 1 || csize > attn::kMaxSplits || ncl < attn->args.H || (attn->D != 64 && attn->D != 128) ||
+               attn->args.n > attn::kRows || attn->args.seq_rows != 0))
+    return MV_ERR_UNSUPPORTED;
   for (int i = 0; i < n; ++i) {
     ps[i].csize = csize;
     ps[i].n_clusters = ncl;
@@ -900,13 +958,20 @@ mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStrea
   }
   ca.n_phases = n;
   ca.csize = csize;
+  if (attn) {
+    ca.attn = attn->args;
+    ca.attn.splits = csize;
+    ca.attn_D = attn->D;
+    maps.kmap = attn->kmap;
+    maps.vmap = attn->vmap;
+  }
   ca.indep = independent ? 1 : 0;
   ca.flags = independent ? nullptr : flags;
-  if (!set_smem_for(nt)) return MV_ERR_CUDA;
+  if (!set_smem_for(v)) return MV_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize * ncl);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes_for(nt);
+  cfg.dynamicSmemBytes = smem_bytes_for(v);
   cfg.stream = stream;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -918,14 +983,13 @@ mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStrea
   cfg.attrs = at;
   cfg.numAttrs = mv_pdl_enabled() ? 2 : 1;
   cudaError_t e;
-  if (nt == 1)
-    e = cudaLaunchKernelEx(&cfg, gemm_kernel<1>, maps, ca);
-  else if (nt == 2)
-    e = cudaLaunchKernelEx(&cfg, gemm_kernel<2>, maps, ca);
-  else if (nt == 3)
-    e = cudaLaunchKernelEx(&cfg, gemm_kernel<3>, maps, ca);
-  else
-    e = cudaLaunchKernelEx(&cfg, gemm_kernel<4>, maps, ca);
+  switch (v) {
+    case 0: e = cudaLaunchKernelEx(&cfg, gemm_kernel<1, false>, maps, ca); break;
+    case 1: e = cudaLaunchKernelEx(&cfg, gemm_kernel<2, false>, maps, ca); break;
+    case 2: e = cudaLaunchKernelEx(&cfg, gemm_kernel<3, false>, maps, ca); break;
+    case 3: e = cudaLaunchKernelEx(&cfg, gemm_kernel<4, false>, maps, ca); break;
+    default: e = cudaLaunchKernelEx(&cfg, gemm_kernel<1, true>, maps, ca); break;
+  }
   if (e != cudaSuccess) return MV_ERR_CUDA;
   return mv_last_launch("gemm");
 }

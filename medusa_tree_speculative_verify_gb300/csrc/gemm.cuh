@@ -1,6 +1,7 @@
 // Parameters and host helpers of the tcgen05 projection kernel (gemm.cu).
 #pragma once
 
+#include "attn_core.cuh"
 #include "common.cuh"
 
 enum { EPI_STORE = 0, EPI_RESIDUAL = 1, EPI_SWIGLU = 2, EPI_QKV = 3 };
@@ -54,9 +55,19 @@ struct GemmPhase {
   CUtensorMap a0, a1, b;  // weights (a1: the up matrix of a paired phase), activations
   GemmParams p;
 };
-// Phase-done counters of a chain (kGemmMaxPhases + 1 words, zero before the first launch; every launch leaves
-// them zero again).
-constexpr int kGemmChainFlagWords = kGemmMaxPhases + 1;
+// Counters of a chain: kGemmMaxPhases phase counters, the exit counter, the attention counter. Zero before the
+// first launch; every launch leaves them zero again.
+constexpr int kGemmAttnFlag = kGemmMaxPhases + 1;
+constexpr int kGemmChainFlagWords = kGemmMaxPhases + 2;
+
+// The tree attention of the chain's layer, run first inside the chain (its output is phase 0's activations):
+// cluster q computes head q, its CTAs the head's key splits, on the epilogue warps, while the producer already
+// streams phase 0's weights. D is 64 or 128; one sequence of at most 64 tree nodes.
+struct GemmAttn {
+  CUtensorMap kmap, vmap;  // the cache planes [H][S_max][D] (attn::Args plane_k / plane_v pick the layer's)
+  attn::Args args;         // splits is set by the launch (= the chain's cluster size)
+  int D;
+};
 
 bool gemm_weight_map(CUtensorMap* map, const void* w, int rows, int K, int box_rows);
 bool gemm_weight_map_packed(CUtensorMap* map, const void* w, int rows, int K, int tile_rows);
@@ -69,5 +80,7 @@ mv_status launch_gemm(int epi, const CUtensorMap& a0, const CUtensorMap& a1, con
 // ph[i].p must have its shape fields set (M, K, paired, F); the cluster plan is computed here. flags: see above
 // (may be null when n == 1).
 // independent: the phases read nothing another phase writes (no counters; flags may be null).
+// attn: the layer's attention first (see GemmAttn); MV_ERR_UNSUPPORTED, with nothing launched, when this chain
+// cannot run it (more than one token group, a cluster size above attn::kMaxSplits, fewer clusters than heads).
 mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStream_t stream,
-                            bool independent = false);
+                            bool independent = false, const GemmAttn* attn = nullptr);

@@ -11,6 +11,8 @@
 //
 // Kernel sequence of one step (L layers): build_candidates, embed, L x {QKV+RoPE+KV append, tree attention,
 // O + residual, gate/up + SiLU-gate, down + residual}, LM head, posterior, KV compaction, heads W1, heads W2.
+#include <stdlib.h>
+
 #include <algorithm>
 #include <vector>
 
@@ -207,6 +209,7 @@ struct mv_session {
   uint16_t* h_pair;           // [32][d] bf16: the heads' inputs of a batch as (hi, lo) rows
   uint64_t* root_counter;     // per sequence: generator counter of the next sampled root
   mv_root_params root{};      // root rule (MV_ROOT_ARGMAX: the posterior's argmax stands)
+  bool fuse_attention = true;  // run each layer's attention inside its projection chain when the shape allows
   int root_epoch = 0;         // bumped by every mv_session_set_root_sampling
   CUtensorMap m_xb, m_attn, m_act, m_kv;
   // CUDA graph of n consecutive steps (medusa_verify_steps_graph), captured on first use
@@ -409,15 +412,11 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     ProfScope ps(s, st, MV_PROF_GEMM_QKV);
     rc = launch_gemm_chain(&g, 1, nullptr, st);
   }
+  const float scale = 1.0f / sqrtf((float)d.head_dim);
+  const bool try_fuse = s->fuse_attention && nseq == 1 && n <= kSeqRows &&
+                        (d.head_dim == 64 || d.head_dim == 128);
   for (int l = 0; l < d.n_layers && rc == MV_OK; ++l) {
-    {
-      ProfScope ps(s, st, MV_PROF_ATTENTION);
-      const int pl = b0 * 2 * d.n_layers + 2 * l;  // sequence b0's planes of layer l
-      rc = launch_tree_attention_n(s->m_kv, s->m_kv, pl, pl + 1, s->q, d.n_heads, d.head_dim, s->s_max,
-                                   s->cur_len + b0, 0, s->s_max - n, t, n, 1.0f / sqrtf((float)d.head_dim), s->attn,
-                                   s->ws_attn, st, nseq, 2 * d.n_layers);
-    }
-    if (rc != MV_OK) break;
+    const int pl = b0 * 2 * d.n_layers + 2 * l;  // sequence b0's planes of layer l
     // O, gate/up and down of this layer, then the next layer's QKV (or the LM head): one launch
     GemmPhase ch[kGemmMaxPhases];
     int nph = 0;
@@ -428,6 +427,34 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
       ch[nph++] = qkv_phase(l + 1);
     else if (lm)
       ch[nph++] = lm_phase();
+    if (try_fuse) {  // the layer's attention inside the same launch, ahead of the O projection
+      GemmAttn ga{};
+      ga.kmap = ga.vmap = s->m_kv;
+      ga.D = d.head_dim;
+      attn::Args& a = ga.args;
+      a.q = s->q;
+      a.out = s->attn;
+      a.anc = t->d_ancestors;
+      a.d_prefix = s->cur_len + b0;
+      a.H = d.n_heads;
+      a.S_max = s->s_max;
+      a.n = n;
+      a.plane_k = pl;
+      a.plane_v = pl + 1;
+      a.scale_log2 = scale * 1.4426950408889634f;
+      a.err = mv_error_word();
+      ProfScope ps(s, st, MV_PROF_GEMM_CHAIN);
+      rc = launch_gemm_chain(ch, nph, s->chain_flags, st, false, &ga);
+      if (rc != MV_ERR_UNSUPPORTED) continue;
+      rc = MV_OK;  // this shape cannot fuse: separate launches below
+    }
+    {
+      ProfScope ps(s, st, MV_PROF_ATTENTION);
+      rc = launch_tree_attention_n(s->m_kv, s->m_kv, pl, pl + 1, s->q, d.n_heads, d.head_dim, s->s_max,
+                                   s->cur_len + b0, 0, s->s_max - n, t, n, scale, s->attn, s->ws_attn, st, nseq,
+                                   2 * d.n_layers);
+    }
+    if (rc != MV_OK) break;
     ProfScope ps(s, st, MV_PROF_GEMM_CHAIN);
     rc = launch_gemm_chain(ch, nph, s->chain_flags, st);
   }
@@ -524,6 +551,10 @@ extern "C" mv_status mv_batch_session_create(mv_model* m, const mv_tree* tree, i
   s->topk = topk;
   s->batch = batch;
   s->kv_seq_elems = (size_t)d.n_layers * 2 * d.n_heads * s_max * d.head_dim;
+  {  // MV_FUSE_ATTN=0 in the environment keeps every attention in its own launch
+    const char* e = getenv("MV_FUSE_ATTN");
+    s->fuse_attention = !(e && e[0] == '0');
+  }
   char* b = static_cast<char*>(ws);
   s->cur_len = reinterpret_cast<int32_t*>(b + L.state);
   s->root_counter = reinterpret_cast<uint64_t*>(b + L.state + 16);

@@ -31,7 +31,7 @@ import torch
 
 __all__ = [
     "GAMMA", "stream_key", "hash_words", "normal", "uniform01", "randint",
-    "ModelDims", "TINY", "LLAMA7B", "model_weights", "weight_names",
+    "ModelDims", "TINY", "SMALL64", "LLAMA7B", "model_weights", "weight_names",
     "dense_tree_choices", "synthetic_tree_choices", "prompt_tokens",
     "planted_tokens_and_logits", "kv_cache", "packed_weights",
 ]
@@ -133,6 +133,8 @@ class ModelDims:
 
 # Tiny decoder: d=64, 4 heads x 16, FFN 128, vocab 512, 2 layers, 2 Medusa heads.
 TINY = ModelDims(d=64, n_layers=2, n_heads=4, head_dim=16, ffn=128, vocab=512, n_medusa=2)
+# Small decoder with 64-wide heads: d=256, 4 heads x 64, FFN 512, vocab 1024, 2 layers, 2 Medusa heads.
+SMALL64 = ModelDims(d=256, n_layers=2, n_heads=4, head_dim=64, ffn=512, vocab=1024, n_medusa=2)
 # Llama-7B shape: d=4096, 32 layers, 32 heads x 128, FFN 11008, vocab 32000, 4 Medusa heads.
 LLAMA7B = ModelDims(d=4096, n_layers=32, n_heads=32, head_dim=128, ffn=11008, vocab=32000, n_medusa=4)
 

@@ -266,3 +266,38 @@ def test_multi_step_graph_equals_eager(mode):
     for o in outs[1:]:
         assert o[0] == outs[0][0] and o[1] == outs[0][1] and o[2] == outs[0][2]
         assert torch.equal(o[3], outs[0][3])
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_small64_decoder_attention_inside_the_chain(fused, monkeypatch):
+    """A decoder with 64-wide heads (d 256, 4 heads, 2 layers): its projection chains run each layer's attention
+    first (cluster q = head q) unless MV_FUSE_ATTN=0. One step's logits match the oracle, and greedy Medusa decoding
+    equals the oracle's greedy AR stream, either way."""
+    monkeypatch.setenv("MV_FUSE_ATTN", "1" if fused else "0")
+    dims = synth.SMALL64
+    choices = synth.synthetic_tree_choices(48, 2, 10)
+    _, _, tree, sess, om, ot = _setup(choices, dims=dims)
+    p = synth.prompt_tokens(3, 40, dims.vocab)
+    sess.prefill(torch.as_tensor(p, dtype=torch.int32, device="cuda"))
+    st = o_prefill(om, p.numpy(), S_MAX, 10)
+    # the oracle's root and head top-k as the step's candidates (the tiny random heads have near ties)
+    sess.result[3] = int(st.root)
+    sess.head_topk.copy_(torch.as_tensor(st.head_topk, dtype=torch.int32, device="cuda"))
+    sess.step(mv.AcceptParams(GREEDY))
+    torch.cuda.synchronize()
+    toks, info = o_verify_step(om, st, ot, GREEDY)
+    assert sess.tree_tokens[: tree.n_nodes].cpu().tolist() == info["tree_tokens"].tolist()
+    got = sess.logits[: tree.n_nodes].double().cpu().numpy()
+    assert np.allclose(got, info["logits"], rtol=RTOL, atol=ATOL)
+    _, _, _, sess2, _, _ = _setup(choices, dims=dims)
+    gen, _ = _gpu_decode(sess2, p.numpy(), 12, mv.AcceptParams(GREEDY))
+    lg = teacher_forced_logits(om, p.numpy(), gen, S_MAX)
+    ar = ar_greedy_decode(om, p.numpy(), 12, S_MAX)
+    first_close = len(gen)
+    for i, tk in enumerate(gen):
+        top = lg[i].max()
+        assert top - lg[i, tk] <= 1e-2 + 2e-2 * abs(top)
+        srt = np.sort(lg[i])
+        if srt[-1] - srt[-2] < 1e-2 + 2e-2 * abs(top):
+            first_close = min(first_close, i)
+    assert gen[:first_close + 1].tolist() == ar[:first_close + 1].tolist()
