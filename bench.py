@@ -326,9 +326,9 @@ def run_gpu(args, world, rank, local):
                                           "tree attention, O, gate/up, down and the next QKV, plus the first QKV)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": GEMM_TRAFFIC_PER_ALGORITHMIC_BYTE * g_bytes / max(g_n, 1),
-                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the LM-head launch "
-                                  "(profiles/gemm_kernel_lm_head_32000x4096_t64.md), scaled to the step's average "
-                                  "projection launch by its algorithmic bytes",
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one chain launch with its "
+                                  "layer's attention (profiles/gemm_kernel_fused_chain_7b_layer_t64.md), scaled to the "
+                                  "step's average projection launch by its algorithmic bytes",
                 "algorithmic_bytes_per_launch": g_bytes / max(g_n, 1),
                 "avg_launch_us": g_ms * 1e3 / max(g_n, 1),
                 "per_kind": {k: {"launches_per_step": c / args.steps, "ms_per_step": ms / args.steps,
@@ -358,10 +358,10 @@ def run_gpu(args, world, rank, local):
     return line
 
 
-# DRAM bytes (read + write) per algorithmic byte of the projection kernel, from the ncu capture of the LM-head
-# launch (32000 x 4096, 64 tokens: 267.9 MB measured for 270.9 MB algorithmic): the kernel reads every weight byte
-# once, so the traffic of a launch scales with its bytes.
-GEMM_TRAFFIC_PER_ALGORITHMIC_BYTE = 0.989
+# DRAM bytes (read + write) per algorithmic byte of the projection kernel, from the ncu capture of one chain launch
+# with its layer's attention (7B shape: 414.7 MB measured for 420.2 MB algorithmic; the LM-head launch alone:
+# 267.9 / 270.9 MB): the kernel reads every weight byte once, so the traffic of a launch scales with its bytes.
+GEMM_TRAFFIC_PER_ALGORITHMIC_BYTE = 0.987
 
 
 def gemm_bytes(dims, n):
@@ -412,6 +412,35 @@ def _time_launches(fn, steps, warmup, flush=True):
         torch.cuda.synchronize()
         times.append(a.elapsed_time(b))
     return statistics.median(times)
+
+
+def run_micro_step2(steps, warmup):
+    """Verify steps of a 2-layer model of the 7B shape (2.7 GB on the device: small enough for a full ncu capture of
+    one projection-chain launch). Prefill of 128 tokens (2 chunks), `warmup` eager steps, then `steps` eager steps
+    timed with CUDA events. Projection launches before the timed steps: 2 x (1 + 2) + warmup x (1 + 2)."""
+    import dataclasses
+    import medusa_tree_speculative_verify_gb300 as mv
+    dims = dataclasses.replace(synth.LLAMA7B, n_layers=2)
+    w = mv.pack_model_weights(synth.packed_weights(dims, 0, torch.bfloat16, "cuda"), drop_source=True)
+    model = mv.Model(dims, w)
+    tree = mv.Tree(tree_choices("synthetic"), TREE["topk"])
+    sess = mv.Session(model, tree, 1024)
+    sess.prefill(synth.prompt_tokens(0, PROMPT_LEN, dims.vocab).to(torch.int32).cuda())
+    prm = mv.AcceptParams(mv.GREEDY)
+    for _ in range(warmup):
+        sess.step(prm)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        sess.step(prm)
+    b.record()
+    torch.cuda.synchronize()
+    st, code = mv.get_error()
+    if st != 0:
+        raise RuntimeError(f"device error word {code:#x}")
+    return {"micro": "step_2layers", "ms_per_step": a.elapsed_time(b) / steps,
+            "gemm_launches_before_timed": 2 * (1 + dims.n_layers) + warmup * (1 + dims.n_layers)}
 
 
 def run_micro_other(name, steps, warmup):
@@ -599,7 +628,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tree", default="synthetic", choices=["synthetic", "page"],
                     help="the tree of the verify step: the synthetic 64-node tree or the page's own 63 choices")
-    ap.add_argument("--micro", choices=sorted(MICRO) + MICRO_OTHER, help="time one kernel alone and exit")
+    ap.add_argument("--micro", choices=sorted(MICRO) + MICRO_OTHER + ["step_2layers"],
+                    help="time one kernel alone and exit")
     ap.add_argument("--sweep-nodes", default=None,
                     help="comma-separated tree sizes (2..256): time the verify step per size and exit")
     ap.add_argument("--sweep-batch", default=None,
@@ -613,6 +643,9 @@ def main():
         run_sweep_batch([int(x) for x in args.sweep_batch.split(",")], args.steps, args.warmup, args.tree)
         return
     if args.micro:
+        if args.micro == "step_2layers":
+            print(json.dumps(run_micro_step2(args.steps, args.warmup)))
+            return
         fn = run_micro if args.micro in MICRO else run_micro_other
         print(json.dumps(fn(args.micro, args.steps, args.warmup)))
         return
