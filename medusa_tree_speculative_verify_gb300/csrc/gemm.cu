@@ -394,6 +394,12 @@ struct EpiClusterSync {
   MV_DEV void done() { step(dbar); }
 };
 
+// *p += 1 with release semantics at GPU scope: every write this thread has made or observed (the other epilogue
+// threads' stores, ordered before it by a CTA barrier) is visible to whoever acquires the new count.
+MV_DEV void count_release(unsigned int* p) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p) : "memory");
+}
+
 // Bounded wait until *p >= target (acquire at GPU scope); false when it expires.
 MV_DEV bool wait_count(const unsigned int* p, unsigned int target) {
   const uint64_t t0 = mv_globaltimer();
@@ -618,8 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
         epi_bar();  // this CTA's attention outputs are stored
         if (i == 0) {
-          __threadfence();
-          atomicAdd(ca.flags + kGemmAttnFlag, 1u);
+          count_release(ca.flags + kGemmAttnFlag);
         }
       }
     }
@@ -694,8 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       if (published < upto) {
         epi_bar();  // every output of those phases written by this CTA
         if (i == 0) {
-          __threadfence();
-          for (int k = published; k < upto; ++k) atomicAdd(ca.flags + k, 1u);
+          for (int k = published; k < upto; ++k) count_release(ca.flags + k);
         }
         published = upto;
       }
