@@ -37,6 +37,7 @@ import synth  # noqa: E402
 METRIC = "verify steps/s (7B shape, 64-node tree)"
 PROMPT_LEN = 128
 TREE = dict(n_nodes=64, depth=4, topk=10)
+FORCED_STEPS = 20  # forced-acceptance steps timed after the main run
 
 
 def tree_choices(name):
@@ -312,6 +313,35 @@ def run_gpu(args, world, rank, local):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     barrier(world)
 
+    # ---- forced acceptance: the heads' rank-0 candidates replaced by the model's own greedy continuation, so
+    # every step accepts the whole depth (greedy Medusa output = greedy AR output), through the same host-buffer
+    # entry point as e2e. The continuation comes from plain steps from the same state, which is then restored.
+    depth = tree.depth
+    snap_ws, snap_kv = sess.ws.clone(), sess.kv.clone()
+    greedy = []
+    while len(greedy) < (depth + 1) * FORCED_STEPS + depth + 2:
+        sess.step(prm)
+        greedy += sess.read_result()["tokens"]
+    sess.ws.copy_(snap_ws)
+    sess.kv.copy_(snap_kv)
+    del snap_ws, snap_kv
+    seeds[1:] = sess.head_topk.reshape(-1).cpu()
+    torch.cuda.synchronize()
+    pos, forced_ok, forced_full, forced_tok = 0, True, True, 0
+    t0 = time.perf_counter()
+    for _ in range(FORCED_STEPS):
+        seeds[0] = greedy[pos]
+        for h in range(dims.n_medusa):  # rank 0 of head h: the token h + 1 places after the root
+            seeds[1 + h * TREE["topk"]] = greedy[pos + 1 + h]
+        sess.step_host(prm, seeds, res_host, seeds_next)
+        got = mv.result_dict(res_host)["tokens"]
+        forced_ok &= got == greedy[pos: pos + len(got)]  # the emitted tokens are the greedy stream
+        forced_full &= len(got) == depth + 1
+        pos += len(got)
+        forced_tok += len(got)
+        seeds.copy_(seeds_next)
+    forced_s = max_over_ranks(time.perf_counter() - t0, world)
+
     steps_per_s = args.steps / (ms / 1e3) * world
     tokens_per_step = tok_e2e / args.steps
     peak, peak_kind = peaks()
@@ -346,6 +376,11 @@ def run_gpu(args, world, rank, local):
                    "tree_nodes": 64, "prompt": PROMPT_LEN, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (14.4 GB of weights streamed per step)"},
         "tokens_per_s": steps_per_s * tokens_per_step, "tokens_per_step": tokens_per_step,
+        "forced_acceptance": {"steps": FORCED_STEPS, "tokens_per_step": forced_tok / FORCED_STEPS,
+                              "e2e_tokens_per_s": forced_tok * world / forced_s,
+                              "e2e_steps_per_s": FORCED_STEPS * world / forced_s,
+                              "tokens_equal_greedy_stream": bool(forced_ok),
+                              "all_steps_accept_the_whole_depth": bool(forced_full)},
         "step_hbm_gbs": step_bytes / (ms / args.steps / 1e3) / 1e9,
         "e2e": {"value": args.steps * world / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": 4 * (1 + k),
                 "d2h_bytes_per_step": 4 * mv.RESULT_INTS + 4 * (1 + k)},
