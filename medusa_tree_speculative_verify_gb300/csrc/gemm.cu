@@ -1,12 +1,14 @@
-// Backbone projections over the (up to) 64 tree tokens on the 5th-generation tensor cores (tcgen05).
+// Backbone projections over the tree tokens on the 5th-generation tensor cores (tcgen05).
 //
 // "大模型推理 memory bandwidth bound (5) - Medusa", 二.5 tree_decoding(): the backbone runs once over all tree
 // tokens; at 64 tokens every weight byte feeds 64 multiply-adds, so these GEMMs stream the weights from HBM.
 //
-// Mapping (swap-AB): D[128 weight rows x 64 tokens] += W[128 x 64 k] . X[64 tokens x 64 k]^T per k-block, one
-// tcgen05.mma.cta_group::1.kind::f16 (M=128, N=64, K=16) per 16 k. Operands come from shared memory through
-// TMA (128-byte swizzle, K-major), the accumulator lives in tensor memory (two 64-column buffers, so the
-// epilogue of one segment overlaps the MMAs of the next).
+// Mapping (swap-AB): D[128 weight rows x 64 NT tokens] += W[128 x 64 k] . X[64 NT tokens x 64 k]^T per k-block,
+// one tcgen05.mma.cta_group::1.kind::f16 (M=128, N=64 NT, K=16) per 16 k, for NT = 1..4 token groups of 64 (up to
+// 256 tokens: larger trees, or one group per sequence of a batch). Operands come from shared memory through TMA
+// (128-byte swizzle, K-major), the accumulators live in tensor memory (two buffers, so the epilogue of one tile
+// overlaps the MMAs of the next). With one group the chain can also run its layer's tree attention first, on the
+// epilogue warps (attn_core.cuh), while the producer streams the first projection's weights.
 //
 // Work split: split-K inside a thread-block cluster. Cluster q of C CTAs owns a contiguous range of tiles;
 // CTA rank r of the cluster streams k-blocks [r*kbt/C, (r+1)*kbt/C) of each, so the weight bytes of a tile are

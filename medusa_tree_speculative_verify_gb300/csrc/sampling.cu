@@ -17,7 +17,7 @@
 // E = round(e 2^40) with e = exp((z - max) / T) <= 1, so every sum is exact and the drawn token does not depend
 // on the order of the additions.
 //
-// The nucleus boundary is found without a sort, in three rounds over the row:
+// The nucleus boundary is found without a sort, in three levels over the row:
 //   1. histogram of masses over 2048 bins of x = 16 (max - z) / T (1/16 nat of probability each; x is
 //      monotone in z, so bins follow the token order exactly), and the bin where the cumulative mass from the
 //      top first reaches ceil(top_p * S);
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kST, 1) sample_root_kernel(const SampleArgs a)
     unsigned long long T = (unsigned long long)ceil((double)a.prm.top_p * (double)S);
     if (T > S) T = S;
     if (T == 0) T = 1;  // keep at least the first token
-    // round 1: bins of x = 16 (max - z) / T
+    // level 1: bins of x = 16 (max - z) / T
     for (int b = tid; b < kBins; b += kST) hist[b] = 0ull;
     __syncthreads();
     for (int i = tid; i < V; i += kST) {
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kST, 1) sample_root_kernel(const SampleArgs a)
     const int b1 = sc.sel[0];
     unsigned long long A = sc.selu[0];
     __syncthreads();
-    // round 2: sub-bins of bin b1
+    // level 2: sub-bins of bin b1
     for (int b = tid; b < kBins; b += kST) hist[b] = 0ull;
     __syncthreads();
     auto sub_of = [&](float zi, int& bin) {
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kST, 1) sample_root_kernel(const SampleArgs a)
     const int b2 = sc.sel[0];
     A = sc.selu[0];
     __syncthreads();
-    // round 3: distinct logits of sub-bin (b1, b2), largest first, until the cumulative mass reaches T
+    // level 3: distinct logits of sub-bin (b1, b2), largest first, until the cumulative mass reaches T
     uint32_t kprev = 0xffffffffu;
     bool first = true;
     kstar = 0u;
