@@ -95,6 +95,8 @@ void mv_tree_destroy(mv_tree* tree);
  *   w2     device bf16 [K][V][d]         w_lm device bf16 [V][d] or NULL
  *   out_idx device int32 [B][K][topk]    out_val device fp32 [B][K][topk]   out_root device int32 [B] or NULL
  * Limits: 1 <= B <= 16, d % 8 == 0, 8 <= d <= 8192, 1 <= topk <= 16, topk <= V, 1 <= K <= 8.
+ * workspace: device memory of medusa_heads_topk_workspace() bytes, 16-byte aligned, zero-filled before its first
+ * use; a call leaves its control words zero again, so the same workspace serves later calls on the same stream.
  */
 mv_status medusa_heads_topk_workspace(int32_t B, int32_t d, int32_t K, int32_t V, int32_t topk, size_t* bytes);
 mv_status medusa_heads_topk(const mv_bf16* h, int32_t B, int32_t d, int32_t K, const mv_bf16* w1,

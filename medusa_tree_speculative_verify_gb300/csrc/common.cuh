@@ -212,6 +212,14 @@ MV_DEV void tma_load_3d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, i
       "l"(pol)
       : "memory");
 }
+// Untiled bulk copy global -> shared of `bytes` (both addresses 16-byte aligned, bytes a multiple of 16),
+// counted on `bar` like the tensor copies, with an L2 policy.
+MV_DEV void bulk_load_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
 MV_DEV void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2, int c3) {
   asm volatile(
       "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], [%2];"

@@ -27,15 +27,14 @@ mv_status launch_sample_root(const float* logits, int V, int ld, int n_rows, mv_
 mv_status launch_kv_compact(mv_bf16* kv, int L, int H, int S_max, int D, const int32_t* d_prefix, int prefix,
                             const mv_posterior_result* d_res, int32_t* d_cur_len, cudaStream_t stream);
 
-int heads_w2_ctas_per_mat(int n_mat, int V);
 // Heads + top-k of B rows given as bf16 (hi, lo) pairs: h_pair [32][d], hi row b and lo row 16 + b (fp32-grade
 // input); the weights are read once for all rows (tensor-core projections). out_idx [B][K][topk]. ws:
 // heads_ws_bytes(B >= 2, ...).
 mv_status launch_heads_rows_pair(const uint16_t* h_pair, int B, int d, int K, const uint16_t* w1, const uint16_t* w2,
                                  int V, int topk, int32_t* out_idx, void* ws, cudaStream_t stream);
 size_t heads_ws_bytes(int B, int d, int K, int V, int topk);
-// h (bf16 [B][d]) or, in step mode, x (fp32 rows) + res: h = RMSNorm(x[res->next_node]); commit_len (step mode)
-// receives += res->n_tokens.
+// Batch-1 GEMV path, one launch pair per row: h (bf16 [B][d]) or, in step mode (B = 1), x (fp32 rows) + res:
+// h = RMSNorm(x[res->next_node]); commit_len (step mode) receives += res->n_tokens.
 mv_status launch_heads(const uint16_t* h, const float* x, const mv_posterior_result* res, float norm_eps, int B,
                        int d, int K, const uint16_t* w1, const uint16_t* w2, int V, int topk, const uint16_t* w_lm,
                        int32_t* out_idx, float* out_val, int32_t* out_root, int32_t* commit_len, void* ws,
