@@ -269,6 +269,36 @@ def test_heads_topk_small(B, d, K, V, topk):
     _heads_case(B, d, K, V, topk, True)
 
 
+def test_heads_topk_workspace_reused_across_calls():
+    """One zero-filled workspace serves repeated calls, batch-1 and batched ones interleaved: each batch-1 pass
+    leaves its tile counters and tickets at zero, and the batched path does not touch them."""
+    d, K, V, topk = 520, 3, 777, 5
+    dims = synth.ModelDims(d=d, n_layers=0, n_heads=1, head_dim=d, ffn=d, vocab=V, n_medusa=K)
+    w = synth.model_weights(dims, 0, torch.bfloat16, "cuda",
+                            names=[f"medusa{k}.w{i}" for k in range(K) for i in (1, 2)] + ["lm_head"])
+    w1 = torch.stack([w[f"medusa{k}.w1"] for k in range(K)])
+    w2 = torch.stack([w[f"medusa{k}.w2"] for k in range(K)])
+    wk = ws(mv.medusa_heads_topk_workspace(4, d, K, V, topk))
+    get = lambda name: w[name].double().cpu().numpy()
+    for call, B in enumerate([1, 1, 4, 1, 2, 1]):
+        h = synth.normal(call, "h", (B, d), 1.0, dtype=torch.bfloat16, device="cuda")
+        out_idx = torch.full((B, K, topk), -1, dtype=torch.int32, device="cuda")
+        out_val = torch.zeros(B, K, topk, dtype=torch.float32, device="cuda")
+        root = torch.full((B,), -1, dtype=torch.int32, device="cuda")
+        mv.medusa_heads_topk(h, w1, w2, topk, out_idx, out_val, w_lm=w["lm_head"], out_root=root, workspace=wk)
+        torch.cuda.synchronize()
+        hh = h.double().cpu().numpy()
+        gi, gv, gr = out_idx.cpu().numpy(), out_val.cpu().numpy(), root.cpu().numpy()
+        for b in range(B):
+            z = medusa_heads(get, K, hh[b])
+            for k in range(K):
+                _check_topk(gi[b, k], gv[b, k], z[k], topk)
+            zl = get("lm_head") @ hh[b]
+            ri = int(np.argmax(zl))
+            assert gr[b] == ri or abs(zl[gr[b]] - zl[ri]) < MARGIN, (call, b)
+        assert int(wk[:256].view(torch.int32).abs().sum().item()) == 0, call  # the control block is zero again
+
+
 # --------------------------------------------------------------------------------------------- tree attention
 
 def _attn_case(H, D, P, tree_name, S_max=None, seed=0):
