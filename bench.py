@@ -302,6 +302,8 @@ def run_gpu(args, world, rank, local):
     res_host = torch.zeros(mv.RESULT_INTS, dtype=torch.int32).pin_memory()
     seeds[0] = int(r["next_root"])
     seeds[1:] = sess.head_topk.reshape(-1).cpu()
+    sess.step_host(prm, seeds, res_host, seeds_next)  # untimed: captures the host step's graph
+    seeds.copy_(seeds_next)
     torch.cuda.synchronize()
     tok_e2e = 0
     barrier(world)

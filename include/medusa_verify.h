@@ -356,8 +356,11 @@ mv_status medusa_verify_step(mv_session* session, mv_accept_params params, mv_st
 
 /* The same step driven from host memory: h_seeds_in (nullable) = [root, head_topk[n_medusa][topk]] copied to
  * the device first; afterwards the result (mv_posterior_result, as int32s) is copied to h_result and, if
- * h_seeds_out is not NULL, the next seeds to h_seeds_out. Synchronises `stream` before returning. Host
- * buffers should be pinned for asynchronous copies. A batched session returns MV_ERR_UNSUPPORTED. */
+ * h_seeds_out is not NULL, the next seeds to h_seeds_out. Synchronises `stream` before returning. With
+ * page-locked host buffers (and per-launch profiling off) the copies and the step are captured once as a CUDA
+ * graph and replayed by later calls with the same params and buffers (re-captured when either changes or the
+ * root sampling is set); other buffers take the launches one by one. A batched session returns
+ * MV_ERR_UNSUPPORTED. */
 mv_status medusa_verify_step_host(mv_session* session, mv_accept_params params, const int32_t* h_seeds_in,
                                   int32_t* h_result, int32_t* h_seeds_out, mv_stream stream);
 

@@ -219,6 +219,12 @@ struct mv_session {
   int graph_steps = 0;
   int graph_root_epoch = 0;
   bool graph_profiled = false;
+  // CUDA graph of one host-buffer step (medusa_verify_step_host with pinned buffers): the seed copies, the step
+  // and the result copies, replayed while the parameters and host buffers stay the same
+  cudaGraphExec_t host_graph = nullptr;
+  mv_accept_params host_prm{};
+  int host_root_epoch = 0;
+  const void* host_ptrs[3] = {nullptr, nullptr, nullptr};
   // optional per-launch timing (mv_session_profile): event pairs recorded around every launch
   bool profiling = false;
   std::vector<cudaEvent_t> ev_pool;
@@ -625,6 +631,7 @@ extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16
 extern "C" void mv_session_destroy(mv_session* s) {
   if (!s) return;
   if (s->graph_exec) cudaGraphExecDestroy(s->graph_exec);
+  if (s->host_graph) cudaGraphExecDestroy(s->host_graph);
   if (s->capture_stream) cudaStreamDestroy(s->capture_stream);
   for (cudaEvent_t e : s->ev_pool) cudaEventDestroy(e);
   if (s->chain) {
@@ -746,18 +753,18 @@ extern "C" mv_status medusa_verify_step(mv_session* s, mv_accept_params prm, mv_
   return launch_heads_rows_pair(s->h_pair, B, d.d, K, m->w1, m->w2, d.vocab, s->topk, s->head_topk, s->ws_heads, st);
 }
 
-extern "C" mv_status medusa_verify_step_host(mv_session* s, mv_accept_params prm, const int32_t* h_seeds_in,
-                                             int32_t* h_result, int32_t* h_seeds_out, mv_stream stream) {
-  if (!s || !h_result) return MV_ERR_INVALID_ARG;
-  if (s->batch != 1) return MV_ERR_UNSUPPORTED;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+namespace {
+
+// Enqueues one host-buffer step on `st`: seeds in, the step, result and next seeds out.
+mv_status enqueue_host_step(mv_session* s, mv_accept_params prm, const int32_t* h_seeds_in, int32_t* h_result,
+                            int32_t* h_seeds_out, cudaStream_t st) {
   const int k = s->model->dims.n_medusa * s->topk;
   if (h_seeds_in) {
     if (cudaMemcpyAsync(&s->result->next_root, h_seeds_in, 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemcpyAsync(s->head_topk, h_seeds_in + 1, (size_t)k * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
       return MV_ERR_CUDA;
   }
-  mv_status rc = medusa_verify_step(s, prm, stream);
+  mv_status rc = medusa_verify_step(s, prm, st);
   if (rc != MV_OK) return rc;
   if (cudaMemcpyAsync(h_result, s->result, sizeof(mv_posterior_result), cudaMemcpyDeviceToHost, st) !=
       cudaSuccess)
@@ -767,6 +774,69 @@ extern "C" mv_status medusa_verify_step_host(mv_session* s, mv_accept_params prm
         cudaMemcpyAsync(h_seeds_out + 1, s->head_topk, (size_t)k * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
       return MV_ERR_CUDA;
   }
+  return MV_OK;
+}
+
+// Page-locked host memory (allocated or registered with CUDA): copies from it can be captured in a graph.
+bool host_pinned(const void* p) {
+  if (!p) return true;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+}  // namespace
+
+extern "C" mv_status medusa_verify_step_host(mv_session* s, mv_accept_params prm, const int32_t* h_seeds_in,
+                                             int32_t* h_result, int32_t* h_seeds_out, mv_stream stream) {
+  if (!s || !h_result) return MV_ERR_INVALID_ARG;
+  if (s->batch != 1) return MV_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (s->profiling || !host_pinned(h_seeds_in) || !host_pinned(h_result) || !host_pinned(h_seeds_out)) {
+    const mv_status rc = enqueue_host_step(s, prm, h_seeds_in, h_result, h_seeds_out, st);
+    if (rc != MV_OK) return rc;
+    return cudaStreamSynchronize(st) == cudaSuccess ? MV_OK : MV_ERR_CUDA;
+  }
+  // pinned buffers: the whole step as one graph launch (captured on first use, replayed while nothing changed)
+  const bool same = s->host_graph && s->host_prm.mode == prm.mode && s->host_prm.temperature == prm.temperature &&
+                    s->host_prm.eps == prm.eps && s->host_prm.delta == prm.delta &&
+                    s->host_root_epoch == s->root_epoch && s->host_ptrs[0] == h_seeds_in &&
+                    s->host_ptrs[1] == h_result && s->host_ptrs[2] == h_seeds_out;
+  if (!same) {
+    if (prm.mode != MV_GREEDY && prm.mode != MV_TYPICAL) return MV_ERR_INVALID_ARG;
+    if (prm.mode == MV_TYPICAL && !(prm.temperature > 0.0f)) return MV_ERR_INVALID_ARG;
+    if (s->host_graph) {
+      cudaGraphExecDestroy(s->host_graph);
+      s->host_graph = nullptr;
+    }
+    if (!s->capture_stream && cudaStreamCreateWithFlags(&s->capture_stream, cudaStreamNonBlocking) != cudaSuccess)
+      return MV_ERR_CUDA;
+    if (cudaStreamBeginCapture(s->capture_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+      return MV_ERR_CUDA;
+    const mv_status rc = enqueue_host_step(s, prm, h_seeds_in, h_result, h_seeds_out, s->capture_stream);
+    cudaGraph_t g = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(s->capture_stream, &g);
+    if (rc != MV_OK || e != cudaSuccess) {
+      if (g) cudaGraphDestroy(g);
+      cudaGetLastError();  // a failed capture leaves nothing behind for later launches to report
+      return rc != MV_OK ? rc : MV_ERR_CUDA;
+    }
+    const cudaError_t ei = cudaGraphInstantiate(&s->host_graph, g, 0);
+    cudaGraphDestroy(g);
+    if (ei != cudaSuccess) {
+      s->host_graph = nullptr;
+      return MV_ERR_CUDA;
+    }
+    s->host_prm = prm;
+    s->host_root_epoch = s->root_epoch;
+    s->host_ptrs[0] = h_seeds_in;
+    s->host_ptrs[1] = h_result;
+    s->host_ptrs[2] = h_seeds_out;
+  }
+  if (cudaGraphLaunch(s->host_graph, st) != cudaSuccess) return MV_ERR_CUDA;
   return cudaStreamSynchronize(st) == cudaSuccess ? MV_OK : MV_ERR_CUDA;
 }
 

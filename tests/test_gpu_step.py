@@ -217,21 +217,30 @@ def test_typical_steps_match_oracle():
         assert int(sess.cur_len.item()) == st.cur_len
 
 
-def test_host_step_api_matches_device_step():
+@pytest.mark.parametrize("buffers", ["pinned", "pageable", "pinned_alternating"])
+def test_host_step_api_matches_device_step(buffers):
+    """Pinned buffers run the host step as a replayed graph (re-captured when the buffers change), pageable ones
+    launch by launch; both decode as the device-buffer step does."""
     _, _, tree, sess, om, ot = _setup(synth.dense_tree_choices([2, 3]))
     p = torch.as_tensor(_prompt(), dtype=torch.int32, device="cuda")
     sess.prefill(p)
     k = DIMS.n_medusa * 10
-    seeds = torch.zeros(1 + k, dtype=torch.int32).pin_memory()
-    out = torch.zeros(mv.RESULT_INTS, dtype=torch.int32).pin_memory()
-    seeds_next = torch.zeros(1 + k, dtype=torch.int32).pin_memory()
+
+    def bufs():
+        t = [torch.zeros(1 + k, dtype=torch.int32), torch.zeros(mv.RESULT_INTS, dtype=torch.int32),
+             torch.zeros(1 + k, dtype=torch.int32)]
+        return [x.pin_memory() for x in t] if buffers != "pageable" else t
+
+    sets = [bufs(), bufs()] if buffers == "pinned_alternating" else [bufs()]
+    seeds = sets[0][0]
     seeds[0] = int(sess.read_result()["next_root"])
     seeds[1:] = sess.head_topk.reshape(-1).cpu()
     toks_host = []
-    for _ in range(4):
+    for i in range(4):
+        seeds, out, seeds_next = sets[i % len(sets)]
         sess.step_host(mv.AcceptParams(GREEDY), seeds, out, seeds_next)
         toks_host += mv.result_dict(out)["tokens"]
-        seeds.copy_(seeds_next)
+        sets[(i + 1) % len(sets)][0].copy_(seeds_next)
     _, _, _, sess2, _, _ = _setup(synth.dense_tree_choices([2, 3]))
     sess2.prefill(p)
     toks_dev = []
