@@ -264,7 +264,7 @@ def test_heads_topk_full_size(B):
 
 @pytest.mark.parametrize("B,d,K,V,topk", [(1, 64, 2, 512, 10), (3, 64, 2, 512, 10), (2, 8, 1, 16, 16),
                                           (5, 1024, 3, 1000, 7), (1, 8192, 1, 300, 1), (1, 8, 1, 16, 16),
-                                          (1, 520, 3, 777, 5), (1, 2056, 2, 4099, 10)])
+                                          (1, 520, 3, 777, 5), (1, 2056, 2, 4099, 10), (1, 64, 8, 300, 16)])
 def test_heads_topk_small(B, d, K, V, topk):
     _heads_case(B, d, K, V, topk, True)
 
