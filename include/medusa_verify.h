@@ -21,6 +21,9 @@
  *     returns. They must be zero-filled before their first use; every call leaves the counters it uses in
  *     them back at zero. Calls that share a workspace must be ordered on one stream.
  *   - Not thread-safe per handle.
+ *   - The library looks up the device addresses of its own device arrays (the error word, the scratch of
+ *     evaluate_posterior_noalloc) once per device and keeps them: do not call cudaDeviceReset on a device the
+ *     library has used while the process goes on using the library.
  */
 #ifndef MEDUSA_VERIFY_H
 #define MEDUSA_VERIFY_H
@@ -175,11 +178,13 @@ mv_status evaluate_posterior(const float* logits, int32_t V, int32_t ld, const i
  * allocation, or a serving loop that must not touch the device allocator after start-up. It computes exactly
  * what evaluate_posterior computes (same arguments minus the workspace). Its scratch is a fixed 2048-byte
  * __device__ array inside the library (every GPU that loads the library holds it until the process exits),
- * enough for 64 tree nodes; a larger tree is rejected with MV_ERR_CAPACITY. The first call on
+ * enough for MV_NOALLOC_MAX_NODES tree nodes (a limit of its own, below MV_MAX_NODES); a larger tree is rejected
+ * with MV_ERR_CAPACITY. The first call on
  * a device looks up that array's device address (cudaGetSymbolAddress) with the device current; make that
  * first call before any stream capture. Each call clears the array's completion counter on `stream` before
  * its kernel. All calls share the one array, so calls that overlap on the GPU (other streams, other threads)
  * race: order them. Never allocates. */
+#define MV_NOALLOC_MAX_NODES 64 /* tree nodes evaluate_posterior_noalloc accepts */
 mv_status evaluate_posterior_noalloc(const float* logits, int32_t V, int32_t ld, const int32_t* d_tree_tokens,
                                      const mv_tree* tree, mv_accept_params params, mv_posterior_result* d_out,
                                      float* d_node_stats, int32_t* d_node_argmax, mv_stream stream);
@@ -287,18 +292,61 @@ mv_status mv_pack_weight(const mv_bf16* src, mv_bf16* dst, int32_t M, int32_t K,
 typedef struct mv_model mv_model;
 typedef struct mv_session mv_session;
 
+/* Storage and arithmetic type of a model: its weights, activations and KV cache. */
+typedef enum { MV_DTYPE_BF16 = 0, MV_DTYPE_F32 = 1 } mv_dtype;
+
 /* Limits: d % 8 == 0, d <= 8192, head_dim in {16, 32, 64, 128}, ffn % 8 == 0, 1 <= n_medusa <= 8; every
  * pointer 16-byte aligned. MV_ERR_SHAPE otherwise. Builds the weights' TMA descriptors (host only). */
 mv_status mv_model_create(const mv_model_dims* dims, const mv_model_weights* weights, mv_model** out);
+
+/* An fp32 model: the same decoder with fp32 weights (row-major [out][in], the layouts of mv_model_weights, never
+ * packed), fp32 activations and an fp32 KV cache; every product and sum of its verify step is fp32 (plain FMA on
+ * the CUDA cores: a correctness precision for small models, not tuned for speed). Caller-owned device weights that
+ * must outlive the handle. Limits as mv_model_create; its sessions take batch 1 only. */
+typedef struct mv_model_weights_f32 {
+  const float* embed;         /* [vocab][d] */
+  const float* const* wqkv;   /* host array of n_layers device pointers, each [3*n_heads*head_dim][d] */
+  const float* const* wo;     /* [d][n_heads*head_dim] per layer */
+  const float* const* w_gate; /* [ffn][d] per layer */
+  const float* const* w_up;   /* [ffn][d] per layer */
+  const float* const* w_down; /* [d][ffn] per layer */
+  const float* lm_head;       /* [vocab][d] */
+  const float* medusa_w1;     /* [n_medusa][d][d] */
+  const float* medusa_w2;     /* [n_medusa][vocab][d] */
+} mv_model_weights_f32;
+mv_status mv_model_create_f32(const mv_model_dims* dims, const mv_model_weights_f32* weights, mv_model** out);
+
+/* A random-init model of `dtype` (MV_DTYPE_BF16 or MV_DTYPE_F32) whose weights the library draws into device
+ * memory it allocates (on the current device) and frees in mv_model_destroy. Every matrix and the embedding is
+ * N(0, std^2) from mv_fill_normal's generator under `seed`, one stream per tensor name: "embed", "lm_head",
+ * "layer<l>.wq", "layer<l>.wk", "layer<l>.wv", "layer<l>.wo", "layer<l>.w_gate", "layer<l>.w_up",
+ * "layer<l>.w_down", "medusa<k>.w1", "medusa<k>.w2" (element i = row-major index within the tensor). The
+ * projections of a bf16 model are stored in the packed layout. Synchronises the device.
+ * Errors: MV_ERR_INVALID_ARG (null, bad dtype, std < 0), MV_ERR_SHAPE (as mv_model_create), MV_ERR_CAPACITY (the
+ * allocation failed), MV_ERR_CUDA. */
+mv_status mv_model_create_random(const mv_model_dims* dims, uint64_t seed, double std, int32_t dtype,
+                                 mv_model** out);
+/* MV_DTYPE_BF16 or MV_DTYPE_F32; -1 for NULL. */
+int32_t mv_model_dtype(const mv_model* model);
 void mv_model_destroy(mv_model* model);
 
-/* A session binds a model, a tree, a KV cache kv [n_layers][2][n_heads][s_max][head_dim] (bf16, caller-owned,
- * 256-byte aligned) and a workspace (caller-owned device memory of mv_session_workspace() bytes, 256-byte
+/* The library's generator of random inputs: dst[i] (i < count, device memory of `dtype`) = round(z_i * std) with
+ * z_i the Box-Muller normal (Box and Muller, 1958; cosine branch) sqrt(-2 ln u1) cos(2 pi u2) of
+ * u1 = ((w_{2i} >> 11) + 1) 2^-53 and u2 = (w_{2i+1} >> 11) 2^-53, w_j the SplitMix64 output (Steele, Lea
+ * and Flood, OOPSLA 2014) of key + (j + 1) * 0x9E3779B97F4A7C15, key = mix(fnv1a64(name) ^ mix(seed)) with mix
+ * the SplitMix64 output function. Evaluated in float64 without fused multiply-adds, rounded to fp32 and, for bf16, from there to
+ * bf16 (round to nearest even both times). Asynchronous on `stream`. */
+mv_status mv_fill_normal(void* dst, int32_t dtype, int64_t count, uint64_t seed, const char* name, double std,
+                         mv_stream stream);
+
+/* A session binds a model, a tree, a KV cache kv [n_layers][2][n_heads][s_max][head_dim] (of the model's dtype:
+ * bf16, or fp32 for an fp32 model; caller-owned, 256-byte aligned, finite values in every row (e.g. zero-filled):
+ * a key tile that ends past the tree reads rows beyond it and weights them by zero) and a workspace (caller-owned device memory of mv_session_workspace() bytes, 256-byte
  * aligned; zero-filled by mv_session_create, which is synchronous). The decode state (current length, the
  * last posterior result whose next_root is the next root, the head top-k) lives in the workspace.
  * Limits: tree depth <= n_medusa, tree topk <= topk <= 16, s_max >= 65. */
 mv_status mv_session_workspace(const mv_model* model, int32_t s_max, int32_t topk, size_t* bytes);
-mv_status mv_session_create(mv_model* model, const mv_tree* tree, mv_bf16* kv, int32_t s_max, int32_t topk,
+mv_status mv_session_create(mv_model* model, const mv_tree* tree, void* kv, int32_t s_max, int32_t topk,
                             void* workspace, size_t ws_bytes, mv_session** out);
 /* Batch > 1 verify (the pages' code supports only batch 1, 二.1 medusa_generate()): `batch` independent
  * sequences (1 .. MV_MAX_BATCH) of the same tree (at most 64 nodes when batch > 1) in one session, kv
@@ -306,8 +354,9 @@ mv_status mv_session_create(mv_model* model, const mv_tree* tree, mv_bf16* kv, i
  * sequences' trees, so every weight byte is read once per step for the whole batch; candidates, posterior,
  * root, KV compaction and heads run per sequence. Same workspace size as mv_session_workspace(). A batch of one
  * is mv_session_create. Errors: MV_ERR_INVALID_ARG (batch outside 1 .. MV_MAX_BATCH, null pointers),
- * MV_ERR_SHAPE (as mv_session_create; also a tree over 64 nodes with batch > 1). */
-mv_status mv_batch_session_create(mv_model* model, const mv_tree* tree, int32_t batch, mv_bf16* kv, int32_t s_max,
+ * MV_ERR_SHAPE (as mv_session_create; also a tree over 64 nodes with batch > 1), MV_ERR_UNSUPPORTED (batch > 1 of
+ * an fp32 model). */
+mv_status mv_batch_session_create(mv_model* model, const mv_tree* tree, int32_t batch, void* kv, int32_t s_max,
                                   int32_t topk, void* workspace, size_t ws_bytes, mv_session** out);
 void mv_session_destroy(mv_session* session);
 
@@ -396,6 +445,16 @@ mv_status mv_get_error(uint32_t* code);
 /* Detail value recorded with the first device error since the last clear (e.g. an offending index); read
  * it before mv_get_error(), which clears both. Synchronous. */
 mv_status mv_get_error_detail(uint32_t* detail);
+/* Self-test of the device-side failure detection (no counterpart on the pages; a diagnostic, not part of the
+ * verify path). One CTA runs the two bounded waits every kernel of the path relies on -- the acquire wait on a
+ * device counter that the projection chain uses between phases, and the mbarrier wait of the TMA and bulk-copy
+ * rings -- on a counter and a barrier that nothing ever completes, each with a limit of limit_ns nanoseconds
+ * instead of the kernels' 2 s. Each wait gives up at its limit; the kernel then sets the device error word (site
+ * 20, MV_DEVERR_TIMEOUT; detail bit 0: the counter wait expired, bit 1: the mbarrier wait expired) and returns.
+ * d_out: device int32 [4]: [0] 1 if the counter wait succeeded, [1] the same for the mbarrier wait, [2] the
+ * counter itself (set to 0), [3] microseconds both waits took. Nothing faults or hangs: read the result with
+ * mv_get_error(). Errors: MV_ERR_INVALID_ARG (null or unaligned d_out, limit_ns outside 1 us .. 10 ms). */
+mv_status mv_selftest_wait_timeout(uint32_t limit_ns, int32_t* d_out, mv_stream stream);
 /* Human-readable name of a status. */
 const char* mv_status_string(mv_status s);
 

@@ -19,12 +19,15 @@ __all__ = ["lib", "MVError", "Tree", "AcceptParams", "PosteriorResult", "GREEDY"
            "linear_bf16", "linear_bf16_workspace", "ModelDims",
            "medusa_heads_topk", "medusa_heads_topk_workspace", "build_candidates", "tree_attention",
            "tree_attention_workspace", "evaluate_posterior", "evaluate_posterior_workspace", "kv_compact",
-           "get_error", "MAX_NODES", "MAX_DEPTH", "EXPORTED_SYMBOLS"]
+           "get_error", "fill_normal", "selftest_wait_timeout", "DTYPE_BF16", "DTYPE_F32", "MAX_NODES",
+           "MAX_DEPTH", "EXPORTED_SYMBOLS"]
 
 MAX_NODES = 256
+NOALLOC_MAX_NODES = 64
 MAX_DEPTH = 8
 MASK_WORDS = 4
 GREEDY, TYPICAL = 0, 1
+DTYPE_BF16, DTYPE_F32 = 0, 1
 ROOT_ARGMAX, ROOT_TYPICAL, ROOT_NUCLEUS = 0, 1, 2
 
 _lib = None
@@ -93,7 +96,11 @@ _SIGS = {
     "mv_packed_weight_bytes": ([_I, _I, _I, ctypes.POINTER(_S)], _I),
     "mv_pack_weight": ([_P, _P, _I, _I, _I, _P], _I),
     "mv_model_create": ([_P, _P, ctypes.POINTER(_P)], _I),
+    "mv_model_create_f32": ([_P, _P, ctypes.POINTER(_P)], _I),
+    "mv_model_create_random": ([_P, ctypes.c_uint64, ctypes.c_double, _I, ctypes.POINTER(_P)], _I),
+    "mv_model_dtype": ([_P], _I),
     "mv_model_destroy": ([_P], None),
+    "mv_fill_normal": ([_P, _I, ctypes.c_int64, ctypes.c_uint64, ctypes.c_char_p, ctypes.c_double, _P], _I),
     "mv_session_workspace": ([_P, _I, _I, ctypes.POINTER(_S)], _I),
     "mv_session_create": ([_P, _P, _P, _I, _I, _P, _S, ctypes.POINTER(_P)], _I),
     "mv_batch_session_create": ([_P, _P, _I, _P, _I, _I, _P, _S, ctypes.POINTER(_P)], _I),
@@ -109,6 +116,7 @@ _SIGS = {
     "mv_session_profile_read": ([_P, _P, _P], _I),
     "mv_get_error": ([ctypes.POINTER(_U)], _I),
     "mv_get_error_detail": ([ctypes.POINTER(_U)], _I),
+    "mv_selftest_wait_timeout": ([_U, _P, _P], _I),
     "mv_status_string": ([_I], ctypes.c_char_p),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
@@ -265,6 +273,22 @@ def get_error(with_detail=False):
     return (st, code.value, detail.value) if with_detail else (st, code.value)
 
 
+def fill_normal(out, seed, name, std=1.0, stream=None):
+    """Fills the contiguous bf16 or fp32 device tensor ``out`` with the library's N(0, std^2) stream ``name``
+    under ``seed`` (see mv_fill_normal)."""
+    import torch
+    dt = DTYPE_F32 if out.dtype == torch.float32 else DTYPE_BF16
+    assert out.dtype in (torch.float32, torch.bfloat16) and out.is_contiguous()
+    _check(lib().mv_fill_normal(_ptr(out), dt, out.numel(), seed % 2 ** 64, name.encode(), float(std),
+                                _stream(stream)), "mv_fill_normal")
+
+
+def selftest_wait_timeout(limit_ns, out, stream=None):
+    """Runs the library's two bounded waits on a counter and a barrier nothing completes (see
+    mv_selftest_wait_timeout); out: int32 [4] device tensor."""
+    _check(lib().mv_selftest_wait_timeout(limit_ns, _ptr(out), _stream(stream)), "mv_selftest_wait_timeout")
+
+
 def result_dict(buf):
     """Decode a PosteriorResult from an int32 tensor / array of RESULT_INTS entries."""
     a = np.asarray(buf.cpu() if hasattr(buf, "cpu") else buf, dtype=np.int32)
@@ -332,33 +356,66 @@ class _Weights(ctypes.Structure):
                 ("lm_head", _P), ("medusa_w1", _P), ("medusa_w2", _P), ("packed", _I)]
 
 
+class _WeightsF32(ctypes.Structure):
+    _fields_ = [("embed", _P), ("wqkv", _P), ("wo", _P), ("w_gate", _P), ("w_up", _P), ("w_down", _P),
+                ("lm_head", _P), ("medusa_w1", _P), ("medusa_w2", _P)]
+
+
 class _StatePtrs(ctypes.Structure):
     _fields_ = [("cur_len", _P), ("result", _P), ("head_topk", _P), ("tree_tokens", _P), ("cart", _P),
                 ("logits", _P), ("ld_logits", _I), ("hidden", _P), ("root_counter", _P), ("batch", _I)]
 
 
+def _c_dims(dims):
+    return ModelDims(dims.d, dims.n_layers, dims.n_heads, dims.head_dim, dims.ffn, dims.vocab, dims.n_medusa,
+                     dims.rope_theta, dims.norm_eps)
+
+
 class Model:
-    """A model handle over caller-owned bf16 device weights.
+    """A model handle over caller-owned device weights: bf16 (mv_model_create) or fp32 (mv_model_create_f32),
+    chosen by the dtype of ``w["embed"]``.
 
     ``w`` maps embed, lm_head, medusa_w1 [K,d,d], medusa_w2 [K,V,d] to tensors and wqkv, wo, w_gate, w_up,
-    w_down to per-layer lists of tensors (see mv_model_weights in include/medusa_verify.h).
+    w_down to per-layer lists of tensors (see mv_model_weights in include/medusa_verify.h). ``Model.random``
+    makes a model whose weights the library draws and owns.
     """
 
     def __init__(self, dims, w):
-        self.dims = ModelDims(dims.d, dims.n_layers, dims.n_heads, dims.head_dim, dims.ffn, dims.vocab,
-                              dims.n_medusa, dims.rope_theta, dims.norm_eps)
+        import torch
+        self.dims = _c_dims(dims)
         self.w = w  # keep the tensors alive
         L = dims.n_layers
         arrs = {k: (ctypes.c_void_p * L)(*[t.data_ptr() for t in w[k]]) for k in
                 ("wqkv", "wo", "w_gate", "w_up", "w_down")}
         self._arrs = arrs
-        cw = _Weights(w["embed"].data_ptr(), ctypes.cast(arrs["wqkv"], _P), ctypes.cast(arrs["wo"], _P),
-                      ctypes.cast(arrs["w_gate"], _P), ctypes.cast(arrs["w_up"], _P), ctypes.cast(arrs["w_down"], _P),
-                      w["lm_head"].data_ptr(), w["medusa_w1"].data_ptr(), w["medusa_w2"].data_ptr(),
-                      1 if w.get("packed") else 0)
+        lists = [ctypes.cast(arrs[k], _P) for k in ("wqkv", "wo", "w_gate", "w_up", "w_down")]
+        heads = (w["lm_head"].data_ptr(), w["medusa_w1"].data_ptr(), w["medusa_w2"].data_ptr())
         h = ctypes.c_void_p()
-        _check(lib().mv_model_create(ctypes.byref(self.dims), ctypes.byref(cw), ctypes.byref(h)), "mv_model_create")
+        if w["embed"].dtype == torch.float32:
+            self.dtype = DTYPE_F32
+            cw = _WeightsF32(w["embed"].data_ptr(), *lists, *heads)
+            _check(lib().mv_model_create_f32(ctypes.byref(self.dims), ctypes.byref(cw), ctypes.byref(h)),
+                   "mv_model_create_f32")
+        else:
+            self.dtype = DTYPE_BF16
+            cw = _Weights(w["embed"].data_ptr(), *lists, *heads, 1 if w.get("packed") else 0)
+            _check(lib().mv_model_create(ctypes.byref(self.dims), ctypes.byref(cw), ctypes.byref(h)),
+                   "mv_model_create")
         self.handle = h
+
+    @classmethod
+    def random(cls, dims, seed=0, std=None, dtype=DTYPE_BF16):
+        """A random-init model whose weights the library draws (mv_model_create_random) and owns."""
+        self = cls.__new__(cls)
+        self.dims = _c_dims(dims)
+        self.w = None
+        self.dtype = dtype
+        h = ctypes.c_void_p()
+        std = dims.std if std is None else std
+        _check(lib().mv_model_create_random(ctypes.byref(self.dims), seed % 2 ** 64, float(std), dtype,
+                                            ctypes.byref(h)), "mv_model_create_random")
+        self.handle = h
+        return self
 
     def __del__(self):
         if getattr(self, "handle", None) is not None and _lib is not None:
@@ -378,7 +435,8 @@ class Session:
         shape = (d.n_layers, 2, d.n_heads, s_max, d.head_dim)
         if batch > 1:
             shape = (batch,) + shape
-        self.kv = kv if kv is not None else torch.zeros(*shape, dtype=torch.bfloat16, device="cuda")
+        kv_dtype = torch.float32 if getattr(model, "dtype", DTYPE_BF16) == DTYPE_F32 else torch.bfloat16
+        self.kv = kv if kv is not None else torch.zeros(*shape, dtype=kv_dtype, device="cuda")
         nbytes = _ws_size(lib().mv_session_workspace, model.handle, s_max, self.topk)
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
         h = ctypes.c_void_p()
@@ -403,7 +461,9 @@ class Session:
             self.cur_len = view(sp.cur_len, B, torch.int32)
             self.result = view(sp.result, B * RESULT_INTS, torch.int32).view(B, RESULT_INTS)
             self.head_topk = view(sp.head_topk, B * K * self.topk, torch.int32).view(B, K, self.topk)
-        self.tree_tokens = view(sp.tree_tokens, tree.n_nodes, torch.int32)
+        # the tree tokens of sequence b start at row 64 b (a batch of one: rows 0 .. n - 1)
+        self.tree_tokens = view(sp.tree_tokens, tree.n_nodes if B == 1 else 64 * (B - 1) + tree.n_nodes,
+                                torch.int32)
         self.cart = view(sp.cart, tree.n_paths * (tree.depth + 1), torch.int32).view(tree.n_paths, tree.depth + 1)
         self.ld_logits = sp.ld_logits
         self.logits = view(sp.logits, MAX_NODES * sp.ld_logits, torch.float32).view(MAX_NODES, sp.ld_logits)[:, : d.vocab]

@@ -20,7 +20,6 @@ constexpr int kKeys = 64;   // keys per tile
 constexpr int kRows = 64;   // query rows per CTA (tree nodes, padded)
 constexpr int kStages = 2;  // key/value tiles in flight
 constexpr int kMinTiles = 2;       // key tiles per split at the longest prefix, at least (sets the cluster size)
-constexpr int kTilesPerSplit = 1;  // key tiles per working split at the actual prefix (measured best)
 // CTAs per cluster. Measured on GB300: with clusters of 8 (two 81 KB CTAs per SM) a few clusters of a 32-head
 // launch only start when others leave (a second wave, +11 us at short prefixes), although the occupancy query
 // reports room for all; clusters of 4 start together.
@@ -133,18 +132,22 @@ MV_DEV void head(const Args& a, const CUtensorMap* kmap, const CUtensorMap* vmap
   const int n = min(kRows, n_all - row0);         // query rows of this block
   const int n_keys = min(n_all, row0 + kRows);    // tree keys any of them can see
   const int total_tiles = (P + n_keys + kKeys - 1) / kKeys;
-  // The cluster is sized for the longest prefix. At this prefix only S splits get tiles, about kTilesPerSplit
-  // each (a split costs a merge). With S = 1 the first CTA does the whole head and writes it directly; the
-  // others leave at once (no cluster barrier is used then). With S > 1 the idle splits still take part in the
-  // barriers but contribute nothing to the merge.
-  const int S = max(1, min(C, (total_tiles + kTilesPerSplit - 1) / kTilesPerSplit));
+  // Key tile t (keys 64 t .. 64 t + 63, absolute positions) goes to split t mod C, whatever the prefix length
+  // and the tree size. A query row's result then depends only on the keys it can see: the tiles past its last
+  // visible key are fully masked and leave its running max, sum and output exactly as they were, and a split
+  // with no visible key adds exact zeros to the merge. So a tree node's row is bit for bit the row the same
+  // token gets when it is decoded alone at the same position (a tree of the root only, prefix = its position),
+  // and greedy verification emits exactly the library's own autoregressive greedy stream.
+  // The cluster is sized for the longest prefix; at this prefix the first S = min(C, tiles) splits get tiles.
+  // With S = 1 the first CTA does the whole head and writes it directly (the same arithmetic as a one-split
+  // merge); the others leave at once (no cluster barrier is used then). With S > 1 the idle splits still take
+  // part in the barriers but contribute nothing to the merge.
+  const int S = max(1, min(C, total_tiles));
   if (S == 1 && split > 0) return;
-  const int t_begin = split < S ? (int)((long long)split * total_tiles / S) : 0;
-  const int t_end = split < S ? (int)((long long)(split + 1) * total_tiles / S) : 0;
-  const int count = t_end - t_begin;
+  const int count = split < S ? (total_tiles - split + C - 1) / C : 0;  // tiles split, split + C, ...
 
-  auto issue = [&](int i) {  // tile t_begin + i into stage i % kStages
-    const int st = i % kStages, key0 = (t_begin + i) * kKeys;
+  auto issue = [&](int i) {  // tile split + i C into stage i % kStages
+    const int st = i % kStages, key0 = (split + i * C) * kKeys;
     mbar_arrive_expect_tx(&full[st], 2 * kTileBytes);
 #pragma unroll
     for (int b = 0; b < kBoxes; ++b) {
@@ -198,7 +201,7 @@ MV_DEV void head(const Args& a, const CUtensorMap* kmap, const CUtensorMap* vmap
       break;
     }
     const uint32_t kb = smem_u32(sk + st * kTileBytes), vb = smem_u32(sv + st * kTileBytes);
-    const int key0 = (t_begin + i) * kKeys;
+    const int key0 = (split + i * C) * kKeys;
     // S = Q K^T for 16 rows x 64 keys
     float s[8][4];
 #pragma unroll

@@ -107,13 +107,26 @@ MV_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for phase `parity` of `bar` to complete; false if MV_WAIT_LIMIT_NS passed first.
-MV_DEV bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for phase `parity` of `bar` to complete; false if limit_ns (default MV_WAIT_LIMIT_NS) passed first.
+MV_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = MV_WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = mv_globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (mv_globaltimer() - t0 > MV_WAIT_LIMIT_NS) return false;
+    if (mv_globaltimer() - t0 > limit_ns) return false;
+  }
+}
+
+// Bounded wait until *p >= target (acquire at GPU scope), the wait on a device counter that other CTAs bump;
+// false when limit_ns (default MV_WAIT_LIMIT_NS) passes first.
+MV_DEV bool wait_count(const unsigned int* p, unsigned int target, uint64_t limit_ns = MV_WAIT_LIMIT_NS) {
+  const uint64_t t0 = mv_globaltimer();
+  while (true) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    if (mv_globaltimer() - t0 > limit_ns) return false;
+    __nanosleep(64);
   }
 }
 

@@ -402,18 +402,9 @@ MV_DEV void count_release(unsigned int* p) {
   asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p) : "memory");
 }
 
-// Bounded wait until *p >= target (acquire at GPU scope); false when it expires.
-MV_DEV bool wait_count(const unsigned int* p, unsigned int target) {
-  const uint64_t t0 = mv_globaltimer();
-  while (true) {
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    if (v >= target) return true;
-    if (mv_globaltimer() - t0 > MV_WAIT_LIMIT_NS) return false;
-    __nanosleep(64);
-  }
-}
-
+// No thread of this kernel returns early, not even after a bounded wait expired: every CTA must reach the
+// end, where the last one out resets the chain's phase counters. A CTA that left before would leave them
+// non-zero, and the next launch's waits on them would pass at once and read activations that are not ready.
 template <int NT, bool kAttn>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ ChainMaps maps,
                                                            const __grid_constant__ ChainArgs ca) {

@@ -57,3 +57,27 @@ mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vm
                                   const mv_bf16* q, int H, int D, int S_max, const int32_t* d_prefix, int prefix,
                                   int max_prefix, const mv_tree* t, int n, float scale, mv_bf16* out, void* ws,
                                   cudaStream_t stream, int nseq = 1, int seq_planes = 0);
+
+// ---- the fp32 model path (f32.cu): plain FFMA kernels over fp32 weights, activations and KV cache
+mv_status launch_f32_embed(const int32_t* tokens, int n, const float* E, int vocab, int d, float* x, cudaStream_t st);
+mv_status launch_f32_rmsnorm(const float* x, int n, int d, float eps, float* xn, cudaStream_t st);
+// epi: 0 out = in W^T, 1 out += in W^T, 2 out = SiLU(in W^T) * (in W_up^T)
+mv_status launch_f32_linear(const float* in, int ld_in, const float* w, const float* w_up, int M, int K, int n,
+                            float* out, int ld_out, int epi, cudaStream_t st);
+mv_status launch_f32_rope_append(const float* qkv, int n, int H, int D, int S_max, const int32_t* cur_len,
+                                 const int32_t* pos_ids, float rope_theta, float* q_out, float* kv_layer,
+                                 cudaStream_t st);
+mv_status launch_f32_tree_attention(const float* q, const float* kv_layer, int H, int D, int S_max, int n,
+                                    const int32_t* cur_len, const uint64_t* anc, float scale, float* out,
+                                    cudaStream_t st);
+size_t f32_heads_ws_bytes(int d, int K, int V);
+// heads on h = RMSNorm(x[res->next_node]) (next_node < n_rows), top-k per head into out_idx [K][topk], then
+// cur_len += res->n_tokens
+mv_status launch_f32_heads(const float* x, int n_rows, const mv_posterior_result* res, float eps, int d, int K,
+                           const float* w1, const float* w2, int V, int topk, int32_t* out_idx, int32_t* cur_len,
+                           void* ws, cudaStream_t st);
+// The library's random weight generator (see mv_fill_normal): a logical [M][K] matrix whose rows fall in
+// segments of seg_rows rows drawn from keys[0..n_keys), written row-major (tile_rows = 0) or in the packed layout.
+uint64_t mv_stream_key(uint64_t seed, const char* name);
+mv_status launch_gen_normal(void* dst, int dtype, int64_t M, int64_t K, int tile_rows, const uint64_t* keys,
+                            int n_keys, int64_t seg_rows, double std, cudaStream_t st);

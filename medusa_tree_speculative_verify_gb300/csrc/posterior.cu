@@ -322,7 +322,7 @@ extern "C" mv_status evaluate_posterior(const float* logits, int32_t V, int32_t 
 // ------------------------------------------------------------------------------------------------------------
 namespace {
 
-constexpr int kNoAllocMaxNodes = 64;
+constexpr int kNoAllocMaxNodes = MV_NOALLOC_MAX_NODES;
 constexpr size_t kNoAllocScratchBytes = 2048;  // >= posterior_ws_bytes(kNoAllocMaxNodes) = 64 * 20 + 64 = 1344
 static __device__ __align__(256) unsigned char g_posterior_scratch[kNoAllocScratchBytes];
 

@@ -80,6 +80,42 @@ extern "C" mv_status mv_get_error(uint32_t* code) {
   return MV_OK;
 }
 
+namespace {
+
+// The two bounded waits every kernel of the path relies on, run with a short limit on a counter and an mbarrier
+// that nothing completes: the counter wait of the projection chain's phase boundaries and the mbarrier wait of
+// the TMA / bulk-copy rings. Each must give up, report MV_DEVERR_TIMEOUT and let the kernel return.
+__global__ void selftest_wait_kernel(uint64_t limit_ns, int32_t* out, unsigned int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  unsigned int* counter = reinterpret_cast<unsigned int*>(out + 2);  // nothing bumps it
+  if (threadIdx.x == 0) {
+    *counter = 0u;
+    __threadfence();
+    mbar_init(&bar, 1);  // count 1, and nothing arrives
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = mv_globaltimer();
+    const bool c = wait_count(counter, 1u, limit_ns);
+    const bool m = mbar_wait(&bar, 0u, limit_ns);
+    const uint64_t t1 = mv_globaltimer();
+    out[0] = c ? 1 : 0;
+    out[1] = m ? 1 : 0;
+    out[3] = (int32_t)min((uint64_t)0x7fffffff, (t1 - t0) / 1000u);  // microseconds both waits took
+    if (!c || !m) mv_set_error_detail(err, 20, MV_DEVERR_TIMEOUT, (c ? 0u : 1u) | (m ? 0u : 2u));
+  }
+}
+
+}  // namespace
+
+extern "C" mv_status mv_selftest_wait_timeout(uint32_t limit_ns, int32_t* d_out, mv_stream stream) {
+  if (!d_out || limit_ns < 1000u || limit_ns > 10000000u) return MV_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(d_out) & 3) return MV_ERR_INVALID_ARG;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, d_out, mv_error_word());
+  return mv_last_launch("selftest_wait");
+}
+
 extern "C" mv_status mv_get_error_detail(uint32_t* detail) {
   unsigned int* w = mv_error_word();
   if (!w || !detail) return MV_ERR_INVALID_ARG;

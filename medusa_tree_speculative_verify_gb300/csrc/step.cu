@@ -14,6 +14,7 @@
 #include <stdlib.h>
 
 #include <algorithm>
+#include <string>
 #include <vector>
 
 #include "common.cuh"
@@ -169,6 +170,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct mv_model {
   mv_model_dims dims;
+  int dtype = MV_DTYPE_BF16;  // MV_DTYPE_F32: the fp32 path (f32.cu) on the f_* weights
   int packed;  // projection weights in the packed layout
   const uint16_t* embed;
   std::vector<const uint16_t*> wqkv, wo, w_gate, w_up, w_down;
@@ -177,6 +179,13 @@ struct mv_model {
   const uint16_t* w2;
   std::vector<CUtensorMap> m_qkv, m_o, m_gate, m_up, m_down;
   CUtensorMap m_lm;
+  // fp32 weights (row-major [out][in])
+  const float* f_embed = nullptr;
+  std::vector<const float*> f_wqkv, f_wo, f_gate, f_up, f_down;
+  const float* f_lm = nullptr;
+  const float* f_w1 = nullptr;
+  const float* f_w2 = nullptr;
+  void* owned = nullptr;  // device memory of a model whose weights the library drew (mv_model_create_random)
 };
 
 struct mv_session {
@@ -205,6 +214,11 @@ struct mv_session {
   void* ws_post;
   void* ws_heads;
   unsigned int* chain_flags;  // phase counters of the projection chains (zero between launches)
+  float* xn = nullptr;        // fp32 path: the normalised projection operand [kTok][d]
+  float* qkv_f = nullptr;     // fp32 path: [kTok][3 H D] projections, then q [kTok][H][D] (rotated)
+  float* q_f = nullptr;
+  float* attn_f = nullptr;    // fp32 path: attention output [kTok][H D]
+  float* act_f = nullptr;     // fp32 path: SiLU-gate product [kTok][ffn]
   float2* row_max;            // [vocab/128][64]: per LM-head tile and token, max and first argmax
   uint16_t* h_pair;           // [32][d] bf16: the heads' inputs of a batch as (hi, lo) rows
   uint64_t* root_counter;     // per sequence: generator counter of the next sampled root
@@ -270,7 +284,7 @@ struct SessionLayout {
       total;
 };
 
-SessionLayout session_layout(const mv_model_dims& d, int s_max, int topk) {
+SessionLayout session_layout(const mv_model_dims& d, int s_max, int topk, int dtype = MV_DTYPE_BF16) {
   SessionLayout L{};
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -285,6 +299,18 @@ SessionLayout session_layout(const mv_model_dims& d, int s_max, int topk) {
   L.state = take(512 + (size_t)MV_MAX_BATCH * d.n_medusa * topk * 4);
   L.tree_tokens = take(kTok * 4);
   L.cart = take((size_t)kTok * (MV_MAX_DEPTH + 1) * 4);
+  if (dtype == MV_DTYPE_F32) {  // fp32 path: every activation in fp32 (xb holds xn, q holds q and qkv)
+    L.x = take((size_t)kTok * d.d * 4);
+    L.xb = take((size_t)kTok * d.d * 4);
+    L.q = take((size_t)kTok * (4 * HD) * 4);
+    L.attn = take((size_t)kTok * HD * 4);
+    L.act = take((size_t)kTok * d.ffn * 4);
+    L.logits = take((size_t)kTok * ldl * 4);
+    L.post = take(posterior_ws_bytes(kTok));
+    L.heads = take(f32_heads_ws_bytes(d.d, d.n_medusa, d.vocab));
+    L.total = o;
+    return L;
+  }
   L.x = take((size_t)kTok * d.d * 4);
   L.xb = take((size_t)kTok * d.d * 2);
   L.ssq = take((size_t)((d.d + 127) / 128) * kTok * 4);
@@ -322,11 +348,48 @@ GemmParams base_params(const mv_session* s, int n_tok) {
   return p;
 }
 
+// The fp32 model's backbone pass over n tokens of the session's one sequence (see forward below): plain FFMA
+// kernels, every intermediate in fp32.
+mv_status forward_f32(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int n, bool lm, cudaStream_t st) {
+  const mv_model* m = s->model;
+  const mv_model_dims& d = m->dims;
+  const int H = d.n_heads, D = d.head_dim, HD = H * D;
+  const float scale = 1.0f / sqrtf((float)D);
+  float* kvf = reinterpret_cast<float*>(s->kv);
+  ProfScope ps(s, st, MV_PROF_OTHER);
+  mv_status rc = launch_f32_embed(d_tokens, n, m->f_embed, d.vocab, d.d, s->x, st);
+  for (int l = 0; l < d.n_layers && rc == MV_OK; ++l) {
+    float* kvl = kvf + (size_t)l * 2 * H * s->s_max * D;
+    if ((rc = launch_f32_rmsnorm(s->x, n, d.d, d.norm_eps, s->xn, st)) != MV_OK) break;
+    if ((rc = launch_f32_linear(s->xn, d.d, m->f_wqkv[l], nullptr, 3 * HD, d.d, n, s->qkv_f, 3 * HD, 0, st)) != MV_OK)
+      break;
+    if ((rc = launch_f32_rope_append(s->qkv_f, n, H, D, s->s_max, s->cur_len, t->d_position_ids, d.rope_theta,
+                                     s->q_f, kvl, st)) != MV_OK)
+      break;
+    if ((rc = launch_f32_tree_attention(s->q_f, kvl, H, D, s->s_max, n, s->cur_len, t->d_ancestors, scale,
+                                        s->attn_f, st)) != MV_OK)
+      break;
+    if ((rc = launch_f32_linear(s->attn_f, HD, m->f_wo[l], nullptr, d.d, HD, n, s->x, d.d, 1, st)) != MV_OK) break;
+    if ((rc = launch_f32_rmsnorm(s->x, n, d.d, d.norm_eps, s->xn, st)) != MV_OK) break;
+    if ((rc = launch_f32_linear(s->xn, d.d, m->f_gate[l], m->f_up[l], d.ffn, d.d, n, s->act_f, d.ffn, 2, st)) !=
+        MV_OK)
+      break;
+    rc = launch_f32_linear(s->act_f, d.ffn, m->f_down[l], nullptr, d.d, d.ffn, n, s->x, d.d, 1, st);
+  }
+  if (rc == MV_OK && lm) {
+    rc = launch_f32_rmsnorm(s->x, n, d.d, d.norm_eps, s->xn, st);
+    if (rc == MV_OK)
+      rc = launch_f32_linear(s->xn, d.d, m->f_lm, nullptr, d.vocab, d.d, n, s->logits, s->ld_logits, 0, st);
+  }
+  return rc;
+}
+
 // One backbone pass over the n tokens (tree nodes or a prefill chunk) of nseq sequences b0 .. b0 + nseq - 1,
 // whose ids are at d_tokens (sequence b's at row 64 (b - b0) when nseq > 1). `t` gives the attention mask
 // (ancestor words) and positions (depth); each prefix length is read from s->cur_len[b].
 mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int n, bool lm, cudaStream_t st,
                   int nseq = 1, int b0 = 0) {
+  if (s->model->dtype == MV_DTYPE_F32) return forward_f32(s, t, d_tokens, n, lm, st);
   const mv_model* m = s->model;
   const mv_model_dims& d = m->dims;
   const int HD = d.n_heads * d.head_dim;
@@ -473,6 +536,10 @@ mv_status run_heads(mv_session* s, int b, int row0, cudaStream_t st) {
   ProfScope ps(s, st, MV_PROF_HEADS);
   const mv_model* m = s->model;
   const mv_model_dims& d = m->dims;
+  if (m->dtype == MV_DTYPE_F32)
+    return launch_f32_heads(s->x, kTok, s->result + b, d.norm_eps, d.d, d.n_medusa, m->f_w1, m->f_w2, d.vocab,
+                            s->topk, s->head_topk + (size_t)b * d.n_medusa * s->topk, s->cur_len + b, s->ws_heads,
+                            st);
   return launch_heads(nullptr, s->x + (size_t)row0 * d.d, s->result + b, d.norm_eps, 1, d.d, d.n_medusa, m->w1,
                       m->w2, d.vocab, s->topk, nullptr, s->head_topk + (size_t)b * d.n_medusa * s->topk, nullptr,
                       nullptr, s->cur_len + b, s->ws_heads, st);
@@ -528,15 +595,180 @@ extern "C" mv_status mv_model_create(const mv_model_dims* dims, const mv_model_w
   return MV_OK;
 }
 
-extern "C" void mv_model_destroy(mv_model* m) { delete m; }
-
-extern "C" mv_status mv_session_workspace(const mv_model* m, int32_t s_max, int32_t topk, size_t* bytes) {
-  if (!m || !bytes || s_max < 1 || topk < 1 || topk > 16) return MV_ERR_INVALID_ARG;
-  *bytes = session_layout(m->dims, s_max, topk).total;
+extern "C" mv_status mv_model_create_f32(const mv_model_dims* dims, const mv_model_weights_f32* w, mv_model** out) {
+  if (!dims || !w || !out) return MV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!dims_ok(*dims)) return MV_ERR_SHAPE;
+  const mv_model_dims& d = *dims;
+  if (!w->embed || !w->lm_head || !w->medusa_w1 || !w->medusa_w2 || !w->wqkv || !w->wo || !w->w_gate ||
+      !w->w_up || !w->w_down)
+    return MV_ERR_INVALID_ARG;
+  mv_model* m = new mv_model();
+  m->dims = d;
+  m->dtype = MV_DTYPE_F32;
+  m->packed = 0;
+  m->embed = m->lm_head = m->w1 = m->w2 = nullptr;
+  m->f_embed = w->embed;
+  m->f_lm = w->lm_head;
+  m->f_w1 = w->medusa_w1;
+  m->f_w2 = w->medusa_w2;
+  for (int l = 0; l < d.n_layers; ++l) {
+    const float* ptrs[5] = {w->wqkv[l], w->wo[l], w->w_gate[l], w->w_up[l], w->w_down[l]};
+    for (const float* p : ptrs)
+      if (!p) {
+        delete m;
+        return MV_ERR_INVALID_ARG;
+      }
+    m->f_wqkv.push_back(w->wqkv[l]);
+    m->f_wo.push_back(w->wo[l]);
+    m->f_gate.push_back(w->w_gate[l]);
+    m->f_up.push_back(w->w_up[l]);
+    m->f_down.push_back(w->w_down[l]);
+  }
+  *out = m;
   return MV_OK;
 }
 
-extern "C" mv_status mv_batch_session_create(mv_model* m, const mv_tree* tree, int32_t batch, mv_bf16* kv,
+extern "C" mv_status mv_model_create_random(const mv_model_dims* dims, uint64_t seed, double std, int32_t dtype,
+                                            mv_model** out) {
+  if (!dims || !out || (dtype != MV_DTYPE_BF16 && dtype != MV_DTYPE_F32) || !(std >= 0.0)) return MV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!dims_ok(*dims)) return MV_ERR_SHAPE;
+  const mv_model_dims& d = *dims;
+  const int64_t qd = (int64_t)d.n_heads * d.head_dim, L = d.n_layers, K = d.n_medusa;
+  const bool bf = dtype == MV_DTYPE_BF16;
+  const size_t esz = bf ? 2 : 4;
+  // One tensor of the model: [M][Kc] drawn from the named streams of its row segments; the projections of a bf16
+  // model in the packed layout (tile_rows), everything else row-major.
+  struct T {
+    std::vector<std::string> names;
+    int64_t M, Kc, seg;
+    int tile_rows;
+    size_t off, bytes;
+  };
+  std::vector<T> ts;
+  auto add = [&](std::vector<std::string> names, int64_t M, int64_t Kc, int64_t seg, int tr) {
+    T t{std::move(names), M, Kc, seg, bf ? tr : 0, 0, 0};
+    size_t n = (size_t)M * Kc;
+    if (t.tile_rows) {
+      size_t b = 0;
+      mv_packed_weight_bytes((int32_t)M, (int32_t)Kc, t.tile_rows, &b);
+      n = b / 2;
+    }
+    t.bytes = (n * esz + 255) & ~size_t(255);
+    ts.push_back(std::move(t));
+  };
+  add({"embed"}, d.vocab, d.d, d.vocab, 0);
+  for (int l = 0; l < L; ++l) {
+    const std::string p = "layer" + std::to_string(l) + ".";
+    add({p + "wq", p + "wk", p + "wv"}, 3 * qd, d.d, qd, 128);
+    add({p + "wo"}, d.d, qd, d.d, 128);
+    add({p + "w_gate"}, d.ffn, d.d, d.ffn, 64);
+    add({p + "w_up"}, d.ffn, d.d, d.ffn, 64);
+    add({p + "w_down"}, d.d, d.ffn, d.d, 128);
+  }
+  add({"lm_head"}, d.vocab, d.d, d.vocab, 128);
+  std::vector<std::string> w1n, w2n;
+  for (int k = 0; k < K; ++k) {
+    w1n.push_back("medusa" + std::to_string(k) + ".w1");
+    w2n.push_back("medusa" + std::to_string(k) + ".w2");
+  }
+  add(w1n, K * d.d, d.d, d.d, 0);
+  add(w2n, K * d.vocab, d.d, d.vocab, 0);
+  size_t total = 0;
+  for (T& t : ts) {
+    t.off = total;
+    total += t.bytes;
+  }
+  char* base = nullptr;
+  if (cudaMalloc(&base, total) != cudaSuccess) {
+    cudaGetLastError();
+    return MV_ERR_CAPACITY;
+  }
+  mv_status rc = MV_OK;
+  for (const T& t : ts) {
+    std::vector<uint64_t> keys;
+    for (const std::string& nm : t.names) keys.push_back(mv_stream_key(seed, nm.c_str()));
+    rc = launch_gen_normal(base + t.off, dtype, t.M, t.Kc, t.tile_rows, keys.data(), (int)keys.size(), t.seg, std,
+                           nullptr);
+    if (rc != MV_OK) break;
+  }
+  if (rc == MV_OK && cudaDeviceSynchronize() != cudaSuccess) rc = MV_ERR_CUDA;
+  if (rc != MV_OK) {
+    cudaFree(base);
+    return rc;
+  }
+  size_t i = 0;
+  auto next = [&]() { return base + ts[i++].off; };
+  mv_model* m = nullptr;
+  if (bf) {
+    std::vector<const mv_bf16*> qkv(L), o(L), g(L), u(L), dn(L);
+    const mv_bf16* emb = reinterpret_cast<const mv_bf16*>(next());
+    for (int l = 0; l < L; ++l) {
+      qkv[l] = reinterpret_cast<const mv_bf16*>(next());
+      o[l] = reinterpret_cast<const mv_bf16*>(next());
+      g[l] = reinterpret_cast<const mv_bf16*>(next());
+      u[l] = reinterpret_cast<const mv_bf16*>(next());
+      dn[l] = reinterpret_cast<const mv_bf16*>(next());
+    }
+    mv_model_weights w{};
+    w.embed = emb;
+    w.wqkv = qkv.data();
+    w.wo = o.data();
+    w.w_gate = g.data();
+    w.w_up = u.data();
+    w.w_down = dn.data();
+    w.lm_head = reinterpret_cast<const mv_bf16*>(next());
+    w.medusa_w1 = reinterpret_cast<const mv_bf16*>(next());
+    w.medusa_w2 = reinterpret_cast<const mv_bf16*>(next());
+    w.packed = 1;
+    rc = mv_model_create(dims, &w, &m);
+  } else {
+    std::vector<const float*> qkv(L), o(L), g(L), u(L), dn(L);
+    const float* emb = reinterpret_cast<const float*>(next());
+    for (int l = 0; l < L; ++l) {
+      qkv[l] = reinterpret_cast<const float*>(next());
+      o[l] = reinterpret_cast<const float*>(next());
+      g[l] = reinterpret_cast<const float*>(next());
+      u[l] = reinterpret_cast<const float*>(next());
+      dn[l] = reinterpret_cast<const float*>(next());
+    }
+    mv_model_weights_f32 w{};
+    w.embed = emb;
+    w.wqkv = qkv.data();
+    w.wo = o.data();
+    w.w_gate = g.data();
+    w.w_up = u.data();
+    w.w_down = dn.data();
+    w.lm_head = reinterpret_cast<const float*>(next());
+    w.medusa_w1 = reinterpret_cast<const float*>(next());
+    w.medusa_w2 = reinterpret_cast<const float*>(next());
+    rc = mv_model_create_f32(dims, &w, &m);
+  }
+  if (rc != MV_OK) {
+    cudaFree(base);
+    return rc;
+  }
+  m->owned = base;
+  *out = m;
+  return MV_OK;
+}
+
+extern "C" int32_t mv_model_dtype(const mv_model* m) { return m ? m->dtype : -1; }
+
+extern "C" void mv_model_destroy(mv_model* m) {
+  if (!m) return;
+  if (m->owned) cudaFree(m->owned);
+  delete m;
+}
+
+extern "C" mv_status mv_session_workspace(const mv_model* m, int32_t s_max, int32_t topk, size_t* bytes) {
+  if (!m || !bytes || s_max < 1 || topk < 1 || topk > 16) return MV_ERR_INVALID_ARG;
+  *bytes = session_layout(m->dims, s_max, topk, m->dtype).total;
+  return MV_OK;
+}
+
+extern "C" mv_status mv_batch_session_create(mv_model* m, const mv_tree* tree, int32_t batch, void* kv,
                                              int32_t s_max, int32_t topk, void* ws, size_t ws_bytes,
                                              mv_session** out) {
   if (!m || !tree || !kv || !ws || !out || batch < 1 || batch > MV_MAX_BATCH) return MV_ERR_INVALID_ARG;
@@ -545,14 +777,16 @@ extern "C" mv_status mv_batch_session_create(mv_model* m, const mv_tree* tree, i
   const mv_model_dims& d = m->dims;
   if (topk < tree->topk || topk > 16 || tree->depth > d.n_medusa || tree->n_nodes > kTok) return MV_ERR_SHAPE;
   if (batch > 1 && tree->n_nodes > kSeqRows) return MV_ERR_SHAPE;  // one token group per sequence
+  if (batch > 1 && m->dtype != MV_DTYPE_BF16) return MV_ERR_UNSUPPORTED;  // the fp32 path runs one sequence
+  if (m->dtype == MV_DTYPE_F32 && d.head_dim > 128) return MV_ERR_SHAPE;
   if (s_max < kChunk + 1) return MV_ERR_CAPACITY;
-  const SessionLayout L = session_layout(d, s_max, topk);
+  const SessionLayout L = session_layout(d, s_max, topk, m->dtype);
   if (ws_bytes < L.total) return MV_ERR_CAPACITY;
   if ((reinterpret_cast<uintptr_t>(ws) | reinterpret_cast<uintptr_t>(kv)) & 255) return MV_ERR_INVALID_ARG;
   mv_session* s = new mv_session();
   s->model = m;
   s->tree = tree;
-  s->kv = kv;
+  s->kv = static_cast<uint16_t*>(kv);
   s->s_max = s_max;
   s->topk = topk;
   s->batch = batch;
@@ -583,11 +817,28 @@ extern "C" mv_status mv_batch_session_create(mv_model* m, const mv_tree* tree, i
   s->row_max = reinterpret_cast<float2*>(b + L.row_max);
   s->h_pair = reinterpret_cast<uint16_t*>(b + L.h_pair);
   const int HD = d.n_heads * d.head_dim;
-  bool ok = gemm_act_map(&s->m_xb, s->xb, kTok, d.d) && gemm_act_map(&s->m_attn, s->attn, kTok, HD) &&
-            gemm_act_map(&s->m_act, s->act, kTok, d.ffn);
-  CUtensorMap vdummy;
-  ok = ok && tree_attn_make_maps(&s->m_kv, &vdummy, kv, kv, d.n_heads, d.head_dim, s_max, 2 * d.n_layers * batch,
-                                 (size_t)d.n_heads * s_max * d.head_dim * 2);
+  bool ok = true;
+  if (m->dtype == MV_DTYPE_F32) {  // fp32 buffers over the same regions (see session_layout)
+    s->xn = reinterpret_cast<float*>(b + L.xb);
+    s->qkv_f = reinterpret_cast<float*>(b + L.q);
+    s->q_f = s->qkv_f + (size_t)kTok * 3 * HD;
+    s->attn_f = reinterpret_cast<float*>(b + L.attn);
+    s->act_f = reinterpret_cast<float*>(b + L.act);
+    s->xb = nullptr;
+    s->ssq = nullptr;
+    s->q = s->attn = s->act = nullptr;
+    s->chain_flags = nullptr;
+    s->row_max = nullptr;
+    s->h_pair = nullptr;
+    s->ws_attn = nullptr;
+    s->fuse_attention = false;
+  } else {
+    ok = gemm_act_map(&s->m_xb, s->xb, kTok, d.d) && gemm_act_map(&s->m_attn, s->attn, kTok, HD) &&
+         gemm_act_map(&s->m_act, s->act, kTok, d.ffn);
+    CUtensorMap vdummy;
+    ok = ok && tree_attn_make_maps(&s->m_kv, &vdummy, kv, kv, d.n_heads, d.head_dim, s_max,
+                                   2 * d.n_layers * batch, (size_t)d.n_heads * s_max * d.head_dim * 2);
+  }
   // 64-node chain (causal) tree for prefill chunks
   s->chain = nullptr;
   if (ok) {
@@ -623,7 +874,7 @@ extern "C" mv_status mv_batch_session_create(mv_model* m, const mv_tree* tree, i
   return MV_OK;
 }
 
-extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, mv_bf16* kv, int32_t s_max, int32_t topk,
+extern "C" mv_status mv_session_create(mv_model* m, const mv_tree* tree, void* kv, int32_t s_max, int32_t topk,
                                        void* ws, size_t ws_bytes, mv_session** out) {
   return mv_batch_session_create(m, tree, 1, kv, s_max, topk, ws, ws_bytes, out);
 }
@@ -726,8 +977,11 @@ extern "C" mv_status medusa_verify_step(mv_session* s, mv_accept_params prm, mv_
     const float* lg = s->logits + (size_t)row0(b) * s->ld_logits;
     {
       ProfScope ps(s, st, MV_PROF_POSTERIOR);
+      // the bf16 path's LM-head projection leaves per-tile max / argmax (greedy then reads no logits row); the
+      // fp32 path's posterior reads the rows
       rc = launch_posterior(lg, d.vocab, s->ld_logits, s->tree_tokens + row0(b), t, prm, s->result + b, nullptr,
-                            nullptr, s->ws_post, st, s->row_max + row0(b), (d.vocab + 127) / 128, kTok);
+                            nullptr, s->ws_post, st, s->row_max ? s->row_max + row0(b) : nullptr,
+                            s->row_max ? (d.vocab + 127) / 128 : 0, kTok);
     }
     if (rc == MV_OK && s->root.mode != MV_ROOT_ARGMAX) {  // the next root drawn from node retrieve[best][acc]
       ProfScope ps(s, st, MV_PROF_OTHER);
@@ -736,8 +990,10 @@ extern "C" mv_status medusa_verify_step(mv_session* s, mv_accept_params prm, mv_
     }
     if (rc == MV_OK) {
       ProfScope ps(s, st, MV_PROF_KV_COMPACT);
-      rc = launch_kv_compact(s->kv + (size_t)b * s->kv_seq_elems, d.n_layers, d.n_heads, s->s_max, d.head_dim,
-                             s->cur_len + b, 0, s->result + b, nullptr, st);
+      // an fp32 row of head_dim values moves as 2 head_dim bf16-sized halves: the compaction is a bit copy
+      const int e = s->model->dtype == MV_DTYPE_F32 ? 2 : 1;
+      rc = launch_kv_compact(s->kv + (size_t)b * s->kv_seq_elems * e, d.n_layers, d.n_heads, s->s_max,
+                             d.head_dim * e, s->cur_len + b, 0, s->result + b, nullptr, st);
     }
   }
   if (rc != MV_OK) return rc;

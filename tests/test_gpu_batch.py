@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import decision_check
 import medusa_tree_speculative_verify_gb300 as mv
 import synth
 from oracle.decode import ar_greedy_decode, prefill as o_prefill, teacher_forced_logits, verify_step as o_verify_step
@@ -95,8 +96,11 @@ def test_batched_typical_steps_match_oracle():
         for b in list(live):
             toks, info = o_verify_step(om, states[b], ot, TYPICAL, 0.7, 0.09, 0.3)
             res, post = sess.read_result(b), info["post"]
-            if res["nodes"] != post["nodes"].tolist():
-                assert any(m < MARGIN for (_, _, m) in post["margins"])
+            n = ot["n_nodes"]
+            acc = decision_check.decisions_from_logits(sess.logits[64 * b: 64 * b + n].cpu().numpy(),
+                                                       sess.tree_tokens[64 * b: 64 * b + n].cpu().numpy(),
+                                                       TYPICAL, 0.7, 0.09, 0.3)
+            if decision_check.check(res, acc, post, ot["retrieve"], TYPICAL):
                 live.remove(b)  # this stream legitimately diverges after a near-threshold decision
                 continue
             assert res["tokens"] == toks.tolist()

@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import decision_check
 import medusa_tree_speculative_verify_gb300 as mv
 import synth
 from oracle.decode import generate_candidates
@@ -84,21 +85,6 @@ def test_build_candidates_bit_exact(name):
 
 # --------------------------------------------------------------------------------------------- posterior
 
-def _decisions_match(res, ref, mode):
-    """GPU result equals the oracle's, unless the oracle had a decision within MARGIN of its threshold."""
-    same = (res["best"] == ref["best"] and res["acc"] == ref["acc"] and res["nodes"] == ref["nodes"].tolist())
-    if same:
-        return True
-    if any(m < MARGIN for (_, _, m) in ref["margins"]):
-        return True
-    if mode == TYPICAL and res["acc"] == ref["acc"]:
-        # equal accept lengths: the best row is chosen by likelihood; allow a near tie
-        rows = np.flatnonzero(ref["accept_len"] == ref["acc"])
-        like = np.sort(ref["likelihood"][rows])[::-1]
-        return len(like) > 1 and like[0] - like[1] < MARGIN
-    return False
-
-
 def _run_posterior(logits, tokens, t, mode, T=0.7, eps=0.09, delta=0.3):
     n, V = logits.shape
     out = torch.zeros(mv.RESULT_INTS, dtype=torch.int32, device="cuda")
@@ -107,6 +93,12 @@ def _run_posterior(logits, tokens, t, mode, T=0.7, eps=0.09, delta=0.3):
     mv.evaluate_posterior(logits, tokens, t, mv.AcceptParams(mode, T, eps, delta), out,
                           ws(mv.evaluate_posterior_workspace(n)), stats, amax)
     return mv.result_dict(out), stats.cpu().numpy(), amax.cpu().numpy()
+
+
+def _check_decisions(res, stats, amax, z, tokens, ref, retrieve, mode, T):
+    """Each row's first decision that differs from the oracle's must have an oracle margin below MARGIN."""
+    acc = decision_check.decisions_from_stats(z, tokens, mode, amax, stats, T)
+    return decision_check.check(res, acc, ref, retrieve, mode)
 
 
 @pytest.mark.parametrize("tree", ["synthetic64", "page63", "synthetic256"])
@@ -122,8 +114,8 @@ def test_posterior_planted_full_size(mode, seed, tree):
     tokens, logits = synth.planted_tokens_and_logits(seed, o["n_nodes"], 32000, path, L)
     res, stats, amax = _run_posterior(logits.cuda(), i32(tokens.numpy()), t, mode)
     ref = oracle_posterior(logits.numpy(), tokens.numpy(), r, mode, 0.7, 0.09, 0.3)
-    assert _decisions_match(res, ref, mode)
-    assert res["acc"] >= L or any(m < MARGIN for (_, _, m) in ref["margins"])
+    dv = _check_decisions(res, stats, amax, logits.numpy(), tokens.numpy(), ref, r, mode, 0.7)
+    assert res["acc"] >= L or dv
     assert res["tokens"] == tokens.numpy()[res["nodes"]].tolist()
     assert res["n_tokens"] == res["acc"] + 1
     assert res["next_node"] == res["nodes"][-1]
@@ -153,9 +145,9 @@ def test_posterior_small_ragged(mode, V):
     ld = (V + 3) // 4 * 4                        # rows padded to a multiple of 4 floats (API contract)
     zp = torch.full((9, ld), float("nan"), dtype=torch.float32)
     zp[:, :V] = torch.tensor(z)
-    res, _, _ = _run_posterior(zp.cuda()[:, :V], i32(tokens), t, mode, T=1.0)
+    res, stats, amax = _run_posterior(zp.cuda()[:, :V], i32(tokens), t, mode, T=1.0)
     ref = oracle_posterior(z, tokens, o["retrieve"], mode, 1.0)
-    assert _decisions_match(res, ref, mode)
+    _check_decisions(res, stats, amax, z, tokens, ref, o["retrieve"], mode, 1.0)
 
 
 def test_posterior_rejects_unaligned_rows():

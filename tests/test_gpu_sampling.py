@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import decision_check
 import medusa_tree_speculative_verify_gb300 as mv
 import synth
 from oracle.decode import chain_mask, prefill as o_prefill, verify_step as o_verify_step
@@ -212,9 +213,10 @@ def test_sampled_decode_matches_oracle():
         sess.step(mv.AcceptParams(TYPICAL, 0.7, 0.09, 0.3))
         toks, info = o_verify_step(om, st, ot, TYPICAL, 0.7, 0.09, 0.3, root=rs)
         res, post = sess.read_result(), info["post"]
-        if res["nodes"] != post["nodes"].tolist():
-            assert any(m < 2e-2 for (_, _, m) in post["margins"])
-            return
+        acc = decision_check.decisions_from_logits(sess.logits[: tree.n_nodes].cpu().numpy(),
+                                                   sess.tree_tokens.cpu().numpy(), TYPICAL, 0.7, 0.09, 0.3)
+        if decision_check.check(res, acc, post, ot["retrieve"], TYPICAL):
+            return  # a near-threshold decision: the streams legitimately diverge from here
         assert res["tokens"] == toks.tolist()
         if res["next_root"] != st.root:
             c, u, _ = rs.draws[-1]

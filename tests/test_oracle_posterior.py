@@ -109,3 +109,39 @@ def test_kv_compact_overlapping_rows():
     assert (out[:, :10] == cache[:, :10]).all() and (out[:, 14:] == cache[:, 14:]).all()
     out, L = kv_compact(cache, 10, [0])                       # nothing accepted: length + 1
     assert L == 11 and (out == cache).all()
+
+
+def test_margins_by_hand():
+    # The margin of each decision ("大模型推理 memory bandwidth bound (5) - Medusa", 二.6 evaluate_posterior()):
+    # greedy top-1 - top-2 when the candidate is the argmax (accepted), top-1 - its logit when it is not; typical
+    # |ln p(candidate) - ln tau|. Every decision up to a row's first rejection is listed, and none after it.
+    t = tree_buffers([(0,), (1,)], 10)                   # retrieve rows [0, 2] and [0, 1]
+    # an exact tie at the top: tokens 3 and 5 share the largest logit; the argmax is the lower id (3)
+    z = np.zeros((3, 8))
+    z[0, [3, 5]] = 1.0
+    r = evaluate_posterior(z, np.array([0, 3, 5]), t["retrieve"], GREEDY)
+    m = {(p, j): v for (p, j, v) in r["margins"]}
+    assert m == {(0, 0): 0.0, (1, 0): 0.0}
+    assert r["accept_len"].tolist() == [0, 1] and r["nodes"].tolist() == [0, 1]
+    # the row [2, 1, 0, -1]: candidate token 0 accepted with margin 2 - 1; candidate token 2 rejected, 2 - 0
+    z = np.full((3, 4), -5.0)
+    z[0] = [2.0, 1.0, 0.0, -1.0]
+    r = evaluate_posterior(z, np.array([9, 0, 2]) % 4, t["retrieve"], GREEDY)
+    m = {(p, j): v for (p, j, v) in r["margins"]}
+    assert m == {(0, 0): 2.0, (1, 0): 1.0}
+    # typical at T = 1 on the same row: p = [.643914, .236883, .087144, .032059], tau = eps = .09;
+    # token 2 is rejected by ln(.09 / .087144) = .032244, token 1 accepted by ln(.236883 / .09) = .967756
+    r = evaluate_posterior(z, np.array([0, 1, 2]), t["retrieve"], TYPICAL, 1.0, 0.09, 0.3)
+    m = {(p, j): v for (p, j, v) in r["margins"]}
+    assert abs(m[(0, 0)] - 0.032244) < 1e-6 and abs(m[(1, 0)] - 0.967756) < 1e-6
+    assert r["accept_len"].tolist() == [0, 1]
+    # a rejection ends the row: with the depth-1 candidate of row [0, 1, 3] rejected, its depth-2 decision is
+    # never made (no margin listed for it); the other row is accepted at depth 1 and ends there
+    t = tree_buffers([(0,), (1,), (0, 0)], 10)          # rows [0, 1, 3] and [0, 2, -1]
+    z = np.zeros((4, 8))
+    z[0, 6] = 3.0                                       # root predicts token 6 = node 2
+    z[1, 7] = 3.0
+    r = evaluate_posterior(z, np.array([0, 5, 6, 7]), t["retrieve"], GREEDY)
+    assert sorted((p, j) for (p, j, _) in r["margins"]) == [(0, 0), (1, 0)]
+    m = {(p, j): v for (p, j, v) in r["margins"]}
+    assert m[(0, 0)] == 3.0 and m[(1, 0)] == 3.0        # rejected: 3 - z[5] = 3; accepted: 3 - 0 = 3

@@ -55,3 +55,16 @@ def test_noalloc_posterior_matches_workspace_posterior_twice():
         assert np.array_equal(got[2], ref[2])
         assert np.allclose(got[1], ref[1], rtol=RTOL, atol=ATOL)
         assert got[0]["acc"] >= 1            # the planted path is accepted
+
+
+def test_noalloc_posterior_rejects_trees_past_its_limit():
+    """A tree of more nodes than the fixed array holds is refused before anything is launched."""
+    big = mv.Tree(synth.synthetic_tree_choices(65, 4, 10), 10)
+    assert big.n_nodes == 65 > mv.NOALLOC_MAX_NODES
+    logits, tokens = _case(0, big)
+    out = torch.full((mv.RESULT_INTS,), -5, dtype=torch.int32, device="cuda")
+    with pytest.raises(mv.MVError) as e:
+        mv.evaluate_posterior_noalloc(logits, tokens, big, mv.AcceptParams(mv.GREEDY), out)
+    assert e.value.status == 4  # MV_ERR_CAPACITY
+    torch.cuda.synchronize()
+    assert (out == -5).all()    # nothing ran
