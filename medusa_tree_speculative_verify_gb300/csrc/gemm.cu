@@ -42,7 +42,11 @@ constexpr int kMaxGroups = 4;              // token groups per launch: up to 256
 constexpr int kTokMax = BN * kMaxGroups;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kBBytes = BN * BK * 2;  // 8 KB per token group
-constexpr int kEpiThreads = 128;
+// Epilogue: 8 warps, two per TMEM sub-partition (warp w reads lanes 32 (w % 4) ..); the two halves of a pair drain
+// the two halves of a token group's columns and finish alternate tokens of the CTA's share, so a tile's epilogue --
+// the step every phase boundary waits for -- takes half as long as with one warp per sub-partition.
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kAcc = 2;  // accumulator buffers in tensor memory (the MMA may run kAcc - 1 tiles ahead)
 constexpr int kMaxCluster = 8;  // CTAs per cluster (portable limit)
@@ -50,14 +54,21 @@ constexpr int kMaxCluster = 8;  // CTAs per cluster (portable limit)
 // Per number of token groups NT (1 to 4): a stage holds one weight block and NT activation blocks, so fewer
 // stages fit; one MMA of N = 64 NT per 16 k; the accumulator buffers take 2 x 64 NT TMEM columns (allocated as
 // a power of two).
+//
+// A pipeline stage holds kKps consecutive k-blocks: their weight blocks, then their activation blocks. Two k-blocks
+// per stage (32 KB of weights) stream faster than one (16 KB) with the same bytes in flight -- measured on GB300
+// with a plain TMA ring of weight + activation stages: 41.8 GB/s per SM at 16 + 8 KB stages, 50.1 GB/s at 32 + 16
+// KB -- since every stage costs a full / empty handshake on top of its bytes.
 template <int NT, bool kAttn = false>
 struct Cfg {
-  static constexpr int kStages = NT == 1 ? 6 : NT == 2 ? 5 : NT == 3 ? 4 : 3;
+  static constexpr int kKps = NT <= 3 ? 2 : 1;  // k-blocks per stage
+  static constexpr int kStages = NT == 1 ? 3 : NT == 2 ? 2 : NT == 3 ? 2 : 3;
   // after the stages: the cluster partial buffer, which a fused attention head uses first (kAttn)
   static constexpr size_t kPartBytes = (size_t)BM * BN * 4;
   static constexpr size_t kRegionBytes =
       kAttn && attn::smem_bytes<128>() > kPartBytes ? attn::smem_bytes<128>() : kPartBytes;
-  static constexpr int kStageBytes = kABytes + NT * kBBytes;
+  static constexpr int kStageBytes = kKps * (kABytes + NT * kBBytes);
+  static constexpr int kBOff = kKps * kABytes;  // the activation blocks of a stage start after its weight blocks
   static constexpr int kTmemCols = kAcc * BN * NT;
   static constexpr int kTmemAlloc = kTmemCols <= 128 ? 128 : kTmemCols <= 256 ? 256 : 512;
   static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kRegionBytes + 256;
@@ -104,12 +115,13 @@ MV_DEV void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 MV_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-MV_DEV void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
-// OR of `v` over the 128 epilogue threads (named barrier 1), the same answer in every thread.
+// Named barrier 2 over the epilogue warps (barrier 1 belongs to a fused attention's 128 threads).
+MV_DEV void epi_bar() { asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory"); }
+// OR of `v` over the epilogue threads (named barrier 2), the same answer in every thread.
 MV_DEV bool epi_any(bool v) {
   uint32_t r;
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\t"
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 2, %2, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"((uint32_t)v), "n"(kEpiThreads)
@@ -142,9 +154,10 @@ struct EpiConst {
   int kv_row0[kMaxSeq];  // per sequence; -1: the cache rows would run past S_max (nothing is appended)
 };
 
+// i: epilogue thread 0 .. kEpiThreads - 1 (threads 128 and up only take part in the barriers)
 MV_DEV void load_epi_const(const GemmParams& p, EpiConst* ec, int i, int ngroups) {
-  const int half = i >> 6;  // two threads per token, each summing half of the partials
-  for (int g = 0; g < ngroups; ++g) {
+  const int half = (i >> 6) & 1;  // two threads per token, each summing half of the partials
+  for (int g = 0; g < ngroups && i < 128; ++g) {
     const int j = g * BN + (i & (BN - 1));
     float t = 0.0f;
     if (p.ssq) {
@@ -178,7 +191,7 @@ MV_DEV void load_epi_const(const GemmParams& p, EpiConst* ec, int i, int ngroups
     ec->kv_row0[i] = r0;
   }
   epi_bar();
-  for (int g = 0; g < ngroups; ++g) {
+  for (int g = 0; g < ngroups && i < 128; ++g) {
     const int j = g * BN + (i & (BN - 1));
     if (half == 0)
       ec->scale[j] = p.ssq ? rsqrtf((ec->part[0][j] + ec->part[1][j]) / (float)p.norm_d + p.eps) : 1.0f;
@@ -410,6 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                                                            const __grid_constant__ ChainArgs ca) {
   constexpr int kStages = Cfg<NT>::kStages;
   constexpr int kStageBytes = Cfg<NT>::kStageBytes;
+  constexpr int kKps = Cfg<NT>::kKps;
+  constexpr int kBOff = Cfg<NT>::kBOff;
   constexpr int kTmemAlloc = Cfg<NT>::kTmemAlloc;
   constexpr uint32_t kIdesc = Cfg<NT>::kIdesc;
   extern __shared__ uint8_t smem_raw[];
@@ -441,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     for (int b = 0; b < kAcc; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], kEpiWarps);
     }
     mbar_init(&pfull, C);  // one arrive from every CTA of the cluster: all partials of the tile written
     mbar_init(&pfree, C);  // one arrive from every CTA of the cluster: all reads of this CTA's partial done
@@ -484,13 +499,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         // The weights do not depend on anything: their loads run ahead. The activations are the previous
         // kernel's output (phase 0: wait for that grid) or the previous phase's (wait for its counter).
         bool waited = false;
-        int pend_s[kStages], pend_kb[kStages];
+        int pend_s[kStages], pend_kb[kStages], pend_n[kStages];
         int pend = 0;
-        auto issue_b = [&](int stage, int kb) {  // the activation blocks of the NT token groups
+        auto issue_b = [&](int stage, int kb, int nk) {  // the activation blocks of the NT token groups, nk k-blocks
+          for (int u = 0; u < nk; ++u)
 #pragma unroll
-          for (int g = 0; g < NT; ++g)
-            tma_load_2d(stages + (size_t)stage * kStageBytes + kABytes + g * kBBytes, bm, &full[stage], kb * BK,
-                        g * BN);
+            for (int g = 0; g < NT; ++g)
+              tma_load_2d(stages + (size_t)stage * kStageBytes + kBOff + (u * NT + g) * kBBytes, bm, &full[stage],
+                          (kb + u) * BK, g * BN);
         };
         auto release = [&]() -> bool {  // on an expired wait the loads are still issued, so every barrier completes
           bool got = true;
@@ -508,33 +524,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             asm volatile("fence.proxy.async.global;" ::: "memory");
           }
           waited = true;
-          for (int j = 0; j < pend; ++j) issue_b(pend_s[j], pend_kb[j]);
+          for (int j = 0; j < pend; ++j) issue_b(pend_s[j], pend_kb[j], pend_n[j]);
           return got;
         };
         for (int tile = t0; ok && tile < t1; ++tile) {
-          for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          for (int kb = kb0; kb < kb1; kb += kKps, ++it) {
             const int s = it % kStages, r = it / kStages;
+            const int nk = min(kKps, kb1 - kb);  // k-blocks of this stage (the last of a tile may hold fewer)
             if (s_abort || !mbar_wait(&empty[s], (uint32_t)((r & 1) ^ 1))) {
               ok = false;
               break;
             }
             uint8_t* a = stages + (size_t)s * kStageBytes;
-            mbar_arrive_expect_tx(&full[s], kStageBytes);
-            if (p.packed_a) {  // one contiguous block per matrix
-              const int tb = tile * p.kbt + kb;
-              tma_load_3d_hint(a, am0, &full[s], 0, 0, tb, wpol);
-              if (p.paired) tma_load_3d_hint(a + kABytes / 2, am1, &full[s], 0, 0, tb, wpol);
-            } else if (p.paired) {
-              tma_load_2d_hint(a, am0, &full[s], kb * BK, tile * 64, wpol);
-              tma_load_2d_hint(a + kABytes / 2, am1, &full[s], kb * BK, tile * 64, wpol);
-            } else {
-              tma_load_2d_hint(a, am0, &full[s], kb * BK, tile * BM, wpol);
+            mbar_arrive_expect_tx(&full[s], (uint32_t)(nk * (kABytes + NT * kBBytes)));
+            for (int u = 0; u < nk; ++u) {
+              uint8_t* au = a + u * kABytes;
+              if (p.packed_a) {  // one contiguous block per matrix
+                const int tb = tile * p.kbt + kb + u;
+                tma_load_3d_hint(au, am0, &full[s], 0, 0, tb, wpol);
+                if (p.paired) tma_load_3d_hint(au + kABytes / 2, am1, &full[s], 0, 0, tb, wpol);
+              } else if (p.paired) {
+                tma_load_2d_hint(au, am0, &full[s], (kb + u) * BK, tile * 64, wpol);
+                tma_load_2d_hint(au + kABytes / 2, am1, &full[s], (kb + u) * BK, tile * 64, wpol);
+              } else {
+                tma_load_2d_hint(au, am0, &full[s], (kb + u) * BK, tile * BM, wpol);
+              }
             }
             if (waited) {
-              issue_b(s, kb);
+              issue_b(s, kb, nk);
             } else {
               pend_s[pend] = s;
               pend_kb[pend] = kb;
+              pend_n[pend] = nk;
               if (++pend == kStages && !release()) {
                 ok = false;
                 break;
@@ -571,18 +592,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           }
           tc_fence_after();
           const uint32_t dt = tmem_base + (uint32_t)(buf * BN * NT);
-          for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          for (int kb = kb0; kb < kb1; kb += kKps, ++it) {
             const int s = it % kStages, r = it / kStages;
+            const int nk = min(kKps, kb1 - kb);
             if (s_abort || !mbar_wait(&full[s], (uint32_t)(r & 1))) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a = st0 + (uint32_t)(s * kStageBytes), b = a + kABytes;
-            const uint64_t ad = sw128_desc(a), bd = sw128_desc(b);
+            const uint32_t a = st0 + (uint32_t)(s * kStageBytes);
+            for (int u = 0; u < nk; ++u) {
+              const uint64_t ad = sw128_desc(a + (uint32_t)(u * kABytes));
+              const uint64_t bd = sw128_desc(a + (uint32_t)(kBOff + u * NT * kBBytes));
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k)
-              tc_mma(dt, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < BK / 16; ++k)
+                tc_mma(dt, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), kIdesc,
+                       (kb > kb0 || u > 0 || k > 0) ? 1u : 0u);
+            }
             tc_commit(&empty[s]);
           }
           if (!ok) break;
@@ -597,17 +623,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
     }
   } else {
-    // ------------------------------------------------------------------ epilogue (128 threads)
+    // ------------------------------------------------------------------ epilogue (kEpiWarps warps)
     // Pipelined over the tiles: iteration n first sums and finishes tile n-1 (its partials were published a
     // whole tile ago, and this runs while the MMA works on tile n), then drains tile n's accumulator from TMEM
     // into this CTA's partial buffer and signals the cluster. At a phase boundary the last tile of the phase is
     // finished, the phase is published (one count per CTA), and this phase's scales wait for every CTA.
-    const int sub = warp & 3;       // TMEM sub-partition this warp may read
-    const int i = sub * 32 + lane;  // tile row = TMEM lane
-    pdl_wait();                     // the epilogue reads what earlier kernels wrote
+    const int sub = warp & 3;                 // TMEM sub-partition this warp may read
+    const int row = sub * 32 + lane;          // tile row = TMEM lane
+    const int hw = (warp - 2) >> 2;           // which warp of the sub-partition's pair: half of the columns
+    const int i = hw * 128 + row;             // epilogue thread 0 .. kEpiThreads - 1
+    pdl_wait();                               // the epilogue reads what earlier kernels wrote
     if constexpr (kAttn) {
-      if (ca.attn_D) {  // the layer's attention first: cluster q = head q, CTA rank = key split
-        if (q < ca.attn.H) {
+      if (ca.attn_D) {  // the layer's attention first: cluster q = head q, CTA rank = key split (128 threads)
+        if (q < ca.attn.H && hw == 0) {
           EpiClusterSync sy{&aready, &adone, C, i, err};
           uint8_t* region = reinterpret_cast<uint8_t*>(part);  // the partial buffer is not in use yet
           if (ca.attn_D == 128)
@@ -623,8 +651,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     const uint32_t part_s = smem_u32(part) + (uint32_t)(lane * 16);  // + token row
     bool ok = true;
-    int n = 0, m = 0, prev_tile = -1, prev_ph = 0;
-    auto finish = [&](int ph_r, int tile_r, int g_r, int nr) {  // token group g_r of the tile; nr: item number
+    int n = 0, m = 0, prev_tile = -1, prev_ph = 0, published = 0;
+    // token group g_r of the tile; nr: item number; publish_to: phases before it are finished in this CTA once this
+    // item is (they are published right after its stores, ahead of releasing the partial buffers)
+    auto finish = [&](int ph_r, int tile_r, int g_r, int nr, int publish_to) {
       const bool all = mbar_wait_cluster(&pfull, (uint32_t)(nr & 1));
       if (epi_any(!all)) {
         if (i == 0) mv_set_error(err, 11, MV_DEVERR_TIMEOUT);
@@ -634,15 +664,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
       const GemmParams& pr = ca.ph[ph_r];
       const int epi = ca.epi[ph_r];
-      // this CTA's token share t = rank, rank + C, ... in chunks of kChunk tokens per thread (one chunk at
-      // C >= 4), each summed over the C partials of the cluster in rank order (16-byte DSMEM loads); only the
-      // fused epilogue itself depends on the kind
-      for (int u0 = 0; rank + u0 * C < kTokPerThread; u0 += kChunk) {
+      // this CTA's token share t = rank, rank + C, ..., alternate ones to the two warps of a sub-partition
+      // (t0 = rank + hw C, stride 2 C), in chunks of kChunk tokens per thread, each summed over the C partials of
+      // the cluster in rank order (16-byte DSMEM loads); only the fused epilogue itself depends on the kind
+      const int t0 = rank + hw * C, ts = 2 * C;
+      for (int u0 = 0; t0 + u0 * ts < kTokPerThread; u0 += kChunk) {
         float4 acc[kChunk];
 #pragma unroll
         for (int u = 0; u < kChunk; ++u) {
           acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          const int t = rank + (u0 + u) * C;
+          const int t = t0 + (u0 + u) * ts;
           if (t >= kTokPerThread) break;
           const int j = sub + 4 * t;  // token within the group
           if (g_r * BN + j >= pr.n_tok) continue;
@@ -655,24 +686,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           for (int c = 0; c < kMaxCluster; ++c)
             if (c < C) add4(acc[u], part_c[c]);
         }
-        const int r0 = rank + u0 * C;
+        const int r0 = t0 + u0 * ts;
         if (epi == EPI_RESIDUAL)
-          final_epilogue<EPI_RESIDUAL, kChunk>(pr, tile_r, g_r * BN, sub, lane, r0, C, acc, &s_ec);
+          final_epilogue<EPI_RESIDUAL, kChunk>(pr, tile_r, g_r * BN, sub, lane, r0, ts, acc, &s_ec);
         else if (epi == EPI_SWIGLU)
-          final_epilogue<EPI_SWIGLU, kChunk>(pr, tile_r, g_r * BN, sub, lane, r0, C, acc, &s_ec);
+          final_epilogue<EPI_SWIGLU, kChunk>(pr, tile_r, g_r * BN, sub, lane, r0, ts, acc, &s_ec);
         else if (epi == EPI_QKV)
-          final_epilogue<EPI_QKV, kChunk>(pr, tile_r, g_r * BN, sub, lane, r0, C, acc, &s_ec);
+          final_epilogue<EPI_QKV, kChunk>(pr, tile_r, g_r * BN, sub, lane, r0, ts, acc, &s_ec);
         else
-          final_epilogue<EPI_STORE, kChunk>(pr, tile_r, g_r * BN, sub, lane, r0, C, acc, &s_ec);
+          final_epilogue<EPI_STORE, kChunk>(pr, tile_r, g_r * BN, sub, lane, r0, ts, acc, &s_ec);
       }
-      // the partials were consumed above (stores issued from them): release the buffers to their owners, one
-      // release arrive per CTA of the cluster from C lanes at once (each costs a cluster round trip)
+      // the partials were consumed above (stores issued from them): publish the phases this item completes (one
+      // count per CTA and phase; the barrier orders every epilogue thread's stores before it), then release the
+      // buffers to their owners, one release arrive per CTA of the cluster from C lanes at once
       epi_bar();
+      if (publish_to > published) {
+        if (i == 0)
+          for (int k = published; k < publish_to; ++k) count_release(ca.flags + k);
+        published = publish_to;
+      }
       if (i < C) mbar_arrive_remote(map_rank(smem_u32(&pfree), (uint32_t)i));
     };
     // One loop over this CTA's tiles of every phase, so that each tile is finished at a single place in the code.
     const int NP = ca.n_phases;
-    int ph = 0, t0 = 0, t1 = 0, tile = 0, published = 0, ec_ph = -1;
+    int ph = 0, t0 = 0, t1 = 0, tile = 0, ec_ph = -1;
     tile_range(ca.ph[0], t0, t1);
     tile = t0;
     while (true) {
@@ -682,13 +719,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           tile = t0;
         }
       }
+      // every phase before `upto` is finished in this CTA once the previous tile is: publish them, in order
+      const int upto = ca.indep ? 0 : (ph < NP ? ph : NP - 1);
       if (prev_tile >= 0) {
-        finish(prev_ph, prev_tile, NT - 1, m - 1);
+        finish(prev_ph, prev_tile, NT - 1, m - 1, upto);
         prev_tile = -1;
         if (!ok) break;
       }
-      // every phase before `upto` is finished in this CTA: publish them, in order (one count per CTA and phase)
-      const int upto = ca.indep ? 0 : (ph < NP ? ph : NP - 1);
       if (published < upto) {
         epi_bar();  // every output of those phases written by this CTA
         if (i == 0) {
@@ -714,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       bool got = !s_abort && mbar_wait(&tfull[buf], (uint32_t)((n / kAcc) & 1));
       // the partial buffer is free again once every CTA of the cluster has finished item m - 1
       if (got && m >= 1) got = mbar_wait_cluster(&pfree, (uint32_t)((m - 1) & 1));
-      if (epi_any(!got)) {  // uniform over the 4 epilogue warps
+      if (epi_any(!got)) {  // uniform over the epilogue warps
         if (i == 0) mv_set_error(err, 10, MV_DEVERR_TIMEOUT);
         s_abort = 1;
         ok = false;
@@ -725,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       // group g - 1 of this tile is finished before group g is drained into the buffer it frees.
       for (int g = 0; g < NT; ++g) {
         if (g > 0) {
-          finish(ph, tile, g - 1, m - 1);
+          finish(ph, tile, g - 1, m - 1, published);
           if (!ok) break;
           const bool free_ok = mbar_wait_cluster(&pfree, (uint32_t)((m - 1) & 1));
           if (epi_any(!free_ok)) {
@@ -735,10 +772,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             break;
           }
         }
-        float v[BN];
-        const uint32_t ta = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(buf * BN * NT + g * BN);
+        float v[BN / 2];  // this warp's half of the group's columns (tokens 32 hw .. 32 hw + 31)
+        const uint32_t ta =
+            tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(buf * BN * NT + g * BN + hw * (BN / 2));
         tmem_ld32(ta, v);
-        tmem_ld32(ta + 32, v + 32);
         tmem_ld_wait();
         if (g == NT - 1) {  // the whole accumulator buffer is read: the MMA may reuse it
           tc_fence_before();
@@ -747,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
         // this CTA's partial, token-major: part[j][row] (consecutive rows in consecutive lanes)
 #pragma unroll
-        for (int j = 0; j < BN; ++j) part[j * BM + i] = v[j];
+        for (int j = 0; j < BN / 2; ++j) part[(hw * (BN / 2) + j) * BM + row] = v[j];
         epi_bar();  // the CTA's writes are ordered before the cluster-scope release arrives below
         if (i < C) mbar_arrive_remote(map_rank(smem_u32(&pfull), (uint32_t)i));
         ++m;
