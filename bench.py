@@ -440,8 +440,9 @@ MICRO_OTHER = ["heads_b1", "heads_b4", "heads_b16", "attn_p64", "attn_p512", "at
 
 
 def _time_launches(fn, steps, warmup, flush=True):
-    """Median CUDA-event time (ms) of fn() on the current stream, L2 flushed (256 MB write) before each."""
-    buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda") if flush else None
+    """Median CUDA-event time (ms) of fn() on the current stream, L2 flushed before each by READING a 256 MB buffer
+    (a flush by writing would leave dirty lines whose write-back then competes with the timed kernel's reads)."""
+    buf = torch.ones(64 << 20, dtype=torch.float32, device="cuda") if flush else None
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
@@ -449,7 +450,7 @@ def _time_launches(fn, steps, warmup, flush=True):
     times = []
     for _ in range(steps):
         if buf is not None:
-            buf.zero_()
+            buf.sum()
         torch.cuda._sleep(200000)  # keep the GPU busy while the launch is enqueued: no host latency in the event pair
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -550,7 +551,7 @@ def run_micro_other(name, steps, warmup):
         raise RuntimeError(f"device error word {code:#x}")
     gbs = nbytes / (ms / 1e3) / 1e9
     return {"micro": name, "median_us": ms * 1e3, "algorithmic_bytes": nbytes, "gbs": gbs, "frac": gbs / peak,
-            "peak": peak, "peak_kind": kind, "l2": "flushed"}
+            "peak": peak, "peak_kind": kind, "l2": "flushed (256 MB read before each launch)"}
 
 
 def run_micro(name, steps, warmup):
@@ -569,7 +570,7 @@ def run_micro(name, steps, warmup):
     gbs = nbytes / (ms_packed / 1e3) / 1e9
     return {"micro": name, "M": M, "K": K, "n": n, "median_us": ms_packed * 1e3, "gbs": gbs, "frac": gbs / peak,
             "rowmajor_us": ms_rowmajor * 1e3, "rowmajor_gbs": nbytes / (ms_rowmajor / 1e3) / 1e9,
-            "peak": peak, "peak_kind": kind, "l2": "flushed", "layout": "packed"}
+            "peak": peak, "peak_kind": kind, "l2": "flushed (256 MB read before each launch)", "layout": "packed"}
 
 
 def run_sweep_nodes(sizes, steps, warmup):
