@@ -5,9 +5,13 @@
 // are computed once per tree node (each node's row is read once) and the per-path walk reads only the
 // candidate's own logit.
 //
-// One CTA per node row: pass 1 (max, first argmax, softmax normaliser of z/T by online rescaling), pass 2
-// (entropy, typical only; the row is then L1/L2-resident). The last CTA to finish (atomic ticket, no waiting)
-// walks the paths and writes the result.
+// One CTA per node row: pass 1 (max, first argmax; the softmax normaliser of z/T by online rescaling when the
+// row does not fit in registers), pass 2 (typical: the exponentials and their sum), pass 3 (typical: the
+// entropy). The node's CTA then decides the acceptance of each of the node's children in the tree (greedy: the
+// child's token is the node's argmax; typical: log p(child's token) > log tau) and leaves a flag and the log
+// probability. The last CTA to finish (atomic ticket, no waiting) walks the paths over those flags and writes
+// the result. Exponentials and logarithms of the typical statistics use the hardware approximations (relative
+// error near 2^-22), far below the 1e-3 margins the decisions are held to.
 #include <float.h>
 
 #include <mutex>
@@ -58,9 +62,10 @@ MV_DEV Stat stat_merge(Stat a, Stat b, float inv_t, bool typical) {
 
 __global__ void __launch_bounds__(kThreads) posterior_kernel(
     const float* logits, int V, int ld, const int32_t* tree_tokens, const int32_t* __restrict__ retrieve,
-    int n_nodes, int n_paths, int width, mv_accept_params prm, mv_posterior_result* out, float* node_stats_out,
-    int32_t* node_argmax_out, float* ws_stats, int32_t* ws_argmax, unsigned int* ticket, unsigned int* err,
-    const float2* row_max, int n_row_tiles, int row_ld) {
+    const int32_t* __restrict__ parent, int n_nodes, int n_paths, int width, mv_accept_params prm,
+    mv_posterior_result* out, float* node_stats_out, int32_t* node_argmax_out, float* ws_stats, int32_t* ws_argmax,
+    int32_t* ws_child_ok, float* ws_child_lp, unsigned int* ticket, unsigned int* err, const float2* row_max,
+    int n_row_tiles, int row_ld) {
   pdl_trigger();
   pdl_wait();
   const bool typical = prm.mode == MV_TYPICAL;
@@ -147,19 +152,19 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
         if (tid + u * kThreads < V4) {
-          buf[u].x = expf((buf[u].x - T.m) * inv_t);
-          buf[u].y = expf((buf[u].y - T.m) * inv_t);
-          buf[u].z = expf((buf[u].z - T.m) * inv_t);
-          buf[u].w = expf((buf[u].w - T.m) * inv_t);
+          buf[u].x = __expf((buf[u].x - T.m) * inv_t);
+          buf[u].y = __expf((buf[u].y - T.m) * inv_t);
+          buf[u].z = __expf((buf[u].z - T.m) * inv_t);
+          buf[u].w = __expf((buf[u].w - T.m) * inv_t);
           z += (buf[u].x + buf[u].y) + (buf[u].z + buf[u].w);
         }
       }
-      for (int i = 4 * V4 + tid; i < V; i += kThreads) z += expf((__ldcg(row + i) - T.m) * inv_t);
+      for (int i = 4 * V4 + tid; i < V; i += kThreads) z += __expf((__ldcg(row + i) - T.m) * inv_t);
       T.s = block_sum(z);
     }
     const float inv_s = 1.0f / T.s;
     float h = 0.0f;
-    auto ent = [&](float p) { h += p * logf(p + 1e-5f); };
+    auto ent = [&](float p) { h += p * __logf(p + 1e-5f); };
     if (in_regs) {  // pass 3
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
@@ -180,15 +185,15 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           if (c0 + tid + u * kThreads < V4) {
-            ent(expf((buf[u].x - T.m) * inv_t) * inv_s);
-            ent(expf((buf[u].y - T.m) * inv_t) * inv_s);
-            ent(expf((buf[u].z - T.m) * inv_t) * inv_s);
-            ent(expf((buf[u].w - T.m) * inv_t) * inv_s);
+            ent(__expf((buf[u].x - T.m) * inv_t) * inv_s);
+            ent(__expf((buf[u].y - T.m) * inv_t) * inv_s);
+            ent(__expf((buf[u].z - T.m) * inv_t) * inv_s);
+            ent(__expf((buf[u].w - T.m) * inv_t) * inv_s);
           }
         }
       }
     }
-    for (int i = 4 * V4 + tid; i < V; i += kThreads) ent(expf((__ldcg(row + i) - T.m) * inv_t) * inv_s);
+    for (int i = 4 * V4 + tid; i < V; i += kThreads) ent(__expf((__ldcg(row + i) - T.m) * inv_t) * inv_s);
     H = -block_sum(h);
     tau = fminf(prm.eps, prm.delta * expf(-H));
   }
@@ -206,6 +211,30 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
       node_stats_out[node * 4 + 3] = tau;
     }
     if (node_argmax_out) node_argmax_out[node] = T.i;
+  }
+  // the acceptance of this node's children: their candidate tokens against this node's distribution
+  {
+    const float lnz = typical ? logf(T.s) : 0.0f;
+    const float ltau = typical ? logf(tau) : 0.0f;
+    for (int c = tid; c < n_nodes; c += kThreads) {
+      if (__ldg(parent + c) != node) continue;
+      const int tok = tree_tokens[c];
+      int ok = 0;
+      float lp = 0.0f;
+      if (tok < 0 || tok >= V) {
+        mv_set_error(err, 3, MV_DEVERR_INDEX);
+      } else if (typical) {
+        lp = (__ldcg(row + tok) - T.m) * inv_t - lnz;  // log p(tok) under softmax(z / T)
+        ok = lp > ltau;
+      } else {
+        ok = tok == T.i;
+      }
+      ws_child_ok[c] = ok;
+      ws_child_lp[c] = lp;
+    }
+  }
+  __syncthreads();  // every child decision of this node is written
+  if (tid == 0) {
     __threadfence();
     last = atomicAdd(ticket, 1u) == (unsigned)(n_nodes - 1);
   }
@@ -220,36 +249,29 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
   if (tid == 0) s_bad = 0;
   __syncthreads();
   if (tid < n_paths) {
+    // the path's nodes, then their acceptance flags and log probabilities, each batch of loads in flight at once
     const int32_t* r = retrieve + tid * width;
+    int nd[MV_MAX_DEPTH + 1], okv[MV_MAX_DEPTH + 1];
+    float lpv[MV_MAX_DEPTH + 1];
+#pragma unroll
+    for (int j = 0; j <= MV_MAX_DEPTH; ++j) nd[j] = j < width ? __ldg(r + j) : -1;
+#pragma unroll
+    for (int j = 1; j <= MV_MAX_DEPTH; ++j) {
+      const bool in = nd[j] >= 0 && nd[j] < n_nodes;
+      if (nd[j] >= n_nodes) s_bad = 1;
+      okv[j] = in ? __ldcg(ws_child_ok + nd[j]) : 0;
+      lpv[j] = in ? __ldcg(ws_child_lp + nd[j]) : 0.0f;
+    }
     int acc = 0;
     float like = 0.0f;
-    for (int j = 0; j + 1 < width; ++j) {
-      const int par = r[j], child = r[j + 1];
-      if (child < 0) break;
-      if (par < 0 || par >= n_nodes || child >= n_nodes) {
-        s_bad = 1;
-        break;
-      }
-      const int tok = tree_tokens[child];
-      if (tok < 0 || tok >= V) {
-        s_bad = 1;
-        break;
-      }
-      bool ok;
-      if (typical) {
-        const float m = __ldcg(ws_stats + par * 4 + 0), s = __ldcg(ws_stats + par * 4 + 1);
-        const float p = expf((__ldcg(logits + (size_t)par * ld + tok) - m) * inv_t) / s;
-        ok = p > __ldcg(ws_stats + par * 4 + 3);
-        if (ok) like += logf(p);
-      } else {
-        ok = tok == __ldcg(ws_argmax + par);
-      }
-      if (!ok) break;
+    for (int j = 1; j < width && nd[j] >= 0 && okv[j]; ++j) {
       ++acc;
+      like += lpv[j];
     }
     s_acc[tid] = acc;
     s_like[tid] = like;
   }
+  __shared__ int s_best, s_bacc;
   __syncthreads();
   if (tid == 0) {
     if (s_bad) mv_set_error(err, 3, MV_DEVERR_INDEX);
@@ -259,25 +281,32 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
     }
     const int acc = s_acc[best] > 0 ? s_acc[best] : 0;
     if (acc == 0) best = 0;
-    const int32_t* r = retrieve + best * width;
+    s_best = best;
+    s_bacc = acc;
+    *ticket = 0u;  // leave the counter zeroed for the next call
+  }
+  __syncthreads();
+  // the result, one thread per field (the loads of the best path's nodes and tokens in flight together)
+  const int best = s_best, acc = s_bacc;
+  const int32_t* r = retrieve + best * width;
+  if (tid <= MV_MAX_DEPTH) {
+    const int nd = tid <= acc ? __ldg(r + tid) : -1;
+    out->nodes[tid] = nd;
+    out->tokens[tid] = nd >= 0 ? tree_tokens[nd] : -1;
+  } else if (tid == 32) {
+    const int nn = __ldg(r + acc);
     out->best = best;
     out->acc = acc;
     out->n_tokens = acc + 1;
-    for (int j = 0; j <= MV_MAX_DEPTH; ++j) {
-      const int nd = j <= acc ? r[j] : -1;
-      out->nodes[j] = nd;
-      out->tokens[j] = nd >= 0 ? tree_tokens[nd] : -1;
-    }
-    const int nn = r[acc];
     out->next_node = nn;
     out->next_root = __ldcg(ws_argmax + nn);
-    *ticket = 0u;  // leave the counter zeroed for the next call
   }
 }
 
 }  // namespace
 
-size_t posterior_ws_bytes(int n_nodes) { return (size_t)n_nodes * 5 * sizeof(float) + 64; }
+// ticket, then per node: stats [4], argmax, child flag, child log probability
+size_t posterior_ws_bytes(int n_nodes) { return (size_t)n_nodes * 7 * sizeof(float) + 64; }
 
 mv_status launch_posterior(const float* logits, int V, int ld, const int32_t* d_tree_tokens, const mv_tree* t,
                            mv_accept_params prm, mv_posterior_result* d_out, float* d_stats, int32_t* d_argmax,
@@ -286,9 +315,11 @@ mv_status launch_posterior(const float* logits, int V, int ld, const int32_t* d_
   unsigned int* ticket = reinterpret_cast<unsigned int*>(w);
   float* ws_stats = reinterpret_cast<float*>(w + 64);
   int32_t* ws_arg = reinterpret_cast<int32_t*>(w + 64 + (size_t)t->n_nodes * 4 * sizeof(float));
+  int32_t* ws_ok = ws_arg + t->n_nodes;
+  float* ws_lp = reinterpret_cast<float*>(ws_ok + t->n_nodes);
   if (mv_launch(posterior_kernel, dim3(t->n_nodes), dim3(kThreads), 0, stream, logits, V, ld, d_tree_tokens,
-                t->d_retrieve, t->n_nodes, t->n_paths, t->depth + 1, prm, d_out, d_stats, d_argmax, ws_stats, ws_arg,
-                ticket, mv_error_word(), row_max, n_row_tiles, row_ld) != cudaSuccess)
+                t->d_retrieve, t->d_parent, t->n_nodes, t->n_paths, t->depth + 1, prm, d_out, d_stats, d_argmax,
+                ws_stats, ws_arg, ws_ok, ws_lp, ticket, mv_error_word(), row_max, n_row_tiles, row_ld) != cudaSuccess)
     return MV_ERR_CUDA;
   return mv_last_launch("evaluate_posterior");
 }
@@ -304,7 +335,7 @@ extern "C" mv_status evaluate_posterior(const float* logits, int32_t V, int32_t 
                                         float* d_node_stats, int32_t* d_node_argmax, void* workspace,
                                         size_t ws_bytes, mv_stream stream) {
   if (!logits || !d_tree_tokens || !tree || !d_out || !workspace) return MV_ERR_INVALID_ARG;
-  if (!tree->d_retrieve) return MV_ERR_CUDA;
+  if (!tree->d_retrieve || !tree->d_parent) return MV_ERR_CUDA;
   if (V < 2 || ld < V || (ld & 3) || (reinterpret_cast<uintptr_t>(logits) & 15)) return MV_ERR_SHAPE;
   if (params.mode != MV_GREEDY && params.mode != MV_TYPICAL) return MV_ERR_INVALID_ARG;
   if (params.mode == MV_TYPICAL && !(params.temperature > 0.0f)) return MV_ERR_INVALID_ARG;
@@ -323,7 +354,7 @@ extern "C" mv_status evaluate_posterior(const float* logits, int32_t V, int32_t 
 namespace {
 
 constexpr int kNoAllocMaxNodes = MV_NOALLOC_MAX_NODES;
-constexpr size_t kNoAllocScratchBytes = 2048;  // >= posterior_ws_bytes(kNoAllocMaxNodes) = 64 * 20 + 64 = 1344
+constexpr size_t kNoAllocScratchBytes = 2048;  // >= posterior_ws_bytes(kNoAllocMaxNodes) = 64 * 28 + 64 = 1856
 static __device__ __align__(256) unsigned char g_posterior_scratch[kNoAllocScratchBytes];
 
 // Device address of g_posterior_scratch on the current device, looked up once per device with that device
@@ -350,7 +381,7 @@ extern "C" mv_status evaluate_posterior_noalloc(const float* logits, int32_t V, 
                                                 mv_accept_params params, mv_posterior_result* d_out,
                                                 float* d_node_stats, int32_t* d_node_argmax, mv_stream stream) {
   if (!logits || !d_tree_tokens || !tree || !d_out) return MV_ERR_INVALID_ARG;
-  if (!tree->d_retrieve) return MV_ERR_CUDA;
+  if (!tree->d_retrieve || !tree->d_parent) return MV_ERR_CUDA;
   if (V < 2 || ld < V || (ld & 3) || (reinterpret_cast<uintptr_t>(logits) & 15)) return MV_ERR_SHAPE;
   if (params.mode != MV_GREEDY && params.mode != MV_TYPICAL) return MV_ERR_INVALID_ARG;
   if (params.mode == MV_TYPICAL && !(params.temperature > 0.0f)) return MV_ERR_INVALID_ARG;
