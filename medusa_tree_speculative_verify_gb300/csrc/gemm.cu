@@ -61,10 +61,11 @@ constexpr int kMaxCluster = 8;  // CTAs per cluster (portable limit)
 // KB -- since every stage costs a full / empty handshake on top of its bytes.
 template <int NT, bool kAttn = false>
 struct Cfg {
-  static constexpr int kKps = NT <= 3 ? 2 : 1;  // k-blocks per stage
-  static constexpr int kStages = NT == 1 ? 3 : NT == 2 ? 2 : NT == 3 ? 2 : 3;
-  // after the stages: the cluster partial buffer, which a fused attention head uses first (kAttn)
-  static constexpr size_t kPartBytes = (size_t)BM * BN * 4;
+  static constexpr int kKps = NT <= 2 ? 2 : 1;  // k-blocks per stage
+  static constexpr int kStages = NT == 1 ? 3 : NT == 2 ? 2 : 3;
+  // after the stages: the split-K exchange region, two receive buffers of a token group's partials from every CTA
+  // of the cluster, which a fused attention head uses first (kAttn)
+  static constexpr size_t kPartBytes = 2 * (size_t)BM * BN * 4;
   static constexpr size_t kRegionBytes =
       kAttn && attn::smem_bytes<128>() > kPartBytes ? attn::smem_bytes<128>() : kPartBytes;
   static constexpr int kStageBytes = kKps * (kABytes + NT * kBBytes);
@@ -127,6 +128,15 @@ MV_DEV bool epi_any(bool v) {
       : "r"((uint32_t)v), "n"(kEpiThreads)
       : "memory");
   return r != 0;
+}
+
+// Asynchronous 4-byte store into the shared memory of a CTA of the cluster (dst and mbar are shared::cluster
+// addresses), counted on that CTA's mbarrier as complete_tx: the value is visible to whoever waits there, with no
+// release fence on the storing side.
+MV_DEV void st_async_f32(uint32_t dst, float v, uint32_t mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst),
+               "r"(__float_as_uint(v)), "r"(mbar)
+               : "memory");
 }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row core groups 1024 bytes apart.
@@ -431,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
   float* part = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);  // [BN tokens][BM rows], a group
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[kAcc], tempty[kAcc], drain, pfull, pfree;
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[kAcc], tempty[kAcc], drain, pfull[2], rfree[2];
   __shared__ __align__(8) uint64_t afull[attn::kStages], aready, adone;  // fused attention
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int s_abort;
@@ -458,8 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], kEpiWarps);
     }
-    mbar_init(&pfull, C);  // one arrive from every CTA of the cluster: all partials of the tile written
-    mbar_init(&pfree, C);  // one arrive from every CTA of the cluster: all reads of this CTA's partial done
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&pfull[b], 1);  // this CTA's arrive with the expected bytes; the cluster's stores complete it
+      mbar_init(&rfree[b], C);  // one arrive from every CTA of the cluster: it has consumed this CTA's slice
+    }
     mbar_init(&drain, 1);
     for (int s = 0; s < attn::kStages; ++s) mbar_init(&afull[s], 1);
     mbar_init(&aready, C);  // one arrive from every CTA of the cluster per attention step
@@ -649,13 +661,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
       }
     }
-    const uint32_t part_s = smem_u32(part) + (uint32_t)(lane * 16);  // + token row
+    // Split-K exchange of a token group ("item" m, receive buffer m % 2): token t of a group belongs to CTA t mod C
+    // (slot t / C). Every CTA drains its partial accumulator from TMEM and stores each value straight into its
+    // owner's receive buffer, slice [sender rank], with st.async counted on the owner's pfull[m % 2]. Each CTA then
+    // sums the C slices of its own tokens from its own shared memory (rank order: deterministic) and runs the fused
+    // epilogue on them. A sender may reuse a buffer once every owner has consumed the item two before (rfree).
+    const int U = kTokPerThread / C;  // token slots per owner (C is a power of two)
+    const uint32_t slice_bytes = (uint32_t)(U * 4 * BM * 4);
+    const uint32_t recv_s = smem_u32(part);  // [2][C senders][U][4][BM] floats
+    if (i == 0) {  // items 0 and 1: C slices each
+      mbar_arrive_expect_tx(&pfull[0], (uint32_t)C * slice_bytes);
+      mbar_arrive_expect_tx(&pfull[1], (uint32_t)C * slice_bytes);
+    }
     bool ok = true;
     int n = 0, m = 0, prev_tile = -1, prev_ph = 0, published = 0;
     // token group g_r of the tile; nr: item number; publish_to: phases before it are finished in this CTA once this
-    // item is (they are published right after its stores, ahead of releasing the partial buffers)
+    // item is (they are published right after its stores, ahead of releasing the receive buffer)
     auto finish = [&](int ph_r, int tile_r, int g_r, int nr, int publish_to) {
-      const bool all = mbar_wait_cluster(&pfull, (uint32_t)(nr & 1));
+      const int rb = nr & 1;
+      const bool all = mbar_wait_cluster(&pfull[rb], (uint32_t)((nr >> 1) & 1));
+      const float* recv = part + (size_t)rb * (C * U * 4 * BM);
       if (epi_any(!all)) {
         if (i == 0) mv_set_error(err, 11, MV_DEVERR_TIMEOUT);
         s_abort = 1;
@@ -677,11 +702,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           if (t >= kTokPerThread) break;
           const int j = sub + 4 * t;  // token within the group
           if (g_r * BN + j >= pr.n_tok) continue;
-          const uint32_t off = part_s + (uint32_t)(j * BM * 4);
+          const int slot = t / C;  // this token's place in every sender's slice
           float4 part_c[kMaxCluster];
 #pragma unroll
           for (int c = 0; c < kMaxCluster; ++c)
-            if (c < C) part_c[c] = ld_cluster_f4(map_rank(off, (uint32_t)c));
+            if (c < C) part_c[c] = reinterpret_cast<const float4*>(recv + ((c * U + slot) * 4 + sub) * BM)[lane];
 #pragma unroll
           for (int c = 0; c < kMaxCluster; ++c)
             if (c < C) add4(acc[u], part_c[c]);
@@ -705,7 +730,41 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           for (int k = published; k < publish_to; ++k) count_release(ca.flags + k);
         published = publish_to;
       }
-      if (i < C) mbar_arrive_remote(map_rank(smem_u32(&pfree), (uint32_t)i));
+      // arm this buffer for item nr + 2, then tell every sender its slice here may be overwritten
+      if (i == 0) mbar_arrive_expect_tx(&pfull[rb], (uint32_t)C * slice_bytes);
+      if (i < C) mbar_arrive_remote(map_rank(smem_u32(&rfree[rb]), (uint32_t)i));
+    };
+    // Drains token group g of TMEM accumulator buffer `buf` and stores it into the owners' receive buffers (item m).
+    auto drain_push = [&](int buf, int g) -> bool {
+      const int rb = m & 1;
+      bool free_ok = true;
+      if (m >= 2) free_ok = mbar_wait_cluster(&rfree[rb], (uint32_t)(((m >> 1) - 1) & 1));  // item m - 2 consumed
+      if (epi_any(!free_ok)) {
+        if (i == 0) mv_set_error(err, 10, MV_DEVERR_TIMEOUT);
+        s_abort = 1;
+        return false;
+      }
+      float v[BN / 2];  // this warp's half of the group's columns (tokens 32 hw .. 32 hw + 31)
+      const uint32_t ta =
+          tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(buf * BN * NT + g * BN + hw * (BN / 2));
+      tmem_ld32(ta, v);
+      tmem_ld_wait();
+      if (g == NT - 1) {  // the whole accumulator buffer is read: the MMA may reuse it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+      }
+      // token j = 32 hw + jj is token t = j / 4 of sub-partition j % 4, owned by CTA t % C at slot t / C
+      const uint32_t mine = recv_s + (uint32_t)((rb * C + rank) * U * 4 * BM * 4);  // my slice in every owner
+      const uint32_t bar = smem_u32(&pfull[rb]);
+#pragma unroll
+      for (int jj = 0; jj < BN / 2; ++jj) {
+        const int j = hw * (BN / 2) + jj, t = j >> 2, c = t & (C - 1);
+        const uint32_t off = (uint32_t)((((t / C) * 4 + (j & 3)) * BM + row) * 4);
+        st_async_f32(map_rank(mine + off, (uint32_t)c), v[jj], map_rank(bar, (uint32_t)c));
+      }
+      ++m;
+      return true;
     };
     // One loop over this CTA's tiles of every phase, so that each tile is finished at a single place in the code.
     const int NP = ca.n_phases;
@@ -748,9 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         ec_ph = ph;
       }
       const int buf = n % kAcc;
-      bool got = !s_abort && mbar_wait(&tfull[buf], (uint32_t)((n / kAcc) & 1));
-      // the partial buffer is free again once every CTA of the cluster has finished item m - 1
-      if (got && m >= 1) got = mbar_wait_cluster(&pfree, (uint32_t)((m - 1) & 1));
+      const bool got = !s_abort && mbar_wait(&tfull[buf], (uint32_t)((n / kAcc) & 1));
       if (epi_any(!got)) {  // uniform over the epilogue warps
         if (i == 0) mv_set_error(err, 10, MV_DEVERR_TIMEOUT);
         s_abort = 1;
@@ -758,36 +815,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         break;
       }
       tc_fence_after();
-      // The tile's token groups one after another through the partial buffer (item m = one group of one tile):
-      // group g - 1 of this tile is finished before group g is drained into the buffer it frees.
+      // The tile's token groups one after another (item m = one group of one tile): group g - 1 is finished
+      // before group g is drained, so the receive buffers hold at most two items.
       for (int g = 0; g < NT; ++g) {
         if (g > 0) {
           finish(ph, tile, g - 1, m - 1, published);
           if (!ok) break;
-          const bool free_ok = mbar_wait_cluster(&pfree, (uint32_t)((m - 1) & 1));
-          if (epi_any(!free_ok)) {
-            if (i == 0) mv_set_error(err, 10, MV_DEVERR_TIMEOUT);
-            s_abort = 1;
-            ok = false;
-            break;
-          }
         }
-        float v[BN / 2];  // this warp's half of the group's columns (tokens 32 hw .. 32 hw + 31)
-        const uint32_t ta =
-            tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(buf * BN * NT + g * BN + hw * (BN / 2));
-        tmem_ld32(ta, v);
-        tmem_ld_wait();
-        if (g == NT - 1) {  // the whole accumulator buffer is read: the MMA may reuse it
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[buf]);
+        if (!drain_push(buf, g)) {
+          ok = false;
+          break;
         }
-        // this CTA's partial, token-major: part[j][row] (consecutive rows in consecutive lanes)
-#pragma unroll
-        for (int j = 0; j < BN / 2; ++j) part[(hw * (BN / 2) + j) * BM + row] = v[j];
-        epi_bar();  // the CTA's writes are ordered before the cluster-scope release arrives below
-        if (i < C) mbar_arrive_remote(map_rank(smem_u32(&pfull), (uint32_t)i));
-        ++m;
       }
       if (!ok) break;
       prev_tile = tile;
@@ -929,7 +967,7 @@ void plan_chain(GemmParams* p, int n, int v, int* csize, int* ncl_out) {
   long long best = -1;
   *csize = 1;
   *ncl_out = std::min(max_tiles, mv_sm_count());
-  for (int c = 1; c <= kMaxCluster && c <= min_kbt; ++c) {
+  for (int c = 1; c <= kMaxCluster && c <= min_kbt; c *= 2) {  // powers of two: a group's 16 token slots split evenly
     const int mc = gemm_max_clusters(c, v);
     if (mc < 1) continue;
     const int ncl = std::min(mc, max_tiles);
