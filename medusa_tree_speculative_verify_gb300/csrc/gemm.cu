@@ -10,12 +10,12 @@
 // overlaps the MMAs of the next). With one group the chain can also run its layer's tree attention first, on the
 // epilogue warps (attn_core.cuh), while the producer streams the first projection's weights.
 //
-// Work split: split-K inside a thread-block cluster. Cluster q of C CTAs owns a contiguous range of tiles;
-// CTA rank r of the cluster streams k-blocks [r*kbt/C, (r+1)*kbt/C) of each, so the weight bytes of a tile are
-// read once. The C partial accumulators of a tile meet in distributed shared memory: each CTA writes its
-// partial (token-major fp32) into its own shared memory, signals every CTA of the cluster through a remote
-// mbarrier arrive, and then sums the C partials (in rank order: deterministic) for its own share of the tokens
-// and runs the fused epilogue on that share, so the epilogue is spread over the cluster as well:
+// Work split: split-K inside a thread-block cluster. Cluster q of C CTAs (C = 1, 2, 4 or 8) owns a contiguous range
+// of tiles; CTA rank r of the cluster streams k-blocks [r*kbt/C, (r+1)*kbt/C) of each, so the weight bytes of a tile
+// are read once. Token t of a token group belongs to CTA t mod C: after each tile every CTA drains its partial
+// accumulator from TMEM and stores each value straight into the owning CTA's receive buffer with st.async, counted
+// on the owner's mbarrier (no release fence on the sending side). Each owner sums the C slices of its own tokens in
+// rank order (deterministic) and runs the fused epilogue on them, so the epilogue is spread over the cluster too:
 //   STORE    out[token][row] = acc * s[token]                    (LM head logits, plain projections)
 //   RESIDUAL x[token][row] += acc; bf16 copy; per-token sum of squares of the 128-row slice (next RMSNorm)
 //   SWIGLU   act[token][f] = SiLU(s*gate) * (s*up), tile = 64 gate rows + the same 64 up rows
@@ -23,9 +23,10 @@
 // s[token] = 1/sqrt(mean(x^2) + eps) of the RMSNorm that precedes the projection (its gains are 1), applied
 // to the accumulator instead of the input: x W^T * s = (x * s) W^T.
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer + TMEM owner, warps 2..5 = epilogue
-// (warp w reads TMEM lanes 32*(w%4) .. +31). Every mbarrier wait is bounded; on expiry the kernel records
-// MV_DEVERR_TIMEOUT, lets its in-flight copies and MMAs land, frees its tensor memory and returns.
+// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer + TMEM owner, warps 2..9 = epilogue, two
+// per TMEM sub-partition (warp w reads TMEM lanes 32*(w%4) .. +31, the two of a pair take half of the columns
+// each). Every mbarrier wait is bounded; on expiry the kernel records MV_DEVERR_TIMEOUT, lets its in-flight copies
+// and MMAs land, frees its tensor memory and returns.
 #include <float.h>
 
 #include <algorithm>
