@@ -141,6 +141,30 @@ def test_nucleus_allow_set_exact_on_ties():
         assert g == inverse_cdf(p, allow, uniform(5, c))
 
 
+@pytest.mark.parametrize("top_p", [0.3, 0.8, 1.0])
+def test_nucleus_cluster_equals_single_cta(top_p):
+    """Rows up to 131072 logits are drawn by a cluster of CTAs, longer rows by one CTA. The masses are exact
+    fixed-point sums, so both give the same token: a row, and the same row with one -inf logit appended
+    (131072 -> 131073 logits, the other kernel), for the same counters."""
+    V = 131072
+    z = synth.normal(7, "root_long", (V,), 2.0, dtype=torch.float32)
+    z2 = torch.cat([z, torch.tensor([-float("inf")], dtype=torch.float32)])
+    prm = mv.RootParams(mv.ROOT_NUCLEUS, 0.7, top_p=top_p, key=3)
+    counters = list(range(40))
+    assert _draws(z.cuda(), prm, counters) == _draws(z2.cuda(), prm, counters)
+
+
+@pytest.mark.parametrize("top_p", [0.5, 0.9])
+def test_nucleus_dense_bin(top_p):
+    """32000 distinct logits within 0.032 of each other: every token falls in the first bin of 1/16 nat, so the
+    boundary is found among the sub-bins of that bin."""
+    V = 32000
+    order = torch.argsort(synth.normal(5, "root_perm", (V,), 1.0, dtype=torch.float32))
+    z = order.to(torch.float32) * 1e-6
+    exact, n = _check_row(z, NUCLEUS, 0.7, top_p, key=11, n_draws=120)
+    assert exact >= 0.9 * n
+
+
 def test_argmax_mode_and_bad_params():
     z = synth.normal(0, "root_row", (32000,), 1.0, dtype=torch.float32).cuda()
     out = torch.empty(1, dtype=torch.int32, device="cuda")
