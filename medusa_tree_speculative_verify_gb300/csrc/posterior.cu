@@ -5,13 +5,16 @@
 // are computed once per tree node (each node's row is read once) and the per-path walk reads only the
 // candidate's own logit.
 //
-// One CTA per node row: pass 1 (max, first argmax; the softmax normaliser of z/T by online rescaling when the
-// row does not fit in registers), pass 2 (typical: the exponentials and their sum), pass 3 (typical: the
-// entropy). The node's CTA then decides the acceptance of each of the node's children in the tree (greedy: the
-// child's token is the node's argmax; typical: log p(child's token) > log tau) and leaves a flag and the log
-// probability. The last CTA to finish (atomic ticket, no waiting) walks the paths over those flags and writes
-// the result. Exponentials and logarithms of the typical statistics use the hardware approximations (relative
-// error near 2^-22), far below the 1e-3 margins the decisions are held to.
+// A cluster of two CTAs per node row (128 CTAs at 64 nodes), each reducing half of it held in registers: the
+// half's max and first argmax and, for typical acceptance, the exponentials against the half's own max and their
+// sum; the two halves exchange (max, argmax, sum) once over distributed shared memory and merge them by
+// rescaling, in rank order, so both CTAs hold the same values; typical acceptance then sums the entropy
+// -sum p log(p + 1e-5) the same way. The node's first CTA decides the acceptance of each of the node's children
+// (greedy: the child's token is the node's argmax; typical: log p(child's token) > log tau) and leaves a flag
+// and the log probability. The last CTA to finish (atomic ticket, no waiting) walks the paths over those flags,
+// one thread per path with the path's nodes loaded at the start, picks the best path by warp-shuffle argmax and
+// writes the result from that path's thread. Exponentials and logarithms of the typical statistics use the
+// hardware approximations (relative error near 2^-22), far below the 1e-3 margins the decisions are held to.
 #include <float.h>
 
 #include <mutex>
@@ -22,7 +25,7 @@
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kBatch = 16;  // float4 per thread per chunk: 512 x 16 x 4 = 32768 logits
+constexpr int kBatch = 8;  // float4 per thread per chunk: 512 x 8 x 4 = 16384 logits, half of a row
 
 struct Stat {
   float m;  // running max of z
@@ -60,6 +63,71 @@ MV_DEV Stat stat_merge(Stat a, Stat b, float inv_t, bool typical) {
   return r;
 }
 
+// Partial statistics of one half of a row, pushed into both CTAs of the pair (slot = the sender's rank).
+struct Xchg {
+  Stat st[2];
+  float h[2];
+};
+MV_DEV void push_f32(float* slot, float v) {  // slot: this CTA's entry of a table of the pair
+#pragma unroll
+  for (uint32_t c = 0; c < 2; ++c)
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(map_rank(smem_u32(slot), c)), "f"(v) : "memory");
+}
+MV_DEV void push_i32(int* slot, int v) {
+#pragma unroll
+  for (uint32_t c = 0; c < 2; ++c)
+    asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(map_rank(smem_u32(slot), c)), "r"(v) : "memory");
+}
+
+MV_DEV Stat shfl_stat(const Stat& a, int o) {
+  Stat b;
+  b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+  b.i = __shfl_xor_sync(0xffffffffu, a.i, o);
+  b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+  return b;
+}
+// Merge of the CTA's threads' statistics (warp shuffles, then warp 0 over the warps); every thread gets it.
+MV_DEV Stat block_stat(Stat a, Stat* red, float inv_t, bool online) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) a = stat_merge(a, shfl_stat(a, o), inv_t, online);
+  if (lane == 0) red[warp] = a;
+  __syncthreads();
+  if (warp == 0) {
+    Stat t = lane < kThreads / 32 ? red[lane] : Stat{-FLT_MAX, 0x7fffffff, 0.0f};
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) t = stat_merge(t, shfl_stat(t, o), inv_t, online);
+    if (lane == 0) red[kThreads / 32] = t;
+  }
+  __syncthreads();
+  return red[kThreads / 32];
+}
+MV_DEV float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    float t = lane < kThreads / 32 ? red[lane] : 0.0f;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (lane == 0) red[kThreads / 32] = t;
+  }
+  __syncthreads();
+  const float r = red[kThreads / 32];
+  __syncthreads();  // red may be reused
+  return r;
+}
+
+// Whether path (acc_a, like_a, index a) is chosen over (acc_b, like_b, b): more accepted tokens, then (typical)
+// the larger likelihood, then the lower index.
+MV_DEV bool path_better(int acc_a, float like_a, int a, int acc_b, float like_b, int b, bool typical) {
+  if (acc_a != acc_b) return acc_a > acc_b;
+  if (typical && like_a != like_b) return like_a > like_b;
+  return a < b;
+}
+
 __global__ void __launch_bounds__(kThreads) posterior_kernel(
     const float* logits, int V, int ld, const int32_t* tree_tokens, const int32_t* __restrict__ retrieve,
     const int32_t* __restrict__ parent, int n_nodes, int n_paths, int width, mv_accept_params prm,
@@ -67,112 +135,124 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
     int32_t* ws_child_ok, float* ws_child_lp, unsigned int* ticket, unsigned int* err, const float2* row_max,
     int n_row_tiles, int row_ld) {
   pdl_trigger();
-  pdl_wait();
+  // No CTA touches its partner's shared memory before the partner has started: arrive now, wait before the first
+  // remote store (the row loads and the local reductions overlap the wait).
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   const bool typical = prm.mode == MV_TYPICAL;
   const float inv_t = typical ? 1.0f / prm.temperature : 1.0f;
-  const int node = blockIdx.x;
+  const int half = (int)cluster_rank();  // which half of the row this CTA reduces
+  const int node = blockIdx.x >> 1;
   const float* row = logits + (size_t)node * ld;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __shared__ Stat red[kThreads / 32];
-  __shared__ float fred[kThreads / 32];
-  __shared__ Stat tot;
+  const int tid = threadIdx.x;
+  __shared__ Stat red[kThreads / 32 + 1];
+  __shared__ float fred[kThreads / 32 + 1];
+  __shared__ Xchg xc;
   __shared__ bool last;
+  pdl_wait();
 
-  // The row (32000 logits) is held in registers, kBatch float4 per thread, all loaded before any is used.
-  // pass 1: max and first argmax; pass 2 (typical): e = exp((z - max) / T) kept in place, Z = sum e;
-  // pass 3 (typical): H = -sum p log(p + 1e-5) with p = e / Z. Rows longer than 32768 stream in chunks with
-  // an online (rescaled) normaliser instead.
+  // This CTA's half of the row (float4 units [v0, v1); the scalar tail beyond 4 (V / 4) belongs to the second
+  // half) is held in registers, kBatch float4 per thread, all loaded before any is used.
+  // Typical: the max of the half, e = exp((z - m_half) / T) kept in place and their sum; the halves exchange
+  // (max, first argmax, sum) once and merge them by rescaling (the same value in both CTAs); then the entropy
+  // H = -sum p log(p + 1e-5), p = e exp((m_half - m) / T) / Z, exchanged the same way. Greedy: the max and first
+  // argmax only. Halves longer than kBatch x kThreads float4 stream in chunks with an online (rescaled) sum.
   // Greedy with row_max: the LM-head projection already left each 128-row tile's max and first argmax of
   // every token; merging those replaces the pass over the row.
   const bool from_tiles = row_max && !typical;
-  const int V4 = from_tiles ? 0 : V >> 2;
-  const float4* row4 = reinterpret_cast<const float4*>(row);
-  const bool in_regs = V4 <= kBatch * kThreads;
+  const int V4all = from_tiles ? 0 : V >> 2;
+  const int hv = (V4all + 1) >> 1;
+  const int v0 = half ? hv : 0, v1 = half ? V4all : hv, V4 = v1 - v0;
+  const float4* row4 = reinterpret_cast<const float4*>(row) + v0;
+  const bool in_regs = hv <= kBatch * kThreads;  // the same in both CTAs: they take the same cluster barriers
+  const int t0 = from_tiles ? V : 4 * V4all + tid, t1 = half ? V : 0;  // the scalar tail (second half only)
   float4 buf[kBatch];
+  if (in_regs) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = tid + u * kThreads;
+      buf[u] = i < V4 ? __ldcg(row4 + i) : make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
+    }
+  }
+  // while the row loads are in flight: this thread's tree node (the children decisions: its parent, token and
+  // the token's logit) and, in every pair's first CTA (any may be the last to finish), its path of the walk
+  const int my_parent = tid < n_nodes ? __ldg(parent + tid) : -1;
+  const bool my_child = my_parent == node && half == 0;
+  const int my_tok = my_child ? tree_tokens[tid] : 0;
+  const float z_tok = my_child && my_tok >= 0 && my_tok < V ? __ldcg(row + my_tok) : 0.0f;
+  int nd[MV_MAX_DEPTH + 1];
+#pragma unroll
+  for (int j = 0; j <= MV_MAX_DEPTH; ++j)
+    nd[j] = (half == 0 && tid < n_paths && j < width) ? __ldg(retrieve + tid * width + j) : -1;
+
   Stat a{-FLT_MAX, 0x7fffffff, 0.0f};
   if (from_tiles) {
-    for (int t = tid; t < n_row_tiles; t += kThreads) {
+    for (int t = tid + half * kThreads; t < n_row_tiles; t += 2 * kThreads) {
       const float2 e = __ldcg(row_max + (size_t)t * row_ld + node);
       a = stat_merge(a, Stat{e.x, __float_as_int(e.y), 0.0f}, 1.0f, false);
     }
   }
+  const bool online = typical && !in_regs;
   for (int c0 = 0; c0 < V4; c0 += kBatch * kThreads) {
+    if (!in_regs) {
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = c0 + tid + u * kThreads;
-      buf[u] = i < V4 ? __ldcg(row4 + i) : make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = c0 + tid + u * kThreads;
+        buf[u] = i < V4 ? __ldcg(row4 + i) : make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
+      }
     }
-    const bool online = typical && !in_regs;
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int i = c0 + tid + u * kThreads;
       if (i < V4) {
-        stat_push(a, buf[u].x, 4 * i + 0, inv_t, online);
-        stat_push(a, buf[u].y, 4 * i + 1, inv_t, online);
-        stat_push(a, buf[u].z, 4 * i + 2, inv_t, online);
-        stat_push(a, buf[u].w, 4 * i + 3, inv_t, online);
+        const int k = 4 * (v0 + i);
+        stat_push(a, buf[u].x, k + 0, inv_t, online);
+        stat_push(a, buf[u].y, k + 1, inv_t, online);
+        stat_push(a, buf[u].z, k + 2, inv_t, online);
+        stat_push(a, buf[u].w, k + 3, inv_t, online);
       }
     }
   }
-  if (!from_tiles)
-    for (int i = 4 * V4 + tid; i < V; i += kThreads) stat_push(a, __ldcg(row + i), i, inv_t, typical && !in_regs);
-  const bool online = typical && !in_regs;
+  for (int i = t0; i < t1; i += kThreads) stat_push(a, __ldcg(row + i), i, inv_t, online);
+  Stat mine = block_stat(a, red, inv_t, online);
+  const float m_half = mine.m;
+  if (typical && in_regs) {  // the exponentials against this half's max, in place, and their sum
+    float z = 0.0f;
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    Stat b;
-    b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
-    b.i = __shfl_xor_sync(0xffffffffu, a.i, o);
-    b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
-    a = stat_merge(a, b, inv_t, online);
+    for (int u = 0; u < kBatch; ++u) {
+      if (tid + u * kThreads < V4) {
+        buf[u].x = __expf((buf[u].x - m_half) * inv_t);
+        buf[u].y = __expf((buf[u].y - m_half) * inv_t);
+        buf[u].z = __expf((buf[u].z - m_half) * inv_t);
+        buf[u].w = __expf((buf[u].w - m_half) * inv_t);
+        z += (buf[u].x + buf[u].y) + (buf[u].z + buf[u].w);
+      }
+    }
+    for (int i = t0; i < t1; i += kThreads) z += __expf((__ldcg(row + i) - m_half) * inv_t);
+    mine.s = block_sum(z, fred);
   }
-  if (lane == 0) red[warp] = a;
-  __syncthreads();
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // the partner has started
   if (tid == 0) {
-    Stat t = red[0];
-    for (int w = 1; w < kThreads / 32; ++w) t = stat_merge(t, red[w], inv_t, online);
-    tot = t;
+    push_f32(&xc.st[half].m, mine.m);
+    push_i32(&xc.st[half].i, mine.i);
+    push_f32(&xc.st[half].s, mine.s);
   }
-  __syncthreads();
-  Stat T = tot;
+  cluster_sync_all();
+  const Stat T = stat_merge(xc.st[0], xc.st[1], inv_t, typical);
 
   float H = 0.0f, tau = 0.0f;
   if (typical) {
-    auto block_sum = [&](float v) {
-      __syncthreads();
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) fred[warp] = v;
-      __syncthreads();
-      float s = 0.0f;
-      for (int w = 0; w < kThreads / 32; ++w) s += fred[w];
-      return s;
-    };
-    if (in_regs) {  // pass 2: exponentials in place and their sum
-      float z = 0.0f;
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        if (tid + u * kThreads < V4) {
-          buf[u].x = __expf((buf[u].x - T.m) * inv_t);
-          buf[u].y = __expf((buf[u].y - T.m) * inv_t);
-          buf[u].z = __expf((buf[u].z - T.m) * inv_t);
-          buf[u].w = __expf((buf[u].w - T.m) * inv_t);
-          z += (buf[u].x + buf[u].y) + (buf[u].z + buf[u].w);
-        }
-      }
-      for (int i = 4 * V4 + tid; i < V; i += kThreads) z += __expf((__ldcg(row + i) - T.m) * inv_t);
-      T.s = block_sum(z);
-    }
     const float inv_s = 1.0f / T.s;
     float h = 0.0f;
     auto ent = [&](float p) { h += p * __logf(p + 1e-5f); };
-    if (in_regs) {  // pass 3
+    if (in_regs) {
+      const float c = __expf((m_half - T.m) * inv_t) * inv_s;  // p = e c
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
         if (tid + u * kThreads < V4) {
-          ent(buf[u].x * inv_s);
-          ent(buf[u].y * inv_s);
-          ent(buf[u].z * inv_s);
-          ent(buf[u].w * inv_s);
+          ent(buf[u].x * c);
+          ent(buf[u].y * c);
+          ent(buf[u].z * c);
+          ent(buf[u].w * c);
         }
       }
     } else {
@@ -193,10 +273,15 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
         }
       }
     }
-    for (int i = 4 * V4 + tid; i < V; i += kThreads) ent(__expf((__ldcg(row + i) - T.m) * inv_t) * inv_s);
-    H = -block_sum(h);
+    for (int i = t0; i < t1; i += kThreads) ent(__expf((__ldcg(row + i) - T.m) * inv_t) * inv_s);
+    h = block_sum(h, fred);
+    if (tid == 0) push_f32(&xc.h[half], h);
+    cluster_sync_all();
+    H = -(xc.h[0] + xc.h[1]);
     tau = fminf(prm.eps, prm.delta * expf(-H));
   }
+  // after the last exchange no CTA reads its partner's shared memory: the second CTA of the pair is done
+  if (half) return;
 
   if (tid == 0) {
     ws_stats[node * 4 + 0] = T.m;
@@ -212,26 +297,21 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
     }
     if (node_argmax_out) node_argmax_out[node] = T.i;
   }
-  // the acceptance of this node's children: their candidate tokens against this node's distribution
-  {
-    const float lnz = typical ? logf(T.s) : 0.0f;
-    const float ltau = typical ? logf(tau) : 0.0f;
-    for (int c = tid; c < n_nodes; c += kThreads) {
-      if (__ldg(parent + c) != node) continue;
-      const int tok = tree_tokens[c];
-      int ok = 0;
-      float lp = 0.0f;
-      if (tok < 0 || tok >= V) {
-        mv_set_error(err, 3, MV_DEVERR_INDEX);
-      } else if (typical) {
-        lp = (__ldcg(row + tok) - T.m) * inv_t - lnz;  // log p(tok) under softmax(z / T)
-        ok = lp > ltau;
-      } else {
-        ok = tok == T.i;
-      }
-      ws_child_ok[c] = ok;
-      ws_child_lp[c] = lp;
+  // the acceptance of this node's children (thread c decides child c): their candidate tokens against this
+  // node's distribution
+  if (my_child) {
+    int ok = 0;
+    float lp = 0.0f;
+    if (my_tok < 0 || my_tok >= V) {
+      mv_set_error(err, 3, MV_DEVERR_INDEX);
+    } else if (typical) {
+      lp = (z_tok - T.m) * inv_t - logf(T.s);  // log p(tok) under softmax(z / T)
+      ok = lp > logf(tau);
+    } else {
+      ok = my_tok == T.i;
     }
+    ws_child_ok[tid] = ok;
+    ws_child_lp[tid] = lp;
   }
   __syncthreads();  // every child decision of this node is written
   if (tid == 0) {
@@ -243,63 +323,97 @@ __global__ void __launch_bounds__(kThreads) posterior_kernel(
   __threadfence();
 
   // ---- last CTA: walk every path (one thread per path), then pick the best
-  __shared__ int s_acc[MV_MAX_NODES];
-  __shared__ float s_like[MV_MAX_NODES];
-  __shared__ int s_bad;
-  if (tid == 0) s_bad = 0;
-  __syncthreads();
+  int acc = -1;  // threads without a path lose every comparison
+  float like = 0.0f;
+  bool bad = false;
   if (tid < n_paths) {
-    // the path's nodes, then their acceptance flags and log probabilities, each batch of loads in flight at once
-    const int32_t* r = retrieve + tid * width;
-    int nd[MV_MAX_DEPTH + 1], okv[MV_MAX_DEPTH + 1];
+    int okv[MV_MAX_DEPTH + 1];
     float lpv[MV_MAX_DEPTH + 1];
 #pragma unroll
-    for (int j = 0; j <= MV_MAX_DEPTH; ++j) nd[j] = j < width ? __ldg(r + j) : -1;
-#pragma unroll
-    for (int j = 1; j <= MV_MAX_DEPTH; ++j) {
+    for (int j = 1; j <= MV_MAX_DEPTH; ++j) {  // the flags and log probabilities, all loads in flight at once
       const bool in = nd[j] >= 0 && nd[j] < n_nodes;
-      if (nd[j] >= n_nodes) s_bad = 1;
+      bad |= nd[j] >= n_nodes;
       okv[j] = in ? __ldcg(ws_child_ok + nd[j]) : 0;
       lpv[j] = in ? __ldcg(ws_child_lp + nd[j]) : 0.0f;
     }
-    int acc = 0;
-    float like = 0.0f;
-    for (int j = 1; j < width && nd[j] >= 0 && okv[j]; ++j) {
-      ++acc;
-      like += lpv[j];
+    acc = 0;
+    bool alive = true;
+#pragma unroll
+    for (int j = 1; j <= MV_MAX_DEPTH; ++j) {
+      alive = alive && j < width && nd[j] >= 0 && okv[j];
+      if (alive) {
+        ++acc;
+        like += lpv[j];
+      }
     }
-    s_acc[tid] = acc;
-    s_like[tid] = like;
   }
-  __shared__ int s_best, s_bacc;
-  __syncthreads();
-  if (tid == 0) {
-    if (s_bad) mv_set_error(err, 3, MV_DEVERR_INDEX);
-    int best = 0;
-    for (int p = 1; p < n_paths; ++p) {
-      if (s_acc[p] > s_acc[best] || (typical && s_acc[p] == s_acc[best] && s_like[p] > s_like[best])) best = p;
+  if (__syncthreads_or(bad) && tid == 0) mv_set_error(err, 3, MV_DEVERR_INDEX);
+  // best path: warp argmax, then warp 0 over the warps' winners
+  __shared__ int s_acc[kThreads / 32], s_idx[kThreads / 32];
+  __shared__ float s_like[kThreads / 32];
+  __shared__ int s_best;
+  {
+    const int lane = tid & 31, warp = tid >> 5;
+    int ba = acc, bi = tid;
+    float bl = like;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const int oa = __shfl_xor_sync(0xffffffffu, ba, o), oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
+      if (path_better(oa, ol, oi, ba, bl, bi, typical)) {
+        ba = oa;
+        bi = oi;
+        bl = ol;
+      }
     }
-    const int acc = s_acc[best] > 0 ? s_acc[best] : 0;
-    if (acc == 0) best = 0;
-    s_best = best;
-    s_bacc = acc;
-    *ticket = 0u;  // leave the counter zeroed for the next call
+    if (lane == 0) {
+      s_acc[warp] = ba;
+      s_idx[warp] = bi;
+      s_like[warp] = bl;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      ba = lane < kThreads / 32 ? s_acc[lane] : -1;
+      bi = lane < kThreads / 32 ? s_idx[lane] : 0x7fffffff;
+      bl = lane < kThreads / 32 ? s_like[lane] : 0.0f;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const int oa = __shfl_xor_sync(0xffffffffu, ba, o), oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
+        if (path_better(oa, ol, oi, ba, bl, bi, typical)) {
+          ba = oa;
+          bi = oi;
+          bl = ol;
+        }
+      }
+      if (lane == 0) {
+        s_best = ba > 0 ? bi : 0;  // nothing accepted: path 0 (its root only)
+        *ticket = 0u;              // leave the counter zeroed for the next call
+      }
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  // the result, one thread per field (the loads of the best path's nodes and tokens in flight together)
-  const int best = s_best, acc = s_bacc;
-  const int32_t* r = retrieve + best * width;
-  if (tid <= MV_MAX_DEPTH) {
-    const int nd = tid <= acc ? __ldg(r + tid) : -1;
-    out->nodes[tid] = nd;
-    out->tokens[tid] = nd >= 0 ? tree_tokens[nd] : -1;
-  } else if (tid == 32) {
-    const int nn = __ldg(r + acc);
-    out->best = best;
-    out->acc = acc;
-    out->n_tokens = acc + 1;
+  // the result, written by the best path's own thread (its node list is in registers)
+  if (tid == s_best) {
+    const int n_acc = acc > 0 ? acc : 0;
+    int nn = nd[0];
+    int tk[MV_MAX_DEPTH + 1];
+#pragma unroll
+    for (int j = 0; j <= MV_MAX_DEPTH; ++j) {
+      if (j == n_acc) nn = nd[j];
+      tk[j] = j <= n_acc && nd[j] >= 0 ? tree_tokens[nd[j]] : -1;
+    }
+    const int next_root = __ldcg(ws_argmax + nn);
+#pragma unroll
+    for (int j = 0; j <= MV_MAX_DEPTH; ++j) {
+      out->nodes[j] = j <= n_acc ? nd[j] : -1;
+      out->tokens[j] = tk[j];
+    }
+    out->best = tid;
+    out->acc = n_acc;
+    out->n_tokens = n_acc + 1;
     out->next_node = nn;
-    out->next_root = __ldcg(ws_argmax + nn);
+    out->next_root = next_root;
   }
 }
 
@@ -317,9 +431,22 @@ mv_status launch_posterior(const float* logits, int V, int ld, const int32_t* d_
   int32_t* ws_arg = reinterpret_cast<int32_t*>(w + 64 + (size_t)t->n_nodes * 4 * sizeof(float));
   int32_t* ws_ok = ws_arg + t->n_nodes;
   float* ws_lp = reinterpret_cast<float*>(ws_ok + t->n_nodes);
-  if (mv_launch(posterior_kernel, dim3(t->n_nodes), dim3(kThreads), 0, stream, logits, V, ld, d_tree_tokens,
-                t->d_retrieve, t->d_parent, t->n_nodes, t->n_paths, t->depth + 1, prm, d_out, d_stats, d_argmax,
-                ws_stats, ws_arg, ws_ok, ws_lp, ticket, mv_error_word(), row_max, n_row_tiles, row_ld) != cudaSuccess)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * t->n_nodes);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;  // one pair of CTAs per node row
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = mv_pdl_enabled() ? 2 : 1;
+  if (cudaLaunchKernelEx(&cfg, posterior_kernel, logits, V, ld, d_tree_tokens, t->d_retrieve, t->d_parent,
+                         t->n_nodes, t->n_paths, t->depth + 1, prm, d_out, d_stats, d_argmax, ws_stats, ws_arg, ws_ok,
+                         ws_lp, ticket, mv_error_word(), row_max, n_row_tiles, row_ld) != cudaSuccess)
     return MV_ERR_CUDA;
   return mv_last_launch("evaluate_posterior");
 }
