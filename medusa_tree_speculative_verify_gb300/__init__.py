@@ -319,26 +319,44 @@ def linear_bf16_packed(w_packed, M, K, x, out, workspace, stream=None):
            "mv_linear_bf16_packed")
 
 
-def pack_weight(w, tile_rows, stream=None):
-    """A new bf16 tensor with w [M, K] in the projection kernel's packed layout (see mv_pack_weight)."""
+def pack_weight(w, tile_rows, stream=None, out=None):
+    """w [M, K] in the projection kernel's packed layout (see mv_pack_weight), in a new bf16 tensor or in ``out``
+    (a bf16 tensor of at least mv_packed_weight_bytes / 2 elements)."""
     import torch
     M, K = w.shape
     nbytes = _ws_size(lib().mv_packed_weight_bytes, M, K, tile_rows)
-    out = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=w.device)
+    if out is None:
+        out = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=w.device)
+    elif out.dtype != torch.bfloat16 or out.numel() * 2 < nbytes:
+        raise ValueError("pack_weight: out is not a bf16 tensor of the packed size")
     _check(lib().mv_pack_weight(_ptr(w), _ptr(out), M, K, tile_rows, _stream(stream)), "mv_pack_weight")
     return out
 
 
 def pack_model_weights(w, drop_source=False):
-    """Model weights with the projection matrices packed (embed and the Medusa matrices unchanged)."""
+    """Model weights with the projection matrices packed (embed and the Medusa matrices unchanged). A layer's
+    gate and up matrices share one allocation, up right after gate, so the projection kernel loads the gate and
+    up rows of a k-block with one copy."""
+    import torch
     out = dict(w)
-    for key, tr in (("wqkv", 128), ("wo", 128), ("w_gate", 64), ("w_up", 64), ("w_down", 128)):
+    for key, tr in (("wqkv", 128), ("wo", 128), ("w_down", 128)):
         packed = []
         for i in range(len(w[key])):
             packed.append(pack_weight(w[key][i], tr))
             if drop_source:
                 w[key][i] = None
         out[key] = packed
+    gates, ups = [], []
+    for i in range(len(w["w_gate"])):
+        F, K = w["w_gate"][i].shape
+        n = _ws_size(lib().mv_packed_weight_bytes, F, K, 64) // 2
+        both = torch.empty(2 * n, dtype=torch.bfloat16, device=w["w_gate"][i].device)
+        gates.append(pack_weight(w["w_gate"][i], 64, out=both[:n]))
+        ups.append(pack_weight(w["w_up"][i], 64, out=both[n:]))
+        if drop_source:
+            w["w_gate"][i] = None
+            w["w_up"][i] = None
+    out["w_gate"], out["w_up"] = gates, ups
     out["lm_head"] = pack_weight(w["lm_head"], 128)
     out["packed"] = True
     return out

@@ -550,7 +550,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
             uint8_t* a = stages + (size_t)s * kStageBytes;
             mbar_arrive_expect_tx(&full[s], (uint32_t)(nk * (kABytes + NT * kBBytes)));
-            for (int u = 0; u < nk; ++u) {
+            if (p.packed_a >= 2) {  // the stage's weights in one box, or one box per k-block
+              const int tb = tile * p.kbt + kb;
+              const CUtensorMap* m = nk == kKps ? am0 : am1;
+              for (int u = 0; u < (nk == kKps ? 1 : nk); ++u) {
+                if (p.packed_a == 3)
+                  tma_load_4d_hint(a + u * kABytes, m, &full[s], 0, 0, 0, tb + u, wpol);
+                else
+                  tma_load_3d_hint(a + u * kABytes, m, &full[s], 0, 0, tb + u, wpol);
+              }
+            }
+            for (int u = 0; u < nk && p.packed_a < 2; ++u) {
               uint8_t* au = a + u * kABytes;
               if (p.packed_a) {  // one contiguous block per matrix
                 const int tb = tile * p.kbt + kb + u;
@@ -903,6 +913,30 @@ bool gemm_weight_map_packed(CUtensorMap* map, const void* w, int rows, int K, in
                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+bool gemm_weight_map_packed_depth(CUtensorMap* map, const void* w, int rows, int K, int tile_rows, int depth) {
+  const uint64_t n_blocks = (uint64_t)((rows + tile_rows - 1) / tile_rows) * ((K + BK - 1) / BK);
+  const uint64_t dims[3] = {(uint64_t)BK, (uint64_t)tile_rows, n_blocks};
+  const uint64_t strides[2] = {(uint64_t)BK * 2, (uint64_t)tile_rows * BK * 2};
+  const uint32_t box[3] = {(uint32_t)BK, (uint32_t)tile_rows, (uint32_t)depth};
+  return mv_encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool gemm_weight_map_paired(CUtensorMap* map, const void* gate, const void* up, int F, int K, int depth) {
+  const uint64_t n_blocks = (uint64_t)((F + 63) / 64) * ((K + BK - 1) / BK);
+  const uint64_t block_bytes = 64ull * BK * 2;  // one packed (64 rows x 64) block of a matrix
+  const uintptr_t g = reinterpret_cast<uintptr_t>(gate), u = reinterpret_cast<uintptr_t>(up);
+  if (u != g + n_blocks * block_bytes) return false;
+  // dims: k within the block, row, matrix (gate, up), block; the box takes both matrices of `depth` blocks
+  const uint64_t dims[4] = {(uint64_t)BK, 64, 2, n_blocks};
+  const uint64_t strides[3] = {(uint64_t)BK * 2, n_blocks * block_bytes, block_bytes};
+  const uint32_t box[4] = {(uint32_t)BK, 64, 2, (uint32_t)depth};
+  return mv_encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, gate, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int gemm_stage_kblocks(int n_tok) { return token_groups(n_tok) <= 2 ? 2 : 1; }
+
 bool gemm_act_map_strided(CUtensorMap* map, const void* x, int rows, int K, int ld) {
   const uint64_t dims[2] = {(uint64_t)K, (uint64_t)rows};
   const uint64_t strides[1] = {(uint64_t)ld * 2};
@@ -1108,18 +1142,20 @@ extern "C" mv_status mv_linear_bf16_packed(const mv_bf16* w_packed, const mv_bf1
   if (!w_packed || !x || !out) return MV_ERR_INVALID_ARG;
   if (M < 1 || K < 8 || (K & 7) || n < 1 || n > kTokMax || ld_out < M) return MV_ERR_SHAPE;
   if ((reinterpret_cast<uintptr_t>(w_packed) | reinterpret_cast<uintptr_t>(x)) & 15) return MV_ERR_SHAPE;
-  CUtensorMap a, b;
-  if (!gemm_weight_map_packed(&a, w_packed, M, K, BM) || !gemm_act_map(&b, x, n, K)) return MV_ERR_CUDA;
+  CUtensorMap a0, a, b;
+  if (!gemm_weight_map_packed_depth(&a0, w_packed, M, K, BM, gemm_stage_kblocks(n)) ||
+      !gemm_weight_map_packed(&a, w_packed, M, K, BM) || !gemm_act_map(&b, x, n, K))
+    return MV_ERR_CUDA;
   GemmParams p{};
   p.M = M;
   p.K = K;
   p.n_tok = n;
-  p.packed_a = 1;
+  p.packed_a = 2;
   p.out_f32 = out;
   p.ld_out = ld_out;
   p.err = mv_error_word();
   gemm_finish_params(p);
-  return launch_gemm(EPI_STORE, a, a, b, p, static_cast<cudaStream_t>(stream));
+  return launch_gemm(EPI_STORE, a0, a, b, p, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" mv_status mv_linear_bf16_workspace(size_t* bytes) {

@@ -13,7 +13,11 @@ struct GemmParams {
   int n_tok;     // valid token columns (1..256; up to 64 per token group)
   int tok_ld;    // token stride of ssq, ssq_out and row_max (0: 64 x the launch's token groups)
   int paired;    // SWIGLU: tile = 64 rows of amap0 (gate) + the same 64 rows of amap1 (up)
-  int packed_a;  // weights in the [row tile][k-block][rows][64] layout (3-D maps, one contiguous box per load)
+  // Weight maps: 0 row-major (2-D maps); packed [row tile][k-block][rows][64] layout: 1 one k-block per load
+  // (a0, and a1 for the up matrix of a paired phase); 2 a0 loads kKps consecutive k-blocks of a tile in one box,
+  // a1 one; 3 (paired) gate and up of a layer in one allocation, a0 / a1 4-D maps whose box holds the gate and up
+  // rows of kKps / one k-block in the order the MMA reads them.
+  int packed_a;
   // derived (gemm_finish_params): k-blocks, tiles, CTAs per cluster (K slices per tile), clusters, CTAs
   int kbt, n_tiles, csize, n_clusters, grid;
   // RMSNorm scale of the input columns: s = 1/sqrt(sum(ssq[0..ssq_parts)) / norm_d + eps); null = 1
@@ -71,6 +75,13 @@ struct GemmAttn {
 
 bool gemm_weight_map(CUtensorMap* map, const void* w, int rows, int K, int box_rows);
 bool gemm_weight_map_packed(CUtensorMap* map, const void* w, int rows, int K, int tile_rows);
+// packed weights: a box of `depth` consecutive k-blocks of one row tile (one load per pipeline stage)
+bool gemm_weight_map_packed_depth(CUtensorMap* map, const void* w, int rows, int K, int tile_rows, int depth);
+// gate and up of a SwiGLU layer, both packed with 64-row tiles, up = gate + (packed bytes of gate): a box of
+// `depth` k-blocks, each holding 64 gate rows then the same 64 up rows. False if the two are not laid out so.
+bool gemm_weight_map_paired(CUtensorMap* map, const void* gate, const void* up, int F, int K, int depth);
+// The k-blocks per pipeline stage of a launch over n_tok tokens (the box depth of packed_a 2 / 3 maps' a0).
+int gemm_stage_kblocks(int n_tok);
 bool gemm_act_map(CUtensorMap* map, const void* x, int rows, int K);
 // rows x K bf16 activations whose rows are ld elements apart (ld % 8 == 0)
 bool gemm_act_map_strided(CUtensorMap* map, const void* x, int rows, int K, int ld);

@@ -179,6 +179,11 @@ struct mv_model {
   const uint16_t* w2;
   std::vector<CUtensorMap> m_qkv, m_o, m_gate, m_up, m_down;
   CUtensorMap m_lm;
+  // packed models: boxes of two consecutive k-blocks (one load per pipeline stage), and gate + up of a layer as
+  // one 4-D map (depth 1 and 2) when the two sit back to back (gu_combined)
+  std::vector<CUtensorMap> m_qkv2, m_o2, m_down2, m_gu1, m_gu2;
+  CUtensorMap m_lm2;
+  int gu_combined = 0;
   // fp32 weights (row-major [out][in])
   const float* f_embed = nullptr;
   std::vector<const float*> f_wqkv, f_wo, f_gate, f_up, f_down;
@@ -342,7 +347,7 @@ GemmParams base_params(const mv_session* s, int n_tok) {
   GemmParams p{};
   p.n_tok = n_tok;
   p.tok_ld = kTok;  // the stride of the session's sum-of-squares and tile-statistics arrays
-  p.packed_a = s->model->packed;
+  p.packed_a = s->model->packed ? 2 : 0;
   p.eps = s->model->dims.norm_eps;
   p.err = mv_error_word();
   return p;
@@ -405,10 +410,13 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
              : MV_ERR_CUDA;
   }
   // the projections, as chain phases: each phase's activations are the previous phase's output
+  // packed weights: a0 loads a whole pipeline stage (two k-blocks) when the launch streams two per stage
+  const bool two = m->packed && gemm_stage_kblocks(rows) == 2;
   auto qkv_phase = [&](int l) {  // QKV + RoPE + KV append
     GemmPhase g;
     g.epi = EPI_QKV;
-    g.a0 = g.a1 = m->m_qkv[l];
+    g.a0 = two ? m->m_qkv2[l] : m->m_qkv[l];
+    g.a1 = m->m_qkv[l];
     g.b = s->m_xb;
     GemmParams& p = g.p = base_params(s, rows);
     p.M = 3 * HD;
@@ -430,10 +438,11 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     p.log2_theta = log2f(d.rope_theta);
     return g;
   };
-  auto residual_phase = [&](const CUtensorMap& w, const CUtensorMap& act, int K) {  // O or down + residual
-    GemmPhase g;
+  auto residual_phase = [&](const CUtensorMap& w, const CUtensorMap* w2, const CUtensorMap& act, int K) {
+    GemmPhase g;  // O or down + residual
     g.epi = EPI_RESIDUAL;
-    g.a0 = g.a1 = w;
+    g.a0 = two ? *w2 : w;
+    g.a1 = w;
     g.b = act;
     GemmParams& p = g.p = base_params(s, rows);
     p.M = d.d;
@@ -450,6 +459,13 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     g.a1 = m->m_up[l];
     g.b = s->m_xb;
     GemmParams& p = g.p = base_params(s, rows);
+    if (m->gu_combined) {  // gate and up rows of a k-block in one box
+      g.a0 = two ? m->m_gu2[l] : m->m_gu1[l];
+      g.a1 = m->m_gu1[l];
+      p.packed_a = 3;
+    } else if (m->packed) {
+      p.packed_a = 1;
+    }
     p.paired = 1;
     p.F = d.ffn;
     p.M = d.ffn;
@@ -463,7 +479,8 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
   auto lm_phase = [&]() {  // final RMSNorm (as a column scale) + LM head -> fp32 logits
     GemmPhase g;
     g.epi = EPI_STORE;
-    g.a0 = g.a1 = m->m_lm;
+    g.a0 = two ? m->m_lm2 : m->m_lm;
+    g.a1 = m->m_lm;
     g.b = s->m_xb;
     GemmParams& p = g.p = base_params(s, rows);
     p.M = d.vocab;
@@ -489,9 +506,9 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     // O, gate/up and down of this layer, then the next layer's QKV (or the LM head): one launch
     GemmPhase ch[kGemmMaxPhases];
     int nph = 0;
-    ch[nph++] = residual_phase(m->m_o[l], s->m_attn, HD);
+    ch[nph++] = residual_phase(m->m_o[l], two ? &m->m_o2[l] : nullptr, s->m_attn, HD);
     ch[nph++] = gate_up_phase(l);
-    ch[nph++] = residual_phase(m->m_down[l], s->m_act, d.ffn);
+    ch[nph++] = residual_phase(m->m_down[l], two ? &m->m_down2[l] : nullptr, s->m_act, d.ffn);
     if (l + 1 < d.n_layers)
       ch[nph++] = qkv_phase(l + 1);
     else if (lm)
@@ -587,6 +604,23 @@ extern "C" mv_status mv_model_create(const mv_model_dims* dims, const mv_model_w
   }
   ok = ok && (m->packed ? gemm_weight_map_packed(&m->m_lm, w->lm_head, d.vocab, d.d, 128)
                         : gemm_weight_map(&m->m_lm, w->lm_head, d.vocab, d.d, 128));
+  if (ok && m->packed) {
+    m->m_qkv2.resize(d.n_layers);
+    m->m_o2.resize(d.n_layers);
+    m->m_down2.resize(d.n_layers);
+    m->m_gu1.resize(d.n_layers);
+    m->m_gu2.resize(d.n_layers);
+    bool gu = true;
+    for (int l = 0; l < d.n_layers && ok; ++l) {
+      ok = gemm_weight_map_packed_depth(&m->m_qkv2[l], w->wqkv[l], 3 * HD, d.d, 128, 2) &&
+           gemm_weight_map_packed_depth(&m->m_o2[l], w->wo[l], d.d, HD, 128, 2) &&
+           gemm_weight_map_packed_depth(&m->m_down2[l], w->w_down[l], d.d, d.ffn, 128, 2);
+      gu = gu && gemm_weight_map_paired(&m->m_gu1[l], w->w_gate[l], w->w_up[l], d.ffn, d.d, 1) &&
+           gemm_weight_map_paired(&m->m_gu2[l], w->w_gate[l], w->w_up[l], d.ffn, d.d, 2);
+    }
+    ok = ok && gemm_weight_map_packed_depth(&m->m_lm2, w->lm_head, d.vocab, d.d, 128, 2);
+    m->gu_combined = gu ? 1 : 0;
+  }
   if (!ok) {
     delete m;
     return MV_ERR_SHAPE;

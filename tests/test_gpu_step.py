@@ -314,3 +314,33 @@ def test_small64_decoder_attention_inside_the_chain(fused, monkeypatch):
         if srt[-1] - srt[-2] < 1e-2 + 2e-2 * abs(top):
             first_close = min(first_close, i)
     assert gen[:first_close + 1].tolist() == ar[:first_close + 1].tolist()
+
+
+@pytest.mark.parametrize("wide", [False, True])
+def test_gate_up_layouts_bit_identical(wide):
+    """pack_model_weights puts a layer's gate and up matrices in one allocation, up right after gate, and the
+    projection kernel then loads both halves of a k-block with one copy; gate and up packed into separate
+    allocations take one copy per matrix. Both fill shared memory with the same bytes, so prefill and steps give
+    bit-identical logits, cache and decode state (one token group, and several: a wide tree)."""
+    w = synth.packed_weights(DIMS, 0, torch.bfloat16, "cuda")
+    joint = mv.pack_model_weights(w)
+    gu = joint["w_up"][0].data_ptr() - joint["w_gate"][0].data_ptr()
+    assert gu == joint["w_gate"][0].numel() * 2  # up right after gate
+    apart = dict(joint)
+    apart["w_gate"] = [mv.pack_weight(t, 64) for t in w["w_gate"]]
+    apart["w_up"] = [mv.pack_weight(t, 64) for t in w["w_up"]]
+    choices, topk = (synth.synthetic_tree_choices(200, 2, 16), 16) if wide else (synth.dense_tree_choices([2, 3]), 10)
+    prm = mv.AcceptParams(GREEDY)
+    p = torch.as_tensor(_prompt(), dtype=torch.int32, device="cuda")
+    outs = []
+    for ws in (joint, apart):
+        sess = mv.Session(mv.Model(DIMS, ws), mv.Tree(choices, topk), S_MAX)
+        sess.prefill(p)
+        for _ in range(3):
+            sess.step(prm)
+        torch.cuda.synchronize()
+        n = int(sess.cur_len.item())
+        outs.append((sess.read_result(), n, sess.head_topk.cpu(), sess.kv[:, :, :, :n].cpu(), sess.logits.cpu()))
+    a, b = outs
+    assert a[0] == b[0] and a[1] == b[1]
+    assert torch.equal(a[2], b[2]) and torch.equal(a[3], b[3]) and torch.equal(a[4], b[4])
