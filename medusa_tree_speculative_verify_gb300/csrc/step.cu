@@ -231,6 +231,8 @@ struct mv_session {
   bool fuse_attention = true;  // run each layer's attention inside its projection chain when the shape allows
   int root_epoch = 0;         // bumped by every mv_session_set_root_sampling
   CUtensorMap m_xb, m_attn, m_act, m_kv;
+  CUtensorMap m_xb2, m_attn2, m_act2;  // the same as boxes of two k-blocks of one token group (act_pair)
+  bool act_pair = false;
   // CUDA graph of n consecutive steps (medusa_verify_steps_graph), captured on first use
   cudaGraphExec_t graph_exec = nullptr;
   cudaStream_t capture_stream = nullptr;
@@ -348,6 +350,7 @@ GemmParams base_params(const mv_session* s, int n_tok) {
   p.n_tok = n_tok;
   p.tok_ld = kTok;  // the stride of the session's sum-of-squares and tile-statistics arrays
   p.packed_a = s->model->packed ? 2 : 0;
+  p.act_pair = s->act_pair && n_tok <= 64 ? 1 : 0;  // one token group
   p.eps = s->model->dims.norm_eps;
   p.err = mv_error_word();
   return p;
@@ -418,6 +421,7 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     g.a0 = two ? m->m_qkv2[l] : m->m_qkv[l];
     g.a1 = m->m_qkv[l];
     g.b = s->m_xb;
+    g.b2 = s->m_xb2;
     GemmParams& p = g.p = base_params(s, rows);
     p.M = 3 * HD;
     p.K = d.d;
@@ -438,12 +442,14 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     p.log2_theta = log2f(d.rope_theta);
     return g;
   };
-  auto residual_phase = [&](const CUtensorMap& w, const CUtensorMap* w2, const CUtensorMap& act, int K) {
+  auto residual_phase = [&](const CUtensorMap& w, const CUtensorMap* w2, const CUtensorMap& act,
+                            const CUtensorMap& act2, int K) {
     GemmPhase g;  // O or down + residual
     g.epi = EPI_RESIDUAL;
     g.a0 = two ? *w2 : w;
     g.a1 = w;
     g.b = act;
+    g.b2 = act2;
     GemmParams& p = g.p = base_params(s, rows);
     p.M = d.d;
     p.K = K;
@@ -458,6 +464,7 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     g.a0 = m->m_gate[l];
     g.a1 = m->m_up[l];
     g.b = s->m_xb;
+    g.b2 = s->m_xb2;
     GemmParams& p = g.p = base_params(s, rows);
     if (m->gu_combined) {  // gate and up rows of a k-block in one box
       g.a0 = two ? m->m_gu2[l] : m->m_gu1[l];
@@ -482,6 +489,7 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     g.a0 = two ? m->m_lm2 : m->m_lm;
     g.a1 = m->m_lm;
     g.b = s->m_xb;
+    g.b2 = s->m_xb2;
     GemmParams& p = g.p = base_params(s, rows);
     p.M = d.vocab;
     p.K = d.d;
@@ -506,9 +514,9 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     // O, gate/up and down of this layer, then the next layer's QKV (or the LM head): one launch
     GemmPhase ch[kGemmMaxPhases];
     int nph = 0;
-    ch[nph++] = residual_phase(m->m_o[l], two ? &m->m_o2[l] : nullptr, s->m_attn, HD);
+    ch[nph++] = residual_phase(m->m_o[l], two ? &m->m_o2[l] : nullptr, s->m_attn, s->m_attn2, HD);
     ch[nph++] = gate_up_phase(l);
-    ch[nph++] = residual_phase(m->m_down[l], two ? &m->m_down2[l] : nullptr, s->m_act, d.ffn);
+    ch[nph++] = residual_phase(m->m_down[l], two ? &m->m_down2[l] : nullptr, s->m_act, s->m_act2, d.ffn);
     if (l + 1 < d.n_layers)
       ch[nph++] = qkv_phase(l + 1);
     else if (lm)
@@ -869,6 +877,8 @@ extern "C" mv_status mv_batch_session_create(mv_model* m, const mv_tree* tree, i
   } else {
     ok = gemm_act_map(&s->m_xb, s->xb, kTok, d.d) && gemm_act_map(&s->m_attn, s->attn, kTok, HD) &&
          gemm_act_map(&s->m_act, s->act, kTok, d.ffn);
+    s->act_pair = ok && gemm_act_map_pair(&s->m_xb2, s->xb, kTok, d.d) &&
+                  gemm_act_map_pair(&s->m_attn2, s->attn, kTok, HD) && gemm_act_map_pair(&s->m_act2, s->act, kTok, d.ffn);
     CUtensorMap vdummy;
     ok = ok && tree_attn_make_maps(&s->m_kv, &vdummy, kv, kv, d.n_heads, d.head_dim, s_max,
                                    2 * d.n_layers * batch, (size_t)d.n_heads * s_max * d.head_dim * 2);
