@@ -447,6 +447,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int s_abort;
   __shared__ EpiConst s_ec;
+  // the current phase's parameters and epilogue kind, copied once per phase: the epilogue of a phase's last tile
+  // -- the step every phase boundary waits for -- then reads shared memory instead of the kernel parameters
+  // through a runtime phase index
+  __shared__ GemmParams s_par;
+  __shared__ int s_epi;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = ca.csize;                  // CTAs per cluster = K slices per tile
@@ -703,8 +708,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         ok = false;
         return;
       }
-      const GemmParams& pr = ca.ph[ph_r];
-      const int epi = ca.epi[ph_r];
+      const GemmParams& pr = s_par;  // phase ph_r's (copied when the phase began in this CTA)
+      const int epi = s_epi;
       // this CTA's token share t = rank, rank + C, ..., alternate ones to the two warps of a sub-partition
       // (t0 = rank + hw C, stride 2 C), in chunks of kChunk tokens per thread, each summed over the C partials of
       // the cluster in rank order (16-byte DSMEM loads); only the fused epilogue itself depends on the kind
@@ -820,6 +825,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           break;
         }
         load_epi_const(ca.ph[ph], &s_ec, i, NT);  // scales and positions: the same for every tile of the phase
+        {
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(&ca.ph[ph]);
+          uint32_t* dst = reinterpret_cast<uint32_t*>(&s_par);
+          for (int k = i; k < (int)(sizeof(GemmParams) / 4); k += kEpiThreads) dst[k] = src[k];
+          if (i == 0) s_epi = ca.epi[ph];
+        }
         ec_ph = ph;
       }
       const int buf = n % kAcc;
