@@ -842,16 +842,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         break;
       }
       tc_fence_after();
-      // The tile's token groups one after another (item m = one group of one tile): group g - 1 is finished
-      // before group g is drained, so the receive buffers hold at most two items.
+      // The tile's token groups (item m = one group of one tile): group g is drained and pushed before group g - 1
+      // is finished, so one item's exchange overlaps the other's reduce and epilogue; the two receive buffers
+      // hold items g - 1 and g (drain_push waits until every owner has consumed item g - 2). Across tiles the
+      // previous tile's last group is finished first (above): a phase's last item publishes the phase, which the
+      // next tile's activations may wait for.
       for (int g = 0; g < NT; ++g) {
-        if (g > 0) {
-          finish(ph, tile, g - 1, m - 1, published);
-          if (!ok) break;
-        }
         if (!drain_push(buf, g)) {
           ok = false;
           break;
+        }
+        if (g > 0) {
+          finish(ph, tile, g - 1, m - 2, published);
+          if (!ok) break;
         }
       }
       if (!ok) break;
