@@ -149,6 +149,9 @@ mv_status launch_tree_attention_n(const CUtensorMap& kmap, const CUtensorMap& vm
                                   cudaStream_t stream, int nseq, int seq_planes) {
   (void)ws;  // reserved
   if (n < 1 || n > MV_MAX_NODES || nseq < 1 || (nseq > 1 && (n > kRows || !d_prefix))) return MV_ERR_SHAPE;
+  if ((D == 64 || D == 128) && S_max > kAttnLongCacheRows)  // long caches: the tensor-memory kernel
+    return launch_tree_attention_tc(kmap, vmap, plane_k, plane_v, q, H, D, S_max, d_prefix, prefix, max_prefix, t,
+                                    n, scale, out, stream, nseq, seq_planes);
   // blocks of 64 query rows of one tree, or one block per sequence
   const int blocks = nseq > 1 ? nseq : (n + kRows - 1) / kRows;
   const int max_tiles = (max_prefix + n + kKeys - 1) / kKeys;

@@ -41,6 +41,14 @@ mv_status launch_heads(const uint16_t* h, const float* x, const mv_posterior_res
                        cudaStream_t stream);
 
 // Tree attention over one layer. k/v tensor maps cover [H][S_max][D] planes; prefix from d_prefix if non-null.
+// Caches longer than kAttnLongCacheRows rows (head dim 64 or 128) run on the tcgen05 kernel (attention_tc.cu),
+// shorter ones on the warp-level kernel; a session takes one of the two for every step, so rows computed in
+// different steps (a tree node and the same token decoded alone) come from the same arithmetic.
+constexpr int kAttnLongCacheRows = 1024;
+mv_status launch_tree_attention_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, int plane_k, int plane_v,
+                                   const mv_bf16* q, int H, int D, int S_max, const int32_t* d_prefix, int prefix,
+                                   int max_prefix, const mv_tree* t, int n, float scale, mv_bf16* out,
+                                   cudaStream_t stream, int nseq, int seq_planes);
 struct TreeAttnPlan {
   int H, D, S_max, n_nodes, splits;
 };

@@ -507,8 +507,10 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     rc = launch_gemm_chain(&g, 1, nullptr, st);
   }
   const float scale = 1.0f / sqrtf((float)d.head_dim);
+  // the layer's attention inside its projection chain: one sequence of at most 64 rows, and a cache short enough
+  // for the warp-level attention (longer caches take the tcgen05 attention as its own launch, every step)
   const bool try_fuse = s->fuse_attention && nseq == 1 && n <= kSeqRows &&
-                        (d.head_dim == 64 || d.head_dim == 128);
+                        (d.head_dim == 64 || d.head_dim == 128) && s->s_max <= kAttnLongCacheRows;
   for (int l = 0; l < d.n_layers && rc == MV_OK; ++l) {
     const int pl = b0 * 2 * d.n_layers + 2 * l;  // sequence b0's planes of layer l
     // O, gate/up and down of this layer, then the next layer's QKV (or the LM head): one launch

@@ -324,3 +324,37 @@ def test_tree_attention_full_size(P, tree):
                                               (1, 32, 70, "synthetic256", None)])
 def test_tree_attention_small_ragged(H, D, P, tree, S_max):
     _attn_case(H, D, P, tree, S_max)
+
+
+@pytest.mark.parametrize("H,D,P,tree,S_max", [(2, 128, 0, "synthetic64", 2048), (3, 64, 37, "synthetic100", 1500),
+                                              (1, 128, 1100, "root", None), (2, 128, 1000, "synthetic256", 2048),
+                                              (1, 64, 1500, "chain5", None), (4, 128, 3000, "page63", None),
+                                              (2, 128, 131, "dense1x2x3", 1100), (3, 64, 0, "synthetic256", 1025)])
+def test_tree_attention_long_cache(H, D, P, tree, S_max):
+    """Caches longer than 1024 rows (head dim 64 or 128) run on the tcgen05 attention: 128-key tiles on the tensor
+    memory accumulators, 128 query rows per CTA. Short and long prefixes, trees of 1 to 256 nodes (two blocks of
+    128 rows), ragged ends."""
+    _attn_case(H, D, P, tree, S_max)
+
+
+@pytest.mark.parametrize("S_max", [700, 2048])
+def test_tree_attention_root_row_independent_of_the_tree(S_max):
+    """Both attention kernels: the root row of a 64-node tree is bit for bit the row of the same token attending
+    alone (a tree of the root only) at the same prefix, since key tiles go to splits by absolute position and
+    fully masked tiles add exact zeros."""
+    H, D, P = 8, 128, 600
+    k = synth.normal(1, "k", (H, S_max, D), dtype=torch.bfloat16, device="cuda")
+    v = synth.normal(1, "v", (H, S_max, D), dtype=torch.bfloat16, device="cuda")
+    rows = []
+    for name in ("root", "synthetic64"):
+        t, o = both_trees(name)
+        n = o["n_nodes"]
+        q = synth.normal(1, "q", (n, H, D), dtype=torch.bfloat16, device="cuda")
+        if name == "synthetic64":
+            q[0] = rows_q0
+        rows_q0 = q[0].clone()
+        out = torch.zeros(n, H, D, dtype=torch.bfloat16, device="cuda")
+        mv.tree_attention(q, k, v, P, t, 1.0 / math.sqrt(D), out, ws(mv.tree_attention_workspace(H, D, S_max, n)))
+        torch.cuda.synchronize()
+        rows.append(out[0].cpu())
+    assert torch.equal(rows[0], rows[1])

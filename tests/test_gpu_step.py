@@ -344,3 +344,36 @@ def test_gate_up_layouts_bit_identical(wide):
     a, b = outs
     assert a[0] == b[0] and a[1] == b[1]
     assert torch.equal(a[2], b[2]) and torch.equal(a[3], b[3]) and torch.equal(a[4], b[4])
+
+
+def test_long_cache_session_runs_the_tcgen05_attention():
+    """A session whose cache holds more than 1024 rows runs each layer's tree attention on the tcgen05 kernel as its
+    own launch (its projection chains carry no attention), every step. One step's logits match the oracle, and
+    greedy Medusa decoding emits exactly the library's own greedy stream of a root-only tree in a session of the
+    same cache length (random heads: nothing beyond the root is accepted, every token is a root row's argmax)."""
+    dims = synth.SMALL64
+    w = synth.packed_weights(dims, 0, torch.bfloat16, "cuda")
+    model = mv.Model(dims, mv.pack_model_weights(w))
+    om = Backbone(dims, synth.unpacked_getter(dims, w))
+    choices = synth.synthetic_tree_choices(48, 2, 10)
+    tree = mv.Tree(choices, 10)
+    s_long = 1100
+    p = synth.prompt_tokens(3, 40, dims.vocab)
+    sess = mv.Session(model, tree, s_long)
+    sess.prefill(torch.as_tensor(p, dtype=torch.int32, device="cuda"))
+    st = o_prefill(om, p.numpy(), s_long, 10)
+    sess.result[3] = int(st.root)
+    sess.head_topk.copy_(torch.as_tensor(st.head_topk, dtype=torch.int32, device="cuda"))
+    sess.step(mv.AcceptParams(GREEDY))
+    torch.cuda.synchronize()
+    toks, info = o_verify_step(om, st, tree_buffers(choices, 10), GREEDY)
+    assert sess.tree_tokens[: tree.n_nodes].cpu().tolist() == info["tree_tokens"].tolist()
+    got = sess.logits[: tree.n_nodes].double().cpu().numpy()
+    assert np.allclose(got, info["logits"], rtol=RTOL, atol=ATOL)
+    streams = []
+    for t in (tree, mv.Tree([], 10)):
+        s2 = mv.Session(model, t, s_long)
+        gen, accs = _gpu_decode(s2, p.numpy(), 16, mv.AcceptParams(GREEDY))
+        streams.append((gen.tolist(), accs))
+    assert sum(streams[0][1]) == 0 and sum(streams[1][1]) == 0
+    assert streams[0][0] == streams[1][0]
