@@ -43,8 +43,11 @@ mv_status launch_heads(const uint16_t* h, const float* x, const mv_posterior_res
 // Tree attention over one layer. k/v tensor maps cover [H][S_max][D] planes; prefix from d_prefix if non-null.
 // Caches longer than kAttnLongCacheRows rows (head dim 64 or 128) run on the tcgen05 kernel (attention_tc.cu),
 // shorter ones on the warp-level kernel; a session takes one of the two for every step, so rows computed in
-// different steps (a tree node and the same token decoded alone) come from the same arithmetic.
-constexpr int kAttnLongCacheRows = 1024;
+// different steps (a tree node and the same token decoded alone) come from the same arithmetic. The choice is
+// made by capacity because the prefix length lives on the device: a session sized for long contexts spends most
+// steps at long prefixes, where the tensor-core kernel is faster (at a 4096-key prefix, 26.6 against 33 us on
+// GB300); at short prefixes the warp-level attention inside the projection chain costs less (7 against 16 us).
+constexpr int kAttnLongCacheRows = 4096;
 mv_status launch_tree_attention_tc(const CUtensorMap& kmap, const CUtensorMap& vmap, int plane_k, int plane_v,
                                    const mv_bf16* q, int H, int D, int S_max, const int32_t* d_prefix, int prefix,
                                    int max_prefix, const mv_tree* t, int n, float scale, mv_bf16* out,

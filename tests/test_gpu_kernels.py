@@ -326,18 +326,18 @@ def test_tree_attention_small_ragged(H, D, P, tree, S_max):
     _attn_case(H, D, P, tree, S_max)
 
 
-@pytest.mark.parametrize("H,D,P,tree,S_max", [(2, 128, 0, "synthetic64", 2048), (3, 64, 37, "synthetic100", 1500),
-                                              (1, 128, 1100, "root", None), (2, 128, 1000, "synthetic256", 2048),
-                                              (1, 64, 1500, "chain5", None), (4, 128, 3000, "page63", None),
-                                              (2, 128, 131, "dense1x2x3", 1100), (3, 64, 0, "synthetic256", 1025)])
+@pytest.mark.parametrize("H,D,P,tree,S_max", [(2, 128, 0, "synthetic64", 4200), (3, 64, 37, "synthetic100", 4400),
+                                              (1, 128, 4100, "root", None), (2, 128, 1000, "synthetic256", 4300),
+                                              (1, 64, 4200, "chain5", None), (4, 128, 4500, "page63", None),
+                                              (2, 128, 131, "dense1x2x3", 4200), (3, 64, 0, "synthetic256", 4097)])
 def test_tree_attention_long_cache(H, D, P, tree, S_max):
-    """Caches longer than 1024 rows (head dim 64 or 128) run on the tcgen05 attention: 128-key tiles on the tensor
-    memory accumulators, 128 query rows per CTA. Short and long prefixes, trees of 1 to 256 nodes (two blocks of
-    128 rows), ragged ends."""
+    """Caches longer than 4096 rows (head dim 64 or 128) run on the tcgen05 attention: 128-key tiles on the tensor
+    memory accumulators, 64 query rows per CTA. Short and long prefixes, trees of 1 to 256 nodes (up to four blocks
+    of 64 rows), ragged ends."""
     _attn_case(H, D, P, tree, S_max)
 
 
-@pytest.mark.parametrize("S_max", [700, 2048])
+@pytest.mark.parametrize("S_max", [700, 4200])
 def test_tree_attention_root_row_independent_of_the_tree(S_max):
     """Both attention kernels: the root row of a 64-node tree is bit for bit the row of the same token attending
     alone (a tree of the root only) at the same prefix, since key tiles go to splits by absolute position and

@@ -347,7 +347,7 @@ def test_gate_up_layouts_bit_identical(wide):
 
 
 def test_long_cache_session_runs_the_tcgen05_attention():
-    """A session whose cache holds more than 1024 rows runs each layer's tree attention on the tcgen05 kernel as its
+    """A session whose cache holds more than 4096 rows runs each layer's tree attention on the tcgen05 kernel as its
     own launch (its projection chains carry no attention), every step. One step's logits match the oracle, and
     greedy Medusa decoding emits exactly the library's own greedy stream of a root-only tree in a session of the
     same cache length (random heads: nothing beyond the root is accepted, every token is a root row's argmax)."""
@@ -357,7 +357,7 @@ def test_long_cache_session_runs_the_tcgen05_attention():
     om = Backbone(dims, synth.unpacked_getter(dims, w))
     choices = synth.synthetic_tree_choices(48, 2, 10)
     tree = mv.Tree(choices, 10)
-    s_long = 1100
+    s_long = 4200
     p = synth.prompt_tokens(3, 40, dims.vocab)
     sess = mv.Session(model, tree, s_long)
     sess.prefill(torch.as_tensor(p, dtype=torch.int32, device="cuda"))
