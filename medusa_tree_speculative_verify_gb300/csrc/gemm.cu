@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         tma_prefetch_desc(&maps.a0[ph]);
         if (ca.ph[ph].paired) tma_prefetch_desc(&maps.a1[ph]);
         tma_prefetch_desc(&maps.b[ph]);
-        if (ca.ph[ph].act_pair) tma_prefetch_desc(&maps.b2[ph]);
+        if (ca.ph[ph].act_box) tma_prefetch_desc(&maps.b2[ph]);
       }
       int it = 0;
       bool ok = true, flag_timeout = false;
@@ -521,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         int pend_s[kStages], pend_kb[kStages], pend_n[kStages];
         int pend = 0;
         auto issue_b = [&](int stage, int kb, int nk) {  // the activation blocks of the NT token groups, nk k-blocks
-          if (NT == 1 && p.act_pair && nk == 2) {  // both k-blocks of the stage in one box
+          if (p.act_box == NT && nk == kKps) {  // every k-block and token group of the stage in one box
             tma_load_3d(stages + (size_t)stage * kStageBytes + kBOff, &maps.b2[ph], &full[stage], 0, 0, kb);
             return;
           }
@@ -964,11 +964,11 @@ bool gemm_act_map_strided(CUtensorMap* map, const void* x, int rows, int K, int 
                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-bool gemm_act_map_pair(CUtensorMap* map, const void* x, int rows, int K) {
-  if (K % BK) return false;
+bool gemm_act_map_stage(CUtensorMap* map, const void* x, int rows, int K, int groups) {
+  if (K % BK || groups < 1 || groups > kMaxGroups || rows < BN * groups) return false;
   const uint64_t dims[3] = {(uint64_t)BK, (uint64_t)rows, (uint64_t)(K / BK)};
   const uint64_t strides[2] = {(uint64_t)K * 2, (uint64_t)BK * 2};
-  const uint32_t box[3] = {(uint32_t)BK, (uint32_t)BN, 2};
+  const uint32_t box[3] = {(uint32_t)BK, (uint32_t)(BN * groups), (uint32_t)gemm_stage_kblocks(BN * groups)};
   return mv_encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, dims, strides, box,
                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -1090,11 +1090,11 @@ mv_status launch_gemm_chain(GemmPhase* ph, int n, unsigned int* flags, cudaStrea
     maps.a0[i] = ph[i].a0;
     maps.a1[i] = ph[i].a1;
     maps.b[i] = ph[i].b;
-    if (ps[i].act_pair) {
-      if (nt != 1 || (ps[i].K % BK) != 0) {
-        ps[i].act_pair = 0;  // more than one token group per stage, or a ragged last k-block: one box per block
-        ca.ph[i].act_pair = 0;
-        ph[i].p.act_pair = 0;
+    if (ps[i].act_box) {
+      if (ps[i].act_box != nt || (ps[i].K % BK) != 0) {
+        ps[i].act_box = 0;  // a map for another number of token groups, or a ragged last k-block: one box per block
+        ca.ph[i].act_box = 0;
+        ph[i].p.act_box = 0;
       } else {
         maps.b2[i] = ph[i].b2;
       }

@@ -18,7 +18,7 @@ struct GemmParams {
   // a1 one; 3 (paired) gate and up of a layer in one allocation, a0 / a1 4-D maps whose box holds the gate and up
   // rows of kKps / one k-block in the order the MMA reads them.
   int packed_a;
-  int act_pair;  // one token group: the activations of a two-k-block stage come in one box of map b2
+  int act_box;   // token groups of map b2's box (0: none): a stage's activations, all its k-blocks and groups, in one box
   // derived (gemm_finish_params): k-blocks, tiles, CTAs per cluster (K slices per tile), clusters, CTAs
   int kbt, n_tiles, csize, n_clusters, grid;
   // RMSNorm scale of the input columns: s = 1/sqrt(sum(ssq[0..ssq_parts)) / norm_d + eps); null = 1
@@ -58,7 +58,7 @@ constexpr int kGemmMaxPhases = 4;
 struct GemmPhase {
   int epi;
   CUtensorMap a0, a1, b;  // weights (a1: the up matrix of a paired phase), activations
-  CUtensorMap b2;         // p.act_pair: the activations as a box of two k-blocks of one token group
+  CUtensorMap b2;         // p.act_box: the activations as one box per pipeline stage (gemm_act_map_stage)
   GemmParams p;
 };
 // Counters of a chain: kGemmMaxPhases phase counters, the exit counter, the attention counter. Zero before the
@@ -85,8 +85,9 @@ bool gemm_weight_map_paired(CUtensorMap* map, const void* gate, const void* up, 
 // The k-blocks per pipeline stage of a launch over n_tok tokens (the box depth of packed_a 2 / 3 maps' a0).
 int gemm_stage_kblocks(int n_tok);
 bool gemm_act_map(CUtensorMap* map, const void* x, int rows, int K);
-// rows x K bf16 activations (K % 64 == 0) as [k-block][row][64]: a box of 64 rows x two consecutive k-blocks
-bool gemm_act_map_pair(CUtensorMap* map, const void* x, int rows, int K);
+// rows x K bf16 activations (K % 64 == 0) as [k-block][row][64]: a box of 64 groups rows x the k-blocks of one
+// pipeline stage of a launch over `groups` token groups (gemm_stage_kblocks), in the order the MMAs read them
+bool gemm_act_map_stage(CUtensorMap* map, const void* x, int rows, int K, int groups);
 // rows x K bf16 activations whose rows are ld elements apart (ld % 8 == 0)
 bool gemm_act_map_strided(CUtensorMap* map, const void* x, int rows, int K, int ld);
 void gemm_finish_params(GemmParams& p);

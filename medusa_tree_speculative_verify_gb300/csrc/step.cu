@@ -231,8 +231,10 @@ struct mv_session {
   bool fuse_attention = true;  // run each layer's attention inside its projection chain when the shape allows
   int root_epoch = 0;         // bumped by every mv_session_set_root_sampling
   CUtensorMap m_xb, m_attn, m_act, m_kv;
-  CUtensorMap m_xb2, m_attn2, m_act2;  // the same as boxes of two k-blocks of one token group (act_pair)
-  bool act_pair = false;
+  // the same as one box per pipeline stage, for passes of 1 .. kStageMaps token groups (gemm_act_map_stage)
+  static constexpr int kStageMaps = kTok / 64;
+  CUtensorMap m_xb2[kStageMaps], m_attn2[kStageMaps], m_act2[kStageMaps];
+  bool act_box = false;
   // CUDA graph of n consecutive steps (medusa_verify_steps_graph), captured on first use
   cudaGraphExec_t graph_exec = nullptr;
   cudaStream_t capture_stream = nullptr;
@@ -350,7 +352,8 @@ GemmParams base_params(const mv_session* s, int n_tok) {
   p.n_tok = n_tok;
   p.tok_ld = kTok;  // the stride of the session's sum-of-squares and tile-statistics arrays
   p.packed_a = s->model->packed ? 2 : 0;
-  p.act_pair = s->act_pair && n_tok <= 64 ? 1 : 0;  // one token group
+  const int groups = (n_tok + 63) / 64;
+  p.act_box = s->act_box && groups >= 1 && groups <= mv_session::kStageMaps ? groups : 0;
   p.eps = s->model->dims.norm_eps;
   p.err = mv_error_word();
   return p;
@@ -415,13 +418,14 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
   // the projections, as chain phases: each phase's activations are the previous phase's output
   // packed weights: a0 loads a whole pipeline stage (two k-blocks) when the launch streams two per stage
   const bool two = m->packed && gemm_stage_kblocks(rows) == 2;
+  const int gi = std::min(std::max((rows + 63) / 64, 1), (int)mv_session::kStageMaps) - 1;  // stage maps of the pass
   auto qkv_phase = [&](int l) {  // QKV + RoPE + KV append
     GemmPhase g;
     g.epi = EPI_QKV;
     g.a0 = two ? m->m_qkv2[l] : m->m_qkv[l];
     g.a1 = m->m_qkv[l];
     g.b = s->m_xb;
-    g.b2 = s->m_xb2;
+    g.b2 = s->m_xb2[gi];
     GemmParams& p = g.p = base_params(s, rows);
     p.M = 3 * HD;
     p.K = d.d;
@@ -464,7 +468,7 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     g.a0 = m->m_gate[l];
     g.a1 = m->m_up[l];
     g.b = s->m_xb;
-    g.b2 = s->m_xb2;
+    g.b2 = s->m_xb2[gi];
     GemmParams& p = g.p = base_params(s, rows);
     if (m->gu_combined) {  // gate and up rows of a k-block in one box
       g.a0 = two ? m->m_gu2[l] : m->m_gu1[l];
@@ -489,7 +493,7 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     g.a0 = two ? m->m_lm2 : m->m_lm;
     g.a1 = m->m_lm;
     g.b = s->m_xb;
-    g.b2 = s->m_xb2;
+    g.b2 = s->m_xb2[gi];
     GemmParams& p = g.p = base_params(s, rows);
     p.M = d.vocab;
     p.K = d.d;
@@ -516,9 +520,9 @@ mv_status forward(mv_session* s, const mv_tree* t, const int32_t* d_tokens, int 
     // O, gate/up and down of this layer, then the next layer's QKV (or the LM head): one launch
     GemmPhase ch[kGemmMaxPhases];
     int nph = 0;
-    ch[nph++] = residual_phase(m->m_o[l], two ? &m->m_o2[l] : nullptr, s->m_attn, s->m_attn2, HD);
+    ch[nph++] = residual_phase(m->m_o[l], two ? &m->m_o2[l] : nullptr, s->m_attn, s->m_attn2[gi], HD);
     ch[nph++] = gate_up_phase(l);
-    ch[nph++] = residual_phase(m->m_down[l], two ? &m->m_down2[l] : nullptr, s->m_act, s->m_act2, d.ffn);
+    ch[nph++] = residual_phase(m->m_down[l], two ? &m->m_down2[l] : nullptr, s->m_act, s->m_act2[gi], d.ffn);
     if (l + 1 < d.n_layers)
       ch[nph++] = qkv_phase(l + 1);
     else if (lm)
@@ -879,8 +883,11 @@ extern "C" mv_status mv_batch_session_create(mv_model* m, const mv_tree* tree, i
   } else {
     ok = gemm_act_map(&s->m_xb, s->xb, kTok, d.d) && gemm_act_map(&s->m_attn, s->attn, kTok, HD) &&
          gemm_act_map(&s->m_act, s->act, kTok, d.ffn);
-    s->act_pair = ok && gemm_act_map_pair(&s->m_xb2, s->xb, kTok, d.d) &&
-                  gemm_act_map_pair(&s->m_attn2, s->attn, kTok, HD) && gemm_act_map_pair(&s->m_act2, s->act, kTok, d.ffn);
+    s->act_box = ok;
+    for (int g = 1; g <= mv_session::kStageMaps; ++g)
+      s->act_box = s->act_box && gemm_act_map_stage(&s->m_xb2[g - 1], s->xb, kTok, d.d, g) &&
+                   gemm_act_map_stage(&s->m_attn2[g - 1], s->attn, kTok, HD, g) &&
+                   gemm_act_map_stage(&s->m_act2[g - 1], s->act, kTok, d.ffn, g);
     CUtensorMap vdummy;
     ok = ok && tree_attn_make_maps(&s->m_kv, &vdummy, kv, kv, d.n_heads, d.head_dim, s_max,
                                    2 * d.n_layers * batch, (size_t)d.n_heads * s_max * d.head_dim * 2);
