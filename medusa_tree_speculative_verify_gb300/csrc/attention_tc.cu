@@ -51,7 +51,7 @@ struct TcLayout {
   static constexpr int kV = kK + 2 * kTile;
   static constexpr int kEnd = kV + 2 * kTile;
   static constexpr int kPo = D + 4;  // merge: row pitch (floats) of the partial output
-  static constexpr int kMergeBytes = (kTcRows * kPo + kTcRows * 2 + kTcRows * kTcSplits) * 4;
+  static constexpr int kMergeBytes = (kTcRows * kPo + kTcRows * 2) * 4;
   static_assert(kTcKeys == kTcM, "the key tile fills the regions like the rows");
   static_assert(kK + kMergeBytes <= kEnd, "the merge buffers fit over the rings");
 };
@@ -174,6 +174,7 @@ MV_DEV uint64_t block_bits(uint64_t w0, uint64_t w1, uint64_t w2, uint64_t w3, i
 template <int D>
 __global__ void __launch_bounds__(kTcThreads + 32, 1) tree_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                         const __grid_constant__ CUtensorMap vmap,
+                                                                        const __grid_constant__ CUtensorMap qmap,
                                                                         const attn::Args a) {
   using Ly = TcLayout<D>;
   constexpr int kHalves = Ly::kHalves;
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(kTcThreads + 32, 1) tree_attn_tc_kernel(const 
       mbar_init(&odone[st], 1);
       mbar_init(&pfull[st], kTcThreads);
     }
-    mbar_init(&qready, kTcThreads);
+    mbar_init(&qready, 1);  // the copies of Q (expected bytes)
     mbar_init(&drain, 1);
     s_abort = 0;
     mbar_fence_init();
@@ -248,23 +249,25 @@ __global__ void __launch_bounds__(kTcThreads + 32, 1) tree_attn_tc_kernel(const 
     return false;
   };
 
+  // 64-key halves of this split's j-th tile that hold a key some row of the block can see (the prefix, then the
+  // tree keys up to the block's last row): a half past them is neither copied nor multiplied by P (its S columns
+  // are masked, so O is the same bits), which spares the copy of the empty half of the last tile.
+  auto halves = [&](int j) { return (split + j * C) * kTcKeys + 64 < P + n_keys ? 2 : 1; };
   auto issue_k = [&](int j) {  // key tile of this split's j-th tile into stage j % 2
-    const int st = j & 1, key0 = (split + j * C) * kTcKeys;
-    mbar_arrive_expect_tx(&kfull[st], (uint32_t)Ly::kTile);
+    const int st = j & 1, key0 = (split + j * C) * kTcKeys, nh = halves(j);
+    mbar_arrive_expect_tx(&kfull[st], (uint32_t)(nh * kHalves * 64 * 128));
 #pragma unroll
     for (int hb = 0; hb < kHalves; ++hb)
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb)
+      for (int kb = 0; kb < nh; ++kb)
         tma_load_4d(sK + st * Ly::kTile + hb * Ly::kRegion + kb * 64 * 128, &kmap, &kfull[st], hb * 64,
                     key0 + 64 * kb, h, plane_k);
   };
   auto issue_v = [&](int j) {
-    const int st = j & 1, key0 = (split + j * C) * kTcKeys;
-    mbar_arrive_expect_tx(&vfull[st], (uint32_t)Ly::kTile);
+    const int st = j & 1, key0 = (split + j * C) * kTcKeys, nh = halves(j);
+    mbar_arrive_expect_tx(&vfull[st], (uint32_t)(nh * kHalves * 64 * 128));
 #pragma unroll
     for (int hb = 0; hb < kHalves; ++hb)
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb)
+      for (int kb = 0; kb < nh; ++kb)
         tma_load_4d(sV + st * Ly::kTile + hb * Ly::kRegion + kb * 64 * 128, &vmap, &vfull[st], hb * 64,
                     key0 + 64 * kb, h, plane_v);
   };
@@ -282,8 +285,8 @@ __global__ void __launch_bounds__(kTcThreads + 32, 1) tree_attn_tc_kernel(const 
   };
   auto mma_o = [&](int j) {
     const uint32_t pb = smem_u32(sP + (j & 1) * 2 * Ly::kRegion), vb = smem_u32(sV + (j & 1) * Ly::kTile);
-#pragma unroll
-    for (int c = 0; c < 2; ++c)      // 64-key halves of the tile
+    const int nh = halves(j);
+    for (int c = 0; c < nh; ++c)     // 64-key halves of the tile
 #pragma unroll
       for (int k = 0; k < 4; ++k)    // 16 keys each
         tc_mma_f16(tmem + kColO, desc_kmajor(pb + c * Ly::kRegion) + (uint64_t)(2 * k),
@@ -306,7 +309,15 @@ __global__ void __launch_bounds__(kTcThreads + 32, 1) tree_attn_tc_kernel(const 
     // of tile vl - 2 is done. No barrier can run two phases past a probe: each next use is gated on this thread.
     if (lane == 0) {
       if (count > 0) {
-        issue_k(k_issued++);  // the first tiles' copies overlap the staging of Q
+        // Q (rows past the tensor's are zero-filled) into MMA rows 0..63 and again 64..127, with the first tiles
+        tma_prefetch_desc(&qmap);
+        mbar_arrive_expect_tx(&qready, (uint32_t)(2 * kHalves * kTcRows * 128));
+#pragma unroll
+        for (int hb = 0; hb < kHalves; ++hb)
+#pragma unroll
+          for (int dup = 0; dup < 2; ++dup)
+            tma_load_3d(sQ + hb * Ly::kRegion + dup * kTcRows * 128, &qmap, &qready, hb * 64, h, qrow0);
+        issue_k(k_issued++);
         issue_v(v_issued++);
       }
       bool ok = count == 0 || wait(&qready, 0);
@@ -349,6 +360,7 @@ __global__ void __launch_bounds__(kTcThreads + 32, 1) tree_attn_tc_kernel(const 
         mv_set_error(a.err, 4, MV_DEVERR_TIMEOUT);
         tc_commit_to(&drain);
         mbar_wait(&drain, 0u);
+        if (count > 0) mbar_wait(&qready, 0u);
         for (int j = k_waited; j < k_issued; ++j)
           if (!mbar_wait(&kfull[j & 1], (uint32_t)((j >> 1) & 1))) break;
         for (int j = v_waited; j < v_issued; ++j)
@@ -358,21 +370,10 @@ __global__ void __launch_bounds__(kTcThreads + 32, 1) tree_attn_tc_kernel(const 
   } else {
     // ------------------------------------------------------------------ softmax (128 threads)
     // Thread t reads TMEM lane t: query row r = t % 64 of the block, key half kh = t / 64 of every tile. Q rows
-    // r and r + 64 of the MMA hold the same query, so both halves of the row find its S values in their own
-    // lanes; P rows 64..127 stay zero. Q (zero past the block's queries) in the K-major swizzled layout, every
-    // load first.
-    if (kh == 0) {  // the query once, into rows r and r + 64
-      uint4 qv[D / 8];
-      const uint4* src = reinterpret_cast<const uint4*>(a.q + ((size_t)(qrow0 + (valid ? r : 0)) * a.H + h) * D);
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) qv[c] = valid ? __ldcg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        uint8_t* d = sQ + (c >> 3) * Ly::kRegion + (((c & 7) ^ (r & 7)) << 4);  // rows r, r + 64: same swizzle
-        *reinterpret_cast<uint4*>(d + r * 128) = qv[c];
-        *reinterpret_cast<uint4*>(d + (r + 64) * 128) = qv[c];
-      }
-    } else {  // P rows 64..127 of both buffers: zero (their outputs are not used)
+    // r and r + 64 of the MMA hold the same query (copied there by the issuing warp), so both halves of the row
+    // find its S values in their own lanes; P rows 64..127 stay zero. Rows of Q past the block's queries hold
+    // other rows of the q buffer or zeros: their S, P and O rows are neither kept nor stored.
+    if (kh == 1) {  // P rows 64..127 of both buffers: zero (their outputs are not used)
 #pragma unroll
       for (int c = 0; c < 32; ++c)
         *reinterpret_cast<uint4*>(sP + (c >> 3) * Ly::kRegion + tid * 128 + (((c & 7) ^ (tid & 7)) << 4)) =
@@ -387,8 +388,7 @@ __global__ void __launch_bounds__(kTcThreads + 32, 1) tree_attn_tc_kernel(const 
       w2 = ar[2];
       w3 = ar[3];
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic-proxy writes -> the tensor core
-    mbar_arrive(&qready);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the zeros of P -> the tensor core
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     for (int i = 0; i < count; ++i) {
       bool got = wait(&sdone[i & 1], i >> 1);
@@ -491,7 +491,6 @@ __global__ void __launch_bounds__(kTcThreads + 32, 1) tree_attn_tc_kernel(const 
   // CTA of the cluster merges a slice of the rows over distributed shared memory, the splits in rank order
   float* po = reinterpret_cast<float*>(smem + Ly::kK);  // [64][D + 4]
   float* pml = po + kTcRows * Ly::kPo;                 // [64][2] exponent reference and sum
-  float* pw = pml + kTcRows * 2;                       // [64][kTcSplits] merge weights of this CTA's rows
   __syncthreads();
   if (kh == 0) {
 #pragma unroll
@@ -518,57 +517,61 @@ __global__ void __launch_bounds__(kTcThreads + 32, 1) tree_attn_tc_kernel(const 
   cluster_sync_all();  // every partial of the head is in place
   const int r0 = split * n / C, r1 = (split + 1) * n / C;  // this CTA's rows of the merge
   const uint32_t ml_s = smem_u32(pml), po_s = smem_u32(po);
-  if (tid < r1 - r0) {
-    // w_s = 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s' over the S splits with tiles (rank order)
-    const int q = r0 + tid;
-    float m[kTcSplits], ll[kTcSplits];
+  // Consecutive threads take consecutive 16-byte columns of a row (a warp reads whole rows of the partials),
+  // each thread kU elements of the CTA's rows; every split's (reference, sum) and partial values of those
+  // elements are loaded before any is used. O = sum_s w_s O_s with w_s = 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s',
+  // in rank order.
+  constexpr int kF4 = D / 4, kU = 4;  // float4 per row; elements per thread and pass
+  const int total = (r1 - r0) * kF4;
+  for (int e0 = tid; tid < kTcThreads && e0 < total; e0 += kU * kTcThreads) {
+    float2 ml[kU][kTcSplits];
+    float4 v[kU][kTcSplits];
 #pragma unroll
-    for (int sp = 0; sp < kTcSplits; ++sp) {
-      m[sp] = -INFINITY;
-      ll[sp] = 0.0f;
-      if (sp < S) {
-        const float2 v = ld_cluster_f2(map_rank(ml_s + (uint32_t)(q * 8), (uint32_t)sp));
-        m[sp] = v.x;
-        ll[sp] = v.y;
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * kTcThreads;
+      if (e >= total) break;
+      const int q = r0 + e / kF4, c4 = (e % kF4) * 4;
+#pragma unroll
+      for (int sp = 0; sp < kTcSplits; ++sp) {
+        if (sp < S) {
+          ml[u][sp] = ld_cluster_f2(map_rank(ml_s + (uint32_t)(q * 8), (uint32_t)sp));
+          v[u][sp] = ld_cluster_f4(map_rank(po_s + (uint32_t)((q * Ly::kPo + c4) * 4), (uint32_t)sp));
+        }
       }
     }
-    float M = -INFINITY;
 #pragma unroll
-    for (int sp = 0; sp < kTcSplits; ++sp) M = fmaxf(M, m[sp]);
-    const float bs = M == -INFINITY ? 0.0f : M;
-    float L = 0.0f;
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * kTcThreads;
+      if (e >= total) break;
+      const int q = r0 + e / kF4, c4 = (e % kF4) * 4;
+      float M = -INFINITY;
 #pragma unroll
-    for (int sp = 0; sp < kTcSplits; ++sp) {
-      m[sp] = sp < S ? exp2f(m[sp] - bs) : 0.0f;
-      L += m[sp] * ll[sp];
-    }
-    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+      for (int sp = 0; sp < kTcSplits; ++sp)
+        if (sp < S) M = fmaxf(M, ml[u][sp].x);
+      const float bs = M == -INFINITY ? 0.0f : M;
+      float w[kTcSplits], L = 0.0f;
 #pragma unroll
-    for (int sp = 0; sp < kTcSplits; ++sp) pw[tid * kTcSplits + sp] = m[sp] * inv;
-  }
-  __syncthreads();
-  for (int e = tid; tid < kTcThreads && e < (r1 - r0) * (D / 4); e += kTcThreads) {
-    const int rq = e / (D / 4), c4 = (e % (D / 4)) * 4, q = r0 + rq;
-    const uint32_t off = po_s + (uint32_t)((q * Ly::kPo + c4) * 4);
-    float4 v[kTcSplits];
-#pragma unroll
-    for (int sp = 0; sp < kTcSplits; ++sp)
-      if (sp < S) v[sp] = ld_cluster_f4(map_rank(off, (uint32_t)sp));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int sp = 0; sp < kTcSplits; ++sp) {
-      if (sp < S) {
-        const float w = pw[rq * kTcSplits + sp];
-        acc.x += w * v[sp].x;
-        acc.y += w * v[sp].y;
-        acc.z += w * v[sp].z;
-        acc.w += w * v[sp].w;
+      for (int sp = 0; sp < kTcSplits; ++sp) {
+        w[sp] = sp < S ? exp2f(ml[u][sp].x - bs) : 0.0f;
+        L += sp < S ? w[sp] * ml[u][sp].y : 0.0f;
       }
+      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int sp = 0; sp < kTcSplits; ++sp) {
+        if (sp < S) {
+          const float ws = w[sp] * inv;
+          acc.x += ws * v[u][sp].x;
+          acc.y += ws * v[u][sp].y;
+          acc.z += ws * v[u][sp].z;
+          acc.w += ws * v[u][sp].w;
+        }
+      }
+      uint2 pk;
+      pk.x = pack_bf16x2(acc.x, acc.y);
+      pk.y = pack_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(a.out + ((size_t)(qrow0 + q) * a.H + h) * D + c4) = pk;
     }
-    uint2 pk;
-    pk.x = pack_bf16x2(acc.x, acc.y);
-    pk.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(a.out + ((size_t)(qrow0 + q) * a.H + h) * D + c4) = pk;
   }
   cluster_sync_all();  // no CTA leaves while another may still read its partial
 }
@@ -620,6 +623,17 @@ mv_status launch_tree_attention_tc(const CUtensorMap& kmap, const CUtensorMap& v
   if (D != 64 && D != 128) return MV_ERR_UNSUPPORTED;
   if (n < 1 || n > MV_MAX_NODES || nseq < 1 || (nseq > 1 && (n > attn::kRows || !d_prefix))) return MV_ERR_SHAPE;
   if (reinterpret_cast<uintptr_t>(q) & 15) return MV_ERR_SHAPE;
+  // q [rows][H][D] as (d, head, row) boxes of 64 d x one head x 64 rows
+  CUtensorMap qmap;
+  {
+    const int q_rows = nseq > 1 ? nseq * attn::kRows : n;
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)H, (uint64_t)q_rows};
+    const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)H * D * 2};
+    const uint32_t box[3] = {64, 1, (uint32_t)kTcRows};
+    if (!mv_encode_tmap(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+      return MV_ERR_CUDA;
+  }
   // blocks of 128 query rows of one tree, or one block per sequence (its rows 64 b ..)
   const int blocks = nseq > 1 ? nseq : (n + kTcRows - 1) / kTcRows;
   const int max_tiles = (max_prefix + n + kTcKeys - 1) / kTcKeys;
@@ -656,8 +670,8 @@ mv_status launch_tree_attention_tc(const CUtensorMap& kmap, const CUtensorMap& v
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = mv_pdl_enabled() ? 2 : 1;
-  const cudaError_t e = D == 64 ? cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<64>, kmap, vmap, a)
-                                : cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<128>, kmap, vmap, a);
+  const cudaError_t e = D == 64 ? cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<64>, kmap, vmap, qmap, a)
+                                : cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<128>, kmap, vmap, qmap, a);
   if (e != cudaSuccess) return MV_ERR_CUDA;
   return mv_last_launch("tree_attention_tc");
 }
