@@ -143,3 +143,35 @@ def test_batched_session_rejects_large_trees_and_single_sequence_calls():
     sess = mv.Session(model, mv.Tree(synth.dense_tree_choices([2, 3]), 10), S_MAX, batch=2)
     with pytest.raises(mv.MVError):
         sess.prefill(torch.as_tensor(_prompts(1)[0], dtype=torch.int32, device="cuda"))
+
+
+def test_batched_long_cache_runs_the_tcgen05_attention():
+    """A batched session whose caches hold more than 4096 rows runs each layer's tree attention for all its
+    sequences in one launch of the tcgen05 kernel (one query block and one set of cache planes per sequence, q
+    copied by TMA from the sequence's 64 rows). Each sequence decodes as the oracle decodes it alone, up to its
+    first position whose oracle top-2 margin is inside the bf16 tolerance."""
+    dims, B, s_long, n_new = synth.SMALL64, 2, 4200, 8
+    w = synth.packed_weights(dims, 0, torch.bfloat16, "cuda")
+    model = mv.Model(dims, mv.pack_model_weights(w))
+    om = Backbone(dims, synth.unpacked_getter(dims, w))
+    sess = mv.Session(model, mv.Tree(synth.synthetic_tree_choices(48, 2, 10), 10), s_long, batch=B)
+    prompts = [synth.prompt_tokens(200 + b, 24 + 5 * b, dims.vocab).numpy() for b in range(B)]
+    for b, p in enumerate(prompts):
+        sess.prefill_seq(b, torch.as_tensor(p, dtype=torch.int32, device="cuda"))
+    outs = [[] for _ in range(B)]
+    while min(len(o) for o in outs) < n_new:
+        sess.step(mv.AcceptParams(GREEDY))
+        for b in range(B):
+            outs[b].extend(sess.read_result(b)["tokens"])
+    for b in range(B):
+        gen = np.asarray(outs[b][:n_new])
+        lg = teacher_forced_logits(om, prompts[b], gen, S_MAX)
+        first_close = len(gen)
+        for i, t in enumerate(gen):
+            top = lg[i].max()
+            assert top - lg[i, t] <= 1e-2 + 2e-2 * abs(top), (b, i, t, int(np.argmax(lg[i])))
+            srt = np.sort(lg[i])
+            if srt[-1] - srt[-2] < 1e-2 + 2e-2 * abs(top):
+                first_close = min(first_close, i)
+        ar = ar_greedy_decode(om, prompts[b], n_new, S_MAX)
+        assert gen[:first_close + 1].tolist() == ar[:first_close + 1].tolist(), b
