@@ -86,7 +86,7 @@ struct Args {
 template <int D>
 constexpr size_t smem_bytes() {
   constexpr size_t ring = (size_t)2 * kStages * kKeys * D * 2;
-  constexpr size_t merge = ((size_t)kRows * (D + 4) + kRows * 2 + kRows * kMaxSplits) * sizeof(float);
+  constexpr size_t merge = ((size_t)kRows * (D + 4) + kRows * 2) * sizeof(float);
   return ring > merge ? ring : merge;
 }
 
@@ -317,7 +317,6 @@ MV_DEV void head(const Args& a, const CUtensorMap* kmap, const CUtensorMap* vmap
   grp_bar();
   float* po = reinterpret_cast<float*>(smem);  // [64][D + 4] (padded rows: conflict-free float2 stores)
   float* pml = po + kRows * kPo;               // [64][2] running max (log2 domain) and sum
-  float* pw = pml + kRows * 2;                 // [64][kMaxSplits] merge weights of this CTA's rows
 #pragma unroll
   for (int dn = 0; dn < DN; ++dn) {
     const int col = 8 * dn + 2 * t4;
@@ -333,57 +332,61 @@ MV_DEV void head(const Args& a, const CUtensorMap* kmap, const CUtensorMap* vmap
   sync.ready();  // every partial of the head is in place
   const int r0 = split * n / C, r1 = (split + 1) * n / C;  // this CTA's query rows
   const uint32_t ml_s = smem_u32(pml), po_s = smem_u32(po);
-  if (tid < r1 - r0) {
-    // w_s = 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s' for the row's S splits (rank order)
-    const int q = r0 + tid;
-    float m[kMaxSplits], l[kMaxSplits];
+  // Consecutive threads take consecutive 16-byte columns of a row (a warp reads whole rows of the partials),
+  // each thread kU elements of the CTA's rows; every split's (max, sum) and partial values of those elements are
+  // loaded before any is used. O = sum_s w_s O_s, w_s = 2^(m_s - M) / sum_s' 2^(m_s' - M) l_s' over the row's S
+  // splits, in rank order.
+  constexpr int kF4 = D / 4, kU = 2;  // float4 per row; elements per thread and pass
+  const int total = (r1 - r0) * kF4;
+  for (int e0 = tid; e0 < total; e0 += kU * kThreads) {
+    float2 ml[kU][kMaxSplits];
+    float4 v[kU][kMaxSplits];
 #pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) {
-      m[s] = -INFINITY;
-      l[s] = 0.0f;
-      if (s < S) {
-        const float2 v = ld_cluster_f2(map_rank(ml_s + (uint32_t)(q * 8), (uint32_t)s));
-        m[s] = v.x;
-        l[s] = v.y;
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * kThreads;
+      if (e >= total) break;
+      const int q = r0 + e / kF4, c4 = (e % kF4) * 4;
+#pragma unroll
+      for (int sp = 0; sp < kMaxSplits; ++sp) {
+        if (sp < S) {
+          ml[u][sp] = ld_cluster_f2(map_rank(ml_s + (uint32_t)(q * 8), (uint32_t)sp));
+          v[u][sp] = ld_cluster_f4(map_rank(po_s + (uint32_t)((q * kPo + c4) * 4), (uint32_t)sp));
+        }
       }
     }
-    float M = -INFINITY;
 #pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) M = fmaxf(M, m[s]);
-    const float base = M == -INFINITY ? 0.0f : M;
-    float L = 0.0f;
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * kThreads;
+      if (e >= total) break;
+      const int q = r0 + e / kF4, c4 = (e % kF4) * 4;
+      float M = -INFINITY;
 #pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) {
-      m[s] = s < S ? exp2f(m[s] - base) : 0.0f;
-      L += m[s] * l[s];
-    }
-    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+      for (int sp = 0; sp < kMaxSplits; ++sp)
+        if (sp < S) M = fmaxf(M, ml[u][sp].x);
+      const float base = M == -INFINITY ? 0.0f : M;
+      float w[kMaxSplits], L = 0.0f;
 #pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) pw[tid * kMaxSplits + s] = m[s] * inv;
-  }
-  grp_bar();
-  for (int e = tid; e < (r1 - r0) * (D / 4); e += kThreads) {
-    const int rq = e / (D / 4), c4 = (e % (D / 4)) * 4, q = r0 + rq;
-    const uint32_t off = po_s + (uint32_t)((q * kPo + c4) * 4);
-    float4 v[kMaxSplits];
-#pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s)
-      if (s < S) v[s] = ld_cluster_f4(map_rank(off, (uint32_t)s));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) {
-      if (s < S) {
-        const float w = pw[rq * kMaxSplits + s];
-        acc.x += w * v[s].x;
-        acc.y += w * v[s].y;
-        acc.z += w * v[s].z;
-        acc.w += w * v[s].w;
+      for (int sp = 0; sp < kMaxSplits; ++sp) {
+        w[sp] = sp < S ? exp2f(ml[u][sp].x - base) : 0.0f;
+        L += sp < S ? w[sp] * ml[u][sp].y : 0.0f;
       }
+      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int sp = 0; sp < kMaxSplits; ++sp) {
+        if (sp < S) {
+          const float ws = w[sp] * inv;
+          acc.x += ws * v[u][sp].x;
+          acc.y += ws * v[u][sp].y;
+          acc.z += ws * v[u][sp].z;
+          acc.w += ws * v[u][sp].w;
+        }
+      }
+      uint2 pk;
+      pk.x = pack_bf16x2(acc.x, acc.y);
+      pk.y = pack_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(a.out + ((size_t)(qrow0 + q) * a.H + h) * D + c4) = pk;
     }
-    uint2 pk;
-    pk.x = pack_bf16x2(acc.x, acc.y);
-    pk.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(a.out + ((size_t)(qrow0 + q) * a.H + h) * D + c4) = pk;
   }
   sync.done();  // no CTA goes on while another may still read its partial
 }
