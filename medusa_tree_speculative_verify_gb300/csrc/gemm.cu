@@ -63,17 +63,21 @@ constexpr int kMaxCluster = 8;  // CTAs per cluster (portable limit)
 template <int NT, bool kAttn = false>
 struct Cfg {
   static constexpr int kKps = NT <= 2 ? 2 : 1;  // k-blocks per stage
-  static constexpr int kStages = NT == 1 ? 3 : NT == 2 ? 2 : 3;
-  // after the stages: the split-K exchange region, two receive buffers of a token group's partials from every CTA
-  // of the cluster, which a fused attention head uses first (kAttn)
-  static constexpr size_t kPartBytes = 2 * (size_t)BM * BN * 4;
-  static constexpr size_t kRegionBytes =
-      kAttn && attn::smem_bytes<128>() > kPartBytes ? attn::smem_bytes<128>() : kPartBytes;
+  static constexpr int kStages = NT == 1 ? 4 : NT == 2 ? 2 : 3;
   static constexpr int kStageBytes = kKps * (kABytes + NT * kBBytes);
   static constexpr int kBOff = kKps * kABytes;  // the activation blocks of a stage start after its weight blocks
+  // After the stages: the split-K exchange region, receive buffers of a token group's partials from every CTA of
+  // the cluster. One group needs one buffer (a tile's item is finished before the next tile is drained); several
+  // groups alternate two, so that one group's exchange overlaps the previous group's reduce.
+  static constexpr int kRecv = NT == 1 ? 1 : 2;
+  static constexpr size_t kPartBytes = kRecv * (size_t)BM * BN * 4;
+  // A fused attention head (kAttn) runs first in the last stage and the receive buffer: the producer fills that
+  // stage only once the head is done.
+  static_assert(!kAttn || NT == 1, "the layer's attention is fused only into one-group chains");
+  static_assert(!kAttn || kStageBytes + kPartBytes >= attn::smem_bytes<128>(), "attention region");
   static constexpr int kTmemCols = kAcc * BN * NT;
   static constexpr int kTmemAlloc = kTmemCols <= 128 ? 128 : kTmemCols <= 256 ? 256 : 512;
-  static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kRegionBytes + 256;
+  static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kPartBytes + 256;
   // kind::f16 instruction descriptor: D fp32, A/B bf16, both K-major, N = 64 NT, M = 128.
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)((BN * NT) >> 3) << 17) |
                                      ((uint32_t)(BM >> 4) << 24);
@@ -158,15 +162,17 @@ MV_DEV uint64_t sw128_desc(uint32_t saddr) {
 // norm), and for the QKV epilogue the token positions prefix + depth. The 128 epilogue threads split the
 // partial sums so the loads are independent and in flight together.
 constexpr int kMaxSeq = kTokMax / BN;  // sequences of one pass (one token group each)
+template <int NTOK>  // the launch's tokens: 64 per token group
 struct EpiConst {
-  float scale[kTokMax];
-  int pos[kTokMax];
-  float part[2][kTokMax];
+  float scale[NTOK];
+  int pos[NTOK];
+  float part[2][NTOK];
   int kv_row0[kMaxSeq];  // per sequence; -1: the cache rows would run past S_max (nothing is appended)
 };
 
 // i: epilogue thread 0 .. kEpiThreads - 1 (threads 128 and up only take part in the barriers)
-MV_DEV void load_epi_const(const GemmParams& p, EpiConst* ec, int i, int ngroups) {
+template <class EC>
+MV_DEV void load_epi_const(const GemmParams& p, EC* ec, int i, int ngroups) {
   const int half = (i >> 6) & 1;  // two threads per token, each summing half of the partials
   for (int g = 0; g < ngroups && i < 128; ++g) {
     const int j = g * BN + (i & (BN - 1));
@@ -246,9 +252,9 @@ MV_DEV void rope_sincos(float a, float* s, float* c) {
 
 // This CTA's share of the tile: tokens j = w + 4t for t = r0, r0 + cs, ... (acc[u] holds t = r0 + u * cs, rows
 // 4l..4l+3, summed over every K slice of the cluster). Writes the outputs of the launch's epilogue kind.
-template <int EPI, int NU>
+template <int EPI, int NU, class EC>
 MV_DEV void final_epilogue(const GemmParams& p, int tile, int jb, int w, int l, int r0, int cs,
-                           float4 (&acc)[NU], const EpiConst* ec) {
+                           float4 (&acc)[NU], const EC* ec) {
   const int ntok = p.n_tok;
   if constexpr (EPI == EPI_STORE) {
     const int R = tile * BM + 4 * l;
@@ -438,15 +444,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   constexpr int kBOff = Cfg<NT>::kBOff;
   constexpr int kTmemAlloc = Cfg<NT>::kTmemAlloc;
   constexpr uint32_t kIdesc = Cfg<NT>::kIdesc;
+  constexpr int kRecv = Cfg<NT>::kRecv;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
   float* part = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);  // [BN tokens][BM rows], a group
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], tfull[kAcc], tempty[kAcc], drain, pfull[2], rfree[2];
-  __shared__ __align__(8) uint64_t afull[attn::kStages], aready, adone;  // fused attention
+  // fused attention: its key/value ring, its cluster steps, and this CTA's head done (the last stage is free)
+  __shared__ __align__(8) uint64_t afull[attn::kStages], aready, adone, alocal;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int s_abort;
-  __shared__ EpiConst s_ec;
+  __shared__ EpiConst<BN * NT> s_ec;
   // the current phase's parameters and epilogue kind, copied once per phase: the epilogue of a phase's last tile
   // -- the step every phase boundary waits for -- then reads shared memory instead of the kernel parameters
   // through a runtime phase index
@@ -482,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     for (int s = 0; s < attn::kStages; ++s) mbar_init(&afull[s], 1);
     mbar_init(&aready, C);  // one arrive from every CTA of the cluster per attention step
     mbar_init(&adone, C);
+    mbar_init(&alocal, 1);
     s_abort = 0;
     mbar_fence_init();
   }
@@ -555,6 +564,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const int s = it % kStages, r = it / kStages;
             const int nk = min(kKps, kb1 - kb);  // k-blocks of this stage (the last of a tile may hold fewer)
             if (s_abort || !mbar_wait(&empty[s], (uint32_t)((r & 1) ^ 1))) {
+              ok = false;
+              break;
+            }
+            // the last stage holds this CTA's attention head until it is done
+            if (kAttn && ca.attn_D && it == kStages - 1 && !mbar_wait(&alocal, 0u)) {
               ok = false;
               break;
             }
@@ -670,37 +684,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       if (ca.attn_D) {  // the layer's attention first: cluster q = head q, CTA rank = key split (128 threads)
         if (q < ca.attn.H && hw == 0) {
           EpiClusterSync sy{&aready, &adone, C, i, err};
-          uint8_t* region = reinterpret_cast<uint8_t*>(part);  // the partial buffer is not in use yet
+          // the last stage and the receive buffer: the producer leaves that stage empty until the head is done,
+          // and no CTA stores partials before every head of the layer is done
+          uint8_t* region = stages + (size_t)(kStages - 1) * kStageBytes;
           if (ca.attn_D == 128)
             attn::head<128>(ca.attn, &maps.kmap, &maps.vmap, region, afull, rank, q, 0, 0, i, sy);
           else
             attn::head<64>(ca.attn, &maps.kmap, &maps.vmap, region, afull, rank, q, 0, 0, i, sy);
         }
+        // the head's shared-memory accesses come before the bulk copies that refill the last stage
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         epi_bar();  // this CTA's attention outputs are stored
         if (i == 0) {
+          mbar_arrive(&alocal);
           count_release(ca.flags + kGemmAttnFlag);
         }
       }
     }
-    // Split-K exchange of a token group ("item" m, receive buffer m % 2): token t of a group belongs to CTA t mod C
+    // Split-K exchange of a token group ("item" m, receive buffer m % kRecv): token t of a group belongs to CTA t mod C
     // (slot t / C). Every CTA drains its partial accumulator from TMEM and stores each value straight into its
     // owner's receive buffer, slice [sender rank], with st.async counted on the owner's pfull[m % 2]. Each CTA then
     // sums the C slices of its own tokens from its own shared memory (rank order: deterministic) and runs the fused
-    // epilogue on them. A sender may reuse a buffer once every owner has consumed the item two before (rfree).
+    // epilogue on them. A sender may reuse a buffer once every owner has consumed the item kRecv before (rfree).
     const int U = kTokPerThread / C;  // token slots per owner (C is a power of two)
     const uint32_t slice_bytes = (uint32_t)(U * 4 * BM * 4);
-    const uint32_t recv_s = smem_u32(part);  // [2][C senders][U][4][BM] floats
-    if (i == 0) {  // items 0 and 1: C slices each
-      mbar_arrive_expect_tx(&pfull[0], (uint32_t)C * slice_bytes);
-      mbar_arrive_expect_tx(&pfull[1], (uint32_t)C * slice_bytes);
-    }
+    const uint32_t recv_s = smem_u32(part);  // [kRecv][C senders][U][4][BM] floats
+    if (i == 0)  // items 0 .. kRecv - 1: C slices each
+      for (int b = 0; b < kRecv; ++b) mbar_arrive_expect_tx(&pfull[b], (uint32_t)C * slice_bytes);
     bool ok = true;
     int n = 0, m = 0, prev_tile = -1, prev_ph = 0, published = 0;
     // token group g_r of the tile; nr: item number; publish_to: phases before it are finished in this CTA once this
     // item is (they are published right after its stores, ahead of releasing the receive buffer)
     auto finish = [&](int ph_r, int tile_r, int g_r, int nr, int publish_to) {
-      const int rb = nr & 1;
-      const bool all = mbar_wait_cluster(&pfull[rb], (uint32_t)((nr >> 1) & 1));
+      const int rb = nr % kRecv;
+      const bool all = mbar_wait_cluster(&pfull[rb], (uint32_t)((nr / kRecv) & 1));
       const float* recv = part + (size_t)rb * (C * U * 4 * BM);
       if (epi_any(!all)) {
         if (i == 0) mv_set_error(err, 11, MV_DEVERR_TIMEOUT);
@@ -751,15 +768,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           for (int k = published; k < publish_to; ++k) count_release(ca.flags + k);
         published = publish_to;
       }
-      // arm this buffer for item nr + 2, then tell every sender its slice here may be overwritten
+      // arm this buffer for item nr + kRecv, then tell every sender its slice here may be overwritten
       if (i == 0) mbar_arrive_expect_tx(&pfull[rb], (uint32_t)C * slice_bytes);
       if (i < C) mbar_arrive_remote(map_rank(smem_u32(&rfree[rb]), (uint32_t)i));
     };
     // Drains token group g of TMEM accumulator buffer `buf` and stores it into the owners' receive buffers (item m).
     auto drain_push = [&](int buf, int g) -> bool {
-      const int rb = m & 1;
+      const int rb = m % kRecv;
       bool free_ok = true;
-      if (m >= 2) free_ok = mbar_wait_cluster(&rfree[rb], (uint32_t)(((m >> 1) - 1) & 1));  // item m - 2 consumed
+      if (m >= kRecv)  // item m - kRecv consumed
+        free_ok = mbar_wait_cluster(&rfree[rb], (uint32_t)(((m / kRecv) - 1) & 1));
       if (epi_any(!free_ok)) {
         if (i == 0) mv_set_error(err, 10, MV_DEVERR_TIMEOUT);
         s_abort = 1;
@@ -843,10 +861,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
       tc_fence_after();
       // The tile's token groups (item m = one group of one tile): group g is drained and pushed before group g - 1
-      // is finished, so one item's exchange overlaps the other's reduce and epilogue; the two receive buffers
-      // hold items g - 1 and g (drain_push waits until every owner has consumed item g - 2). Across tiles the
-      // previous tile's last group is finished first (above): a phase's last item publishes the phase, which the
-      // next tile's activations may wait for.
+      // is finished, so one item's exchange overlaps the other's reduce and epilogue; with several groups the two
+      // receive buffers hold items g - 1 and g (drain_push waits until every owner has consumed item g - 2).
+      // Across tiles the previous tile's last group is finished first (above): a phase's last item publishes the
+      // phase, which the next tile's activations may wait for.
       for (int g = 0; g < NT; ++g) {
         if (!drain_push(buf, g)) {
           ok = false;
