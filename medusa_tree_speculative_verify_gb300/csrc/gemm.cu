@@ -422,8 +422,17 @@ struct EpiClusterSync {
     if (i < C) mbar_arrive_remote(map_rank(smem_u32(bar), (uint32_t)i));
     if (!mbar_wait_cluster(bar, 0u) && i == 0) mv_set_error(err, 16, MV_DEVERR_TIMEOUT);
   }
-  MV_DEV void ready() { step(rbar); }
-  MV_DEV void done() { step(dbar); }
+  bool stepped = false;  // the head took its first step (it has more than one working split)
+  MV_DEV void ready() {
+    step(rbar);
+    stepped = true;
+  }
+  // The head's last step is taken by the chain itself, after the outputs are published (finish): until then this
+  // CTA's partials stay in place, and only the producer's refill of the last stage, where they lie, waits for it.
+  MV_DEV void done() {}
+  MV_DEV void finish() {
+    if (stepped) step(dbar);
+  }
 };
 
 // *p += 1 with release semantics at GPU scope: every write this thread has made or observed (the other epilogue
@@ -682,8 +691,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     pdl_wait();                               // the epilogue reads what earlier kernels wrote
     if constexpr (kAttn) {
       if (ca.attn_D) {  // the layer's attention first: cluster q = head q, CTA rank = key split (128 threads)
-        if (q < ca.attn.H && hw == 0) {
-          EpiClusterSync sy{&aready, &adone, C, i, err};
+        const bool head_here = q < ca.attn.H && hw == 0;
+        EpiClusterSync sy{&aready, &adone, C, i, err};
+        if (head_here) {
           // the last stage and the receive buffer: the producer leaves that stage empty until the head is done,
           // and no CTA stores partials before every head of the layer is done
           uint8_t* region = stages + (size_t)(kStages - 1) * kStageBytes;
@@ -692,13 +702,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           else
             attn::head<64>(ca.attn, &maps.kmap, &maps.vmap, region, afull, rank, q, 0, 0, i, sy);
         }
+        epi_bar();  // this CTA's attention outputs are stored: publish them
+        if (i == 0) count_release(ca.flags + kGemmAttnFlag);
+        if (head_here) sy.finish();  // every CTA of the cluster has read this CTA's partials
         // the head's shared-memory accesses come before the bulk copies that refill the last stage
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        epi_bar();  // this CTA's attention outputs are stored
-        if (i == 0) {
-          mbar_arrive(&alocal);
-          count_release(ca.flags + kGemmAttnFlag);
-        }
+        epi_bar();
+        if (i == 0) mbar_arrive(&alocal);
       }
     }
     // Split-K exchange of a token group ("item" m, receive buffer m % kRecv): token t of a group belongs to CTA t mod C
