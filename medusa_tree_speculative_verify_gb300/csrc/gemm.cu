@@ -743,8 +743,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const int t0 = rank + hw * C, ts = 2 * C;
       for (int u0 = 0; t0 + u0 * ts < kTokPerThread; u0 += kChunk) {
         float4 acc[kChunk];
+        if (C == 4) {
+          // clusters of four: two tokens per thread, t0 and t0 + 8 (slots t0 / 4 and t0 / 4 + 2), all eight
+          // partials loaded before any is added; the sums of tokens past n_tok are not used by any epilogue
+          float4 pa[4], pb[4];
+          const int sa = t0 >> 2, sb = (t0 + ts) >> 2;
 #pragma unroll
-        for (int u = 0; u < kChunk; ++u) {
+          for (int c = 0; c < 4; ++c) {
+            pa[c] = reinterpret_cast<const float4*>(recv + ((c * U + sa) * 4 + sub) * BM)[lane];
+            pb[c] = reinterpret_cast<const float4*>(recv + ((c * U + sb) * 4 + sub) * BM)[lane];
+          }
+#pragma unroll
+          for (int u = 0; u < kChunk; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            add4(acc[0], pa[c]);
+            add4(acc[1], pb[c]);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kChunk && C != 4; ++u) {
           acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
           const int t = t0 + (u0 + u) * ts;
           if (t >= kTokPerThread) break;
