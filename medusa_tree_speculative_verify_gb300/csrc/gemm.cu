@@ -353,13 +353,33 @@ MV_DEV void final_epilogue(const GemmParams& p, int tile, int jb, int w, int l, 
     const int R = tile * BM + 4 * l;
     const bool valid = R < p.M;
     const int HD = p.H * p.D;
-    const int which = R / HD, within = R % HD, head = within / p.D, dim = within % p.D;
     const int half = p.D >> 1;
+    // Row R's part (q, k or v), head and dimension. Divisions by run-time sizes cost a long dependent chain at
+    // the tile's end, which a phase boundary waits for: with D and H D powers of two (every shape here) they are
+    // shifts and masks, with the same results.
+    int which, head, dim, dh;  // dh = dim mod D/2
+    if (((p.D & (p.D - 1)) | (HD & (HD - 1))) == 0) {
+      const int dsh = __ffs(p.D) - 1, hsh = __ffs(HD) - 1;
+      which = R >> hsh;
+      const int within = R & (HD - 1);
+      head = within >> dsh;
+      dim = within & (p.D - 1);
+      dh = dim & (half - 1);
+    } else {
+      which = R / HD;
+      const int within = R % HD;
+      head = within / p.D;
+      dim = within % p.D;
+      dh = dim % half;
+    }
     const bool lo = dim < half;
+    // theta^(-2k/D) for the rotary pair index k = (dim + q) mod D/2 of each of the lane's 4 rows. dim is a multiple
+    // of 4, so where D/2 is one too k = dim mod D/2 + q. -2 log2(theta) / D is exact for D a power of two, and the
+    // exponent then takes one rounding as before: the frequencies are the same bits.
+    const float c = -2.0f * p.log2_theta / (float)p.D;
     float inv_freq[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      inv_freq[q] = exp2f(-(float)(2 * ((dim + q) % half)) / (float)p.D * p.log2_theta);
+    for (int q = 0; q < 4; ++q) inv_freq[q] = exp2f(c * (float)((half & 3) ? (dim + q) % half : dh + q));
     // q: row j of q_out; k / v: row kv_row0[b] + r of sequence b's cache plane (j = b * seq_rows + r)
     const size_t plane = (size_t)p.layer * 2 + ((which == 1 || which == 2) ? which - 1 : 0);
     uint16_t* const kv_base = p.kv ? p.kv + (plane * p.H + head) * p.S_max * p.D + dim : nullptr;
