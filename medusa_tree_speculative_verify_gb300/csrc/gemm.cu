@@ -491,7 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   __shared__ int s_epi;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int C = ca.csize;                  // CTAs per cluster = K slices per tile
+  const int C = ca.csize;                  // CTAs per cluster = K slices per tile (a power of two)
+  const int csh = __ffs(C) - 1;            // log2 C: divisions by C are shifts
   const int rank = (int)cluster_rank();    // this CTA's K slice and token share
   // in every phase cluster q owns the contiguous tiles [t0, t1) (adjacent in the packed weight layout)
   const int q = blockIdx.x / C, ncl = gridDim.x / C;
@@ -552,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const CUtensorMap* bm = &maps.b[ph];
         int t0, t1;
         tile_range(p, t0, t1);
-        const int kb0 = rank * p.kbt / C, kb1 = (rank + 1) * p.kbt / C;  // this CTA's K slice
+        const int kb0 = (rank * p.kbt) >> csh, kb1 = ((rank + 1) * p.kbt) >> csh;  // this CTA's K slice
         // The weights do not depend on anything: their loads run ahead. The activations are the previous
         // kernel's output (phase 0: wait for that grid) or the previous phase's (wait for its counter).
         bool waited = false;
@@ -659,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const GemmParams& p = ca.ph[ph];
         int t0, t1;
         tile_range(p, t0, t1);
-        const int kb0 = rank * p.kbt / C, kb1 = (rank + 1) * p.kbt / C;
+        const int kb0 = (rank * p.kbt) >> csh, kb1 = ((rank + 1) * p.kbt) >> csh;
         for (int tile = t0; ok && tile < t1; ++tile, ++n) {
           const int buf = n % kAcc, rr = n / kAcc;
           if (s_abort || !mbar_wait(&tempty[buf], (uint32_t)((rr & 1) ^ 1))) {
@@ -736,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     // owner's receive buffer, slice [sender rank], with st.async counted on the owner's pfull[m % 2]. Each CTA then
     // sums the C slices of its own tokens from its own shared memory (rank order: deterministic) and runs the fused
     // epilogue on them. A sender may reuse a buffer once every owner has consumed the item kRecv before (rfree).
-    const int U = kTokPerThread / C;  // token slots per owner (C is a power of two)
+    const int U = kTokPerThread >> csh;  // token slots per owner
     const uint32_t slice_bytes = (uint32_t)(U * 4 * BM * 4);
     const uint32_t recv_s = smem_u32(part);  // [kRecv][C senders][U][4][BM] floats
     if (i == 0)  // items 0 .. kRecv - 1: C slices each
@@ -788,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           if (t >= kTokPerThread) break;
           const int j = sub + 4 * t;  // token within the group
           if (g_r * BN + j >= pr.n_tok) continue;
-          const int slot = t / C;  // this token's place in every sender's slice
+          const int slot = t >> csh;  // this token's place in every sender's slice
           float4 part_c[kMaxCluster];
 #pragma unroll
           for (int c = 0; c < kMaxCluster; ++c)
@@ -847,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
       for (int jj = 0; jj < BN / 2; ++jj) {
         const int j = hw * (BN / 2) + jj, t = j >> 2, c = t & (C - 1);
-        const uint32_t off = (uint32_t)((((t / C) * 4 + (j & 3)) * BM + row) * 4);
+        const uint32_t off = (uint32_t)((((t >> csh) * 4 + (j & 3)) * BM + row) * 4);
         st_async_f32(map_rank(mine + off, (uint32_t)c), v[jj], map_rank(bar, (uint32_t)c));
       }
       ++m;
