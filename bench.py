@@ -405,9 +405,9 @@ def run_gpu(args, world, rank, local):
 
 
 # DRAM bytes (read + write) per algorithmic byte of the projection kernel, from the ncu capture of one chain launch
-# with its layer's attention (7B shape: 414.3 MB measured for 420.2 MB algorithmic; the LM-head launch alone:
-# 268.2 / 270.9 MB): the kernel reads every weight byte once, so the traffic of a launch scales with its bytes.
-GEMM_TRAFFIC_PER_ALGORITHMIC_BYTE = 0.986
+# with its layer's attention (7B shape: 414.6 MB measured for 420.2 MB algorithmic; the LM-head launch alone:
+# 268.4 / 270.9 MB): the kernel reads every weight byte once, so the traffic of a launch scales with its bytes.
+GEMM_TRAFFIC_PER_ALGORITHMIC_BYTE = 0.987
 
 
 def gemm_bytes(dims, n):
