@@ -110,6 +110,25 @@ def test_prefill_matches_oracle():
     _check_topk_rows(sess.head_topk.cpu().numpy(), medusa_heads(om.get, DIMS.n_medusa, hs[-1]), 10)
 
 
+def test_three_heads_step_matches_oracle():
+    """A decoder with 3 heads of 16 (48 q rows, not a power of two): the QKV epilogue takes a row's part, head and
+    dimension by division instead of shifts. Prefill and one greedy verify step against the oracle, every node's
+    logits and the prefill's cache rows element by element."""
+    dims = dataclasses.replace(DIMS, n_heads=3)
+    _, _, tree, sess, om, ot = _setup(synth.dense_tree_choices([2, 3]), dims=dims)
+    p = synth.prompt_tokens(0, 32, dims.vocab)
+    sess.prefill(torch.as_tensor(p, dtype=torch.int32, device="cuda"))
+    st = o_prefill(om, p.numpy(), S_MAX, 10)
+    P = len(p)
+    kv = sess.kv[:, :, :, :P].double().cpu().numpy()
+    assert np.allclose(kv, st.cache.data[:, :, :, :P], rtol=RTOL, atol=ATOL)
+    sess.step(mv.AcceptParams(GREEDY))
+    torch.cuda.synchronize()
+    _, info = o_verify_step(om, st, ot, GREEDY)
+    got = sess.logits[:tree.n_nodes].double().cpu().numpy()
+    assert np.allclose(got, info["logits"], rtol=RTOL, atol=ATOL)
+
+
 @pytest.mark.parametrize("wide", [False, True])
 def test_one_step_internals(wide):
     """One verify step against the oracle: candidates, every node's logits, the accepted path, the compacted
